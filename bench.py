@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Benchmark of the F^H D / Q gather on GB300.
+
+Headline: F^H D voxel-sample pairs per second on the 128^3-voxel, 3D-radial
+workload (M = 262,144 samples, 2,097,152 voxels), MUFU trig path, one
+mri_fhd call per step (cmpMu + tile staging + phase + trig + complex
+multiply-accumulate + epilogue).  The same JSON line also carries the other
+rows of the hot path measured the same way: F^H D with accurate trig, Q on the
+128^3 stack-of-spirals trajectory (M = 1,048,576) and batched F^H D with 8
+coils (M = 524,288).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs its own 128^3 voxel slab of a stacked
+volume against the same trajectory (independent problems, no collective on
+the data path); the timing is the maximum over ranks.  ``--impl reference``
+times the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from non_cartesian_mri_gb300 import workloads as wl  # noqa: E402
+
+HEADLINE = "fhd_128_radial"
+METRIC = "F^H D voxel-sample pairs/sec (G/s) and % of SFU/FP32 roofline, 1xGB300"
+UNIT = "Gpairs/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# Algorithmic operations per unit of work (the method's own minimum): the
+# phase is 1 FMUL + 2 FFMA, the complex multiply-accumulate 4 FFMA (Q: 2), and
+# sin + cos are two SFU (MUFU) operations.  Batched: per pair-coil.
+ALGO_OPS = {
+    "fhd": {"mufu": 2.0, "fp32": 7.0, "unit": "pair"},
+    "q": {"mufu": 2.0, "fp32": 5.0, "unit": "pair"},
+    "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
+}
+# Per-SM-per-clock issue rates of sm_103a: FP32 FFMA 128 lanes; MUFU sin/cos
+# measured at 32 by the mri_microbench probe (reported live below).
+NOMINAL = {"mufu": 32.0, "fp32": 128.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--trig", choices=["fast", "accurate", "fast_rr"], default="fast")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-paths", action="store_true",
+                    help="skip the accurate/Q/batched sub-measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# process group (one rank per GPU under torchrun)
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    def __init__(self, world, rank, device):
+        self.world, self.rank = world, rank
+        self.pg = None
+        if world > 1:
+            import torch.distributed as td
+            backend = "nccl" if device.type == "cuda" else "gloo"
+            td.init_process_group(backend=backend, world_size=world, rank=rank)
+            self.td = td
+
+    def barrier(self):
+        if self.world > 1:
+            self.td.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.td.all_reduce(t, op=self.td.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.td.destroy_process_group()
+
+
+def slab(w: wl.Workload, rank: int) -> wl.Workload:
+    """Rank r's problem: the same trajectory against the voxel slab z + r*L."""
+    if rank == 0:
+        return w
+    z = (w.z + np.float32(rank * w.L)).astype(np.float32)
+    return wl.Workload(w.name, w.kind, w.L, w.kx, w.ky, w.kz, w.x, w.y, z, w.rPhi, w.iPhi,
+                       w.rD, w.iD, w.B, dict(w.meta, slab=rank))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.fh = None
+
+    def __enter__(self):
+        try:
+            self.fh = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.fh is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.fh.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.fh.read())) if len(r) >= 9]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def to_dev(w: wl.Workload, torch):
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    out = {k: d(getattr(w, k)) for k in ("kx", "ky", "kz", "x", "y", "z", "rPhi", "iPhi")}
+    if w.rD is not None:
+        out["rD"] = d(w.rD)
+        out["iD"] = d(w.iD)
+    return out
+
+
+def call(mri, kind, t, trig, out=None):
+    if kind == "fhd":
+        return mri.fhd(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"], t["rPhi"], t["iPhi"],
+                       t["rD"], t["iD"], trig=trig, out=out)
+    if kind == "q":
+        return mri.q(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"], t["rPhi"], t["iPhi"],
+                     trig=trig, out=out)
+    return mri.fhd_batched(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"], t["rPhi"],
+                           t["iPhi"], t["rD"], t["iD"], trig=trig, out=out)
+
+
+def timed_steps(torch, mri, dist, fn, steps, warmup, flush):
+    """W untimed steps, then K steps bracketed by barrier + synchronize; each
+    step's device time from CUDA events on the launching stream, the L2
+    flushed (256 MiB write) before every step outside the events."""
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    wall0 = time.perf_counter()
+    with mri.gather_timing() as gt:
+        for k in range(steps):
+            flush()
+            evs[k][0].record(stream)
+            fn()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    return {"step_ms": step_ms, "gather_ms": gt.ms, "gather_launches": gt.launches,
+            "wall_s": wall}
+
+
+def unit_rates(mri):
+    r = {}
+    for probe in ("sin", "cos", "ffma"):
+        mri.microbench(probe, ctas_per_sm=1, threads=1024, iters=1 << 10)
+        r[probe] = round(mri.microbench(probe, ctas_per_sm=1, threads=1024,
+                                        iters=1 << 13)["per_sm_per_clk"], 2)
+    return r
+
+
+def peak_per_sm_clk(kind, rates):
+    """Binding roofline in work units per SM per clock: min over the two units."""
+    ops = ALGO_OPS[kind]
+    mufu = NOMINAL["mufu"] if rates is None else min(rates["sin"], rates["cos"])
+    fp32 = NOMINAL["fp32"] if rates is None else rates["ffma"]
+    # nominal integers when the probe agrees within 10%
+    if abs(mufu - NOMINAL["mufu"]) <= 0.1 * NOMINAL["mufu"]:
+        mufu = NOMINAL["mufu"]
+    if abs(fp32 - NOMINAL["fp32"]) <= 0.1 * NOMINAL["fp32"]:
+        fp32 = NOMINAL["fp32"]
+    by_mufu = mufu / ops["mufu"]
+    by_fp32 = fp32 / ops["fp32"]
+    return min(by_mufu, by_fp32), ("mufu" if by_mufu <= by_fp32 else "fp32"), mufu, fp32
+
+
+def gather_source_hash():
+    h = hashlib.sha256()
+    for f in ("gather.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "non_cartesian_mri_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind, trig):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(f"{kind}:{trig}")
+    if not entry or entry.get("source_hash") != gather_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig):
+    units = w.pairs * (w.B if kind == "fhd_batched" else 1)
+    per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
+    launches_per_step = res["gather_launches"] / len(res["step_ms"])
+    achieved = units / launches_per_step / per_launch / 1e9
+    per_clk, unit, mufu, fp32 = peak_per_sm_clk(kind, rates)
+    peak = per_clk * sms * sm_max_mhz * 1e6 / 1e9
+    out = {"bound": "alu", "binding_unit": unit, "achieved": round(achieved, 2),
+           "peak": round(peak, 2),
+           "unit": "G" + ALGO_OPS[kind]["unit"] + "s/s",
+           "frac": round(achieved / peak, 4),
+           "traffic": profiled_traffic(kind, trig),
+           "peak_basis": (f"{sms} SMs x {sm_max_mhz:.0f} MHz x min(MUFU {mufu:g}/"
+                          f"{ALGO_OPS[kind]['mufu']:g}, FP32 {fp32:g}/{ALGO_OPS[kind]['fp32']:g})"
+                          " per SM-clock"),
+           "gather_ms_per_launch": round(per_launch * 1e3, 3)}
+    if sm_mhz:
+        out["frac_at_sampled_clock"] = round(achieved / (per_clk * sms * sm_mhz * 1e-3), 4)
+        out["units_per_sm_clk"] = round(achieved * 1e9 / (sms * sm_mhz * 1e6), 3)
+    return out
+
+
+def cpu_baseline(w: wl.Workload, target_s: float = 12.0):
+    """The oracle, as it stands, on a seeded voxel sample of the workload."""
+    import oracle
+    cores = oracle.threads(0)
+    probe = wl.voxel_subset(w.N, 32, 9)
+    t0 = time.perf_counter()
+    oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    count = int(min(max(32 * target_s / dt, 64), 65536, w.N))
+    idx = wl.voxel_subset(w.N, count, 10)
+    t0 = time.perf_counter()
+    oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
+    dt = time.perf_counter() - t0
+    pairs = count * w.M
+    return {"value": round(pairs / dt / 1e9, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{count} seeded voxels x all {w.M} samples of {w.name} "
+                      f"({pairs:.3g} pairs, {dt:.1f} s, fp64, OpenMP over voxels)"}
+
+
+def e2e(torch, mri, dist, w, trig, steps, warmup):
+    """Public API with pinned host buffers: H2D of the inputs, the call, D2H of
+    the outputs, all inside the timed region."""
+    names = ("kx", "ky", "kz", "x", "y", "z", "rPhi", "iPhi", "rD", "iD")
+    host = [torch.from_numpy(np.ascontiguousarray(getattr(w, n))).pin_memory() for n in names]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = 2 * w.N * 4
+
+    def step():
+        r, i = mri.fhd(*host, trig=trig)
+        return r, i
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    dist.barrier()
+    mean_s = dist.max(statistics.mean(times))
+    return {"value": round(w.pairs * dist.world / mean_s / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(mean_s * 1e3, 3)}
+
+
+def run_ours(args):
+    import torch
+    import non_cartesian_mri_gb300 as mri
+    from non_cartesian_mri_gb300 import build
+
+    world, rank, local = dist_info()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    build.build()
+    mri.load()
+    dist = Dist(world, rank, torch.device("cuda", local))
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            peaks = json.load(fh)
+    except (OSError, ValueError):
+        pass
+    sm_max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush_ctr = [0]
+
+    def flush():
+        flush_ctr[0] += 1
+        flush_buf.fill_(float(flush_ctr[0] & 7))
+
+    rates = unit_rates(mri)
+
+    w = slab(wl.make_workload(args.workload), rank)
+    kind = w.kind
+    t = to_dev(w, torch)
+    out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
+           torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"))
+    plan = mri.plan(kind, w.M, w.N, B=w.B)
+    with ClockSampler(local) as clk:
+        res = timed_steps(torch, mri, dist, lambda: call(mri, kind, t, args.trig, out),
+                          args.steps, args.warmup, flush)
+    clocks = clk.summary()
+    mean_s = dist.max(statistics.mean(res["step_ms"]) / 1e3)
+    units = w.pairs * (w.B if kind == "fhd_batched" else 1)
+    value = units * world / mean_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded generators, no dataset)",
+        "config": {"workload": f"{w.name}: {wl.WORKLOADS[w.name]}", "voxels": w.N,
+                   "samples": w.M, "coils": w.B, "trig": args.trig,
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "parallelism": "one independent voxel slab per rank" if world > 1
+                   else "single GPU",
+                   "plan": plan},
+        "roofline": roofline(kind, w, res, rates, sms, sm_max_mhz, clocks.get("sm_mhz"),
+                             args.trig),
+        "gpu_launches": plan["launches"] * args.steps,
+        "clocks": clocks,
+        "unit_rates_per_sm_clk": rates,
+    }
+    line["roofline"]["sm_max_mhz_basis"] = "MEASURED_PEAKS.json sm_max_mhz" if peaks else "recipe"
+
+    if not args.no_e2e and kind == "fhd":
+        line["e2e"] = e2e(torch, mri, dist, w, args.trig, max(args.steps, 2), 1)
+    del t, out
+    torch.cuda.empty_cache()
+
+    if not args.no_paths and args.workload == HEADLINE and world == 1:
+        paths = {}
+        for name, wname, trig in (("fhd_accurate", HEADLINE, "accurate"),
+                                  ("q_fast", "q_128", "fast"),
+                                  ("fhd_batched_fast", "fhd_batched_128", "fast")):
+            pw = wl.make_workload(wname)
+            pt = to_dev(pw, torch)
+            po = None
+            pres = timed_steps(torch, mri, dist, lambda: call(mri, pw.kind, pt, trig, po),
+                               args.steps, args.warmup, flush)
+            pm = statistics.mean(pres["step_ms"]) / 1e3
+            punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
+            paths[name] = {
+                "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}", "trig": trig,
+                "value": round(punits / pm / 1e9, 2),
+                "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
+                "ms_per_step": round(pm * 1e3, 3),
+                "roofline": roofline(pw.kind, pw, pres, rates, sms, sm_max_mhz,
+                                     clocks.get("sm_mhz"), trig),
+                "gpu_launches": mri.plan(pw.kind, pw.M, pw.N, B=pw.B)["launches"] * args.steps,
+            }
+            if pw.kind == "fhd_batched":
+                paths[name]["trajectory_pairs_per_s_G"] = round(pw.pairs / pm / 1e9, 2)
+            del pt
+            torch.cuda.empty_cache()
+        line["paths"] = paths
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl.make_workload(args.workload))
+    errs = mri.device_errors(clear=True)
+    if errs:
+        line["device_errors"] = errs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    w = wl.make_workload(args.workload)
+    cores = oracle.threads(0)
+    probe = wl.voxel_subset(w.N, 16, 11)
+    t0 = time.perf_counter()
+    run = {"fhd": oracle.fhd, "q": oracle.q, "fhd_batched": oracle.fhd_batched}[w.kind]
+
+    def step(idx):
+        if w.kind == "q":
+            run(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
+        else:
+            run(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
+
+    step(probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_step_s = min(150.0 / max(args.steps + args.warmup, 1), 15.0)
+    count = int(min(max(16 * per_step_s / dt, 16), 65536, w.N))
+    times = []
+    for k in range(args.warmup + args.steps):
+        idx = wl.voxel_subset(w.N, count, 1000 + k)
+        t0 = time.perf_counter()
+        step(idx)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    mean_s = statistics.mean(times)
+    units = count * w.M * (w.B if w.kind == "fhd_batched" else 1)
+    value = units / mean_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators, no dataset)",
+        "config": {"workload": f"{w.name}: {wl.WORKLOADS[w.name]}", "voxels": w.N,
+                   "samples": w.M, "coils": w.B,
+                   "sample_per_step": f"{count} seeded voxels x all {w.M} samples"},
+        "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{count} seeded voxels per step x all {w.M} samples "
+                                   f"of {w.name}, fp64, OpenMP over voxels"},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

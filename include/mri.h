@@ -1,0 +1,178 @@
+/*
+ * mri.h -- C ABI of the GB300 F^H D / Q gather library (libmri.so).
+ *
+ * The operations are the data-parallel core of iterative non-Cartesian MRI
+ * reconstruction as the chapter "Iterative MRI reconstruction" (PMPP ch. 17)
+ * describes it:
+ *
+ *   cmpMu  (section 17.3, Figs. 17.6-17.7):  Mu[m] = conj(Phi[m]) * D[m]
+ *   cmpFhD (section 17.3, Figs. 17.9-17.11): FhD[n] = sum_m Mu[m] * e^{+i 2 pi k_m . x_n}
+ *   Q      (section 17.2):                   Q[n]   = sum_m |Phi[m]|^2 * e^{+i 2 pi k_m . x_n}
+ *
+ * The sign +i and k in cycles per unit of x follow Eq. 17.1 and the phase
+ * 2*PI*(kx*x + ky*y + kz*z) of the register-promoted kernel (Fig. 17.11).
+ * The pages print no formula for Mu or Q; the readings above are the ones
+ * this library implements.
+ *
+ * Conventions for every entry point
+ *   - Arrays are float32, structure of arrays, caller-owned DEVICE memory on
+ *     the current CUDA device, each at least 4-byte aligned.  Nothing is kept
+ *     after a call returns.
+ *   - Sample arrays have M elements, voxel arrays N elements; batched data and
+ *     outputs are coil-major [B][M] and [B][N].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  The return value covers argument checks and launch
+ *     errors; errors during execution surface at the caller's next
+ *     synchronisation or through mri_device_errors().
+ *   - Scratch memory (tile records, per-split partial sums) is taken from a
+ *     library-owned stream-ordered memory pool on `stream` and returned to it
+ *     before the call returns; the pool keeps freed memory for reuse.
+ *   - No C++ exception crosses this interface; no call traps or aborts.
+ *   - The kernels are built for sm_103a only; any other device gives
+ *     MRI_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef MRI_H
+#define MRI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mri_status {
+    MRI_OK = 0,
+    MRI_ERR_NULL = 1,               /* a required pointer is NULL */
+    MRI_ERR_SIZE = 2,               /* M, N or B negative or too large */
+    MRI_ERR_ALIGN = 3,              /* a pointer is not 4-byte aligned */
+    MRI_ERR_NOT_DEVICE = 4,         /* a pointer is not device memory of the current device */
+    MRI_ERR_MODE = 5,               /* unknown trig mode or accumulate flag not 0/1 */
+    MRI_ERR_CUDA = 6,               /* a CUDA runtime call failed (launch, pool, query) */
+    MRI_ERR_UNSUPPORTED_DEVICE = 7  /* the current device is not compute capability 10.3 */
+} mri_status;
+
+typedef enum mri_trig {
+    /* sin/cos with fp32 software accuracy (sincospif on the FP32 pipe): the
+     * software trig of the chapter's sequential and early kernels. */
+    MRI_TRIG_ACCURATE = 0,
+    /* hardware sin/cos on the SFU (MUFU), the chapter's step 3 (Fig. 17.17);
+     * the phase is formed in radians directly. */
+    MRI_TRIG_FAST = 1,
+    /* MUFU sin/cos after exact reduction of the phase to [-1/2, 1/2] turn;
+     * slower than MRI_TRIG_FAST, for phases far beyond 100*pi. */
+    MRI_TRIG_FAST_RR = 2
+} mri_trig;
+
+/* Kinds understood by mri_plan_gather. */
+typedef enum mri_kind {
+    MRI_KIND_FHD = 0,
+    MRI_KIND_Q = 1,
+    MRI_KIND_FHD_BATCHED = 2
+} mri_kind;
+
+/*
+ * cmpMu (section 17.3, Fig. 17.7; loop fission of Fig. 17.6):
+ *   rMu[m] = rPhi[m]*rD[m] + iPhi[m]*iD[m]
+ *   iMu[m] = rPhi[m]*iD[m] - iPhi[m]*rD[m]        for 0 <= m < M.
+ * Inputs rPhi, iPhi, rD, iD [M]; outputs rMu, iMu [M] (may not alias the
+ * inputs).  M == 0 is a no-op.  mri_fhd does this internally; this entry
+ * point exposes it on its own.
+ */
+mri_status mri_mu(const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                  float* rMu, float* iMu, int64_t M, void* stream);
+
+/*
+ * F^H D (section 17.3: cmpMu, then the voxel gather of Figs. 17.10-17.11):
+ *   rFhD[n] + i*iFhD[n] = sum_{m<M} conj(Phi[m]) D[m] e^{+i 2 pi (kx[m] x[n] + ky[m] y[n] + kz[m] z[n])}
+ * Inputs kx, ky, kz, rPhi, iPhi, rD, iD [M]; x, y, z [N].  Outputs rFhD,
+ * iFhD [N] are overwritten, or added to when accumulate == 1 (the kernel of
+ * Fig. 17.11 reads rFhD[n] first and adds to it, so chunks of k-space can be
+ * processed by successive calls).  M == 0 writes zeros (accumulate == 0) or
+ * leaves the outputs unchanged; N == 0 is a no-op.  Outputs may not alias
+ * inputs.
+ */
+mri_status mri_fhd(const float* kx, const float* ky, const float* kz,
+                   const float* x, const float* y, const float* z,
+                   const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                   int64_t M, int64_t N, float* rFhD, float* iFhD,
+                   mri_trig trig, int accumulate, void* stream);
+
+/*
+ * Q (section 17.2; "the same core structure as F^H D", once per trajectory):
+ *   rQ[n] + i*iQ[n] = sum_{m<M} (rPhi[m]^2 + iPhi[m]^2) e^{+i 2 pi k_m . x_n}
+ * Arguments and edge cases as mri_fhd, without D.
+ */
+mri_status mri_q(const float* kx, const float* ky, const float* kz,
+                 const float* x, const float* y, const float* z,
+                 const float* rPhi, const float* iPhi,
+                 int64_t M, int64_t N, float* rQ, float* iQ,
+                 mri_trig trig, int accumulate, void* stream);
+
+/*
+ * Batched F^H D: B data vectors (e.g. coils) acquired on one trajectory,
+ *   FhD_b[n] = sum_m conj(Phi[m]) D_b[m] e^{+i 2 pi k_m . x_n},   0 <= b < B.
+ * rD, iD are coil-major [B][M]; rFhD, iFhD are coil-major [B][N].  Each
+ * sin/cos pair is computed once and used for up to 8 coils.  The pages do
+ * not describe this variant; it is F^H D applied to several D.
+ * B >= 1.  Other arguments and edge cases as mri_fhd.
+ */
+mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz,
+                           const float* x, const float* y, const float* z,
+                           const float* rPhi, const float* iPhi,
+                           const float* rD, const float* iD,
+                           int64_t B, int64_t M, int64_t N,
+                           float* rFhD, float* iFhD,
+                           mri_trig trig, int accumulate, void* stream);
+
+/* A static, NUL-terminated description of a status code. */
+const char* mri_status_string(mri_status status);
+
+/*
+ * How a gather call will be launched (host-only; no CUDA call is made when
+ * num_sms > 0).  The chapter tunes threads per block and unrolling jointly
+ * (section 17.3 step 4); this reports the shape the library picks.
+ *   kind: MRI_KIND_*; B: coils (1 unless batched); num_sms: SM count of the
+ *   target device, or 0 for the current device.
+ */
+typedef struct mri_plan {
+    int threads_per_cta;      /* threads per CTA */
+    int voxels_per_thread;    /* V: voxels held in registers by each thread */
+    int samples_per_tile;     /* samples per shared-memory k-tile */
+    int splits;               /* CTAs along the sample axis (1: no split) */
+    int64_t voxel_ctas;       /* CTAs along the voxel axis */
+    int64_t tiles;            /* k-tiles covering M */
+    int coil_groups;          /* gather launches over coil groups (batched) */
+    int launches;             /* kernel launches one call makes */
+    int64_t scratch_bytes;    /* pool memory one call takes */
+} mri_plan;
+
+mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,
+                           mri_plan* plan);
+
+/*
+ * Device-side error bits of the current device (bit 0: a k-tile wait timed
+ * out; bit 1: in-flight copies did not drain).  Synchronises the device.
+ * clear != 0 resets the bits.  Kernels never trap; a non-zero word means the
+ * outputs of some earlier call are not valid.
+ */
+mri_status mri_device_errors(unsigned int* bits, int clear);
+
+/*
+ * Gather-kernel timing, for benchmarks and profiling.  Between
+ * mri_timing_begin() and mri_timing_end(), every gather-kernel launch made on
+ * the current device is bracketed by two CUDA events recorded on the
+ * launch's own stream (the events are the library's; at most 4096 launches
+ * per window are timed).  mri_timing_end() waits for those events and
+ * returns the summed gather-kernel time in milliseconds and the number of
+ * launches timed.  The prep and split-reduction kernels are not included.
+ * Timing adds two event records per launch and changes nothing else.
+ */
+mri_status mri_timing_begin(void);
+mri_status mri_timing_end(double* gather_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MRI_H */

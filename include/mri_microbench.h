@@ -1,0 +1,43 @@
+/*
+ * mri_microbench.h -- throughput probes of the two units the gather is bound
+ * by, for the roofline of the F^H D / Q kernels.
+ *
+ * The chapter "Iterative MRI reconstruction" (section 17.3) counts about 13
+ * floating-point operations and 2 trig operations per voxel-sample pair and
+ * moves sin/cos onto the SFUs (step 3, Fig. 17.17) because trig would
+ * otherwise dominate.  How many MUFU and FFMA results an SM delivers per
+ * clock on this GPU decides which unit binds; these probes measure it.
+ *
+ * mri_microbench launches ONE wave of CTAs (ctas_per_sm per SM, `threads`
+ * threads each) on `stream`; each CTA takes 1/ctas_per_sm of the SM's shared
+ * memory, so exactly ctas_per_sm CTAs share every SM.  Each thread runs `iters` iterations of 8
+ * independent dependency chains of the probed instruction:
+ *   which = 0: __sinf (MUFU sine),   which = 1: __cosf (MUFU cosine),
+ *   which = 2: fmaf (FFMA),          which = 3: exp2f (MUFU base-2 exponential).
+ * Each CTA writes its elapsed SM clock cycles (clock64) to cycles[cta] and a
+ * value derived from its chains to sink[cta * threads + thread] (so the work
+ * is not removed).  Rate per SM per clock =
+ *   ctas_per_sm * threads * iters * 8 / cycles.
+ * cycles: device array of (num_sms * ctas_per_sm) uint64; sink: device array
+ * of (num_sms * ctas_per_sm * threads) floats.  num_sms is the current
+ * device's SM count.  Returns MRI_ERR_MODE for an unknown probe.
+ */
+#ifndef MRI_MICROBENCH_H
+#define MRI_MICROBENCH_H
+
+#include <stdint.h>
+
+#include "mri.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+mri_status mri_microbench(int which, int ctas_per_sm, int threads, int64_t iters,
+                          unsigned long long* cycles, float* sink, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MRI_MICROBENCH_H */

@@ -1,1 +1,20 @@
-"""GB300-native F^H D / Q gather for iterative non-Cartesian MRI reconstruction."""
+"""GB300-native F^H D / Q gather for iterative non-Cartesian MRI reconstruction.
+
+Public API (torch tensors in, torch tensors out; see ``binding``):
+    mu, fhd, q, fhd_batched, plan, device_errors, microbench
+The CUDA library is built with ``non_cartesian_mri_gb300.build.build()``.
+``workloads`` holds the seeded synthetic input generators.
+"""
+
+_API = ("mu", "fhd", "q", "fhd_batched", "plan", "device_errors", "microbench",
+        "status_string", "MriError", "load", "lib_path", "TRIG", "gather_timing")
+
+
+def __getattr__(name):
+    if name in _API:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
+
+
+__all__ = list(_API)

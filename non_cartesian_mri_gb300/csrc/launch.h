@@ -1,0 +1,42 @@
+// launch.h -- internal host-side interface between the C ABI and the kernel
+// translation units.  Not part of the public API.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gather.cuh"
+
+namespace mri {
+
+struct KernelShape {
+    int threads;
+    int v;                  // voxels per thread
+    int voxels_per_cta;
+    int min_blocks;         // CTAs per SM the kernel is built for
+    size_t smem;            // dynamic shared memory per CTA
+    int tile_floats;        // floats per record tile
+};
+
+// bc: coils in one group (1, 2, 4, 8); realw: Q's real weight (bc == 1).
+KernelShape gather_shape(int bc, bool realw);
+
+cudaError_t launch_prep(int bc, bool realw, const PrepParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gather(int bc, bool realw, int trig, const GatherParams& p, dim3 grid,
+                          cudaStream_t s);
+cudaError_t launch_reduce(const float* part, int splits, int bc, int64_t N, float* out_r,
+                          float* out_i, int64_t out_coil_stride, int accumulate, int grid,
+                          cudaStream_t s);
+cudaError_t launch_mu(const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                      float* rMu, float* iMu, int64_t M, int grid, cudaStream_t s);
+
+cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
+
+// per-TU dispatchers
+cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, dim3 grid,
+                                 cudaStream_t s);
+cudaError_t launch_gather_coils(int bc, int trig, const GatherParams& p, dim3 grid,
+                                cudaStream_t s);
+cudaError_t launch_prep_coils(int bc, const PrepParams& p, int grid, cudaStream_t s);
+
+}  // namespace mri

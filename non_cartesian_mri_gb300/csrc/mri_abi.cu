@@ -1,0 +1,537 @@
+// mri_abi.cu -- the extern "C" entry points of libmri.so (declared in
+// include/mri.h): argument checks, launch planning, scratch, launches.
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "mri.h"
+
+namespace {
+
+using mri::KernelShape;
+using mri::kTile;
+
+// OR-ed by kernels whose bounded waits gave up (see ptx.cuh).
+__device__ unsigned int g_device_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxM = int64_t(1) << 38;
+constexpr int64_t kMaxN = int64_t(1) << 40;
+constexpr int64_t kMaxB = int64_t(1) << 20;
+constexpr int64_t kMaxBN = int64_t(1) << 42;
+
+constexpr int kMaxTimed = 4096;
+
+struct DeviceState {
+    bool ready = false;
+    mri_status status = MRI_OK;
+    int sms = 0;
+    cudaMemPool_t pool = nullptr;
+    unsigned int* err = nullptr;
+    // gather-kernel timing window (mri_timing_begin / mri_timing_end)
+    bool timing = false;
+    int timed = 0;
+    int events_made = 0;
+    cudaEvent_t ev[2 * kMaxTimed];
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_timing_mutex;
+
+mri_status cuda_fail()
+{
+    (void)cudaGetLastError();   // clear a sticky non-fatal error
+    return MRI_ERR_CUDA;
+}
+
+// Per-device set-up on first use: capability check, SM count, the scratch
+// pool and the address of the device error word.
+mri_status device_state(DeviceState** out, int* dev_out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+    if (dev < 0 || dev >= kMaxDevices) return MRI_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cuda_fail();
+        d.sms = sms;
+        if (major != 10 || minor != 3) {
+            d.status = MRI_ERR_UNSUPPORTED_DEVICE;
+        } else {
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) return cuda_fail();
+            uint64_t keep = UINT64_MAX;   // keep freed scratch for the next call
+            if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) !=
+                cudaSuccess)
+                return cuda_fail();
+            void* err = nullptr;
+            if (cudaGetSymbolAddress(&err, g_device_error_word) != cudaSuccess)
+                return cuda_fail();
+            d.err = static_cast<unsigned int*>(err);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return d.status;
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+mri_status check_device_ptr(const void* p, int dev)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRI_ERR_NOT_DEVICE;
+    }
+    if (a.type == cudaMemoryTypeManaged) return MRI_OK;
+    if (a.type == cudaMemoryTypeDevice && a.device == dev) return MRI_OK;
+    return MRI_ERR_NOT_DEVICE;
+}
+
+// Checks a list of pointers: NULL, alignment, then (device known) residency.
+mri_status check_ptrs(const void* const* ptrs, int n, int dev)
+{
+    for (int i = 0; i < n; ++i)
+        if (ptrs[i] == nullptr) return MRI_ERR_NULL;
+    for (int i = 0; i < n; ++i)
+        if (!aligned4(ptrs[i])) return MRI_ERR_ALIGN;
+    if (dev < 0) return MRI_OK;
+    for (int i = 0; i < n; ++i) {
+        mri_status s = check_device_ptr(ptrs[i], dev);
+        if (s != MRI_OK) return s;
+    }
+    return MRI_OK;
+}
+
+// ---------------------------------------------------------------------------
+// launch planning (host only)
+// ---------------------------------------------------------------------------
+struct GroupPlan {
+    int bc;
+    bool realw;
+    KernelShape shape;
+    int64_t ntiles;
+    int64_t vblocks;
+    int splits;
+    int64_t rec_bytes;
+    int64_t part_bytes;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Samples are split across CTAs when that finishes sooner: every CTA of the
+// gather costs the same, so the run time is (waves of CTAs) x (tiles per CTA),
+// plus a per-CTA fixed cost and the reduction of the splits.  Costs are in
+// units of one tile of gather work.
+int choose_splits(int64_t ntiles, int64_t vblocks, int64_t slots, int bc, int64_t N)
+{
+    const double overhead_tiles = 0.1;     // prologue / epilogue of one CTA
+    const double launch_tiles = 0.07;      // one extra kernel launch
+    const double bytes_per_tile = 3.5e8;   // HBM bytes moved in one tile's time
+    int best = 1;
+    double best_cost = 0.0;
+    const int64_t max_s = ntiles < 1024 ? ntiles : 1024;
+    for (int64_t s = 1; s <= max_s; ++s) {
+        const int64_t units = vblocks * s;
+        const double waves = double(ceil_div(units, slots));
+        double cost = waves * (double(ceil_div(ntiles, s)) + overhead_tiles);
+        if (s > 1)
+            cost += launch_tiles + double(s + 1) * double(bc) * 2.0 * 4.0 * double(N) /
+                                       bytes_per_tile;
+        if (s == 1 || cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best = int(s);
+        }
+    }
+    return best;
+}
+
+GroupPlan plan_group(int bc, bool realw, int64_t M, int64_t N, int sms)
+{
+    GroupPlan g{};
+    g.bc = bc;
+    g.realw = realw;
+    g.shape = mri::gather_shape(bc, realw);
+    g.ntiles = ceil_div(M, kTile);
+    g.vblocks = ceil_div(N, g.shape.voxels_per_cta);
+    const int64_t slots = int64_t(sms) * g.shape.min_blocks;
+    g.splits = (g.ntiles > 0 && g.vblocks > 0)
+                   ? choose_splits(g.ntiles, g.vblocks, slots > 0 ? slots : 1, bc, N)
+                   : 1;
+    g.rec_bytes = g.ntiles * int64_t(g.shape.tile_floats) * 4;
+    g.part_bytes = g.splits > 1 ? int64_t(g.splits) * bc * 2 * N * 4 : 0;
+    return g;
+}
+
+// Coil groups of a batched call: as many 8s as fit, then at most one each of
+// 4, 2, 1.  Index into the per-size plan table.
+int group_index(int64_t left) { return left >= 8 ? 0 : left >= 4 ? 1 : left >= 2 ? 2 : 3; }
+constexpr int kGroupSizes[4] = {8, 4, 2, 1};
+
+int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+int grid_for(int64_t elements, int sms)
+{
+    int64_t g = ceil_div(elements, 256);
+    const int64_t cap = int64_t(sms) * 8;
+    if (g > cap) g = cap;
+    return g < 1 ? 1 : int(g);
+}
+
+mri_status check_mode(int trig, int accumulate)
+{
+    if (trig != MRI_TRIG_ACCURATE && trig != MRI_TRIG_FAST && trig != MRI_TRIG_FAST_RR)
+        return MRI_ERR_MODE;
+    if (accumulate != 0 && accumulate != 1) return MRI_ERR_MODE;
+    return MRI_OK;
+}
+
+float kscale_for(int trig)
+{
+    if (trig == MRI_TRIG_ACCURATE) return 2.0f;                  // half-turns for sincospif
+    if (trig == MRI_TRIG_FAST) return 6.28318530717958647692f;   // radians
+    return 1.0f;                                                 // turns
+}
+
+// The next event pair of an open timing window, or nullptr.
+cudaEvent_t* timing_slot(DeviceState* d)
+{
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    if (!d->timing || d->timed >= kMaxTimed) return nullptr;
+    const int i = d->timed;
+    while (d->events_made < 2 * (i + 1)) {
+        if (cudaEventCreate(&d->ev[d->events_made]) != cudaSuccess) return nullptr;
+        ++d->events_made;
+    }
+    ++d->timed;
+    return &d->ev[2 * i];
+}
+
+// One gather (one coil group): prep records, gather, reduce splits.
+mri_status run_group(DeviceState* d, const GroupPlan& g, int sms, const float* kx, const float* ky,
+                     const float* kz, const float* x, const float* y, const float* z,
+                     const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                     int64_t b0, int64_t M, int64_t N, float* out_r, float* out_i, int trig,
+                     int accumulate, char* scratch, unsigned int* err, cudaStream_t s)
+{
+    float* rec = reinterpret_cast<float*>(scratch);
+    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
+
+    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, b0, g.ntiles, kscale_for(trig), rec};
+    if (mri::launch_prep(g.bc, g.realw, pp, grid_for(g.ntiles * kTile, sms), s) != cudaSuccess)
+        return cuda_fail();
+
+    mri::GatherParams gp{};
+    gp.rec = rec;
+    gp.ntiles = g.ntiles;
+    gp.splits = g.splits;
+    gp.x = x;
+    gp.y = y;
+    gp.z = z;
+    gp.N = N;
+    gp.err = err;
+    if (g.splits == 1) {
+        gp.out_r = out_r + b0 * N;
+        gp.out_i = out_i + b0 * N;
+        gp.coil_stride = N;
+        gp.split_stride = 0;
+        gp.accumulate = accumulate;
+    } else {
+        gp.out_r = part;
+        gp.out_i = part + N;
+        gp.coil_stride = 2 * N;
+        gp.split_stride = int64_t(g.bc) * 2 * N;
+        gp.accumulate = 0;
+    }
+    dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
+    cudaEvent_t* ev = timing_slot(d);
+    if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) return cuda_fail();
+    if (mri::launch_gather(g.bc, g.realw, trig, gp, grid, s) != cudaSuccess) return cuda_fail();
+    if (ev && cudaEventRecord(ev[1], s) != cudaSuccess) return cuda_fail();
+
+    if (g.splits > 1) {
+        if (mri::launch_reduce(part, g.splits, g.bc, N, out_r + b0 * N, out_i + b0 * N, N,
+                               accumulate, grid_for(int64_t(g.bc) * 2 * N, sms),
+                               s) != cudaSuccess)
+            return cuda_fail();
+    }
+    return MRI_OK;
+}
+
+// One plan per coil-group size (Q: only the single-weight plan, index 3).
+void group_plans(bool realw, int64_t B, int64_t M, int64_t N, int sms, GroupPlan plans[4],
+                 bool used[4])
+{
+    for (int i = 0; i < 4; ++i) used[i] = false;
+    if (realw) {
+        plans[3] = plan_group(1, true, M, N, sms);
+        used[3] = true;
+        return;
+    }
+    if (B >= 8) used[0] = true;
+    const int64_t rest = B % 8;
+    if (rest >= 4) used[1] = true;
+    if (rest % 4 >= 2) used[2] = true;
+    if (rest % 2 == 1) used[3] = true;
+    for (int i = 0; i < 4; ++i)
+        if (used[i]) plans[i] = plan_group(kGroupSizes[i], false, M, N, sms);
+}
+
+// Shared driver of mri_fhd / mri_q / mri_fhd_batched after argument checks.
+mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* ky,
+                           const float* kz, const float* x, const float* y, const float* z,
+                           const float* rPhi, const float* iPhi, const float* rD,
+                           const float* iD, int64_t M, int64_t N, float* out_r, float* out_i,
+                           int trig, int accumulate, DeviceState* d, cudaStream_t s)
+{
+    if (M == 0) {
+        if (!accumulate) {
+            if (mri::launch_zero(out_r, B * N, grid_for(B * N, d->sms), s) != cudaSuccess ||
+                mri::launch_zero(out_i, B * N, grid_for(B * N, d->sms), s) != cudaSuccess)
+                return cuda_fail();
+        }
+        return MRI_OK;
+    }
+    GroupPlan plans[4];
+    bool used[4];
+    group_plans(realw, B, M, N, d->sms, plans, used);
+    int64_t scratch_bytes = 0;
+    for (int i = 0; i < 4; ++i) {
+        const int64_t b = used[i] ? align256(plans[i].rec_bytes) + plans[i].part_bytes : 0;
+        if (b > scratch_bytes) scratch_bytes = b;
+    }
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), size_t(scratch_bytes),
+                                d->pool, s) != cudaSuccess)
+        return cuda_fail();
+
+    mri_status st = MRI_OK;
+    for (int64_t b0 = 0; b0 < B && st == MRI_OK;) {
+        const int i = realw ? 3 : group_index(B - b0);
+        st = run_group(d, plans[i], d->sms, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, b0, M, N,
+                       out_r, out_i, trig, accumulate, scratch, d->err, s);
+        b0 += plans[i].bc;
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
+mri_status check_sizes(int64_t B, int64_t M, int64_t N)
+{
+    if (B < 1 || M < 0 || N < 0) return MRI_ERR_SIZE;
+    if (B > kMaxB || M > kMaxM || N > kMaxN) return MRI_ERR_SIZE;
+    if (N > 0 && B > kMaxBN / N) return MRI_ERR_SIZE;
+    return MRI_OK;
+}
+
+// Full argument check shared by the gather entry points.
+mri_status prepare(int trig, int accumulate, int64_t B, int64_t M, int64_t N,
+                   const void* const* sample_ptrs, int n_sample, const void* const* voxel_ptrs,
+                   int n_voxel, DeviceState** d)
+{
+    mri_status st = check_mode(trig, accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_sizes(B, M, N)) != MRI_OK) return st;
+    if (N == 0) return MRI_OK;
+    if ((st = check_ptrs(voxel_ptrs, n_voxel, -1)) != MRI_OK) return st;
+    if (M > 0 && (st = check_ptrs(sample_ptrs, n_sample, -1)) != MRI_OK) return st;
+    int dev = -1;
+    if ((st = device_state(d, &dev)) != MRI_OK) return st;
+    if ((st = check_ptrs(voxel_ptrs, n_voxel, dev)) != MRI_OK) return st;
+    if (M > 0 && (st = check_ptrs(sample_ptrs, n_sample, dev)) != MRI_OK) return st;
+    return MRI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mri_status mri_mu(const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                  float* rMu, float* iMu, int64_t M, void* stream)
+{
+    if (M < 0 || M > kMaxM) return MRI_ERR_SIZE;
+    if (M == 0) return MRI_OK;
+    const void* ptrs[6] = {rPhi, iPhi, rD, iD, rMu, iMu};
+    mri_status st = check_ptrs(ptrs, 6, -1);
+    if (st != MRI_OK) return st;
+    DeviceState* d = nullptr;
+    int dev = -1;
+    if ((st = device_state(&d, &dev)) != MRI_OK) return st;
+    if ((st = check_ptrs(ptrs, 6, dev)) != MRI_OK) return st;
+    if (mri::launch_mu(rPhi, iPhi, rD, iD, rMu, iMu, M, grid_for(M, d->sms),
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return cuda_fail();
+    return MRI_OK;
+}
+
+mri_status mri_fhd(const float* kx, const float* ky, const float* kz, const float* x,
+                   const float* y, const float* z, const float* rPhi, const float* iPhi,
+                   const float* rD, const float* iD, int64_t M, int64_t N, float* rFhD,
+                   float* iFhD, mri_trig trig, int accumulate, void* stream)
+{
+    const void* sp[7] = {kx, ky, kz, rPhi, iPhi, rD, iD};
+    const void* vp[5] = {x, y, z, rFhD, iFhD};
+    DeviceState* d = nullptr;
+    mri_status st = prepare(int(trig), accumulate, 1, M, N, sp, 7, vp, 5, &d);
+    if (st != MRI_OK || N == 0) return st;
+    return run_gather_call(false, 1, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, M, N, rFhD, iFhD,
+                           int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_q(const float* kx, const float* ky, const float* kz, const float* x,
+                 const float* y, const float* z, const float* rPhi, const float* iPhi,
+                 int64_t M, int64_t N, float* rQ, float* iQ, mri_trig trig, int accumulate,
+                 void* stream)
+{
+    const void* sp[5] = {kx, ky, kz, rPhi, iPhi};
+    const void* vp[5] = {x, y, z, rQ, iQ};
+    DeviceState* d = nullptr;
+    mri_status st = prepare(int(trig), accumulate, 1, M, N, sp, 5, vp, 5, &d);
+    if (st != MRI_OK || N == 0) return st;
+    return run_gather_call(true, 1, kx, ky, kz, x, y, z, rPhi, iPhi, nullptr, nullptr, M, N, rQ,
+                           iQ, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz, const float* x,
+                           const float* y, const float* z, const float* rPhi,
+                           const float* iPhi, const float* rD, const float* iD, int64_t B,
+                           int64_t M, int64_t N, float* rFhD, float* iFhD, mri_trig trig,
+                           int accumulate, void* stream)
+{
+    const void* sp[7] = {kx, ky, kz, rPhi, iPhi, rD, iD};
+    const void* vp[5] = {x, y, z, rFhD, iFhD};
+    DeviceState* d = nullptr;
+    mri_status st = prepare(int(trig), accumulate, B, M, N, sp, 7, vp, 5, &d);
+    if (st != MRI_OK || N == 0) return st;
+    return run_gather_call(false, B, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, M, N, rFhD, iFhD,
+                           int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+const char* mri_status_string(mri_status status)
+{
+    switch (status) {
+        case MRI_OK: return "ok";
+        case MRI_ERR_NULL: return "a required pointer is NULL";
+        case MRI_ERR_SIZE: return "M, N or B is negative or too large";
+        case MRI_ERR_ALIGN: return "a pointer is not 4-byte aligned";
+        case MRI_ERR_NOT_DEVICE: return "a pointer is not device memory of the current device";
+        case MRI_ERR_MODE: return "unknown trig mode or accumulate flag not 0/1";
+        case MRI_ERR_CUDA: return "a CUDA runtime call failed";
+        case MRI_ERR_UNSUPPORTED_DEVICE: return "the current device is not sm_103 (GB300)";
+    }
+    return "unknown status";
+}
+
+mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,
+                           mri_plan* plan)
+{
+    if (plan == nullptr) return MRI_ERR_NULL;
+    if (kind != MRI_KIND_FHD && kind != MRI_KIND_Q && kind != MRI_KIND_FHD_BATCHED)
+        return MRI_ERR_MODE;
+    if (kind != MRI_KIND_FHD_BATCHED) B = 1;
+    mri_status st = check_sizes(B, M, N);
+    if (st != MRI_OK) return st;
+    if (num_sms < 0) return MRI_ERR_SIZE;
+    if (num_sms == 0) {
+        DeviceState* d = nullptr;
+        if ((st = device_state(&d, nullptr)) != MRI_OK && st != MRI_ERR_UNSUPPORTED_DEVICE)
+            return st;
+        num_sms = d->sms;
+    }
+    const bool realw = kind == MRI_KIND_Q;
+    std::memset(plan, 0, sizeof(*plan));
+    if (N == 0) return MRI_OK;
+    if (M == 0) {
+        plan->launches = 2;   // zero fill of both outputs
+        return MRI_OK;
+    }
+    GroupPlan plans[4];
+    bool used[4];
+    group_plans(realw, B, M, N, num_sms, plans, used);
+    const GroupPlan& g0 = plans[realw ? 3 : group_index(B)];
+    plan->threads_per_cta = g0.shape.threads;
+    plan->voxels_per_thread = g0.shape.v;
+    plan->samples_per_tile = kTile;
+    plan->splits = g0.splits;
+    plan->voxel_ctas = g0.vblocks;
+    plan->tiles = g0.ntiles;
+    int64_t scratch = 0;
+    for (int64_t b0 = 0; b0 < B;) {
+        const int i = realw ? 3 : group_index(B - b0);
+        plan->coil_groups += 1;
+        plan->launches += 2 + (plans[i].splits > 1 ? 1 : 0);
+        const int64_t b = align256(plans[i].rec_bytes) + plans[i].part_bytes;
+        if (b > scratch) scratch = b;
+        b0 += plans[i].bc;
+    }
+    plan->scratch_bytes = scratch;
+    return MRI_OK;
+}
+
+mri_status mri_device_errors(unsigned int* bits, int clear)
+{
+    if (bits == nullptr) return MRI_ERR_NULL;
+    DeviceState* d = nullptr;
+    mri_status st = device_state(&d, nullptr);
+    if (st != MRI_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail();
+    if (cudaMemcpy(bits, d->err, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_fail();
+    if (clear) {
+        if (cudaMemset(d->err, 0, sizeof(unsigned int)) != cudaSuccess) return cuda_fail();
+        if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail();
+    }
+    return MRI_OK;
+}
+
+mri_status mri_timing_begin(void)
+{
+    DeviceState* d = nullptr;
+    mri_status st = device_state(&d, nullptr);
+    if (st != MRI_OK) return st;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    d->timing = true;
+    d->timed = 0;
+    return MRI_OK;
+}
+
+mri_status mri_timing_end(double* gather_ms, int64_t* launches)
+{
+    if (gather_ms == nullptr || launches == nullptr) return MRI_ERR_NULL;
+    DeviceState* d = nullptr;
+    mri_status st = device_state(&d, nullptr);
+    if (st != MRI_OK) return st;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    d->timing = false;
+    double total = 0.0;
+    for (int i = 0; i < d->timed; ++i) {
+        if (cudaEventSynchronize(d->ev[2 * i + 1]) != cudaSuccess) return cuda_fail();
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, d->ev[2 * i], d->ev[2 * i + 1]) != cudaSuccess)
+            return cuda_fail();
+        total += ms;
+    }
+    *gather_ms = total;
+    *launches = d->timed;
+    d->timed = 0;
+    return MRI_OK;
+}
+
+}  // extern "C"

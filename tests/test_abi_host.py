@@ -1,0 +1,163 @@
+"""The C ABI on a machine without a GPU: the library builds and loads, exports
+every function the headers declare, and rejects bad arguments with the
+documented status before any CUDA call.  The launch planner is host-only."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from non_cartesian_mri_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+OK, NULL, SIZE, ALIGN, NOT_DEVICE, MODE, CUDA, UNSUPPORTED = range(8)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = lib_build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(mri_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_the_entry_points():
+    names = declared_functions()
+    for n in ("mri_mu", "mri_fhd", "mri_q", "mri_fhd_batched", "mri_status_string",
+              "mri_plan_gather", "mri_device_errors", "mri_timing_begin", "mri_timing_end",
+              "mri_microbench"):
+        assert n in names
+
+
+def test_every_declared_function_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    lib.mri_status_string.restype = ctypes.c_char_p
+    seen = set()
+    for s in range(8):
+        txt = lib.mri_status_string(s).decode()
+        assert txt and txt not in seen
+        seen.add(txt)
+    assert lib.mri_status_string(99).decode() == "unknown status"
+
+
+P = ctypes.c_void_p
+I64 = ctypes.c_int64
+
+
+def _fhd(lib, ptrs, M, N, trig=1, acc=0):
+    f = lib.mri_fhd
+    f.argtypes = [P] * 10 + [I64, I64, P, P, ctypes.c_int, ctypes.c_int, P]
+    f.restype = ctypes.c_int
+    return f(*ptrs[:10], M, N, ptrs[10], ptrs[11], trig, acc, None)
+
+
+def fake(n=12, addr=0x100000):
+    """Distinct, aligned, never-dereferenced addresses."""
+    return [P(addr + 256 * i) for i in range(n)]
+
+
+def test_fhd_argument_checks_before_any_cuda_call(lib):
+    good = fake()
+    assert _fhd(lib, good, 10, 10, trig=7) == MODE
+    assert _fhd(lib, good, 10, 10, acc=2) == MODE
+    assert _fhd(lib, good, -1, 10) == SIZE
+    assert _fhd(lib, good, 10, -5) == SIZE
+    assert _fhd(lib, good, 1 << 40, 10) == SIZE
+    assert _fhd(lib, good, 10, 0) == OK                 # N == 0 is a no-op
+    for i in range(12):
+        bad = list(good)
+        bad[i] = P(None)
+        assert _fhd(lib, bad, 10, 10) == NULL, f"NULL in slot {i}"
+        bad[i] = P(0x100001 + 256 * i)
+        assert _fhd(lib, bad, 10, 10) == ALIGN, f"misaligned slot {i}"
+
+
+def test_sample_pointers_unused_when_M_is_zero(lib):
+    ptrs = fake()
+    for i in (0, 1, 2, 6, 7, 8, 9):          # kx ky kz rPhi iPhi rD iD
+        ptrs[i] = P(None)
+    # gets past the argument checks; stops at the device query without a GPU
+    assert _fhd(lib, ptrs, 0, 10) in (OK, CUDA, UNSUPPORTED)
+    ptrs[3] = P(None)                        # x is still required
+    assert _fhd(lib, ptrs, 0, 10) == NULL
+
+
+def test_batched_and_q_checks(lib):
+    fb = lib.mri_fhd_batched
+    fb.argtypes = [P] * 10 + [I64, I64, I64, P, P, ctypes.c_int, ctypes.c_int, P]
+    fb.restype = ctypes.c_int
+    g = fake()
+    assert fb(*g[:10], 0, 10, 10, g[10], g[11], 0, 0, None) == SIZE     # B = 0
+    assert fb(*g[:10], 2, 10, 10, g[10], g[11], 3, 0, None) == MODE
+    q = lib.mri_q
+    q.argtypes = [P] * 8 + [I64, I64, P, P, ctypes.c_int, ctypes.c_int, P]
+    q.restype = ctypes.c_int
+    assert q(*g[:8], 10, 10, P(None), g[9], 0, 0, None) == NULL
+    mu = lib.mri_mu
+    mu.argtypes = [P] * 6 + [I64, P]
+    mu.restype = ctypes.c_int
+    assert mu(*g[:6], -3, None) == SIZE
+    assert mu(*g[:6], 0, None) == OK
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("threads_per_cta", ctypes.c_int), ("voxels_per_thread", ctypes.c_int),
+                ("samples_per_tile", ctypes.c_int), ("splits", ctypes.c_int),
+                ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
+                ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
+                ("scratch_bytes", ctypes.c_int64)]
+
+
+def plan(lib, kind, B, M, N, sms=152):
+    p = Plan()
+    lib.mri_plan_gather.argtypes = [ctypes.c_int, I64, I64, I64, ctypes.c_int,
+                                    ctypes.POINTER(Plan)]
+    lib.mri_plan_gather.restype = ctypes.c_int
+    assert lib.mri_plan_gather(kind, B, M, N, sms, ctypes.byref(p)) == OK
+    return p
+
+
+def test_plan_covers_every_voxel_and_sample(lib):
+    for kind, B, M, N in [(0, 1, 262144, 128 ** 3), (1, 1, 1 << 20, 128 ** 3),
+                          (2, 8, 524288, 128 ** 3), (0, 1, 32768, 64 ** 3),
+                          (0, 1, 2048, 16 ** 3), (0, 1, 1, 1), (0, 1, 257, 2049)]:
+        p = plan(lib, kind, B, M, N)
+        assert p.voxel_ctas * p.threads_per_cta * p.voxels_per_thread >= N
+        assert (p.voxel_ctas - 1) * p.threads_per_cta * p.voxels_per_thread < N
+        assert p.tiles * p.samples_per_tile >= M > (p.tiles - 1) * p.samples_per_tile
+        assert 1 <= p.splits <= p.tiles
+        assert p.launches == p.coil_groups * 2 + (p.coil_groups if p.splits > 1 else 0)
+
+
+def test_plan_splits_samples_when_voxels_underfill_the_gpu(lib):
+    small = plan(lib, 0, 1, 32768, 64 ** 3)        # 128 voxel CTAs < 304 slots
+    assert small.splits > 1
+    # 1024 voxel CTAs on 304 slots is 3.37 waves: splitting must beat the tail
+    big = plan(lib, 0, 1, 262144, 128 ** 3)
+    waves = -(-big.voxel_ctas * big.splits // 304)
+    eff = big.voxel_ctas * big.splits / (waves * 304)
+    assert eff > 0.95
+
+
+def test_plan_coil_groups(lib):
+    assert plan(lib, 2, 13, 1000, 5000).coil_groups == 3      # 8 + 4 + 1
+    assert plan(lib, 2, 8, 1000, 5000).coil_groups == 1
+    assert plan(lib, 2, 17, 1000, 5000).coil_groups == 3      # 8 + 8 + 1
+    p = plan(lib, 0, 1, 0, 100)
+    assert p.launches == 2                                   # zero fill only
