@@ -125,6 +125,37 @@ mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz,
                            float* rFhD, float* iFhD,
                            mri_trig trig, int accumulate, void* stream);
 
+/*
+ * F^H D without any memory allocation.  The pages have no counterpart: this
+ * is an interface for callers that may not allocate GPU memory while they
+ * run -- a process whose device memory is reserved up front, a real-time
+ * reconstruction loop that must not stall in an allocator, or a framework
+ * that owns every allocation.  Arguments, results and edge cases are those
+ * of mri_fhd; the scratch it needs (the tile records and, when it splits the
+ * samples, the partial sums) lives in one fixed array of
+ * MRI_FHD_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - The call makes no cudaMalloc, cudaFree, pool or other allocating call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array: calls that may overlap on
+ *     the GPU (different streams, or different host threads) race and must be
+ *     serialised by the caller.  Each call rewrites every byte of the array it
+ *     reads, so nothing in it needs to start at zero.
+ *   - M is limited by the records: ceil(M/256) * 5120 bytes must fit in the
+ *     array (M <= 1,677,568 for 32 MiB), else MRI_ERR_SIZE.  The sample
+ *     splits are capped to the partial sums that fit after the records (for
+ *     a 128^3 grid none do, and the call runs unsplit).
+ */
+#define MRI_FHD_NOALLOC_SCRATCH_BYTES (32ll * 1024 * 1024)
+mri_status mri_fhd_noalloc(const float* kx, const float* ky, const float* kz,
+                           const float* x, const float* y, const float* z,
+                           const float* rPhi, const float* iPhi,
+                           const float* rD, const float* iD,
+                           int64_t M, int64_t N, float* rFhD, float* iFhD,
+                           mri_trig trig, int accumulate, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
 

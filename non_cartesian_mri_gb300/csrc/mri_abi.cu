@@ -361,6 +361,30 @@ mri_status prepare(int trig, int accumulate, int64_t B, int64_t M, int64_t N,
 
 }  // namespace
 
+namespace mri {
+
+// Device address of the error word on device `dev` (which must be current):
+// a symbol lookup, cached per device, that creates no pool and allocates
+// nothing.  Used by the allocation-free entry point.
+unsigned int* error_word_address(int dev)
+{
+    static std::mutex m;
+    static unsigned int* addr[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(m);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = static_cast<unsigned int*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace mri
+
 extern "C" {
 
 mri_status mri_mu(const float* rPhi, const float* iPhi, const float* rD, const float* iD,
