@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--trig", choices=["fast", "accurate", "fast_rr"], default="fast")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--grid-edge", type=int, default=None,
+                    help="override the voxel-grid edge L (smaller cases for profiling)")
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the accurate/Q/batched sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -379,7 +381,7 @@ def run_ours(args):
 
     rates = unit_rates(mri)
 
-    w = slab(wl.make_workload(args.workload), rank)
+    w = slab(wl.make_workload(args.workload, L=args.grid_edge), rank)
     kind = w.kind
     t = to_dev(w, torch)
     out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
@@ -416,7 +418,7 @@ def run_ours(args):
     del t, out
     torch.cuda.empty_cache()
 
-    if not args.no_paths and args.workload == HEADLINE and world == 1:
+    if not args.no_paths and args.workload == HEADLINE and world == 1 and not args.grid_edge:
         paths = {}
         for name, wname, trig in (("fhd_accurate", HEADLINE, "accurate"),
                                   ("q_fast", "q_128", "fast"),
@@ -444,7 +446,7 @@ def run_ours(args):
         line["paths"] = paths
 
     if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(wl.make_workload(args.workload))
+        line["cpu_baseline"] = cpu_baseline(wl.make_workload(args.workload, L=args.grid_edge))
     errs = mri.device_errors(clear=True)
     if errs:
         line["device_errors"] = errs

@@ -44,7 +44,8 @@ class _Plan(ctypes.Structure):
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The library to load: ``MRI_LIB`` if set (a variant build), else the default."""
+    return os.environ.get("MRI_LIB") or _build.LIB
 
 
 def load():

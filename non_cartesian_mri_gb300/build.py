@@ -47,19 +47,27 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libmri.so; return its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compile and link libmri.so; return its path.
+
+    ``defines`` (e.g. ``["MRI_NP_FP32_Q=3"]``) and ``out`` build a variant
+    library elsewhere, for tuning sweeps; the default build is ``LIB``.
+    """
+    lib = LIB if out is None else out
+    if not force and out is None and not defines and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = BUILD if out is None else os.path.dirname(os.path.abspath(out))
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
+    dflags = [f"-D{d}" for d in defines]
+    tag = "" if out is None else "_" + os.path.basename(out).replace(".so", "")
 
     def compile_unit(unit):
         src = os.path.join(CSRC, unit)
-        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, unit.replace(".cu", f"{tag}.o"))
+        cmd = [nvcc, *ARCH, *FLAGS, *dflags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
-        with open(os.path.join(BUILD, f"ptxas_{unit.replace('.cu', '')}.log"), "w") as fh:
+        with open(os.path.join(bdir, f"ptxas_{unit.replace('.cu', '')}{tag}.log"), "w") as fh:
             fh.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {unit}:\n{r.stderr[-4000:]}")
@@ -69,13 +77,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
         objs = list(ex.map(compile_unit, UNITS))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libmri.so failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -28,14 +28,23 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "sincospi_coeffs.h"
 
 namespace mri {
 
 enum TrigMode : int {
-    TRIG_ACCURATE = 0,  // sincospif on the phase in half-turns (FP32 pipe)
-    TRIG_FAST = 1,      // __sincosf (MUFU) on the phase in radians
+    TRIG_ACCURATE = 0,  // minimax polynomials on the FP32 pipe, phase in quarter turns
+    TRIG_FAST = 1,      // MUFU on the phase in radians; a fixed share of voxels on the FP32 pipe
     TRIG_FAST_RR = 2,   // MUFU after explicit reduction of the phase to [-1/2, 1/2] turn
 };
+
+// Voxels per thread whose fast-path trig runs on the FP32 pipe (see Shape).
+#ifndef MRI_NP_FP32_FHD
+#define MRI_NP_FP32_FHD 0
+#endif
+#ifndef MRI_NP_FP32_Q
+#define MRI_NP_FP32_Q 1
+#endif
 
 constexpr int kTile = 256;   // samples per k-tile
 constexpr int kStages = 3;   // tiles resident per CTA
@@ -56,13 +65,34 @@ struct Rec {
     static constexpr uint32_t TILE_BYTES = TILE_FLOATS * 4u;
 };
 
+// Launch shape of the coil-group kernels (BC >= 4), overridable for sweeps.
+#ifndef MRI_COIL_V
+#define MRI_COIL_V 2
+#endif
+#ifndef MRI_COIL_THREADS
+#define MRI_COIL_THREADS 256
+#endif
+#ifndef MRI_COIL_UNROLL
+#define MRI_COIL_UNROLL 1
+#endif
+constexpr int kCoilUnroll = MRI_COIL_UNROLL;
+
 // Per-kernel launch shape.
 template <int BC, bool REALW>
 struct Shape {
-    static constexpr int THREADS = 256;
-    static constexpr int V = (BC >= 4) ? 4 : 8;   // voxels per thread
-    static constexpr int MIN_BLOCKS = 2;
+    static constexpr int THREADS = (BC >= 4) ? MRI_COIL_THREADS : 256;
+    static constexpr int V = (BC >= 4) ? MRI_COIL_V : 8;   // voxels per thread
+    static constexpr int MIN_BLOCKS = 512 / THREADS;
     static constexpr int VOXELS_PER_CTA = THREADS * V;
+    // Fast trig: of the V voxels a thread holds, the last NP_FP32 take their
+    // sin/cos from the quarter-turn polynomial on the FP32 pipe instead of the
+    // SFU.  The SFU delivers 16 results per SM per clock and binds F^H D and
+    // Q, while issue slots are left over (59 % issue-active on F^H D).  On the
+    // 128^3 workloads one voxel in 8 on the FP32 pipe makes Q 6 % faster and
+    // F^H D 2 % slower (it spends 4 FFMA per pair on the multiply-accumulate
+    // against Q's 2, so fewer slots are left); coil groups are FP32-bound and
+    // keep every pair on the SFU.
+    static constexpr int NP_FP32 = REALW ? MRI_NP_FP32_Q : (BC == 1 ? MRI_NP_FP32_FHD : 0);
     static constexpr size_t SMEM = size_t(kStages) * Rec<BC, REALW>::TILE_BYTES;
 };
 
@@ -73,7 +103,7 @@ struct PrepParams {
     int64_t M;
     int64_t b0;
     int64_t ntiles;
-    float kscale;           // 2 (half-turns), 2*pi (radians) or 1 (turns)
+    float kscale;           // 4 (quarter turns), 2*pi (radians) or 1 (turns)
     float* rec;
 };
 
@@ -141,18 +171,52 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
 // ---------------------------------------------------------------------------
 // trig on one phase value
 // ---------------------------------------------------------------------------
+
+// sin and cos of (pi/2) u for u in quarter turns (|u| < 2^22), on the FP32
+// pipe: exact reduction q = rint(u), f = u - q in [-1/2, 1/2] (adding and
+// removing 1.5 * 2^23 rounds to an integer and leaves q in the low mantissa
+// bits of the sum), minimax polynomials for sin and cos of (pi/2) f
+// (coefficients from gen_sincospi.py), then a rotation by q quarter turns:
+// odd q swaps sin and cos; sin changes sign when bit 1 of q is set, cos when
+// bit 1 of q + 1 is.
+__device__ __forceinline__ void sincos_quarter_turns(float u, float& s, float& c)
+{
+    using Coef = SinCosQuarter;
+    const float v = u + 12582912.0f;
+    const float f = u - (v - 12582912.0f);
+    const float f2 = f * f;
+    float p = Coef::P(Coef::P_TERMS - 1);
+#pragma unroll
+    for (int i = Coef::P_TERMS - 2; i >= 0; --i) p = fmaf(p, f2, Coef::P(i));
+    float q = Coef::Q(Coef::Q_TERMS - 1);
+#pragma unroll
+    for (int i = Coef::Q_TERMS - 2; i >= 0; --i) q = fmaf(q, f2, Coef::Q(i));
+    const float sf = f * p;
+    const unsigned qi = __float_as_uint(v);
+    const bool odd = (qi & 1u) != 0u;
+    const float s_sel = odd ? q : sf;
+    const float c_sel = odd ? sf : q;
+    const unsigned m1 = qi << 30;   // bit 31 = bit 1 of q
+    const unsigned m0 = qi << 31;   // bit 31 = bit 0 of q
+    s = __uint_as_float(__float_as_uint(s_sel) ^ (m1 & 0x80000000u));
+    c = __uint_as_float(__float_as_uint(c_sel) ^ ((m1 ^ m0) & 0x80000000u));
+}
+
+// `on_fp32` is a compile-time constant after unrolling (the voxel slot).
 template <int TRIG>
-__device__ __forceinline__ void phase_sincos(float ph, float& s, float& c)
+__device__ __forceinline__ void phase_sincos(float ph, bool on_fp32, float& s, float& c)
 {
     if (TRIG == TRIG_ACCURATE) {
-        // records hold 2k, so ph = 2 (k.x) and sin(pi*ph) = sin(2 pi k.x)
-        sincospif(ph, &s, &c);
+        // records hold 4k, so ph is the phase in quarter turns
+        sincos_quarter_turns(ph, s, c);
     } else if (TRIG == TRIG_FAST) {
         // records hold 2 pi k, so ph is the phase in radians
-        __sincosf(ph, &s, &c);
+        if (on_fp32)
+            sincos_quarter_turns(ph * 0.636619772367581343076f, s, c);
+        else
+            __sincosf(ph, &s, &c);
     } else {
         // records hold k in turns; subtract the nearest integer exactly
-        // (adding and removing 1.5 * 2^23 rounds to an integer for |ph| < 2^22)
         const float rn = (ph + 12582912.0f) - 12582912.0f;
         const float r = ph - rn;
         __sincosf(r * 6.28318530717958647692f, &s, &c);
@@ -231,7 +295,7 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
         if (ok) {
             if (!R::AOS) {
                 // four samples per step: one broadcast 16-byte load per field
-#pragma unroll 2
+#pragma unroll 1
                 for (int j = 0; j < kTile; j += 4) {
                     const float4 kx4 = *reinterpret_cast<const float4*>(tile + 0 * kTile + j);
                     const float4 ky4 = *reinterpret_cast<const float4*>(tile + 1 * kTile + j);
@@ -251,7 +315,7 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
                             const float ph =
                                 fmaf(kzs[q], zv[v], fmaf(kys[q], yv[v], kxs[q] * xv[v]));
                             float sn, cs;
-                            phase_sincos<TRIG>(ph, sn, cs);
+                            phase_sincos<TRIG>(ph, v >= V - S::NP_FP32, sn, cs);
                             if (REALW) {
                                 pr[v][0] = fmaf(w0s[q], cs, pr[v][0]);
                                 pi[v][0] = fmaf(w0s[q], sn, pi[v][0]);
@@ -267,7 +331,7 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
                 }
             } else {
                 // coil groups: one record per step, one sin/cos per voxel for all coils
-#pragma unroll 1
+#pragma unroll kCoilUnroll
                 for (int j = 0; j < kTile; ++j) {
                     const float4* rec4 = reinterpret_cast<const float4*>(tile + j * R::F4);
                     float f[R::F4];
@@ -283,7 +347,7 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
                     for (int v = 0; v < V; ++v) {
                         const float ph = fmaf(f[2], zv[v], fmaf(f[1], yv[v], f[0] * xv[v]));
                         float sn, cs;
-                        phase_sincos<TRIG>(ph, sn, cs);
+                        phase_sincos<TRIG>(ph, v >= V - S::NP_FP32, sn, cs);
 #pragma unroll
                         for (int b = 0; b < BC; ++b) {
                             const float rm = f[3 + b], im = f[3 + BC + b];

@@ -153,7 +153,7 @@ extern "C" mri_status mri_fhd_noalloc(const float* kx, const float* ky, const fl
     float* rec = reinterpret_cast<float*>(d->scratch);
     float* part = reinterpret_cast<float*>(d->scratch + rec_bytes);
 
-    const float kscale = tr == MRI_TRIG_ACCURATE ? 2.0f
+    const float kscale = tr == MRI_TRIG_ACCURATE ? 4.0f
                          : tr == MRI_TRIG_FAST   ? 6.28318530717958647692f
                                                  : 1.0f;
     mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, ntiles, kscale, rec};
