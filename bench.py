@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--grid-edge", type=int, default=None,
                     help="override the voxel-grid edge L (smaller cases for profiling)")
+    ap.add_argument("--grid", action="store_true",
+                    help="run F^H D / Q through the separable-grid entry points")
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the accurate/Q/batched sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -193,10 +195,17 @@ def to_dev(w: wl.Workload, torch):
     if w.rD is not None:
         out["rD"] = d(w.rD)
         out["iD"] = d(w.iD)
+    out["xs"], out["ys"], out["zs"] = (d(a) for a in w.axes())
     return out
 
 
-def call(mri, kind, t, trig, out=None):
+def call(mri, kind, t, trig, out=None, grid=False):
+    if grid and kind == "fhd":
+        return mri.fhd_grid(t["kx"], t["ky"], t["kz"], t["xs"], t["ys"], t["zs"], t["rPhi"],
+                            t["iPhi"], t["rD"], t["iD"], trig=trig, out=out)
+    if grid and kind == "q":
+        return mri.q_grid(t["kx"], t["ky"], t["kz"], t["xs"], t["ys"], t["zs"], t["rPhi"],
+                          t["iPhi"], trig=trig, out=out)
     if kind == "fhd":
         return mri.fhd(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"], t["rPhi"], t["iPhi"],
                        t["rD"], t["iD"], trig=trig, out=out)
@@ -386,9 +395,11 @@ def run_ours(args):
     t = to_dev(w, torch)
     out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
            torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"))
-    plan = mri.plan(kind, w.M, w.N, B=w.B)
+    grid = args.grid and kind in ("fhd", "q")
+    plan = (mri.plan_grid(kind, w.M, w.L, w.L, w.L) if grid
+            else mri.plan(kind, w.M, w.N, B=w.B))
     with ClockSampler(local) as clk:
-        res = timed_steps(torch, mri, dist, lambda: call(mri, kind, t, args.trig, out),
+        res = timed_steps(torch, mri, dist, lambda: call(mri, kind, t, args.trig, out, grid),
                           args.steps, args.warmup, flush)
     clocks = clk.summary()
     mean_s = dist.max(statistics.mean(res["step_ms"]) / 1e3)
@@ -401,6 +412,8 @@ def run_ours(args):
         "data": "synthetic (seeded generators, no dataset)",
         "config": {"workload": f"{w.name}: {wl.WORKLOADS[w.name]}", "voxels": w.N,
                    "samples": w.M, "coils": w.B, "trig": args.trig,
+                   "entry": ("mri_fhd_grid" if kind == "fhd" else "mri_q_grid") if grid
+                   else {"fhd": "mri_fhd", "q": "mri_q", "fhd_batched": "mri_fhd_batched"}[kind],
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
                    "parallelism": "one independent voxel slab per rank" if world > 1
                    else "single GPU",

@@ -156,6 +156,33 @@ mri_status mri_fhd_noalloc(const float* kx, const float* ky, const float* kz,
                            int64_t M, int64_t N, float* rFhD, float* iFhD,
                            mri_trig trig, int accumulate, void* stream);
 
+/*
+ * F^H D and Q on a separable voxel grid: voxel n = (iz*ny + iy)*nx + ix sits
+ * at (xs[ix], ys[iy], zs[iz]) (x fastest), the layout of every image the
+ * chapter reconstructs.  Same sums as mri_fhd / mri_q over those N = nx*ny*nz
+ * voxels; xs, ys, zs are device arrays of nx, ny, nz floats, outputs [N].
+ * The exponential factors, e^{i2pi k.x} = e^{i2pi kx x} e^{i2pi (ky y + kz z)}
+ * (the grid form of the gather's phase, Fig. 17.11), so per tile of samples
+ * the kernel tabulates the x factor per column and Mu times the (y, z)
+ * factor per row and spends one complex multiply-accumulate per
+ * voxel-sample pair; sin/cos are evaluated per (sample, column) and
+ * (sample, row) only.  The table kernel covers nx in {16, 32, 64, 128, 256};
+ * other grids are expanded to coordinates and take the general kernel.
+ * Edge cases as mri_fhd.
+ */
+mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz,
+                        const float* xs, int nx, const float* ys, int ny,
+                        const float* zs, int nz,
+                        const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                        int64_t M, float* rFhD, float* iFhD,
+                        mri_trig trig, int accumulate, void* stream);
+mri_status mri_q_grid(const float* kx, const float* ky, const float* kz,
+                      const float* xs, int nx, const float* ys, int ny,
+                      const float* zs, int nz,
+                      const float* rPhi, const float* iPhi,
+                      int64_t M, float* rQ, float* iQ,
+                      mri_trig trig, int accumulate, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
 
@@ -180,6 +207,10 @@ typedef struct mri_plan {
 
 mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,
                            mri_plan* plan);
+
+/* The same for mri_fhd_grid (kind MRI_KIND_FHD) and mri_q_grid (MRI_KIND_Q). */
+mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
+                         mri_plan* plan);
 
 /*
  * Device-side error bits of the current device (bit 0: a k-tile wait timed

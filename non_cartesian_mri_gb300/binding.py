@@ -77,6 +77,14 @@ def load():
         lib.mri_device_errors.restype = ctypes.c_int
         lib.mri_microbench.argtypes = [I, I, I, I64, P, P, P]
         lib.mri_microbench.restype = ctypes.c_int
+        lib.mri_fhd_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 4
+                                     + [I64, P, P, I, I, P])
+        lib.mri_fhd_grid.restype = ctypes.c_int
+        lib.mri_q_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 2
+                                   + [I64, P, P, I, I, P])
+        lib.mri_q_grid.restype = ctypes.c_int
+        lib.mri_plan_grid.argtypes = [I, I64, I, I, I, I, ctypes.POINTER(_Plan)]
+        lib.mri_plan_grid.restype = ctypes.c_int
         lib.mri_timing_begin.argtypes = []
         lib.mri_timing_begin.restype = ctypes.c_int
         lib.mri_timing_end.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -221,6 +229,51 @@ def fhd_batched(kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, *, trig="fast", accumul
                                       _ptr(r), _ptr(i), TRIG[trig], int(bool(accumulate)),
                                       _stream_handle(stream)), "mri_fhd_batched")
     return m.result((r, i))
+
+
+def fhd_grid(kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD, *, trig="fast", accumulate=False,
+             out=None, stream=None):
+    """F^H D on the separable grid xs x ys x zs; returns (rFhD, iFhD) [N], x fastest."""
+    m = _Marshal([kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD])
+    kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD = m.tensors
+    M = kx.shape[0]
+    _same_len("sample", [kx, ky, kz, rPhi, iPhi, rD, iD], M)
+    for t in (xs, ys, zs):
+        if t.dim() != 1:
+            raise ValueError("grid axes must be 1-D")
+    nx, ny, nz = xs.shape[0], ys.shape[0], zs.shape[0]
+    r, i = _outputs(out, (nx * ny * nz,), m.device)
+    with torch.cuda.device(m.device):
+        _check(load().mri_fhd_grid(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(xs), nx, _ptr(ys), ny,
+                                   _ptr(zs), nz, _ptr(rPhi), _ptr(iPhi), _ptr(rD), _ptr(iD), M,
+                                   _ptr(r), _ptr(i), TRIG[trig], int(bool(accumulate)),
+                                   _stream_handle(stream)), "mri_fhd_grid")
+    return m.result((r, i))
+
+
+def q_grid(kx, ky, kz, xs, ys, zs, rPhi, iPhi, *, trig="fast", accumulate=False, out=None,
+           stream=None):
+    """Q on the separable grid xs x ys x zs; returns (rQ, iQ) [N], x fastest."""
+    m = _Marshal([kx, ky, kz, xs, ys, zs, rPhi, iPhi])
+    kx, ky, kz, xs, ys, zs, rPhi, iPhi = m.tensors
+    M = kx.shape[0]
+    _same_len("sample", [kx, ky, kz, rPhi, iPhi], M)
+    nx, ny, nz = xs.shape[0], ys.shape[0], zs.shape[0]
+    r, i = _outputs(out, (nx * ny * nz,), m.device)
+    with torch.cuda.device(m.device):
+        _check(load().mri_q_grid(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(xs), nx, _ptr(ys), ny,
+                                 _ptr(zs), nz, _ptr(rPhi), _ptr(iPhi), M, _ptr(r), _ptr(i),
+                                 TRIG[trig], int(bool(accumulate)), _stream_handle(stream)),
+               "mri_q_grid")
+    return m.result((r, i))
+
+
+def plan_grid(kind: str, M: int, nx: int, ny: int, nz: int, num_sms: int = 0) -> dict:
+    """The launch shape of mri_fhd_grid / mri_q_grid."""
+    p = _Plan()
+    _check(load().mri_plan_grid(KIND[kind], M, nx, ny, nz, num_sms, ctypes.byref(p)),
+           "mri_plan_grid")
+    return {name: getattr(p, name) for name, _ in _Plan._fields_}
 
 
 def plan(kind: str, M: int, N: int, B: int = 1, num_sms: int = 0) -> dict:

@@ -54,14 +54,14 @@ constexpr int kStages = 3;   // tiles resident per CTA
 //       F^H D: kx ky kz rMu iMu     Q: kx ky kz w
 //   coil groups (BC > 1): array of records [kTile][F4]
 //       kx ky kz rMu_0..rMu_{BC-1} iMu_0..iMu_{BC-1} (zero padding to F4)
-template <int BC, bool REALW>
+template <int BC, bool REALW, int TILE = kTile>
 struct Rec {
     static_assert(!REALW || BC == 1, "a real weight has one coil");
     static constexpr int F = REALW ? 4 : 3 + 2 * BC;
     static constexpr bool AOS = BC > 1;
     static constexpr int F4 = (F + 3) / 4 * 4;
     static constexpr int STRIDE = AOS ? F4 : F;
-    static constexpr int TILE_FLOATS = kTile * STRIDE;
+    static constexpr int TILE_FLOATS = TILE * STRIDE;
     static constexpr uint32_t TILE_BYTES = TILE_FLOATS * 4u;
 };
 
@@ -126,15 +126,15 @@ struct GatherParams {
 // ---------------------------------------------------------------------------
 // prep: cmpMu fused with the tile-record layout
 // ---------------------------------------------------------------------------
-template <int BC, bool REALW>
+template <int BC, bool REALW, int TILE = kTile>
 __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
 {
-    using R = Rec<BC, REALW>;
-    const int64_t total = p.ntiles * kTile;
+    using R = Rec<BC, REALW, TILE>;
+    const int64_t total = p.ntiles * TILE;
     for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < total;
          m += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t tile = m / kTile;
-        const int j = int(m - tile * kTile);
+        const int64_t tile = m / TILE;
+        const int j = int(m - tile * TILE);
         float* base = p.rec + tile * R::TILE_FLOATS;
         float f[R::F4];
 #pragma unroll
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
                 dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
         } else {
 #pragma unroll
-            for (int i = 0; i < R::F; ++i) base[i * kTile + j] = f[i];
+            for (int i = 0; i < R::F; ++i) base[i * TILE + j] = f[i];
         }
     }
 }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gather.cuh"
+#include "gather_grid.cuh"
 
 namespace mri {
 
@@ -31,6 +32,12 @@ cudaError_t launch_mu(const float* rPhi, const float* iPhi, const float* rD, con
                       float* rMu, float* iMu, int64_t M, int grid, cudaStream_t s);
 
 cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
+
+// separable-grid path (kernels_grid.cu)
+cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_prep_grid(bool realw, const PrepParams& p, int grid, cudaStream_t s);
+cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
+                               int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);
 
 // per-TU dispatchers
 cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, dim3 grid,

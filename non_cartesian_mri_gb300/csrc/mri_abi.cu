@@ -140,11 +140,13 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // gather costs the same, so the run time is (waves of CTAs) x (tiles per CTA),
 // plus a per-CTA fixed cost and the reduction of the splits.  Costs are in
 // units of one tile of gather work.
-int choose_splits(int64_t ntiles, int64_t vblocks, int64_t slots, int bc, int64_t N)
+// tile_us: rough time of one tile of one CTA; overhead_tiles: a CTA's fixed
+// cost (prologue, first copy, epilogue) in tiles.
+int choose_splits(int64_t ntiles, int64_t vblocks, int64_t slots, int bc, int64_t N,
+                  double tile_us = 70.0, double overhead_tiles = 0.1)
 {
-    const double overhead_tiles = 0.1;     // prologue / epilogue of one CTA
-    const double launch_tiles = 0.07;      // one extra kernel launch
-    const double bytes_per_tile = 3.5e8;   // HBM bytes moved in one tile's time
+    const double launch_tiles = 5.0 / tile_us;             // one extra kernel launch, ~5 us
+    const double bytes_per_tile = 5e6 * tile_us;           // HBM bytes in one tile's time
     int best = 1;
     double best_cost = 0.0;
     const int64_t max_s = ntiles < 1024 ? ntiles : 1024;
@@ -333,6 +335,131 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
     return st;
 }
 
+// ---------------------------------------------------------------------------
+// separable grids
+// ---------------------------------------------------------------------------
+struct GridPlan {
+    bool table_kernel;      // false: coordinates expanded, general kernel
+    int64_t ntiles;
+    int64_t vblocks;
+    int rows_per_cta;
+    int splits;
+    int64_t rec_bytes;
+    int64_t part_bytes;
+    int ctas_per_sm;
+};
+
+GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
+{
+    GridPlan g{};
+    g.table_kernel = mri::grid_kernel_fits(nx);
+    if (!g.table_kernel) return g;
+    const int64_t N = int64_t(nx) * ny * nz;
+    g.rows_per_cta = mri::kGridVoxelsPerCta / nx;
+    g.ntiles = ceil_div(M, mri::kGridTile);
+    g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
+    const size_t smem = mri::grid_smem_bytes(nx, realw);
+    g.ctas_per_sm = smem <= 110 * 1024 ? 2 : 1;
+    const int64_t slots = int64_t(sms) * g.ctas_per_sm;
+    g.splits = (g.ntiles > 0 && g.vblocks > 0)
+                   ? choose_splits(g.ntiles, g.vblocks, slots > 0 ? slots : 1, 1, N, 3.0, 1.0)
+                   : 1;
+    g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 5) * mri::kGridTile * 4;
+    g.part_bytes = g.splits > 1 ? int64_t(g.splits) * 2 * N * 4 : 0;
+    return g;
+}
+
+mri_status run_grid_call(bool realw, const float* kx, const float* ky, const float* kz,
+                         const float* xs, int nx, const float* ys, int ny, const float* zs,
+                         int nz, const float* rPhi, const float* iPhi, const float* rD,
+                         const float* iD, int64_t M, float* out_r, float* out_i, int trig,
+                         int accumulate, DeviceState* d, cudaStream_t s)
+{
+    const int64_t N = int64_t(nx) * ny * nz;
+    if (M == 0) {
+        if (!accumulate) {
+            if (mri::launch_zero(out_r, N, grid_for(N, d->sms), s) != cudaSuccess ||
+                mri::launch_zero(out_i, N, grid_for(N, d->sms), s) != cudaSuccess)
+                return cuda_fail();
+        }
+        return MRI_OK;
+    }
+    const GridPlan g = plan_grid(realw, M, nx, ny, nz, d->sms);
+    if (!g.table_kernel) {
+        // expand the coordinates and take the general kernel
+        float* xyz = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
+                                    s) != cudaSuccess)
+            return cuda_fail();
+        mri_status st = MRI_OK;
+        if (mri::launch_expand_grid(xs, ys, zs, nx, ny, N, xyz, xyz + N, xyz + 2 * N,
+                                    grid_for(N, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+        if (st == MRI_OK)
+            st = run_gather_call(realw, 1, kx, ky, kz, xyz, xyz + N, xyz + 2 * N, rPhi, iPhi, rD,
+                                 iD, M, N, out_r, out_i, trig, accumulate, d, s);
+        if (cudaFreeAsync(xyz, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+        return st;
+    }
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                size_t(align256(g.rec_bytes) + g.part_bytes), d->pool,
+                                s) != cudaSuccess)
+        return cuda_fail();
+    float* rec = reinterpret_cast<float*>(scratch);
+    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
+    mri_status st = MRI_OK;
+    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
+    if (mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * mri::kGridTile, d->sms), s) !=
+        cudaSuccess)
+        st = cuda_fail();
+    mri::GridParams gp{};
+    gp.rec = rec;
+    gp.ntiles = g.ntiles;
+    gp.splits = g.splits;
+    gp.xs = xs;
+    gp.ys = ys;
+    gp.zs = zs;
+    gp.nx = nx;
+    gp.ny = ny;
+    gp.nz = nz;
+    gp.rows_per_cta = g.rows_per_cta;
+    gp.err = d->err;
+    if (g.splits == 1) {
+        gp.out_r = out_r;
+        gp.out_i = out_i;
+        gp.split_stride = 0;
+        gp.accumulate = accumulate;
+    } else {
+        gp.out_r = part;
+        gp.out_i = part + N;
+        gp.split_stride = 2 * N;
+        gp.accumulate = 0;
+    }
+    if (st == MRI_OK) {
+        cudaEvent_t* ev = timing_slot(d);
+        if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
+        const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
+        if (st == MRI_OK && mri::launch_grid(realw, trig, gp, grid, s) != cudaSuccess)
+            st = cuda_fail();
+        if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
+    }
+    if (st == MRI_OK && g.splits > 1) {
+        if (mri::launch_reduce(part, g.splits, 1, N, out_r, out_i, N, accumulate,
+                               grid_for(2 * N, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
+mri_status check_grid_dims(int nx, int ny, int nz, int64_t M)
+{
+    if (nx < 0 || ny < 0 || nz < 0 || M < 0 || M > kMaxM) return MRI_ERR_SIZE;
+    if (int64_t(nx) * ny * nz > kMaxN) return MRI_ERR_SIZE;
+    return MRI_OK;
+}
+
 mri_status check_sizes(int64_t B, int64_t M, int64_t N)
 {
     if (B < 1 || M < 0 || N < 0) return MRI_ERR_SIZE;
@@ -446,6 +573,85 @@ mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz, co
     if (st != MRI_OK || N == 0) return st;
     return run_gather_call(false, B, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, M, N, rFhD, iFhD,
                            int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz, const float* xs,
+                        int nx, const float* ys, int ny, const float* zs, int nz,
+                        const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                        int64_t M, float* rFhD, float* iFhD, mri_trig trig, int accumulate,
+                        void* stream)
+{
+    mri_status st = check_mode(int(trig), accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_grid_dims(nx, ny, nz, M)) != MRI_OK) return st;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* sp[7] = {kx, ky, kz, rPhi, iPhi, rD, iD};
+    const void* vp[5] = {xs, ys, zs, rFhD, iFhD};
+    DeviceState* d = nullptr;
+    if ((st = prepare(int(trig), accumulate, 1, M, N, sp, 7, vp, 5, &d)) != MRI_OK || N == 0)
+        return st;
+    return run_grid_call(false, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, rD, iD, M, rFhD,
+                         iFhD, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_q_grid(const float* kx, const float* ky, const float* kz, const float* xs, int nx,
+                      const float* ys, int ny, const float* zs, int nz, const float* rPhi,
+                      const float* iPhi, int64_t M, float* rQ, float* iQ, mri_trig trig,
+                      int accumulate, void* stream)
+{
+    mri_status st = check_mode(int(trig), accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_grid_dims(nx, ny, nz, M)) != MRI_OK) return st;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* sp[5] = {kx, ky, kz, rPhi, iPhi};
+    const void* vp[5] = {xs, ys, zs, rQ, iQ};
+    DeviceState* d = nullptr;
+    if ((st = prepare(int(trig), accumulate, 1, M, N, sp, 5, vp, 5, &d)) != MRI_OK || N == 0)
+        return st;
+    return run_grid_call(true, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, nullptr, nullptr,
+                         M, rQ, iQ, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
+                         mri_plan* plan)
+{
+    if (plan == nullptr) return MRI_ERR_NULL;
+    if (kind != MRI_KIND_FHD && kind != MRI_KIND_Q) return MRI_ERR_MODE;
+    mri_status st = check_grid_dims(nx, ny, nz, M);
+    if (st != MRI_OK) return st;
+    if (num_sms < 0) return MRI_ERR_SIZE;
+    if (num_sms == 0) {
+        DeviceState* d = nullptr;
+        if ((st = device_state(&d, nullptr)) != MRI_OK && st != MRI_ERR_UNSUPPORTED_DEVICE)
+            return st;
+        num_sms = d->sms;
+    }
+    const bool realw = kind == MRI_KIND_Q;
+    const int64_t N = int64_t(nx) * ny * nz;
+    std::memset(plan, 0, sizeof(*plan));
+    if (N == 0) return MRI_OK;
+    if (M == 0) {
+        plan->launches = 2;
+        return MRI_OK;
+    }
+    const GridPlan g = plan_grid(realw, M, nx, ny, nz, num_sms);
+    if (!g.table_kernel) {
+        // expanded coordinates, then the general plan
+        st = mri_plan_gather(kind, 1, M, N, num_sms, plan);
+        plan->launches += 1;
+        plan->scratch_bytes += 3 * N * 4;
+        return st;
+    }
+    plan->threads_per_cta = mri::kGridThreads;
+    plan->voxels_per_thread = mri::kGridV;
+    plan->samples_per_tile = mri::kGridTile;
+    plan->splits = g.splits;
+    plan->voxel_ctas = g.vblocks;
+    plan->tiles = g.ntiles;
+    plan->coil_groups = 1;
+    plan->launches = 2 + (g.splits > 1 ? 1 : 0);
+    plan->scratch_bytes = align256(g.rec_bytes) + g.part_bytes;
+    return MRI_OK;
 }
 
 const char* mri_status_string(mri_status status)

@@ -47,6 +47,13 @@ def voxel_grid(L: int, Ly: int | None = None, Lz: int | None = None):
             z.reshape(-1).astype(F32))
 
 
+def grid_axes(L: int, Ly: int | None = None, Lz: int | None = None):
+    """The axes of voxel_grid: xs, ys, zs with voxel_grid = xs x ys x zs, x fastest."""
+    Ly = L if Ly is None else Ly
+    Lz = L if Lz is None else Lz
+    return tuple((np.arange(n) - n // 2).astype(F32) for n in (L, Ly, Lz))
+
+
 def voxel_subset(N: int, count: int, seed: int) -> np.ndarray:
     """Sorted, distinct voxel indices (int64) drawn uniformly from range(N)."""
     count = min(count, N)
@@ -150,6 +157,10 @@ class Workload:
     @property
     def pairs(self) -> int:
         return self.M * self.N
+
+    def axes(self):
+        """xs, ys, zs of the workload's cubic voxel grid (x, y, z = their product)."""
+        return grid_axes(self.L)
 
 
 WORKLOADS = {

@@ -1,0 +1,111 @@
+"""The separable-grid path (mri_fhd_grid / mri_q_grid) against the oracle.
+
+The oracle gets the expanded voxel coordinates of the same grid; tolerances
+as for the general path (1e-5 accurate, 2e-4 fast).  Covers the table kernel
+(nx in 16..256), the fallback through expanded coordinates (other nx), ragged
+row counts, ragged sample counts, non-uniform axes and accumulate.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from non_cartesian_mri_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"accurate": 1e-5, "fast": 2e-4, "fast_rr": 2e-4}
+
+
+@pytest.fixture(scope="module")
+def mri():
+    from non_cartesian_mri_gb300 import build
+    build.build()
+    import non_cartesian_mri_gb300 as m
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def cplx(r, i):
+    return r.cpu().numpy().astype(np.float64) + 1j * i.cpu().numpy()
+
+
+def expand(xs, ys, zs):
+    z, y, x = np.meshgrid(zs, ys, xs, indexing="ij")
+    return x.reshape(-1), y.reshape(-1), z.reshape(-1)
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast", "fast_rr"])
+@pytest.mark.parametrize("name,nsub", [("fhd_tiny", None), ("fhd_64", 2048),
+                                       ("fhd_128_radial", 512)])
+def test_fhd_grid_workloads(mri, name, nsub, trig):
+    w = wl.make_workload(name)
+    xs, ys, zs = w.axes()
+    r, i = mri.fhd_grid(dev(w.kx), dev(w.ky), dev(w.kz), dev(xs), dev(ys), dev(zs),
+                        dev(w.rPhi), dev(w.iPhi), dev(w.rD), dev(w.iD), trig=trig)
+    idx = None if nsub is None else wl.voxel_subset(w.N, nsub, 201)
+    ref = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
+    got = cplx(r, i) if idx is None else cplx(r, i)[idx]
+    assert oracle.rel_l2(got, ref) <= TOL[trig]
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+def test_q_grid_128(mri, trig):
+    w = wl.make_workload("q_128")
+    xs, ys, zs = w.axes()
+    r, i = mri.q_grid(dev(w.kx), dev(w.ky), dev(w.kz), dev(xs), dev(ys), dev(zs),
+                      dev(w.rPhi), dev(w.iPhi), trig=trig)
+    idx = wl.voxel_subset(w.N, 192, 202)
+    origin = (64 * 128 + 64) * 128 + 64
+    idx = np.unique(np.concatenate([idx, [origin]]))
+    ref = oracle.q(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
+    assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
+
+
+@pytest.mark.parametrize("nx,ny,nz", [(16, 3, 5), (32, 7, 1), (256, 5, 3), (128, 17, 2),
+                                      (64, 1, 1), (100, 4, 3), (8, 9, 9), (1, 40, 3),
+                                      (300, 2, 2)])
+@pytest.mark.parametrize("M", [1, 33, 1000])
+def test_grid_shapes(mri, nx, ny, nz, M):
+    rng = np.random.default_rng(nx * 1000 + ny * 10 + nz + M)
+    xs = np.sort(rng.uniform(-40, 40, nx)).astype(np.float32)       # non-uniform
+    ys = (np.arange(ny) - ny // 2).astype(np.float32)
+    zs = (np.arange(nz) * 1.5 - 2.0).astype(np.float32)
+    a = wl.random_fhd_inputs(M, 1, seed=M + nx)
+    x, y, z = expand(xs, ys, zs)
+    for trig in ("accurate", "fast"):
+        r, i = mri.fhd_grid(dev(a["kx"]), dev(a["ky"]), dev(a["kz"]), dev(xs), dev(ys), dev(zs),
+                            dev(a["rPhi"]), dev(a["iPhi"]), dev(a["rD"]), dev(a["iD"]), trig=trig)
+        ref = oracle.fhd(a["kx"], a["ky"], a["kz"], x, y, z, a["rPhi"], a["iPhi"], a["rD"],
+                         a["iD"])
+        assert oracle.rel_l2(cplx(r, i), ref) <= TOL[trig], trig
+    r, i = mri.q_grid(dev(a["kx"]), dev(a["ky"]), dev(a["kz"]), dev(xs), dev(ys), dev(zs),
+                      dev(a["rPhi"]), dev(a["iPhi"]), trig="accurate")
+    ref = oracle.q(a["kx"], a["ky"], a["kz"], x, y, z, a["rPhi"], a["iPhi"])
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL["accurate"]
+
+
+def test_grid_matches_general_path_and_accumulates(mri):
+    w = wl.make_workload("fhd_64")
+    xs, ys, zs = w.axes()
+    args = [dev(v) for v in (w.kx, w.ky, w.kz)]
+    rest = [dev(v) for v in (w.rPhi, w.iPhi, w.rD, w.iD)]
+    rg, ig = mri.fhd_grid(*args, dev(xs), dev(ys), dev(zs), *rest, trig="accurate")
+    rf, i_f = mri.fhd(*args, dev(w.x), dev(w.y), dev(w.z), *rest, trig="accurate")
+    assert oracle.rel_l2(cplx(rg, ig), cplx(rf, i_f)) <= 4e-6
+    out = (torch.full_like(rg, 0.5), torch.full_like(ig, -0.5))
+    mri.fhd_grid(*args, dev(xs), dev(ys), dev(zs), *rest, trig="accurate", accumulate=True,
+                 out=out)
+    assert oracle.rel_l2(cplx(out[0] - 0.5, out[1] + 0.5), cplx(rg, ig)) <= 1e-6
+
+
+def test_grid_empty_and_no_errors(mri):
+    e = torch.empty(0, device="cuda")
+    xs = dev(np.arange(16, dtype=np.float32))
+    r, i = mri.fhd_grid(e, e, e, xs, xs[:2], xs[:3], e, e, e, e)
+    assert r.numel() == 96 and torch.count_nonzero(r) == 0
+    assert mri.device_errors(clear=True) == 0
