@@ -2,12 +2,14 @@
 """Benchmark of the F^H D / Q gather on GB300.
 
 Headline: F^H D voxel-sample pairs per second on the 128^3-voxel, 3D-radial
-workload (M = 262,144 samples, 2,097,152 voxels), MUFU trig path, one
-mri_fhd call per step (cmpMu + tile staging + phase + trig + complex
-multiply-accumulate + epilogue).  The same JSON line also carries the other
-rows of the hot path measured the same way: F^H D with accurate trig, Q on the
-128^3 stack-of-spirals trajectory (M = 1,048,576) and batched F^H D with 8
-coils (M = 524,288).
+workload (M = 262,144 samples, 2,097,152 voxels), one call per step (cmpMu +
+tile staging + phase + trig + complex multiply-accumulate + epilogue).  The
+workload's voxels form a 128^3 grid, so the headline call is mri_fhd_grid
+(the lattice-factored gather, MUFU trig for its tables); ``--general`` times
+mri_fhd (per-pair phase and trig) instead.  The same JSON line also carries
+the other rows of the hot path measured the same way: both entry points with
+both trig paths, Q on the 128^3 stack-of-spirals trajectory (M = 1,048,576)
+and batched F^H D with 8 coils (M = 524,288).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -45,13 +47,18 @@ METRIC = "F^H D voxel-sample pairs/sec (G/s) and % of SFU/FP32 roofline, 1xGB300
 UNIT = "Gpairs/s"
 L2_FLUSH_BYTES = 256 << 20
 
-# Algorithmic operations per unit of work (the method's own minimum): the
-# phase is 1 FMUL + 2 FFMA, the complex multiply-accumulate 4 FFMA (Q: 2), and
-# sin + cos are two SFU (MUFU) operations.  Batched: per pair-coil.
+# Algorithmic operations per unit of work (the method's own minimum).
+# General gather: the phase is 1 FMUL + 2 FFMA, the complex multiply-accumulate
+# 4 FFMA (Q: 2), and sin + cos are two SFU (MUFU) operations.  Batched: per
+# pair-coil.  Grid gather: one complex multiply-accumulate of a tabulated
+# x factor and a tabulated Mu * (y, z) factor, 4 FFMA; the tables' sin/cos
+# (1/R + 1/nx per pair) are excluded like the general path's range
+# reduction.
 ALGO_OPS = {
     "fhd": {"mufu": 2.0, "fp32": 7.0, "unit": "pair"},
     "q": {"mufu": 2.0, "fp32": 5.0, "unit": "pair"},
     "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
+    "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
 # Per-SM-per-clock issue rates of sm_103a: FP32 FFMA 128 lanes; MUFU sin/cos
 # measured at 32 by the mri_microbench probe (reported live below).
@@ -68,8 +75,8 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--grid-edge", type=int, default=None,
                     help="override the voxel-grid edge L (smaller cases for profiling)")
-    ap.add_argument("--grid", action="store_true",
-                    help="run F^H D / Q through the separable-grid entry points")
+    ap.add_argument("--general", action="store_true",
+                    help="time F^H D / Q through mri_fhd / mri_q instead of the grid entry points")
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the accurate/Q/batched sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -264,7 +271,7 @@ def peak_per_sm_clk(kind, rates):
         mufu = NOMINAL["mufu"]
     if abs(fp32 - NOMINAL["fp32"]) <= 0.1 * NOMINAL["fp32"]:
         fp32 = NOMINAL["fp32"]
-    by_mufu = mufu / ops["mufu"]
+    by_mufu = mufu / ops["mufu"] if ops["mufu"] else float("inf")
     by_fp32 = fp32 / ops["fp32"]
     return min(by_mufu, by_fp32), ("mufu" if by_mufu <= by_fp32 else "fp32"), mufu, fp32
 
@@ -292,21 +299,24 @@ def profiled_traffic(kind, trig):
     return entry.get("dram_bytes_per_launch")
 
 
-def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig):
+def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False):
     units = w.pairs * (w.B if kind == "fhd_batched" else 1)
+    akind = "grid" if grid else kind
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
     launches_per_step = res["gather_launches"] / len(res["step_ms"])
     achieved = units / launches_per_step / per_launch / 1e9
-    per_clk, unit, mufu, fp32 = peak_per_sm_clk(kind, rates)
+    per_clk, unit, mufu, fp32 = peak_per_sm_clk(akind, rates)
     peak = per_clk * sms * sm_max_mhz * 1e6 / 1e9
+    ops = ALGO_OPS[akind]
+    basis = (f"{sms} SMs x {sm_max_mhz:.0f} MHz x min(MUFU {mufu:g}/{ops['mufu']:g}, "
+             f"FP32 {fp32:g}/{ops['fp32']:g}) per SM-clock") if ops["mufu"] else (
+             f"{sms} SMs x {sm_max_mhz:.0f} MHz x FP32 {fp32:g}/{ops['fp32']:g} per SM-clock")
     out = {"bound": "alu", "binding_unit": unit, "achieved": round(achieved, 2),
            "peak": round(peak, 2),
-           "unit": "G" + ALGO_OPS[kind]["unit"] + "s/s",
+           "unit": "G" + ops["unit"] + "s/s",
            "frac": round(achieved / peak, 4),
-           "traffic": profiled_traffic(kind, trig),
-           "peak_basis": (f"{sms} SMs x {sm_max_mhz:.0f} MHz x min(MUFU {mufu:g}/"
-                          f"{ALGO_OPS[kind]['mufu']:g}, FP32 {fp32:g}/{ALGO_OPS[kind]['fp32']:g})"
-                          " per SM-clock"),
+           "traffic": profiled_traffic(akind if grid else kind, trig),
+           "peak_basis": basis,
            "gather_ms_per_launch": round(per_launch * 1e3, 3)}
     if sm_mhz:
         out["frac_at_sampled_clock"] = round(achieved / (per_clk * sms * sm_mhz * 1e-3), 4)
@@ -333,17 +343,20 @@ def cpu_baseline(w: wl.Workload, target_s: float = 12.0):
                       f"({pairs:.3g} pairs, {dt:.1f} s, fp64, OpenMP over voxels)"}
 
 
-def e2e(torch, mri, dist, w, trig, steps, warmup):
+def e2e(torch, mri, dist, w, trig, steps, warmup, grid=False):
     """Public API with pinned host buffers: H2D of the inputs, the call, D2H of
     the outputs, all inside the timed region."""
-    names = ("kx", "ky", "kz", "x", "y", "z", "rPhi", "iPhi", "rD", "iD")
-    host = [torch.from_numpy(np.ascontiguousarray(getattr(w, n))).pin_memory() for n in names]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    k = [pin(getattr(w, n)) for n in ("kx", "ky", "kz")]
+    wts = [pin(getattr(w, n)) for n in ("rPhi", "iPhi", "rD", "iD")]
+    vox = [pin(a) for a in w.axes()] if grid else [pin(getattr(w, n)) for n in ("x", "y", "z")]
+    host = k + vox + wts
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = 2 * w.N * 4
 
     def step():
-        r, i = mri.fhd(*host, trig=trig)
-        return r, i
+        f = mri.fhd_grid if grid else mri.fhd
+        return f(*k, *vox, *wts, trig=trig)
 
     for _ in range(warmup):
         step()
@@ -395,7 +408,7 @@ def run_ours(args):
     t = to_dev(w, torch)
     out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
            torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"))
-    grid = args.grid and kind in ("fhd", "q")
+    grid = (not args.general) and kind in ("fhd", "q")
     plan = (mri.plan_grid(kind, w.M, w.L, w.L, w.L) if grid
             else mri.plan(kind, w.M, w.N, B=w.B))
     with ClockSampler(local) as clk:
@@ -419,7 +432,7 @@ def run_ours(args):
                    else "single GPU",
                    "plan": plan},
         "roofline": roofline(kind, w, res, rates, sms, sm_max_mhz, clocks.get("sm_mhz"),
-                             args.trig),
+                             args.trig, grid),
         "gpu_launches": plan["launches"] * args.steps,
         "clocks": clocks,
         "unit_rates_per_sm_clk": rates,
@@ -427,30 +440,45 @@ def run_ours(args):
     line["roofline"]["sm_max_mhz_basis"] = "MEASURED_PEAKS.json sm_max_mhz" if peaks else "recipe"
 
     if not args.no_e2e and kind == "fhd":
-        line["e2e"] = e2e(torch, mri, dist, w, args.trig, max(args.steps, 2), 1)
+        line["e2e"] = e2e(torch, mri, dist, w, args.trig, max(args.steps, 2), 1, grid)
     del t, out
     torch.cuda.empty_cache()
 
     if not args.no_paths and args.workload == HEADLINE and world == 1 and not args.grid_edge:
         paths = {}
-        for name, wname, trig in (("fhd_accurate", HEADLINE, "accurate"),
-                                  ("q_fast", "q_128", "fast"),
-                                  ("fhd_batched_fast", "fhd_batched_128", "fast")):
+        for name, wname, trig, pgrid in (
+                ("fhd_grid_accurate", HEADLINE, "accurate", True),
+                ("fhd_general_fast", HEADLINE, "fast", False),
+                ("fhd_general_accurate", HEADLINE, "accurate", False),
+                ("q_grid_fast", "q_128", "fast", True),
+                ("q_grid_accurate", "q_128", "accurate", True),
+                ("q_general_fast", "q_128", "fast", False),
+                ("fhd_batched_fast", "fhd_batched_128", "fast", False),
+                ("fhd_batched_accurate", "fhd_batched_128", "accurate", False)):
+            if name.startswith("fhd_") and (name.startswith("fhd_grid") == grid) and \
+                    trig == args.trig and not name.startswith("fhd_batched"):
+                continue                     # the headline itself
             pw = wl.make_workload(wname)
             pt = to_dev(pw, torch)
             po = None
-            pres = timed_steps(torch, mri, dist, lambda: call(mri, pw.kind, pt, trig, po),
+            pres = timed_steps(torch, mri, dist,
+                               lambda: call(mri, pw.kind, pt, trig, po, pgrid),
                                args.steps, args.warmup, flush)
             pm = statistics.mean(pres["step_ms"]) / 1e3
             punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
+            pplan = (mri.plan_grid(pw.kind, pw.M, pw.L, pw.L, pw.L) if pgrid
+                     else mri.plan(pw.kind, pw.M, pw.N, B=pw.B))
             paths[name] = {
                 "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}", "trig": trig,
+                "entry": {("fhd", True): "mri_fhd_grid", ("q", True): "mri_q_grid",
+                          ("fhd", False): "mri_fhd", ("q", False): "mri_q",
+                          ("fhd_batched", False): "mri_fhd_batched"}[(pw.kind, pgrid)],
                 "value": round(punits / pm / 1e9, 2),
                 "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
                 "ms_per_step": round(pm * 1e3, 3),
                 "roofline": roofline(pw.kind, pw, pres, rates, sms, sm_max_mhz,
-                                     clocks.get("sm_mhz"), trig),
-                "gpu_launches": mri.plan(pw.kind, pw.M, pw.N, B=pw.B)["launches"] * args.steps,
+                                     clocks.get("sm_mhz"), trig, pgrid),
+                "gpu_launches": pplan["launches"] * args.steps,
             }
             if pw.kind == "fhd_batched":
                 paths[name]["trajectory_pairs_per_s_G"] = round(pw.pairs / pm / 1e9, 2)

@@ -166,7 +166,7 @@ mri_status mri_fhd_noalloc(const float* kx, const float* ky, const float* kz,
  * the kernel tabulates the x factor per column and Mu times the (y, z)
  * factor per row and spends one complex multiply-accumulate per
  * voxel-sample pair; sin/cos are evaluated per (sample, column) and
- * (sample, row) only.  The table kernel covers nx in {16, 32, 64, 128, 256};
+ * (sample, row) only.  The table kernel covers nx in {32, 64, 128, 256};
  * other grids are expanded to coordinates and take the general kernel.
  * Edge cases as mri_fhd.
  */

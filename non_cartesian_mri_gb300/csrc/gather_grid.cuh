@@ -7,15 +7,18 @@
 //   e^{i 2 pi k.x_n} = Ex[m][ix] * Eyz[m][iy, iz]
 //   Ex  = e^{i 2 pi kx xs[ix]},   Eyz = e^{i 2 pi (ky ys[iy] + kz zs[iz])}.
 //
-// A CTA owns R = 2048 / nx whole grid rows (fixed iy, iz; all ix).  For each
+// A CTA owns R = 4096 / nx whole grid rows (fixed iy, iz; all ix).  For each
 // tile of kGridTile samples it builds, in shared memory,
 //   Ex[s][ix]   for the tile's samples and all nx columns, and
-//   Mz[s][r]    = Mu[s] * Eyz[s][row r]   for its R rows
+//   Mz[r][s]    = Mu[s] * Eyz[s][row r]   for its R rows
 // (Mu = conj(Phi) D for F^H D, |Phi|^2 for Q), after which every voxel-sample
-// pair is one complex multiply-accumulate, acc += Mz[s][r] * Ex[s][ix]: four
-// FFMA and one broadcast shared-memory load.  The sin/cos work drops from two
-// per pair to (nx + R) per (tile sample, CTA), i.e. 1/R + 1/nx per pair, so
-// the accurate polynomial trig costs little more than the SFU one.
+// pair is one complex multiply-accumulate, acc += Mz[r][s] * Ex[s][ix]: four
+// FFMA.  Each thread holds a 4 x 4 block of voxels (4 columns, 4 rows) in
+// registers, so per two samples it loads four Ex and four Mz vectors
+// (16-byte loads, two samples each) for 32 pairs: a quarter of a shared-memory
+// load per pair.  The sin/cos work drops from two per pair to (nx + R) per
+// (tile sample, CTA), i.e. 1/R + 1/nx per pair, so the accurate polynomial
+// trig costs little more than the SFU one.
 //
 // Tables are double-buffered: the tables of tile t+1 are written while no
 // thread can still read that buffer (it was last read for tile t-1, before
@@ -32,8 +35,10 @@ namespace mri {
 
 constexpr int kGridTile = 32;      // samples per table tile
 constexpr int kGridThreads = 256;
-constexpr int kGridV = 8;          // voxels per thread
-constexpr int kGridVoxelsPerCta = kGridThreads * kGridV;   // 2048: R = 2048 / nx rows
+constexpr int kGridVX = 4;         // columns per thread
+constexpr int kGridVY = 4;         // rows per thread
+constexpr int kGridV = kGridVX * kGridVY;                  // voxels per thread
+constexpr int kGridVoxelsPerCta = kGridThreads * kGridV;   // 4096: R = 4096 / nx rows
 
 struct GridParams {
     const float* rec;       // tile-major records, kGridTile samples per tile
@@ -41,7 +46,7 @@ struct GridParams {
     int splits;
     const float *xs, *ys, *zs;
     int nx, ny, nz;
-    int rows_per_cta;       // 2048 / nx
+    int rows_per_cta;       // 4096 / nx
     float* out_r;           // as GatherParams, one coil
     float* out_i;
     int64_t split_stride;
@@ -49,13 +54,18 @@ struct GridParams {
     unsigned int* err;
 };
 
-// The table kernel takes nx in {16, 32, ..., 256}: nx divides 256, so each
-// thread keeps one column ix for all its voxels, and the tables fit shared
-// memory (nx = 16 gives R = 128 rows).
+// The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks
+// divide the 256 threads, and the tables fit shared memory (nx = 32 gives
+// R = 128 rows).  nx is a template parameter so that every table address is a
+// base register plus an immediate offset.
 inline bool grid_kernel_fits(int nx)
 {
-    return nx >= 16 && nx <= 256 && (256 % nx) == 0;
+    return nx == 32 || nx == 64 || nx == 128 || nx == 256;
 }
+
+// Row stride of the Mz table in float2: T + 2 keeps 16-byte alignment for
+// two-sample loads and puts consecutive rows in different banks.
+constexpr int kMzStride = kGridTile + 2;
 
 // Dynamic shared memory of the grid kernel for a given nx.
 inline size_t grid_smem_bytes(int nx, bool realw)
@@ -63,8 +73,9 @@ inline size_t grid_smem_bytes(int nx, bool realw)
     const int F = realw ? 4 : 5;
     const int R = kGridVoxelsPerCta / nx;
     size_t b = size_t(kStages) * F * kGridTile * 4;          // record ring
-    b += 2 * size_t(kGridTile) * (size_t(nx) + R) * 8;        // Ex and Mz, double-buffered
-    b += size_t(nx) * 4 + size_t(R) * 8;                      // xs, (y, z) of the rows
+    b += 2 * size_t(kGridTile) * nx * 8;                      // Ex [T/2][nx][2], double-buffered
+    b += 2 * size_t(R) * kMzStride * 8;                       // Mz [R][T+2], double-buffered
+    b += size_t(R) * 8;                                       // (y, z) of the rows
     return b;
 }
 
@@ -81,43 +92,45 @@ __device__ __forceinline__ void table_sincos(float ph, float& s, float& c)
     }
 }
 
-template <bool REALW, int TRIG, bool FIXED_IX>
+template <bool REALW, int TRIG, int NX>
 __global__ void __launch_bounds__(kGridThreads, 2) gather_grid_kernel(GridParams p)
 {
     constexpr int T = kGridTile;
     constexpr int F = REALW ? 4 : 5;
     constexpr uint32_t TILE_BYTES = uint32_t(F) * T * 4;
-    constexpr int V = kGridV;
+    constexpr int VX = kGridVX, VY = kGridVY;
+    constexpr int R = kGridVoxelsPerCta / NX;     // rows per CTA
+    constexpr int NXB = NX / VX;                  // column blocks: column cb + NXB * i
+    constexpr int SB = kGridThreads / NX;         // sample pairs per Ex-build pass
+    static_assert(kGridThreads % NXB == 0 && kGridThreads % NX == 0 && T == 32 &&
+                      (T / 2) % SB == 0, "grid shape");
 
-    const int nx = p.nx;
-    const int R = p.rows_per_cta;
     const int64_t total_rows = int64_t(p.ny) * p.nz;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float* const ring = reinterpret_cast<float*>(smem_raw);
-    float2* const ex_tab = reinterpret_cast<float2*>(ring + kStages * F * T);   // [2][T][nx]
-    float2* const mz_tab = ex_tab + 2 * T * nx;                                 // [2][T][R]
-    float2* const yz_sh = mz_tab + 2 * T * R;                                   // [R] (y, z)
-    float* const xs_sh = reinterpret_cast<float*>(yz_sh + R);                   // [nx]
+    float4* const ex_tab = reinterpret_cast<float4*>(ring + kStages * F * T);   // [2][T/2][NX]
+    float2* const mz_tab = reinterpret_cast<float2*>(ex_tab + 2 * (T / 2) * NX); // [2][R][T+2]
+    float2* const yz_sh = mz_tab + 2 * R * kMzStride;                           // [R]
     __shared__ __align__(8) uint64_t full_bar[kStages];
 
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
     const int split = blockIdx.y;
     const int64_t t_begin = (p.ntiles * split) / p.splits;
     const int64_t t_end = (p.ntiles * (split + 1)) / p.splits;
     const int nt = int(t_end - t_begin);
     const int64_t row0 = int64_t(blockIdx.x) * R;
 
-    // the thread's voxels: local slot j*256 + tid -> (row, ix)
-    int ix_of[V], row_of[V];
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int local = j * kGridThreads + tid;
-        ix_of[j] = local % nx;
-        row_of[j] = local / nx;
-    }
+    // this thread's voxels: columns cb + NXB*i (i < 4), rows 4*rb + j (j < 4)
+    const int cb = tid % NXB;
+    const int rb = tid / NXB;
+    // its share of the Ex build: column ix_b, sample pairs sb0 + SB*it
+    const int ix_b = tid % NX;
+    const int sb0 = tid / NX;
+    const float x_b = p.xs[ix_b];
 
-    for (int i = tid; i < nx; i += kGridThreads) xs_sh[i] = p.xs[i];
     for (int r = tid; r < R; r += kGridThreads) {
         const int64_t row = row0 + r;
         float2 yz = make_float2(0.f, 0.f);
@@ -142,40 +155,44 @@ __global__ void __launch_bounds__(kGridThreads, 2) gather_grid_kernel(GridParams
         }
     }
 
-    float run_r[V], run_i[V];
+    float run_r[VY][VX], run_i[VY][VX];
 #pragma unroll
-    for (int j = 0; j < V; ++j) run_r[j] = run_i[j] = 0.0f;
+    for (int j = 0; j < VY; ++j)
+#pragma unroll
+        for (int i = 0; i < VX; ++i) run_r[j][i] = run_i[j][i] = 0.0f;
 
     int failed_at = -1;
     for (int t = 0; t < nt; ++t) {
         const int st = t % kStages;
         const bool ok = mbar_wait_bounded(&full_bar[st], uint32_t(t / kStages) & 1u);
         const float* rec = ring + st * F * T;
-        float2* const ex = ex_tab + (t & 1) * T * nx;
-        float2* const mz = mz_tab + (t & 1) * T * R;
+        float4* const ex = ex_tab + (t & 1) * (T / 2) * NX;
+        float2* const mz = mz_tab + (t & 1) * R * kMzStride;
         if (ok) {
-            // Ex[s][ix] = e^{i phase(kx[s] xs[ix])}
-            for (int e = tid; e < T * nx; e += kGridThreads) {
-                const int s = e / nx;
-                const int i = e - s * nx;
-                float sn, cs;
-                table_sincos<TRIG>(rec[s] * xs_sh[i], sn, cs);
-                ex[e] = make_float2(cs, sn);
+            // Ex[s][ix] = e^{i phase(kx[s] xs[ix])}, stored as (sample pair, column):
+            // each thread fills whole 16-byte slots, consecutive lanes consecutive
+            // columns
+#pragma unroll
+            for (int it = 0; it < T / (2 * SB); ++it) {
+                const int q = sb0 + SB * it;          // sample pair
+                float s0, c0, s1, c1;
+                table_sincos<TRIG>(rec[2 * q] * x_b, s0, c0);
+                table_sincos<TRIG>(rec[2 * q + 1] * x_b, s1, c1);
+                ex[q * NX + ix_b] = make_float4(c0, s0, c1, s1);
             }
-            // Mz[s][r] = Mu[s] * e^{i phase(ky[s] y_r + kz[s] z_r)}
-            for (int e = tid; e < T * R; e += kGridThreads) {
-                const int s = e / R;
-                const int r = e - s * R;
+            // Mz[r][s] = Mu[s] * e^{i phase(ky[s] y_r + kz[s] z_r)}: lane = sample
+            const float ky = rec[T + lane], kz = rec[2 * T + lane];
+            const float wr = rec[3 * T + lane];
+            const float wi = REALW ? 0.0f : rec[4 * T + lane];
+#pragma unroll
+            for (int it = 0; it < R / 8; ++it) {
+                const int r = warp + 8 * it;
                 const float2 yz = yz_sh[r];
                 float sn, cs;
-                table_sincos<TRIG>(fmaf(rec[2 * T + s], yz.y, rec[T + s] * yz.x), sn, cs);
-                const float wr = rec[3 * T + s];
-                if (REALW) {
-                    mz[e] = make_float2(wr * cs, wr * sn);
-                } else {
-                    const float wi = rec[4 * T + s];
-                    mz[e] = make_float2(fmaf(wr, cs, -wi * sn), fmaf(wi, cs, wr * sn));
-                }
+                table_sincos<TRIG>(fmaf(kz, yz.y, ky * yz.x), sn, cs);
+                mz[r * kMzStride + lane] =
+                    REALW ? make_float2(wr * cs, wr * sn)
+                          : make_float2(fmaf(wr, cs, -wi * sn), fmaf(wi, cs, wr * sn));
             }
         }
         // tables of tile t complete; record stage st no longer read
@@ -190,29 +207,42 @@ __global__ void __launch_bounds__(kGridThreads, 2) gather_grid_kernel(GridParams
                          &full_bar[st]);
         }
 
-        float pr[V], pi[V];
+        float pr[VY][VX], pi[VY][VX];
 #pragma unroll
-        for (int j = 0; j < V; ++j) pr[j] = pi[j] = 0.0f;
-#pragma unroll 4
-        for (int s = 0; s < T; ++s) {
-            float2 e0 = make_float2(0.f, 0.f);
-            if (FIXED_IX) e0 = ex[s * nx + ix_of[0]];
+        for (int j = 0; j < VY; ++j)
 #pragma unroll
-            for (int j = 0; j < V; ++j) {
-                const float2 e = FIXED_IX ? e0 : ex[s * nx + ix_of[j]];
-                const float2 m = mz[s * R + row_of[j]];
-                // (m.x + i m.y)(e.x + i e.y)
-                pr[j] = fmaf(m.x, e.x, pr[j]);
-                pr[j] = fmaf(-m.y, e.y, pr[j]);
-                pi[j] = fmaf(m.x, e.y, pi[j]);
-                pi[j] = fmaf(m.y, e.x, pi[j]);
+            for (int i = 0; i < VX; ++i) pr[j][i] = pi[j][i] = 0.0f;
+        const float4* const ex_cols = ex + cb;
+        const float4* const mz_rows = reinterpret_cast<const float4*>(mz + 4 * rb * kMzStride);
+#pragma unroll 2
+        for (int s = 0; s < T; s += 2) {
+            float4 e[VX], m[VY];
+#pragma unroll
+            for (int i = 0; i < VX; ++i) e[i] = ex_cols[(s >> 1) * NX + NXB * i];
+#pragma unroll
+            for (int j = 0; j < VY; ++j) m[j] = mz_rows[(j * kMzStride + s) >> 1];
+#pragma unroll
+            for (int j = 0; j < VY; ++j)
+#pragma unroll
+                for (int i = 0; i < VX; ++i) {
+                    // samples s (x, y) and s+1 (z, w): acc += Mz * Ex
+                    pr[j][i] = fmaf(m[j].x, e[i].x, pr[j][i]);
+                    pr[j][i] = fmaf(-m[j].y, e[i].y, pr[j][i]);
+                    pi[j][i] = fmaf(m[j].x, e[i].y, pi[j][i]);
+                    pi[j][i] = fmaf(m[j].y, e[i].x, pi[j][i]);
+                    pr[j][i] = fmaf(m[j].z, e[i].z, pr[j][i]);
+                    pr[j][i] = fmaf(-m[j].w, e[i].w, pr[j][i]);
+                    pi[j][i] = fmaf(m[j].z, e[i].w, pi[j][i]);
+                    pi[j][i] = fmaf(m[j].w, e[i].z, pi[j][i]);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < VY; ++j)
+#pragma unroll
+            for (int i = 0; i < VX; ++i) {
+                run_r[j][i] += pr[j][i];
+                run_i[j][i] += pi[j][i];
             }
-        }
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            run_r[j] += pr[j];
-            run_i[j] += pi[j];
-        }
     }
 
     if (failed_at >= 0) {
@@ -231,17 +261,20 @@ __global__ void __launch_bounds__(kGridThreads, 2) gather_grid_kernel(GridParams
     float* const out_r = p.out_r + split * p.split_stride;
     float* const out_i = p.out_i + split * p.split_stride;
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int64_t row = row0 + row_of[j];
+    for (int j = 0; j < VY; ++j) {
+        const int64_t row = row0 + 4 * rb + j;
         if (row < total_rows) {
-            const int64_t n = row * nx + ix_of[j];
-            float r = run_r[j], i = run_i[j];
-            if (p.accumulate) {
-                r = out_r[n] + r;
-                i = out_i[n] + i;
+#pragma unroll
+            for (int i = 0; i < VX; ++i) {
+                const int64_t n = row * NX + cb + NXB * i;
+                float r = run_r[j][i], im = run_i[j][i];
+                if (p.accumulate) {
+                    r = out_r[n] + r;
+                    im = out_i[n] + im;
+                }
+                out_r[n] = r;
+                out_i[n] = im;
             }
-            out_r[n] = r;
-            out_i[n] = i;
         }
     }
 }

@@ -24,35 +24,13 @@ __global__ void __launch_bounds__(256) expand_grid_kernel(const float* xs, const
 }
 
 
-namespace {
-template <bool REALW, int TRIG>
-cudaError_t run_grid(const GridParams& p, dim3 grid, cudaStream_t s)
-{
-    const size_t smem = grid_smem_bytes(p.nx, REALW);
-    const cudaError_t attr = cudaFuncSetAttribute(
-        gather_grid_kernel<REALW, TRIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        int(smem));
-    if (attr != cudaSuccess) return attr;
-    gather_grid_kernel<REALW, TRIG, true><<<grid, kGridThreads, smem, s>>>(p);
-    return cudaGetLastError();
-}
-}  // namespace
-
 cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s)
 {
-    if (!grid_kernel_fits(p.nx)) return cudaErrorInvalidValue;
-    if (realw) {
-        switch (trig) {
-            case TRIG_ACCURATE: return run_grid<true, TRIG_ACCURATE>(p, grid, s);
-            case TRIG_FAST: return run_grid<true, TRIG_FAST>(p, grid, s);
-            case TRIG_FAST_RR: return run_grid<true, TRIG_FAST_RR>(p, grid, s);
-        }
-    } else {
-        switch (trig) {
-            case TRIG_ACCURATE: return run_grid<false, TRIG_ACCURATE>(p, grid, s);
-            case TRIG_FAST: return run_grid<false, TRIG_FAST>(p, grid, s);
-            case TRIG_FAST_RR: return run_grid<false, TRIG_FAST_RR>(p, grid, s);
-        }
+    switch (p.nx) {
+        case 32: return launch_grid_32(realw, trig, p, grid, s);
+        case 64: return launch_grid_64(realw, trig, p, grid, s);
+        case 128: return launch_grid_128(realw, trig, p, grid, s);
+        case 256: return launch_grid_256(realw, trig, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -35,6 +35,11 @@ cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
 
 // separable-grid path (kernels_grid.cu)
 cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+// one translation unit per grid width (kernels_grid_<nx>.cu)
+cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_grid_64(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_grid_128(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_grid_256(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_prep_grid(bool realw, const PrepParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
                                int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);
