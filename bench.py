@@ -60,6 +60,14 @@ ALGO_OPS = {
     "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
     "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
+# The tensor-core grid kernel (nx = 128): one complex multiply-accumulate is
+# 8 real flops per pair; each fp32-accurate product takes three tf32 MMA
+# passes (hi*hi + hi*lo + lo*hi), so its peak is the tf32 peak / 3.  The tf32
+# peak is the measured bf16 peak times the nominal tf32 / bf16 ratio
+# (1.1 / 2.25 PFLOP/s dense).
+TC_FLOPS_PER_PAIR = 8.0
+TC_PASSES = 3.0
+TF32_PER_BF16 = 1.1 / 2.25
 # Per-SM-per-clock issue rates of sm_103a: FP32 FFMA 128 lanes; MUFU sin/cos
 # measured at 32 by the mri_microbench probe (reported live below).
 NOMINAL = {"mufu": 32.0, "fp32": 128.0}
@@ -68,7 +76,7 @@ NOMINAL = {"mufu": 32.0, "fp32": 128.0}
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--trig", choices=["fast", "accurate", "fast_rr"], default="fast")
@@ -151,7 +159,7 @@ class ClockSampler:
             self.fh = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -299,7 +307,27 @@ def profiled_traffic(kind, trig):
     return entry.get("dram_bytes_per_launch")
 
 
-def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False):
+def roofline_tensor(w, res, peaks):
+    per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
+    launches_per_step = res["gather_launches"] / len(res["step_ms"])
+    pairs_s = w.pairs / launches_per_step / per_launch
+    achieved = pairs_s * TC_FLOPS_PER_PAIR / 1e12
+    bf16 = float(peaks.get("bf16_tflops", 1900.0))
+    peak = bf16 * TF32_PER_BF16 / TC_PASSES
+    return {"bound": "tensor", "binding_unit": "tcgen05 kind::tf32", "achieved": round(achieved, 2),
+            "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic("grid_tc", "any"),
+            "peak_basis": (f"bf16 {bf16:g} TFLOP/s ({'MEASURED_PEAKS.json' if 'bf16_tflops' in peaks else 'recipe fallback'})"
+                           f" x tf32/bf16 {TF32_PER_BF16:.3f} / {TC_PASSES:g} tf32 passes per fp32 product;"
+                           f" algorithmic {TC_FLOPS_PER_PAIR:g} flops per voxel-sample pair"),
+            "pairs_per_s": round(pairs_s / 1e9, 2), "unit_pairs": "Gpairs/s",
+            "gather_ms_per_launch": round(per_launch * 1e3, 3)}
+
+
+def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, plan=None,
+             peaks=None):
+    if grid and plan and plan.get("tensor_cores"):
+        return roofline_tensor(w, res, peaks or {})
     units = w.pairs * (w.B if kind == "fhd_batched" else 1)
     akind = "grid" if grid else kind
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
@@ -432,7 +460,7 @@ def run_ours(args):
                    else "single GPU",
                    "plan": plan},
         "roofline": roofline(kind, w, res, rates, sms, sm_max_mhz, clocks.get("sm_mhz"),
-                             args.trig, grid),
+                             args.trig, grid, plan, peaks),
         "gpu_launches": plan["launches"] * args.steps,
         "clocks": clocks,
         "unit_rates_per_sm_clk": rates,
@@ -477,7 +505,7 @@ def run_ours(args):
                 "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
                 "ms_per_step": round(pm * 1e3, 3),
                 "roofline": roofline(pw.kind, pw, pres, rates, sms, sm_max_mhz,
-                                     clocks.get("sm_mhz"), trig, pgrid),
+                                     clocks.get("sm_mhz"), trig, pgrid, pplan, peaks),
                 "gpu_launches": pplan["launches"] * args.steps,
             }
             if pw.kind == "fhd_batched":

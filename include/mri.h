@@ -203,6 +203,7 @@ typedef struct mri_plan {
     int coil_groups;          /* gather launches over coil groups (batched) */
     int launches;             /* kernel launches one call makes */
     int64_t scratch_bytes;    /* pool memory one call takes */
+    int tensor_cores;         /* 1: the gather runs on the tcgen05 tensor cores */
 } mri_plan;
 
 mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,

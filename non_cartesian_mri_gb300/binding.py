@@ -40,7 +40,7 @@ class _Plan(ctypes.Structure):
                 ("samples_per_tile", ctypes.c_int), ("splits", ctypes.c_int),
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
-                ("scratch_bytes", ctypes.c_int64)]
+                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int)]
 
 
 def lib_path() -> str:

@@ -7,6 +7,7 @@
 
 #include "gather.cuh"
 #include "gather_grid.cuh"
+#include "gather_grid_tc.cuh"
 
 namespace mri {
 
@@ -35,6 +36,9 @@ cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
 
 // separable-grid path (kernels_grid.cu)
 cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+// tensor-core grid path (kernels_grid_tc.cu), nx = 128
+cudaError_t launch_grid_tc(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
+cudaError_t launch_prep_grid_tc(bool realw, const PrepParams& p, int grid, cudaStream_t s);
 // one translation unit per grid width (kernels_grid_<nx>.cu)
 cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_grid_64(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);

@@ -340,6 +340,7 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
 // ---------------------------------------------------------------------------
 struct GridPlan {
     bool table_kernel;      // false: coordinates expanded, general kernel
+    bool tensor_cores;      // nx = 128: the tcgen05 kernel
     int64_t ntiles;
     int64_t vblocks;
     int rows_per_cta;
@@ -355,6 +356,19 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
     g.table_kernel = mri::grid_kernel_fits(nx);
     if (!g.table_kernel) return g;
     const int64_t N = int64_t(nx) * ny * nz;
+    g.tensor_cores = mri::grid_tc_fits(nx);
+    if (g.tensor_cores) {
+        g.rows_per_cta = mri::kTcRows;
+        g.ntiles = ceil_div(M, mri::kTcTile);
+        g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
+        g.ctas_per_sm = 1;
+        g.splits = (g.ntiles > 0 && g.vblocks > 0)
+                       ? choose_splits(g.ntiles, g.vblocks, sms > 0 ? sms : 1, 1, N, 1.0, 3.0)
+                       : 1;
+        g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 5) * mri::kTcTile * 4;
+        g.part_bytes = g.splits > 1 ? int64_t(g.splits) * 2 * N * 4 : 0;
+        return g;
+    }
     g.rows_per_cta = mri::kGridVoxelsPerCta / nx;
     g.ntiles = ceil_div(M, mri::kGridTile);
     g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
@@ -410,7 +424,9 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
     mri_status st = MRI_OK;
     mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
-    if (mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * mri::kGridTile, d->sms), s) !=
+    const int tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
+    if ((g.tensor_cores ? mri::launch_prep_grid_tc(realw, pp, grid_for(g.ntiles * tile, d->sms), s)
+                        : mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * tile, d->sms), s)) !=
         cudaSuccess)
         st = cuda_fail();
     mri::GridParams gp{};
@@ -440,7 +456,9 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
         cudaEvent_t* ev = timing_slot(d);
         if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
         const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
-        if (st == MRI_OK && mri::launch_grid(realw, trig, gp, grid, s) != cudaSuccess)
+        if (st == MRI_OK &&
+            (g.tensor_cores ? mri::launch_grid_tc(realw, trig, gp, grid, s)
+                            : mri::launch_grid(realw, trig, gp, grid, s)) != cudaSuccess)
             st = cuda_fail();
         if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
     }
@@ -642,15 +660,17 @@ mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sm
         plan->scratch_bytes += 3 * N * 4;
         return st;
     }
-    plan->threads_per_cta = mri::kGridThreads;
-    plan->voxels_per_thread = mri::kGridV;
-    plan->samples_per_tile = mri::kGridTile;
+    plan->threads_per_cta = g.tensor_cores ? mri::kTcThreads : mri::kGridThreads;
+    plan->voxels_per_thread = g.tensor_cores ? mri::kTcRows * mri::kTcCols / mri::kTcThreads
+                                             : mri::kGridV;
+    plan->samples_per_tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
     plan->splits = g.splits;
     plan->voxel_ctas = g.vblocks;
     plan->tiles = g.ntiles;
     plan->coil_groups = 1;
     plan->launches = 2 + (g.splits > 1 ? 1 : 0);
     plan->scratch_bytes = align256(g.rec_bytes) + g.part_bytes;
+    plan->tensor_cores = g.tensor_cores ? 1 : 0;
     return MRI_OK;
 }
 

@@ -121,7 +121,7 @@ class Plan(ctypes.Structure):
                 ("samples_per_tile", ctypes.c_int), ("splits", ctypes.c_int),
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
-                ("scratch_bytes", ctypes.c_int64)]
+                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int)]
 
 
 def plan(lib, kind, B, M, N, sms=152):

@@ -109,3 +109,28 @@ def test_grid_empty_and_no_errors(mri):
     r, i = mri.fhd_grid(e, e, e, xs, xs[:2], xs[:3], e, e, e, e)
     assert r.numel() == 96 and torch.count_nonzero(r) == 0
     assert mri.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+def test_tensor_core_width_against_general_path(mri, trig):
+    """nx = 128 runs on the tensor cores: ragged rows (3 x 7 = 21 of 128 in
+    a CTA), a sample count that splits unevenly, accumulate."""
+    w = wl.make_workload("fhd_128_radial")
+    M = 70001
+    xs = (np.arange(128) - 64).astype(np.float32)
+    ys = np.array([-40, 3, 57], np.float32)
+    zs = (np.arange(7) * 9 - 30).astype(np.float32)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    wts = [dev(a[:M]) for a in (w.rPhi, w.iPhi, w.rD, w.iD)]
+    rg, ig = mri.fhd_grid(*k, dev(xs), dev(ys), dev(zs), *wts, trig=trig)
+    x, y, z = expand(xs, ys, zs)
+    ref = oracle.fhd(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M],
+                     w.rD[:M], w.iD[:M])
+    assert oracle.rel_l2(cplx(rg, ig), ref) <= TOL[trig]
+    out = (torch.full_like(rg, 2.0), torch.full_like(ig, -1.0))
+    mri.fhd_grid(*k, dev(xs), dev(ys), dev(zs), *wts, trig=trig, accumulate=True, out=out)
+    assert oracle.rel_l2(cplx(out[0] - 2.0, out[1] + 1.0), ref) <= TOL[trig]
+    qr, qi = mri.q_grid(*k, dev(xs), dev(ys), dev(zs), wts[0], wts[1], trig=trig)
+    qref = oracle.q(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M])
+    assert oracle.rel_l2(cplx(qr, qi), qref) <= TOL[trig]
+    assert mri.plan_grid("fhd", M, 128, 3, 7)["samples_per_tile"] == 16
