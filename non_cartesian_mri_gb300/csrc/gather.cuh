@@ -105,6 +105,9 @@ struct PrepParams {
     int64_t ntiles;
     float kscale;           // 4 (quarter turns), 2*pi (radians) or 1 (turns)
     float* rec;
+    // Optional (single weight only): raised by atomicMax to the float bits of
+    // max over samples of |w_r| + |w_i|; the caller zeroes it first.
+    unsigned int* wbound = nullptr;
 };
 
 struct GatherParams {
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
 {
     using R = Rec<BC, REALW, TILE>;
     const int64_t total = p.ntiles * TILE;
+    float wmax = 0.0f;
     for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < total;
          m += int64_t(gridDim.x) * blockDim.x) {
         const int64_t tile = m / TILE;
@@ -155,6 +159,10 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
                     f[3 + BC + b] = fmaf(-ip, rd, rp * id);         // Im conj(Phi) D
                 }
             }
+            if constexpr (REALW)
+                wmax = fmaxf(wmax, fabsf(f[3]));
+            else if constexpr (BC == 1)
+                wmax = fmaxf(wmax, fabsf(f[3]) + fabsf(f[4]));
         }
         if (R::AOS) {
             float4* dst = reinterpret_cast<float4*>(base + j * R::F4);
@@ -165,6 +173,11 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
 #pragma unroll
             for (int i = 0; i < R::F; ++i) base[i * TILE + j] = f[i];
         }
+    }
+    if (BC == 1 && p.wbound != nullptr) {
+        // non-negative floats order like their bit patterns (a NaN sorts last)
+        const unsigned int w = __reduce_max_sync(0xffffffffu, __float_as_uint(wmax));
+        if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(p.wbound, w);
     }
 }
 

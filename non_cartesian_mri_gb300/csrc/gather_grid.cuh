@@ -52,6 +52,8 @@ struct GridParams {
     int64_t split_stride;
     int accumulate;
     unsigned int* err;
+    // tensor-core kernel: float bits of max |w_r| + |w_i| over the samples
+    const unsigned int* wbound;
 };
 
 // The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks

@@ -5,29 +5,34 @@
 //   Mz = Mu * e^{i2pi(ky y + kz z)},  Ex = e^{i2pi kx x},
 // a complex matrix product over the samples: a dense contraction.  Here a CTA
 // owns 128 grid rows (the MMA M) of a grid with nx = 128 columns (the MMA N).
-// For each tile of 16 samples (two K = 8 steps) the warps evaluate Mz
-// (128 rows x 16 samples) and Ex (16 samples x 128 columns) into shared
-// memory, each value split into a tf32 high part and the float remainder;
-// one thread then issues, per K step, two N = 256 products into [D_r | D_i]:
+// For each tile of 32 samples (two K = 16 steps) the warps evaluate Mz
+// (128 rows x 32 samples) and Ex (32 samples x 128 columns) into shared
+// memory, each value split into an f16 high part and the f16-rounded
+// remainder; one thread then issues, per K step, two N = 256 products into
+// [D_r | D_i]:
 //   [D_r | D_i] += A_r [B_r | B_i]  +  A_i [-B_i | B_r],
 // reading the B operands as two 256-row windows of one 384-row block
 // S = [-B_i; B_r; B_i], with each real product done as hi*hi + hi*lo + lo*hi
-// (12 tcgen05.mma of 128 x 256 x 8 per tile), which keeps about 21 bits of
-// every product.  Shared-memory bandwidth (operand reads by the tensor core
-// plus operand writes by the warps) is what binds this kernel, and the N = 256
-// form reads each A operand once per pass instead of twice.  The
-// accumulators live in tensor memory: D_r, D_i (columns 0-255) collect one
-// block of tiles and are then added into the running sums R_r, R_i (columns
-// 256-511), the blocked summation that keeps accumulation error below the
-// trig error over a million samples.
+// (12 tcgen05.mma of 128 x 256 x 16 per tile).  The two f16 parts carry about
+// 22 significant bits, and the dropped lo*lo term is below 2^-22 of a
+// product, so every product keeps close to fp32 accuracy.  f16 has a narrow
+// exponent range: the A operand (Mz) is multiplied by a power of two chosen
+// from the largest |w_r| + |w_i| of the call so that every |A| < 2^15, and
+// the results are multiplied back exactly; |B| <= 1 needs no scale.
+// Shared-memory bandwidth (operand reads by the tensor core plus operand
+// writes by the warps) and the tensor pipe bind this kernel about equally.
+// The accumulators live in tensor memory: D_r, D_i (columns 0-255) collect
+// one block of tiles and are then added into the running sums R_r, R_i
+// (columns 256-511), the blocked summation that keeps accumulation error
+// below the trig error over a million samples.
 //
-// Operand tiles are K-major without swizzle: core matrices of 8 rows x 4
-// tf32 (128 B), LBO = 128 B along K, SBO = 512 B between 8-row groups.  The
+// Operand tiles are K-major without swizzle: core matrices of 8 rows x 8 f16
+// (128 B), LBO = 128 B along K, SBO = 512 B between 8-row groups.  The
 // operand stages rotate; stage s is rewritten only after the MMAs that read
 // it have signalled their mbarrier, so operand generation runs ahead of the
-// tensor core by up to kTcStages - 1 tiles.  Every wait is bounded; a CTA that gives
-// up sets the device error word, waits (bounded) for its MMAs and copies, and
-// still frees its tensor memory.
+// tensor core by up to kTcStages - 1 tiles.  Every wait is bounded; a CTA
+// that gives up sets the device error word, waits (bounded) for its MMAs and
+// copies, and still frees its tensor memory.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -36,77 +41,118 @@
 
 namespace mri {
 
-constexpr int kTcTile = 16;                          // samples per tile (two K = 8 steps)
+constexpr int kTcTile = 32;                          // samples per tile (two K = 16 steps)
 constexpr int kTcRows = 128;                         // grid rows per CTA = MMA M
 constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
-#ifndef MRI_TC_THREADS
-#define MRI_TC_THREADS 256
-#endif
+constexpr int kTcThreads = 256;
 #ifndef MRI_TC_STAGES
 #define MRI_TC_STAGES 2
 #endif
-constexpr int kTcThreads = MRI_TC_THREADS;           // 256 or 512
+// Waits on the operand-stage barriers: 0 polls, 1 suspends the warp between polls.
+#ifndef MRI_TC_SLEEP_WAIT
+#define MRI_TC_SLEEP_WAIT 0
+#endif
 // Tiles per summation block.  The tensor core's own fp32 accumulation loses
 // a little with every add, with a consistent sign, so the error of a block
 // grows with its length (measured on the 128^3 radial workload: rel-L2 1.4e-5
-// for 64 tiles, 1.9e-6 for 8); the accurate path folds every 8 tiles (128
-// samples), the fast paths every 64.
-constexpr int kTcDrainAccurate = 8;
-constexpr int kTcDrainFast = 64;
-constexpr int kTcPartFloats = kTcRows * kTcTile;     // one A part: 128 x 16 tf32 (8 KB)
-constexpr int kTcSFloats = 3 * kTcPartFloats;        // S = [-B_i; B_r; B_i]: 384 x 16 (24 KB)
-constexpr int kTcStageFloats = 4 * kTcPartFloats + 2 * kTcSFloats;   // A r/i hi/lo, S hi/lo (80 KB)
+// for blocks of 1024 samples, 1.9e-6 for 128); the accurate path folds every
+// 128 samples, the fast paths every 1024.
+constexpr int kTcDrainAccurate = 4;
+constexpr int kTcDrainFast = 32;
+constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // one A part: 128 x 32 f16 (8 KB)
+constexpr int kTcSBytes = 3 * kTcPartBytes;          // S = [-B_i; B_r; B_i]: 384 x 32 (24 KB)
+constexpr int kTcStageBytes = 4 * kTcPartBytes + 2 * kTcSBytes;   // A r/i hi/lo, S hi/lo (80 KB)
 constexpr int kTcStages = MRI_TC_STAGES;             // operand stages in the ring
-constexpr int kTcSpt = kTcTile * kTcRows / kTcThreads;   // samples per thread per table (8 or 4)
+constexpr int kTcSpt = kTcTile * kTcRows / kTcThreads;   // samples per thread per table (16)
 constexpr int kTcColsPerWarp = 256 * 4 / (kTcThreads / 32);  // D columns one warp folds
 constexpr uint32_t kTcTmemCols = 512;
+constexpr int kTcAExp = 15;                          // |A| * scale < 2^kTcAExp
+static_assert(kTcSpt % 8 == 0, "a thread writes whole 8-sample core-matrix rows");
 
-// A parts at part * kTcPartFloats; S hi / lo after them
+// A parts at part * kTcPartBytes; S hi / lo after them
 enum TcPart { A_RH = 0, A_RL, A_IH, A_IL };
-constexpr int kTcSHi = 4 * kTcPartFloats;
-constexpr int kTcSLo = kTcSHi + kTcSFloats;
+constexpr int kTcSHi = 4 * kTcPartBytes;
+constexpr int kTcSLo = kTcSHi + kTcSBytes;
 
 inline bool grid_tc_fits(int nx) { return nx == kTcCols; }
 
 inline size_t grid_tc_smem_bytes(bool realw)
 {
     const int F = realw ? 4 : 5;
-    size_t b = size_t(kTcStages) * kTcStageFloats * 4;    // operand stages
-    b += size_t(kStages) * F * kTcTile * 4;               // record ring
+    size_t b = size_t(kTcStages) * kTcStageBytes;          // operand stages
+    b += size_t(kStages) * F * kTcTile * 4;                // record ring
     b += size_t(kTcRows) * 8 + size_t(kTcCols) * 4;        // (y, z) of the rows, x of the columns
     return b;
 }
 
-// float offset of element (row, k) in a [128][16] K-major no-swizzle tile
-__device__ __forceinline__ int tc_kmaj(int row, int k)
+// byte offset of samples 8 kc .. 8 kc + 7 of row `row` in a [128][32] K-major
+// no-swizzle f16 tile (one 16-byte core-matrix row)
+__device__ __forceinline__ int tc_kmaj_bytes(int row, int kc)
 {
-    return (row >> 3) * 128 + (k >> 2) * 32 + (row & 7) * 4 + (k & 3);
+    return (row >> 3) * 512 + kc * 128 + (row & 7) * 16;
 }
 
-// v = hi + lo with hi = v rounded to the nearest tf32 and lo the exact float
-// remainder (|lo| <= 2^-11 |v|, either sign, so the dropped lo*lo term has no
-// preferred sign)
-__device__ __forceinline__ void tc_split(float v, float& hi, float& lo)
+// Exponent e of the power-of-two scale 2^e applied to the A operand, from the
+// float bits of the bound b = max |w_r| + |w_i|: b < 2^(E - 126) for the
+// biased exponent E, so |A| <= b 2^e < 2^kTcAExp.  Clamped so that 2^e and
+// 2^-e are normal floats (b = 0 or subnormal, or b = inf / NaN, whose results
+// are then inf / NaN anyway).
+__device__ __forceinline__ int tc_scale_exp(unsigned int bound_bits)
 {
-    uint32_t h;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(v));
-    hi = __uint_as_float(h);
-    lo = v - hi;
+    const int E = int((bound_bits >> 23) & 0xFFu);
+    int e = kTcAExp - (E - 126);
+    e = e < -120 ? -120 : (e > 120 ? 120 : e);
+    return e;
 }
 
-// store kTcSpt consecutive samples (k = kTcSpt*q ..) of row i into a part as hi and lo
-__device__ __forceinline__ void tc_store(float* part_hi, float* part_lo, int i, int q,
-                                         const float (&v)[kTcSpt])
+__device__ __forceinline__ float exp2_int(int e)   // 2^e, |e| <= 126
 {
+    return __uint_as_float(uint32_t(e + 127) << 23);
+}
+
+// two floats -> packed f16x2 (round to nearest even), `lo_elem` in bits 0-15
+__device__ __forceinline__ uint32_t pack_f16x2(float lo_elem, float hi_elem)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_elem), "f"(lo_elem));
+    return d;
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t d)
+{
+    float a, b;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(a), "=f"(b)
+        : "r"(d));
+    return make_float2(a, b);
+}
+
+// v = hi + lo for 8 values, two per word: hi = v rounded to f16, lo = the
+// exact float remainder v - hi rounded to f16 (|lo| <= 2^-11 |v|, either
+// sign, so the dropped lo*lo term has no preferred sign)
+__device__ __forceinline__ void tc_split8(const float (&v)[8], uint4& hi, uint4& lo)
+{
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int c = 0; c < kTcSpt / 4; ++c) {
-        float hi[4], lo[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) tc_split(v[4 * c + s], hi[s], lo[s]);
-        const int o = tc_kmaj(i, kTcSpt * q + 4 * c);
-        *reinterpret_cast<float4*>(part_hi + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<float4*>(part_lo + o) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+    for (int j = 0; j < 4; ++j) {
+        h[j] = pack_f16x2(v[2 * j], v[2 * j + 1]);
+        const float2 hf = unpack_f16x2(h[j]);
+        l[j] = pack_f16x2(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
     }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ uint4 neg_f16x8(uint4 v)
+{
+    constexpr uint32_t S = 0x80008000u;
+    return make_uint4(v.x ^ S, v.y ^ S, v.z ^ S, v.w ^ S);
+}
+
+__device__ __forceinline__ void st_shared16(unsigned char* p, uint4 v)
+{
+    *reinterpret_cast<uint4*>(p) = v;
 }
 
 // The D columns warp w folds and writes: lanes 32 (w % 4) .., columns
@@ -140,18 +186,27 @@ __device__ __forceinline__ void tc_drain(uint32_t tmem, int warp, bool have_r)
     tmem_wait_st();
 }
 
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
+{
+#if MRI_TC_SLEEP_WAIT
+    return mbar_wait_bounded_sleep(bar, parity);
+#else
+    return mbar_wait_bounded(bar, parity);
+#endif
+}
+
 template <bool REALW, int TRIG>
 __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParams p)
 {
     constexpr int T = kTcTile;
     constexpr int F = REALW ? 4 : 5;
     constexpr uint32_t TILE_BYTES = uint32_t(F) * T * 4;
-    constexpr uint32_t ID = umma_idesc_tf32(kTcRows, 2 * kTcCols, false);   // N = 256
+    constexpr uint32_t ID = umma_idesc_f16(kTcRows, 2 * kTcCols);   // N = 256
     constexpr int drain_tiles = (TRIG == TRIG_ACCURATE) ? kTcDrainAccurate : kTcDrainFast;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    float* const ops = reinterpret_cast<float*>(smem_raw);
-    float* const ring = ops + kTcStages * kTcStageFloats;
+    unsigned char* const ops = smem_raw;
+    float* const ring = reinterpret_cast<float*>(ops + kTcStages * kTcStageBytes);
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
     float* const xs_sh = reinterpret_cast<float*>(yz_sh + kTcRows);
     __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -167,6 +222,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     const int nt = int(t_end - t_begin);
     const int64_t total_rows = int64_t(p.ny) * p.nz;
     const int64_t row0 = int64_t(blockIdx.x) * kTcRows;
+    const int scale_e = tc_scale_exp(*p.wbound);
+    const float a_scale = exp2_int(scale_e);
 
     for (int r = tid; r < kTcRows; r += kTcThreads) {
         const int64_t row = row0 + r;
@@ -212,15 +269,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         const int st = t % kTcStages;
         const bool new_block = (t % drain_tiles) == 0;
         bool ok = true;
-        // the MMAs of tile t - 3 read stage st
+        // the MMAs of tile t - kTcStages read stage st
         if (t >= kTcStages)
-            ok = mbar_wait_bounded(&mma_bar[st], uint32_t((t - kTcStages) / kTcStages) & 1u);
+            ok = tc_wait(&mma_bar[st], uint32_t((t - kTcStages) / kTcStages) & 1u);
         // a new summation block: fold D into R once tile t - 1 is done (the
         // decision is the same in every thread, so the barrier is uniform)
         if (new_block && t > 0) {
             if (ok)
-                ok = mbar_wait_bounded(&mma_bar[(t - 1) % kTcStages],
-                                       uint32_t((t - 1) / kTcStages) & 1u);
+                ok = tc_wait(&mma_bar[(t - 1) % kTcStages], uint32_t((t - 1) / kTcStages) & 1u);
             if (__syncthreads_or(!ok)) {
                 failed_at = t;
                 break;
@@ -229,52 +285,66 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             tc_drain(tmem, warp, have_r);
             have_r = true;
         }
-        if (ok) ok = mbar_wait_bounded(&full_bar[t % kStages], uint32_t(t / kStages) & 1u);
+        if (ok) ok = tc_wait(&full_bar[t % kStages], uint32_t(t / kStages) & 1u);
         if (ok) {
             const float* rec = ring + (t % kStages) * F * T;
-            float ar[kTcSpt], ai[kTcSpt], br[kTcSpt], bi[kTcSpt], nbi[kTcSpt];
-            // this thread's samples are contiguous in every field of the record tile
-            float kx[kTcSpt], ky[kTcSpt], kz[kTcSpt], wr[kTcSpt], wi[kTcSpt];
-            const int s0 = kTcSpt * gq;
+            unsigned char* const stage = ops + st * kTcStageBytes;
 #pragma unroll
-            for (int c = 0; c < kTcSpt / 4; ++c) {
-                const float4 a = *reinterpret_cast<const float4*>(rec + s0 + 4 * c);
-                const float4 b = *reinterpret_cast<const float4*>(rec + T + s0 + 4 * c);
-                const float4 d = *reinterpret_cast<const float4*>(rec + 2 * T + s0 + 4 * c);
-                const float4 e = *reinterpret_cast<const float4*>(rec + 3 * T + s0 + 4 * c);
-                kx[4 * c] = a.x; kx[4 * c + 1] = a.y; kx[4 * c + 2] = a.z; kx[4 * c + 3] = a.w;
-                ky[4 * c] = b.x; ky[4 * c + 1] = b.y; ky[4 * c + 2] = b.z; ky[4 * c + 3] = b.w;
-                kz[4 * c] = d.x; kz[4 * c + 1] = d.y; kz[4 * c + 2] = d.z; kz[4 * c + 3] = d.w;
-                wr[4 * c] = e.x; wr[4 * c + 1] = e.y; wr[4 * c + 2] = e.z; wr[4 * c + 3] = e.w;
-                if (!REALW) {
-                    const float4 g = *reinterpret_cast<const float4*>(rec + 4 * T + s0 + 4 * c);
-                    wi[4 * c] = g.x; wi[4 * c + 1] = g.y; wi[4 * c + 2] = g.z; wi[4 * c + 3] = g.w;
-                } else {
-                    wi[4 * c] = wi[4 * c + 1] = wi[4 * c + 2] = wi[4 * c + 3] = 0.0f;
-                }
-            }
+            for (int c = 0; c < kTcSpt / 8; ++c) {
+                // this thread's 8 samples are contiguous in every field of the record tile
+                const int s0 = kTcSpt * gq + 8 * c;
+                float kx[8], ky[8], kz[8], wr[8], wi[8];
 #pragma unroll
-            for (int s8 = 0; s8 < kTcSpt; ++s8) {
-                float sn, cs;
-                table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
-                if (REALW) {
-                    ar[s8] = wr[s8] * cs;
-                    ai[s8] = wr[s8] * sn;
-                } else {
-                    ar[s8] = fmaf(wr[s8], cs, -wi[s8] * sn);
-                    ai[s8] = fmaf(wi[s8], cs, wr[s8] * sn);
+                for (int h = 0; h < 2; ++h) {
+                    const float4 a = *reinterpret_cast<const float4*>(rec + s0 + 4 * h);
+                    const float4 b = *reinterpret_cast<const float4*>(rec + T + s0 + 4 * h);
+                    const float4 d = *reinterpret_cast<const float4*>(rec + 2 * T + s0 + 4 * h);
+                    const float4 e = *reinterpret_cast<const float4*>(rec + 3 * T + s0 + 4 * h);
+                    kx[4 * h] = a.x; kx[4 * h + 1] = a.y; kx[4 * h + 2] = a.z; kx[4 * h + 3] = a.w;
+                    ky[4 * h] = b.x; ky[4 * h + 1] = b.y; ky[4 * h + 2] = b.z; ky[4 * h + 3] = b.w;
+                    kz[4 * h] = d.x; kz[4 * h + 1] = d.y; kz[4 * h + 2] = d.z; kz[4 * h + 3] = d.w;
+                    wr[4 * h] = e.x; wr[4 * h + 1] = e.y; wr[4 * h + 2] = e.z; wr[4 * h + 3] = e.w;
+                    if (!REALW) {
+                        const float4 g = *reinterpret_cast<const float4*>(rec + 4 * T + s0 + 4 * h);
+                        wi[4 * h] = g.x; wi[4 * h + 1] = g.y; wi[4 * h + 2] = g.z; wi[4 * h + 3] = g.w;
+                    } else {
+                        wi[4 * h] = wi[4 * h + 1] = wi[4 * h + 2] = wi[4 * h + 3] = 0.0f;
+                    }
                 }
-                table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
-                nbi[s8] = -bi[s8];
+                float ar[8], ai[8], br[8], bi[8];
+#pragma unroll
+                for (int s8 = 0; s8 < 8; ++s8) {
+                    float sn, cs;
+                    table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
+                    const float swr = wr[s8] * a_scale;
+                    if (REALW) {
+                        ar[s8] = swr * cs;
+                        ai[s8] = swr * sn;
+                    } else {
+                        const float swi = wi[s8] * a_scale;
+                        ar[s8] = fmaf(swr, cs, -swi * sn);
+                        ai[s8] = fmaf(swi, cs, swr * sn);
+                    }
+                    table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+                }
+                const int off = tc_kmaj_bytes(gi, (kTcSpt / 8) * gq + c);
+                uint4 h, l;
+                tc_split8(ar, h, l);
+                st_shared16(stage + A_RH * kTcPartBytes + off, h);
+                st_shared16(stage + A_RL * kTcPartBytes + off, l);
+                tc_split8(ai, h, l);
+                st_shared16(stage + A_IH * kTcPartBytes + off, h);
+                st_shared16(stage + A_IL * kTcPartBytes + off, l);
+                // S rows: gi = -B_i, 128 + gi = B_r, 256 + gi = B_i (column gi)
+                tc_split8(bi, h, l);
+                st_shared16(stage + kTcSHi + 2 * kTcPartBytes + off, h);
+                st_shared16(stage + kTcSLo + 2 * kTcPartBytes + off, l);
+                st_shared16(stage + kTcSHi + off, neg_f16x8(h));
+                st_shared16(stage + kTcSLo + off, neg_f16x8(l));
+                tc_split8(br, h, l);
+                st_shared16(stage + kTcSHi + kTcPartBytes + off, h);
+                st_shared16(stage + kTcSLo + kTcPartBytes + off, l);
             }
-            float* const stage = ops + st * kTcStageFloats;
-            tc_store(stage + A_RH * kTcPartFloats, stage + A_RL * kTcPartFloats, gi, gq, ar);
-            tc_store(stage + A_IH * kTcPartFloats, stage + A_IL * kTcPartFloats, gi, gq, ai);
-            // S rows: gi = -B_i, 128 + gi = B_r, 256 + gi = B_i (column gi)
-            tc_store(stage + kTcSHi, stage + kTcSLo, gi, gq, nbi);
-            tc_store(stage + kTcSHi + kTcPartFloats, stage + kTcSLo + kTcPartFloats, gi, gq, br);
-            tc_store(stage + kTcSHi + 2 * kTcPartFloats, stage + kTcSLo + 2 * kTcPartFloats, gi, gq,
-                     bi);
         }
         // generic-proxy writes of the operands -> visible to the tensor core
         fence_proxy_async_smem();
@@ -291,27 +361,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 tma_bulk_g2s(ring + (t % kStages) * F * T, p.rec + (t_begin + t + kStages) * F * T,
                              TILE_BYTES, &full_bar[t % kStages]);
             }
-            const float* stage = ops + st * kTcStageFloats;
+            const unsigned char* stage = ops + st * kTcStageBytes;
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                // K block kb: 2 core matrices = 64 floats into every K-major tile
+                // K step kb: 2 core matrices = 256 B into every K-major tile
                 auto adesc = [&](int part) {
-                    return umma_desc_kmajor(stage + part * kTcPartFloats + kb * 64, 128, 512);
+                    return umma_desc_kmajor(stage + part * kTcPartBytes + kb * 256, 128, 512);
                 };
                 // window of 256 S rows starting at row r0 (16 row groups per 128 rows)
                 auto sdesc = [&](int base, int r0) {
-                    return umma_desc_kmajor(stage + base + (r0 / 128) * kTcPartFloats + kb * 64, 128,
-                                            512);
+                    return umma_desc_kmajor(stage + base + (r0 / 128) * kTcPartBytes + kb * 256,
+                                            128, 512);
                 };
                 const uint32_t acc0 = (new_block && kb == 0) ? 0u : 1u;
                 // [D_r | D_i] += A_r [B_r | B_i]
-                umma_tf32(tmem, adesc(A_RH), sdesc(kTcSHi, 128), ID, acc0);
-                umma_tf32(tmem, adesc(A_RH), sdesc(kTcSLo, 128), ID, 1u);
-                umma_tf32(tmem, adesc(A_RL), sdesc(kTcSHi, 128), ID, 1u);
+                umma_f16(tmem, adesc(A_RH), sdesc(kTcSHi, 128), ID, acc0);
+                umma_f16(tmem, adesc(A_RH), sdesc(kTcSLo, 128), ID, 1u);
+                umma_f16(tmem, adesc(A_RL), sdesc(kTcSHi, 128), ID, 1u);
                 // [D_r | D_i] += A_i [-B_i | B_r]
-                umma_tf32(tmem, adesc(A_IH), sdesc(kTcSHi, 0), ID, 1u);
-                umma_tf32(tmem, adesc(A_IH), sdesc(kTcSLo, 0), ID, 1u);
-                umma_tf32(tmem, adesc(A_IL), sdesc(kTcSHi, 0), ID, 1u);
+                umma_f16(tmem, adesc(A_IH), sdesc(kTcSHi, 0), ID, 1u);
+                umma_f16(tmem, adesc(A_IH), sdesc(kTcSLo, 0), ID, 1u);
+                umma_f16(tmem, adesc(A_IL), sdesc(kTcSHi, 0), ID, 1u);
             }
             umma_commit(&mma_bar[st]);
         }
@@ -320,8 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 
     bool ok = failed_at < 0;
     if (ok && nt > 0) {
-        ok = mbar_wait_bounded(&mma_bar[(nt - 1) % kTcStages],
-                               uint32_t((nt - 1) / kTcStages) & 1u);
+        ok = tc_wait(&mma_bar[(nt - 1) % kTcStages], uint32_t((nt - 1) / kTcStages) & 1u);
         if (__syncthreads_or(!ok)) {
             ok = false;
             failed_at = nt;
@@ -334,6 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 
     if (ok) {
         // R -> outputs: warp w holds rows 32 (w % 4) + lane and its D columns
+        const float inv_scale = exp2_int(-scale_e);
         const int row_local = 32 * (warp & 3) + lane;
         const int64_t row = row0 + row_local;
         const uint32_t wcols = tc_warp_cols(warp);
@@ -348,7 +418,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             if (row < total_rows && nt > 0) {
                 float* o = out + row * kTcCols + col0 + c0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = p.accumulate ? o[j] + v[j] : v[j];
+                for (int j = 0; j < 32; ++j)
+                    o[j] = p.accumulate ? fmaf(v[j], inv_scale, o[j]) : v[j] * inv_scale;
             }
         }
     } else {

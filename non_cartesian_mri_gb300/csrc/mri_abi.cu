@@ -338,6 +338,9 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
 // ---------------------------------------------------------------------------
 // separable grids
 // ---------------------------------------------------------------------------
+// scratch slot of the weight bound the tensor-core grid kernel scales by
+constexpr int64_t kBoundBytes = 256;
+
 struct GridPlan {
     bool table_kernel;      // false: coordinates expanded, general kernel
     bool tensor_cores;      // nx = 128: the tcgen05 kernel
@@ -417,17 +420,23 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     }
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(align256(g.rec_bytes) + g.part_bytes), d->pool,
-                                s) != cudaSuccess)
+                                size_t(align256(g.rec_bytes) + kBoundBytes + g.part_bytes),
+                                d->pool, s) != cudaSuccess)
         return cuda_fail();
     float* rec = reinterpret_cast<float*>(scratch);
-    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
+    unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(g.rec_bytes));
+    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes) + kBoundBytes);
     mri_status st = MRI_OK;
     mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
+    if (g.tensor_cores) {
+        pp.wbound = wbound;
+        if (cudaMemsetAsync(wbound, 0, sizeof(unsigned int), s) != cudaSuccess) st = cuda_fail();
+    }
     const int tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
-    if ((g.tensor_cores ? mri::launch_prep_grid_tc(realw, pp, grid_for(g.ntiles * tile, d->sms), s)
+    if (st == MRI_OK &&
+        (g.tensor_cores ? mri::launch_prep_grid_tc(realw, pp, grid_for(g.ntiles * tile, d->sms), s)
                         : mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * tile, d->sms), s)) !=
-        cudaSuccess)
+            cudaSuccess)
         st = cuda_fail();
     mri::GridParams gp{};
     gp.rec = rec;
@@ -441,6 +450,7 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     gp.nz = nz;
     gp.rows_per_cta = g.rows_per_cta;
     gp.err = d->err;
+    gp.wbound = wbound;
     if (g.splits == 1) {
         gp.out_r = out_r;
         gp.out_i = out_i;
@@ -669,7 +679,7 @@ mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sm
     plan->tiles = g.ntiles;
     plan->coil_groups = 1;
     plan->launches = 2 + (g.splits > 1 ? 1 : 0);
-    plan->scratch_bytes = align256(g.rec_bytes) + g.part_bytes;
+    plan->scratch_bytes = align256(g.rec_bytes) + kBoundBytes + g.part_bytes;
     plan->tensor_cores = g.tensor_cores ? 1 : 0;
     return MRI_OK;
 }

@@ -78,6 +78,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// As mbar_wait_bounded, but each try_wait asks the hardware to suspend the
+// warp for up to `hint_ns` while the phase is incomplete, so a waiting warp
+// does not re-poll shared memory (whose bandwidth the tensor core's operand
+// reads need) in a tight loop.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // 1-D bulk copy global -> shared through the TMA engine; completion is
 // signalled as transaction bytes on `bar`.  dst, src and bytes must be
 // multiples of 16.
@@ -116,6 +144,25 @@ __host__ __device__ constexpr uint32_t umma_idesc_tf32(int M, int N, bool negate
 {
     return (1u << 4) | (2u << 7) | (2u << 10) | (negate_b ? (1u << 14) : 0u) |
            (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B and an f32 D, both
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N)
+{
+    return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// D (tensor memory) (+)= A (smem) * B (smem)^T in f16 x f16 -> f32, K = 16,
+// issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D (tensor memory) (+)= A (smem) * B (smem)^T, issued by one thread.

@@ -133,4 +133,29 @@ def test_tensor_core_width_against_general_path(mri, trig):
     qr, qi = mri.q_grid(*k, dev(xs), dev(ys), dev(zs), wts[0], wts[1], trig=trig)
     qref = oracle.q(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M])
     assert oracle.rel_l2(cplx(qr, qi), qref) <= TOL[trig]
-    assert mri.plan_grid("fhd", M, 128, 3, 7)["samples_per_tile"] == 16
+    assert mri.plan_grid("fhd", M, 128, 3, 7)["samples_per_tile"] == 32
+
+
+@pytest.mark.parametrize("k", [-100, 60])
+def test_tensor_core_weight_scale_is_exact(mri, k):
+    """The tensor-core kernel scales its f16 operands by a power of two taken
+    from the largest weight, so multiplying D by 2^k must multiply F^H D by
+    exactly 2^k (the same bits up to the exponent), far outside f16's range;
+    all-zero weights give exact zeros."""
+    w = wl.make_workload("fhd_128_radial")
+    M = 4099
+    xs = (np.arange(128) - 64).astype(np.float32)
+    ys = np.array([-7, 12], np.float32)
+    zs = np.array([5], np.float32)
+    k3 = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    axes = [dev(xs), dev(ys), dev(zs)]
+    phi = [dev(w.rPhi[:M]), dev(w.iPhi[:M])]
+    d = [dev(w.rD[:M]), dev(w.iD[:M])]
+    for trig in ("accurate", "fast"):
+        r0, i0 = mri.fhd_grid(*k3, *axes, *phi, *d, trig=trig)
+        s = float(2.0 ** k)
+        r1, i1 = mri.fhd_grid(*k3, *axes, *phi, d[0] * s, d[1] * s, trig=trig)
+        assert torch.equal(r1, r0 * s) and torch.equal(i1, i0 * s), trig
+        z = torch.zeros_like(d[0])
+        rz, iz = mri.fhd_grid(*k3, *axes, *phi, z, z, trig=trig)
+        assert torch.count_nonzero(rz) == 0 and torch.count_nonzero(iz) == 0
