@@ -6,27 +6,30 @@
 // a complex matrix product over the samples: a dense contraction.  Here a CTA
 // owns 128 grid rows (the MMA M) of a grid with nx = 128 columns (the MMA N).
 // For each tile of 32 samples (two K = 16 steps) the warps evaluate Mz
-// (128 rows x 32 samples) and Ex (32 samples x 128 columns) into shared
-// memory, each value split into an f16 high part and the f16-rounded
-// remainder; one thread then issues, per K step, two N = 256 products into
-// [D_r | D_i]:
+// (128 rows x 32 samples, the A operand) into tensor memory and Ex (32
+// samples x 128 columns, the B operand) into shared memory, each value split
+// into an f16 high part and the f16-rounded remainder; one thread then
+// issues, per K step, two N = 256 products into [D_r | D_i]:
 //   [D_r | D_i] += A_r [B_r | B_i]  +  A_i [-B_i | B_r],
 // reading the B operands as two 256-row windows of one 384-row block
 // S = [-B_i; B_r; B_i], with each real product done as hi*hi + hi*lo + lo*hi
 // (12 tcgen05.mma of 128 x 256 x 16 per tile).  The two f16 parts carry about
 // 22 significant bits, and the dropped lo*lo term is below 2^-22 of a
 // product, so every product keeps close to fp32 accuracy.  f16 has a narrow
-// exponent range: the A operand (Mz) is multiplied by a power of two chosen
-// from the largest |w_r| + |w_i| of the call so that every |A| < 2^15, and
-// the results are multiplied back exactly; |B| <= 1 needs no scale.
-// Shared-memory bandwidth (operand reads by the tensor core plus operand
-// writes by the warps) and the tensor pipe bind this kernel about equally.
-// The accumulators live in tensor memory: D_r, D_i (columns 0-255) collect
-// one block of tiles and are then added into the running sums R_r, R_i
-// (columns 256-511), the blocked summation that keeps accumulation error
-// below the trig error over a million samples.
+// exponent range: the A operand is multiplied by a power of two chosen from
+// the largest |w_r| + |w_i| of the call so that every |A| < 2^15, and the
+// results are multiplied back exactly; |B| <= 1 needs no scale.
 //
-// Operand tiles are K-major without swizzle: core matrices of 8 rows x 8 f16
+// Shared-memory bandwidth binds a kernel whose operands all pass through
+// shared memory (operand writes by the warps plus operand reads by the
+// tensor core); with A in tensor memory only B takes that path.  D (tensor
+// memory columns 0-255) collects one block of tiles and is then added into
+// running sums R held in registers (each thread owns 128 of the 128 x 256
+// sums: its warp's lane quarter and half of the columns), the blocked
+// summation that keeps accumulation error below the trig error over a
+// million samples.  Columns 256.. hold the A stages (64 columns each).
+//
+// B tiles are K-major without swizzle: core matrices of 8 rows x 8 f16
 // (128 B), LBO = 128 B along K, SBO = 512 B between 8-row groups.  The
 // operand stages rotate; stage s is rewritten only after the MMAs that read
 // it have signalled their mbarrier, so operand generation runs ahead of the
@@ -46,7 +49,7 @@ constexpr int kTcRows = 128;                         // grid rows per CTA = MMA 
 constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
 constexpr int kTcThreads = 256;
 #ifndef MRI_TC_STAGES
-#define MRI_TC_STAGES 2
+#define MRI_TC_STAGES 3
 #endif
 // Waits on the operand-stage barriers: 0 polls, 1 suspends the warp between polls.
 #ifndef MRI_TC_SLEEP_WAIT
@@ -57,29 +60,40 @@ constexpr int kTcThreads = 256;
 // grows with its length (measured on the 128^3 radial workload: rel-L2 1.4e-5
 // for blocks of 1024 samples, 1.9e-6 for 128); the accurate path folds every
 // 128 samples, the fast paths every 1024.
-constexpr int kTcDrainAccurate = 4;
-constexpr int kTcDrainFast = 32;
-constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // one A part: 128 x 32 f16 (8 KB)
+#ifndef MRI_TC_DRAIN_ACCURATE
+#define MRI_TC_DRAIN_ACCURATE 4
+#endif
+#ifndef MRI_TC_DRAIN_FAST
+#define MRI_TC_DRAIN_FAST 32
+#endif
+constexpr int kTcDrainAccurate = MRI_TC_DRAIN_ACCURATE;
+constexpr int kTcDrainFast = MRI_TC_DRAIN_FAST;
+constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // 128 S rows x 32 f16 (8 KB)
 constexpr int kTcSBytes = 3 * kTcPartBytes;          // S = [-B_i; B_r; B_i]: 384 x 32 (24 KB)
-constexpr int kTcStageBytes = 4 * kTcPartBytes + 2 * kTcSBytes;   // A r/i hi/lo, S hi/lo (80 KB)
+constexpr int kTcStageBytes = 2 * kTcSBytes;         // S hi, S lo (48 KB)
 constexpr int kTcStages = MRI_TC_STAGES;             // operand stages in the ring
 constexpr int kTcSpt = kTcTile * kTcRows / kTcThreads;   // samples per thread per table (16)
-constexpr int kTcColsPerWarp = 256 * 4 / (kTcThreads / 32);  // D columns one warp folds
+constexpr int kTcColsPerWarp = 256 * 4 / (kTcThreads / 32);  // D columns one warp folds (128)
+constexpr uint32_t kTcDCols = 256;                   // D_r | D_i
+constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per lane (16 columns)
+constexpr uint32_t kTcAStageCols = 4 * kTcAPartCols; // A r/i hi/lo (64 columns)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcAExp = 15;                          // |A| * scale < 2^kTcAExp
-static_assert(kTcSpt % 8 == 0, "a thread writes whole 8-sample core-matrix rows");
+static_assert(kTcSpt == 16 && kTcThreads == 256, "generation mapping");
+static_assert(kTcStages >= 1 && kTcDCols + kTcStages * kTcAStageCols <= kTcTmemCols,
+              "A stages fit tensor memory");
 
-// A parts at part * kTcPartBytes; S hi / lo after them
+// A parts (tensor-memory column offset / kTcAPartCols within a stage)
 enum TcPart { A_RH = 0, A_RL, A_IH, A_IL };
-constexpr int kTcSHi = 4 * kTcPartBytes;
-constexpr int kTcSLo = kTcSHi + kTcSBytes;
+constexpr int kTcSHi = 0;
+constexpr int kTcSLo = kTcSBytes;
 
 inline bool grid_tc_fits(int nx) { return nx == kTcCols; }
 
 inline size_t grid_tc_smem_bytes(bool realw)
 {
     const int F = realw ? 4 : 5;
-    size_t b = size_t(kTcStages) * kTcStageBytes;          // operand stages
+    size_t b = size_t(kTcStages) * kTcStageBytes;          // B operand stages
     b += size_t(kStages) * F * kTcTile * 4;                // record ring
     b += size_t(kTcRows) * 8 + size_t(kTcCols) * 4;        // (y, z) of the rows, x of the columns
     return b;
@@ -162,30 +176,6 @@ __device__ __forceinline__ uint32_t tc_warp_cols(int warp)
     return uint32_t(kTcColsPerWarp) * uint32_t(warp >> 2);
 }
 
-// Fold D (columns 0-255) into R (256-511).
-__device__ __forceinline__ void tc_drain(uint32_t tmem, int warp, bool have_r)
-{
-    const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
-    const uint32_t dcol = tc_warp_cols(warp);
-    const uint32_t rcol = dcol + 256u;
-#pragma unroll 1
-    for (uint32_t c0 = 0; c0 < uint32_t(kTcColsPerWarp); c0 += 32) {
-        float d[32];
-        tmem_ld32(tmem + lanes + dcol + c0, d);
-        if (have_r) {
-            float r[32];
-            tmem_ld32(tmem + lanes + rcol + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] += r[j];
-        } else {
-            tmem_wait_ld();
-        }
-        tmem_st32(tmem + lanes + rcol + c0, d);
-    }
-    tmem_wait_st();
-}
-
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 {
 #if MRI_TC_SLEEP_WAIT
@@ -193,6 +183,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 #else
     return mbar_wait_bounded(bar, parity);
 #endif
+}
+
+// this thread's 8 samples s0 .. s0 + 7 of record field f (contiguous in the tile)
+__device__ __forceinline__ void tc_load8(const float* rec, int f, int s0, float (&v)[8])
+{
+    const float4 a = *reinterpret_cast<const float4*>(rec + f * kTcTile + s0);
+    const float4 b = *reinterpret_cast<const float4*>(rec + f * kTcTile + s0 + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 template <bool REALW, int TRIG>
@@ -256,62 +255,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         }
     }
 
-    // generation: row / column gi, samples kTcSpt*gq .. of the tile
-    const int gi = tid / (kTcTile / kTcSpt);
-    const int gq = tid % (kTcTile / kTcSpt);
-    const float2 yz = yz_sh[gi];
+    // A (Mz) generation: row ra = this thread's tensor-memory lane (a warp
+    // reaches only its own lane quarter), samples 16 ah .. 16 ah + 15, which
+    // are the 8 columns of K step ah in every A part.
+    const int ra = 32 * (warp & 3) + lane;
+    const int ah = warp >> 2;
+    const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
+    // B (Ex) generation: column gi, samples 16 gq ..  Lane bits 0-2 pick the
+    // column within an 8-row group of S, bit 3 the sample half, bit 4 one of
+    // the warp's two groups: the 8 lanes of each quarter warp, which share a
+    // 16-byte store phase, write 8 core-matrix rows in distinct banks.
+    const int gi = ((2 * warp + ((lane >> 4) & 1)) << 3) | (lane & 7);
+    const int gq = (lane >> 3) & 1;
+    const float2 yz = yz_sh[ra];
     const float xc = xs_sh[gi];
 
-    bool have_r = false;
+    // running sums: lanes of this warp's quarter, D columns tc_warp_cols(warp) ..
+    float R[kTcColsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kTcColsPerWarp; ++j) R[j] = 0.0f;
+    const uint32_t dcols = tmem + lanes + tc_warp_cols(warp);
+    auto drain = [&]() {
+#pragma unroll
+        for (int c = 0; c < kTcColsPerWarp / 32; ++c) {
+            float d[32];
+            tmem_ld32(dcols + uint32_t(32 * c), d);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) R[32 * c + j] += d[j];
+        }
+    };
+
     int failed_at = -1;
     int issued = 0;   // tiles whose MMAs were issued
     for (int t = 0; t < nt; ++t) {
         const int st = t % kTcStages;
         const bool new_block = (t % drain_tiles) == 0;
+        const uint32_t acol = tmem + kTcDCols + uint32_t(st) * kTcAStageCols;
         bool ok = true;
         // the MMAs of tile t - kTcStages read stage st
         if (t >= kTcStages)
             ok = tc_wait(&mma_bar[st], uint32_t((t - kTcStages) / kTcStages) & 1u);
-        // a new summation block: fold D into R once tile t - 1 is done (the
-        // decision is the same in every thread, so the barrier is uniform)
-        if (new_block && t > 0) {
-            if (ok)
-                ok = tc_wait(&mma_bar[(t - 1) % kTcStages], uint32_t((t - 1) / kTcStages) & 1u);
-            if (__syncthreads_or(!ok)) {
-                failed_at = t;
-                break;
-            }
-            tc_fence_after_sync();
-            tc_drain(tmem, warp, have_r);
-            have_r = true;
-        }
         if (ok) ok = tc_wait(&full_bar[t % kStages], uint32_t(t / kStages) & 1u);
+        // warp-uniform: the tensor-memory stores below are .sync.aligned
+        ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             const float* rec = ring + (t % kStages) * F * T;
-            unsigned char* const stage = ops + st * kTcStageBytes;
 #pragma unroll
-            for (int c = 0; c < kTcSpt / 8; ++c) {
-                // this thread's 8 samples are contiguous in every field of the record tile
-                const int s0 = kTcSpt * gq + 8 * c;
-                float kx[8], ky[8], kz[8], wr[8], wi[8];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float4 a = *reinterpret_cast<const float4*>(rec + s0 + 4 * h);
-                    const float4 b = *reinterpret_cast<const float4*>(rec + T + s0 + 4 * h);
-                    const float4 d = *reinterpret_cast<const float4*>(rec + 2 * T + s0 + 4 * h);
-                    const float4 e = *reinterpret_cast<const float4*>(rec + 3 * T + s0 + 4 * h);
-                    kx[4 * h] = a.x; kx[4 * h + 1] = a.y; kx[4 * h + 2] = a.z; kx[4 * h + 3] = a.w;
-                    ky[4 * h] = b.x; ky[4 * h + 1] = b.y; ky[4 * h + 2] = b.z; ky[4 * h + 3] = b.w;
-                    kz[4 * h] = d.x; kz[4 * h + 1] = d.y; kz[4 * h + 2] = d.z; kz[4 * h + 3] = d.w;
-                    wr[4 * h] = e.x; wr[4 * h + 1] = e.y; wr[4 * h + 2] = e.z; wr[4 * h + 3] = e.w;
-                    if (!REALW) {
-                        const float4 g = *reinterpret_cast<const float4*>(rec + 4 * T + s0 + 4 * h);
-                        wi[4 * h] = g.x; wi[4 * h + 1] = g.y; wi[4 * h + 2] = g.z; wi[4 * h + 3] = g.w;
-                    } else {
-                        wi[4 * h] = wi[4 * h + 1] = wi[4 * h + 2] = wi[4 * h + 3] = 0.0f;
-                    }
-                }
-                float ar[8], ai[8], br[8], bi[8];
+            for (int c = 0; c < 2; ++c) {
+                const int s0 = 16 * ah + 8 * c;
+                float ky[8], kz[8], wr[8], wi[8];
+                tc_load8(rec, 1, s0, ky);
+                tc_load8(rec, 2, s0, kz);
+                tc_load8(rec, 3, s0, wr);
+                if (!REALW) tc_load8(rec, 4, s0, wi);
+                float ar[8], ai[8];
 #pragma unroll
                 for (int s8 = 0; s8 < 8; ++s8) {
                     float sn, cs;
@@ -325,16 +323,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                         ar[s8] = fmaf(swr, cs, -swi * sn);
                         ai[s8] = fmaf(swi, cs, swr * sn);
                     }
-                    table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
                 }
-                const int off = tc_kmaj_bytes(gi, (kTcSpt / 8) * gq + c);
+                // samples s0 .. s0 + 7 = columns 8 ah + 4 c .. of each part
+                const uint32_t col = acol + uint32_t(8 * ah + 4 * c);
                 uint4 h, l;
                 tc_split8(ar, h, l);
-                st_shared16(stage + A_RH * kTcPartBytes + off, h);
-                st_shared16(stage + A_RL * kTcPartBytes + off, l);
+                tmem_st4(col + A_RH * kTcAPartCols, h);
+                tmem_st4(col + A_RL * kTcAPartCols, l);
                 tc_split8(ai, h, l);
-                st_shared16(stage + A_IH * kTcPartBytes + off, h);
-                st_shared16(stage + A_IL * kTcPartBytes + off, l);
+                tmem_st4(col + A_IH * kTcAPartCols, h);
+                tmem_st4(col + A_IL * kTcAPartCols, l);
+            }
+            unsigned char* const stage = ops + st * kTcStageBytes;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int s0 = 16 * gq + 8 * c;
+                float kx[8], br[8], bi[8];
+                tc_load8(rec, 0, s0, kx);
+#pragma unroll
+                for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+                const int off = tc_kmaj_bytes(gi, 2 * gq + c);
+                uint4 h, l;
                 // S rows: gi = -B_i, 128 + gi = B_r, 256 + gi = B_i (column gi)
                 tc_split8(bi, h, l);
                 st_shared16(stage + kTcSHi + 2 * kTcPartBytes + off, h);
@@ -345,8 +354,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 st_shared16(stage + kTcSHi + kTcPartBytes + off, h);
                 st_shared16(stage + kTcSLo + kTcPartBytes + off, l);
             }
+            tmem_wait_st();
         }
-        // generic-proxy writes of the operands -> visible to the tensor core
+        // a new summation block: fold D into R once tile t - 1 is done, before
+        // the first MMA of tile t overwrites D (the decision is the same in
+        // every thread, so the barrier is uniform)
+        if (new_block && t > 0) {
+            if (ok)
+                ok = tc_wait(&mma_bar[(t - 1) % kTcStages], uint32_t((t - 1) / kTcStages) & 1u);
+            if (__syncthreads_or(!ok)) {
+                failed_at = t;
+                break;
+            }
+            tc_fence_after_sync();
+            drain();
+        }
+        // operand writes (generic proxy to shared memory, tcgen05.st to
+        // tensor memory) -> visible to the tensor core
         fence_proxy_async_smem();
         tc_fence_before_sync();
         if (__syncthreads_or(!ok)) {
@@ -364,9 +388,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             const unsigned char* stage = ops + st * kTcStageBytes;
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-                // K step kb: 2 core matrices = 256 B into every K-major tile
-                auto adesc = [&](int part) {
-                    return umma_desc_kmajor(stage + part * kTcPartBytes + kb * 256, 128, 512);
+                // K step kb: 8 columns of every A part, 2 core matrices = 256 B of S
+                auto a = [&](int part) {
+                    return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
                 };
                 // window of 256 S rows starting at row r0 (16 row groups per 128 rows)
                 auto sdesc = [&](int base, int r0) {
@@ -375,13 +399,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 };
                 const uint32_t acc0 = (new_block && kb == 0) ? 0u : 1u;
                 // [D_r | D_i] += A_r [B_r | B_i]
-                umma_f16(tmem, adesc(A_RH), sdesc(kTcSHi, 128), ID, acc0);
-                umma_f16(tmem, adesc(A_RH), sdesc(kTcSLo, 128), ID, 1u);
-                umma_f16(tmem, adesc(A_RL), sdesc(kTcSHi, 128), ID, 1u);
+                umma_f16_ta(tmem, a(A_RH), sdesc(kTcSHi, 128), ID, acc0);
+                umma_f16_ta(tmem, a(A_RH), sdesc(kTcSLo, 128), ID, 1u);
+                umma_f16_ta(tmem, a(A_RL), sdesc(kTcSHi, 128), ID, 1u);
                 // [D_r | D_i] += A_i [-B_i | B_r]
-                umma_f16(tmem, adesc(A_IH), sdesc(kTcSHi, 0), ID, 1u);
-                umma_f16(tmem, adesc(A_IH), sdesc(kTcSLo, 0), ID, 1u);
-                umma_f16(tmem, adesc(A_IL), sdesc(kTcSHi, 0), ID, 1u);
+                umma_f16_ta(tmem, a(A_IH), sdesc(kTcSHi, 0), ID, 1u);
+                umma_f16_ta(tmem, a(A_IH), sdesc(kTcSLo, 0), ID, 1u);
+                umma_f16_ta(tmem, a(A_IL), sdesc(kTcSHi, 0), ID, 1u);
             }
             umma_commit(&mma_bar[st]);
         }
@@ -396,30 +420,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             failed_at = nt;
         } else {
             tc_fence_after_sync();
-            tc_drain(tmem, warp, have_r);
-            have_r = true;
+            drain();
         }
     }
 
     if (ok) {
-        // R -> outputs: warp w holds rows 32 (w % 4) + lane and its D columns
+        // R -> outputs: this thread holds row ra and its warp's D columns
         const float inv_scale = exp2_int(-scale_e);
-        const int row_local = 32 * (warp & 3) + lane;
-        const int64_t row = row0 + row_local;
+        const int64_t row = row0 + ra;
         const uint32_t wcols = tc_warp_cols(warp);
         float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride;
-        const uint32_t taddr = tmem + (uint32_t(32 * (warp & 3)) << 16) + 256u + wcols;
-        const int col0 = int(wcols & 127u);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTcColsPerWarp; c0 += 32) {
-            float v[32];
-            tmem_ld32(taddr + c0, v);
-            tmem_wait_ld();
-            if (row < total_rows && nt > 0) {
-                float* o = out + row * kTcCols + col0 + c0;
+        if (row < total_rows && nt > 0) {
+            float* o = out + row * kTcCols + (wcols & 127u);
+            if (p.accumulate) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    o[j] = p.accumulate ? fmaf(v[j], inv_scale, o[j]) : v[j] * inv_scale;
+                for (int j = 0; j < kTcColsPerWarp; ++j) o[j] = fmaf(R[j], inv_scale, o[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kTcColsPerWarp; ++j) o[j] = R[j] * inv_scale;
             }
         }
     } else {

@@ -165,6 +165,19 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D (tensor memory) (+)= A (tensor memory) * B (smem)^T in f16 x f16 -> f32,
+// K = 16: A's M rows are the tensor-memory lanes, its 16 K elements packed
+// two per 32-bit column (8 columns).  Issued by one thread.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D (tensor memory) (+)= A (smem) * B (smem)^T, issued by one thread.
 __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate)
@@ -246,6 +259,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
         : "memory");
+}
+
+// 4 consecutive columns of this warp's 32 lanes from each thread's registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld()
