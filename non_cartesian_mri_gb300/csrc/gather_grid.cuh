@@ -52,8 +52,10 @@ struct GridParams {
     int64_t split_stride;
     int accumulate;
     unsigned int* err;
-    // tensor-core kernel: float bits of max |w_r| + |w_i| over the samples
+    // tensor-core kernel: float bits of max |w_r| + |w_i| over the samples,
+    // and the B operand tiles (kTcStageBytes per record tile)
     const unsigned int* wbound;
+    const unsigned char* s_tab;
 };
 
 // The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks

@@ -5,11 +5,13 @@
 //   Mz = Mu * e^{i2pi(ky y + kz z)},  Ex = e^{i2pi kx x},
 // a complex matrix product over the samples: a dense contraction.  Here a CTA
 // owns 128 grid rows (the MMA M) of a grid with nx = 128 columns (the MMA N).
-// For each tile of 32 samples (two K = 16 steps) the warps evaluate Mz
-// (128 rows x 32 samples, the A operand) into tensor memory and Ex (32
-// samples x 128 columns, the B operand) into shared memory, each value split
+// Ex (32 samples x 128 columns per tile of 32 samples, the B operand) is the
+// same for every CTA: build_ex_tiles_kernel evaluates it once per call into
+// a table of operand tiles in the tensor core's shared-memory layout, and a
+// CTA fetches each tile with one TMA bulk copy.  The warps evaluate Mz (128
+// rows x 32 samples, the A operand) into tensor memory.  Every value is split
 // into an f16 high part and the f16-rounded remainder; one thread then
-// issues, per K step, two N = 256 products into [D_r | D_i]:
+// issues, per K step (two per tile), two N = 256 products into [D_r | D_i]:
 //   [D_r | D_i] += A_r [B_r | B_i]  +  A_i [-B_i | B_r],
 // reading the B operands as two 256-row windows of one 384-row block
 // S = [-B_i; B_r; B_i], with each real product done as hi*hi + hi*lo + lo*hi
@@ -21,8 +23,8 @@
 // results are multiplied back exactly; |B| <= 1 needs no scale.
 //
 // Shared-memory bandwidth binds a kernel whose operands all pass through
-// shared memory (operand writes by the warps plus operand reads by the
-// tensor core); with A in tensor memory only B takes that path.  D (tensor
+// shared memory (operand writes plus operand reads by the tensor core); with
+// A in tensor memory only B takes that path, written by the TMA.  D (tensor
 // memory columns 0-255) collects one block of tiles and is then added into
 // running sums R held in registers (each thread owns 128 of the 128 x 256
 // sums: its warp's lane quarter and half of the columns), the blocked
@@ -47,9 +49,18 @@ namespace mri {
 constexpr int kTcTile = 32;                          // samples per tile (two K = 16 steps)
 constexpr int kTcRows = 128;                         // grid rows per CTA = MMA M
 constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
-constexpr int kTcThreads = 256;
+#ifndef MRI_TC_THREADS
+#define MRI_TC_THREADS 256
+#endif
+constexpr int kTcThreads = MRI_TC_THREADS;           // 256 or 512
+constexpr int kTcWarps = kTcThreads / 32;
 #ifndef MRI_TC_STAGES
-#define MRI_TC_STAGES 3
+#define MRI_TC_STAGES 4
+#endif
+// How many tiles ahead of the MMAs the B tile copies run (1 or 2); the stage
+// a copy fills must have been released by the MMAs of tile u - kTcStages.
+#ifndef MRI_TC_S_LEAD
+#define MRI_TC_S_LEAD 2
 #endif
 // Waits on the operand-stage barriers: 0 polls, 1 suspends the warp between polls.
 #ifndef MRI_TC_SLEEP_WAIT
@@ -72,14 +83,14 @@ constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // 128 S rows x 32 f16 (8 K
 constexpr int kTcSBytes = 3 * kTcPartBytes;          // S = [-B_i; B_r; B_i]: 384 x 32 (24 KB)
 constexpr int kTcStageBytes = 2 * kTcSBytes;         // S hi, S lo (48 KB)
 constexpr int kTcStages = MRI_TC_STAGES;             // operand stages in the ring
-constexpr int kTcSpt = kTcTile * kTcRows / kTcThreads;   // samples per thread per table (16)
-constexpr int kTcColsPerWarp = 256 * 4 / (kTcThreads / 32);  // D columns one warp folds (128)
+constexpr int kTcColsPerWarp = 256 * 4 / kTcWarps;  // D columns one warp folds (128 or 64)
 constexpr uint32_t kTcDCols = 256;                   // D_r | D_i
 constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per lane (16 columns)
 constexpr uint32_t kTcAStageCols = 4 * kTcAPartCols; // A r/i hi/lo (64 columns)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcAExp = 15;                          // |A| * scale < 2^kTcAExp
-static_assert(kTcSpt == 16 && kTcThreads == 256, "generation mapping");
+static_assert(kTcThreads == 256 || kTcThreads == 512, "generation mapping");
+constexpr int kTcAChunks = kTcTile / 8 / (kTcWarps / 4);   // 8-sample A chunks per thread
 static_assert(kTcStages >= 1 && kTcDCols + kTcStages * kTcAStageCols <= kTcTmemCols,
               "A stages fit tensor memory");
 
@@ -95,7 +106,7 @@ inline size_t grid_tc_smem_bytes(bool realw)
     const int F = realw ? 4 : 5;
     size_t b = size_t(kTcStages) * kTcStageBytes;          // B operand stages
     b += size_t(kStages) * F * kTcTile * 4;                // record ring
-    b += size_t(kTcRows) * 8 + size_t(kTcCols) * 4;        // (y, z) of the rows, x of the columns
+    b += size_t(kTcRows) * 8;                              // (y, z) of the rows
     return b;
 }
 
@@ -185,6 +196,44 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 #endif
 }
 
+// The B operand tiles: tile t holds, for every grid column c and sample s of
+// record tile t, the f16 hi / lo parts of -sin, cos and sin of the phase
+// kx[s] x[c] in S = [-B_i; B_r; B_i] row order (hi block, then lo block),
+// each block K-major as the MMA reads it.  One thread per (tile, 8-row
+// group, 8-sample chunk, row): consecutive threads write consecutive 16-byte
+// core-matrix rows, so a warp's stores are contiguous.
+template <int TRIG>
+__global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, int fields,
+                                                             int64_t ntiles, const float* xs,
+                                                             unsigned char* s_tab)
+{
+    constexpr int ITEMS = kTcCols * kTcTile / 8;       // 512 (column, chunk) items per tile
+    const int64_t total = ntiles * ITEMS;
+    for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
+         item += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = item / ITEMS;
+        const int r = int(item - t * ITEMS);
+        const int gi = ((r >> 5) << 3) | (r & 7);     // column
+        const int kc = (r >> 3) & 3;                  // samples 8 kc ..
+        const float* kx = rec + t * fields * kTcTile + 8 * kc;
+        const float xc = xs[gi];
+        float br[8], bi[8];
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+        unsigned char* const tile = s_tab + t * kTcStageBytes;
+        const int off = tc_kmaj_bytes(gi, kc);        // == 16 r
+        uint4 h, l;
+        tc_split8(bi, h, l);
+        *reinterpret_cast<uint4*>(tile + kTcSHi + 2 * kTcPartBytes + off) = h;
+        *reinterpret_cast<uint4*>(tile + kTcSLo + 2 * kTcPartBytes + off) = l;
+        *reinterpret_cast<uint4*>(tile + kTcSHi + off) = neg_f16x8(h);
+        *reinterpret_cast<uint4*>(tile + kTcSLo + off) = neg_f16x8(l);
+        tc_split8(br, h, l);
+        *reinterpret_cast<uint4*>(tile + kTcSHi + kTcPartBytes + off) = h;
+        *reinterpret_cast<uint4*>(tile + kTcSLo + kTcPartBytes + off) = l;
+    }
+}
+
 // this thread's 8 samples s0 .. s0 + 7 of record field f (contiguous in the tile)
 __device__ __forceinline__ void tc_load8(const float* rec, int f, int s0, float (&v)[8])
 {
@@ -207,9 +256,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     unsigned char* const ops = smem_raw;
     float* const ring = reinterpret_cast<float*>(ops + kTcStages * kTcStageBytes);
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
-    float* const xs_sh = reinterpret_cast<float*>(yz_sh + kTcRows);
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t mma_bar[kTcStages];
+    __shared__ __align__(8) uint64_t full_bar[kStages];     // record tile landed
+    __shared__ __align__(8) uint64_t s_bar[kTcStages];      // B operand tile landed
+    __shared__ __align__(8) uint64_t mma_bar[kTcStages];    // MMAs of the stage done
     __shared__ uint32_t tmem_base_sh;
 
     const int tid = threadIdx.x;
@@ -234,41 +283,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         }
         yz_sh[r] = yz;
     }
-    for (int c = tid; c < kTcCols; c += kTcThreads) xs_sh[c] = p.xs[c];
     if (warp == 0) tmem_alloc(&tmem_base_sh, kTcTmemCols);
     if (tid == 0) {
 #pragma unroll
         for (int st = 0; st < kStages; ++st) mbar_init(&full_bar[st], 1);
 #pragma unroll
-        for (int st = 0; st < kTcStages; ++st) mbar_init(&mma_bar[st], 1);
+        for (int st = 0; st < kTcStages; ++st) {
+            mbar_init(&s_bar[st], 1);
+            mbar_init(&mma_bar[st], 1);
+        }
         fence_barrier_init();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
+    // B tile u into stage u % kTcStages (thread 0 only)
+    auto load_s = [&](int u) {
+        uint64_t* bar = &s_bar[u % kTcStages];
+        mbar_arrive_expect_tx(bar, uint32_t(kTcStageBytes));
+        tma_bulk_g2s(ops + (u % kTcStages) * kTcStageBytes, p.s_tab + (t_begin + u) * kTcStageBytes,
+                     uint32_t(kTcStageBytes), bar);
+    };
+    int s_loaded = 0;     // B tiles whose copy thread 0 has issued
+    int s_consumed = 0;   // B tiles thread 0 has seen land
     if (tid == 0) {
         for (int st = 0; st < kStages && st < nt; ++st) {
             mbar_arrive_expect_tx(&full_bar[st], TILE_BYTES);
             tma_bulk_g2s(ring + st * F * T, p.rec + (t_begin + st) * F * T, TILE_BYTES,
                          &full_bar[st]);
         }
+        for (; s_loaded < kTcStages && s_loaded < nt; ++s_loaded) load_s(s_loaded);
     }
 
     // A (Mz) generation: row ra = this thread's tensor-memory lane (a warp
-    // reaches only its own lane quarter), samples 16 ah .. 16 ah + 15, which
-    // are the 8 columns of K step ah in every A part.
+    // reaches only its own lane quarter), samples 8 kTcAChunks ah .., which
+    // are columns 4 kTcAChunks ah .. of every A part (two f16 per column).
     const int ra = 32 * (warp & 3) + lane;
     const int ah = warp >> 2;
     const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
-    // B (Ex) generation: column gi, samples 16 gq ..  Lane bits 0-2 pick the
-    // column within an 8-row group of S, bit 3 the sample half, bit 4 one of
-    // the warp's two groups: the 8 lanes of each quarter warp, which share a
-    // 16-byte store phase, write 8 core-matrix rows in distinct banks.
-    const int gi = ((2 * warp + ((lane >> 4) & 1)) << 3) | (lane & 7);
-    const int gq = (lane >> 3) & 1;
     const float2 yz = yz_sh[ra];
-    const float xc = xs_sh[gi];
 
     // running sums: lanes of this warp's quarter, D columns tc_warp_cols(warp) ..
     float R[kTcColsPerWarp];
@@ -287,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     };
 
     int failed_at = -1;
-    int issued = 0;   // tiles whose MMAs were issued
+    bool s_fail = false;   // thread 0: a B tile or stage wait timed out
     for (int t = 0; t < nt; ++t) {
         const int st = t % kTcStages;
         const bool new_block = (t % drain_tiles) == 0;
@@ -302,8 +356,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         if (ok) {
             const float* rec = ring + (t % kStages) * F * T;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int s0 = 16 * ah + 8 * c;
+            for (int c = 0; c < kTcAChunks; ++c) {
+                const int s0 = 8 * (kTcAChunks * ah + c);
                 float ky[8], kz[8], wr[8], wi[8];
                 tc_load8(rec, 1, s0, ky);
                 tc_load8(rec, 2, s0, kz);
@@ -324,8 +378,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                         ai[s8] = fmaf(swi, cs, swr * sn);
                     }
                 }
-                // samples s0 .. s0 + 7 = columns 8 ah + 4 c .. of each part
-                const uint32_t col = acol + uint32_t(8 * ah + 4 * c);
+                // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
+                const uint32_t col = acol + uint32_t(s0 / 2);
                 uint4 h, l;
                 tc_split8(ar, h, l);
                 tmem_st4(col + A_RH * kTcAPartCols, h);
@@ -333,26 +387,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 tc_split8(ai, h, l);
                 tmem_st4(col + A_IH * kTcAPartCols, h);
                 tmem_st4(col + A_IL * kTcAPartCols, l);
-            }
-            unsigned char* const stage = ops + st * kTcStageBytes;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int s0 = 16 * gq + 8 * c;
-                float kx[8], br[8], bi[8];
-                tc_load8(rec, 0, s0, kx);
-#pragma unroll
-                for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
-                const int off = tc_kmaj_bytes(gi, 2 * gq + c);
-                uint4 h, l;
-                // S rows: gi = -B_i, 128 + gi = B_r, 256 + gi = B_i (column gi)
-                tc_split8(bi, h, l);
-                st_shared16(stage + kTcSHi + 2 * kTcPartBytes + off, h);
-                st_shared16(stage + kTcSLo + 2 * kTcPartBytes + off, l);
-                st_shared16(stage + kTcSHi + off, neg_f16x8(h));
-                st_shared16(stage + kTcSLo + off, neg_f16x8(l));
-                tc_split8(br, h, l);
-                st_shared16(stage + kTcSHi + kTcPartBytes + off, h);
-                st_shared16(stage + kTcSLo + kTcPartBytes + off, l);
             }
             tmem_wait_st();
         }
@@ -362,60 +396,74 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         if (new_block && t > 0) {
             if (ok)
                 ok = tc_wait(&mma_bar[(t - 1) % kTcStages], uint32_t((t - 1) / kTcStages) & 1u);
-            if (__syncthreads_or(!ok)) {
+            if (__syncthreads_or(!ok || s_fail)) {
                 failed_at = t;
                 break;
             }
             tc_fence_after_sync();
             drain();
         }
-        // operand writes (generic proxy to shared memory, tcgen05.st to
-        // tensor memory) -> visible to the tensor core
-        fence_proxy_async_smem();
+        // A written to tensor memory -> visible to the MMAs
         tc_fence_before_sync();
-        if (__syncthreads_or(!ok)) {
+        if (__syncthreads_or(!ok || s_fail)) {
             failed_at = t;
             break;
         }
         tc_fence_after_sync();
         if (tid == 0) {
             if (t + kStages < nt) {
-                fence_proxy_async_smem();
                 mbar_arrive_expect_tx(&full_bar[t % kStages], TILE_BYTES);
                 tma_bulk_g2s(ring + (t % kStages) * F * T, p.rec + (t_begin + t + kStages) * F * T,
                              TILE_BYTES, &full_bar[t % kStages]);
             }
-            const unsigned char* stage = ops + st * kTcStageBytes;
+            bool s_ok = mbar_wait_bounded(&s_bar[st], uint32_t(t / kTcStages) & 1u);
+            if (s_ok) {
+                s_consumed = t + 1;
+                const unsigned char* stage = ops + st * kTcStageBytes;
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                // K step kb: 8 columns of every A part, 2 core matrices = 256 B of S
-                auto a = [&](int part) {
-                    return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
-                };
-                // window of 256 S rows starting at row r0 (16 row groups per 128 rows)
-                auto sdesc = [&](int base, int r0) {
-                    return umma_desc_kmajor(stage + base + (r0 / 128) * kTcPartBytes + kb * 256,
-                                            128, 512);
-                };
-                const uint32_t acc0 = (new_block && kb == 0) ? 0u : 1u;
-                // [D_r | D_i] += A_r [B_r | B_i]
-                umma_f16_ta(tmem, a(A_RH), sdesc(kTcSHi, 128), ID, acc0);
-                umma_f16_ta(tmem, a(A_RH), sdesc(kTcSLo, 128), ID, 1u);
-                umma_f16_ta(tmem, a(A_RL), sdesc(kTcSHi, 128), ID, 1u);
-                // [D_r | D_i] += A_i [-B_i | B_r]
-                umma_f16_ta(tmem, a(A_IH), sdesc(kTcSHi, 0), ID, 1u);
-                umma_f16_ta(tmem, a(A_IH), sdesc(kTcSLo, 0), ID, 1u);
-                umma_f16_ta(tmem, a(A_IL), sdesc(kTcSHi, 0), ID, 1u);
+                for (int kb = 0; kb < 2; ++kb) {
+                    // K step kb: 8 columns of every A part, 2 core matrices = 256 B of S
+                    auto a = [&](int part) {
+                        return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
+                    };
+                    // window of 256 S rows starting at row r0 (16 row groups per 128 rows)
+                    auto sdesc = [&](int base, int r0) {
+                        return umma_desc_kmajor(stage + base + (r0 / 128) * kTcPartBytes + kb * 256,
+                                                128, 512);
+                    };
+                    const uint32_t acc0 = (new_block && kb == 0) ? 0u : 1u;
+                    // [D_r | D_i] += A_r [B_r | B_i]
+                    umma_f16_ta(tmem, a(A_RH), sdesc(kTcSHi, 128), ID, acc0);
+                    umma_f16_ta(tmem, a(A_RH), sdesc(kTcSLo, 128), ID, 1u);
+                    umma_f16_ta(tmem, a(A_RL), sdesc(kTcSHi, 128), ID, 1u);
+                    // [D_r | D_i] += A_i [-B_i | B_r]
+                    umma_f16_ta(tmem, a(A_IH), sdesc(kTcSHi, 0), ID, 1u);
+                    umma_f16_ta(tmem, a(A_IH), sdesc(kTcSLo, 0), ID, 1u);
+                    umma_f16_ta(tmem, a(A_IL), sdesc(kTcSHi, 0), ID, 1u);
+                }
+                umma_commit(&mma_bar[st]);
+                // refill a stage for tile t + lead as soon as the MMAs that
+                // read it (tile t + lead - kTcStages) are done
+                const int u = t + MRI_TC_S_LEAD;
+                if (u >= kTcStages && u < nt && s_loaded == u) {
+                    s_ok = mbar_wait_bounded(&mma_bar[u % kTcStages],
+                                             uint32_t((u - kTcStages) / kTcStages) & 1u);
+                    if (s_ok) {
+                        load_s(u);
+                        ++s_loaded;
+                    }
+                }
             }
-            umma_commit(&mma_bar[st]);
+            // a timeout here stops every thread at the next barrier
+            if (!s_ok) s_fail = true;
         }
-        issued = t + 1;
     }
 
     bool ok = failed_at < 0;
     if (ok && nt > 0) {
-        ok = tc_wait(&mma_bar[(nt - 1) % kTcStages], uint32_t((nt - 1) / kTcStages) & 1u);
-        if (__syncthreads_or(!ok)) {
+        if (!s_fail)
+            ok = tc_wait(&mma_bar[(nt - 1) % kTcStages], uint32_t((nt - 1) / kTcStages) & 1u);
+        if (__syncthreads_or(!ok || s_fail)) {
             ok = false;
             failed_at = nt;
         } else {
@@ -444,7 +492,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         // Report, then let the MMAs and copies in flight finish before the
         // CTA's shared and tensor memory are released.
         if (tid == 0) {
+            // thread 0 issued the MMAs of exactly the first s_consumed tiles
             unsigned int bits = DEVERR_TILE_WAIT_TIMEOUT;
+            const int issued = s_consumed;
             if (issued > 0 && !mbar_wait_bounded(&mma_bar[(issued - 1) % kTcStages],
                                                  uint32_t((issued - 1) / kTcStages) & 1u))
                 bits |= DEVERR_DRAIN_TIMEOUT;
@@ -452,6 +502,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             const int last = (first + kStages < nt) ? first + kStages : nt;
             for (int u = first; u < last; ++u)
                 if (!mbar_wait_bounded(&full_bar[u % kStages], uint32_t(u / kStages) & 1u))
+                    bits |= DEVERR_DRAIN_TIMEOUT;
+            for (int u = s_consumed; u < s_loaded; ++u)
+                if (!mbar_wait_bounded(&s_bar[u % kTcStages], uint32_t(u / kTcStages) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
             atomicOr(p.err, bits);
         }

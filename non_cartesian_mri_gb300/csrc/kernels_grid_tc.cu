@@ -37,6 +37,25 @@ cudaError_t launch_grid_tc(bool realw, int trig, const GridParams& p, dim3 grid,
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_build_ex_tiles(int trig, const float* rec, bool realw, int64_t ntiles,
+                                  const float* xs, unsigned char* s_tab, int grid, cudaStream_t s)
+{
+    const int fields = realw ? 4 : 5;
+    switch (trig) {
+        case TRIG_ACCURATE:
+            build_ex_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            break;
+        case TRIG_FAST:
+            build_ex_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            break;
+        case TRIG_FAST_RR:
+            build_ex_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prep_grid_tc(bool realw, const PrepParams& p, int grid, cudaStream_t s)
 {
     if (realw)

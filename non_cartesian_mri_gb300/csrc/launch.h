@@ -39,6 +39,9 @@ cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cu
 // tensor-core grid path (kernels_grid_tc.cu), nx = 128
 cudaError_t launch_grid_tc(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_prep_grid_tc(bool realw, const PrepParams& p, int grid, cudaStream_t s);
+// B operand tiles of the tensor-core grid kernel from its records (kx) and xs
+cudaError_t launch_build_ex_tiles(int trig, const float* rec, bool realw, int64_t ntiles,
+                                  const float* xs, unsigned char* s_tab, int grid, cudaStream_t s);
 // one translation unit per grid width (kernels_grid_<nx>.cu)
 cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_grid_64(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);

@@ -350,6 +350,7 @@ struct GridPlan {
     int splits;
     int64_t rec_bytes;
     int64_t part_bytes;
+    int64_t s_bytes;        // tensor cores: the B operand tiles
     int ctas_per_sm;
 };
 
@@ -370,6 +371,7 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
                        : 1;
         g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 5) * mri::kTcTile * 4;
         g.part_bytes = g.splits > 1 ? int64_t(g.splits) * 2 * N * 4 : 0;
+        g.s_bytes = g.ntiles * int64_t(mri::kTcStageBytes);
         return g;
     }
     g.rows_per_cta = mri::kGridVoxelsPerCta / nx;
@@ -420,12 +422,15 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     }
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(align256(g.rec_bytes) + kBoundBytes + g.part_bytes),
+                                size_t(align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes) +
+                                       g.s_bytes),
                                 d->pool, s) != cudaSuccess)
         return cuda_fail();
     float* rec = reinterpret_cast<float*>(scratch);
     unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(g.rec_bytes));
     float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes) + kBoundBytes);
+    unsigned char* s_tab = reinterpret_cast<unsigned char*>(
+        scratch + align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes));
     mri_status st = MRI_OK;
     mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
     if (g.tensor_cores) {
@@ -437,6 +442,10 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
         (g.tensor_cores ? mri::launch_prep_grid_tc(realw, pp, grid_for(g.ntiles * tile, d->sms), s)
                         : mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * tile, d->sms), s)) !=
             cudaSuccess)
+        st = cuda_fail();
+    if (st == MRI_OK && g.tensor_cores &&
+        mri::launch_build_ex_tiles(trig, rec, realw, g.ntiles, xs, s_tab,
+                                   grid_for(g.ntiles * 512, d->sms), s) != cudaSuccess)
         st = cuda_fail();
     mri::GridParams gp{};
     gp.rec = rec;
@@ -451,6 +460,7 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     gp.rows_per_cta = g.rows_per_cta;
     gp.err = d->err;
     gp.wbound = wbound;
+    gp.s_tab = s_tab;
     if (g.splits == 1) {
         gp.out_r = out_r;
         gp.out_i = out_i;
@@ -679,7 +689,8 @@ mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sm
     plan->tiles = g.ntiles;
     plan->coil_groups = 1;
     plan->launches = 2 + (g.splits > 1 ? 1 : 0);
-    plan->scratch_bytes = align256(g.rec_bytes) + kBoundBytes + g.part_bytes;
+    plan->scratch_bytes = align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes) + g.s_bytes;
+    plan->launches += g.tensor_cores ? 1 : 0;
     plan->tensor_cores = g.tensor_cores ? 1 : 0;
     return MRI_OK;
 }
