@@ -168,6 +168,10 @@ mri_status mri_fhd_noalloc(const float* kx, const float* ky, const float* kz,
  * voxel-sample pair; sin/cos are evaluated per (sample, column) and
  * (sample, row) only.  The table kernel covers nx in {32, 64, 128, 256};
  * other grids are expanded to coordinates and take the general kernel.
+ * With nx = 128 the sum over samples is done as a complex matrix product on
+ * the tensor cores (tcgen05, f16 operands split into high and low parts so
+ * that each product keeps ~22 bits, fp32 accumulation, blocked summation);
+ * the results meet the same tolerances as the other paths.
  * Edge cases as mri_fhd.
  */
 mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz,
@@ -182,6 +186,26 @@ mri_status mri_q_grid(const float* kx, const float* ky, const float* kz,
                       const float* rPhi, const float* iPhi,
                       int64_t M, float* rQ, float* iQ,
                       mri_trig trig, int accumulate, void* stream);
+
+/*
+ * Batched F^H D on a separable grid: mri_fhd_batched's B coils (rD, iD
+ * coil-major [B][M]; outputs rFhD, iFhD coil-major [B][N], N = nx*ny*nz,
+ * voxel order as mri_fhd_grid).  One trajectory, so the x factor of the
+ * phase is tabulated once per call and the (y, z) factor once per (row,
+ * sample) for up to 8 coils at a time, each sin/cos pair serving every coil
+ * of the group.  As for mri_fhd_batched, the pages do not describe this
+ * variant; it is F^H D applied to several D.  nx = 128 runs on the tensor
+ * cores with the coils of a group sharing each MMA's rows; other grids are
+ * expanded to coordinates and take mri_fhd_batched.  Edge cases as
+ * mri_fhd_batched.
+ */
+mri_status mri_fhd_batched_grid(const float* kx, const float* ky, const float* kz,
+                                const float* xs, int nx, const float* ys, int ny,
+                                const float* zs, int nz,
+                                const float* rPhi, const float* iPhi,
+                                const float* rD, const float* iD, int64_t B, int64_t M,
+                                float* rFhD, float* iFhD,
+                                mri_trig trig, int accumulate, void* stream);
 
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
@@ -212,6 +236,10 @@ mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sm
 /* The same for mri_fhd_grid (kind MRI_KIND_FHD) and mri_q_grid (MRI_KIND_Q). */
 mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
                          mri_plan* plan);
+
+/* The same for mri_fhd_batched_grid with B coils (first coil group's shape). */
+mri_status mri_plan_grid_batched(int64_t B, int64_t M, int nx, int ny, int nz, int num_sms,
+                                 mri_plan* plan);
 
 /*
  * Device-side error bits of the current device (bit 0: a k-tile wait timed

@@ -85,6 +85,11 @@ def load():
         lib.mri_q_grid.restype = ctypes.c_int
         lib.mri_plan_grid.argtypes = [I, I64, I, I, I, I, ctypes.POINTER(_Plan)]
         lib.mri_plan_grid.restype = ctypes.c_int
+        lib.mri_fhd_batched_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 4
+                                             + [I64, I64, P, P, I, I, P])
+        lib.mri_fhd_batched_grid.restype = ctypes.c_int
+        lib.mri_plan_grid_batched.argtypes = [I64, I64, I, I, I, I, ctypes.POINTER(_Plan)]
+        lib.mri_plan_grid_batched.restype = ctypes.c_int
         lib.mri_timing_begin.argtypes = []
         lib.mri_timing_begin.restype = ctypes.c_int
         lib.mri_timing_end.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -251,6 +256,31 @@ def fhd_grid(kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD, *, trig="fast", accumul
     return m.result((r, i))
 
 
+def fhd_batched_grid(kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD, *, trig="fast",
+                     accumulate=False, out=None, stream=None):
+    """Batched F^H D on the separable grid xs x ys x zs over coil-major rD, iD
+    [B, M]; returns (rFhD, iFhD) [B, N], x fastest."""
+    m = _Marshal([kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD])
+    kx, ky, kz, xs, ys, zs, rPhi, iPhi, rD, iD = m.tensors
+    M = kx.shape[0]
+    _same_len("sample", [kx, ky, kz, rPhi, iPhi], M)
+    if rD.dim() != 2 or rD.shape[1] != M or iD.shape != rD.shape:
+        raise ValueError(f"rD, iD must be [B, {M}]")
+    for t in (xs, ys, zs):
+        if t.dim() != 1:
+            raise ValueError("grid axes must be 1-D")
+    B = rD.shape[0]
+    nx, ny, nz = xs.shape[0], ys.shape[0], zs.shape[0]
+    r, i = _outputs(out, (B, nx * ny * nz), m.device)
+    with torch.cuda.device(m.device):
+        _check(load().mri_fhd_batched_grid(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(xs), nx, _ptr(ys),
+                                           ny, _ptr(zs), nz, _ptr(rPhi), _ptr(iPhi), _ptr(rD),
+                                           _ptr(iD), B, M, _ptr(r), _ptr(i), TRIG[trig],
+                                           int(bool(accumulate)), _stream_handle(stream)),
+               "mri_fhd_batched_grid")
+    return m.result((r, i))
+
+
 def q_grid(kx, ky, kz, xs, ys, zs, rPhi, iPhi, *, trig="fast", accumulate=False, out=None,
            stream=None):
     """Q on the separable grid xs x ys x zs; returns (rQ, iQ) [N], x fastest."""
@@ -273,6 +303,14 @@ def plan_grid(kind: str, M: int, nx: int, ny: int, nz: int, num_sms: int = 0) ->
     p = _Plan()
     _check(load().mri_plan_grid(KIND[kind], M, nx, ny, nz, num_sms, ctypes.byref(p)),
            "mri_plan_grid")
+    return {name: getattr(p, name) for name, _ in _Plan._fields_}
+
+
+def plan_grid_batched(B: int, M: int, nx: int, ny: int, nz: int, num_sms: int = 0) -> dict:
+    """The launch shape of mri_fhd_batched_grid."""
+    p = _Plan()
+    _check(load().mri_plan_grid_batched(B, M, nx, ny, nz, num_sms, ctypes.byref(p)),
+           "mri_plan_grid_batched")
     return {name: getattr(p, name) for name, _ in _Plan._fields_}
 
 

@@ -54,11 +54,13 @@ constexpr int kStages = 3;   // tiles resident per CTA
 //       F^H D: kx ky kz rMu iMu     Q: kx ky kz w
 //   coil groups (BC > 1): array of records [kTile][F4]
 //       kx ky kz rMu_0..rMu_{BC-1} iMu_0..iMu_{BC-1} (zero padding to F4)
-template <int BC, bool REALW, int TILE = kTile>
+//   SOA forces the structure-of-arrays layout for coil groups too
+//       kx ky kz rMu_0..rMu_{BC-1} iMu_0..iMu_{BC-1}, each [TILE]
+template <int BC, bool REALW, int TILE = kTile, bool SOA = false>
 struct Rec {
     static_assert(!REALW || BC == 1, "a real weight has one coil");
     static constexpr int F = REALW ? 4 : 3 + 2 * BC;
-    static constexpr bool AOS = BC > 1;
+    static constexpr bool AOS = BC > 1 && !SOA;
     static constexpr int F4 = (F + 3) / 4 * 4;
     static constexpr int STRIDE = AOS ? F4 : F;
     static constexpr int TILE_FLOATS = TILE * STRIDE;
@@ -105,9 +107,11 @@ struct PrepParams {
     int64_t ntiles;
     float kscale;           // 4 (quarter turns), 2*pi (radians) or 1 (turns)
     float* rec;
-    // Optional (single weight only): raised by atomicMax to the float bits of
-    // max over samples of |w_r| + |w_i|; the caller zeroes it first.
+    // Optional: raised by atomicMax to the float bits of the largest
+    // |w_r| + |w_i| over samples and coils; the caller zeroes it first.
     unsigned int* wbound = nullptr;
+    // Coils b0 .. b0 + coils_valid - 1 exist; the rest of a group get weight 0.
+    int coils_valid = 1 << 30;
 };
 
 struct GatherParams {
@@ -129,10 +133,10 @@ struct GatherParams {
 // ---------------------------------------------------------------------------
 // prep: cmpMu fused with the tile-record layout
 // ---------------------------------------------------------------------------
-template <int BC, bool REALW, int TILE = kTile>
+template <int BC, bool REALW, int TILE = kTile, bool SOA = false>
 __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
 {
-    using R = Rec<BC, REALW, TILE>;
+    using R = Rec<BC, REALW, TILE, SOA>;
     const int64_t total = p.ntiles * TILE;
     float wmax = 0.0f;
     for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < total;
@@ -153,16 +157,20 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
             } else {
 #pragma unroll
                 for (int b = 0; b < BC; ++b) {
-                    const float rd = p.rD[(p.b0 + b) * p.M + m];
-                    const float id = p.iD[(p.b0 + b) * p.M + m];
-                    f[3 + b] = fmaf(ip, id, rp * rd);               // Re conj(Phi) D
-                    f[3 + BC + b] = fmaf(-ip, rd, rp * id);         // Im conj(Phi) D
+                    if (b < p.coils_valid) {
+                        const float rd = p.rD[(p.b0 + b) * p.M + m];
+                        const float id = p.iD[(p.b0 + b) * p.M + m];
+                        f[3 + b] = fmaf(ip, id, rp * rd);           // Re conj(Phi) D
+                        f[3 + BC + b] = fmaf(-ip, rd, rp * id);     // Im conj(Phi) D
+                    }
                 }
             }
-            if constexpr (REALW)
+            if constexpr (REALW) {
                 wmax = fmaxf(wmax, fabsf(f[3]));
-            else if constexpr (BC == 1)
-                wmax = fmaxf(wmax, fabsf(f[3]) + fabsf(f[4]));
+            } else {
+#pragma unroll
+                for (int b = 0; b < BC; ++b) wmax = fmaxf(wmax, fabsf(f[3 + b]) + fabsf(f[3 + BC + b]));
+            }
         }
         if (R::AOS) {
             float4* dst = reinterpret_cast<float4*>(base + j * R::F4);
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
             for (int i = 0; i < R::F; ++i) base[i * TILE + j] = f[i];
         }
     }
-    if (BC == 1 && p.wbound != nullptr) {
+    if (p.wbound != nullptr) {
         // non-negative floats order like their bit patterns (a NaN sorts last)
         const unsigned int w = __reduce_max_sync(0xffffffffu, __float_as_uint(wmax));
         if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(p.wbound, w);

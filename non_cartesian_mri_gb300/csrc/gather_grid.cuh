@@ -56,6 +56,10 @@ struct GridParams {
     // and the B operand tiles (kTcStageBytes per record tile)
     const unsigned int* wbound;
     const unsigned char* s_tab;
+    // tensor-core coil groups: coils present, and the output offset of coil b
+    // (out_r + b * coil_stride ..)
+    int coils;
+    int64_t coil_stride;
 };
 
 // The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks

@@ -49,10 +49,7 @@ namespace mri {
 constexpr int kTcTile = 32;                          // samples per tile (two K = 16 steps)
 constexpr int kTcRows = 128;                         // grid rows per CTA = MMA M
 constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
-#ifndef MRI_TC_THREADS
-#define MRI_TC_THREADS 256
-#endif
-constexpr int kTcThreads = MRI_TC_THREADS;           // 256 or 512
+constexpr int kTcThreads = 256;
 constexpr int kTcWarps = kTcThreads / 32;
 #ifndef MRI_TC_STAGES
 #define MRI_TC_STAGES 4
@@ -61,10 +58,6 @@ constexpr int kTcWarps = kTcThreads / 32;
 // a copy fills must have been released by the MMAs of tile u - kTcStages.
 #ifndef MRI_TC_S_LEAD
 #define MRI_TC_S_LEAD 2
-#endif
-// Waits on the operand-stage barriers: 0 polls, 1 suspends the warp between polls.
-#ifndef MRI_TC_SLEEP_WAIT
-#define MRI_TC_SLEEP_WAIT 0
 #endif
 // Tiles per summation block.  The tensor core's own fp32 accumulation loses
 // a little with every add, with a consistent sign, so the error of a block
@@ -89,7 +82,7 @@ constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per l
 constexpr uint32_t kTcAStageCols = 4 * kTcAPartCols; // A r/i hi/lo (64 columns)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcAExp = 15;                          // |A| * scale < 2^kTcAExp
-static_assert(kTcThreads == 256 || kTcThreads == 512, "generation mapping");
+static_assert(kTcThreads == 256, "generation mapping");
 constexpr int kTcAChunks = kTcTile / 8 / (kTcWarps / 4);   // 8-sample A chunks per thread
 static_assert(kTcStages >= 1 && kTcDCols + kTcStages * kTcAStageCols <= kTcTmemCols,
               "A stages fit tensor memory");
@@ -101,13 +94,41 @@ constexpr int kTcSLo = kTcSBytes;
 
 inline bool grid_tc_fits(int nx) { return nx == kTcCols; }
 
-inline size_t grid_tc_smem_bytes(bool realw)
+// Coils per CTA (a coil group): the MMA's 128 rows are bc coils x 128 / bc
+// grid rows, m = b * (128 / bc) + r.
+inline bool grid_tc_coils_ok(int bc) { return bc == 1 || bc == 4 || bc == 8; }
+
+inline size_t grid_tc_smem_bytes(bool realw, int bc = 1)
 {
-    const int F = realw ? 4 : 5;
+    const int F = realw ? 4 : 3 + 2 * bc;
+    const int rc = kTcRows / bc;
     size_t b = size_t(kTcStages) * kTcStageBytes;          // B operand stages
     b += size_t(kStages) * F * kTcTile * 4;                // record ring
-    b += size_t(kTcRows) * 8;                              // (y, z) of the rows
+    b += size_t(rc) * 8;                                   // (y, z) of the rows
+    if (bc > 1) b += size_t(2) * kTcTile * rc * 8;         // row factors, two tiles
     return b;
+}
+
+// e[s * RC + r] = a_scale e^{i phase(ky[s] y_r + kz[s] z_r)} for the RC grid
+// rows of a CTA and the samples of one record tile: with several coils per
+// CTA the (y, z) factor of a row is shared by its coils, so it is evaluated
+// once per (row, sample) and read back by each coil's thread.
+template <int TRIG, int RC>
+__device__ __forceinline__ void tc_row_factors(const float* rec, const float2* yz_sh, float2* e,
+                                               float a_scale, int tid)
+{
+    constexpr int ITEMS = kTcTile * RC;
+    static_assert(ITEMS % kTcThreads == 0, "row-factor items");
+#pragma unroll
+    for (int k = 0; k < ITEMS / kTcThreads; ++k) {
+        const int i = tid + k * kTcThreads;
+        const int s = i / RC;
+        const int r = i % RC;
+        const float2 yz = yz_sh[r];
+        float sn, cs;
+        table_sincos<TRIG>(fmaf(rec[2 * kTcTile + s], yz.y, rec[kTcTile + s] * yz.x), sn, cs);
+        e[i] = make_float2(cs * a_scale, sn * a_scale);
+    }
 }
 
 // byte offset of samples 8 kc .. 8 kc + 7 of row `row` in a [128][32] K-major
@@ -189,11 +210,7 @@ __device__ __forceinline__ uint32_t tc_warp_cols(int warp)
 
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 {
-#if MRI_TC_SLEEP_WAIT
-    return mbar_wait_bounded_sleep(bar, parity);
-#else
     return mbar_wait_bounded(bar, parity);
-#endif
 }
 
 // The B operand tiles: tile t holds, for every grid column c and sample s of
@@ -243,11 +260,13 @@ __device__ __forceinline__ void tc_load8(const float* rec, int f, int s0, float 
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <bool REALW, int TRIG>
+template <int BC, bool REALW, int TRIG>
 __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParams p)
 {
+    static_assert(BC == 1 || (!REALW && (BC == 4 || BC == 8)), "coil group");
     constexpr int T = kTcTile;
-    constexpr int F = REALW ? 4 : 5;
+    constexpr int F = REALW ? 4 : 3 + 2 * BC;
+    constexpr int RC = kTcRows / BC;                  // grid rows per CTA
     constexpr uint32_t TILE_BYTES = uint32_t(F) * T * 4;
     constexpr uint32_t ID = umma_idesc_f16(kTcRows, 2 * kTcCols);   // N = 256
     constexpr int drain_tiles = (TRIG == TRIG_ACCURATE) ? kTcDrainAccurate : kTcDrainFast;
@@ -256,6 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     unsigned char* const ops = smem_raw;
     float* const ring = reinterpret_cast<float*>(ops + kTcStages * kTcStageBytes);
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
+    float2* const e_sh = yz_sh + RC;                  // BC > 1: row factors of two tiles
     __shared__ __align__(8) uint64_t full_bar[kStages];     // record tile landed
     __shared__ __align__(8) uint64_t s_bar[kTcStages];      // B operand tile landed
     __shared__ __align__(8) uint64_t mma_bar[kTcStages];    // MMAs of the stage done
@@ -269,11 +289,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     const int64_t t_end = (p.ntiles * (split + 1)) / p.splits;
     const int nt = int(t_end - t_begin);
     const int64_t total_rows = int64_t(p.ny) * p.nz;
-    const int64_t row0 = int64_t(blockIdx.x) * kTcRows;
+    const int64_t row0 = int64_t(blockIdx.x) * RC;
     const int scale_e = tc_scale_exp(*p.wbound);
     const float a_scale = exp2_int(scale_e);
 
-    for (int r = tid; r < kTcRows; r += kTcThreads) {
+    for (int r = tid; r < RC; r += kTcThreads) {
         const int64_t row = row0 + r;
         float2 yz = make_float2(0.f, 0.f);
         if (row < total_rows) {
@@ -319,10 +339,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     // A (Mz) generation: row ra = this thread's tensor-memory lane (a warp
     // reaches only its own lane quarter), samples 8 kTcAChunks ah .., which
     // are columns 4 kTcAChunks ah .. of every A part (two f16 per column).
+    // With BC coils, lane ra is coil ra / RC of grid row ra % RC.
     const int ra = 32 * (warp & 3) + lane;
     const int ah = warp >> 2;
+    const int coil = ra / RC;
+    const int rr = ra % RC;
     const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
-    const float2 yz = yz_sh[ra];
+    const float2 yz = yz_sh[rr];
 
     // running sums: lanes of this warp's quarter, D columns tc_warp_cols(warp) ..
     float R[kTcColsPerWarp];
@@ -342,7 +365,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 
     int failed_at = -1;
     bool s_fail = false;   // thread 0: a B tile or stage wait timed out
-    for (int t = 0; t < nt; ++t) {
+    if constexpr (BC > 1) {
+        // row factors of tile 0; later tiles' are made one tile ahead
+        bool ok0 = true;
+        if (nt > 0) {
+            ok0 = mbar_wait_bounded(&full_bar[0], 0u);
+            if (ok0) tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, a_scale, tid);
+        }
+        if (__syncthreads_or(!ok0)) failed_at = 0;
+    }
+    for (int t = 0; t < nt && failed_at < 0; ++t) {
         const int st = t % kTcStages;
         const bool new_block = (t % drain_tiles) == 0;
         const uint32_t acol = tmem + kTcDCols + uint32_t(st) * kTcAStageCols;
@@ -358,24 +390,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 #pragma unroll
             for (int c = 0; c < kTcAChunks; ++c) {
                 const int s0 = 8 * (kTcAChunks * ah + c);
-                float ky[8], kz[8], wr[8], wi[8];
-                tc_load8(rec, 1, s0, ky);
-                tc_load8(rec, 2, s0, kz);
-                tc_load8(rec, 3, s0, wr);
-                if (!REALW) tc_load8(rec, 4, s0, wi);
                 float ar[8], ai[8];
+                if constexpr (BC == 1) {
+                    float ky[8], kz[8], wr[8], wi[8];
+                    tc_load8(rec, 1, s0, ky);
+                    tc_load8(rec, 2, s0, kz);
+                    tc_load8(rec, 3, s0, wr);
+                    if (!REALW) tc_load8(rec, 4, s0, wi);
 #pragma unroll
-                for (int s8 = 0; s8 < 8; ++s8) {
-                    float sn, cs;
-                    table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
-                    const float swr = wr[s8] * a_scale;
-                    if (REALW) {
-                        ar[s8] = swr * cs;
-                        ai[s8] = swr * sn;
-                    } else {
-                        const float swi = wi[s8] * a_scale;
-                        ar[s8] = fmaf(swr, cs, -swi * sn);
-                        ai[s8] = fmaf(swi, cs, swr * sn);
+                    for (int s8 = 0; s8 < 8; ++s8) {
+                        float sn, cs;
+                        table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
+                        const float swr = wr[s8] * a_scale;
+                        if (REALW) {
+                            ar[s8] = swr * cs;
+                            ai[s8] = swr * sn;
+                        } else {
+                            const float swi = wi[s8] * a_scale;
+                            ar[s8] = fmaf(swr, cs, -swi * sn);
+                            ai[s8] = fmaf(swi, cs, swr * sn);
+                        }
+                    }
+                } else {
+                    // Mu of this thread's coil times the row's shared factor
+                    const float2* e = e_sh + (t & 1) * T * RC;
+                    float wr[8], wi[8];
+                    tc_load8(rec, 3 + coil, s0, wr);
+                    tc_load8(rec, 3 + BC + coil, s0, wi);
+#pragma unroll
+                    for (int s8 = 0; s8 < 8; ++s8) {
+                        const float2 f = e[(s0 + s8) * RC + rr];
+                        ar[s8] = fmaf(wr[s8], f.x, -wi[s8] * f.y);
+                        ai[s8] = fmaf(wi[s8], f.x, wr[s8] * f.y);
                     }
                 }
                 // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
@@ -389,6 +435,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 tmem_st4(col + A_IL * kTcAPartCols, l);
             }
             tmem_wait_st();
+            if constexpr (BC > 1) {
+                // row factors of the next tile (its buffer was last read by
+                // tile t - 1, before the previous barrier)
+                if (t + 1 < nt) {
+                    ok = mbar_wait_bounded(&full_bar[(t + 1) % kStages],
+                                           uint32_t((t + 1) / kStages) & 1u);
+                    if (ok)
+                        tc_row_factors<TRIG, RC>(ring + ((t + 1) % kStages) * F * T, yz_sh,
+                                                 e_sh + ((t + 1) & 1) * T * RC, a_scale, tid);
+                }
+            }
         }
         // a new summation block: fold D into R once tile t - 1 is done, before
         // the first MMA of tile t overwrites D (the decision is the same in
@@ -473,12 +530,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     }
 
     if (ok) {
-        // R -> outputs: this thread holds row ra and its warp's D columns
+        // R -> outputs: this thread holds grid row rr of coil `coil` and its
+        // warp's D columns
         const float inv_scale = exp2_int(-scale_e);
-        const int64_t row = row0 + ra;
+        const int64_t row = row0 + rr;
         const uint32_t wcols = tc_warp_cols(warp);
-        float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride;
-        if (row < total_rows && nt > 0) {
+        float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride +
+                           coil * p.coil_stride;
+        if (row < total_rows && coil < p.coils && nt > 0) {
             float* o = out + row * kTcCols + (wcols & 127u);
             if (p.accumulate) {
 #pragma unroll

@@ -37,10 +37,12 @@ cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
 // separable-grid path (kernels_grid.cu)
 cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 // tensor-core grid path (kernels_grid_tc.cu), nx = 128
-cudaError_t launch_grid_tc(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-cudaError_t launch_prep_grid_tc(bool realw, const PrepParams& p, int grid, cudaStream_t s);
+// tensor-core grid kernel over a group of bc coils (1, or 4 / 8 for F^H D)
+cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
+                           cudaStream_t s);
+cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s);
 // B operand tiles of the tensor-core grid kernel from its records (kx) and xs
-cudaError_t launch_build_ex_tiles(int trig, const float* rec, bool realw, int64_t ntiles,
+cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
                                   const float* xs, unsigned char* s_tab, int grid, cudaStream_t s);
 // one translation unit per grid width (kernels_grid_<nx>.cu)
 cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
+#include <algorithm>
 
 #include <cuda_runtime.h>
 
@@ -344,6 +346,7 @@ constexpr int64_t kBoundBytes = 256;
 struct GridPlan {
     bool table_kernel;      // false: coordinates expanded, general kernel
     bool tensor_cores;      // nx = 128: the tcgen05 kernel
+    int bc;                 // tensor cores: coils per CTA
     int64_t ntiles;
     int64_t vblocks;
     int rows_per_cta;
@@ -354,7 +357,30 @@ struct GridPlan {
     int ctas_per_sm;
 };
 
-GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
+// A group of coils of a tensor-core grid call: coils b0 .. b0 + nb - 1 run in
+// one launch whose CTAs hold bc coils each (bc >= nb; the rest carry weight 0).
+struct TcGroup {
+    int64_t b0;
+    int nb;
+    int bc;
+};
+
+// Groups of 8 coils; a remainder of 2..4 runs as one padded group of 4, 5..7
+// as a padded group of 8 (the MMA work of a launch does not depend on how
+// many of its coils are real), a single coil alone.
+std::vector<TcGroup> tc_groups(int64_t B)
+{
+    std::vector<TcGroup> g;
+    int64_t b0 = 0;
+    for (; B - b0 >= 8; b0 += 8) g.push_back({b0, 8, 8});
+    const int r = int(B - b0);
+    if (r == 1) g.push_back({b0, 1, 1});
+    else if (r >= 2 && r <= 4) g.push_back({b0, r, 4});
+    else if (r >= 5) g.push_back({b0, r, 8});
+    return g;
+}
+
+GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int bc = 1, int nb = 1)
 {
     GridPlan g{};
     g.table_kernel = mri::grid_kernel_fits(nx);
@@ -362,18 +388,20 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
     const int64_t N = int64_t(nx) * ny * nz;
     g.tensor_cores = mri::grid_tc_fits(nx);
     if (g.tensor_cores) {
-        g.rows_per_cta = mri::kTcRows;
+        g.bc = bc;
+        g.rows_per_cta = mri::kTcRows / bc;
         g.ntiles = ceil_div(M, mri::kTcTile);
         g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
         g.ctas_per_sm = 1;
         g.splits = (g.ntiles > 0 && g.vblocks > 0)
-                       ? choose_splits(g.ntiles, g.vblocks, sms > 0 ? sms : 1, 1, N, 1.0, 3.0)
+                       ? choose_splits(g.ntiles, g.vblocks, sms > 0 ? sms : 1, nb, N, 1.0, 3.0)
                        : 1;
-        g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 5) * mri::kTcTile * 4;
-        g.part_bytes = g.splits > 1 ? int64_t(g.splits) * 2 * N * 4 : 0;
+        g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
+        g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
         g.s_bytes = g.ntiles * int64_t(mri::kTcStageBytes);
         return g;
     }
+    g.bc = 1;
     g.rows_per_cta = mri::kGridVoxelsPerCta / nx;
     g.ntiles = ceil_div(M, mri::kGridTile);
     g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
@@ -388,65 +416,25 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms)
     return g;
 }
 
-mri_status run_grid_call(bool realw, const float* kx, const float* ky, const float* kz,
-                         const float* xs, int nx, const float* ys, int ny, const float* zs,
-                         int nz, const float* rPhi, const float* iPhi, const float* rD,
-                         const float* iD, int64_t M, float* out_r, float* out_i, int trig,
-                         int accumulate, DeviceState* d, cudaStream_t s)
+// One gather launch of the grid kernels (timing events around it).
+mri_status launch_grid_gather(const GridPlan& g, bool realw, int trig,
+                              const mri::GridParams& gp, DeviceState* d, cudaStream_t s)
 {
-    const int64_t N = int64_t(nx) * ny * nz;
-    if (M == 0) {
-        if (!accumulate) {
-            if (mri::launch_zero(out_r, N, grid_for(N, d->sms), s) != cudaSuccess ||
-                mri::launch_zero(out_i, N, grid_for(N, d->sms), s) != cudaSuccess)
-                return cuda_fail();
-        }
-        return MRI_OK;
-    }
-    const GridPlan g = plan_grid(realw, M, nx, ny, nz, d->sms);
-    if (!g.table_kernel) {
-        // expand the coordinates and take the general kernel
-        float* xyz = nullptr;
-        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
-                                    s) != cudaSuccess)
-            return cuda_fail();
-        mri_status st = MRI_OK;
-        if (mri::launch_expand_grid(xs, ys, zs, nx, ny, N, xyz, xyz + N, xyz + 2 * N,
-                                    grid_for(N, d->sms), s) != cudaSuccess)
-            st = cuda_fail();
-        if (st == MRI_OK)
-            st = run_gather_call(realw, 1, kx, ky, kz, xyz, xyz + N, xyz + 2 * N, rPhi, iPhi, rD,
-                                 iD, M, N, out_r, out_i, trig, accumulate, d, s);
-        if (cudaFreeAsync(xyz, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
-        return st;
-    }
-    char* scratch = nullptr;
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes) +
-                                       g.s_bytes),
-                                d->pool, s) != cudaSuccess)
-        return cuda_fail();
-    float* rec = reinterpret_cast<float*>(scratch);
-    unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(g.rec_bytes));
-    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes) + kBoundBytes);
-    unsigned char* s_tab = reinterpret_cast<unsigned char*>(
-        scratch + align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes));
     mri_status st = MRI_OK;
-    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
-    if (g.tensor_cores) {
-        pp.wbound = wbound;
-        if (cudaMemsetAsync(wbound, 0, sizeof(unsigned int), s) != cudaSuccess) st = cuda_fail();
-    }
-    const int tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
+    cudaEvent_t* ev = timing_slot(d);
+    if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
+    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
     if (st == MRI_OK &&
-        (g.tensor_cores ? mri::launch_prep_grid_tc(realw, pp, grid_for(g.ntiles * tile, d->sms), s)
-                        : mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * tile, d->sms), s)) !=
-            cudaSuccess)
+        (g.tensor_cores ? mri::launch_grid_tc(realw, trig, g.bc, gp, grid, s)
+                        : mri::launch_grid(realw, trig, gp, grid, s)) != cudaSuccess)
         st = cuda_fail();
-    if (st == MRI_OK && g.tensor_cores &&
-        mri::launch_build_ex_tiles(trig, rec, realw, g.ntiles, xs, s_tab,
-                                   grid_for(g.ntiles * 512, d->sms), s) != cudaSuccess)
-        st = cuda_fail();
+    if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
+    return st;
+}
+
+mri::GridParams grid_params(const GridPlan& g, const float* rec, const float* xs, int nx,
+                            const float* ys, int ny, const float* zs, int nz, DeviceState* d)
+{
     mri::GridParams gp{};
     gp.rec = rec;
     gp.ntiles = g.ntiles;
@@ -459,32 +447,135 @@ mri_status run_grid_call(bool realw, const float* kx, const float* ky, const flo
     gp.nz = nz;
     gp.rows_per_cta = g.rows_per_cta;
     gp.err = d->err;
-    gp.wbound = wbound;
-    gp.s_tab = s_tab;
-    if (g.splits == 1) {
-        gp.out_r = out_r;
-        gp.out_i = out_i;
-        gp.split_stride = 0;
-        gp.accumulate = accumulate;
-    } else {
-        gp.out_r = part;
-        gp.out_i = part + N;
-        gp.split_stride = 2 * N;
-        gp.accumulate = 0;
+    gp.coils = 1;
+    return gp;
+}
+
+// F^H D over B coils (coil-major rD / iD [B][M], outputs [B][N]) or Q (B = 1)
+// on a separable grid.
+mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky, const float* kz,
+                         const float* xs, int nx, const float* ys, int ny, const float* zs,
+                         int nz, const float* rPhi, const float* iPhi, const float* rD,
+                         const float* iD, int64_t M, float* out_r, float* out_i, int trig,
+                         int accumulate, DeviceState* d, cudaStream_t s)
+{
+    const int64_t N = int64_t(nx) * ny * nz;
+    if (M == 0) {
+        if (!accumulate) {
+            if (mri::launch_zero(out_r, B * N, grid_for(B * N, d->sms), s) != cudaSuccess ||
+                mri::launch_zero(out_i, B * N, grid_for(B * N, d->sms), s) != cudaSuccess)
+                return cuda_fail();
+        }
+        return MRI_OK;
     }
-    if (st == MRI_OK) {
-        cudaEvent_t* ev = timing_slot(d);
-        if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
-        const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
-        if (st == MRI_OK &&
-            (g.tensor_cores ? mri::launch_grid_tc(realw, trig, gp, grid, s)
-                            : mri::launch_grid(realw, trig, gp, grid, s)) != cudaSuccess)
+    const GridPlan g1 = plan_grid(realw, M, nx, ny, nz, d->sms);
+    if (!g1.table_kernel || (B > 1 && !g1.tensor_cores)) {
+        // expand the coordinates and take the general kernel
+        float* xyz = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
+                                    s) != cudaSuccess)
+            return cuda_fail();
+        mri_status st = MRI_OK;
+        if (mri::launch_expand_grid(xs, ys, zs, nx, ny, N, xyz, xyz + N, xyz + 2 * N,
+                                    grid_for(N, d->sms), s) != cudaSuccess)
             st = cuda_fail();
-        if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
+        if (st == MRI_OK)
+            st = run_gather_call(realw, B, kx, ky, kz, xyz, xyz + N, xyz + 2 * N, rPhi, iPhi, rD,
+                                 iD, M, N, out_r, out_i, trig, accumulate, d, s);
+        if (cudaFreeAsync(xyz, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+        return st;
     }
-    if (st == MRI_OK && g.splits > 1) {
-        if (mri::launch_reduce(part, g.splits, 1, N, out_r, out_i, N, accumulate,
+    if (!g1.tensor_cores) {
+        // table kernel, one weight
+        const GridPlan& g = g1;
+        char* scratch = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                    size_t(align256(g.rec_bytes) + g.part_bytes), d->pool,
+                                    s) != cudaSuccess)
+            return cuda_fail();
+        float* rec = reinterpret_cast<float*>(scratch);
+        float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
+        mri_status st = MRI_OK;
+        mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
+        if (mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * mri::kGridTile, d->sms), s) !=
+            cudaSuccess)
+            st = cuda_fail();
+        mri::GridParams gp = grid_params(g, rec, xs, nx, ys, ny, zs, nz, d);
+        gp.out_r = g.splits == 1 ? out_r : part;
+        gp.out_i = g.splits == 1 ? out_i : part + N;
+        gp.split_stride = g.splits == 1 ? 0 : 2 * N;
+        gp.accumulate = g.splits == 1 ? accumulate : 0;
+        if (st == MRI_OK) st = launch_grid_gather(g, realw, trig, gp, d, s);
+        if (st == MRI_OK && g.splits > 1 &&
+            mri::launch_reduce(part, g.splits, 1, N, out_r, out_i, N, accumulate,
                                grid_for(2 * N, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+        if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+        return st;
+    }
+
+    // tensor cores: coil groups sharing one table of B operand tiles
+    const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
+    std::vector<GridPlan> plans;
+    int64_t rec_max = 0, part_max = 0;
+    for (const TcGroup& grp : groups) {
+        plans.push_back(plan_grid(realw, M, nx, ny, nz, d->sms, grp.bc, grp.nb));
+        rec_max = std::max(rec_max, plans.back().rec_bytes);
+        part_max = std::max(part_max, plans.back().part_bytes);
+    }
+    const int64_t s_bytes = plans[0].s_bytes;
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                size_t(align256(rec_max) + kBoundBytes + align256(part_max) +
+                                       s_bytes),
+                                d->pool, s) != cudaSuccess)
+        return cuda_fail();
+    float* rec = reinterpret_cast<float*>(scratch);
+    unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(rec_max));
+    float* part = reinterpret_cast<float*>(scratch + align256(rec_max) + kBoundBytes);
+    unsigned char* s_tab = reinterpret_cast<unsigned char*>(scratch + align256(rec_max) +
+                                                            kBoundBytes + align256(part_max));
+    mri_status st = MRI_OK;
+    for (size_t i = 0; i < groups.size() && st == MRI_OK; ++i) {
+        const TcGroup& grp = groups[i];
+        const GridPlan& g = plans[i];
+        const int fields = realw ? 4 : 3 + 2 * grp.bc;
+        mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, grp.b0, g.ntiles, kscale_for(trig),
+                           rec};
+        pp.wbound = wbound;
+        pp.coils_valid = grp.nb;
+        if (cudaMemsetAsync(wbound, 0, sizeof(unsigned int), s) != cudaSuccess ||
+            mri::launch_prep_grid_tc(realw, grp.bc, pp,
+                                     grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+        // the B tiles depend on kx and the columns only: built once
+        if (st == MRI_OK && i == 0 &&
+            mri::launch_build_ex_tiles(trig, rec, fields, g.ntiles, xs, s_tab,
+                                       grid_for(g.ntiles * 512, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+        mri::GridParams gp = grid_params(g, rec, xs, nx, ys, ny, zs, nz, d);
+        gp.wbound = wbound;
+        gp.s_tab = s_tab;
+        gp.coils = grp.nb;
+        if (g.splits == 1) {
+            gp.out_r = out_r + grp.b0 * N;
+            gp.out_i = out_i + grp.b0 * N;
+            gp.coil_stride = N;
+            gp.split_stride = 0;
+            gp.accumulate = accumulate;
+        } else {
+            // partials [split][coil][r / i][N], the reduction's layout
+            gp.out_r = part;
+            gp.out_i = part + N;
+            gp.coil_stride = 2 * N;
+            gp.split_stride = int64_t(grp.nb) * 2 * N;
+            gp.accumulate = 0;
+        }
+        if (st == MRI_OK) st = launch_grid_gather(g, realw, trig, gp, d, s);
+        if (st == MRI_OK && g.splits > 1 &&
+            mri::launch_reduce(part, g.splits, grp.nb, N, out_r + grp.b0 * N, out_i + grp.b0 * N,
+                               N, accumulate, grid_for(int64_t(grp.nb) * 2 * N, d->sms),
+                               s) != cudaSuccess)
             st = cuda_fail();
     }
     if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
@@ -628,8 +719,27 @@ mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz, const
     DeviceState* d = nullptr;
     if ((st = prepare(int(trig), accumulate, 1, M, N, sp, 7, vp, 5, &d)) != MRI_OK || N == 0)
         return st;
-    return run_grid_call(false, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, rD, iD, M, rFhD,
-                         iFhD, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+    return run_grid_call(false, 1, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, rD, iD, M,
+                         rFhD, iFhD, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_fhd_batched_grid(const float* kx, const float* ky, const float* kz,
+                                const float* xs, int nx, const float* ys, int ny, const float* zs,
+                                int nz, const float* rPhi, const float* iPhi, const float* rD,
+                                const float* iD, int64_t B, int64_t M, float* rFhD, float* iFhD,
+                                mri_trig trig, int accumulate, void* stream)
+{
+    mri_status st = check_mode(int(trig), accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_grid_dims(nx, ny, nz, M)) != MRI_OK) return st;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* sp[7] = {kx, ky, kz, rPhi, iPhi, rD, iD};
+    const void* vp[5] = {xs, ys, zs, rFhD, iFhD};
+    DeviceState* d = nullptr;
+    if ((st = prepare(int(trig), accumulate, B, M, N, sp, 7, vp, 5, &d)) != MRI_OK || N == 0)
+        return st;
+    return run_grid_call(false, B, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, rD, iD, M,
+                         rFhD, iFhD, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
 }
 
 mri_status mri_q_grid(const float* kx, const float* ky, const float* kz, const float* xs, int nx,
@@ -646,18 +756,21 @@ mri_status mri_q_grid(const float* kx, const float* ky, const float* kz, const f
     DeviceState* d = nullptr;
     if ((st = prepare(int(trig), accumulate, 1, M, N, sp, 5, vp, 5, &d)) != MRI_OK || N == 0)
         return st;
-    return run_grid_call(true, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, nullptr, nullptr,
-                         M, rQ, iQ, int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+    return run_grid_call(true, 1, kx, ky, kz, xs, nx, ys, ny, zs, nz, rPhi, iPhi, nullptr,
+                         nullptr, M, rQ, iQ, int(trig), accumulate, d,
+                         static_cast<cudaStream_t>(stream));
 }
 
-mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
-                         mri_plan* plan)
+namespace {
+mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz, int num_sms,
+                          mri_plan* plan)
 {
     if (plan == nullptr) return MRI_ERR_NULL;
-    if (kind != MRI_KIND_FHD && kind != MRI_KIND_Q) return MRI_ERR_MODE;
+    if (kind != MRI_KIND_FHD && kind != MRI_KIND_Q && kind != MRI_KIND_FHD_BATCHED)
+        return MRI_ERR_MODE;
     mri_status st = check_grid_dims(nx, ny, nz, M);
     if (st != MRI_OK) return st;
-    if (num_sms < 0) return MRI_ERR_SIZE;
+    if (num_sms < 0 || B < 1 || B > kMaxB) return MRI_ERR_SIZE;
     if (num_sms == 0) {
         DeviceState* d = nullptr;
         if ((st = device_state(&d, nullptr)) != MRI_OK && st != MRI_ERR_UNSUPPORTED_DEVICE)
@@ -673,26 +786,59 @@ mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sm
         return MRI_OK;
     }
     const GridPlan g = plan_grid(realw, M, nx, ny, nz, num_sms);
-    if (!g.table_kernel) {
+    if (!g.table_kernel || (B > 1 && !g.tensor_cores)) {
         // expanded coordinates, then the general plan
-        st = mri_plan_gather(kind, 1, M, N, num_sms, plan);
+        st = mri_plan_gather(B > 1 ? MRI_KIND_FHD_BATCHED : kind, B, M, N, num_sms, plan);
         plan->launches += 1;
         plan->scratch_bytes += 3 * N * 4;
         return st;
     }
     plan->threads_per_cta = g.tensor_cores ? mri::kTcThreads : mri::kGridThreads;
-    plan->voxels_per_thread = g.tensor_cores ? mri::kTcRows * mri::kTcCols / mri::kTcThreads
-                                             : mri::kGridV;
     plan->samples_per_tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
-    plan->splits = g.splits;
-    plan->voxel_ctas = g.vblocks;
     plan->tiles = g.ntiles;
-    plan->coil_groups = 1;
-    plan->launches = 2 + (g.splits > 1 ? 1 : 0);
-    plan->scratch_bytes = align256(g.rec_bytes) + kBoundBytes + align256(g.part_bytes) + g.s_bytes;
-    plan->launches += g.tensor_cores ? 1 : 0;
     plan->tensor_cores = g.tensor_cores ? 1 : 0;
+    if (!g.tensor_cores) {
+        plan->voxels_per_thread = mri::kGridV;
+        plan->splits = g.splits;
+        plan->voxel_ctas = g.vblocks;
+        plan->coil_groups = 1;
+        plan->launches = 2 + (g.splits > 1 ? 1 : 0);
+        plan->scratch_bytes = align256(g.rec_bytes) + g.part_bytes;
+        return MRI_OK;
+    }
+    // tensor cores: per coil group a prep, a gather and (split) a reduction,
+    // plus one build of the B tiles; the first group's shape is reported
+    const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
+    int64_t rec_max = 0, part_max = 0;
+    plan->launches = 1;
+    for (size_t i = 0; i < groups.size(); ++i) {
+        const GridPlan gi = plan_grid(realw, M, nx, ny, nz, num_sms, groups[i].bc, groups[i].nb);
+        if (i == 0) {
+            plan->voxels_per_thread = mri::kTcRows * mri::kTcCols / mri::kTcThreads;
+            plan->splits = gi.splits;
+            plan->voxel_ctas = gi.vblocks;
+        }
+        rec_max = std::max(rec_max, gi.rec_bytes);
+        part_max = std::max(part_max, gi.part_bytes);
+        plan->launches += 2 + (gi.splits > 1 ? 1 : 0);
+    }
+    plan->coil_groups = int(groups.size());
+    plan->scratch_bytes = align256(rec_max) + kBoundBytes + align256(part_max) + g.s_bytes;
     return MRI_OK;
+}
+}  // namespace
+
+mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
+                         mri_plan* plan)
+{
+    if (kind == MRI_KIND_FHD_BATCHED) return MRI_ERR_MODE;
+    return plan_grid_call(kind, 1, M, nx, ny, nz, num_sms, plan);
+}
+
+mri_status mri_plan_grid_batched(int64_t B, int64_t M, int nx, int ny, int nz, int num_sms,
+                                 mri_plan* plan)
+{
+    return plan_grid_call(MRI_KIND_FHD_BATCHED, B, M, nx, ny, nz, num_sms, plan);
 }
 
 const char* mri_status_string(mri_status status)

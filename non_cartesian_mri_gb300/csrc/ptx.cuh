@@ -78,34 +78,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
-// As mbar_wait_bounded, but each try_wait asks the hardware to suspend the
-// warp for up to `hint_ns` while the phase is incomplete, so a waiting warp
-// does not re-poll shared memory (whose bandwidth the tensor core's operand
-// reads need) in a tight loop.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                    uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity)
-{
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // 1-D bulk copy global -> shared through the TMA engine; completion is
 // signalled as transaction bytes on `bar`.  dst, src and bytes must be
 // multiples of 16.

@@ -161,3 +161,36 @@ def test_plan_coil_groups(lib):
     assert plan(lib, 2, 17, 1000, 5000).coil_groups == 3      # 8 + 8 + 1
     p = plan(lib, 0, 1, 0, 100)
     assert p.launches == 2                                   # zero fill only
+
+
+def test_batched_grid_plan_groups(lib):
+    """Coil groups of the tensor-core grid path (host-only planning)."""
+    f = lib.mri_plan_grid_batched
+    f.argtypes = [I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.POINTER(Plan)]
+    f.restype = ctypes.c_int
+    for B, groups in [(1, 1), (2, 1), (4, 1), (5, 1), (8, 1), (9, 2), (13, 2), (16, 2), (17, 3)]:
+        p = Plan()
+        assert f(B, 524288, 128, 128, 128, 152, ctypes.byref(p)) == OK
+        assert p.tensor_cores == 1 and p.coil_groups == groups, B
+        assert p.samples_per_tile * p.tiles >= 524288
+    p = Plan()
+    assert f(0, 1000, 128, 4, 4, 152, ctypes.byref(p)) == SIZE
+    assert f(3, 1000, 64, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 0
+    assert lib.mri_plan_grid(2, 1000, 128, 4, 4, 152, ctypes.byref(p)) == MODE
+
+
+def test_batched_grid_argument_checks(lib):
+    f = lib.mri_fhd_batched_grid
+    f.argtypes = ([P] * 3 + [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int] + [P] * 4
+                  + [I64, I64, P, P, ctypes.c_int, ctypes.c_int, P])
+    f.restype = ctypes.c_int
+    g = fake()
+    args = lambda B=2, M=10, nx=128, trig=0, acc=0: (g[0], g[1], g[2], g[3], nx, g[4], 4, g[5], 4,
+                                                     g[6], g[7], g[8], g[9], B, M, g[10], g[11],
+                                                     trig, acc, None)
+    assert f(*args(trig=5)) == MODE
+    assert f(*args(acc=3)) == MODE
+    assert f(*args(B=0)) == SIZE
+    assert f(*args(M=-1)) == SIZE
+    assert f(*args(nx=-2)) == SIZE
