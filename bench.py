@@ -214,6 +214,9 @@ def to_dev(w: wl.Workload, torch):
 
 
 def call(mri, kind, t, trig, out=None, grid=False):
+    if grid and kind == "fhd_batched":
+        return mri.fhd_batched_grid(t["kx"], t["ky"], t["kz"], t["xs"], t["ys"], t["zs"],
+                                    t["rPhi"], t["iPhi"], t["rD"], t["iD"], trig=trig, out=out)
     if grid and kind == "fhd":
         return mri.fhd_grid(t["kx"], t["ky"], t["kz"], t["xs"], t["ys"], t["zs"], t["rPhi"],
                             t["iPhi"], t["rD"], t["iD"], trig=trig, out=out)
@@ -228,6 +231,20 @@ def call(mri, kind, t, trig, out=None, grid=False):
                      trig=trig, out=out)
     return mri.fhd_batched(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"], t["rPhi"],
                            t["iPhi"], t["rD"], t["iD"], trig=trig, out=out)
+
+
+ENTRY = {("fhd", True): "mri_fhd_grid", ("q", True): "mri_q_grid",
+         ("fhd_batched", True): "mri_fhd_batched_grid",
+         ("fhd", False): "mri_fhd", ("q", False): "mri_q",
+         ("fhd_batched", False): "mri_fhd_batched"}
+
+
+def grid_or_general_plan(mri, w, grid):
+    if grid and w.kind == "fhd_batched":
+        return mri.plan_grid_batched(w.B, w.M, w.L, w.L, w.L)
+    if grid:
+        return mri.plan_grid(w.kind, w.M, w.L, w.L, w.L)
+    return mri.plan(w.kind, w.M, w.N, B=w.B)
 
 
 def timed_steps(torch, mri, dist, fn, steps, warmup, flush):
@@ -308,10 +325,10 @@ def profiled_traffic(kind, trig):
     return entry.get("dram_bytes_per_launch")
 
 
-def roofline_tensor(w, res, peaks, trig):
+def roofline_tensor(w, res, peaks, trig, units):
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
     launches_per_step = res["gather_launches"] / len(res["step_ms"])
-    pairs_s = w.pairs / launches_per_step / per_launch
+    pairs_s = units / launches_per_step / per_launch
     achieved = pairs_s * TC_FLOPS_PER_PAIR / 1e12
     bf16 = float(peaks.get("bf16_tflops", 1900.0))
     peak = bf16 * F16_PER_BF16 / TC_PASSES
@@ -323,14 +340,16 @@ def roofline_tensor(w, res, peaks, trig):
                            f" = dense f16 rate, / {TC_PASSES:g} f16 products per fp32 product;"
                            f" algorithmic {TC_FLOPS_PER_PAIR:g} flops per voxel-sample pair"),
             "executed_tflops": round(achieved * TC_PASSES, 2),
-            "pairs_per_s": round(pairs_s / 1e9, 2), "unit_pairs": "Gpairs/s",
+            "pairs_per_s": round(pairs_s / 1e9, 2),
+            "unit_pairs": "Gpair-coils/s" if w.B > 1 else "Gpairs/s",
             "gather_ms_per_launch": round(per_launch * 1e3, 3)}
 
 
 def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, plan=None,
              peaks=None):
     if grid and plan and plan.get("tensor_cores"):
-        return roofline_tensor(w, res, peaks or {}, trig)
+        return roofline_tensor(w, res, peaks or {}, trig,
+                               w.pairs * (w.B if kind == "fhd_batched" else 1))
     units = w.pairs * (w.B if kind == "fhd_batched" else 1)
     akind = "grid" if grid else kind
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
@@ -439,9 +458,8 @@ def run_ours(args):
     t = to_dev(w, torch)
     out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
            torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"))
-    grid = (not args.general) and kind in ("fhd", "q")
-    plan = (mri.plan_grid(kind, w.M, w.L, w.L, w.L) if grid
-            else mri.plan(kind, w.M, w.N, B=w.B))
+    grid = not args.general
+    plan = grid_or_general_plan(mri, w, grid)
     with ClockSampler(local) as clk:
         res = timed_steps(torch, mri, dist, lambda: call(mri, kind, t, args.trig, out, grid),
                           args.steps, args.warmup, flush)
@@ -456,8 +474,7 @@ def run_ours(args):
         "data": "synthetic (seeded generators, no dataset)",
         "config": {"workload": f"{w.name}: {wl.WORKLOADS[w.name]}", "voxels": w.N,
                    "samples": w.M, "coils": w.B, "trig": args.trig,
-                   "entry": ("mri_fhd_grid" if kind == "fhd" else "mri_q_grid") if grid
-                   else {"fhd": "mri_fhd", "q": "mri_q", "fhd_batched": "mri_fhd_batched"}[kind],
+                   "entry": ENTRY[(kind, grid)],
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
                    "parallelism": "one independent voxel slab per rank" if world > 1
                    else "single GPU",
@@ -484,6 +501,8 @@ def run_ours(args):
                 ("q_grid_fast", "q_128", "fast", True),
                 ("q_grid_accurate", "q_128", "accurate", True),
                 ("q_general_fast", "q_128", "fast", False),
+                ("fhd_batched_grid_fast", "fhd_batched_128", "fast", True),
+                ("fhd_batched_grid_accurate", "fhd_batched_128", "accurate", True),
                 ("fhd_batched_fast", "fhd_batched_128", "fast", False),
                 ("fhd_batched_accurate", "fhd_batched_128", "accurate", False)):
             if name.startswith("fhd_") and (name.startswith("fhd_grid") == grid) and \
@@ -497,13 +516,10 @@ def run_ours(args):
                                args.steps, args.warmup, flush)
             pm = statistics.mean(pres["step_ms"]) / 1e3
             punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
-            pplan = (mri.plan_grid(pw.kind, pw.M, pw.L, pw.L, pw.L) if pgrid
-                     else mri.plan(pw.kind, pw.M, pw.N, B=pw.B))
+            pplan = grid_or_general_plan(mri, pw, pgrid)
             paths[name] = {
                 "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}", "trig": trig,
-                "entry": {("fhd", True): "mri_fhd_grid", ("q", True): "mri_q_grid",
-                          ("fhd", False): "mri_fhd", ("q", False): "mri_q",
-                          ("fhd_batched", False): "mri_fhd_batched"}[(pw.kind, pgrid)],
+                "entry": ENTRY[(pw.kind, pgrid)],
                 "value": round(punits / pm / 1e9, 2),
                 "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
                 "ms_per_step": round(pm * 1e3, 3),

@@ -36,6 +36,19 @@ extern "C" {
 mri_status mri_microbench(int which, int ctas_per_sm, int threads, int64_t iters,
                           unsigned long long* cycles, float* sink, void* stream);
 
+/*
+ * Failure-detection self-test (no counterpart on the pages).  Every wait in
+ * the gather kernels (an mbarrier for a TMA copy or for the tensor core) is
+ * bounded: after 1 s it gives up, sets a bit in the device error word that
+ * mri_device_errors() returns, lets its own copies land and exits, so a copy
+ * that never completes costs an error code, not a hung GPU.  This launches
+ * one CTA that waits with the same helper on an mbarrier nothing arrives on
+ * (arrive = 0: expect bit 0x1 after about a second) or on one it arrived on
+ * first (arrive = 1: no bit).  Asynchronous on `stream`; MRI_ERR_MODE for
+ * arrive not 0/1, MRI_ERR_UNSUPPORTED_DEVICE off sm_103.
+ */
+mri_status mri_wait_selftest(int arrive, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,6 +76,8 @@ def load():
         lib.mri_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
         lib.mri_device_errors.restype = ctypes.c_int
         lib.mri_microbench.argtypes = [I, I, I, I64, P, P, P]
+        lib.mri_wait_selftest.argtypes = [I, P]
+        lib.mri_wait_selftest.restype = ctypes.c_int
         lib.mri_microbench.restype = ctypes.c_int
         lib.mri_fhd_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 4
                                      + [I64, P, P, I, I, P])
@@ -320,6 +322,12 @@ def plan(kind: str, M: int, N: int, B: int = 1, num_sms: int = 0) -> dict:
     _check(load().mri_plan_gather(KIND[kind], B, M, N, num_sms, ctypes.byref(p)),
            "mri_plan_gather")
     return {name: getattr(p, name) for name, _ in _Plan._fields_}
+
+
+def wait_selftest(arrive: bool, stream=None) -> None:
+    """Launch the bounded-wait self-test (see include/mri_microbench.h)."""
+    _check(load().mri_wait_selftest(int(bool(arrive)), _stream_handle(stream)),
+           "mri_wait_selftest")
 
 
 def device_errors(clear: bool = True) -> int:

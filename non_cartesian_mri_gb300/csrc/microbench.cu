@@ -5,6 +5,11 @@
 
 #include "mri.h"
 #include "mri_microbench.h"
+#include "ptx.cuh"
+
+namespace mri {
+unsigned int* error_word_address(int dev);   // mri_abi.cu; symbol lookup only
+}
 
 namespace {
 
@@ -47,7 +52,42 @@ cudaError_t launch_probe(dim3 grid, int threads, int smem, cudaStream_t s, int64
     return cudaGetLastError();
 }
 
+// One CTA waits, bounded, on an mbarrier of arrival count 1 with the wait
+// helper every kernel uses.  arrive = 0: nothing ever arrives, the wait must
+// give up after its time limit and report through the device error word;
+// arrive = 1: thread 0 arrives first and the wait completes at once.
+__global__ void wait_selftest_kernel(int arrive, unsigned int* err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mri::mbar_init(&bar, 1);
+        mri::fence_barrier_init();
+    }
+    __syncthreads();
+    if (arrive && threadIdx.x == 0) mri::mbar_arrive(&bar);
+    const bool ok = mri::mbar_wait_bounded(&bar, 0u);
+    if (!ok && threadIdx.x == 0) atomicOr(err, mri::DEVERR_TILE_WAIT_TIMEOUT);
+}
+
 }  // namespace
+
+extern "C" mri_status mri_wait_selftest(int arrive, void* stream)
+{
+    if (arrive != 0 && arrive != 1) return MRI_ERR_MODE;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRI_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return MRI_ERR_UNSUPPORTED_DEVICE;
+    unsigned int* err = mri::error_word_address(dev);
+    if (err == nullptr) return MRI_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(arrive, err);
+    if (cudaGetLastError() != cudaSuccess) return MRI_ERR_CUDA;
+    return MRI_OK;
+}
 
 extern "C" mri_status mri_microbench(int which, int ctas_per_sm, int threads, int64_t iters,
                                      unsigned long long* cycles, float* sink, void* stream)
