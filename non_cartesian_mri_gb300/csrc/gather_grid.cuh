@@ -60,6 +60,10 @@ struct GridParams {
     // (out_r + b * coil_stride ..)
     int coils;
     int64_t coil_stride;
+    // tensor-core kernel with the Ey table: per record tile and block of 128
+    // y values, e^{i phase(ky y)} as [sample][128] float2; ny / 128 blocks
+    const float2* ey_tab;
+    int ey_blocks;
 };
 
 // The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks

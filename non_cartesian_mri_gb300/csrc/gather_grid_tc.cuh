@@ -76,6 +76,15 @@ constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // 128 S rows x 32 f16 (8 K
 constexpr int kTcSBytes = 3 * kTcPartBytes;          // S = [-B_i; B_r; B_i]: 384 x 32 (24 KB)
 constexpr int kTcStageBytes = 2 * kTcSBytes;         // S hi, S lo (48 KB)
 constexpr int kTcStages = MRI_TC_STAGES;             // operand stages in the ring
+constexpr int kTcSLead = MRI_TC_S_LEAD;
+// The Ey table replaces the per-(row, sample) sin/cos of the accurate path
+// (and of the fast paths when MRI_TC_EY_FAST is 1).
+#ifndef MRI_TC_EY_FAST
+#define MRI_TC_EY_FAST 0
+#endif
+// With the Ey table two 32 KB Ey stages take shared memory from the B ring.
+constexpr int kTcStagesEy = 3;
+constexpr int kTcEyBytes = kTcTile * kTcRows * 8;   // 32 samples x 128 rows of float2
 constexpr int kTcColsPerWarp = 256 * 4 / kTcWarps;  // D columns one warp folds (128 or 64)
 constexpr uint32_t kTcDCols = 256;                   // D_r | D_i
 constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per lane (16 columns)
@@ -98,11 +107,12 @@ inline bool grid_tc_fits(int nx) { return nx == kTcCols; }
 // grid rows, m = b * (128 / bc) + r.
 inline bool grid_tc_coils_ok(int bc) { return bc == 1 || bc == 4 || bc == 8; }
 
-inline size_t grid_tc_smem_bytes(bool realw, int bc = 1)
+inline size_t grid_tc_smem_bytes(bool realw, int bc = 1, bool eyt = false)
 {
     const int F = realw ? 4 : 3 + 2 * bc;
     const int rc = kTcRows / bc;
-    size_t b = size_t(kTcStages) * kTcStageBytes;          // B operand stages
+    size_t b = size_t(eyt ? kTcStagesEy : kTcStages) * kTcStageBytes;   // B operand stages
+    if (eyt) b += size_t(2) * kTcEyBytes + size_t(2) * kTcTile * 8;   // Ey tiles, z factors
     b += size_t(kStages) * F * kTcTile * 4;                // record ring
     b += size_t(rc) * 8;                                   // (y, z) of the rows
     if (bc > 1) b += size_t(2) * kTcTile * rc * 8;         // row factors, two tiles
@@ -251,6 +261,29 @@ __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, i
     }
 }
 
+// The Ey table: for record tile t and block yb of 128 y values,
+// e^{i phase(ky[s] ys[128 yb + r])} at [(t * nyb + yb) * 32 + s] * 128 + r
+// (float2: cos, sin).  Consecutive threads take consecutive r.
+template <int TRIG>
+__global__ void __launch_bounds__(256) build_ey_tiles_kernel(const float* rec, int fields,
+                                                             int64_t ntiles, const float* ys,
+                                                             int nyb, float2* ey_tab)
+{
+    const int64_t per_tile = int64_t(nyb) * kTcTile * kTcRows;
+    const int64_t total = ntiles * per_tile;
+    for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
+         item += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = item / per_tile;
+        const int rem = int(item - t * per_tile);
+        const int yb = rem / (kTcTile * kTcRows);
+        const int s = (rem / kTcRows) % kTcTile;
+        const int r = rem % kTcRows;
+        float sn, cs;
+        table_sincos<TRIG>(rec[t * fields * kTcTile + kTcTile + s] * ys[yb * kTcRows + r], sn, cs);
+        ey_tab[item] = make_float2(cs, sn);
+    }
+}
+
 // this thread's 8 samples s0 .. s0 + 7 of record field f (contiguous in the tile)
 __device__ __forceinline__ void tc_load8(const float* rec, int f, int s0, float (&v)[8])
 {
@@ -260,9 +293,13 @@ __device__ __forceinline__ void tc_load8(const float* rec, int f, int s0, float 
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <int BC, bool REALW, int TRIG>
+template <int BC, bool REALW, int TRIG, bool EYT>
 __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParams p)
 {
+    // EYT: the y factor of Mz comes from the Ey table (one z-plane per CTA)
+    static_assert(!EYT || BC == 1, "Ey table for single-weight calls");
+    constexpr int kS = EYT ? kTcStagesEy : kTcStages;   // B / A stages
+    constexpr int kLead = EYT ? 1 : kTcSLead;
     static_assert(BC == 1 || (!REALW && (BC == 4 || BC == 8)), "coil group");
     constexpr int T = kTcTile;
     constexpr int F = REALW ? 4 : 3 + 2 * BC;
@@ -273,12 +310,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const ops = smem_raw;
-    float* const ring = reinterpret_cast<float*>(ops + kTcStages * kTcStageBytes);
+    float2* const ey_sh = reinterpret_cast<float2*>(ops + kS * kTcStageBytes);   // EYT: 2 Ey tiles
+    float* const ring = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ey_sh) +
+                                                 (EYT ? 2 * kTcEyBytes : 0));
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
-    float2* const e_sh = yz_sh + RC;                  // BC > 1: row factors of two tiles
+    // BC > 1: row factors of two tiles; EYT: Mu e^{i phase(kz z)} of two tiles
+    float2* const e_sh = yz_sh + RC;
     __shared__ __align__(8) uint64_t full_bar[kStages];     // record tile landed
-    __shared__ __align__(8) uint64_t s_bar[kTcStages];      // B operand tile landed
-    __shared__ __align__(8) uint64_t mma_bar[kTcStages];    // MMAs of the stage done
+    __shared__ __align__(8) uint64_t ey_bar[2];             // EYT: Ey tile landed
+    __shared__ __align__(8) uint64_t s_bar[kS];      // B operand tile landed
+    __shared__ __align__(8) uint64_t mma_bar[kS];    // MMAs of the stage done
     __shared__ uint32_t tmem_base_sh;
 
     const int tid = threadIdx.x;
@@ -307,8 +348,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     if (tid == 0) {
 #pragma unroll
         for (int st = 0; st < kStages; ++st) mbar_init(&full_bar[st], 1);
+        mbar_init(&ey_bar[0], 1);
+        mbar_init(&ey_bar[1], 1);
 #pragma unroll
-        for (int st = 0; st < kTcStages; ++st) {
+        for (int st = 0; st < kS; ++st) {
             mbar_init(&s_bar[st], 1);
             mbar_init(&mma_bar[st], 1);
         }
@@ -318,13 +361,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
-    // B tile u into stage u % kTcStages (thread 0 only)
+    // B tile u into stage u % kS (thread 0 only)
     auto load_s = [&](int u) {
-        uint64_t* bar = &s_bar[u % kTcStages];
+        uint64_t* bar = &s_bar[u % kS];
         mbar_arrive_expect_tx(bar, uint32_t(kTcStageBytes));
-        tma_bulk_g2s(ops + (u % kTcStages) * kTcStageBytes, p.s_tab + (t_begin + u) * kTcStageBytes,
+        tma_bulk_g2s(ops + (u % kS) * kTcStageBytes, p.s_tab + (t_begin + u) * kTcStageBytes,
                      uint32_t(kTcStageBytes), bar);
     };
+    // EYT: this CTA's 128 rows are grid rows iy0 .. iy0 + 127 of plane iz
+    const int ey_block = EYT ? int((row0 % p.ny) / kTcRows) : 0;
+    const float z_plane = EYT ? p.zs[row0 / p.ny] : 0.0f;
+    auto load_ey = [&](int u) {
+        uint64_t* bar = &ey_bar[u & 1];
+        mbar_arrive_expect_tx(bar, uint32_t(kTcEyBytes));
+        tma_bulk_g2s(ey_sh + (u & 1) * (T * kTcRows),
+                     p.ey_tab + ((t_begin + u) * p.ey_blocks + ey_block) * (T * kTcRows),
+                     uint32_t(kTcEyBytes), bar);
+    };
+    int ey_loaded = 0;    // Ey tiles whose copy thread 0 has issued
     int s_loaded = 0;     // B tiles whose copy thread 0 has issued
     int s_consumed = 0;   // B tiles thread 0 has seen land
     if (tid == 0) {
@@ -333,8 +387,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             tma_bulk_g2s(ring + st * F * T, p.rec + (t_begin + st) * F * T, TILE_BYTES,
                          &full_bar[st]);
         }
-        for (; s_loaded < kTcStages && s_loaded < nt; ++s_loaded) load_s(s_loaded);
+        for (; s_loaded < kS && s_loaded < nt; ++s_loaded) load_s(s_loaded);
+        if constexpr (EYT)
+            for (; ey_loaded < 2 && ey_loaded < nt; ++ey_loaded) load_ey(ey_loaded);
     }
+    // EYT: e[s] = scale Mu[s] e^{i phase(kz[s] z)} of this CTA's plane, by warp 0
+    auto z_factors = [&](const float* rec, float2* e) {
+        if (warp == 0) {
+            const int s = lane;
+            float sn, cs;
+            table_sincos<TRIG>(rec[2 * T + s] * z_plane, sn, cs);
+            const float wr = rec[3 * T + s] * a_scale;
+            const float wi = REALW ? 0.0f : rec[4 * T + s] * a_scale;
+            e[s] = make_float2(fmaf(wr, cs, -wi * sn), fmaf(wi, cs, wr * sn));
+        }
+    };
 
     // A (Mz) generation: row ra = this thread's tensor-memory lane (a warp
     // reaches only its own lane quarter), samples 8 kTcAChunks ah .., which
@@ -365,25 +432,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
 
     int failed_at = -1;
     bool s_fail = false;   // thread 0: a B tile or stage wait timed out
-    if constexpr (BC > 1) {
-        // row factors of tile 0; later tiles' are made one tile ahead
+    if constexpr (BC > 1 || EYT) {
+        // row (or plane) factors of tile 0; later tiles' are made one tile ahead
         bool ok0 = true;
         if (nt > 0) {
             ok0 = mbar_wait_bounded(&full_bar[0], 0u);
-            if (ok0) tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, a_scale, tid);
+            if (ok0) {
+                if constexpr (EYT)
+                    z_factors(ring, e_sh);
+                else
+                    tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, a_scale, tid);
+            }
         }
         if (__syncthreads_or(!ok0)) failed_at = 0;
     }
     for (int t = 0; t < nt && failed_at < 0; ++t) {
-        const int st = t % kTcStages;
+        const int st = t % kS;
         const bool new_block = (t % drain_tiles) == 0;
         const uint32_t acol = tmem + kTcDCols + uint32_t(st) * kTcAStageCols;
         bool ok = true;
-        // the MMAs of tile t - kTcStages read stage st
-        if (t >= kTcStages)
-            ok = tc_wait(&mma_bar[st], uint32_t((t - kTcStages) / kTcStages) & 1u);
+        // the MMAs of tile t - kS read stage st
+        if (t >= kS)
+            ok = tc_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u);
         if (ok) ok = tc_wait(&full_bar[t % kStages], uint32_t(t / kStages) & 1u);
-        // warp-uniform: the tensor-memory stores below are .sync.aligned
+        if (EYT && ok) ok = tc_wait(&ey_bar[t & 1], uint32_t(t >> 1) & 1u);
+        // warp-uniform: the tensor-memory store below is .sync.aligned
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             const float* rec = ring + (t % kStages) * F * T;
@@ -391,7 +464,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             for (int c = 0; c < kTcAChunks; ++c) {
                 const int s0 = 8 * (kTcAChunks * ah + c);
                 float ar[8], ai[8];
-                if constexpr (BC == 1) {
+                if constexpr (EYT) {
+                    // Mz = (scale Mu e^{i phase(kz z)}) e^{i phase(ky y)}
+                    const float2* ez = e_sh + (t & 1) * T;
+                    const float2* ey = ey_sh + (t & 1) * (T * kTcRows);
+#pragma unroll
+                    for (int s8 = 0; s8 < 8; ++s8) {
+                        const float2 f = ez[s0 + s8];
+                        const float2 e = ey[(s0 + s8) * kTcRows + ra];
+                        ar[s8] = fmaf(f.x, e.x, -f.y * e.y);
+                        ai[s8] = fmaf(f.x, e.y, f.y * e.x);
+                    }
+                } else if constexpr (BC == 1) {
                     float ky[8], kz[8], wr[8], wi[8];
                     tc_load8(rec, 1, s0, ky);
                     tc_load8(rec, 2, s0, kz);
@@ -435,15 +519,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 tmem_st4(col + A_IL * kTcAPartCols, l);
             }
             tmem_wait_st();
-            if constexpr (BC > 1) {
-                // row factors of the next tile (its buffer was last read by
-                // tile t - 1, before the previous barrier)
+            if constexpr (BC > 1 || EYT) {
+                // row (or plane) factors of the next tile (its buffer was last
+                // read by tile t - 1, before the previous barrier)
                 if (t + 1 < nt) {
                     ok = mbar_wait_bounded(&full_bar[(t + 1) % kStages],
                                            uint32_t((t + 1) / kStages) & 1u);
-                    if (ok)
-                        tc_row_factors<TRIG, RC>(ring + ((t + 1) % kStages) * F * T, yz_sh,
-                                                 e_sh + ((t + 1) & 1) * T * RC, a_scale, tid);
+                    if (ok) {
+                        const float* rec1 = ring + ((t + 1) % kStages) * F * T;
+                        if constexpr (EYT)
+                            z_factors(rec1, e_sh + ((t + 1) & 1) * T);
+                        else
+                            tc_row_factors<TRIG, RC>(rec1, yz_sh, e_sh + ((t + 1) & 1) * T * RC,
+                                                     a_scale, tid);
+                    }
                 }
             }
         }
@@ -452,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         // every thread, so the barrier is uniform)
         if (new_block && t > 0) {
             if (ok)
-                ok = tc_wait(&mma_bar[(t - 1) % kTcStages], uint32_t((t - 1) / kTcStages) & 1u);
+                ok = tc_wait(&mma_bar[(t - 1) % kS], uint32_t((t - 1) / kS) & 1u);
             if (__syncthreads_or(!ok || s_fail)) {
                 failed_at = t;
                 break;
@@ -468,12 +557,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         }
         tc_fence_after_sync();
         if (tid == 0) {
+            // Ey tile t + 2 into the buffer tile t has just finished with
+            if constexpr (EYT) {
+                if (t + 2 < nt && ey_loaded == t + 2) {
+                    load_ey(t + 2);
+                    ++ey_loaded;
+                }
+            }
             if (t + kStages < nt) {
                 mbar_arrive_expect_tx(&full_bar[t % kStages], TILE_BYTES);
                 tma_bulk_g2s(ring + (t % kStages) * F * T, p.rec + (t_begin + t + kStages) * F * T,
                              TILE_BYTES, &full_bar[t % kStages]);
             }
-            bool s_ok = mbar_wait_bounded(&s_bar[st], uint32_t(t / kTcStages) & 1u);
+            bool s_ok = mbar_wait_bounded(&s_bar[st], uint32_t(t / kS) & 1u);
             if (s_ok) {
                 s_consumed = t + 1;
                 const unsigned char* stage = ops + st * kTcStageBytes;
@@ -500,11 +596,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 }
                 umma_commit(&mma_bar[st]);
                 // refill a stage for tile t + lead as soon as the MMAs that
-                // read it (tile t + lead - kTcStages) are done
-                const int u = t + MRI_TC_S_LEAD;
-                if (u >= kTcStages && u < nt && s_loaded == u) {
-                    s_ok = mbar_wait_bounded(&mma_bar[u % kTcStages],
-                                             uint32_t((u - kTcStages) / kTcStages) & 1u);
+                // read it (tile t + lead - kS) are done
+                const int u = t + kLead;
+                if (u >= kS && u < nt && s_loaded == u) {
+                    s_ok = mbar_wait_bounded(&mma_bar[u % kS],
+                                             uint32_t((u - kS) / kS) & 1u);
                     if (s_ok) {
                         load_s(u);
                         ++s_loaded;
@@ -519,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     bool ok = failed_at < 0;
     if (ok && nt > 0) {
         if (!s_fail)
-            ok = tc_wait(&mma_bar[(nt - 1) % kTcStages], uint32_t((nt - 1) / kTcStages) & 1u);
+            ok = tc_wait(&mma_bar[(nt - 1) % kS], uint32_t((nt - 1) / kS) & 1u);
         if (__syncthreads_or(!ok || s_fail)) {
             ok = false;
             failed_at = nt;
@@ -554,8 +650,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             // thread 0 issued the MMAs of exactly the first s_consumed tiles
             unsigned int bits = DEVERR_TILE_WAIT_TIMEOUT;
             const int issued = s_consumed;
-            if (issued > 0 && !mbar_wait_bounded(&mma_bar[(issued - 1) % kTcStages],
-                                                 uint32_t((issued - 1) / kTcStages) & 1u))
+            if (issued > 0 && !mbar_wait_bounded(&mma_bar[(issued - 1) % kS],
+                                                 uint32_t((issued - 1) / kS) & 1u))
                 bits |= DEVERR_DRAIN_TIMEOUT;
             const int first = failed_at < nt ? failed_at : nt;
             const int last = (first + kStages < nt) ? first + kStages : nt;
@@ -563,7 +659,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 if (!mbar_wait_bounded(&full_bar[u % kStages], uint32_t(u / kStages) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
             for (int u = s_consumed; u < s_loaded; ++u)
-                if (!mbar_wait_bounded(&s_bar[u % kTcStages], uint32_t(u / kTcStages) & 1u))
+                if (!mbar_wait_bounded(&s_bar[u % kS], uint32_t(u / kS) & 1u))
+                    bits |= DEVERR_DRAIN_TIMEOUT;
+            // the last Ey copy into each buffer
+            for (int u = ey_loaded > 2 ? ey_loaded - 2 : 0; u < ey_loaded; ++u)
+                if (!mbar_wait_bounded(&ey_bar[u & 1], uint32_t(u >> 1) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
             atomicOr(p.err, bits);
         }

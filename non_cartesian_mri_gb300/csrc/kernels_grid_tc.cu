@@ -5,41 +5,78 @@
 namespace mri {
 
 namespace {
-template <int BC, bool REALW, int TRIG>
+template <int BC, bool REALW, int TRIG, bool EYT>
 cudaError_t run(const GridParams& p, dim3 grid, cudaStream_t s)
 {
-    const size_t smem = grid_tc_smem_bytes(REALW, BC);
+    const size_t smem = grid_tc_smem_bytes(REALW, BC, EYT);
     const cudaError_t attr = cudaFuncSetAttribute(
-        gather_grid_tc_kernel<BC, REALW, TRIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        gather_grid_tc_kernel<BC, REALW, TRIG, EYT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         int(smem));
     if (attr != cudaSuccess) return attr;
-    gather_grid_tc_kernel<BC, REALW, TRIG><<<grid, kTcThreads, smem, s>>>(p);
+    gather_grid_tc_kernel<BC, REALW, TRIG, EYT><<<grid, kTcThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int BC, bool REALW>
+template <int BC, bool REALW, bool EYT>
 cudaError_t run_trig(int trig, const GridParams& p, dim3 grid, cudaStream_t s)
 {
     switch (trig) {
-        case TRIG_ACCURATE: return run<BC, REALW, TRIG_ACCURATE>(p, grid, s);
-        case TRIG_FAST: return run<BC, REALW, TRIG_FAST>(p, grid, s);
-        case TRIG_FAST_RR: return run<BC, REALW, TRIG_FAST_RR>(p, grid, s);
+        case TRIG_ACCURATE: return run<BC, REALW, TRIG_ACCURATE, EYT>(p, grid, s);
+        case TRIG_FAST: return run<BC, REALW, TRIG_FAST, EYT>(p, grid, s);
+        case TRIG_FAST_RR: return run<BC, REALW, TRIG_FAST_RR, EYT>(p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
 }  // namespace
 
+bool grid_tc_ey_table(int trig, int bc, int ny)
+{
+    return bc == 1 && ny % kTcRows == 0 && (trig == TRIG_ACCURATE || MRI_TC_EY_FAST);
+}
+
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s)
 {
     if (!grid_tc_fits(p.nx)) return cudaErrorInvalidValue;
-    if (realw) return bc == 1 ? run_trig<1, true>(trig, p, grid, s) : cudaErrorInvalidValue;
+    const bool eyt = grid_tc_ey_table(trig, bc, p.ny);
+    if (eyt && (p.ey_tab == nullptr || p.ey_blocks != p.ny / kTcRows)) return cudaErrorInvalidValue;
+    if (realw) {
+        if (bc != 1) return cudaErrorInvalidValue;
+        return eyt ? run_trig<1, true, true>(trig, p, grid, s)
+                   : run_trig<1, true, false>(trig, p, grid, s);
+    }
     switch (bc) {
-        case 1: return run_trig<1, false>(trig, p, grid, s);
-        case 4: return run_trig<4, false>(trig, p, grid, s);
-        case 8: return run_trig<8, false>(trig, p, grid, s);
+        case 1:
+            return eyt ? run_trig<1, false, true>(trig, p, grid, s)
+                       : run_trig<1, false, false>(trig, p, grid, s);
+        case 4: return run_trig<4, false, false>(trig, p, grid, s);
+        case 8: return run_trig<8, false, false>(trig, p, grid, s);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
+                                  const float* ys, int ny, float2* ey_tab, int grid,
+                                  cudaStream_t s)
+{
+    if (ny % kTcRows != 0) return cudaErrorInvalidValue;
+    const int nyb = ny / kTcRows;
+    switch (trig) {
+        case TRIG_ACCURATE:
+            build_ey_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
+                                                                     ey_tab);
+            break;
+        case TRIG_FAST:
+            build_ey_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
+                                                                 ey_tab);
+            break;
+        case TRIG_FAST_RR:
+            build_ey_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
+                                                                    ey_tab);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,

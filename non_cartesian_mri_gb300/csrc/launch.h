@@ -41,6 +41,12 @@ cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cu
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s);
 cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s);
+// whether a tensor-core grid launch takes its y factors from the Ey table
+bool grid_tc_ey_table(int trig, int bc, int ny);
+// the Ey table (ny % 128 == 0) from the records (ky) and ys
+cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
+                                  const float* ys, int ny, float2* ey_tab, int grid,
+                                  cudaStream_t s);
 // B operand tiles of the tensor-core grid kernel from its records (kx) and xs
 cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
                                   const float* xs, unsigned char* s_tab, int grid, cudaStream_t s);

@@ -354,6 +354,7 @@ struct GridPlan {
     int64_t rec_bytes;
     int64_t part_bytes;
     int64_t s_bytes;        // tensor cores: the B operand tiles
+    int64_t ey_bytes;       // tensor cores, one weight, ny % 128 == 0: the Ey table
     int ctas_per_sm;
 };
 
@@ -380,7 +381,8 @@ std::vector<TcGroup> tc_groups(int64_t B)
     return g;
 }
 
-GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int bc = 1, int nb = 1)
+GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int bc = 1, int nb = 1,
+                   int trig = 0)
 {
     GridPlan g{};
     g.table_kernel = mri::grid_kernel_fits(nx);
@@ -399,6 +401,9 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int b
         g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
         g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
         g.s_bytes = g.ntiles * int64_t(mri::kTcStageBytes);
+        g.ey_bytes = mri::grid_tc_ey_table(trig, bc, ny)
+                         ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
+                         : 0;
         return g;
     }
     g.bc = 1;
@@ -517,19 +522,25 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
     // tensor cores: coil groups sharing one table of B operand tiles
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
     std::vector<GridPlan> plans;
-    int64_t rec_max = 0, part_max = 0;
+    int64_t rec_max = 0, part_max = 0, ey_bytes = 0;
     for (const TcGroup& grp : groups) {
-        plans.push_back(plan_grid(realw, M, nx, ny, nz, d->sms, grp.bc, grp.nb));
+        plans.push_back(plan_grid(realw, M, nx, ny, nz, d->sms, grp.bc, grp.nb, trig));
         rec_max = std::max(rec_max, plans.back().rec_bytes);
         part_max = std::max(part_max, plans.back().part_bytes);
+        ey_bytes = std::max(ey_bytes, plans.back().ey_bytes);   // single-coil groups only
     }
     const int64_t s_bytes = plans[0].s_bytes;
+    bool ey_built = false;
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
                                 size_t(align256(rec_max) + kBoundBytes + align256(part_max) +
-                                       s_bytes),
+                                       align256(s_bytes) + ey_bytes),
                                 d->pool, s) != cudaSuccess)
         return cuda_fail();
+    float2* ey_tab = ey_bytes > 0
+                         ? reinterpret_cast<float2*>(scratch + align256(rec_max) + kBoundBytes +
+                                                     align256(part_max) + align256(s_bytes))
+                         : nullptr;
     float* rec = reinterpret_cast<float*>(scratch);
     unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(rec_max));
     float* part = reinterpret_cast<float*>(scratch + align256(rec_max) + kBoundBytes);
@@ -553,9 +564,19 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
             mri::launch_build_ex_tiles(trig, rec, fields, g.ntiles, xs, s_tab,
                                        grid_for(g.ntiles * 512, d->sms), s) != cudaSuccess)
             st = cuda_fail();
+        // the y factors depend on ky and the rows only: built once, by the
+        // first group that reads them
+        if (st == MRI_OK && g.ey_bytes > 0 && !ey_built) {
+            if (mri::launch_build_ey_tiles(trig, rec, fields, g.ntiles, ys, ny, ey_tab,
+                                           grid_for(g.ey_bytes / 8, d->sms), s) != cudaSuccess)
+                st = cuda_fail();
+            ey_built = true;
+        }
         mri::GridParams gp = grid_params(g, rec, xs, nx, ys, ny, zs, nz, d);
         gp.wbound = wbound;
         gp.s_tab = s_tab;
+        gp.ey_tab = g.ey_bytes > 0 ? ey_tab : nullptr;
+        gp.ey_blocks = g.ey_bytes > 0 ? ny / mri::kTcRows : 0;
         gp.coils = grp.nb;
         if (g.splits == 1) {
             gp.out_r = out_r + grp.b0 * N;

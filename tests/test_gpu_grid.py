@@ -136,8 +136,9 @@ def test_tensor_core_width_against_general_path(mri, trig):
     assert mri.plan_grid("fhd", M, 128, 3, 7)["samples_per_tile"] == 32
 
 
+@pytest.mark.parametrize("ny", [2, 128])
 @pytest.mark.parametrize("k", [-100, 60])
-def test_tensor_core_weight_scale_is_exact(mri, k):
+def test_tensor_core_weight_scale_is_exact(mri, k, ny):
     """The tensor-core kernel scales its f16 operands by a power of two taken
     from the largest weight, so multiplying D by 2^k must multiply F^H D by
     exactly 2^k (the same bits up to the exponent), far outside f16's range;
@@ -145,7 +146,7 @@ def test_tensor_core_weight_scale_is_exact(mri, k):
     w = wl.make_workload("fhd_128_radial")
     M = 4099
     xs = (np.arange(128) - 64).astype(np.float32)
-    ys = np.array([-7, 12], np.float32)
+    ys = np.array([-7, 12], np.float32) if ny == 2 else (np.arange(128) - 64).astype(np.float32)
     zs = np.array([5], np.float32)
     k3 = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
     axes = [dev(xs), dev(ys), dev(zs)]
@@ -159,3 +160,26 @@ def test_tensor_core_weight_scale_is_exact(mri, k):
         z = torch.zeros_like(d[0])
         rz, iz = mri.fhd_grid(*k3, *axes, *phi, z, z, trig=trig)
         assert torch.count_nonzero(rz) == 0 and torch.count_nonzero(iz) == 0
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+def test_tensor_core_y_factor_table_blocks(mri, trig):
+    """ny = 256 (two blocks of 128 rows per plane) and three planes: the
+    accurate path takes the y factors from the per-call table, by block."""
+    w = wl.make_workload("fhd_128_radial")
+    M = 3001
+    xs = (np.arange(128) - 64).astype(np.float32)
+    ys = (np.arange(256) - 128).astype(np.float32) * 0.5
+    zs = np.array([-21.0, 0.0, 13.0], np.float32)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    wts = [dev(a[:M]) for a in (w.rPhi, w.iPhi, w.rD, w.iD)]
+    r, i = mri.fhd_grid(*k, dev(xs), dev(ys), dev(zs), *wts, trig=trig)
+    x, y, z = expand(xs, ys, zs)
+    idx = wl.voxel_subset(x.size, 4096, 17)
+    ref = oracle.fhd(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M],
+                     w.rD[:M], w.iD[:M], idx=idx)
+    assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
+    qr, qi = mri.q_grid(*k, dev(xs), dev(ys), dev(zs), wts[0], wts[1], trig=trig)
+    qref = oracle.q(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M], idx=idx)
+    assert oracle.rel_l2(cplx(qr, qi)[idx], qref) <= TOL[trig]
+    assert mri.device_errors(clear=True) == 0

@@ -58,27 +58,29 @@ def check_per_coil(got, ref, tol):
 
 
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
-@pytest.mark.parametrize("B", [1, 3, 8, 13])
+@pytest.mark.parametrize("B", [1, 3, 8, 9, 13])
 def test_tensor_core_coil_groups(mri, B, trig):
     """Groups of 1, a padded 4, a full 8 and 8 + padded 8; ragged rows
     (3 x 7 = 21) and a ragged sample count."""
     w = wl.make_workload("fhd_128_radial")
     M = 5001
     xs = (np.arange(128) - 64).astype(np.float32)
-    ys = np.array([-40, 3, 57], np.float32)
-    zs = (np.arange(7) * 9 - 30).astype(np.float32)
+    # B = 9: a group of 8 and a single coil; ny = 128 lets the single coil
+    # take the y-factor table on the accurate path
+    ys = (np.arange(128) - 64).astype(np.float32) if B == 9 else np.array([-40, 3, 57], np.float32)
+    zs = np.array([-30.0, 6.0], np.float32) if B == 9 else (np.arange(7) * 9 - 30).astype(np.float32)
     rD, iD = coil_data(w, B, M, 10 + B)
     k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
     phi = [dev(w.rPhi[:M]), dev(w.iPhi[:M])]
     r, i = mri.fhd_batched_grid(*k, dev(xs), dev(ys), dev(zs), *phi, dev(rD), dev(iD), trig=trig)
-    assert r.shape == (B, 128 * 21)
+    assert r.shape == (B, 128 * ys.size * zs.size)
     x, y, z = expand(xs, ys, zs)
     ref = oracle.fhd_batched(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M],
                              rD, iD)
     check_per_coil(cplx(r, i), ref, TOL[trig])
-    plan = mri.plan_grid_batched(B, M, 128, 3, 7)
+    plan = mri.plan_grid_batched(B, M, 128, ys.size, zs.size)
     assert plan["tensor_cores"] == 1
-    assert plan["coil_groups"] == {1: 1, 3: 1, 8: 1, 13: 2}[B]
+    assert plan["coil_groups"] == {1: 1, 3: 1, 8: 1, 9: 2, 13: 2}[B]
 
 
 def test_batched_grid_accumulates_and_matches_single_coil_calls(mri):
