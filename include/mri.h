@@ -126,6 +126,24 @@ mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz,
                            mri_trig trig, int accumulate, void* stream);
 
 /*
+ * Forward model: D[m] = sum_n rho[n] e^{-i 2 pi k_m . x_n}, the F of Fig. 17.3
+ * (section 17.1: F models the physics of the imaging process; F^H D above is
+ * its conjugate transpose applied to the data), e.g. to synthesise k-space
+ * from a phantom or for the F rho products of an iterative solver.  rho
+ * (rRho, iRho) has N elements at voxels (x, y, z); D (rD, iD) has M, one per
+ * k-space sample.  It is the same gather as mri_fhd with the roles of samples
+ * and voxels exchanged and the exponent's sign reversed; launch shape as
+ * mri_plan_gather(MRI_KIND_FHD, 1, N, M).  Edge cases as mri_fhd with M and N
+ * exchanged: M == 0 is a no-op, N == 0 zeroes D (or leaves it when
+ * accumulating).
+ */
+mri_status mri_forward(const float* kx, const float* ky, const float* kz,
+                       const float* x, const float* y, const float* z,
+                       const float* rRho, const float* iRho,
+                       int64_t M, int64_t N, float* rD, float* iD,
+                       mri_trig trig, int accumulate, void* stream);
+
+/*
  * F^H D without any memory allocation.  The pages have no counterpart: this
  * is an interface for callers that may not allocate GPU memory while they
  * run -- a process whose device memory is reserved up front, a real-time

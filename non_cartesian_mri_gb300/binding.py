@@ -67,6 +67,8 @@ def load():
         lib.mri_fhd.argtypes = [P] * 10 + [I64, I64, P, P, I, I, P]
         lib.mri_q.argtypes = [P] * 8 + [I64, I64, P, P, I, I, P]
         lib.mri_fhd_batched.argtypes = [P] * 10 + [I64, I64, I64, P, P, I, I, P]
+        lib.mri_forward.argtypes = [P] * 8 + [I64, I64, P, P, I, I, P]
+        lib.mri_forward.restype = ctypes.c_int
         for f in (lib.mri_mu, lib.mri_fhd, lib.mri_q, lib.mri_fhd_batched):
             f.restype = ctypes.c_int
         lib.mri_status_string.argtypes = [ctypes.c_int]
@@ -235,6 +237,22 @@ def fhd_batched(kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, *, trig="fast", accumul
                                       _ptr(rPhi), _ptr(iPhi), _ptr(rD), _ptr(iD), B, M, N,
                                       _ptr(r), _ptr(i), TRIG[trig], int(bool(accumulate)),
                                       _stream_handle(stream)), "mri_fhd_batched")
+    return m.result((r, i))
+
+
+def forward(kx, ky, kz, x, y, z, rRho, iRho, *, trig="fast", accumulate=False, out=None,
+            stream=None):
+    """Forward model D[m] = sum_n rho[n] e^{-i2pi k_m.x_n}; returns (rD, iD) [M]."""
+    m = _Marshal([kx, ky, kz, x, y, z, rRho, iRho])
+    kx, ky, kz, x, y, z, rRho, iRho = m.tensors
+    M, N = kx.shape[0], x.shape[0]
+    _same_len("sample", [kx, ky, kz], M)
+    _same_len("voxel", [x, y, z, rRho, iRho], N)
+    r, i = _outputs(out, (M,), m.device)
+    with torch.cuda.device(m.device):
+        _check(load().mri_forward(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(x), _ptr(y), _ptr(z),
+                                  _ptr(rRho), _ptr(iRho), M, N, _ptr(r), _ptr(i), TRIG[trig],
+                                  int(bool(accumulate)), _stream_handle(stream)), "mri_forward")
     return m.result((r, i))
 
 

@@ -112,6 +112,8 @@ struct PrepParams {
     unsigned int* wbound = nullptr;
     // Coils b0 .. b0 + coils_valid - 1 exist; the rest of a group get weight 0.
     int coils_valid = 1 << 30;
+    // Phi == 1 (rPhi, iPhi unused): the weight is D itself (the forward model)
+    bool unit_phi = false;
 };
 
 struct GatherParams {
@@ -151,7 +153,8 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
             f[0] = p.kx[m] * p.kscale;
             f[1] = p.ky[m] * p.kscale;
             f[2] = p.kz[m] * p.kscale;
-            const float rp = p.rPhi[m], ip = p.iPhi[m];
+            const float rp = p.unit_phi ? 1.0f : p.rPhi[m];
+            const float ip = p.unit_phi ? 0.0f : p.iPhi[m];
             if (REALW) {
                 f[3] = fmaf(ip, ip, rp * rp);                       // |Phi|^2
             } else {

@@ -49,7 +49,10 @@ namespace mri {
 constexpr int kTcTile = 32;                          // samples per tile (two K = 16 steps)
 constexpr int kTcRows = 128;                         // grid rows per CTA = MMA M
 constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
-constexpr int kTcThreads = 256;
+#ifndef MRI_TC_THREADS
+#define MRI_TC_THREADS 256
+#endif
+constexpr int kTcThreads = MRI_TC_THREADS;           // 256 or 512
 constexpr int kTcWarps = kTcThreads / 32;
 #ifndef MRI_TC_STAGES
 #define MRI_TC_STAGES 4
@@ -91,7 +94,7 @@ constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per l
 constexpr uint32_t kTcAStageCols = 4 * kTcAPartCols; // A r/i hi/lo (64 columns)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcAExp = 15;                          // |A| * scale < 2^kTcAExp
-static_assert(kTcThreads == 256, "generation mapping");
+static_assert(kTcThreads == 256 || kTcThreads == 512, "generation mapping");
 constexpr int kTcAChunks = kTcTile / 8 / (kTcWarps / 4);   // 8-sample A chunks per thread
 static_assert(kTcStages >= 1 && kTcDCols + kTcStages * kTcAStageCols <= kTcTmemCols,
               "A stages fit tensor memory");
@@ -635,12 +638,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                            coil * p.coil_stride;
         if (row < total_rows && coil < p.coils && nt > 0) {
             float* o = out + row * kTcCols + (wcols & 127u);
-            if (p.accumulate) {
+            // a thread's 128 outputs are contiguous: 16-byte accesses when the
+            // array allows them (rows are 512 B apart, so only the base decides)
+            const float keep = p.accumulate ? 1.0f : 0.0f;
+            if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+                float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
-                for (int j = 0; j < kTcColsPerWarp; ++j) o[j] = fmaf(R[j], inv_scale, o[j]);
+                for (int j = 0; j < kTcColsPerWarp / 4; ++j) {
+                    const float4 a = p.accumulate ? o4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    o4[j] = make_float4(fmaf(R[4 * j], inv_scale, keep * a.x),
+                                        fmaf(R[4 * j + 1], inv_scale, keep * a.y),
+                                        fmaf(R[4 * j + 2], inv_scale, keep * a.z),
+                                        fmaf(R[4 * j + 3], inv_scale, keep * a.w));
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < kTcColsPerWarp; ++j) o[j] = R[j] * inv_scale;
+                for (int j = 0; j < kTcColsPerWarp; ++j)
+                    o[j] = fmaf(R[j], inv_scale, p.accumulate ? o[j] : 0.0f);
             }
         }
     } else {

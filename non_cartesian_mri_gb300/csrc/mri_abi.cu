@@ -233,12 +233,18 @@ mri_status run_group(DeviceState* d, const GroupPlan& g, int sms, const float* k
                      const float* kz, const float* x, const float* y, const float* z,
                      const float* rPhi, const float* iPhi, const float* rD, const float* iD,
                      int64_t b0, int64_t M, int64_t N, float* out_r, float* out_i, int trig,
-                     int accumulate, char* scratch, unsigned int* err, cudaStream_t s)
+                     int accumulate, char* scratch, unsigned int* err, cudaStream_t s,
+                     bool forward)
 {
     float* rec = reinterpret_cast<float*>(scratch);
     float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
 
     mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, b0, g.ntiles, kscale_for(trig), rec};
+    if (forward) {
+        // e^{-i2pi k.x}: the sign goes into the record scale; weight = rho
+        pp.kscale = -pp.kscale;
+        pp.unit_phi = true;
+    }
     if (mri::launch_prep(g.bc, g.realw, pp, grid_for(g.ntiles * kTile, sms), s) != cudaSuccess)
         return cuda_fail();
 
@@ -303,7 +309,8 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
                            const float* kz, const float* x, const float* y, const float* z,
                            const float* rPhi, const float* iPhi, const float* rD,
                            const float* iD, int64_t M, int64_t N, float* out_r, float* out_i,
-                           int trig, int accumulate, DeviceState* d, cudaStream_t s)
+                           int trig, int accumulate, DeviceState* d, cudaStream_t s,
+                           bool forward = false)
 {
     if (M == 0) {
         if (!accumulate) {
@@ -330,7 +337,7 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
     for (int64_t b0 = 0; b0 < B && st == MRI_OK;) {
         const int i = realw ? 3 : group_index(B - b0);
         st = run_group(d, plans[i], d->sms, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, b0, M, N,
-                       out_r, out_i, trig, accumulate, scratch, d->err, s);
+                       out_r, out_i, trig, accumulate, scratch, d->err, s, forward);
         b0 += plans[i].bc;
     }
     if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
@@ -723,6 +730,23 @@ mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz, co
     if (st != MRI_OK || N == 0) return st;
     return run_gather_call(false, B, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, M, N, rFhD, iFhD,
                            int(trig), accumulate, d, static_cast<cudaStream_t>(stream));
+}
+
+mri_status mri_forward(const float* kx, const float* ky, const float* kz, const float* x,
+                       const float* y, const float* z, const float* rRho, const float* iRho,
+                       int64_t M, int64_t N, float* rD, float* iD, mri_trig trig, int accumulate,
+                       void* stream)
+{
+    // the gather with roles exchanged: the N voxels are summed over, the M
+    // k-space samples are the outputs
+    const void* sp[5] = {x, y, z, rRho, iRho};
+    const void* vp[5] = {kx, ky, kz, rD, iD};
+    DeviceState* d = nullptr;
+    mri_status st = prepare(int(trig), accumulate, 1, N, M, sp, 5, vp, 5, &d);
+    if (st != MRI_OK || M == 0) return st;
+    return run_gather_call(false, 1, x, y, z, kx, ky, kz, nullptr, nullptr, rRho, iRho, N, M, rD,
+                           iD, int(trig), accumulate, d, static_cast<cudaStream_t>(stream),
+                           /*forward=*/true);
 }
 
 mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz, const float* xs,

@@ -194,3 +194,20 @@ def test_batched_grid_argument_checks(lib):
     assert f(*args(B=0)) == SIZE
     assert f(*args(M=-1)) == SIZE
     assert f(*args(nx=-2)) == SIZE
+
+
+def test_forward_argument_checks(lib):
+    f = lib.mri_forward
+    f.argtypes = [P] * 8 + [I64, I64, P, P, ctypes.c_int, ctypes.c_int, P]
+    f.restype = ctypes.c_int
+    g = fake()
+    assert f(*g[:8], 10, 10, g[8], g[9], 9, 0, None) == MODE
+    assert f(*g[:8], -1, 10, g[8], g[9], 0, 0, None) == SIZE
+    assert f(*g[:8], 10, -1, g[8], g[9], 0, 0, None) == SIZE
+    assert f(*g[:8], 0, 10, g[8], g[9], 0, 0, None) == OK          # no samples: no-op
+    bad = list(g[:8])
+    bad[3] = P(None)                                                 # x
+    assert f(*bad, 10, 10, g[8], g[9], 0, 0, None) == NULL
+    bad = list(g[:8])
+    bad[6] = P(0x100001)                                             # rRho misaligned
+    assert f(*bad, 10, 10, g[8], g[9], 0, 0, None) == ALIGN
