@@ -504,22 +504,34 @@ def run_ours(args):
                 ("fhd_batched_grid_fast", "fhd_batched_128", "fast", True),
                 ("fhd_batched_grid_accurate", "fhd_batched_128", "accurate", True),
                 ("fhd_batched_fast", "fhd_batched_128", "fast", False),
-                ("fhd_batched_accurate", "fhd_batched_128", "accurate", False)):
+                ("fhd_batched_accurate", "fhd_batched_128", "accurate", False),
+                ("forward_general_fast", HEADLINE, "fast", False),
+                ("forward_general_accurate", HEADLINE, "accurate", False)):
             if name.startswith("fhd_") and (name.startswith("fhd_grid") == grid) and \
                     trig == args.trig and not name.startswith("fhd_batched"):
                 continue                     # the headline itself
             pw = wl.make_workload(wname)
             pt = to_dev(pw, torch)
             po = None
-            pres = timed_steps(torch, mri, dist,
-                               lambda: call(mri, pw.kind, pt, trig, po, pgrid),
-                               args.steps, args.warmup, flush)
+            fwd = name.startswith("forward")
+            if fwd:
+                # the forward model D = F rho of a seeded complex image
+                rng = np.random.default_rng(1000 + pw.meta.get("seed", 0))
+                rho = [torch.from_numpy(rng.standard_normal(pw.N).astype(np.float32)).cuda()
+                       for _ in range(2)]
+                fn = lambda: mri.forward(pt["kx"], pt["ky"], pt["kz"], pt["x"], pt["y"],  # noqa: E731
+                                         pt["z"], rho[0], rho[1], trig=trig)
+            else:
+                fn = lambda: call(mri, pw.kind, pt, trig, po, pgrid)  # noqa: E731
+            pres = timed_steps(torch, mri, dist, fn, args.steps, args.warmup, flush)
             pm = statistics.mean(pres["step_ms"]) / 1e3
             punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
-            pplan = grid_or_general_plan(mri, pw, pgrid)
+            pplan = mri.plan("fhd", pw.N, pw.M) if fwd else grid_or_general_plan(mri, pw, pgrid)
             paths[name] = {
-                "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}", "trig": trig,
-                "entry": ENTRY[(pw.kind, pgrid)],
+                "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}"
+                            + (" (forward model of a seeded complex image)" if fwd else ""),
+                "trig": trig,
+                "entry": "mri_forward" if fwd else ENTRY[(pw.kind, pgrid)],
                 "value": round(punits / pm / 1e9, 2),
                 "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
                 "ms_per_step": round(pm * 1e3, 3),

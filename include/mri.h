@@ -225,6 +225,22 @@ mri_status mri_fhd_batched_grid(const float* kx, const float* ky, const float* k
                                 float* rFhD, float* iFhD,
                                 mri_trig trig, int accumulate, void* stream);
 
+/*
+ * The forward model of mri_forward on a separable grid: rho (rRho, iRho) on
+ * the grid xs x ys x zs (voxel order as mri_fhd_grid, N = nx*ny*nz), D (rD,
+ * iD) at the M samples.  With nx = 128 the sum over the columns is a complex
+ * matrix product on the tensor cores (the samples are the MMA rows; f16
+ * operands split into high and low parts, fp32 accumulation) and the sum
+ * over rows follows in the epilogue with blocked summation; other grids are
+ * expanded to coordinates and take mri_forward.  Edge cases as mri_forward.
+ */
+mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
+                            const float* xs, int nx, const float* ys, int ny,
+                            const float* zs, int nz,
+                            const float* rRho, const float* iRho, int64_t M,
+                            float* rD, float* iD,
+                            mri_trig trig, int accumulate, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
 

@@ -6,7 +6,7 @@ The CUDA library is built with ``non_cartesian_mri_gb300.build.build()``.
 ``workloads`` holds the seeded synthetic input generators.
 """
 
-_API = ("mu", "fhd", "q", "fhd_batched", "forward", "fhd_grid", "q_grid", "fhd_batched_grid", "plan",
+_API = ("mu", "fhd", "q", "fhd_batched", "forward", "forward_grid", "fhd_grid", "q_grid", "fhd_batched_grid", "plan",
         "plan_grid", "plan_grid_batched",
         "device_errors", "microbench", "wait_selftest",
         "status_string", "MriError", "load", "lib_path", "TRIG", "gather_timing")

@@ -69,6 +69,9 @@ def load():
         lib.mri_fhd_batched.argtypes = [P] * 10 + [I64, I64, I64, P, P, I, I, P]
         lib.mri_forward.argtypes = [P] * 8 + [I64, I64, P, P, I, I, P]
         lib.mri_forward.restype = ctypes.c_int
+        lib.mri_forward_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 2
+                                         + [I64, P, P, I, I, P])
+        lib.mri_forward_grid.restype = ctypes.c_int
         for f in (lib.mri_mu, lib.mri_fhd, lib.mri_q, lib.mri_fhd_batched):
             f.restype = ctypes.c_int
         lib.mri_status_string.argtypes = [ctypes.c_int]
@@ -253,6 +256,28 @@ def forward(kx, ky, kz, x, y, z, rRho, iRho, *, trig="fast", accumulate=False, o
         _check(load().mri_forward(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(x), _ptr(y), _ptr(z),
                                   _ptr(rRho), _ptr(iRho), M, N, _ptr(r), _ptr(i), TRIG[trig],
                                   int(bool(accumulate)), _stream_handle(stream)), "mri_forward")
+    return m.result((r, i))
+
+
+def forward_grid(kx, ky, kz, xs, ys, zs, rRho, iRho, *, trig="fast", accumulate=False,
+                 out=None, stream=None):
+    """Forward model of an image on the grid xs x ys x zs (rho [N], x fastest);
+    returns (rD, iD) [M]."""
+    m = _Marshal([kx, ky, kz, xs, ys, zs, rRho, iRho])
+    kx, ky, kz, xs, ys, zs, rRho, iRho = m.tensors
+    M = kx.shape[0]
+    _same_len("sample", [kx, ky, kz], M)
+    for t in (xs, ys, zs):
+        if t.dim() != 1:
+            raise ValueError("grid axes must be 1-D")
+    nx, ny, nz = xs.shape[0], ys.shape[0], zs.shape[0]
+    _same_len("voxel", [rRho, iRho], nx * ny * nz)
+    r, i = _outputs(out, (M,), m.device)
+    with torch.cuda.device(m.device):
+        _check(load().mri_forward_grid(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(xs), nx, _ptr(ys), ny,
+                                       _ptr(zs), nz, _ptr(rRho), _ptr(iRho), M, _ptr(r), _ptr(i),
+                                       TRIG[trig], int(bool(accumulate)),
+                                       _stream_handle(stream)), "mri_forward_grid")
     return m.result((r, i))
 
 

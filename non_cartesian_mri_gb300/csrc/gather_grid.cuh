@@ -66,6 +66,24 @@ struct GridParams {
     int ey_blocks;
 };
 
+// Forward model on a grid (tensor-core kernel, gather_grid_tc_fwd.cuh).
+struct FwdParams {
+    const float *kx, *ky, *kz;       // M samples
+    int64_t M;
+    float kscale;                    // phase units of the trig path
+    const float* xs;                 // 128 columns
+    const float2* yz_rows;           // (y, z) of every row, padded to whole blocks
+    int64_t row_blocks;
+    int splits;                      // CTAs along the row blocks
+    const unsigned char* rho_tab;    // chunks [row block][K step], kFwChunkBytes each
+    const unsigned int* bound;       // float bits of max |rho_r| + |rho_i|
+    float* out_r;                    // [split][M] or the caller's arrays
+    float* out_i;
+    int64_t split_stride;
+    int accumulate;
+    unsigned int* err;
+};
+
 // The table kernel takes nx in {32, 64, 128, 256}: nx / 4 column blocks
 // divide the 256 threads, and the tables fit shared memory (nx = 32 gives
 // R = 128 rows).  nx is a template parameter so that every table address is a

@@ -1,5 +1,6 @@
 // kernels_grid_tc.cu -- tensor-core separable-grid kernels (gather_grid_tc.cuh).
 #include "gather_grid_tc.cuh"
+#include "gather_grid_tc_fwd.cuh"
 #include "launch.h"
 
 namespace mri {
@@ -94,6 +95,37 @@ cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_
             break;
         default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cudaStream_t s)
+{
+    const size_t smem = grid_tc_fwd_smem_bytes();
+    auto go = [&](auto kernel) -> cudaError_t {
+        const cudaError_t attr =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (attr != cudaSuccess) return attr;
+        kernel<<<grid, kFwThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    };
+    switch (trig) {
+        case TRIG_ACCURATE: return go(forward_grid_tc_kernel<TRIG_ACCURATE>);
+        case TRIG_FAST: return go(forward_grid_tc_kernel<TRIG_FAST>);
+        case TRIG_FAST_RR: return go(forward_grid_tc_kernel<TRIG_FAST_RR>);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows,
+                                     int64_t row_blocks, const float* ys, int ny, const float* zs,
+                                     unsigned int* bound, unsigned char* tab, float2* yz_rows,
+                                     int grid, cudaStream_t s)
+{
+    if (cudaMemsetAsync(bound, 0, sizeof(unsigned int), s) != cudaSuccess)
+        return cudaErrorUnknown;
+    rho_bound_kernel<<<grid, 256, 0, s>>>(rr, ri, rows * kFwCols, bound);
+    build_rho_tiles_kernel<<<grid, 256, 0, s>>>(rr, ri, rows, row_blocks, bound, tab);
+    build_row_coords_kernel<<<grid, 256, 0, s>>>(ys, ny, zs, rows, row_blocks * kFwRows, yz_rows);
     return cudaGetLastError();
 }
 

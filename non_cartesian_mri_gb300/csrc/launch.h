@@ -41,6 +41,13 @@ cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cu
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s);
 cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s);
+// forward model on a grid (nx = 128) on the tensor cores: the rho table, row
+// coordinates and scale word, then the kernel
+cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows,
+                                     int64_t row_blocks, const float* ys, int ny, const float* zs,
+                                     unsigned int* bound, unsigned char* tab, float2* yz_rows,
+                                     int grid, cudaStream_t s);
+cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cudaStream_t s);
 // whether a tensor-core grid launch takes its y factors from the Ey table
 bool grid_tc_ey_table(int trig, int bc, int ny);
 // the Ey table (ny % 128 == 0) from the records (ky) and ys

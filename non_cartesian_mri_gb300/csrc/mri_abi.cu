@@ -749,6 +749,103 @@ mri_status mri_forward(const float* kx, const float* ky, const float* kz, const 
                            /*forward=*/true);
 }
 
+mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, const float* xs,
+                            int nx, const float* ys, int ny, const float* zs, int nz,
+                            const float* rRho, const float* iRho, int64_t M, float* rD,
+                            float* iD, mri_trig trig, int accumulate, void* stream)
+{
+    mri_status st = check_mode(int(trig), accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_grid_dims(nx, ny, nz, M)) != MRI_OK) return st;
+    const int64_t N = int64_t(nx) * ny * nz;
+    // the voxels (rho and the axes) are summed over, the M samples are outputs
+    const void* sp[5] = {xs, ys, zs, rRho, iRho};
+    const void* vp[5] = {kx, ky, kz, rD, iD};
+    DeviceState* d = nullptr;
+    if ((st = prepare(int(trig), accumulate, 1, N, M, sp, 5, vp, 5, &d)) != MRI_OK || M == 0)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        if (!accumulate &&
+            (mri::launch_zero(rD, M, grid_for(M, d->sms), s) != cudaSuccess ||
+             mri::launch_zero(iD, M, grid_for(M, d->sms), s) != cudaSuccess))
+            return cuda_fail();
+        return MRI_OK;
+    }
+    if (!mri::grid_tc_fits(nx)) {
+        // expand the coordinates and take the general gather
+        float* xyz = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
+                                    s) != cudaSuccess)
+            return cuda_fail();
+        if (mri::launch_expand_grid(xs, ys, zs, nx, ny, N, xyz, xyz + N, xyz + 2 * N,
+                                    grid_for(N, d->sms), s) != cudaSuccess)
+            st = cuda_fail();
+        if (st == MRI_OK)
+            st = run_gather_call(false, 1, xyz, xyz + N, xyz + 2 * N, kx, ky, kz, nullptr, nullptr,
+                                 rRho, iRho, N, M, rD, iD, int(trig), accumulate, d, s,
+                                 /*forward=*/true);
+        if (cudaFreeAsync(xyz, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+        return st;
+    }
+    // tensor cores: a CTA per 128 samples, row blocks split when too few CTAs
+    const int64_t rows = int64_t(ny) * nz;
+    const int64_t row_blocks = ceil_div(rows, int64_t(mri::kTcRows));
+    const int64_t sample_tiles = ceil_div(M, int64_t(mri::kTcRows));
+    const int splits =
+        choose_splits(row_blocks, sample_tiles, d->sms > 0 ? d->sms : 1, 1, M, 1.0, 3.0);
+    const int64_t tab_bytes = row_blocks * 8 * int64_t(24 * 1024);
+    const int64_t yz_bytes = row_blocks * mri::kTcRows * 8;
+    const int64_t part_bytes = splits > 1 ? int64_t(splits) * 2 * M * 4 : 0;
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                size_t(align256(tab_bytes) + align256(yz_bytes) + kBoundBytes +
+                                       part_bytes),
+                                d->pool, s) != cudaSuccess)
+        return cuda_fail();
+    unsigned char* tab = reinterpret_cast<unsigned char*>(scratch);
+    float2* yz_rows = reinterpret_cast<float2*>(scratch + align256(tab_bytes));
+    unsigned int* bound =
+        reinterpret_cast<unsigned int*>(scratch + align256(tab_bytes) + align256(yz_bytes));
+    float* part = reinterpret_cast<float*>(scratch + align256(tab_bytes) + align256(yz_bytes) +
+                                           kBoundBytes);
+    if (mri::launch_forward_grid_prep(rRho, iRho, rows, row_blocks, ys, ny, zs, bound, tab,
+                                      yz_rows, grid_for(row_blocks * 2048, d->sms),
+                                      s) != cudaSuccess)
+        st = cuda_fail();
+    mri::FwdParams fp{};
+    fp.kx = kx;
+    fp.ky = ky;
+    fp.kz = kz;
+    fp.M = M;
+    fp.kscale = kscale_for(int(trig));
+    fp.xs = xs;
+    fp.yz_rows = yz_rows;
+    fp.row_blocks = row_blocks;
+    fp.splits = splits;
+    fp.rho_tab = tab;
+    fp.bound = bound;
+    fp.out_r = splits > 1 ? part : rD;
+    fp.out_i = splits > 1 ? part + M : iD;
+    fp.split_stride = splits > 1 ? 2 * M : 0;
+    fp.accumulate = splits > 1 ? 0 : accumulate;
+    fp.err = d->err;
+    if (st == MRI_OK) {
+        cudaEvent_t* ev = timing_slot(d);
+        if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
+        const dim3 grid(unsigned(sample_tiles), unsigned(splits), 1);
+        if (st == MRI_OK && mri::launch_forward_grid_tc(int(trig), fp, grid, s) != cudaSuccess)
+            st = cuda_fail();
+        if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
+    }
+    if (st == MRI_OK && splits > 1 &&
+        mri::launch_reduce(part, splits, 1, M, rD, iD, M, accumulate, grid_for(2 * M, d->sms),
+                           s) != cudaSuccess)
+        st = cuda_fail();
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
 mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz, const float* xs,
                         int nx, const float* ys, int ny, const float* zs, int nz,
                         const float* rPhi, const float* iPhi, const float* rD, const float* iD,

@@ -86,3 +86,101 @@ def test_forward_accumulate_and_empty(mri):
     re_, ie_ = mri.forward(e, e, e, *x, dev(rho.real), dev(rho.imag))   # no samples
     assert re_.numel() == 0
     assert mri.device_errors(clear=True) == 0
+
+
+def expand(xs, ys, zs):
+    z, y, x = np.meshgrid(zs, ys, xs, indexing="ij")
+    return x.reshape(-1), y.reshape(-1), z.reshape(-1)
+
+
+def grid_case(ny, nz, M, seed):
+    w = wl.make_workload("fhd_128_radial")
+    xs = (np.arange(128) - 64).astype(np.float32)
+    rng = np.random.default_rng(seed)
+    pop = np.arange(-128, 128) * 0.5
+    ys = np.sort(rng.choice(pop, ny, replace=False)).astype(np.float32)
+    zs = np.sort(rng.choice(pop, nz, replace=False)).astype(np.float32)
+    n = 128 * ny * nz
+    rho = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
+    return w, xs, ys, zs, rho
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+@pytest.mark.parametrize("ny,nz,M", [(3, 7, 1000), (256, 2, 3001)])
+def test_forward_grid_tensor_cores(mri, trig, ny, nz, M):
+    """nx = 128: ragged row blocks (21 rows) and several row blocks (512
+    rows), ragged sample counts."""
+    w, xs, ys, zs, rho = grid_case(ny, nz, M, 11 + ny)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    r, i = mri.forward_grid(*k, dev(xs), dev(ys), dev(zs), dev(rho.real), dev(rho.imag), trig=trig)
+    x, y, z = expand(xs, ys, zs)
+    ref = oracle.forward(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, rho)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL[trig]
+    assert mri.device_errors(clear=True) == 0
+
+
+def test_forward_grid_128_sampled_and_accumulate(mri):
+    """The full 128^3 grid, the radial trajectory; the oracle checks 256 samples."""
+    w = wl.make_workload("fhd_128_radial")
+    rng = np.random.default_rng(21)
+    rho = (rng.standard_normal(w.N) + 1j * rng.standard_normal(w.N)).astype(np.complex64)
+    xs, ys, zs = w.axes()
+    k = [dev(w.kx), dev(w.ky), dev(w.kz)]
+    axes = [dev(xs), dev(ys), dev(zs)]
+    for trig in ("accurate", "fast"):
+        r, i = mri.forward_grid(*k, *axes, dev(rho.real), dev(rho.imag), trig=trig)
+        idx = np.sort(rng.choice(w.M, 256, replace=False))
+        ref = oracle.forward(w.kx[idx], w.ky[idx], w.kz[idx], w.x, w.y, w.z, rho)
+        assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig], trig
+    out = (torch.full_like(r, 0.25), torch.full_like(i, 4.0))
+    mri.forward_grid(*k, *axes, dev(rho.real), dev(rho.imag), trig="fast", accumulate=True,
+                     out=out)
+    assert oracle.rel_l2(cplx(out[0] - 0.25, out[1] - 4.0), cplx(r, i)) <= 1e-6
+
+
+def test_forward_grid_adjoint_of_fhd_grid(mri):
+    w, xs, ys, zs, rho = grid_case(8, 4, 2000, 31)
+    M = 2000
+    rng = np.random.default_rng(32)
+    d = (rng.standard_normal(M) + 1j * rng.standard_normal(M)).astype(np.complex64)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    axes = [dev(xs), dev(ys), dev(zs)]
+    fr, fi = mri.forward_grid(*k, *axes, dev(rho.real), dev(rho.imag), trig="accurate")
+    one, zero = dev(np.ones(M, np.float32)), dev(np.zeros(M, np.float32))
+    hr, hi = mri.fhd_grid(*k, *axes, one, zero, dev(d.real), dev(d.imag), trig="accurate")
+    lhs = np.vdot(d.astype(np.complex128), cplx(fr, fi))
+    rhs = np.vdot(cplx(hr, hi), rho.astype(np.complex128))
+    assert abs(lhs - rhs) <= 1e-5 * abs(lhs)
+
+
+@pytest.mark.parametrize("k", [-90, 70])
+def test_forward_grid_scale_is_exact(mri, k):
+    """rho is scaled by a power of two from its largest value: multiplying rho
+    by 2^k multiplies D by exactly 2^k."""
+    w, xs, ys, zs, rho = grid_case(4, 2, 777, 41)
+    kk = [dev(a[:777]) for a in (w.kx, w.ky, w.kz)]
+    axes = [dev(xs), dev(ys), dev(zs)]
+    r0, i0 = mri.forward_grid(*kk, *axes, dev(rho.real), dev(rho.imag), trig="fast")
+    s = float(2.0 ** k)
+    r1, i1 = mri.forward_grid(*kk, *axes, dev(rho.real) * s, dev(rho.imag) * s, trig="fast")
+    assert torch.equal(r1, r0 * s) and torch.equal(i1, i0 * s)
+
+
+def test_forward_grid_fallback_and_empty(mri):
+    """nx = 64 goes through expanded coordinates and mri_forward."""
+    w = wl.make_workload("fhd_64")
+    M = 1500
+    xs = (np.arange(64) - 32).astype(np.float32)
+    ys = np.array([-5.0, 9.0], np.float32)
+    zs = np.array([3.0, -8.0, 12.0], np.float32)
+    rng = np.random.default_rng(51)
+    rho = (rng.standard_normal(64 * 6) + 1j * rng.standard_normal(64 * 6)).astype(np.complex64)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    r, i = mri.forward_grid(*k, dev(xs), dev(ys), dev(zs), dev(rho.real), dev(rho.imag),
+                            trig="accurate")
+    x, y, z = expand(xs, ys, zs)
+    ref = oracle.forward(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, rho)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL["accurate"]
+    e = torch.empty(0, device="cuda")
+    rz, iz = mri.forward_grid(*k, e, dev(ys), dev(zs), e, e)      # nx = 0: no voxels
+    assert torch.count_nonzero(rz) == 0 and torch.count_nonzero(iz) == 0
