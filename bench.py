@@ -505,6 +505,8 @@ def run_ours(args):
                 ("fhd_batched_grid_accurate", "fhd_batched_128", "accurate", True),
                 ("fhd_batched_fast", "fhd_batched_128", "fast", False),
                 ("fhd_batched_accurate", "fhd_batched_128", "accurate", False),
+                ("forward_grid_fast", HEADLINE, "fast", True),
+                ("forward_grid_accurate", HEADLINE, "accurate", True),
                 ("forward_general_fast", HEADLINE, "fast", False),
                 ("forward_general_accurate", HEADLINE, "accurate", False)):
             if name.startswith("fhd_") and (name.startswith("fhd_grid") == grid) and \
@@ -519,19 +521,30 @@ def run_ours(args):
                 rng = np.random.default_rng(1000 + pw.meta.get("seed", 0))
                 rho = [torch.from_numpy(rng.standard_normal(pw.N).astype(np.float32)).cuda()
                        for _ in range(2)]
-                fn = lambda: mri.forward(pt["kx"], pt["ky"], pt["kz"], pt["x"], pt["y"],  # noqa: E731
-                                         pt["z"], rho[0], rho[1], trig=trig)
+                if pgrid:
+                    fn = lambda: mri.forward_grid(pt["kx"], pt["ky"], pt["kz"], pt["xs"],  # noqa: E731
+                                                  pt["ys"], pt["zs"], rho[0], rho[1], trig=trig)
+                else:
+                    fn = lambda: mri.forward(pt["kx"], pt["ky"], pt["kz"], pt["x"],  # noqa: E731
+                                             pt["y"], pt["z"], rho[0], rho[1], trig=trig)
             else:
                 fn = lambda: call(mri, pw.kind, pt, trig, po, pgrid)  # noqa: E731
             pres = timed_steps(torch, mri, dist, fn, args.steps, args.warmup, flush)
             pm = statistics.mean(pres["step_ms"]) / 1e3
             punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
-            pplan = mri.plan("fhd", pw.N, pw.M) if fwd else grid_or_general_plan(mri, pw, pgrid)
+            if fwd and pgrid:
+                # one prep (bound, rho table, row coordinates: 3 kernels) + the gather
+                pplan = {"launches": 4, "tensor_cores": 1, "samples_per_tile": 128}
+            elif fwd:
+                pplan = mri.plan("fhd", pw.N, pw.M)
+            else:
+                pplan = grid_or_general_plan(mri, pw, pgrid)
             paths[name] = {
                 "workload": f"{pw.name}: {wl.WORKLOADS[pw.name]}"
                             + (" (forward model of a seeded complex image)" if fwd else ""),
                 "trig": trig,
-                "entry": "mri_forward" if fwd else ENTRY[(pw.kind, pgrid)],
+                "entry": ("mri_forward_grid" if pgrid else "mri_forward") if fwd
+                         else ENTRY[(pw.kind, pgrid)],
                 "value": round(punits / pm / 1e9, 2),
                 "unit": "G" + ALGO_OPS[pw.kind]["unit"] + "s/s",
                 "ms_per_step": round(pm * 1e3, 3),
@@ -539,6 +552,10 @@ def run_ours(args):
                                      clocks.get("sm_mhz"), trig, pgrid, pplan, peaks),
                 "gpu_launches": pplan["launches"] * args.steps,
             }
+            if fwd:
+                # the forward kernels have their own traffic records
+                paths[name]["roofline"]["traffic"] = profiled_traffic(
+                    "grid_tc_fwd" if pgrid else "forward", trig)
             if pw.kind == "fhd_batched":
                 paths[name]["trajectory_pairs_per_s_G"] = round(pw.pairs / pm / 1e9, 2)
             del pt
