@@ -159,8 +159,11 @@ class Workload:
         return self.M * self.N
 
     def axes(self):
-        """xs, ys, zs of the workload's cubic voxel grid (x, y, z = their product)."""
-        return grid_axes(self.L)
+        """xs, ys, zs of the workload's voxel grid, read from its coordinates
+        (voxel n = (iz L + iy) L + ix), so a shifted slab keeps its shift."""
+        L = self.L
+        return (np.ascontiguousarray(self.x[:L]), np.ascontiguousarray(self.y[0:L * L:L]),
+                np.ascontiguousarray(self.z[0::L * L]))
 
 
 WORKLOADS = {

@@ -43,6 +43,7 @@ def _rank_main(rank, world, port, outdir):
             np.save(os.path.join(outdir, "gathered.npy"), full)
         np.save(os.path.join(outdir, f"max{rank}.npy"), np.array([got]))
         np.save(os.path.join(outdir, f"z{rank}.npy"), w.z)
+        np.save(os.path.join(outdir, f"zs{rank}.npy"), w.axes()[2])
     finally:
         d.close()
 
@@ -61,6 +62,20 @@ def test_two_rank_slabs_equal_the_stacked_volume(tmp_path, world):
         assert float(np.load(tmp_path / f"max{r}.npy")[0]) == 1.5 + world - 1
     z0, z1 = np.load(tmp_path / "z0.npy"), np.load(tmp_path / "z1.npy")
     np.testing.assert_array_equal(z1 - z0, np.full_like(z0, w.L))
+    # the grid entry points get each slab's own z axis
+    zs0, zs1 = np.load(tmp_path / "zs0.npy"), np.load(tmp_path / "zs1.npy")
+    np.testing.assert_array_equal(zs1 - zs0, np.full_like(zs0, w.L))
+
+
+def test_slab_axes_expand_to_its_coordinates():
+    import bench
+    for rank in (0, 1, 3):
+        w = bench.slab(wl.make_workload("fhd_tiny", L=6), rank)
+        xs, ys, zs = w.axes()
+        z, y, x = np.meshgrid(zs, ys, xs, indexing="ij")
+        np.testing.assert_array_equal(x.reshape(-1), w.x)
+        np.testing.assert_array_equal(y.reshape(-1), w.y)
+        np.testing.assert_array_equal(z.reshape(-1), w.z)
 
 
 def test_single_rank_dist_is_a_no_op():
