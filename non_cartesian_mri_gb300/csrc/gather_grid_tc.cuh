@@ -18,9 +18,10 @@
 // (12 tcgen05.mma of 128 x 256 x 16 per tile).  The two f16 parts carry about
 // 22 significant bits, and the dropped lo*lo term is below 2^-22 of a
 // product, so every product keeps close to fp32 accuracy.  f16 has a narrow
-// exponent range: the A operand is multiplied by a power of two chosen from
-// the largest |w_r| + |w_i| of the call so that every |A| < 2^15, and the
-// results are multiplied back exactly; |B| <= 1 needs no scale.
+// exponent range: the weights are multiplied (once per call, in the records)
+// by a power of two chosen from the largest |w_r| + |w_i| of the call so that
+// every |A| < 2^15, and the results are multiplied back exactly; |B| <= 1
+// needs no scale.
 //
 // Shared-memory bandwidth binds a kernel whose operands all pass through
 // shared memory (operand writes plus operand reads by the tensor core); with
@@ -122,13 +123,13 @@ inline size_t grid_tc_smem_bytes(bool realw, int bc = 1, bool eyt = false)
     return b;
 }
 
-// e[s * RC + r] = a_scale e^{i phase(ky[s] y_r + kz[s] z_r)} for the RC grid
+// e[s * RC + r] = e^{i phase(ky[s] y_r + kz[s] z_r)} for the RC grid
 // rows of a CTA and the samples of one record tile: with several coils per
 // CTA the (y, z) factor of a row is shared by its coils, so it is evaluated
 // once per (row, sample) and read back by each coil's thread.
 template <int TRIG, int RC>
 __device__ __forceinline__ void tc_row_factors(const float* rec, const float2* yz_sh, float2* e,
-                                               float a_scale, int tid)
+                                               int tid)
 {
     constexpr int ITEMS = kTcTile * RC;
     static_assert(ITEMS % kTcThreads == 0, "row-factor items");
@@ -140,7 +141,7 @@ __device__ __forceinline__ void tc_row_factors(const float* rec, const float2* y
         const float2 yz = yz_sh[r];
         float sn, cs;
         table_sincos<TRIG>(fmaf(rec[2 * kTcTile + s], yz.y, rec[kTcTile + s] * yz.x), sn, cs);
-        e[i] = make_float2(cs * a_scale, sn * a_scale);
+        e[i] = make_float2(cs, sn);
     }
 }
 
@@ -335,7 +336,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     const int64_t total_rows = int64_t(p.ny) * p.nz;
     const int64_t row0 = int64_t(blockIdx.x) * RC;
     const int scale_e = tc_scale_exp(*p.wbound);
-    const float a_scale = exp2_int(scale_e);
 
     for (int r = tid; r < RC; r += kTcThreads) {
         const int64_t row = row0 + r;
@@ -394,14 +394,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         if constexpr (EYT)
             for (; ey_loaded < 2 && ey_loaded < nt; ++ey_loaded) load_ey(ey_loaded);
     }
-    // EYT: e[s] = scale Mu[s] e^{i phase(kz[s] z)} of this CTA's plane, by warp 0
+    // EYT: e[s] = Mu[s] e^{i phase(kz[s] z)} of this CTA's plane, by warp 0
     auto z_factors = [&](const float* rec, float2* e) {
         if (warp == 0) {
             const int s = lane;
             float sn, cs;
             table_sincos<TRIG>(rec[2 * T + s] * z_plane, sn, cs);
-            const float wr = rec[3 * T + s] * a_scale;
-            const float wi = REALW ? 0.0f : rec[4 * T + s] * a_scale;
+            const float wr = rec[3 * T + s];
+            const float wi = REALW ? 0.0f : rec[4 * T + s];
             e[s] = make_float2(fmaf(wr, cs, -wi * sn), fmaf(wi, cs, wr * sn));
         }
     };
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 if constexpr (EYT)
                     z_factors(ring, e_sh);
                 else
-                    tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, a_scale, tid);
+                    tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, tid);
             }
         }
         if (__syncthreads_or(!ok0)) failed_at = 0;
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 const int s0 = 8 * (kTcAChunks * ah + c);
                 float ar[8], ai[8];
                 if constexpr (EYT) {
-                    // Mz = (scale Mu e^{i phase(kz z)}) e^{i phase(ky y)}
+                    // Mz = (Mu e^{i phase(kz z)}) e^{i phase(ky y)}
                     const float2* ez = e_sh + (t & 1) * T;
                     const float2* ey = ey_sh + (t & 1) * (T * kTcRows);
 #pragma unroll
@@ -488,12 +488,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                     for (int s8 = 0; s8 < 8; ++s8) {
                         float sn, cs;
                         table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
-                        const float swr = wr[s8] * a_scale;
+                        const float swr = wr[s8];
                         if (REALW) {
                             ar[s8] = swr * cs;
                             ai[s8] = swr * sn;
                         } else {
-                            const float swi = wi[s8] * a_scale;
+                            const float swi = wi[s8];
                             ar[s8] = fmaf(swr, cs, -swi * sn);
                             ai[s8] = fmaf(swi, cs, swr * sn);
                         }
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                             z_factors(rec1, e_sh + ((t + 1) & 1) * T);
                         else
                             tc_row_factors<TRIG, RC>(rec1, yz_sh, e_sh + ((t + 1) & 1) * T * RC,
-                                                     a_scale, tid);
+                                                     tid);
                     }
                 }
             }

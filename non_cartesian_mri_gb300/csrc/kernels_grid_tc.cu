@@ -129,6 +129,32 @@ cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t r
     return cudaGetLastError();
 }
 
+// Multiply the weights of the records (fields 3 .. fields - 1 of every
+// tile) by the power of two 2^e taken from the bound word, so that every A
+// value the kernel makes from them is below 2^kTcAExp (see tc_scale_exp); the
+// kernel multiplies its results by 2^-e.
+__global__ void __launch_bounds__(256) scale_records_kernel(float* rec, int fields,
+                                                            int64_t ntiles,
+                                                            const unsigned int* bound)
+{
+    const float scale = exp2_int(tc_scale_exp(*bound));
+    const int per_tile = (fields - 3) * kTcTile;
+    const int64_t total = ntiles * per_tile;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = i / per_tile;
+        const int j = int(i - t * per_tile);
+        rec[t * fields * kTcTile + 3 * kTcTile + j] *= scale;
+    }
+}
+
+cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
+                                 const unsigned int* bound, int grid, cudaStream_t s)
+{
+    scale_records_kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, bound);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s)
 {
     if (realw) {

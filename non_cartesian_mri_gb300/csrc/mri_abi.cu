@@ -564,7 +564,10 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         pp.coils_valid = grp.nb;
         if (cudaMemsetAsync(wbound, 0, sizeof(unsigned int), s) != cudaSuccess ||
             mri::launch_prep_grid_tc(realw, grp.bc, pp,
-                                     grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess)
+                                     grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess ||
+            mri::launch_scale_records(rec, fields, g.ntiles, wbound,
+                                      grid_for(g.ntiles * (fields - 3) * mri::kTcTile, d->sms),
+                                      s) != cudaSuccess)
             st = cuda_fail();
         // the B tiles depend on kx and the columns only: built once
         if (st == MRI_OK && i == 0 &&
@@ -962,7 +965,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         }
         rec_max = std::max(rec_max, gi.rec_bytes);
         part_max = std::max(part_max, gi.part_bytes);
-        plan->launches += 2 + (gi.splits > 1 ? 1 : 0);
+        plan->launches += 3 + (gi.splits > 1 ? 1 : 0);   // prep, scale, gather (+ reduce)
     }
     plan->coil_groups = int(groups.size());
     plan->scratch_bytes = align256(rec_max) + kBoundBytes + align256(part_max) + g.s_bytes;
