@@ -64,6 +64,8 @@ struct GridParams {
     // y values, e^{i phase(ky y)} as [sample][128] float2; ny / 128 blocks
     const float2* ey_tab;
     int ey_blocks;
+    // tensor-core kernel: column blocks of 128 (the last may be partly padding)
+    int ncb;
 };
 
 // Forward model on a grid (tensor-core kernel, gather_grid_tc_fwd.cuh).
@@ -71,11 +73,13 @@ struct FwdParams {
     const float *kx, *ky, *kz;       // M samples
     int64_t M;
     float kscale;                    // phase units of the trig path
-    const float* xs;                 // 128 columns
+    const float* xs;                 // nx columns (64 or a multiple of 128)
+    int nx;
+    int ncb;                         // column blocks of 128
     const float2* yz_rows;           // (y, z) of every row, padded to whole blocks
     int64_t row_blocks;
     int splits;                      // CTAs along the row blocks
-    const unsigned char* rho_tab;    // chunks [row block][K step], kFwChunkBytes each
+    const unsigned char* rho_tab;    // chunks [row block][column block][K step], 24 KB each
     const unsigned int* bound;       // float bits of max |rho_r| + |rho_i|
     float* out_r;                    // [split][M] or the caller's arrays
     float* out_i;

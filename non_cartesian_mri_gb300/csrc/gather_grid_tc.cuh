@@ -49,7 +49,7 @@ namespace mri {
 
 constexpr int kTcTile = 32;                          // samples per tile (two K = 16 steps)
 constexpr int kTcRows = 128;                         // grid rows per CTA = MMA M
-constexpr int kTcCols = 128;                         // grid columns = MMA N (nx = 128)
+constexpr int kTcCols = 128;                         // grid columns per CTA = MMA N / 2
 #ifndef MRI_TC_THREADS
 #define MRI_TC_THREADS 256
 #endif
@@ -105,7 +105,21 @@ enum TcPart { A_RH = 0, A_RL, A_IH, A_IL };
 constexpr int kTcSHi = 0;
 constexpr int kTcSLo = kTcSBytes;
 
-inline bool grid_tc_fits(int nx) { return nx == kTcCols; }
+// nx a multiple of 128 runs in column blocks of 128; nx = 64 as one block
+// with 64 columns of padding (half the MMA work idle, still far ahead of the
+// table kernel)
+inline bool grid_tc_fits(int nx) { return nx == 64 || (nx > 0 && nx % kTcCols == 0); }
+inline int grid_tc_col_blocks(int nx) { return (nx + kTcCols - 1) / kTcCols; }
+
+// Shape of the forward-model kernel (gather_grid_tc_fwd.cuh), which takes the
+// same nx.
+constexpr int kFwSamples = 128;                 // samples per CTA = MMA M
+constexpr int kFwRows = 128;                    // grid rows per block = MMA N / 2
+constexpr int kFwCols = 128;                    // grid columns per block = K
+constexpr int kFwKSteps = kFwCols / 16;         // 8
+constexpr int kFwChunkHalf = 3 * kFwRows * 32;  // 384 rows x 16 f16 = 12 KB (hi or lo)
+constexpr int kFwChunkBytes = 2 * kFwChunkHalf; // 24 KB
+inline bool grid_tc_fwd_fits(int nx) { return grid_tc_fits(nx); }
 
 // Coils per CTA (a coil group): the MMA's 128 rows are bc coils x 128 / bc
 // grid rows, m = b * (128 / bc) + r.
@@ -236,22 +250,26 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 template <int TRIG>
 __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, int fields,
                                                              int64_t ntiles, const float* xs,
+                                                             int nx, int ncb,
                                                              unsigned char* s_tab)
 {
     constexpr int ITEMS = kTcCols * kTcTile / 8;       // 512 (column, chunk) items per tile
-    const int64_t total = ntiles * ITEMS;
+    const int64_t total = ntiles * ncb * ITEMS;
     for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
          item += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = item / ITEMS;
-        const int r = int(item - t * ITEMS);
-        const int gi = ((r >> 5) << 3) | (r & 7);     // column
+        const int64_t tc = item / ITEMS;              // (tile, column block)
+        const int64_t t = tc / ncb;
+        const int cb = int(tc - t * ncb);
+        const int r = int(item - tc * ITEMS);
+        const int gi = ((r >> 5) << 3) | (r & 7);     // column within the block
         const int kc = (r >> 3) & 3;                  // samples 8 kc ..
         const float* kx = rec + t * fields * kTcTile + 8 * kc;
-        const float xc = xs[gi];
+        const int col = cb * kTcCols + gi;
+        const float xc = col < nx ? xs[col] : 0.0f;   // padding columns are never written
         float br[8], bi[8];
 #pragma unroll
         for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
-        unsigned char* const tile = s_tab + t * kTcStageBytes;
+        unsigned char* const tile = s_tab + tc * kTcStageBytes;
         const int off = tc_kmaj_bytes(gi, kc);        // == 16 r
         uint4 h, l;
         tc_split8(bi, h, l);
@@ -368,7 +386,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
     auto load_s = [&](int u) {
         uint64_t* bar = &s_bar[u % kS];
         mbar_arrive_expect_tx(bar, uint32_t(kTcStageBytes));
-        tma_bulk_g2s(ops + (u % kS) * kTcStageBytes, p.s_tab + (t_begin + u) * kTcStageBytes,
+        tma_bulk_g2s(ops + (u % kS) * kTcStageBytes,
+                     p.s_tab + ((t_begin + u) * p.ncb + blockIdx.z) * kTcStageBytes,
                      uint32_t(kTcStageBytes), bar);
     };
     // EYT: this CTA's 128 rows are grid rows iy0 .. iy0 + 127 of plane iz
@@ -637,11 +656,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride +
                            coil * p.coil_stride;
         if (row < total_rows && coil < p.coils && nt > 0) {
-            float* o = out + row * kTcCols + (wcols & 127u);
-            // a thread's 128 outputs are contiguous: 16-byte accesses when the
-            // array allows them (rows are 512 B apart, so only the base decides)
+            const int col0 = int(blockIdx.z) * kTcCols;
+            const int ncols = p.nx - col0 < kTcCols ? p.nx - col0 : kTcCols;
+            float* o = out + row * p.nx + col0 + (wcols & 127u);
+            // a thread's outputs are contiguous: 16-byte accesses when the
+            // array allows them (nx is a multiple of 64, so only the base decides)
             const float keep = p.accumulate ? 1.0f : 0.0f;
-            if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+            if (ncols == kTcCols && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
                 float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
                 for (int j = 0; j < kTcColsPerWarp / 4; ++j) {
@@ -654,7 +675,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             } else {
 #pragma unroll
                 for (int j = 0; j < kTcColsPerWarp; ++j)
-                    o[j] = fmaf(R[j], inv_scale, p.accumulate ? o[j] : 0.0f);
+                    if (int(wcols & 127u) + j < ncols)
+                        o[j] = fmaf(R[j], inv_scale, p.accumulate ? o[j] : 0.0f);
             }
         }
     } else {

@@ -1,29 +1,32 @@
 // gather_grid_tc_fwd.cuh -- the forward model D = F rho on a separable grid,
-// on the tensor cores (nx = 128).
+// on the tensor cores (nx = 64 or a multiple of 128).
 //
 // D[m] = sum_n rho[n] e^{-i2pi k_m . x_n} (F of Fig. 17.3) over the voxels of
 // a grid factors like F^H D does (gather_grid_tc.cuh), with the roles of the
 // two sums exchanged:
 //   T[m][row] = sum_ix Ex*[m][ix] rho[row][ix],   Ex* = e^{-i2pi kx x},
 //   D[m]      = sum_row T[m][row] e^{-i2pi (ky y + kz z)}_row.
-// The first is a complex matrix product (samples x 128 columns) by (128
-// columns x rows): a CTA owns 128 samples (the MMA M) and walks the grid rows
-// in blocks of 128 (the MMA N, [T_r | T_i] = 256 columns), K = the 128
-// columns in 8 steps of 16.  A = Ex* of the CTA's samples is evaluated once
-// into tensor memory (columns 0-255, f16 hi / lo parts) and serves every row
-// block; B = rho arrives per (row block, K step) as a 24 KB chunk of the
-// per-call table built by build_rho_tiles_kernel (rows [-rho_i; rho_r;
-// rho_i], f16 hi / lo, K-major), by TMA into a ring of shared-memory stages.
+// The first is a complex matrix product (samples x nx columns) by (nx
+// columns x rows): a CTA owns 128 samples (the MMA M) and walks the columns
+// in blocks of 128 (K, 8 steps of 16; nx = 64 is one block padded with
+// zeros) and, inside each, the grid rows in blocks of 128 (the MMA N,
+// [T_r | T_i] = 256 columns).  A = Ex* of the CTA's samples for one column
+// block is evaluated into tensor memory (columns 0-255, f16 hi / lo parts)
+// and serves every row block; B = rho arrives per (row block, column block,
+// K step) as a 24 KB chunk of the per-call table built by
+// build_rho_tiles_kernel (rows [-rho_i; rho_r; rho_i], f16 hi / lo,
+// K-major), by TMA into a ring of shared-memory stages.
 // Per K step 6 tcgen05.mma of 128 x 256 x 16 do
 //   [T_r | T_i] += A_r [B_r | B_i] + A_i [-B_i | B_r]
 // with each real product as hi*hi + hi*lo + lo*hi (about 22 bits).  rho is
 // scaled by one power of two so that every |rho| < 2^15 (f16 range) and the
 // result is scaled back exactly.
-// The second sum is the epilogue of each row block: every thread reads the
-// T of its sample for 64 of the block's rows from tensor memory (columns
-// 256-511), multiplies by e^{-i2pi(ky y + kz z)} of each row and adds the
-// block's total to its running sums (blocked summation); the two threads of
-// a sample (two column halves) combine at the end.
+// The second sum is the epilogue of each (column block, row block): every
+// thread reads the T of its sample for 64 of the block's rows from tensor
+// memory (columns 256-511), multiplies by e^{-i2pi(ky y + kz z)} of each row
+// and adds the block's total to its running sums (blocked summation; the
+// row factor distributes over the column blocks); the two threads of a
+// sample (two halves of the rows) combine at the end.
 // Every wait is bounded; a CTA that gives up sets the device error word,
 // waits (bounded) for its MMAs and copies, and frees its tensor memory.
 #pragma once
@@ -34,13 +37,7 @@
 
 namespace mri {
 
-constexpr int kFwSamples = 128;                 // samples per CTA = MMA M
-constexpr int kFwRows = 128;                    // grid rows per block = MMA N / 2
-constexpr int kFwCols = 128;                    // grid columns = K (nx = 128)
-constexpr int kFwKSteps = kFwCols / 16;         // 8
 constexpr int kFwThreads = 256;
-constexpr int kFwChunkHalf = 3 * kFwRows * 32;  // 384 rows x 16 f16 = 12 KB (hi or lo)
-constexpr int kFwChunkBytes = 2 * kFwChunkHalf; // 24 KB
 #ifndef MRI_FW_STAGES
 #define MRI_FW_STAGES 6
 #endif
@@ -52,8 +49,6 @@ constexpr int kFwLead = MRI_FW_LEAD;            // chunk copies issued ahead of 
 static_assert(kFwLead >= 1 && kFwLead < kFwStages, "chunk lead");
 constexpr uint32_t kFwACols = 256;              // A: 4 parts x 64 columns
 constexpr uint32_t kFwDCol = 256;               // D = [T_r | T_i] at columns 256-511
-
-inline bool grid_tc_fwd_fits(int nx) { return nx == kFwCols; }
 
 inline size_t grid_tc_fwd_smem_bytes()
 {
@@ -86,36 +81,41 @@ __global__ void __launch_bounds__(256) build_row_coords_kernel(const float* ys, 
     }
 }
 
-// The rho table: chunk (block b, K step kb) holds rows [-rho_i; rho_r; rho_i]
-// of grid rows 128 b .. 128 b + 127 and columns 16 kb .. 16 kb + 15, scaled
-// by 2^e, split into f16 hi (first 12 KB) and lo.  K-major without swizzle:
-// core matrices of 8 rows x 8 f16, LBO = 128 B (along K), SBO = 256 B.
-// One thread per (block, K step, row, 8-column half).
+// The rho table: chunk (block b, column block cb, K step kb) holds rows
+// [-rho_i; rho_r; rho_i] of grid rows 128 b .. 128 b + 127 and columns
+// 128 cb + 16 kb .. + 15 (zero past nx or the last row), scaled by 2^e,
+// split into f16 hi (first 12 KB) and lo.  K-major without swizzle: core
+// matrices of 8 rows x 8 f16, LBO = 128 B (along K), SBO = 256 B.  One
+// thread per (block, column block, K step, row, 8-column half).
 __global__ void __launch_bounds__(256) build_rho_tiles_kernel(const float* rr, const float* ri,
-                                                              int64_t rows, int64_t row_blocks,
+                                                              int64_t rows, int nx, int ncb,
+                                                              int64_t row_blocks,
                                                               const unsigned int* bound,
                                                               unsigned char* tab)
 {
     const float scale = exp2_int(tc_scale_exp(*bound));
-    constexpr int ITEMS = kFwKSteps * kFwRows * 2;            // per row block
-    const int64_t total = row_blocks * ITEMS;
+    constexpr int ITEMS = kFwKSteps * kFwRows * 2;            // per (row block, column block)
+    const int64_t total = row_blocks * ncb * ITEMS;
     for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
          item += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t b = item / ITEMS;
-        int rem = int(item - b * ITEMS);
+        const int64_t bc = item / ITEMS;                      // b * ncb + cb
+        const int cb = int(bc % ncb);
+        int rem = int(item - bc * ITEMS);
         const int kb = rem / (kFwRows * 2);
         rem -= kb * kFwRows * 2;
         const int r = rem >> 1;
         const int kc = rem & 1;
-        const int64_t row = b * kFwRows + r;
+        const int64_t row = (bc / ncb) * kFwRows + r;
         float vr[8], vi[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int64_t n = row * kFwCols + 16 * kb + 8 * kc + j;
-            vr[j] = row < rows ? rr[n] * scale : 0.0f;
-            vi[j] = row < rows ? ri[n] * scale : 0.0f;
+            const int col = cb * kFwCols + 16 * kb + 8 * kc + j;
+            const bool in = row < rows && col < nx;
+            const int64_t n = row * nx + col;
+            vr[j] = in ? rr[n] * scale : 0.0f;
+            vi[j] = in ? ri[n] * scale : 0.0f;
         }
-        unsigned char* chunk = tab + (b * kFwKSteps + kb) * int64_t(kFwChunkBytes);
+        unsigned char* chunk = tab + (bc * kFwKSteps + kb) * int64_t(kFwChunkBytes);
         auto off = [&](int srow) { return (srow >> 3) * 256 + kc * 128 + (srow & 7) * 16; };
         uint4 h, l;
         tc_split8(vi, h, l);
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
     const int64_t b_begin = (p.row_blocks * split) / p.splits;
     const int64_t b_end = (p.row_blocks * (split + 1)) / p.splits;
     const int nb = int(b_end - b_begin);
-    const int nc = nb * kFwKSteps;                    // chunks of this CTA
+    const int nblk = nb * p.ncb;                      // (column block, row block) pairs
+    const int nc = nblk * kFwKSteps;                  // chunks of this CTA, column block outer
     const int ms = 32 * (warp & 3) + lane;            // this thread's sample = TMEM lane
     const int64_t m = int64_t(blockIdx.x) * kFwSamples + ms;
     const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
@@ -175,9 +176,12 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
 
     auto load_chunk = [&](int c) {
         uint64_t* bar = &s_bar[c % NS];
+        const int blk = c / kFwKSteps;
+        const int cb = blk / nb;
+        const int64_t b = b_begin + (blk - cb * nb);
+        const int64_t chunk = (b * p.ncb + cb) * kFwKSteps + (c - blk * kFwKSteps);
         mbar_arrive_expect_tx(bar, uint32_t(kFwChunkBytes));
-        tma_bulk_g2s(ring + (c % NS) * kFwChunkBytes,
-                     p.rho_tab + (b_begin * kFwKSteps + c) * int64_t(kFwChunkBytes),
+        tma_bulk_g2s(ring + (c % NS) * kFwChunkBytes, p.rho_tab + chunk * int64_t(kFwChunkBytes),
                      uint32_t(kFwChunkBytes), bar);
     };
     int loaded = 0;     // chunks whose copy thread 0 issued
@@ -192,15 +196,19 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
         nky = -p.ky[m] * p.kscale;
         nkz = -p.kz[m] * p.kscale;
     }
-    // A = Ex*[m][ix] for ix = 64 h .. 64 h + 63: columns 32 h .. of every part
-    {
+    // A = Ex*[m][ix] for ix = 128 cb + 64 h .. + 63 (zero past nx, where rho
+    // is zero too): columns 32 h .. of every part
+    auto build_a = [&](int cb) {
         uint32_t hr[32], lr[32], hi_[32], li[32];
+        const int col0 = cb * kFwCols + 64 * h;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
             float ar[8], ai[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                table_sincos<TRIG>(nkx * p.xs[64 * h + 8 * c8 + j], ai[j], ar[j]);
+            for (int j = 0; j < 8; ++j) {
+                const int col = col0 + 8 * c8 + j;
+                table_sincos<TRIG>(nkx * (col < p.nx ? p.xs[col] : 0.0f), ai[j], ar[j]);
+            }
             uint4 hh, ll;
             tc_split8(ar, hh, ll);
             hr[4 * c8] = hh.x; hr[4 * c8 + 1] = hh.y; hr[4 * c8 + 2] = hh.z; hr[4 * c8 + 3] = hh.w;
@@ -215,19 +223,27 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
         tmem_st32u(a0 + 2 * 64, hi_);    // A_IH
         tmem_st32u(a0 + 3 * 64, li);     // A_IL
         tmem_wait_st();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
+    };
 
-    float run_r = 0.0f, run_i = 0.0f;   // running sums over row blocks
+    float run_r = 0.0f, run_i = 0.0f;   // running sums over blocks
     bool ok = true;
     bool c_fail = false;                // thread 0: a chunk wait timed out
     int failed = 0;
-    for (int b = 0; b < nb; ++b) {
+#pragma unroll 1
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int cb = blk / nb;
+        const int b = blk - cb * nb;
+        if (b == 0) {
+            // a new column block: every MMA of the previous one has completed
+            // (its last block's commit was waited for), so A may be rewritten
+            build_a(cb);
+            tc_fence_before_sync();
+            __syncthreads();
+            tc_fence_after_sync();
+        }
         if (tid == 0) {
             for (int kb = 0; kb < kFwKSteps && !c_fail; ++kb) {
-                const int c = b * kFwKSteps + kb;
+                const int c = blk * kFwKSteps + kb;
                 if (!mbar_wait_bounded(&s_bar[c % NS], uint32_t(c / NS) & 1u)) {
                     c_fail = true;
                     break;
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
         }
         // every thread: wait for the block's MMAs (thread 0's failure reaches
         // the others through the barrier; their own wait then gives up too)
-        ok = c_fail ? false : mbar_wait_bounded(&d_bar, uint32_t(b) & 1u);
+        ok = c_fail ? false : mbar_wait_bounded(&d_bar, uint32_t(blk) & 1u);
         if (__syncthreads_or(!ok)) {
             failed = 1;
             break;

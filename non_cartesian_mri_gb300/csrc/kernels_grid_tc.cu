@@ -81,17 +81,22 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
 }
 
 cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* xs, unsigned char* s_tab, int grid, cudaStream_t s)
+                                  const float* xs, int nx, unsigned char* s_tab, int grid,
+                                  cudaStream_t s)
 {
+    const int ncb = grid_tc_col_blocks(nx);
     switch (trig) {
         case TRIG_ACCURATE:
-            build_ex_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            build_ex_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx,
+                                                                     ncb, s_tab);
             break;
         case TRIG_FAST:
-            build_ex_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            build_ex_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx, ncb,
+                                                                 s_tab);
             break;
         case TRIG_FAST_RR:
-            build_ex_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, s_tab);
+            build_ex_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx,
+                                                                    ncb, s_tab);
             break;
         default: return cudaErrorInvalidValue;
     }
@@ -116,15 +121,16 @@ cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cuda
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows,
+cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows, int nx,
                                      int64_t row_blocks, const float* ys, int ny, const float* zs,
                                      unsigned int* bound, unsigned char* tab, float2* yz_rows,
                                      int grid, cudaStream_t s)
 {
     if (cudaMemsetAsync(bound, 0, sizeof(unsigned int), s) != cudaSuccess)
         return cudaErrorUnknown;
-    rho_bound_kernel<<<grid, 256, 0, s>>>(rr, ri, rows * kFwCols, bound);
-    build_rho_tiles_kernel<<<grid, 256, 0, s>>>(rr, ri, rows, row_blocks, bound, tab);
+    rho_bound_kernel<<<grid, 256, 0, s>>>(rr, ri, rows * nx, bound);
+    build_rho_tiles_kernel<<<grid, 256, 0, s>>>(rr, ri, rows, nx, grid_tc_col_blocks(nx),
+                                                row_blocks, bound, tab);
     build_row_coords_kernel<<<grid, 256, 0, s>>>(ys, ny, zs, rows, row_blocks * kFwRows, yz_rows);
     return cudaGetLastError();
 }

@@ -41,9 +41,9 @@ cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cu
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s);
 cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s);
-// forward model on a grid (nx = 128) on the tensor cores: the rho table, row
-// coordinates and scale word, then the kernel
-cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows,
+// forward model on a grid (nx = 64 or a multiple of 128) on the tensor cores:
+// the rho table, row coordinates and scale word, then the kernel
+cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows, int nx,
                                      int64_t row_blocks, const float* ys, int ny, const float* zs,
                                      unsigned int* bound, unsigned char* tab, float2* yz_rows,
                                      int grid, cudaStream_t s);
@@ -59,7 +59,8 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
                                   cudaStream_t s);
 // B operand tiles of the tensor-core grid kernel from its records (kx) and xs
 cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* xs, unsigned char* s_tab, int grid, cudaStream_t s);
+                                  const float* xs, int nx, unsigned char* s_tab, int grid,
+                                  cudaStream_t s);
 // one translation unit per grid width (kernels_grid_<nx>.cu)
 cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_grid_64(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);

@@ -354,6 +354,7 @@ struct GridPlan {
     bool table_kernel;      // false: coordinates expanded, general kernel
     bool tensor_cores;      // nx = 128: the tcgen05 kernel
     int bc;                 // tensor cores: coils per CTA
+    int ncb;                // tensor cores: column blocks of 128
     int64_t ntiles;
     int64_t vblocks;
     int rows_per_cta;
@@ -392,22 +393,24 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int b
                    int trig = 0)
 {
     GridPlan g{};
-    g.table_kernel = mri::grid_kernel_fits(nx);
+    g.tensor_cores = mri::grid_tc_fits(nx);
+    g.table_kernel = g.tensor_cores || mri::grid_kernel_fits(nx);
     if (!g.table_kernel) return g;
     const int64_t N = int64_t(nx) * ny * nz;
-    g.tensor_cores = mri::grid_tc_fits(nx);
     if (g.tensor_cores) {
         g.bc = bc;
+        g.ncb = mri::grid_tc_col_blocks(nx);
         g.rows_per_cta = mri::kTcRows / bc;
         g.ntiles = ceil_div(M, mri::kTcTile);
         g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
         g.ctas_per_sm = 1;
         g.splits = (g.ntiles > 0 && g.vblocks > 0)
-                       ? choose_splits(g.ntiles, g.vblocks, sms > 0 ? sms : 1, nb, N, 1.0, 3.0)
+                       ? choose_splits(g.ntiles, g.vblocks * g.ncb, sms > 0 ? sms : 1, nb, N, 1.0,
+                                       3.0)
                        : 1;
         g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
         g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
-        g.s_bytes = g.ntiles * int64_t(mri::kTcStageBytes);
+        g.s_bytes = g.ntiles * mri::grid_tc_col_blocks(nx) * int64_t(mri::kTcStageBytes);
         g.ey_bytes = mri::grid_tc_ey_table(trig, bc, ny)
                          ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
                          : 0;
@@ -435,7 +438,7 @@ mri_status launch_grid_gather(const GridPlan& g, bool realw, int trig,
     mri_status st = MRI_OK;
     cudaEvent_t* ev = timing_slot(d);
     if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
-    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
+    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), unsigned(g.tensor_cores ? g.ncb : 1));
     if (st == MRI_OK &&
         (g.tensor_cores ? mri::launch_grid_tc(realw, trig, g.bc, gp, grid, s)
                         : mri::launch_grid(realw, trig, gp, grid, s)) != cudaSuccess)
@@ -571,8 +574,10 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
             st = cuda_fail();
         // the B tiles depend on kx and the columns only: built once
         if (st == MRI_OK && i == 0 &&
-            mri::launch_build_ex_tiles(trig, rec, fields, g.ntiles, xs, s_tab,
-                                       grid_for(g.ntiles * 512, d->sms), s) != cudaSuccess)
+            mri::launch_build_ex_tiles(trig, rec, fields, g.ntiles, xs, nx, s_tab,
+                                       grid_for(g.ntiles * mri::grid_tc_col_blocks(nx) * 512,
+                                                d->sms),
+                                       s) != cudaSuccess)
             st = cuda_fail();
         // the y factors depend on ky and the rows only: built once, by the
         // first group that reads them
@@ -588,6 +593,7 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         gp.ey_tab = g.ey_bytes > 0 ? ey_tab : nullptr;
         gp.ey_blocks = g.ey_bytes > 0 ? ny / mri::kTcRows : 0;
         gp.coils = grp.nb;
+        gp.ncb = mri::grid_tc_col_blocks(nx);
         if (g.splits == 1) {
             gp.out_r = out_r + grp.b0 * N;
             gp.out_i = out_i + grp.b0 * N;
@@ -775,7 +781,7 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
             return cuda_fail();
         return MRI_OK;
     }
-    if (!mri::grid_tc_fits(nx)) {
+    if (!mri::grid_tc_fwd_fits(nx)) {
         // expand the coordinates and take the general gather
         float* xyz = nullptr;
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
@@ -793,11 +799,13 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
     }
     // tensor cores: a CTA per 128 samples, row blocks split when too few CTAs
     const int64_t rows = int64_t(ny) * nz;
-    const int64_t row_blocks = ceil_div(rows, int64_t(mri::kTcRows));
-    const int64_t sample_tiles = ceil_div(M, int64_t(mri::kTcRows));
-    const int splits =
-        choose_splits(row_blocks, sample_tiles, d->sms > 0 ? d->sms : 1, 1, M, 1.0, 3.0);
-    const int64_t tab_bytes = row_blocks * 8 * int64_t(24 * 1024);
+    const int64_t row_blocks = ceil_div(rows, int64_t(mri::kFwRows));
+    const int ncb = mri::grid_tc_col_blocks(nx);
+    const int64_t sample_tiles = ceil_div(M, int64_t(mri::kFwSamples));
+    const int splits = choose_splits(row_blocks, sample_tiles, d->sms > 0 ? d->sms : 1, 1, M,
+                                     double(ncb), 3.0);
+    const int64_t tab_bytes =
+        row_blocks * ncb * mri::kFwKSteps * int64_t(mri::kFwChunkBytes);
     const int64_t yz_bytes = row_blocks * mri::kTcRows * 8;
     const int64_t part_bytes = splits > 1 ? int64_t(splits) * 2 * M * 4 : 0;
     char* scratch = nullptr;
@@ -812,8 +820,8 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
         reinterpret_cast<unsigned int*>(scratch + align256(tab_bytes) + align256(yz_bytes));
     float* part = reinterpret_cast<float*>(scratch + align256(tab_bytes) + align256(yz_bytes) +
                                            kBoundBytes);
-    if (mri::launch_forward_grid_prep(rRho, iRho, rows, row_blocks, ys, ny, zs, bound, tab,
-                                      yz_rows, grid_for(row_blocks * 2048, d->sms),
+    if (mri::launch_forward_grid_prep(rRho, iRho, rows, nx, row_blocks, ys, ny, zs, bound, tab,
+                                      yz_rows, grid_for(row_blocks * ncb * 2048, d->sms),
                                       s) != cudaSuccess)
         st = cuda_fail();
     mri::FwdParams fp{};
@@ -823,6 +831,8 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
     fp.M = M;
     fp.kscale = kscale_for(int(trig));
     fp.xs = xs;
+    fp.nx = nx;
+    fp.ncb = ncb;
     fp.yz_rows = yz_rows;
     fp.row_blocks = row_blocks;
     fp.splits = splits;
@@ -961,7 +971,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         if (i == 0) {
             plan->voxels_per_thread = mri::kTcRows * mri::kTcCols / mri::kTcThreads;
             plan->splits = gi.splits;
-            plan->voxel_ctas = gi.vblocks;
+            plan->voxel_ctas = gi.vblocks * gi.ncb;
         }
         rec_max = std::max(rec_max, gi.rec_bytes);
         part_max = std::max(part_max, gi.part_bytes);
