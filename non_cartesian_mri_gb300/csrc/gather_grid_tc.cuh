@@ -4,9 +4,11 @@
 //   FhD[row][ix] = sum_m Mz[row][m] * Ex[m][ix],
 //   Mz = Mu * e^{i2pi(ky y + kz z)},  Ex = e^{i2pi kx x},
 // a complex matrix product over the samples: a dense contraction.  Here a CTA
-// owns 128 grid rows (the MMA M) of a grid with nx = 128 columns (the MMA N).
-// Ex (32 samples x 128 columns per tile of 32 samples, the B operand) is the
-// same for every CTA: build_ex_tiles_kernel evaluates it once per call into
+// owns 128 grid rows (the MMA M) and one block of 128 columns (the MMA N;
+// blockIdx.z picks the block; the last block of an nx that is not a multiple
+// of 128 is padded with zero columns, which are computed and not stored).  Ex (32 samples x 128 columns per tile of 32 samples and column
+// block, the B operand) is the same for every CTA of a column block:
+// build_ex_tiles_kernel evaluates it once per call into
 // a table of operand tiles in the tensor core's shared-memory layout, and a
 // CTA fetches each tile with one TMA bulk copy.  The warps evaluate Mz (128
 // rows x 32 samples, the A operand) into tensor memory.  Every value is split
@@ -105,10 +107,13 @@ enum TcPart { A_RH = 0, A_RL, A_IH, A_IL };
 constexpr int kTcSHi = 0;
 constexpr int kTcSLo = kTcSBytes;
 
-// nx a multiple of 128 runs in column blocks of 128; nx = 64 as one block
-// with 64 columns of padding (half the MMA work idle, still far ahead of the
-// table kernel)
-inline bool grid_tc_fits(int nx) { return nx == 64 || (nx > 0 && nx % kTcCols == 0); }
+// Any nx >= 8 runs in column blocks of 128, the last one padded with zero
+// columns.  The MMA work is that of the padded width, so the rate in
+// voxel-sample pairs is nx / (128 ceil(nx / 128)) of the full one: at nx = 8
+// still about twice the general kernel's; narrower grids take the general
+// kernel on expanded coordinates.
+constexpr int kTcMinCols = 8;
+inline bool grid_tc_fits(int nx) { return nx >= kTcMinCols; }
 inline int grid_tc_col_blocks(int nx) { return (nx + kTcCols - 1) / kTcCols; }
 
 // Shape of the forward-model kernel (gather_grid_tc_fwd.cuh), which takes the
@@ -660,9 +665,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
             const int ncols = p.nx - col0 < kTcCols ? p.nx - col0 : kTcCols;
             float* o = out + row * p.nx + col0 + (wcols & 127u);
             // a thread's outputs are contiguous: 16-byte accesses when the
-            // array allows them (nx is a multiple of 64, so only the base decides)
+            // block is whole and every row starts on a 16-byte boundary
             const float keep = p.accumulate ? 1.0f : 0.0f;
-            if (ncols == kTcCols && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+            if (ncols == kTcCols && (p.nx & 3) == 0 &&
+                (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
                 float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
                 for (int j = 0; j < kTcColsPerWarp / 4; ++j) {

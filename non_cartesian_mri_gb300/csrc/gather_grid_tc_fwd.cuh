@@ -1,5 +1,5 @@
 // gather_grid_tc_fwd.cuh -- the forward model D = F rho on a separable grid,
-// on the tensor cores (nx = 64 or a multiple of 128).
+// on the tensor cores (nx >= 8).
 //
 // D[m] = sum_n rho[n] e^{-i2pi k_m . x_n} (F of Fig. 17.3) over the voxels of
 // a grid factors like F^H D does (gather_grid_tc.cuh), with the roles of the
@@ -8,8 +8,8 @@
 //   D[m]      = sum_row T[m][row] e^{-i2pi (ky y + kz z)}_row.
 // The first is a complex matrix product (samples x nx columns) by (nx
 // columns x rows): a CTA owns 128 samples (the MMA M) and walks the columns
-// in blocks of 128 (K, 8 steps of 16; nx = 64 is one block padded with
-// zeros) and, inside each, the grid rows in blocks of 128 (the MMA N,
+// in blocks of 128 (K, 8 steps of 16; the last block padded with zero
+// columns) and, inside each, the grid rows in blocks of 128 (the MMA N,
 // [T_r | T_i] = 256 columns).  A = Ex* of the CTA's samples for one column
 // block is evaluated into tensor memory (columns 0-255, f16 hi / lo parts)
 // and serves every row block; B = rho arrives per (row block, column block,

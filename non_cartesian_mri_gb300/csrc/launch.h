@@ -34,14 +34,12 @@ cudaError_t launch_mu(const float* rPhi, const float* iPhi, const float* rD, con
 
 cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s);
 
-// separable-grid path (kernels_grid.cu)
-cudaError_t launch_grid(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-// tensor-core grid path (kernels_grid_tc.cu), nx = 128
+// tensor-core grid path (kernels_grid_tc.cu), nx >= 8 in column blocks of 128
 // tensor-core grid kernel over a group of bc coils (1, or 4 / 8 for F^H D)
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s);
 cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int grid, cudaStream_t s);
-// forward model on a grid (nx = 64 or a multiple of 128) on the tensor cores:
+// forward model on a grid (nx >= 8) on the tensor cores:
 // the rho table, row coordinates and scale word, then the kernel
 cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows, int nx,
                                      int64_t row_blocks, const float* ys, int ny, const float* zs,
@@ -61,12 +59,7 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
 cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
                                   const float* xs, int nx, unsigned char* s_tab, int grid,
                                   cudaStream_t s);
-// one translation unit per grid width (kernels_grid_<nx>.cu)
-cudaError_t launch_grid_32(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-cudaError_t launch_grid_64(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-cudaError_t launch_grid_128(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-cudaError_t launch_grid_256(bool realw, int trig, const GridParams& p, dim3 grid, cudaStream_t s);
-cudaError_t launch_prep_grid(bool realw, const PrepParams& p, int grid, cudaStream_t s);
+// voxel coordinates of a grid the tensor-core kernels do not take (kernels_grid.cu)
 cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
                                int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);
 

@@ -351,19 +351,18 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
 constexpr int64_t kBoundBytes = 256;
 
 struct GridPlan {
-    bool table_kernel;      // false: coordinates expanded, general kernel
-    bool tensor_cores;      // nx = 128: the tcgen05 kernel
-    int bc;                 // tensor cores: coils per CTA
-    int ncb;                // tensor cores: column blocks of 128
+    bool tensor_cores;      // nx >= 8: the tcgen05 kernel; else coordinates
+                            // expanded and the general kernel
+    int bc;                 // coils per CTA
+    int ncb;                // column blocks of 128
     int64_t ntiles;
     int64_t vblocks;
     int rows_per_cta;
     int splits;
     int64_t rec_bytes;
     int64_t part_bytes;
-    int64_t s_bytes;        // tensor cores: the B operand tiles
-    int64_t ey_bytes;       // tensor cores, one weight, ny % 128 == 0: the Ey table
-    int ctas_per_sm;
+    int64_t s_bytes;        // the B operand tiles
+    int64_t ey_bytes;       // one weight, accurate, ny % 128 == 0: the Ey table
 };
 
 // A group of coils of a tensor-core grid call: coils b0 .. b0 + nb - 1 run in
@@ -394,54 +393,34 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int b
 {
     GridPlan g{};
     g.tensor_cores = mri::grid_tc_fits(nx);
-    g.table_kernel = g.tensor_cores || mri::grid_kernel_fits(nx);
-    if (!g.table_kernel) return g;
+    if (!g.tensor_cores) return g;
     const int64_t N = int64_t(nx) * ny * nz;
-    if (g.tensor_cores) {
-        g.bc = bc;
-        g.ncb = mri::grid_tc_col_blocks(nx);
-        g.rows_per_cta = mri::kTcRows / bc;
-        g.ntiles = ceil_div(M, mri::kTcTile);
-        g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
-        g.ctas_per_sm = 1;
-        g.splits = (g.ntiles > 0 && g.vblocks > 0)
-                       ? choose_splits(g.ntiles, g.vblocks * g.ncb, sms > 0 ? sms : 1, nb, N, 1.0,
-                                       3.0)
-                       : 1;
-        g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
-        g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
-        g.s_bytes = g.ntiles * mri::grid_tc_col_blocks(nx) * int64_t(mri::kTcStageBytes);
-        g.ey_bytes = mri::grid_tc_ey_table(trig, bc, ny)
-                         ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
-                         : 0;
-        return g;
-    }
-    g.bc = 1;
-    g.rows_per_cta = mri::kGridVoxelsPerCta / nx;
-    g.ntiles = ceil_div(M, mri::kGridTile);
+    g.bc = bc;
+    g.ncb = mri::grid_tc_col_blocks(nx);
+    g.rows_per_cta = mri::kTcRows / bc;
+    g.ntiles = ceil_div(M, mri::kTcTile);
     g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
-    const size_t smem = mri::grid_smem_bytes(nx, realw);
-    g.ctas_per_sm = smem <= 110 * 1024 ? 2 : 1;
-    const int64_t slots = int64_t(sms) * g.ctas_per_sm;
     g.splits = (g.ntiles > 0 && g.vblocks > 0)
-                   ? choose_splits(g.ntiles, g.vblocks, slots > 0 ? slots : 1, 1, N, 3.0, 1.0)
+                   ? choose_splits(g.ntiles, g.vblocks * g.ncb, sms > 0 ? sms : 1, nb, N, 1.0, 3.0)
                    : 1;
-    g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 5) * mri::kGridTile * 4;
-    g.part_bytes = g.splits > 1 ? int64_t(g.splits) * 2 * N * 4 : 0;
+    g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
+    g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
+    g.s_bytes = g.ntiles * g.ncb * int64_t(mri::kTcStageBytes);
+    g.ey_bytes = mri::grid_tc_ey_table(trig, bc, ny)
+                     ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
+                     : 0;
     return g;
 }
 
-// One gather launch of the grid kernels (timing events around it).
+// One launch of the tensor-core grid kernel (timing events around it).
 mri_status launch_grid_gather(const GridPlan& g, bool realw, int trig,
                               const mri::GridParams& gp, DeviceState* d, cudaStream_t s)
 {
     mri_status st = MRI_OK;
     cudaEvent_t* ev = timing_slot(d);
     if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
-    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), unsigned(g.tensor_cores ? g.ncb : 1));
-    if (st == MRI_OK &&
-        (g.tensor_cores ? mri::launch_grid_tc(realw, trig, g.bc, gp, grid, s)
-                        : mri::launch_grid(realw, trig, gp, grid, s)) != cudaSuccess)
+    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), unsigned(g.ncb));
+    if (st == MRI_OK && mri::launch_grid_tc(realw, trig, g.bc, gp, grid, s) != cudaSuccess)
         st = cuda_fail();
     if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
     return st;
@@ -483,8 +462,7 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         }
         return MRI_OK;
     }
-    const GridPlan g1 = plan_grid(realw, M, nx, ny, nz, d->sms);
-    if (!g1.table_kernel || (B > 1 && !g1.tensor_cores)) {
+    if (!mri::grid_tc_fits(nx)) {
         // expand the coordinates and take the general kernel
         float* xyz = nullptr;
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&xyz), size_t(3 * N) * 4, d->pool,
@@ -500,35 +478,6 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         if (cudaFreeAsync(xyz, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
         return st;
     }
-    if (!g1.tensor_cores) {
-        // table kernel, one weight
-        const GridPlan& g = g1;
-        char* scratch = nullptr;
-        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                    size_t(align256(g.rec_bytes) + g.part_bytes), d->pool,
-                                    s) != cudaSuccess)
-            return cuda_fail();
-        float* rec = reinterpret_cast<float*>(scratch);
-        float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
-        mri_status st = MRI_OK;
-        mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, g.ntiles, kscale_for(trig), rec};
-        if (mri::launch_prep_grid(realw, pp, grid_for(g.ntiles * mri::kGridTile, d->sms), s) !=
-            cudaSuccess)
-            st = cuda_fail();
-        mri::GridParams gp = grid_params(g, rec, xs, nx, ys, ny, zs, nz, d);
-        gp.out_r = g.splits == 1 ? out_r : part;
-        gp.out_i = g.splits == 1 ? out_i : part + N;
-        gp.split_stride = g.splits == 1 ? 0 : 2 * N;
-        gp.accumulate = g.splits == 1 ? accumulate : 0;
-        if (st == MRI_OK) st = launch_grid_gather(g, realw, trig, gp, d, s);
-        if (st == MRI_OK && g.splits > 1 &&
-            mri::launch_reduce(part, g.splits, 1, N, out_r, out_i, N, accumulate,
-                               grid_for(2 * N, d->sms), s) != cudaSuccess)
-            st = cuda_fail();
-        if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
-        return st;
-    }
-
     // tensor cores: coil groups sharing one table of B operand tiles
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
     std::vector<GridPlan> plans;
@@ -941,26 +890,17 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         return MRI_OK;
     }
     const GridPlan g = plan_grid(realw, M, nx, ny, nz, num_sms);
-    if (!g.table_kernel || (B > 1 && !g.tensor_cores)) {
+    if (!g.tensor_cores) {
         // expanded coordinates, then the general plan
         st = mri_plan_gather(B > 1 ? MRI_KIND_FHD_BATCHED : kind, B, M, N, num_sms, plan);
         plan->launches += 1;
         plan->scratch_bytes += 3 * N * 4;
         return st;
     }
-    plan->threads_per_cta = g.tensor_cores ? mri::kTcThreads : mri::kGridThreads;
-    plan->samples_per_tile = g.tensor_cores ? mri::kTcTile : mri::kGridTile;
+    plan->threads_per_cta = mri::kTcThreads;
+    plan->samples_per_tile = mri::kTcTile;
     plan->tiles = g.ntiles;
-    plan->tensor_cores = g.tensor_cores ? 1 : 0;
-    if (!g.tensor_cores) {
-        plan->voxels_per_thread = mri::kGridV;
-        plan->splits = g.splits;
-        plan->voxel_ctas = g.vblocks;
-        plan->coil_groups = 1;
-        plan->launches = 2 + (g.splits > 1 ? 1 : 0);
-        plan->scratch_bytes = align256(g.rec_bytes) + g.part_bytes;
-        return MRI_OK;
-    }
+    plan->tensor_cores = 1;
     // tensor cores: per coil group a prep, a gather and (split) a reduction,
     // plus one build of the B tiles; the first group's shape is reported
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);

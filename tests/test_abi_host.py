@@ -176,13 +176,14 @@ def test_batched_grid_plan_groups(lib):
         assert p.samples_per_tile * p.tiles >= 524288
     p = Plan()
     assert f(0, 1000, 128, 4, 4, 152, ctypes.byref(p)) == SIZE
-    assert f(3, 1000, 96, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 0
-    # nx = 64 (one padded block) and multiples of 128 run on the tensor cores,
-    # one CTA column per 128 columns
-    assert f(3, 1000, 64, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1
-    c64 = p.voxel_ctas
-    assert f(3, 1000, 384, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1
-    assert p.voxel_ctas == 3 * c64
+    assert f(3, 1000, 7, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 0
+    # nx >= 8 runs on the tensor cores, one CTA column per block of 128
+    # columns (the last one padded)
+    assert f(3, 1000, 8, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1
+    c8 = p.voxel_ctas
+    assert f(3, 1000, 64, 4, 4, 152, ctypes.byref(p)) == OK and p.voxel_ctas == c8
+    assert f(3, 1000, 257, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1
+    assert p.voxel_ctas == 3 * c8
     assert lib.mri_plan_grid(2, 1000, 128, 4, 4, 152, ctypes.byref(p)) == MODE
 
 

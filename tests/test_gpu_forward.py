@@ -167,14 +167,14 @@ def test_forward_grid_scale_is_exact(mri, k):
 
 
 def test_forward_grid_fallback_and_empty(mri):
-    """nx = 96 goes through expanded coordinates and mri_forward."""
+    """nx = 6 goes through expanded coordinates and mri_forward."""
     w = wl.make_workload("fhd_64")
     M = 1500
-    xs = (np.arange(96) - 48).astype(np.float32)
+    xs = np.array([-30.0, -7.5, 0.0, 2.0, 19.0, 31.0], np.float32)
     ys = np.array([-5.0, 9.0], np.float32)
     zs = np.array([3.0, -8.0, 12.0], np.float32)
     rng = np.random.default_rng(51)
-    rho = (rng.standard_normal(96 * 6) + 1j * rng.standard_normal(96 * 6)).astype(np.complex64)
+    rho = (rng.standard_normal(6 * 6) + 1j * rng.standard_normal(6 * 6)).astype(np.complex64)
     k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
     r, i = mri.forward_grid(*k, dev(xs), dev(ys), dev(zs), dev(rho.real), dev(rho.imag),
                             trig="accurate")

@@ -1,9 +1,10 @@
 """The separable-grid path (mri_fhd_grid / mri_q_grid) against the oracle.
 
 The oracle gets the expanded voxel coordinates of the same grid; tolerances
-as for the general path (1e-5 accurate, 2e-4 fast).  Covers the table kernel
-(nx in 16..256), the fallback through expanded coordinates (other nx), ragged
-row counts, ragged sample counts, non-uniform axes and accumulate.
+as for the general path (1e-5 accurate, 2e-4 fast).  Covers the tensor-core
+kernel (nx >= 8: whole and padded column blocks), the fallback through
+expanded coordinates (nx < 8), ragged row counts, ragged sample counts,
+non-uniform axes and accumulate.
 """
 
 import numpy as np
@@ -68,7 +69,7 @@ def test_q_grid_128(mri, trig):
 
 @pytest.mark.parametrize("nx,ny,nz", [(16, 3, 5), (32, 7, 1), (256, 5, 3), (128, 17, 2),
                                       (64, 1, 1), (100, 4, 3), (8, 9, 9), (1, 40, 3),
-                                      (300, 2, 2)])
+                                      (7, 5, 4), (300, 2, 2)])
 @pytest.mark.parametrize("M", [1, 33, 1000])
 def test_grid_shapes(mri, nx, ny, nz, M):
     rng = np.random.default_rng(nx * 1000 + ny * 10 + nz + M)

@@ -1,7 +1,9 @@
-"""Edge shapes of the tensor-core grid paths (nx = 128) against the oracle:
-one sample, one row, sample counts just under / over a tile, row counts just
-over a block, a padded coil group.  Every entry point that runs on the
-tensor cores: F^H D, Q, batched F^H D, the forward model."""
+"""Edge shapes of the tensor-core grid paths against the oracle: one sample,
+one row, sample counts just under / over a tile, row counts just over a
+block, a padded coil group; at nx = 128 (one whole column block), nx = 9
+(one mostly padded block, rows not 16-byte aligned: scalar stores) and
+nx = 200 (a whole block and a partial one).  Every entry point that runs on
+the tensor cores: F^H D, Q, batched F^H D, the forward model."""
 
 import numpy as np
 import pytest
@@ -14,6 +16,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = {"accurate": 1e-5, "fast": 2e-4}
 SHAPES = [(1, 1, 1), (1, 1, 31), (2, 3, 33), (5, 1, 64), (130, 1, 100), (1, 129, 257)]
+WIDTHS = [128, 9, 200]
 
 
 @pytest.fixture(scope="module")
@@ -32,10 +35,13 @@ def cplx(r, i):
     return r.cpu().numpy().astype(np.float64) + 1j * i.cpu().numpy()
 
 
-def case(ny, nz, M, seed):
+def case(nx, ny, nz, M, seed):
     rng = np.random.default_rng(seed)
     k = rng.uniform(-0.5, 0.5, (3, M)).astype(np.float32)
-    xs = (np.arange(128) - 64).astype(np.float32)
+    if nx == 128:
+        xs = (np.arange(128) - 64).astype(np.float32)
+    else:
+        xs = np.sort(rng.uniform(-64.0, 64.0, nx)).astype(np.float32)
     ys = (rng.permutation(256)[:ny] - 128).astype(np.float32) * 0.5
     zs = (rng.permutation(256)[:nz] - 128).astype(np.float32) * 0.5
     z, y, x = (a.reshape(-1) for a in np.meshgrid(zs, ys, xs, indexing="ij"))
@@ -50,8 +56,9 @@ def rel(got, ref):
 
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
 @pytest.mark.parametrize("ny,nz,M", SHAPES)
-def test_fhd_and_q_grid_shapes(mri, ny, nz, M, trig):
-    k, xs, ys, zs, x, y, z, w, _ = case(ny, nz, M, ny * 1000 + nz * 10 + M)
+@pytest.mark.parametrize("nx", WIDTHS)
+def test_fhd_and_q_grid_shapes(mri, nx, ny, nz, M, trig):
+    k, xs, ys, zs, x, y, z, w, _ = case(nx, ny, nz, M, nx + ny * 1000 + nz * 10 + M)
     kk = [dev(a) for a in k]
     axes = [dev(xs), dev(ys), dev(zs)]
     r, i = mri.fhd_grid(*kk, *axes, *[dev(a) for a in w], trig=trig)
@@ -63,8 +70,9 @@ def test_fhd_and_q_grid_shapes(mri, ny, nz, M, trig):
 
 
 @pytest.mark.parametrize("ny,nz,M", SHAPES)
-def test_batched_grid_shapes(mri, ny, nz, M):
-    k, xs, ys, zs, x, y, z, w, rng = case(ny, nz, M, 7 + ny + nz + M)
+@pytest.mark.parametrize("nx", WIDTHS)
+def test_batched_grid_shapes(mri, nx, ny, nz, M):
+    k, xs, ys, zs, x, y, z, w, rng = case(nx, ny, nz, M, 7 + nx + ny + nz + M)
     B = 5                                   # one padded group of 8
     rD = rng.standard_normal((B, M)).astype(np.float32)
     iD = rng.standard_normal((B, M)).astype(np.float32)
@@ -77,9 +85,10 @@ def test_batched_grid_shapes(mri, ny, nz, M):
 
 
 @pytest.mark.parametrize("ny,nz,M", SHAPES)
-def test_forward_grid_shapes(mri, ny, nz, M):
-    k, xs, ys, zs, x, y, z, _, rng = case(ny, nz, M, 99 + ny + nz + M)
-    n = 128 * ny * nz
+@pytest.mark.parametrize("nx", WIDTHS)
+def test_forward_grid_shapes(mri, nx, ny, nz, M):
+    k, xs, ys, zs, x, y, z, _, rng = case(nx, ny, nz, M, 99 + nx + ny + nz + M)
+    n = nx * ny * nz
     rho = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
     r, i = mri.forward_grid(*[dev(a) for a in k], dev(xs), dev(ys), dev(zs), dev(rho.real),
                             dev(rho.imag), trig="accurate")
