@@ -37,6 +37,32 @@ mri_status mri_microbench(int which, int ctas_per_sm, int threads, int64_t iters
                           unsigned long long* cycles, float* sink, void* stream);
 
 /*
+ * Tensor-core issue-rate probe: the ceiling of the MMA form the tensor-core
+ * grid kernels use (mri_fhd_grid and friends), with nothing else running.
+ * Launches one CTA per SM (128 threads; at least 128 KB of shared memory so
+ * that no second CTA fits; all 512 tensor-memory columns) on `stream`.
+ * Thread 0 issues `tiles` times the 12 tcgen05.mma.cta_group::1.kind::f16 of
+ * 128 x 256 x 16 that one 32-sample tile of the grid kernel takes, one
+ * tcgen05.commit per tile, every wait bounded (a wait that gives up sets bit
+ * 0x1 of the device error word):
+ *   mode 0: A and B from shared memory (zeros), at most two tiles in flight;
+ *   mode 1: A from tensor memory, B from shared memory (zeros), likewise;
+ *   mode 2: A from tensor memory, B brought per tile by one 48 KB TMA bulk
+ *           copy (tile t from b_tab + (t mod b_tiles) * 49152, 16-byte
+ *           aligned device memory) into a ring of 4 stages, copies issued two
+ *           tiles ahead, as the grid kernel streams its B-operand table.
+ * b_tab / b_tiles are read in mode 2 only.  cycles[cta] (device, one uint64
+ * per SM) receives the SM clock cycles from the first issue to the last
+ * completion.  One tile is 32 samples x 128 x 128 voxels = 524,288
+ * voxel-sample pairs, so the ceiling in pairs per SM per clock is
+ * tiles * 524288 / cycles.  MRI_ERR_MODE for mode outside 0..2, MRI_ERR_NULL
+ * for a missing array, MRI_ERR_SIZE for tiles outside 1 .. 2^22, b_tiles < 1
+ * or an unaligned b_tab (mode 2), MRI_ERR_UNSUPPORTED_DEVICE off sm_103.
+ */
+mri_status mri_mma_probe(int mode, int tiles, const void* b_tab, int64_t b_tiles,
+                         unsigned long long* cycles, void* stream);
+
+/*
  * Failure-detection self-test (no counterpart on the pages).  Every wait in
  * the gather kernels (an mbarrier for a TMA copy or for the tensor core) is
  * bounded: after 1 s it gives up, sets a bit in the device error word that

@@ -8,7 +8,7 @@ The CUDA library is built with ``non_cartesian_mri_gb300.build.build()``.
 
 _API = ("mu", "fhd", "q", "fhd_batched", "forward", "forward_grid", "fhd_grid", "q_grid", "fhd_batched_grid", "plan",
         "plan_grid", "plan_grid_batched",
-        "device_errors", "microbench", "wait_selftest",
+        "device_errors", "microbench", "mma_probe", "wait_selftest",
         "status_string", "MriError", "load", "lib_path", "TRIG", "gather_timing")
 
 

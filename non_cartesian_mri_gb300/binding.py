@@ -82,6 +82,8 @@ def load():
         lib.mri_device_errors.restype = ctypes.c_int
         lib.mri_microbench.argtypes = [I, I, I, I64, P, P, P]
         lib.mri_wait_selftest.argtypes = [I, P]
+        lib.mri_mma_probe.argtypes = [I, I, P, I64, P, P]
+        lib.mri_mma_probe.restype = ctypes.c_int
         lib.mri_wait_selftest.restype = ctypes.c_int
         lib.mri_microbench.restype = ctypes.c_int
         lib.mri_fhd_grid.argtypes = ([P] * 3 + [P, I, P, I, P, I] + [P] * 4
@@ -422,4 +424,24 @@ def microbench(which: str, ctas_per_sm: int = 4, threads: int = 256, iters: int 
     ops_per_sm = ctas_per_sm * threads * iters * 8
     return {"probe": which, "per_sm_per_clk": float(ops_per_sm / cyc.median()),
             "per_sm_per_clk_min": float(ops_per_sm / cyc.max()),
+            "cycles_median": float(cyc.median()), "sms": sms}
+
+
+def mma_probe(mode: int = 1, tiles: int = 4096, b_tiles: int = 1024):
+    """Pairs per SM per clock of the tensor-core grid kernel's MMA issue
+    pattern alone (mode 0: A and B in shared memory; 1: A in tensor memory;
+    2: A in tensor memory, B streamed by TMA from a table of b_tiles 48 KB
+    tiles; see mri_mma_probe in mri_microbench.h)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=dev)
+    tab = torch.zeros(int(b_tiles) * 49152 if mode == 2 else 16, dtype=torch.uint8, device=dev)
+    _check(load().mri_mma_probe(int(mode), int(tiles), _ptr(tab), int(b_tiles), _ptr(cycles),
+                                _stream_handle(None)), "mri_mma_probe")
+    torch.cuda.synchronize(dev)
+    cyc = cycles.double()
+    pairs = float(tiles) * 32 * 128 * 128
+    return {"mode": int(mode), "tiles": int(tiles), "b_tiles": int(b_tiles),
+            "pairs_per_sm_per_clk": float(pairs / cyc.median()),
+            "pairs_per_sm_per_clk_min": float(pairs / cyc.max()),
             "cycles_median": float(cyc.median()), "sms": sms}

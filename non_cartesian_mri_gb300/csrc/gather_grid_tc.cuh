@@ -22,8 +22,16 @@
 // product, so every product keeps close to fp32 accuracy.  f16 has a narrow
 // exponent range: the weights are multiplied (once per call, in the records)
 // by a power of two chosen from the largest |w_r| + |w_i| of the call so that
-// every |A| < 2^15, and the results are multiplied back exactly; |B| <= 1
-// needs no scale.
+// every weighted operand is below 2^15, and the results are multiplied back
+// exactly; the phase factors (|e^{i phi}| = 1) need no scale.
+//
+// Where the weight goes.  With one coil per CTA (F^H D, Q) the weight Mu is
+// folded into the B table (B = Mu e^{i2pi kx x}, once per call), and A is the
+// bare row factor e^{i2pi(ky y + kz z)}: per (row, sample) element the CTA
+// evaluates one sin/cos pair and splits it, with no weight loads and no
+// complex multiply -- operand generation, not the tensor core, is what a
+// tile waits for.  With a coil group (batched F^H D) B is shared by the
+// group's coils, so A = Mu_coil e^{i2pi(ky y + kz z)} as written above.
 //
 // Shared-memory bandwidth binds a kernel whose operands all pass through
 // shared memory (operand writes plus operand reads by the tensor core); with
@@ -247,17 +255,20 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 }
 
 // The B operand tiles: tile t holds, for every grid column c and sample s of
-// record tile t, the f16 hi / lo parts of -sin, cos and sin of the phase
-// kx[s] x[c] in S = [-B_i; B_r; B_i] row order (hi block, then lo block),
-// each block K-major as the MMA reads it.  One thread per (tile, 8-row
-// group, 8-sample chunk, row): consecutive threads write consecutive 16-byte
-// core-matrix rows, so a warp's stores are contiguous.
-template <int TRIG>
+// record tile t, the f16 hi / lo parts of B = e^{i phase(kx[s] x[c])} (MUB:
+// B = w[s] e^{i phase(kx[s] x[c])}, the sample's scaled weight folded in) as
+// -B_i, B_r and B_i in S = [-B_i; B_r; B_i] row order (hi block, then lo
+// block), each block K-major as the MMA reads it.  One thread per (tile,
+// 8-row group, 8-sample chunk, row): consecutive threads write consecutive
+// 16-byte core-matrix rows, so a warp's stores are contiguous.
+template <int TRIG, bool MUB>
 __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, int fields,
                                                              int64_t ntiles, const float* xs,
                                                              int nx, int ncb,
                                                              unsigned char* s_tab)
 {
+    // MUB: one weight per sample (fields 3, and 4 unless the weight is real)
+    const bool complex_w = fields > 4;
     constexpr int ITEMS = kTcCols * kTcTile / 8;       // 512 (column, chunk) items per tile
     const int64_t total = ntiles * ncb * ITEMS;
     for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
@@ -274,6 +285,16 @@ __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, i
         float br[8], bi[8];
 #pragma unroll
         for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+        if constexpr (MUB) {
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) {
+                const float wr = kx[3 * kTcTile + s8];
+                const float wi = complex_w ? kx[4 * kTcTile + s8] : 0.0f;
+                const float c = br[s8], sn = bi[s8];
+                br[s8] = fmaf(wr, c, -wi * sn);
+                bi[s8] = fmaf(wr, sn, wi * c);
+            }
+        }
         unsigned char* const tile = s_tab + tc * kTcStageBytes;
         const int off = tc_kmaj_bytes(gi, kc);        // == 16 r
         uint4 h, l;
@@ -418,15 +439,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
         if constexpr (EYT)
             for (; ey_loaded < 2 && ey_loaded < nt; ++ey_loaded) load_ey(ey_loaded);
     }
-    // EYT: e[s] = Mu[s] e^{i phase(kz[s] z)} of this CTA's plane, by warp 0
+    // EYT: e[s] = e^{i phase(kz[s] z)} of this CTA's plane (the weight is in
+    // the B table), by warp 0
     auto z_factors = [&](const float* rec, float2* e) {
         if (warp == 0) {
             const int s = lane;
             float sn, cs;
             table_sincos<TRIG>(rec[2 * T + s] * z_plane, sn, cs);
-            const float wr = rec[3 * T + s];
-            const float wi = REALW ? 0.0f : rec[4 * T + s];
-            e[s] = make_float2(fmaf(wr, cs, -wi * sn), fmaf(wi, cs, wr * sn));
+            e[s] = make_float2(cs, sn);
         }
     };
 
@@ -492,7 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                 const int s0 = 8 * (kTcAChunks * ah + c);
                 float ar[8], ai[8];
                 if constexpr (EYT) {
-                    // Mz = (Mu e^{i phase(kz z)}) e^{i phase(ky y)}
+                    // A = e^{i phase(kz z)} e^{i phase(ky y)}
                     const float2* ez = e_sh + (t & 1) * T;
                     const float2* ey = ey_sh + (t & 1) * (T * kTcRows);
 #pragma unroll
@@ -503,25 +523,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gather_grid_tc_kernel(GridParam
                         ai[s8] = fmaf(f.x, e.y, f.y * e.x);
                     }
                 } else if constexpr (BC == 1) {
-                    float ky[8], kz[8], wr[8], wi[8];
+                    // A = e^{i phase(ky y + kz z)} (the weight is in the B table)
+                    float ky[8], kz[8];
                     tc_load8(rec, 1, s0, ky);
                     tc_load8(rec, 2, s0, kz);
-                    tc_load8(rec, 3, s0, wr);
-                    if (!REALW) tc_load8(rec, 4, s0, wi);
 #pragma unroll
-                    for (int s8 = 0; s8 < 8; ++s8) {
-                        float sn, cs;
-                        table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), sn, cs);
-                        const float swr = wr[s8];
-                        if (REALW) {
-                            ar[s8] = swr * cs;
-                            ai[s8] = swr * sn;
-                        } else {
-                            const float swi = wi[s8];
-                            ar[s8] = fmaf(swr, cs, -swi * sn);
-                            ai[s8] = fmaf(swi, cs, swr * sn);
-                        }
-                    }
+                    for (int s8 = 0; s8 < 8; ++s8)
+                        table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), ai[s8], ar[s8]);
                 } else {
                     // Mu of this thread's coil times the row's shared factor
                     const float2* e = e_sh + (t & 1) * T * RC;

@@ -1,14 +1,38 @@
 // kernels_grid_tc.cu -- tensor-core separable-grid kernels (gather_grid_tc.cuh).
 #include "gather_grid_tc.cuh"
 #include "gather_grid_tc_fwd.cuh"
+#include "gather_grid_tc_ws.cuh"
 #include "launch.h"
+
+#ifndef MRI_TC_WS
+#define MRI_TC_WS 1   // single-weight launches without the Ey table take the warp-role kernel
+#endif
 
 namespace mri {
 
 namespace {
+template <bool REALW, int TRIG>
+cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
+{
+    auto kernel = gather_grid_tc_ws_kernel<REALW, TRIG>;
+    // the warpgroup register budgets must fit the registers the CTA is
+    // launched with, or a budget increase would wait forever
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kWsThreads < 32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs)
+        return cudaErrorInvalidConfiguration;
+    const size_t smem = grid_tc_ws_smem_bytes(REALW);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kWsThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int BC, bool REALW, int TRIG, bool EYT>
 cudaError_t run(const GridParams& p, dim3 grid, cudaStream_t s)
 {
+    if constexpr (BC == 1 && !EYT && MRI_TC_WS) return run_ws<REALW, TRIG>(p, grid, s);
     const size_t smem = grid_tc_smem_bytes(REALW, BC, EYT);
     const cudaError_t attr = cudaFuncSetAttribute(
         gather_grid_tc_kernel<BC, REALW, TRIG, EYT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -80,27 +104,27 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* xs, int nx, unsigned char* s_tab, int grid,
-                                  cudaStream_t s)
+cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,
+                                  int64_t ntiles, const float* xs, int nx, unsigned char* s_tab,
+                                  int grid, cudaStream_t s)
 {
     const int ncb = grid_tc_col_blocks(nx);
+    auto go = [&](auto kernel) {
+        kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx, ncb, s_tab);
+        return cudaGetLastError();
+    };
     switch (trig) {
         case TRIG_ACCURATE:
-            build_ex_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx,
-                                                                     ncb, s_tab);
-            break;
+            return mub ? go(build_ex_tiles_kernel<TRIG_ACCURATE, true>)
+                       : go(build_ex_tiles_kernel<TRIG_ACCURATE, false>);
         case TRIG_FAST:
-            build_ex_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx, ncb,
-                                                                 s_tab);
-            break;
+            return mub ? go(build_ex_tiles_kernel<TRIG_FAST, true>)
+                       : go(build_ex_tiles_kernel<TRIG_FAST, false>);
         case TRIG_FAST_RR:
-            build_ex_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx,
-                                                                    ncb, s_tab);
-            break;
-        default: return cudaErrorInvalidValue;
+            return mub ? go(build_ex_tiles_kernel<TRIG_FAST_RR, true>)
+                       : go(build_ex_tiles_kernel<TRIG_FAST_RR, false>);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cudaStream_t s)

@@ -55,10 +55,11 @@ bool grid_tc_ey_table(int trig, int bc, int ny);
 cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
                                   const float* ys, int ny, float2* ey_tab, int grid,
                                   cudaStream_t s);
-// B operand tiles of the tensor-core grid kernel from its records (kx) and xs
-cudaError_t launch_build_ex_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* xs, int nx, unsigned char* s_tab, int grid,
-                                  cudaStream_t s);
+// B operand tiles of the tensor-core grid kernel from its records (kx) and
+// xs; mub: times the records' (scaled) weight, for single-coil launches
+cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,
+                                  int64_t ntiles, const float* xs, int nx, unsigned char* s_tab,
+                                  int grid, cudaStream_t s);
 // voxel coordinates of a grid the tensor-core kernels do not take (kernels_grid.cu)
 cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
                                int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);

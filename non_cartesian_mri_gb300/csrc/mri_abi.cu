@@ -521,9 +521,12 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
                                       grid_for(g.ntiles * (fields - 3) * mri::kTcTile, d->sms),
                                       s) != cudaSuccess)
             st = cuda_fail();
-        // the B tiles depend on kx and the columns only: built once
-        if (st == MRI_OK && i == 0 &&
-            mri::launch_build_ex_tiles(trig, rec, fields, g.ntiles, xs, nx, s_tab,
+        // the B tiles of a coil group depend on kx and the columns only: built
+        // once and shared; a single-coil launch carries its weight in B, so
+        // its table is built from its own records (in place: the launches
+        // before it on this stream are done with the old one)
+        if (st == MRI_OK && (i == 0 || grp.bc == 1) &&
+            mri::launch_build_ex_tiles(trig, grp.bc == 1, rec, fields, g.ntiles, xs, nx, s_tab,
                                        grid_for(g.ntiles * mri::grid_tc_col_blocks(nx) * 512,
                                                 d->sms),
                                        s) != cudaSuccess)
@@ -901,8 +904,9 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
     plan->samples_per_tile = mri::kTcTile;
     plan->tiles = g.ntiles;
     plan->tensor_cores = 1;
-    // tensor cores: per coil group a prep, a gather and (split) a reduction,
-    // plus one build of the B tiles; the first group's shape is reported
+    // tensor cores: per coil group a prep, a scale, a gather and (split) a
+    // reduction, plus one build of the B tiles (and one more for a trailing
+    // single coil); the first group's shape is reported
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
     int64_t rec_max = 0, part_max = 0;
     plan->launches = 1;
@@ -916,6 +920,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         rec_max = std::max(rec_max, gi.rec_bytes);
         part_max = std::max(part_max, gi.part_bytes);
         plan->launches += 3 + (gi.splits > 1 ? 1 : 0);   // prep, scale, gather (+ reduce)
+        if (i > 0 && groups[i].bc == 1) plan->launches += 1;   // its own B tiles
     }
     plan->coil_groups = int(groups.size());
     plan->scratch_bytes = align256(rec_max) + kBoundBytes + align256(part_max) + g.s_bytes;

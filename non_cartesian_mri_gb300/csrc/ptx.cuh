@@ -276,6 +276,22 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v)
                  : "memory");
 }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same one): dec returns registers to the CTA's pool, inc waits until the
+// pool holds enough.  The budgets of all warpgroups must add up to no more
+// than the registers the CTA was launched with, or an inc waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
