@@ -1,12 +1,23 @@
 // gather_grid_tc_ws.cuh -- the tensor-core grid F^H D / Q kernel with warp
-// roles (one weight per CTA, row factors evaluated per element).
+// roles.
 //
 // Same arithmetic as gather_grid_tc_kernel (gather_grid_tc.cuh): per tile of
-// 32 samples, A = e^{i2pi(ky y + kz z)} of the CTA's 128 grid rows goes to
-// tensor memory (f16 hi / lo parts), B = Mu e^{i2pi kx x} of one block of 128
-// columns comes from the per-call table by TMA, and 12 tcgen05.mma of
-// 128 x 256 x 16 add A B into D; D is folded into running sums in registers
-// every block of tiles (blocked summation).
+// 32 samples, A (128 MMA rows: BC coils x 128 / BC grid rows) goes to tensor
+// memory as f16 hi / lo parts, B (one block of 128 columns) comes from the
+// per-call table by TMA, and 12 tcgen05.mma of 128 x 256 x 16 add A B into
+// D; D is folded into running sums in registers every block of tiles
+// (blocked summation).  A per case:
+//   BC = 1:         A = e^{i2pi(ky y + kz z)} (the weight is in the B table),
+//                   one sin/cos per element;
+//   BC = 1, EYT:    A = e^{i2pi kz z} e^{i2pi ky y}: the y factor from the
+//                   per-call Ey table (TMA, one tile of 32 x 128 per record
+//                   tile), the z factor once per sample (lane s of every
+//                   generator warp evaluates sample s, shuffled to the rows);
+//   BC = 4 or 8:    A = Mu_coil e^{i2pi(ky y + kz z)}: the row factor of each
+//                   (grid row, sample) evaluated once into shared memory one
+//                   tile ahead, by all generator threads (a named barrier of
+//                   the generator warps makes it visible), times each coil's
+//                   weight.
 //
 // What differs is who waits for whom.  tcgen05.mma is issued by one thread
 // and stalls that thread while the tensor core's instruction queue is full
@@ -51,11 +62,32 @@ static_assert(32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs <= kWsThreads * k
               "warpgroup register budgets exceed the launch");
 static_assert(kWsGenWarps == kTcWarps, "generator warps map the D columns as the barrier kernel");
 
-inline size_t grid_tc_ws_smem_bytes(bool realw)
+inline size_t grid_tc_ws_smem_bytes(bool realw, int bc, bool eyt)
 {
-    const int F = realw ? 4 : 5;
-    return size_t(kTcStages) * kTcStageBytes + size_t(kStages) * F * kTcTile * 4 +
-           size_t(kTcRows) * 8;
+    const int F = realw ? 4 : 3 + 2 * bc;
+    const int rc = kTcRows / bc;
+    size_t b = size_t(eyt ? kTcStagesEy : kTcStages) * kTcStageBytes;   // B operand stages
+    if (eyt) b += size_t(2) * kTcEyBytes;                               // Ey tiles
+    b += size_t(kStages) * F * kTcTile * 4;                             // record ring
+    b += size_t(rc) * 8;                                                // (y, z) of the rows
+    if (bc > 1) b += size_t(2) * kTcTile * rc * 8;                      // row factors, two tiles
+    return b;
+}
+
+// Barrier of the generator warps alone (named barrier 1; 0 is __syncthreads)
+// that also returns whether `v` holds in every generator thread.  Every
+// generator warp reaches it the same number of times: a failure is carried
+// to the next one as v = false, and all leave together.
+__device__ __forceinline__ bool ws_gen_sync_and(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(v)), "n"(32 * kWsGenWarps)
+        : "memory");
+    return r != 0;
 }
 
 // Bounded wait that also gives up once any role of the CTA has given up.
@@ -73,12 +105,15 @@ __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile
     }
 }
 
-template <bool REALW, int TRIG>
+template <int BC, bool REALW, int TRIG, bool EYT>
 __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridParams p)
 {
-    constexpr int kS = kTcStages;                     // A / B stages
+    static_assert(!EYT || BC == 1, "Ey table for single-weight calls");
+    static_assert(BC == 1 || (!REALW && (BC == 4 || BC == 8)), "coil group");
+    constexpr int kS = EYT ? kTcStagesEy : kTcStages;   // A / B stages
     constexpr int T = kTcTile;
-    constexpr int F = REALW ? 4 : 5;
+    constexpr int F = REALW ? 4 : 3 + 2 * BC;
+    constexpr int RC = kTcRows / BC;                  // grid rows per CTA
     constexpr uint32_t TILE_BYTES = uint32_t(F) * T * 4;
     constexpr uint32_t ID = umma_idesc_f16(kTcRows, 2 * kTcCols);   // N = 256
     constexpr int drain_tiles = (TRIG == TRIG_ACCURATE) ? kTcDrainAccurate : kTcDrainFast;
@@ -86,14 +121,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const ops = smem_raw;
-    float* const ring = reinterpret_cast<float*>(ops + kS * kTcStageBytes);
+    float2* const ey_sh = reinterpret_cast<float2*>(ops + kS * kTcStageBytes);   // EYT: 2 tiles
+    float* const ring = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ey_sh) +
+                                                 (EYT ? 2 * kTcEyBytes : 0));
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
+    float2* const e_sh = yz_sh + RC;                  // BC > 1: row factors of two tiles
     __shared__ __align__(8) uint64_t full_bar[kStages];   // record tile landed
     __shared__ __align__(8) uint64_t rec_free[kStages];   // record tile read by every generator
     __shared__ __align__(8) uint64_t s_bar[kS];           // B tile landed
     __shared__ __align__(8) uint64_t a_full[kS];          // A tile written by every generator
     __shared__ __align__(8) uint64_t mma_bar[kS];         // MMAs of the tile done
     __shared__ __align__(8) uint64_t d_free;              // D folded by every generator
+    __shared__ __align__(8) uint64_t ey_bar[2];           // EYT: Ey tile landed
+    __shared__ __align__(8) uint64_t ey_free[2];          // EYT: Ey tile read by every generator
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     volatile int* const abort_flag = &abort_sh;
@@ -106,9 +146,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
     const int64_t t_end = (p.ntiles * (split + 1)) / p.splits;
     const int nt = int(t_end - t_begin);
     const int64_t total_rows = int64_t(p.ny) * p.nz;
-    const int64_t row0 = int64_t(blockIdx.x) * kTcRows;
+    const int64_t row0 = int64_t(blockIdx.x) * RC;
 
-    for (int r = tid; r < kTcRows; r += kWsThreads) {
+    for (int r = tid; r < RC; r += kWsThreads) {
         const int64_t row = row0 + r;
         float2 yz = make_float2(0.f, 0.f);
         if (row < total_rows) {
@@ -132,6 +172,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             mbar_init(&mma_bar[i], 1);
         }
         mbar_init(&d_free, kWsGenWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ey_bar[i], 1);
+            mbar_init(&ey_free[i], kWsGenWarps);
+        }
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -188,8 +232,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                 atomicOr(p.err, DEVERR_DRAIN_TIMEOUT);
             if (issued < nt) atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
         } else if (warp == kWsGenWarps + 1 && lane == 0) {
-            // ---- copies: record tile u and B tile u ----
-            int r_issued = 0, b_issued = 0;
+            // ---- copies: record tile u, B tile u (and Ey tile u) ----
+            // EYT: this CTA's 128 rows are grid rows iy0 .. iy0 + 127 of one plane
+            const int64_t ey_block = EYT ? (row0 % p.ny) / kTcRows : 0;
+            int r_issued = 0, b_issued = 0, e_issued = 0;
             for (int u = 0; u < nt; ++u) {
                 bool ok = true;
                 if (u >= kStages)
@@ -208,6 +254,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                              p.s_tab + ((t_begin + u) * p.ncb + blockIdx.z) * kTcStageBytes,
                              uint32_t(kTcStageBytes), &s_bar[u % kS]);
                 b_issued = u + 1;
+                if constexpr (EYT) {
+                    if (u >= 2) ok = ws_wait(&ey_free[u & 1], uint32_t((u - 2) >> 1) & 1u, abort_flag);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&ey_bar[u & 1], uint32_t(kTcEyBytes));
+                    tma_bulk_g2s(ey_sh + (u & 1) * (T * kTcRows),
+                                 p.ey_tab + ((t_begin + u) * p.ey_blocks + ey_block) * (T * kTcRows),
+                                 uint32_t(kTcEyBytes), &ey_bar[u & 1]);
+                    e_issued = u + 1;
+                }
             }
             // the latest copy into each slot and stage lands before shared
             // memory is released, whatever the other roles did (the copy
@@ -220,17 +275,24 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             for (int u = b_issued > kS ? b_issued - kS : 0; u < b_issued; ++u)
                 if (!mbar_wait_bounded(&s_bar[u % kS], uint32_t(u / kS) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
-            if (b_issued < nt) bits |= DEVERR_TILE_WAIT_TIMEOUT;
+            for (int u = e_issued > 2 ? e_issued - 2 : 0; u < e_issued; ++u)
+                if (!mbar_wait_bounded(&ey_bar[u & 1], uint32_t(u >> 1) & 1u))
+                    bits |= DEVERR_DRAIN_TIMEOUT;
+            if (b_issued < nt || (EYT && e_issued < nt)) bits |= DEVERR_TILE_WAIT_TIMEOUT;
             if (bits) atomicOr(p.err, bits);
         }
         __syncwarp();
     } else {
         setmaxnreg_inc<kWsGenRegs>();
-        // ---- generators: thread = tensor-memory lane = grid row ra ----
+        // ---- generators: thread = tensor-memory lane ra = coil ra / RC of
+        // grid row ra % RC ----
         const int ra = 32 * (warp & 3) + lane;
         const int ah = warp >> 2;                     // samples 16 ah .. 16 ah + 15 of a tile
+        const int coil = ra / RC;
+        const int rr = ra % RC;
         const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
-        const float2 yz = yz_sh[ra];
+        const float2 yz = yz_sh[rr];
+        const float z_plane = EYT ? yz_sh[0].y : 0.0f;   // EYT: one plane per CTA
         float R[kTcColsPerWarp];
 #pragma unroll
         for (int j = 0; j < kTcColsPerWarp; ++j) R[j] = 0.0f;
@@ -254,8 +316,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
         };
 
         bool ok = true;
+        if constexpr (BC > 1) {
+            // row factors of tile 0; later tiles' are made one tile ahead
+            if (nt > 0) {
+                ok = __all_sync(0xffffffffu, ws_wait(&full_bar[0], 0u, abort_flag));
+                if (ok) tc_row_factors<TRIG, RC>(ring, yz_sh, e_sh, tid);
+            }
+            ok = ws_gen_sync_and(ok);
+        }
         int pend = -1;   // last tile of a block whose D is not folded yet (another block follows)
-        for (int t = 0; t < nt; ++t) {
+        // no early exit inside a tile: with coil groups every generator warp
+        // meets the others at the named barrier closing each tile
+        for (int t = 0; t < nt && ok; ++t) {
             const int st = t % kS;
             if (pend >= 0) {
                 // fold as soon as the block's last MMA is done; at the latest
@@ -267,49 +339,95 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                 done = __all_sync(0xffffffffu, done);
                 if (must && !done) {
                     ok = false;
-                    break;
-                }
-                if (done) {
+                } else if (done) {
                     fold(true);
                     pend = -1;
                 }
             }
             // the stage's previous A (tile t - kS) has been read; the records have landed
-            if (t >= kS) ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
+            if (ok && t >= kS)
+                ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
             if (ok) ok = ws_wait(&full_bar[t % kStages], uint32_t(t / kStages) & 1u, abort_flag);
+            if (EYT && ok) ok = ws_wait(&ey_bar[t & 1], uint32_t(t >> 1) & 1u, abort_flag);
             // warp-uniform: the tensor-memory stores below are .sync.aligned
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const float* rec = ring + (t % kStages) * F * T;
-            const uint32_t acol = tmem + lanes + kTcDCols + uint32_t(st) * kTcAStageCols;
+            if (ok) {
+                tc_fence_after_sync();
+                const float* rec = ring + (t % kStages) * F * T;
+                const uint32_t acol = tmem + lanes + kTcDCols + uint32_t(st) * kTcAStageCols;
+                float ezr = 0.0f, ezi = 0.0f;
+                if constexpr (EYT) {
+                    // e^{i phase(kz z)} of sample `lane`, shuffled to the rows below
+                    table_sincos<TRIG>(rec[2 * T + lane] * z_plane, ezi, ezr);
+                }
 #pragma unroll
-            for (int c = 0; c < kTcAChunks; ++c) {
-                const int s0 = 8 * (kTcAChunks * ah + c);
-                float ky[8], kz[8], ar[8], ai[8];
-                tc_load8(rec, 1, s0, ky);
-                tc_load8(rec, 2, s0, kz);
+                for (int c = 0; c < kTcAChunks; ++c) {
+                    const int s0 = 8 * (kTcAChunks * ah + c);
+                    float ar[8], ai[8];
+                    if constexpr (EYT) {
+                        const float2* ey = ey_sh + (t & 1) * (T * kTcRows);
 #pragma unroll
-                for (int s8 = 0; s8 < 8; ++s8)
-                    table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), ai[s8], ar[s8]);
-                // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
-                const uint32_t col = acol + uint32_t(s0 / 2);
-                uint4 h, l;
-                tc_split8(ar, h, l);
-                tmem_st4(col + A_RH * kTcAPartCols, h);
-                tmem_st4(col + A_RL * kTcAPartCols, l);
-                tc_split8(ai, h, l);
-                tmem_st4(col + A_IH * kTcAPartCols, h);
-                tmem_st4(col + A_IL * kTcAPartCols, l);
+                        for (int s8 = 0; s8 < 8; ++s8) {
+                            const float fr = __shfl_sync(0xffffffffu, ezr, s0 + s8);
+                            const float fi = __shfl_sync(0xffffffffu, ezi, s0 + s8);
+                            const float2 e = ey[(s0 + s8) * kTcRows + ra];
+                            ar[s8] = fmaf(fr, e.x, -fi * e.y);
+                            ai[s8] = fmaf(fr, e.y, fi * e.x);
+                        }
+                    } else if constexpr (BC == 1) {
+                        float ky[8], kz[8];
+                        tc_load8(rec, 1, s0, ky);
+                        tc_load8(rec, 2, s0, kz);
+#pragma unroll
+                        for (int s8 = 0; s8 < 8; ++s8)
+                            table_sincos<TRIG>(fmaf(kz[s8], yz.y, ky[s8] * yz.x), ai[s8], ar[s8]);
+                    } else {
+                        // this coil's weight times the row's shared factor
+                        const float2* e = e_sh + (t & 1) * T * RC;
+                        float wr[8], wi[8];
+                        tc_load8(rec, 3 + coil, s0, wr);
+                        tc_load8(rec, 3 + BC + coil, s0, wi);
+#pragma unroll
+                        for (int s8 = 0; s8 < 8; ++s8) {
+                            const float2 f = e[(s0 + s8) * RC + rr];
+                            ar[s8] = fmaf(wr[s8], f.x, -wi[s8] * f.y);
+                            ai[s8] = fmaf(wi[s8], f.x, wr[s8] * f.y);
+                        }
+                    }
+                    // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
+                    const uint32_t col = acol + uint32_t(s0 / 2);
+                    uint4 h, l;
+                    tc_split8(ar, h, l);
+                    tmem_st4(col + A_RH * kTcAPartCols, h);
+                    tmem_st4(col + A_RL * kTcAPartCols, l);
+                    tc_split8(ai, h, l);
+                    tmem_st4(col + A_IH * kTcAPartCols, h);
+                    tmem_st4(col + A_IL * kTcAPartCols, l);
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&a_full[st]);
+                    mbar_arrive(&rec_free[t % kStages]);
+                    if (EYT) mbar_arrive(&ey_free[t & 1]);
+                }
+                if (t % drain_tiles == drain_tiles - 1 && t + 1 < nt) pend = t;
+                if constexpr (BC > 1) {
+                    // row factors of tile t + 1 into the buffer tile t - 1 used
+                    // (every generator finished with it before the previous
+                    // named barrier)
+                    if (t + 1 < nt) {
+                        ok = __all_sync(0xffffffffu, ws_wait(&full_bar[(t + 1) % kStages],
+                                                             uint32_t((t + 1) / kStages) & 1u,
+                                                             abort_flag));
+                        if (ok)
+                            tc_row_factors<TRIG, RC>(ring + ((t + 1) % kStages) * F * T, yz_sh,
+                                                     e_sh + ((t + 1) & 1) * T * RC, tid);
+                    }
+                }
             }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&a_full[st]);
-                mbar_arrive(&rec_free[t % kStages]);
-            }
-            if (t % drain_tiles == drain_tiles - 1 && t + 1 < nt) pend = t;
+            if constexpr (BC > 1) ok = ws_gen_sync_and(ok);
         }
         // the block still waiting for its fold, then the last block
         if (ok && pend >= 0) {
@@ -327,10 +445,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
         } else if (nt > 0) {
             // R -> outputs: grid row ra, this warp's D columns
             const float inv_scale = exp2_int(-tc_scale_exp(*p.wbound));
-            const int64_t row = row0 + ra;
+            const int64_t row = row0 + rr;
             const uint32_t wcols = tc_warp_cols(warp);
-            float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride;
-            if (row < total_rows) {
+            float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride +
+                               coil * p.coil_stride;
+            if (row < total_rows && coil < p.coils) {
                 const int col0 = int(blockIdx.z) * kTcCols;
                 const int ncols = p.nx - col0 < kTcCols ? p.nx - col0 : kTcCols;
                 float* o = out + row * p.nx + col0 + (wcols & 127u);

@@ -5,16 +5,16 @@
 #include "launch.h"
 
 #ifndef MRI_TC_WS
-#define MRI_TC_WS 1   // single-weight launches without the Ey table take the warp-role kernel
+#define MRI_TC_WS 1   // the warp-role kernel (0: the one with a CTA barrier per tile)
 #endif
 
 namespace mri {
 
 namespace {
-template <bool REALW, int TRIG>
+template <int BC, bool REALW, int TRIG, bool EYT>
 cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
 {
-    auto kernel = gather_grid_tc_ws_kernel<REALW, TRIG>;
+    auto kernel = gather_grid_tc_ws_kernel<BC, REALW, TRIG, EYT>;
     // the warpgroup register budgets must fit the registers the CTA is
     // launched with, or a budget increase would wait forever
     cudaFuncAttributes fa{};
@@ -22,7 +22,7 @@ cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kWsThreads < 32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs)
         return cudaErrorInvalidConfiguration;
-    const size_t smem = grid_tc_ws_smem_bytes(REALW);
+    const size_t smem = grid_tc_ws_smem_bytes(REALW, BC, EYT);
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kernel<<<grid, kWsThreads, smem, s>>>(p);
@@ -32,7 +32,7 @@ cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
 template <int BC, bool REALW, int TRIG, bool EYT>
 cudaError_t run(const GridParams& p, dim3 grid, cudaStream_t s)
 {
-    if constexpr (BC == 1 && !EYT && MRI_TC_WS) return run_ws<REALW, TRIG>(p, grid, s);
+    if constexpr (MRI_TC_WS) return run_ws<BC, REALW, TRIG, EYT>(p, grid, s);
     const size_t smem = grid_tc_smem_bytes(REALW, BC, EYT);
     const cudaError_t attr = cudaFuncSetAttribute(
         gather_grid_tc_kernel<BC, REALW, TRIG, EYT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -53,6 +53,11 @@ cudaError_t run_trig(int trig, const GridParams& p, dim3 grid, cudaStream_t s)
     return cudaErrorInvalidValue;
 }
 }  // namespace
+
+int grid_tc_threads()
+{
+    return MRI_TC_WS ? kWsThreads : kTcThreads;
+}
 
 bool grid_tc_ey_table(int trig, int bc, int ny)
 {

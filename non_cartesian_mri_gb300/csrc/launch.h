@@ -49,6 +49,8 @@ cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cuda
 // weights of tensor-core grid records times the power of two from the bound word
 cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
                                  const unsigned int* bound, int grid, cudaStream_t s);
+// threads per CTA of the tensor-core grid kernel
+int grid_tc_threads();
 // whether a tensor-core grid launch takes its y factors from the Ey table
 bool grid_tc_ey_table(int trig, int bc, int ny);
 // the Ey table (ny % 128 == 0) from the records (ky) and ys

@@ -900,7 +900,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         plan->scratch_bytes += 3 * N * 4;
         return st;
     }
-    plan->threads_per_cta = mri::kTcThreads;
+    plan->threads_per_cta = mri::grid_tc_threads();
     plan->samples_per_tile = mri::kTcTile;
     plan->tiles = g.ntiles;
     plan->tensor_cores = 1;
@@ -913,6 +913,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
     for (size_t i = 0; i < groups.size(); ++i) {
         const GridPlan gi = plan_grid(realw, M, nx, ny, nz, num_sms, groups[i].bc, groups[i].nb);
         if (i == 0) {
+            // voxels whose running sums one generating thread holds
             plan->voxels_per_thread = mri::kTcRows * mri::kTcCols / mri::kTcThreads;
             plan->splits = gi.splits;
             plan->voxel_ctas = gi.vblocks * gi.ncb;
