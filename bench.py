@@ -300,27 +300,41 @@ def peak_per_sm_clk(kind, rates):
     return min(by_mufu, by_fp32), ("mufu" if by_mufu <= by_fp32 else "fp32"), mufu, fp32
 
 
-def gather_source_hash():
+# The sources a kernel's DRAM traffic depends on (its code and the host code
+# that plans its launch); a stored traffic figure is valid while they are
+# unchanged.
+_COMMON_SOURCES = ("ptx.cuh", "gather.cuh", "sincospi_coeffs.h", "launch.h", "mri_abi.cu")
+TRAFFIC_SOURCES = {
+    "grid_tc": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
+                                  "gather_grid_tc_ws.cuh", "kernels_grid_tc.cu"),
+    "grid_tc_fwd": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
+                                      "gather_grid_tc_fwd.cuh", "kernels_grid_tc.cu"),
+}
+
+
+def gather_source_hash(kind="grid_tc"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "non_cartesian_mri_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    names = TRAFFIC_SOURCES.get(kind)
+    if names is None:   # any other kernel: every source
+        names = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind, trig):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
+def profiled_traffic(kind, trig, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    trig path and workload, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    entry = rec.get(f"{kind}:{trig}")
-    if not entry or entry.get("source_hash") != gather_source_hash():
+    entry = rec.get(f"{kind}:{workload}:{trig}")
+    if not entry or entry.get("source_hash") != gather_source_hash(kind):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -335,7 +349,7 @@ def roofline_tensor(w, res, peaks, trig, units):
     return {"bound": "tensor", "binding_unit": "tcgen05 kind::f16 (f16 x f16 -> f32)",
             "achieved": round(achieved, 2),
             "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic("grid_tc", trig),
+            "traffic": profiled_traffic("grid_tc", trig, w.name),
             "peak_basis": (f"bf16 burst {bf16:g} TFLOP/s ({'measured, MEASURED_PEAKS.json' if 'bf16_tflops' in peaks else 'recipe fallback'})"
                            f" = dense f16 rate, / {TC_PASSES:g} f16 products per fp32 product;"
                            f" algorithmic {TC_FLOPS_PER_PAIR:g} flops per voxel-sample pair"),
@@ -365,7 +379,7 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
            "peak": round(peak, 2),
            "unit": "G" + ops["unit"] + "s/s",
            "frac": round(achieved / peak, 4),
-           "traffic": profiled_traffic(akind if grid else kind, trig),
+           "traffic": profiled_traffic(akind if grid else kind, trig, w.name),
            "peak_basis": basis,
            "gather_ms_per_launch": round(per_launch * 1e3, 3)}
     if sm_mhz:
@@ -555,7 +569,7 @@ def run_ours(args):
             if fwd:
                 # the forward kernels have their own traffic records
                 paths[name]["roofline"]["traffic"] = profiled_traffic(
-                    "grid_tc_fwd" if pgrid else "forward", trig)
+                    "grid_tc_fwd" if pgrid else "forward", trig, pw.name)
             if pw.kind == "fhd_batched":
                 paths[name]["trajectory_pairs_per_s_G"] = round(pw.pairs / pm / 1e9, 2)
             del pt

@@ -1,8 +1,7 @@
-// gather_grid_tc_ws.cuh -- the tensor-core grid F^H D / Q kernel with warp
-// roles.
+// gather_grid_tc_ws.cuh -- the tensor-core grid F^H D / Q kernel, with warp
+// roles (operand layouts, tables and helpers in gather_grid_tc.cuh).
 //
-// Same arithmetic as gather_grid_tc_kernel (gather_grid_tc.cuh): per tile of
-// 32 samples, A (128 MMA rows: BC coils x 128 / BC grid rows) goes to tensor
+// Per tile of 32 samples, A (128 MMA rows: BC coils x 128 / BC grid rows) goes to tensor
 // memory as f16 hi / lo parts, B (one block of 128 columns) comes from the
 // per-call table by TMA, and 12 tcgen05.mma of 128 x 256 x 16 add A B into
 // D; D is folded into running sums in registers every block of tiles
@@ -19,13 +18,14 @@
 //                   the generator warps makes it visible), times each coil's
 //                   weight.
 //
-// What differs is who waits for whom.  tcgen05.mma is issued by one thread
-// and stalls that thread while the tensor core's instruction queue is full
-// -- for most of a tile's MMA time.  When the issuing thread also generates
-// operands and the CTA meets at a barrier every tile, every warp waits for
-// it, and operand generation and the MMAs run one after the other.  Here
+// Who waits for whom.  tcgen05.mma is issued by one thread and stalls that
+// thread while the tensor core's instruction queue is full -- for most of a
+// tile's MMA time.  Were the issuing thread also generating operands, with
+// the CTA meeting at a barrier every tile, every warp would wait for it and
+// operand generation and the MMAs would run one after the other (measured:
+// 963 of 2,460 cycles per tile in the issue, 67 against 89 Tpairs/s).  So
 // the roles are separate and meet only at mbarriers:
-//   warps 0-7   (two warpgroups, 240 registers each thread): generate A into
+//   warps 0-7   (two warpgroups, 232 registers each thread): generate A into
 //               the tensor-memory stage of tile t once the MMAs of tile
 //               t - kS are done, signal a_full; fold D into the running sums
 //               when a block's last MMA is done, signal d_free; epilogue.
@@ -36,10 +36,10 @@
 //               every generator warp has signalled rec_free) and of the B
 //               tiles (stage reused once its MMAs are done).
 //   warps 10-11 idle (they complete the third warpgroup, which gives up its
-//               registers to the generators: 24 each).
+//               registers to the generators: 32 each).
 // Launch: 384 threads at 168 registers (the whole register file); the host
 // checks the compiled count before launching, since the warpgroup budgets
-// (2 x 128 x 240 + 128 x 24 = 64,512) must fit what the CTA holds.
+// (2 x 128 x 232 + 128 x 32 = 63,488 of 64,512) must fit what the CTA holds.
 //
 // Every wait is bounded and also gives up when another role has given up
 // (a shared abort flag); a role that gives up reports through the device
@@ -56,8 +56,8 @@ namespace mri {
 constexpr int kWsGenWarps = 8;                        // two warpgroups
 constexpr int kWsThreads = 32 * kWsGenWarps + 128;    // + one warpgroup of helpers
 constexpr int kWsLaunchRegs = 168;                    // 65,536 / 384, a multiple of 8
-constexpr int kWsGenRegs = 240;
-constexpr int kWsAuxRegs = 24;
+constexpr int kWsGenRegs = 232;
+constexpr int kWsAuxRegs = 32;
 static_assert(32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs <= kWsThreads * kWsLaunchRegs,
               "warpgroup register budgets exceed the launch");
 static_assert(kWsGenWarps == kTcWarps, "generator warps map the D columns as the barrier kernel");

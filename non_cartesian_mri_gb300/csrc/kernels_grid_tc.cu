@@ -1,12 +1,9 @@
-// kernels_grid_tc.cu -- tensor-core separable-grid kernels (gather_grid_tc.cuh).
+// kernels_grid_tc.cu -- tensor-core separable-grid kernels (gather_grid_tc_ws.cuh,
+// gather_grid_tc_fwd.cuh) and their per-call operand tables (gather_grid_tc.cuh).
 #include "gather_grid_tc.cuh"
 #include "gather_grid_tc_fwd.cuh"
 #include "gather_grid_tc_ws.cuh"
 #include "launch.h"
-
-#ifndef MRI_TC_WS
-#define MRI_TC_WS 1   // the warp-role kernel (0: the one with a CTA barrier per tile)
-#endif
 
 namespace mri {
 
@@ -29,26 +26,13 @@ cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <int BC, bool REALW, int TRIG, bool EYT>
-cudaError_t run(const GridParams& p, dim3 grid, cudaStream_t s)
-{
-    if constexpr (MRI_TC_WS) return run_ws<BC, REALW, TRIG, EYT>(p, grid, s);
-    const size_t smem = grid_tc_smem_bytes(REALW, BC, EYT);
-    const cudaError_t attr = cudaFuncSetAttribute(
-        gather_grid_tc_kernel<BC, REALW, TRIG, EYT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        int(smem));
-    if (attr != cudaSuccess) return attr;
-    gather_grid_tc_kernel<BC, REALW, TRIG, EYT><<<grid, kTcThreads, smem, s>>>(p);
-    return cudaGetLastError();
-}
-
 template <int BC, bool REALW, bool EYT>
 cudaError_t run_trig(int trig, const GridParams& p, dim3 grid, cudaStream_t s)
 {
     switch (trig) {
-        case TRIG_ACCURATE: return run<BC, REALW, TRIG_ACCURATE, EYT>(p, grid, s);
-        case TRIG_FAST: return run<BC, REALW, TRIG_FAST, EYT>(p, grid, s);
-        case TRIG_FAST_RR: return run<BC, REALW, TRIG_FAST_RR, EYT>(p, grid, s);
+        case TRIG_ACCURATE: return run_ws<BC, REALW, TRIG_ACCURATE, EYT>(p, grid, s);
+        case TRIG_FAST: return run_ws<BC, REALW, TRIG_FAST, EYT>(p, grid, s);
+        case TRIG_FAST_RR: return run_ws<BC, REALW, TRIG_FAST_RR, EYT>(p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -56,12 +40,12 @@ cudaError_t run_trig(int trig, const GridParams& p, dim3 grid, cudaStream_t s)
 
 int grid_tc_threads()
 {
-    return MRI_TC_WS ? kWsThreads : kTcThreads;
+    return kWsThreads;
 }
 
 bool grid_tc_ey_table(int trig, int bc, int ny)
 {
-    return bc == 1 && ny % kTcRows == 0 && (trig == TRIG_ACCURATE || MRI_TC_EY_FAST);
+    return bc == 1 && ny % kTcRows == 0 && trig == TRIG_ACCURATE;
 }
 
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
