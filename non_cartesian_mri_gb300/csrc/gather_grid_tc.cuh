@@ -107,11 +107,13 @@ inline int grid_tc_col_blocks(int nx) { return (nx + kTcCols - 1) / kTcCols; }
 // Shape of the forward-model kernel (gather_grid_tc_fwd.cuh), which takes the
 // same nx.
 constexpr int kFwSamples = 128;                 // samples per CTA = MMA M
-constexpr int kFwRows = 128;                    // grid rows per block = MMA N / 2
+constexpr int kFwRows = 64;                     // grid rows per block = MMA N / 2
 constexpr int kFwCols = 128;                    // grid columns per block = K
-constexpr int kFwKSteps = kFwCols / 16;         // 8
-constexpr int kFwChunkHalf = 3 * kFwRows * 32;  // 384 rows x 16 f16 = 12 KB (hi or lo)
-constexpr int kFwChunkBytes = 2 * kFwChunkHalf; // 24 KB
+constexpr int kFwKSteps = kFwCols / 16;         // 8 K steps of 16 per column block
+constexpr int kFwKPerChunk = 4;                 // K steps per rho chunk
+constexpr int kFwChunks = kFwKSteps / kFwKPerChunk;           // 2 chunks per block
+constexpr int kFwChunkHalf = 3 * kFwRows * 32 * kFwKPerChunk; // 192 rows x 64 f16 = 24 KB
+constexpr int kFwChunkBytes = 2 * kFwChunkHalf;               // hi, lo: 48 KB
 inline bool grid_tc_fwd_fits(int nx) { return grid_tc_fits(nx); }
 
 // Coils per CTA (a coil group): the MMA's 128 rows are bc coils x 128 / bc
@@ -297,6 +299,22 @@ __global__ void __launch_bounds__(256) build_ey_tiles_kernel(const float* rec, i
         float sn, cs;
         table_sincos<TRIG>(rec[t * fields * kTcTile + kTcTile + s] * ys[yb * kTcRows + r], sn, cs);
         ey_tab[item] = make_float2(cs, sn);
+    }
+}
+
+// Bounded wait that also gives up once any role of the CTA has given up (the
+// kernels with warp roles share an abort flag in shared memory).
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            return false;
+        }
     }
 }
 

@@ -90,21 +90,6 @@ __device__ __forceinline__ bool ws_gen_sync_and(bool v)
     return r != 0;
 }
 
-// Bounded wait that also gives up once any role of the CTA has given up.
-__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 template <int BC, bool REALW, int TRIG, bool EYT>
 __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridParams p)
 {

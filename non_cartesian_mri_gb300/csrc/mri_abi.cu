@@ -754,11 +754,12 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
     const int64_t row_blocks = ceil_div(rows, int64_t(mri::kFwRows));
     const int ncb = mri::grid_tc_col_blocks(nx);
     const int64_t sample_tiles = ceil_div(M, int64_t(mri::kFwSamples));
+    // a row block of 64 rows and one column block: about half a microsecond
     const int splits = choose_splits(row_blocks, sample_tiles, d->sms > 0 ? d->sms : 1, 1, M,
-                                     double(ncb), 3.0);
+                                     0.5 * ncb, 3.0);
     const int64_t tab_bytes =
-        row_blocks * ncb * mri::kFwKSteps * int64_t(mri::kFwChunkBytes);
-    const int64_t yz_bytes = row_blocks * mri::kTcRows * 8;
+        row_blocks * ncb * mri::kFwChunks * int64_t(mri::kFwChunkBytes);
+    const int64_t yz_bytes = row_blocks * mri::kFwRows * 8;
     const int64_t part_bytes = splits > 1 ? int64_t(splits) * 2 * M * 4 : 0;
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
