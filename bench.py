@@ -5,11 +5,13 @@ Headline: F^H D voxel-sample pairs per second on the 128^3-voxel, 3D-radial
 workload (M = 262,144 samples, 2,097,152 voxels), one call per step (cmpMu +
 tile staging + phase + trig + complex multiply-accumulate + epilogue).  The
 workload's voxels form a 128^3 grid, so the headline call is mri_fhd_grid
-(the lattice-factored gather, MUFU trig for its tables); ``--general`` times
-mri_fhd (per-pair phase and trig) instead.  The same JSON line also carries
-the other rows of the hot path measured the same way: both entry points with
-both trig paths, Q on the 128^3 stack-of-spirals trajectory (M = 1,048,576)
-and batched F^H D with 8 coils (M = 524,288).
+(the lattice-factored gather as a complex matrix product on the tensor
+cores); ``--general`` times mri_fhd (per-pair phase and trig) instead.  The
+same JSON line also carries the other rows of the hot path measured the same
+way: both entry points with both trig paths, Q on the 128^3 stack-of-spirals
+trajectory (M = 1,048,576), batched F^H D with 8 coils (M = 524,288) and the
+forward model D = F rho.  ``--forward`` times the forward model as the step
+(a profiling aid).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -60,7 +62,7 @@ ALGO_OPS = {
     "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
     "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
-# The tensor-core grid kernel (nx = 128): one complex multiply-accumulate is
+# The tensor-core grid kernels: one complex multiply-accumulate is
 # 8 real flops per pair; each fp32-accurate product takes three f16 MMA
 # passes (hi*hi + hi*lo + lo*hi), so its peak is the dense f16 peak / 3, and
 # dense f16 runs at the measured bf16 rate.
@@ -87,6 +89,10 @@ def parse_args():
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the accurate/Q/batched sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the forward model D = F rho (of a seeded image) on the "
+                         "workload's trajectory and grid instead of F^H D (profiling aid; "
+                         "implies --no-paths --no-e2e)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     return ap.parse_args()
 
@@ -473,10 +479,25 @@ def run_ours(args):
     out = (torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"),
            torch.empty((w.B, w.N) if kind == "fhd_batched" else (w.N,), device="cuda"))
     grid = not args.general
-    plan = grid_or_general_plan(mri, w, grid)
+    if args.forward:
+        # the forward model D = F rho of a seeded complex image
+        args.no_paths = args.no_e2e = True
+        rng = np.random.default_rng(1000 + w.meta.get("seed", 0))
+        rho = [torch.from_numpy(rng.standard_normal(w.N).astype(np.float32)).cuda()
+               for _ in range(2)]
+        if grid:
+            step = lambda: mri.forward_grid(t["kx"], t["ky"], t["kz"], t["xs"], t["ys"],  # noqa: E731
+                                            t["zs"], rho[0], rho[1], trig=args.trig)
+            plan = {"launches": 4, "tensor_cores": 1, "samples_per_tile": 128}
+        else:
+            step = lambda: mri.forward(t["kx"], t["ky"], t["kz"], t["x"], t["y"], t["z"],  # noqa: E731
+                                       rho[0], rho[1], trig=args.trig)
+            plan = mri.plan("fhd", w.N, w.M)
+    else:
+        step = lambda: call(mri, kind, t, args.trig, out, grid)  # noqa: E731
+        plan = grid_or_general_plan(mri, w, grid)
     with ClockSampler(local) as clk:
-        res = timed_steps(torch, mri, dist, lambda: call(mri, kind, t, args.trig, out, grid),
-                          args.steps, args.warmup, flush)
+        res = timed_steps(torch, mri, dist, step, args.steps, args.warmup, flush)
     clocks = clk.summary()
     mean_s = dist.max(statistics.mean(res["step_ms"]) / 1e3)
     units = w.pairs * (w.B if kind == "fhd_batched" else 1)
@@ -488,7 +509,8 @@ def run_ours(args):
         "data": "synthetic (seeded generators, no dataset)",
         "config": {"workload": f"{w.name}: {wl.WORKLOADS[w.name]}", "voxels": w.N,
                    "samples": w.M, "coils": w.B, "trig": args.trig,
-                   "entry": ENTRY[(kind, grid)],
+                   "entry": (("mri_forward_grid" if grid else "mri_forward") if args.forward
+                             else ENTRY[(kind, grid)]),
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
                    "parallelism": "one independent voxel slab per rank" if world > 1
                    else "single GPU",
@@ -500,6 +522,10 @@ def run_ours(args):
         "unit_rates_per_sm_clk": rates,
     }
     line["roofline"]["sm_max_mhz_basis"] = "MEASURED_PEAKS.json sm_max_mhz" if peaks else "recipe"
+    if args.forward:
+        line["config"]["workload"] += " (forward model of a seeded complex image)"
+        line["roofline"]["traffic"] = profiled_traffic("grid_tc_fwd" if grid else "forward",
+                                                       args.trig, w.name)
 
     if not args.no_e2e and kind == "fhd":
         line["e2e"] = e2e(torch, mri, dist, w, args.trig, max(args.steps, 2), 1, grid)
