@@ -60,11 +60,14 @@ constexpr int kTcWarps = kTcThreads / 32;
 #endif
 // Tiles per summation block.  The tensor core's own fp32 accumulation loses
 // a little with every add, with a consistent sign, so the error of a block
-// grows with its length (measured on the 128^3 radial workload: rel-L2 1.4e-5
-// for blocks of 1024 samples, 1.9e-6 for 128); the accurate path folds every
-// 128 samples, the fast paths every 1024.
+// grows with its length (accurate F^H D on the 128^3 radial workload, rel-L2
+// against the oracle: 1.0e-6 for blocks of 128 samples, 1.9e-6 for 256,
+// 4.0e-6 for 512; 1.4e-5 for 1024), while every fold stalls the tensor core
+// (accurate F^H D: 65.5, 74.6, 77.9 Tpairs/s for 128, 256, 512).  The
+// accurate path folds every 256 samples, the fast paths (trig error ~1e-5)
+// every 1024.
 #ifndef MRI_TC_DRAIN_ACCURATE
-#define MRI_TC_DRAIN_ACCURATE 4
+#define MRI_TC_DRAIN_ACCURATE 8
 #endif
 #ifndef MRI_TC_DRAIN_FAST
 #define MRI_TC_DRAIN_FAST 32
