@@ -62,6 +62,12 @@ ALGO_OPS = {
     "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
     "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
+# The accurate paths evaluate sin and cos in software (the MUFU's ~2^-21
+# absolute error is too coarse): the exact reduction to a quarter turn (3
+# FADD), f^2, the odd and even polynomials (3 + 4 FFMA) and f * P: 12 FP32
+# operations per sin/cos pair (the quadrant selects and sign flips run on the
+# ALU pipe).  On those paths the pair's trig work is FP32 work.
+TRIG_FP32_OPS = 12.0
 # The tensor-core grid kernels: one complex multiply-accumulate is
 # 8 real flops per pair; each fp32-accurate product takes three f16 MMA
 # passes (hi*hi + hi*lo + lo*hi), so its peak is the dense f16 peak / 3, and
@@ -291,9 +297,19 @@ def unit_rates(mri):
     return r
 
 
-def peak_per_sm_clk(kind, rates):
+def algo_ops(kind, trig):
+    """Operations per work unit; on the accurate path the sin/cos pairs move
+    from the MUFU to the FP32 pipe."""
+    ops = dict(ALGO_OPS[kind])
+    if trig == "accurate" and ops["mufu"]:
+        ops["fp32"] += TRIG_FP32_OPS * ops["mufu"] / 2.0
+        ops["mufu"] = 0.0
+    return ops
+
+
+def peak_per_sm_clk(kind, rates, trig="fast"):
     """Binding roofline in work units per SM per clock: min over the two units."""
-    ops = ALGO_OPS[kind]
+    ops = algo_ops(kind, trig)
     mufu = NOMINAL["mufu"] if rates is None else min(rates["sin"], rates["cos"])
     fp32 = NOMINAL["fp32"] if rates is None else rates["ffma"]
     # nominal integers when the probe agrees within 10%
@@ -375,9 +391,9 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
     launches_per_step = res["gather_launches"] / len(res["step_ms"])
     achieved = units / launches_per_step / per_launch / 1e9
-    per_clk, unit, mufu, fp32 = peak_per_sm_clk(akind, rates)
+    per_clk, unit, mufu, fp32 = peak_per_sm_clk(akind, rates, trig)
     peak = per_clk * sms * sm_max_mhz * 1e6 / 1e9
-    ops = ALGO_OPS[akind]
+    ops = algo_ops(akind, trig)
     basis = (f"{sms} SMs x {sm_max_mhz:.0f} MHz x min(MUFU {mufu:g}/{ops['mufu']:g}, "
              f"FP32 {fp32:g}/{ops['fp32']:g}) per SM-clock") if ops["mufu"] else (
              f"{sms} SMs x {sm_max_mhz:.0f} MHz x FP32 {fp32:g}/{ops['fp32']:g} per SM-clock")

@@ -62,7 +62,7 @@ struct FwdParams {
     const float2* yz_rows;           // (y, z) of every row, padded to whole blocks
     int64_t row_blocks;
     int splits;                      // CTAs along the row blocks
-    const unsigned char* rho_tab;    // chunks [row block][column block][K step], 24 KB each
+    const unsigned char* rho_tab;    // chunks [row block][column block][chunk], kFwChunkBytes each
     const unsigned int* bound;       // float bits of max |rho_r| + |rho_i|
     float* out_r;                    // [split][M] or the caller's arrays
     float* out_i;

@@ -60,7 +60,7 @@ constexpr int kWsGenRegs = 232;
 constexpr int kWsAuxRegs = 32;
 static_assert(32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs <= kWsThreads * kWsLaunchRegs,
               "warpgroup register budgets exceed the launch");
-static_assert(kWsGenWarps == kTcWarps, "generator warps map the D columns as the barrier kernel");
+static_assert(kWsGenWarps == kTcWarps, "generator warps own the D columns by tc_warp_cols");
 
 inline size_t grid_tc_ws_smem_bytes(bool realw, int bc, bool eyt)
 {

@@ -69,7 +69,7 @@ __global__ void wait_selftest_kernel(int arrive, unsigned int* err)
     if (!ok && threadIdx.x == 0) atomicOr(err, mri::DEVERR_TILE_WAIT_TIMEOUT);
 }
 
-// Tensor-core issue-rate probe: thread 0 issues, per tile, the 12
+// Tensor-core issue-rate probe: one thread issues, per tile, the 12
 // tcgen05.mma (kind::f16, 128 x 256 x 16) of a 32-sample tile of the
 // tensor-core grid kernel, with no operand generation and no CTA barrier.
 // MODE 0: A and B in shared memory (zeroed); MODE 1: A from tensor memory,

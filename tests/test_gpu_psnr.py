@@ -30,7 +30,7 @@ def mri():
 
 @pytest.fixture(scope="module")
 def problem():
-    # 128 x 64 x 64 voxels at integer coordinates: nx = 128 takes the tensor cores
+    # 128 x 64 x 64 voxels at integer coordinates (the tensor-core grid kernels)
     xs = (np.arange(128) - 64).astype(np.float32)
     ys = (np.arange(64) - 32).astype(np.float32)
     zs = (np.arange(64) - 32).astype(np.float32)
