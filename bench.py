@@ -66,7 +66,9 @@ ALGO_OPS = {
 # absolute error is too coarse): the exact reduction to a quarter turn (3
 # FADD), f^2, the odd and even polynomials (3 + 4 FFMA) and f * P: 12 FP32
 # operations per sin/cos pair (the quadrant selects and sign flips run on the
-# ALU pipe).  On those paths the pair's trig work is FP32 work.
+# ALU pipe).  The accurate paths are reported against the same roofline as
+# the fast ones (their software trig is overhead there), and also against
+# the FP32 pipe with that trig work counted ("frac_fp32_with_trig").
 TRIG_FP32_OPS = 12.0
 # The tensor-core grid kernels: one complex multiply-accumulate is
 # 8 real flops per pair; each fp32-accurate product takes three f16 MMA
@@ -297,11 +299,11 @@ def unit_rates(mri):
     return r
 
 
-def algo_ops(kind, trig):
-    """Operations per work unit; on the accurate path the sin/cos pairs move
-    from the MUFU to the FP32 pipe."""
+def algo_ops(kind, trig="fast"):
+    """Operations per work unit; with trig = "accurate_fp32" the sin/cos pairs
+    move from the MUFU to the FP32 pipe as software trig."""
     ops = dict(ALGO_OPS[kind])
-    if trig == "accurate" and ops["mufu"]:
+    if trig == "accurate_fp32" and ops["mufu"]:
         ops["fp32"] += TRIG_FP32_OPS * ops["mufu"] / 2.0
         ops["mufu"] = 0.0
     return ops
@@ -407,6 +409,12 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
     if sm_mhz:
         out["frac_at_sampled_clock"] = round(achieved / (per_clk * sms * sm_mhz * 1e-3), 4)
         out["units_per_sm_clk"] = round(achieved * 1e9 / (sms * sm_mhz * 1e6), 3)
+    if trig == "accurate" and ops["mufu"]:
+        fper, _, _, _ = peak_per_sm_clk(akind, rates, "accurate_fp32")
+        fops = algo_ops(akind, "accurate_fp32")
+        out["frac_fp32_with_trig"] = round(achieved / (fper * sms * sm_max_mhz * 1e-3), 4)
+        out["fp32_with_trig_basis"] = (f"FP32 {fp32:g}/{fops['fp32']:g} per SM-clock "
+                                       f"({TRIG_FP32_OPS:g} FP32 ops per software sin/cos pair)")
     return out
 
 
