@@ -52,12 +52,15 @@ mri_status mri_microbench(int which, int ctas_per_sm, int threads, int64_t iters
  *           aligned device memory) into a ring of 4 stages, copies issued two
  *           tiles ahead, as the grid kernel streams its B-operand table;
  *   mode 3: as mode 1 with each product split into two N = 128 halves
- *           (24 MMAs of 128 x 128 x 16 per tile, the same work).
+ *           (24 MMAs of 128 x 128 x 16 per tile, the same work), the halves
+ *           alternating between two accumulators;
+ *   mode 4: as mode 3 with all 24 MMAs into one accumulator (each depends
+ *           on the one before).
  * b_tab / b_tiles are read in mode 2 only.  cycles[cta] (device, one uint64
  * per SM) receives the SM clock cycles from the first issue to the last
  * completion.  One tile is 32 samples x 128 x 128 voxels = 524,288
  * voxel-sample pairs, so the ceiling in pairs per SM per clock is
- * tiles * 524288 / cycles.  MRI_ERR_MODE for mode outside 0..3, MRI_ERR_NULL
+ * tiles * 524288 / cycles.  MRI_ERR_MODE for mode outside 0..4, MRI_ERR_NULL
  * for a missing array, MRI_ERR_SIZE for tiles outside 1 .. 2^22, b_tiles < 1
  * or an unaligned b_tab (mode 2), MRI_ERR_UNSUPPORTED_DEVICE off sm_103.
  */

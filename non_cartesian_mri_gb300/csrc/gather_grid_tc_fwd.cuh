@@ -208,17 +208,19 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
                         ok = false;
                         break;
                     }
-                    const unsigned char* ch = ring + (c % NS) * kFwChunkBytes;
+                    // one descriptor per chunk; the windows are constant offsets
+                    const uint64_t d0 =
+                        umma_desc_kmajor(ring + (c % NS) * kFwChunkBytes, 128, kSbo);
+                    const uint32_t a0 = tmem + uint32_t(kFwKPerChunk * kp * 8);
 #pragma unroll
                     for (int j = 0; j < kFwKPerChunk; ++j) {
                         const int kb = kFwKPerChunk * kp + j;
-                        auto a = [&](int part) { return tmem + uint32_t(part * 64 + kb * 8); };
+                        auto a = [&](int part) { return a0 + uint32_t(part * 64 + j * 8); };
                         // window of 128 S rows from row r0 (8-row groups of kSbo
                         // bytes), K step j of the chunk (two core matrices of 128 B)
                         auto sdesc = [&](int half, int r0) {
-                            return umma_desc_kmajor(ch + half * kFwChunkHalf + (r0 / 8) * kSbo +
-                                                        j * 256,
-                                                    128, kSbo);
+                            return umma_desc_add(
+                                d0, uint32_t(half * kFwChunkHalf + (r0 / 8) * kSbo + j * 256));
                         };
                         const uint32_t acc0 = kb > 0 ? 1u : 0u;
                         // [T_r | T_i] += A_r [B_r | B_i]   (S rows 64 .. 191)

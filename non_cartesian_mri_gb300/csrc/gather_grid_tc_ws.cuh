@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                 if (ok) ok = ws_wait(&s_bar[st], uint32_t(t / kS) & 1u, abort_flag);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const unsigned char* stage = ops + st * kTcStageBytes;
+                // one descriptor per stage; the windows are constant offsets
+                const uint64_t d0 = umma_desc_kmajor(ops + st * kTcStageBytes, 128, 512);
                 const uint32_t acol = tmem + kTcDCols + uint32_t(st) * kTcAStageCols;
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
@@ -193,8 +194,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                         return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
                     };
                     auto sdesc = [&](int base, int r0) {
-                        return umma_desc_kmajor(stage + base + (r0 / 128) * kTcPartBytes + kb * 256,
-                                                128, 512);
+                        return umma_desc_add(
+                            d0, uint32_t(base + (r0 / 128) * kTcPartBytes + kb * 256));
                     };
                     const uint32_t acc0 = (first && kb == 0) ? 0u : 1u;
                     // [D_r | D_i] += A_r [B_r | B_i]

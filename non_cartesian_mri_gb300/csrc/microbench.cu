@@ -77,7 +77,8 @@ __global__ void wait_selftest_kernel(int arrive, unsigned int* err)
 // one 48 KB TMA bulk copy from a table in global memory into a 4-stage ring
 // (copies issued two tiles ahead, as the grid kernel does); MODE 3: as MODE 1
 // with every product split into two N = 128 halves (24 MMAs of 128 x 128 x
-// 16 per tile, the same work).  One commit per tile.  One CTA per SM (at least 128 KB of shared memory, all 512 TMEM
+// 16 per tile, the same work, alternating between two accumulators); MODE 4:
+// as MODE 3 with every MMA into the same accumulator.  One commit per tile.  One CTA per SM (at least 128 KB of shared memory, all 512 TMEM
 // columns).
 constexpr int kProbePart = 128 * 32 * 2;          // 128 rows x 32 K of f16: 8 KB
 constexpr int kProbeS = 3 * kProbePart;           // 384 B rows: 24 KB (hi; lo follows)
@@ -164,7 +165,12 @@ __global__ void __launch_bounds__(128, 1) mma_probe_kernel(int tiles, const unsi
                                                  128, 512);
                 };
                 auto mma = [&](int part, uint64_t b, uint32_t acc) {
-                    if (MODE == 3) {
+                    if (MODE == 4) {
+                        // the same 24 MMAs, all into one accumulator
+                        const uint32_t a = tmem + 256u + uint32_t(part * 16 + 8 * kb);
+                        mri::umma_f16_ta(tmem, a, b, ID128, acc);
+                        mri::umma_f16_ta(tmem, a, b + uint64_t((16 * 512) >> 4), ID128, 1u);
+                    } else if (MODE == 3) {
                         // the same product as two N = 128 halves (rows 0-127 and
                         // 128-255 of the window, D columns 0-127 and 128-255)
                         const uint32_t a = tmem + 256u + uint32_t(part * 16 + 8 * kb);
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(128, 1) mma_probe_kernel(int tiles, const unsi
 extern "C" mri_status mri_mma_probe(int mode, int tiles, const void* b_tab, int64_t b_tiles,
                                     unsigned long long* cycles, void* stream)
 {
-    if (mode < 0 || mode > 3) return MRI_ERR_MODE;
+    if (mode < 0 || mode > 4) return MRI_ERR_MODE;
     if (cycles == nullptr || (mode == 2 && b_tab == nullptr)) return MRI_ERR_NULL;
     if (tiles < 1 || tiles > (1 << 22)) return MRI_ERR_SIZE;
     if (mode == 2 && b_tiles < 1) return MRI_ERR_SIZE;
@@ -254,6 +260,7 @@ extern "C" mri_status mri_mma_probe(int mode, int tiles, const void* b_tab, int6
         case 0: e = go(mma_probe_kernel<0>, probe_smem(0)); break;
         case 1: e = go(mma_probe_kernel<1>, probe_smem(1)); break;
         case 3: e = go(mma_probe_kernel<3>, probe_smem(3)); break;
+        case 4: e = go(mma_probe_kernel<4>, probe_smem(4)); break;
         default: e = go(mma_probe_kernel<2>, probe_smem(2)); break;
     }
     if (e != cudaSuccess) {

@@ -115,6 +115,16 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor(const void* p, uint32_t lbo
     return d;          // layout type 0: no swizzle
 }
 
+// The descriptor of the same layout `bytes` further on: the start address
+// field holds address / 16 in 14 bits, and shared-memory addresses stay
+// below 256 KB, so the add never carries into the next field.  Lets the
+// thread that issues MMAs build one descriptor per stage and derive the
+// rest with one add each.
+__device__ __forceinline__ uint64_t umma_desc_add(uint64_t desc, uint32_t bytes)
+{
+    return desc + uint64_t(bytes >> 4);
+}
+
 // Instruction descriptor of kind::tf32: D f32, A and B tf32, both K-major,
 // shape M x N; negate_b flips the sign of B.
 __host__ __device__ constexpr uint32_t umma_idesc_tf32(int M, int N, bool negate_b)

@@ -19,7 +19,7 @@ def test_ffma_probe(mri):
     assert 32.0 < r["per_sm_per_clk"] <= 130.0
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_mma_probe(mri, mode):
     """12 MMAs of 128 x 256 x 16 per 32 x 128 x 128 tile: at most 8192 f16
     flops per SM per clock, i.e. 8192 / 24 = 341 pairs."""
