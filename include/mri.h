@@ -283,7 +283,9 @@ mri_status mri_plan_grid_batched(int64_t B, int64_t M, int nx, int ny, int nz, i
 
 /*
  * Device-side error bits of the current device (bit 0: a k-tile wait timed
- * out; bit 1: in-flight copies did not drain).  Synchronises the device.
+ * out; bit 1: in-flight copies did not drain; bit 2, MRI_DEBUG builds only: a
+ * copy's tile index was outside its table and the copy was skipped).
+ * Synchronises the device.
  * clear != 0 resets the bits.  Kernels never trap; a non-zero word means the
  * outputs of some earlier call are not valid.
  */

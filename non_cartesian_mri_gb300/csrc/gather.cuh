@@ -297,9 +297,8 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
     __syncthreads();
     if (tid == 0) {
         for (int st = 0; st < kStages && st < nt; ++st) {
-            mbar_arrive_expect_tx(&full_bar[st], R::TILE_BYTES);
-            tma_bulk_g2s(ring + st * R::TILE_FLOATS, p.rec + (t_begin + st) * R::TILE_FLOATS,
-                         R::TILE_BYTES, &full_bar[st]);
+            tma_load_checked(ring + st * R::TILE_FLOATS, p.rec, t_begin + st, p.ntiles,
+                             R::TILE_BYTES, &full_bar[st], p.err);
         }
     }
 
@@ -423,10 +422,8 @@ __global__ void __launch_bounds__(Shape<BC, REALW>::THREADS, Shape<BC, REALW>::M
         // refill the stage just released with the tile kStages ahead
         if (tid == 0 && t + kStages < nt) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&full_bar[st], R::TILE_BYTES);
-            tma_bulk_g2s(ring + st * R::TILE_FLOATS,
-                         p.rec + (t_begin + t + kStages) * R::TILE_FLOATS, R::TILE_BYTES,
-                         &full_bar[st]);
+            tma_load_checked(ring + st * R::TILE_FLOATS, p.rec, t_begin + t + kStages, p.ntiles,
+                             R::TILE_BYTES, &full_bar[st], p.err);
         }
     }
 

@@ -253,10 +253,9 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
                 const int cb = blk / nb;
                 const int64_t b = b_begin + (blk - cb * nb);
                 const int64_t chunk = (b * p.ncb + cb) * kFwChunks + (u - blk * kFwChunks);
-                mbar_arrive_expect_tx(&s_bar[u % NS], uint32_t(kFwChunkBytes));
-                tma_bulk_g2s(ring + (u % NS) * kFwChunkBytes,
-                             p.rho_tab + chunk * int64_t(kFwChunkBytes), uint32_t(kFwChunkBytes),
-                             &s_bar[u % NS]);
+                tma_load_checked(ring + (u % NS) * kFwChunkBytes, p.rho_tab, chunk,
+                                 p.row_blocks * p.ncb * kFwChunks, uint32_t(kFwChunkBytes),
+                                 &s_bar[u % NS], p.err);
                 loaded = u + 1;
             }
             // the latest copy into each stage lands before shared memory is

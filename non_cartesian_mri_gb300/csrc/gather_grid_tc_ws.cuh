@@ -228,25 +228,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                     ok = ws_wait(&rec_free[u % kStages], uint32_t((u - kStages) / kStages) & 1u,
                                  abort_flag);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&full_bar[u % kStages], TILE_BYTES);
-                tma_bulk_g2s(ring + (u % kStages) * F * T, p.rec + (t_begin + u) * F * T,
-                             TILE_BYTES, &full_bar[u % kStages]);
+                tma_load_checked(ring + (u % kStages) * F * T, p.rec, t_begin + u, p.ntiles,
+                                 TILE_BYTES, &full_bar[u % kStages], p.err);
                 r_issued = u + 1;
                 if (u >= kS)
                     ok = ws_wait(&mma_bar[u % kS], uint32_t((u - kS) / kS) & 1u, abort_flag);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&s_bar[u % kS], uint32_t(kTcStageBytes));
-                tma_bulk_g2s(ops + (u % kS) * kTcStageBytes,
-                             p.s_tab + ((t_begin + u) * p.ncb + blockIdx.z) * kTcStageBytes,
-                             uint32_t(kTcStageBytes), &s_bar[u % kS]);
+                tma_load_checked(ops + (u % kS) * kTcStageBytes, p.s_tab,
+                                 (t_begin + u) * p.ncb + blockIdx.z, p.ntiles * p.ncb,
+                                 uint32_t(kTcStageBytes), &s_bar[u % kS], p.err);
                 b_issued = u + 1;
                 if constexpr (EYT) {
                     if (u >= 2) ok = ws_wait(&ey_free[u & 1], uint32_t((u - 2) >> 1) & 1u, abort_flag);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&ey_bar[u & 1], uint32_t(kTcEyBytes));
-                    tma_bulk_g2s(ey_sh + (u & 1) * (T * kTcRows),
-                                 p.ey_tab + ((t_begin + u) * p.ey_blocks + ey_block) * (T * kTcRows),
-                                 uint32_t(kTcEyBytes), &ey_bar[u & 1]);
+                    tma_load_checked(ey_sh + (u & 1) * (T * kTcRows), p.ey_tab,
+                                     (t_begin + u) * p.ey_blocks + ey_block,
+                                     p.ntiles * p.ey_blocks, uint32_t(kTcEyBytes), &ey_bar[u & 1],
+                                     p.err);
                     e_issued = u + 1;
                 }
             }

@@ -10,7 +10,16 @@ namespace mri {
 enum : unsigned int {
     DEVERR_TILE_WAIT_TIMEOUT = 1u << 0,   // a k-tile never arrived in shared memory
     DEVERR_DRAIN_TIMEOUT = 1u << 1,       // in-flight copies did not land before exit
+    DEVERR_BOUNDS = 1u << 2,              // MRI_DEBUG: a copy's index was outside its table
 };
+
+// MRI_DEBUG = 1 builds (build.build(defines=["MRI_DEBUG=1"], out=...)) check
+// the index of every TMA copy against the size of its table before issuing
+// it (tma_load_checked); compute-sanitizer is not available, so this is the
+// debug build's check of the kernels' index arithmetic.
+#ifndef MRI_DEBUG
+#define MRI_DEBUG 0
+#endif
 
 // A wait on a tile copy normally ends within microseconds; one second means
 // something is wrong (the copy was never issued or faulted).
@@ -94,6 +103,24 @@ __device__ __forceinline__ void tma_bulk_g2s(void* dst, const void* src, uint32_
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Copy element `index` (of `bytes` bytes each) of a table of `count`
+// elements at `base` into `dst`, completing on `bar` (which this thread arms
+// with the byte count).  MRI_DEBUG builds first check 0 <= index < count; a
+// bad index sets DEVERR_BOUNDS in *err and issues nothing, so the consumer's
+// bounded wait gives up and reports too.  No access outside the table.
+__device__ __forceinline__ void tma_load_checked(void* dst, const void* base, int64_t index,
+                                                 int64_t count, uint32_t bytes, uint64_t* bar,
+                                                 unsigned int* err)
+{
+    if (MRI_DEBUG && (index < 0 || index >= count)) {
+        atomicOr(err, DEVERR_BOUNDS);
+        return;
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+    tma_bulk_g2s(dst, static_cast<const unsigned char*>(base) + index * int64_t(bytes), bytes,
+                 bar);
 }
 
 }  // namespace mri
