@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for F^H D, Q and batched F^H D.
+"""fp64 CPU oracle for F^H D, Q, batched F^H D, the forward model and (in
+``oracle.toeplitz``) the Toeplitz F^H F product and the CG solve.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  The product path (the CUDA library and
