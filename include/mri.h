@@ -244,6 +244,63 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
                             float* rD, float* iD,
                             mri_trig trig, int accumulate, void* stream);
 
+/*
+ * The "find rho" step (chapter "Iterative MRI reconstruction", background
+ * section, Fig. 17.3): rho = (F^H F + lambda W^H W)^{-1} F^H D solved by
+ * conjugate gradients, whose cost per iteration is the product of
+ * F^H F + lambda W^H W with the current rho.  F^H F is Toeplitz, so that
+ * product goes through FFTs, built from Q (the chapter's Q).  Readings: F
+ * carries the sensitivity, F[m][n] = Phi_m e^{-i2pi k_m . x_n}, so F^H D is
+ * mri_fhd's and (F^H F)[n][n'] = Q(x_n - x_n') with Q of mri_q; W (from
+ * patient scans, not given) is the identity, lambda >= 0 from the caller.
+ * The voxels form a regular grid x = (ix hx, iy hy, iz hz), ix < nx etc.,
+ * with nx, ny, nz powers of two up to 512 (voxel order as mri_fhd_grid;
+ * any offset of the grid cancels in the differences).
+ *
+ * mri_toeplitz_kernel: Q on the circular grid of voxel differences of the
+ * doubled grid (2nx x 2ny x 2nz: difference i h for i < n, (i - 2n) h for
+ * i >= n per axis), computed by the grid Q path with trig mode `trig`, then
+ * its 3-D FFT, written to K: a device array of 2 * 8 * nx*ny*nz floats, the
+ * complex spectrum interleaved (re, im), 8-byte aligned, x fastest.  Samples
+ * as mri_q (kx, ky, kz, rPhi, iPhi: M floats each; M = 0 gives K = 0).
+ *
+ * mri_toeplitz_apply: out = (F^H F + lambda I) in, from K, for SoA complex
+ * vectors of nx*ny*nz floats (rIn, iIn; rOut, iOut, which may be the same
+ * arrays as the inputs); accumulate = 1 adds into out.  Zero-padding to the
+ * doubled grid, forward FFT, product with K, inverse FFT, crop.
+ *
+ * mri_cg_solve: `iters` conjugate-gradient iterations on
+ * (F^H F + lambda I) x = b from K: rB, iB the right-hand side (typically
+ * F^H D from mri_fhd_grid), rX, iX the starting point on entry and the
+ * iterate on return; rnorms (device, iters + 1 doubles, 8-byte aligned)
+ * receives ||r_0|| .. ||r_iters||, r = b - (F^H F + lambda I) x.  The
+ * iteration's scalars stay on the device (no host synchronisation); once
+ * r = 0 the iterate stops changing.  Scratch from the stream-ordered pool:
+ * 8 nx*ny*nz complex values plus 6 nx*ny*nz floats.
+ *
+ * All three are asynchronous on `stream`.  MRI_ERR_SIZE for a grid edge that
+ * is not a power of two in 1 .. 512, a non-finite spacing or lambda, iters
+ * outside 0 .. 2^20; MRI_ERR_ALIGN for K or rnorms not 8-byte aligned; the
+ * other pointer checks as mri_fhd.
+ */
+/*
+ * The 3-D FFT under mri_toeplitz_*: in place on `data`, Lz x Ly x Lx complex
+ * values interleaved (re, im), x fastest, each length a power of two in
+ * 1 .. 1024; forward X[k] = sum_j x[j] e^{-2 pi i j.k / L}, inverse with
+ * e^{+...} and no scaling.  Asynchronous on `stream`.
+ */
+mri_status mri_fft3(float* data, int Lx, int Ly, int Lz, int inverse, void* stream);
+mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz,
+                               const float* rPhi, const float* iPhi, int64_t M,
+                               int nx, int ny, int nz, float hx, float hy, float hz,
+                               float* K, mri_trig trig, void* stream);
+mri_status mri_toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda,
+                              const float* rIn, const float* iIn, float* rOut, float* iOut,
+                              int accumulate, void* stream);
+mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda,
+                        const float* rB, const float* iB, float* rX, float* iX,
+                        int iters, double* rnorms, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
 

@@ -9,6 +9,7 @@ The CUDA library is built with ``non_cartesian_mri_gb300.build.build()``.
 _API = ("mu", "fhd", "q", "fhd_batched", "forward", "forward_grid", "fhd_grid", "q_grid", "fhd_batched_grid", "plan",
         "plan_grid", "plan_grid_batched",
         "device_errors", "microbench", "mma_probe", "wait_selftest",
+        "fft3", "toeplitz_kernel", "toeplitz_apply", "cg_solve",
         "status_string", "MriError", "load", "lib_path", "TRIG", "gather_timing")
 
 

@@ -83,6 +83,14 @@ def load():
         lib.mri_microbench.argtypes = [I, I, I, I64, P, P, P]
         lib.mri_wait_selftest.argtypes = [I, P]
         lib.mri_mma_probe.argtypes = [I, I, P, I64, P, P]
+        F = ctypes.c_float
+        lib.mri_fft3.argtypes = [P, I, I, I, I, P]
+        lib.mri_toeplitz_kernel.argtypes = [P] * 5 + [I64, I, I, I, F, F, F, P, I, P]
+        lib.mri_toeplitz_apply.argtypes = [P, I, I, I, F, P, P, P, P, I, P]
+        lib.mri_cg_solve.argtypes = [P, I, I, I, F, P, P, P, P, I, P, P]
+        for f in (lib.mri_fft3, lib.mri_toeplitz_kernel, lib.mri_toeplitz_apply,
+                  lib.mri_cg_solve):
+            f.restype = ctypes.c_int
         lib.mri_mma_probe.restype = ctypes.c_int
         lib.mri_wait_selftest.restype = ctypes.c_int
         lib.mri_microbench.restype = ctypes.c_int
@@ -445,3 +453,69 @@ def mma_probe(mode: int = 1, tiles: int = 4096, b_tiles: int = 1024):
             "pairs_per_sm_per_clk": float(pairs / cyc.median()),
             "pairs_per_sm_per_clk_min": float(pairs / cyc.max()),
             "cycles_median": float(cyc.median()), "sms": sms}
+
+
+def fft3(data, inverse: bool = False, stream=None):
+    """In-place 3-D FFT of a complex64 CUDA tensor of shape (Lz, Ly, Lx)
+    (see mri_fft3); returns the tensor."""
+    if data.dtype != torch.complex64 or not data.is_cuda or data.dim() != 3:
+        raise ValueError("fft3 takes a 3-D complex64 CUDA tensor")
+    data = data.contiguous()
+    Lz, Ly, Lx = data.shape
+    _check(load().mri_fft3(_ptr(data), Lx, Ly, Lz, int(bool(inverse)), _stream_handle(stream)),
+           "mri_fft3")
+    return data
+
+
+def toeplitz_kernel(kx, ky, kz, rPhi, iPhi, shape, spacing=(1.0, 1.0, 1.0), *, trig="accurate",
+                    stream=None):
+    """Spectrum of F^H F on a grid of shape (nz, ny, nx) with voxel spacing
+    (hx, hy, hz) (see mri_toeplitz_kernel): a complex64 tensor of shape
+    (2nz, 2ny, 2nx)."""
+    nz, ny, nx = (int(v) for v in shape)
+    kx, ky, kz, rPhi, iPhi = (_as_tensor(t) for t in (kx, ky, kz, rPhi, iPhi))
+    M = kx.numel()
+    _same_len("samples", (kx, ky, kz, rPhi, iPhi), M)
+    K = torch.empty((2 * nz, 2 * ny, 2 * nx), dtype=torch.complex64, device=kx.device)
+    hx, hy, hz = (float(v) for v in spacing)
+    _check(load().mri_toeplitz_kernel(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(rPhi), _ptr(iPhi), M,
+                                      nx, ny, nz, hx, hy, hz, _ptr(K), TRIG[trig],
+                                      _stream_handle(stream)), "mri_toeplitz_kernel")
+    return K
+
+
+def _grid_shape(K):
+    return K.shape[0] // 2, K.shape[1] // 2, K.shape[2] // 2
+
+
+def toeplitz_apply(K, rIn, iIn, *, lam: float = 0.0, accumulate=False, out=None, stream=None):
+    """(F^H F + lam I) applied to a complex vector on the grid of K (see
+    mri_toeplitz_apply); returns (rOut, iOut)."""
+    nz, ny, nx = _grid_shape(K)
+    rIn, iIn = _as_tensor(rIn), _as_tensor(iIn)
+    N = nx * ny * nz
+    _same_len("vector", (rIn, iIn), N)
+    r, i = _outputs(out, (N,), rIn.device)
+    _check(load().mri_toeplitz_apply(_ptr(K), nx, ny, nz, float(lam), _ptr(rIn), _ptr(iIn),
+                                     _ptr(r), _ptr(i), int(bool(accumulate)),
+                                     _stream_handle(stream)), "mri_toeplitz_apply")
+    return r, i
+
+
+def cg_solve(K, rB, iB, *, lam: float = 0.0, iters: int = 10, x0=None, stream=None):
+    """Conjugate gradients on (F^H F + lam I) x = b (see mri_cg_solve).
+    Returns (rX, iX, residual norms as a float64 CUDA tensor of iters + 1)."""
+    nz, ny, nx = _grid_shape(K)
+    rB, iB = _as_tensor(rB), _as_tensor(iB)
+    N = nx * ny * nz
+    _same_len("right-hand side", (rB, iB), N)
+    if x0 is None:
+        rX = torch.zeros(N, device=rB.device)
+        iX = torch.zeros(N, device=rB.device)
+    else:
+        rX, iX = (_as_tensor(t).clone() for t in x0)
+    norms = torch.empty(int(iters) + 1, dtype=torch.float64, device=rB.device)
+    _check(load().mri_cg_solve(_ptr(K), nx, ny, nz, float(lam), _ptr(rB), _ptr(iB), _ptr(rX),
+                               _ptr(iX), int(iters), _ptr(norms), _stream_handle(stream)),
+           "mri_cg_solve")
+    return rX, iX, norms

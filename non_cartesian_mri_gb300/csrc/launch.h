@@ -8,6 +8,7 @@
 #include "gather.cuh"
 #include "gather_grid.cuh"
 #include "gather_grid_tc.cuh"
+#include "fft.cuh"
 
 namespace mri {
 
@@ -65,6 +66,24 @@ cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fiel
 // voxel coordinates of a grid the tensor-core kernels do not take (kernels_grid.cu)
 cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
                                int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);
+
+// the find-rho step on a grid (kernels_toeplitz.cu): FFT twiddle table,
+// 3-D FFTs of the doubled grid, difference axes, Toeplitz product, CG
+cudaError_t launch_fft_twiddles(float2* tw, cudaStream_t s);
+cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const float2* tw,
+                        cudaStream_t s);
+cudaError_t launch_diff_axes(int nx, int ny, int nz, float hx, float hy, float hz, float* axes,
+                             cudaStream_t s);
+cudaError_t launch_interleave(const float* r, const float* i, int64_t n, float2* out, int grid,
+                              cudaStream_t s);
+cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float lambda,
+                                  const float* ir, const float* ii, float* outr, float* outi,
+                                  int accumulate, float2* work, const float2* tw, int grid,
+                                  cudaStream_t s);
+cudaError_t launch_cg(const float2* K, int nx, int ny, int nz, float lambda, const float* br,
+                      const float* bi, float* xr, float* xi, int iters, double* rr,
+                      float* vec, float2* work, double* scal, const float2* tw, int grid,
+                      int dot_blocks, cudaStream_t s);
 
 // per-TU dispatchers
 cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, dim3 grid,

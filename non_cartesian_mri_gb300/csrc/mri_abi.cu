@@ -1,6 +1,7 @@
 // mri_abi.cu -- the extern "C" entry points of libmri.so (declared in
 // include/mri.h): argument checks, launch planning, scratch, launches.
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -34,6 +35,7 @@ struct DeviceState {
     int sms = 0;
     cudaMemPool_t pool = nullptr;
     unsigned int* err = nullptr;
+    float2* fft_tw = nullptr;   // FFT twiddle table (fft.cuh), built with the state
     // gather-kernel timing window (mri_timing_begin / mri_timing_end)
     bool timing = false;
     int timed = 0;
@@ -85,6 +87,12 @@ mri_status device_state(DeviceState** out, int* dev_out)
             if (cudaGetSymbolAddress(&err, g_device_error_word) != cudaSuccess)
                 return cuda_fail();
             d.err = static_cast<unsigned int*>(err);
+            // FFT twiddles: one small table per device, written once
+            if (cudaMalloc(reinterpret_cast<void**>(&d.fft_tw),
+                           sizeof(float2) * (mri::kFftMaxLen / 2)) != cudaSuccess ||
+                mri::launch_fft_twiddles(d.fft_tw, 0) != cudaSuccess ||
+                cudaStreamSynchronize(0) != cudaSuccess)
+                return cuda_fail();
         }
         d.ready = true;
     }
@@ -941,6 +949,139 @@ mri_status mri_plan_grid_batched(int64_t B, int64_t M, int nx, int ny, int nz, i
                                  mri_plan* plan)
 {
     return plan_grid_call(MRI_KIND_FHD_BATCHED, B, M, nx, ny, nz, num_sms, plan);
+}
+
+// ---------------------------------------------------------------------------
+// the find-rho step on a grid: Toeplitz F^H F and conjugate gradients
+// ---------------------------------------------------------------------------
+namespace {
+mri_status check_toeplitz_grid(int nx, int ny, int nz)
+{
+    const int m = mri::kFftMaxLen / 2;   // the doubled grid must be one FFT length
+    auto ok = [&](int n) { return n >= 1 && n <= m && (n & (n - 1)) == 0; };
+    return (ok(nx) && ok(ny) && ok(nz)) ? MRI_OK : MRI_ERR_SIZE;
+}
+
+bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+}  // namespace
+
+mri_status mri_fft3(float* data, int Lx, int Ly, int Lz, int inverse, void* stream)
+{
+    if (inverse != 0 && inverse != 1) return MRI_ERR_MODE;
+    if (!mri::fft_len_ok(Lx) || !mri::fft_len_ok(Ly) || !mri::fft_len_ok(Lz))
+        return MRI_ERR_SIZE;
+    if (data != nullptr && !aligned8(data)) return MRI_ERR_ALIGN;
+    const void* vp[1] = {data};
+    DeviceState* d = nullptr;
+    mri_status st = prepare(0, 0, 1, 0, int64_t(Lx) * Ly * Lz, nullptr, 0, vp, 1, &d);
+    if (st != MRI_OK) return st;
+    if (mri::launch_fft3(reinterpret_cast<float2*>(data), Lx, Ly, Lz, inverse != 0, d->fft_tw,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return cuda_fail();
+    return MRI_OK;
+}
+
+mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz,
+                               const float* rPhi, const float* iPhi, int64_t M, int nx, int ny,
+                               int nz, float hx, float hy, float hz, float* K, mri_trig trig,
+                               void* stream)
+{
+    mri_status st = check_mode(int(trig), 0);
+    if (st != MRI_OK) return st;
+    if ((st = check_toeplitz_grid(nx, ny, nz)) != MRI_OK) return st;
+    if (!std::isfinite(hx) || !std::isfinite(hy) || !std::isfinite(hz)) return MRI_ERR_SIZE;
+    if (M < 0 || M > kMaxM) return MRI_ERR_SIZE;
+    if (K != nullptr && !aligned8(K)) return MRI_ERR_ALIGN;
+    const int64_t N2 = int64_t(8) * nx * ny * nz;   // the doubled grid
+    const void* sp[5] = {kx, ky, kz, rPhi, iPhi};
+    const void* vp[1] = {K};
+    DeviceState* d = nullptr;
+    if ((st = prepare(int(trig), 0, 1, M, N2, sp, 5, vp, 1, &d)) != MRI_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // scratch: the difference axes, Q (real and imaginary parts)
+    const int64_t axes_n = 2 * (int64_t(nx) + ny + nz);
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                size_t(align256(axes_n * 4) + 2 * N2 * 4), d->pool,
+                                s) != cudaSuccess)
+        return cuda_fail();
+    float* axes = reinterpret_cast<float*>(scratch);
+    float* q_r = reinterpret_cast<float*>(scratch + align256(axes_n * 4));
+    float* q_i = q_r + N2;
+    if (mri::launch_diff_axes(nx, ny, nz, hx, hy, hz, axes, s) != cudaSuccess) st = cuda_fail();
+    // Q(d) = sum_m |Phi_m|^2 e^{+i 2 pi k_m . d} on the difference grid: the
+    // grid Q path (tensor cores for 2 nx >= 8)
+    if (st == MRI_OK)
+        st = run_grid_call(true, 1, kx, ky, kz, axes, 2 * nx, axes + 2 * nx, 2 * ny,
+                           axes + 2 * nx + 2 * ny, 2 * nz, rPhi, iPhi, nullptr, nullptr, M, q_r,
+                           q_i, int(trig), 0, d, s);
+    float2* spec = reinterpret_cast<float2*>(K);
+    if (st == MRI_OK &&
+        (mri::launch_interleave(q_r, q_i, N2, spec, grid_for(N2, d->sms), s) != cudaSuccess ||
+         mri::launch_fft3(spec, 2 * nx, 2 * ny, 2 * nz, false, d->fft_tw, s) != cudaSuccess))
+        st = cuda_fail();
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
+mri_status mri_toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda,
+                              const float* rIn, const float* iIn, float* rOut, float* iOut,
+                              int accumulate, void* stream)
+{
+    mri_status st = check_mode(0, accumulate);
+    if (st != MRI_OK) return st;
+    if ((st = check_toeplitz_grid(nx, ny, nz)) != MRI_OK) return st;
+    if (!std::isfinite(lambda)) return MRI_ERR_SIZE;
+    if (K != nullptr && !aligned8(K)) return MRI_ERR_ALIGN;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* vp[5] = {K, rIn, iIn, rOut, iOut};
+    DeviceState* d = nullptr;
+    if ((st = prepare(0, accumulate, 1, 0, N, nullptr, 0, vp, 5, &d)) != MRI_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2* work = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&work), size_t(8 * N) * sizeof(float2),
+                                d->pool, s) != cudaSuccess)
+        return cuda_fail();
+    if (mri::launch_toeplitz_apply(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rIn,
+                                   iIn, rOut, iOut, accumulate, work, d->fft_tw,
+                                   grid_for(8 * N, d->sms), s) != cudaSuccess)
+        st = cuda_fail();
+    if (cudaFreeAsync(work, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
+mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, const float* rB,
+                        const float* iB, float* rX, float* iX, int iters, double* rnorms,
+                        void* stream)
+{
+    mri_status st = check_toeplitz_grid(nx, ny, nz);
+    if (st != MRI_OK) return st;
+    if (!std::isfinite(lambda) || iters < 0 || iters > (1 << 20)) return MRI_ERR_SIZE;
+    if ((K != nullptr && !aligned8(K)) || (rnorms != nullptr && !aligned8(rnorms)))
+        return MRI_ERR_ALIGN;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* vp[6] = {K, rB, iB, rX, iX, rnorms};
+    DeviceState* d = nullptr;
+    if ((st = prepare(0, 0, 1, 0, N, nullptr, 0, vp, 6, &d)) != MRI_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // scratch: r, p, Ap (SoA), the doubled-grid work array, the dot partials
+    const int dot_blocks = int(std::min<int64_t>(ceil_div(N, 256), int64_t(d->sms) * 4));
+    const int64_t vec_bytes = align256(6 * N * 4);
+    const int64_t work_bytes = align256(8 * N * int64_t(sizeof(float2)));
+    char* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
+                                size_t(vec_bytes + work_bytes + (dot_blocks + 1) * 8), d->pool,
+                                s) != cudaSuccess)
+        return cuda_fail();
+    float* vec = reinterpret_cast<float*>(scratch);
+    float2* work = reinterpret_cast<float2*>(scratch + vec_bytes);
+    double* scal = reinterpret_cast<double*>(scratch + vec_bytes + work_bytes);
+    if (mri::launch_cg(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rB, iB, rX, iX,
+                       iters, rnorms, vec, work, scal, d->fft_tw, grid_for(8 * N, d->sms),
+                       dot_blocks, s) != cudaSuccess)
+        st = cuda_fail();
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
 }
 
 const char* mri_status_string(mri_status status)

@@ -1,0 +1,176 @@
+"""The find-rho step on the GPU against the oracle (oracle/toeplitz.py).
+
+- mri_fft3 against numpy's FFT (fp64) on power-of-two shapes, forward and
+  inverse, contiguous and strided axes, a one-point axis;
+- mri_toeplitz_kernel against the FFT of the oracle's Q on the circular
+  difference grid;
+- mri_toeplitz_apply against the oracle's F^H F by its definition (plus
+  lambda I), non-cubic grids with unequal spacings, both trig paths,
+  accumulate and in place;
+- mri_cg_solve against the oracle's CG (same iterations, fp64 operator):
+  iterates and residual norms, and a reconstruction of a seeded image from
+  its own samples (D = F rho, b = F^H D) whose error falls with the
+  iterations;
+- argument errors.
+
+Tolerances: one Toeplitz product is Q (accurate path, ~2e-6) through two
+fp32 FFTs of the doubled grid (~1e-7 log2 per transform): 1e-5 accurate,
+2e-4 fast.  CG amplifies the per-iteration error by the conditioning of the
+operator; after a few iterations on these well-sampled problems 1e-4 holds
+for the iterate and the residual norms.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import toeplitz as T
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"accurate": 1e-5, "fast": 2e-4}
+
+
+@pytest.fixture(scope="module")
+def mri():
+    from non_cartesian_mri_gb300 import build
+    build.build()
+    import non_cartesian_mri_gb300 as m
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def cplx(r, i):
+    return r.cpu().numpy().astype(np.float64) + 1j * i.cpu().numpy()
+
+
+def samples(M, seed, kmax=0.5):
+    rng = np.random.default_rng(seed)
+    k = rng.uniform(-kmax, kmax, (3, M)).astype(np.float32)
+    rPhi = rng.standard_normal(M).astype(np.float32)
+    iPhi = rng.standard_normal(M).astype(np.float32)
+    return k, rPhi, iPhi
+
+
+@pytest.mark.parametrize("shape", [(4, 8, 16), (2, 1, 32), (1, 1, 1024), (16, 16, 16),
+                                   (8, 2, 512), (1, 1, 1)])
+def test_fft3_matches_numpy(mri, shape):
+    rng = np.random.default_rng(sum(shape))
+    x = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    got = mri.fft3(dev(x).clone()).cpu().numpy()
+    ref = np.fft.fftn(x.astype(np.complex128))
+    assert oracle.rel_l2(got, ref) < 1e-6
+    back = mri.fft3(dev(x).clone(), inverse=True).cpu().numpy()
+    assert oracle.rel_l2(back, np.fft.ifftn(x.astype(np.complex128)) * x.size) < 1e-6
+
+
+@pytest.mark.parametrize("shape,spacing", [((2, 4, 8), (1.0, 0.75, 1.5)),
+                                           ((4, 4, 4), (1.0, 1.0, 1.0)),
+                                           ((1, 2, 16), (0.5, 2.0, 1.0))])
+def test_toeplitz_kernel_is_the_spectrum_of_q(mri, shape, spacing):
+    k, rPhi, iPhi = samples(700, 11)
+    K = mri.toeplitz_kernel(dev(k[0]), dev(k[1]), dev(k[2]), dev(rPhi), dev(iPhi), shape,
+                            spacing).cpu().numpy()
+    Qc = T.q_difference_grid(k[0], k[1], k[2], rPhi, iPhi, shape, spacing)
+    assert oracle.rel_l2(K, np.fft.fftn(Qc)) < 1e-5
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+@pytest.mark.parametrize("shape,spacing,lam", [((2, 4, 8), (1.0, 0.75, 1.5), 0.0),
+                                               ((4, 4, 4), (1.0, 1.0, 1.0), 0.7),
+                                               ((1, 2, 16), (0.5, 2.0, 1.0), 2.5),
+                                               ((8, 8, 8), (1.0, 1.0, 1.0), 0.1)])
+def test_toeplitz_apply_matches_fhf(mri, shape, spacing, lam, trig):
+    k, rPhi, iPhi = samples(900, 12 + shape[2])
+    K = mri.toeplitz_kernel(dev(k[0]), dev(k[1]), dev(k[2]), dev(rPhi), dev(iPhi), shape,
+                            spacing, trig=trig)
+    rng = np.random.default_rng(13)
+    v = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    r, i = mri.toeplitz_apply(K, dev(v.real.reshape(-1)), dev(v.imag.reshape(-1)), lam=lam)
+    Qc = T.q_difference_grid(k[0], k[1], k[2], rPhi, iPhi, shape, spacing)
+    ref = (T.fhf_direct(Qc, v) + lam * v).reshape(-1)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL[trig]
+    # accumulate adds onto what is there; in place reads before it writes
+    out = (torch.full_like(r, 0.5), torch.full_like(i, -1.0))
+    mri.toeplitz_apply(K, dev(v.real.reshape(-1)), dev(v.imag.reshape(-1)), lam=lam,
+                       accumulate=True, out=out)
+    assert oracle.rel_l2(cplx(out[0] - 0.5, out[1] + 1.0), ref) <= TOL[trig]
+    vr, vi = dev(v.real.reshape(-1)), dev(v.imag.reshape(-1))
+    mri.toeplitz_apply(K, vr, vi, lam=lam, out=(vr, vi))
+    assert oracle.rel_l2(cplx(vr, vi), ref) <= TOL[trig]
+    assert mri.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("lam", [0.05, 1.0])
+def test_cg_matches_the_oracle(mri, lam):
+    shape, spacing = (4, 8, 8), (1.0, 1.0, 1.0)
+    k, rPhi, iPhi = samples(3000, 21)
+    K = mri.toeplitz_kernel(dev(k[0]), dev(k[1]), dev(k[2]), dev(rPhi), dev(iPhi), shape,
+                            spacing)
+    Qc = T.q_difference_grid(k[0], k[1], k[2], rPhi, iPhi, shape, spacing)
+    rng = np.random.default_rng(22)
+    b = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    x0 = (0.1 * rng.standard_normal(shape)).astype(np.complex64)
+    iters = 6
+    xr, xi, norms = mri.cg_solve(K, dev(b.real.reshape(-1)), dev(b.imag.reshape(-1)), lam=lam,
+                                 iters=iters, x0=(dev(x0.real.reshape(-1)),
+                                                  dev(x0.imag.reshape(-1))))
+    apply = lambda v: T.fhf_fft(Qc, v.reshape(shape)).reshape(-1)   # noqa: E731
+    ref_x, ref_n = T.cg(apply, b.reshape(-1), x0.reshape(-1), lam, iters)
+    assert oracle.rel_l2(cplx(xr, xi), ref_x) < 1e-4
+    assert np.abs(norms.cpu().numpy() - ref_n).max() < 1e-4 * ref_n[0]
+    assert mri.device_errors(clear=True) == 0
+
+
+def test_cg_reconstructs_an_image_from_its_samples(mri):
+    """D = F rho_true (the forward model with the sensitivity), b = F^H D;
+    CG on (F^H F + lam I) x = b approaches rho_true."""
+    shape = (8, 16, 16)
+    nz, ny, nx = shape
+    M = 6 * nx * ny * nz
+    k, _, _ = samples(M, 31)
+    rPhi = np.ones(M, np.float32)
+    iPhi = np.zeros(M, np.float32)
+    xs = np.arange(nx, dtype=np.float32)
+    ys = np.arange(ny, dtype=np.float32)
+    zs = np.arange(nz, dtype=np.float32)
+    z, y, x = np.meshgrid(zs, ys, xs, indexing="ij")
+    rho = (np.exp(-((x - 7.5) ** 2 + (y - 6.0) ** 2) / 20.0 - (z - 3.5) ** 2 / 6.0)
+           * (1.0 + 0.5j)).astype(np.complex64)
+    kk = [dev(a) for a in k]
+    ax = [dev(xs), dev(ys), dev(zs)]
+    dr, di = mri.forward_grid(*kk, *ax, dev(rho.real.reshape(-1)), dev(rho.imag.reshape(-1)),
+                              trig="accurate")
+    br, bi = mri.fhd_grid(*kk, *ax, dev(rPhi), dev(iPhi), dr, di, trig="accurate")
+    K = mri.toeplitz_kernel(*kk, dev(rPhi), dev(iPhi), shape)
+    errs = []
+    for iters in (2, 8, 30):
+        xr, xi, norms = mri.cg_solve(K, br, bi, lam=1e-3, iters=iters)
+        errs.append(oracle.rel_l2(cplx(xr, xi), rho.reshape(-1)))
+    assert errs[0] > errs[1] > errs[2]
+    assert errs[2] < 1e-2
+    n = norms.cpu().numpy()
+    assert n[-1] < 1e-3 * n[0]
+    assert mri.device_errors(clear=True) == 0
+
+
+def test_toeplitz_argument_errors(mri):
+    lib = mri.load()
+    K = torch.zeros((8, 8, 8), dtype=torch.complex64, device="cuda")
+    v = torch.zeros(64, device="cuda")
+    P = ctypes.c_void_p
+    for nx, ny, nz in ((3, 4, 4), (4, 4, 1024), (0, 4, 4)):
+        assert lib.mri_toeplitz_apply(P(K.data_ptr()), nx, ny, nz, 0.0, P(v.data_ptr()),
+                                      P(v.data_ptr()), P(v.data_ptr()), P(v.data_ptr()), 0,
+                                      None) == 2   # MRI_ERR_SIZE
+    assert lib.mri_toeplitz_apply(P(K.data_ptr() + 4), 4, 4, 4, 0.0, P(v.data_ptr()),
+                                  P(v.data_ptr()), P(v.data_ptr()), P(v.data_ptr()), 0,
+                                  None) == 3       # MRI_ERR_ALIGN
+    assert lib.mri_fft3(P(K.data_ptr()), 6, 8, 8, 0, None) == 2
+    assert lib.mri_fft3(P(K.data_ptr()), 8, 8, 8, 2, None) == 5   # MRI_ERR_MODE
