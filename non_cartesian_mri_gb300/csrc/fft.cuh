@@ -5,13 +5,18 @@
 // Layout: float2 (re, im) interleaved, x fastest; an axis of length L (a
 // power of two, 2 .. kFftMaxLen) sits between `outer` slabs and `inner`
 // consecutive elements: element j of line (o, i) is a[(o L + j) inner + i].
-// A CTA transforms kFftLines lines: kFftLines consecutive i (inner > 1, so
-// that a warp's loads cover consecutive addresses) or kFftLines consecutive
-// o (inner == 1, each line contiguous).  The lines go to shared memory in
-// bit-reversed order; log2 L radix-2 butterfly stages run in place, one CTA
-// barrier per stage; the result is stored back in natural order.  Twiddles
-// e^{-2 pi i k / kFftMaxLen} come from a per-device table evaluated in double
-// precision (the twiddle kernel of kernels_toeplitz.cu); the inverse
+// A CTA transforms W lines (16, or 8 for L = 1024): W consecutive i when
+// inner > 1 (so that a warp's loads cover consecutive addresses), W
+// consecutive o when inner == 1 (each line contiguous).  The lines go to
+// shared memory in natural order and the transform is a Stockham
+// auto-sorting FFT: radix-4 passes (one radix-2 pass when log2 L is odd),
+// each thread reading 4 values of a line at stride L / 4, multiplying by
+// the twiddles of the pass and doing the 4-point DFT in registers, then,
+// after a barrier, writing them back in place where the final output ends
+// up in natural order -- no bit reversal, one buffer (six CTAs per SM at
+// L = 256).  Twiddles e^{-2 pi i k / kFftMaxLen} come from a per-device table
+// evaluated in double precision (the twiddle kernel of kernels_toeplitz.cu)
+// and are staged for the line length in shared memory; the inverse
 // transform conjugates them and does not scale (the caller divides by the
 // size).
 #pragma once
@@ -20,71 +25,156 @@
 
 namespace mri {
 
-constexpr int kFftMaxLen = 1024;
-constexpr int kFftLines = 16;                   // lines per CTA
+constexpr int kFftMaxLen = 1024;              // 2^10
 constexpr int kFftThreads = 256;
 
 inline bool fft_len_ok(int64_t L) { return L >= 1 && L <= kFftMaxLen && (L & (L - 1)) == 0; }
 
-inline size_t fft_smem_bytes(int L) { return size_t(kFftLines) * (L + 1) * sizeof(float2); }
+// lines per CTA: 16 (2^4), 8 at the largest length (shared memory)
+__host__ __device__ constexpr int fft_log2_lines(int log2L) { return log2L >= 10 ? 3 : 4; }
 
-__device__ __forceinline__ unsigned int bit_reverse(unsigned int j, int bits)
+// Shared memory: W lines of L + 1 values (the pad keeps the W lines of a
+// strided axis, stored column by column, in different banks), then L
+// twiddles.
+inline size_t fft_smem_total(int log2L)
 {
-    return __brev(j) >> (32 - bits);
+    const size_t L = size_t(1) << log2L;
+    return (size_t(1) << fft_log2_lines(log2L)) * (L + 1) * sizeof(float2) + L * sizeof(float2);
 }
 
-template <bool INVERSE>
-__global__ void __launch_bounds__(kFftThreads) fft_axis_kernel(float2* a, int L, int log2L,
-                                                               int64_t outer, int64_t inner,
-                                                               const float2* tw)
+// One Stockham pass of radix R = 2^LOG2R over the W lines in `buf`, in
+// place: every thread first reads its butterflies' R inputs (times the
+// pass's twiddles) and does the R-point DFTs in registers, then, after a
+// barrier, writes the outputs.  Ns = 2^log2Ns is the length of the
+// sub-transforms already done.
+template <bool INVERSE, int LOG2R, int LOG2L>
+__device__ __forceinline__ void fft_pass(float2* buf, const float2* tws, int log2Ns)
 {
-    extern __shared__ float2 fft_sm[];
-    const int stride = L + 1;                         // one pad element per line
-    const int64_t lines = outer * inner;
-    const int64_t group = int64_t(blockIdx.x) * kFftLines;
-    const bool contiguous = inner == 1;
-    // global index of element j of this CTA's line w
-    auto gidx = [&](int w, int j) -> int64_t {
-        if (contiguous) return (group + w) * L + j;
-        const int64_t line = group + w;               // line = o * inner + i
-        const int64_t o = line / inner;
-        const int64_t i = line - o * inner;
-        return (o * L + j) * inner + i;
-    };
-    const int total = kFftLines * L;
-    for (int e = threadIdx.x; e < total; e += kFftThreads) {
-        int w, j;
-        if (contiguous) { w = e / L; j = e - w * L; }
-        else { j = e / kFftLines; w = e - j * kFftLines; }
-        if (group + w < lines)
-            fft_sm[w * stride + bit_reverse(unsigned(j), log2L)] = a[gidx(w, j)];
+    constexpr int R = 1 << LOG2R;
+    constexpr int log2L = LOG2L;
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int log2per = LOG2L - LOG2R;          // butterflies per line
+    constexpr int per = 1 << log2per;
+    constexpr int work = 1 << (log2W + log2per);
+    // butterflies one thread holds between the read and the write half
+    constexpr int ITEMS = work >= kFftThreads ? work / kFftThreads : 1;
+    const int sh = log2L - log2Ns - LOG2R;          // twiddle index unit
+    const int ns_mask = (1 << log2Ns) - 1;
+    float2 y[ITEMS][R];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int b = threadIdx.x + it * kFftThreads;
+        if (b < work) {
+            const int w = b >> log2per;
+            const int j = b & (per - 1);
+            const int jm = j & ns_mask;
+            const float2* in = buf + w * (per << LOG2R | 1);
+            float2 v[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 x = in[j + r * per];
+                if (r > 0) {
+                    const float2 t = tws[(jm * r) << sh];
+                    x = make_float2(x.x * t.x - x.y * t.y, x.x * t.y + x.y * t.x);
+                }
+                v[r] = x;
+            }
+            if (R == 4) {
+                const float2 a0 = make_float2(v[0].x + v[2].x, v[0].y + v[2].y);
+                const float2 a1 = make_float2(v[0].x - v[2].x, v[0].y - v[2].y);
+                const float2 a2 = make_float2(v[1].x + v[3 % R].x, v[1].y + v[3 % R].y);
+                const float2 a3 = make_float2(v[1].x - v[3 % R].x, v[1].y - v[3 % R].y);
+                // a3 times -i (forward) or +i (inverse)
+                const float2 b3 = INVERSE ? make_float2(-a3.y, a3.x) : make_float2(a3.y, -a3.x);
+                y[it][0] = make_float2(a0.x + a2.x, a0.y + a2.y);
+                y[it][1 % R] = make_float2(a1.x + b3.x, a1.y + b3.y);
+                y[it][2 % R] = make_float2(a0.x - a2.x, a0.y - a2.y);
+                y[it][3 % R] = make_float2(a1.x - b3.x, a1.y - b3.y);
+            } else {
+                y[it][0] = make_float2(v[0].x + v[1 % R].x, v[0].y + v[1 % R].y);
+                y[it][1 % R] = make_float2(v[0].x - v[1 % R].x, v[0].y - v[1 % R].y);
+            }
+        }
     }
     __syncthreads();
-    const int half_total = kFftLines * (L >> 1);
-    for (int s = 1; s <= log2L; ++s) {
-        const int half = 1 << (s - 1);
-        const int tw_step = kFftMaxLen >> s;          // e^{-2 pi i pos / 2 half}
-        for (int b = threadIdx.x; b < half_total; b += kFftThreads) {
-            const int w = b / (L >> 1);
-            const int bb = b - w * (L >> 1);
-            const int pos = bb & (half - 1);
-            const int i0 = ((bb >> (s - 1)) << s) + pos;
-            float2* line = fft_sm + w * stride;
-            float2 t = tw[pos * tw_step];
-            if (INVERSE) t.y = -t.y;
-            const float2 u = line[i0];
-            const float2 v0 = line[i0 + half];
-            const float2 v = make_float2(v0.x * t.x - v0.y * t.y, v0.x * t.y + v0.y * t.x);
-            line[i0] = make_float2(u.x + v.x, u.y + v.y);
-            line[i0 + half] = make_float2(u.x - v.x, u.y - v.y);
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int b = threadIdx.x + it * kFftThreads;
+        if (b < work) {
+            const int w = b >> log2per;
+            const int j = b & (per - 1);
+            float2* out = buf + w * (per << LOG2R | 1);
+            const int base = ((j >> log2Ns) << (log2Ns + LOG2R)) + (j & ns_mask);
+#pragma unroll
+            for (int r = 0; r < R; ++r) out[base + (r << log2Ns)] = y[it][r];
         }
-        __syncthreads();
     }
+    __syncthreads();
+}
+
+template <bool INVERSE, int LOG2L>
+__global__ void __launch_bounds__(kFftThreads) fft_axis_kernel(float2* a, int log2inner,
+                                                               int64_t lines, const float2* tw)
+{
+    extern __shared__ float2 fft_sm[];
+    constexpr int log2L = LOG2L;
+    constexpr int L = 1 << LOG2L;
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int W = 1 << log2W;
+    float2* const buf = fft_sm;
+    constexpr int stride = L + 1;                     // padded line
+    float2* const tws = fft_sm + W * stride;          // e^{-+2 pi i m / L}, m < L
+    const int64_t group = int64_t(blockIdx.x) << log2W;
+    const bool contiguous = log2inner == 0;
+    const int64_t inner_mask = (int64_t(1) << log2inner) - 1;
+    // global index of element j of this CTA's line w (line = o * inner + i)
+    auto gidx = [&](int w, int j) -> int64_t {
+        const int64_t line = group + w;
+        if (contiguous) return (line << log2L) + j;
+        const int64_t o = line >> log2inner;
+        return (((o << log2L) + j) << log2inner) + (line & inner_mask);
+    };
+    for (int m = threadIdx.x; m < L; m += kFftThreads) {
+        // the table holds e^{-2 pi i k / 2^10} for k < 2^9; the upper half of
+        // the circle is its negation
+        const int h = m < (L >> 1) ? m : m - (L >> 1);
+        float2 t = tw[h << (10 - log2L)];
+        if (m >= (L >> 1)) t = make_float2(-t.x, -t.y);
+        if (INVERSE) t.y = -t.y;
+        tws[m] = t;
+    }
+    constexpr int total = W << log2L;
+    // eight loads in flight per thread before their shared-memory stores
+    constexpr int U = 8;
+    for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
+        float2 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * kFftThreads;
+            int w, j;
+            if (contiguous) { w = e >> log2L; j = e & (L - 1); }
+            else { j = e >> log2W; w = e & (W - 1); }
+            v[u] = (e < total && group + w < lines) ? a[gidx(w, j)] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * kFftThreads;
+            int w, j;
+            if (contiguous) { w = e >> log2L; j = e & (L - 1); }
+            else { j = e >> log2W; w = e & (W - 1); }
+            if (e < total) buf[w * stride + j] = v[u];
+        }
+    }
+    __syncthreads();
+    int log2Ns = 0;
+    if constexpr (LOG2L >= 2)
+        for (; log2L - log2Ns >= 2; log2Ns += 2) fft_pass<INVERSE, 2, LOG2L>(buf, tws, log2Ns);
+    if constexpr (LOG2L % 2 == 1) fft_pass<INVERSE, 1, LOG2L>(buf, tws, log2Ns);
     for (int e = threadIdx.x; e < total; e += kFftThreads) {
         int w, j;
-        if (contiguous) { w = e / L; j = e - w * L; }
-        else { j = e / kFftLines; w = e - j * kFftLines; }
-        if (group + w < lines) a[gidx(w, j)] = fft_sm[w * stride + j];
+        if (contiguous) { w = e >> log2L; j = e & (L - 1); }
+        else { j = e >> log2W; w = e & (W - 1); }
+        if (group + w < lines) a[gidx(w, j)] = buf[w * stride + j];
     }
 }
 

@@ -9,6 +9,7 @@
 // IFFT(FFT(Q) * FFT(pad v)) / |2n|.  All buffers are device memory; the
 // CG scalars stay on the device (no host round trip per iteration).
 #include <cstdint>
+#include <type_traits>
 
 #include "fft.cuh"
 #include "launch.h"
@@ -240,18 +241,36 @@ cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const f
     for (int ax = 0; ax < 3; ++ax) {
         if (L[ax] == 1) continue;
         const int len = int(L[ax]);
-        const size_t smem = fft_smem_bytes(len);
-        const int64_t groups = (outer[ax] * inner[ax] + kFftLines - 1) / kFftLines;
+        const int log2L = log2i(len);
+        const size_t smem = fft_smem_total(log2L);
+        const int64_t lines = outer[ax] * inner[ax];
+        const int64_t W = int64_t(1) << fft_log2_lines(log2L);
+        const int64_t groups = (lines + W - 1) / W;
         auto go = [&](auto kernel) -> cudaError_t {
             const cudaError_t e = cudaFuncSetAttribute(
                 kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (e != cudaSuccess) return e;
-            kernel<<<unsigned(groups), kFftThreads, smem, s>>>(a, len, log2i(len), outer[ax],
-                                                               inner[ax], tw);
+            kernel<<<unsigned(groups), kFftThreads, smem, s>>>(a, log2i(int(inner[ax])), lines,
+                                                               tw);
             return cudaGetLastError();
         };
-        const cudaError_t e =
-            inverse ? go(fft_axis_kernel<true>) : go(fft_axis_kernel<false>);
+        auto by_length = [&](auto inv) -> cudaError_t {
+            constexpr bool I = decltype(inv)::value;
+            switch (log2L) {
+                case 1: return go(fft_axis_kernel<I, 1>);
+                case 2: return go(fft_axis_kernel<I, 2>);
+                case 3: return go(fft_axis_kernel<I, 3>);
+                case 4: return go(fft_axis_kernel<I, 4>);
+                case 5: return go(fft_axis_kernel<I, 5>);
+                case 6: return go(fft_axis_kernel<I, 6>);
+                case 7: return go(fft_axis_kernel<I, 7>);
+                case 8: return go(fft_axis_kernel<I, 8>);
+                case 9: return go(fft_axis_kernel<I, 9>);
+                case 10: return go(fft_axis_kernel<I, 10>);
+            }
+            return cudaErrorInvalidValue;
+        };
+        const cudaError_t e = inverse ? by_length(std::true_type{}) : by_length(std::false_type{});
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
