@@ -102,6 +102,9 @@ def parse_args():
                          "workload's trajectory and grid instead of F^H D (profiling aid; "
                          "implies --no-paths --no-e2e)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--find-rho", action="store_true",
+                    help="also measure the find-rho step (Toeplitz product, CG iteration) when "
+                         "the other paths are skipped")
     return ap.parse_args()
 
 
@@ -468,6 +471,65 @@ def e2e(torch, mri, dist, w, trig, steps, warmup, grid=False):
             "ms_per_step": round(mean_s * 1e3, 3)}
 
 
+# The find-rho step (CG on (F^H F + lambda I) x = F^H D with the Toeplitz
+# product): HBM-bound.  Bytes per product for N voxels, stage by stage (the
+# work array holds half the doubled grid, 4N complex values of 8 bytes; the
+# spectrum K the whole doubled grid, 8N):
+#   x forward   read v (8N), write 2N values (16N)
+#   y forward   read 2N values (16N), write 4N (32N)
+#   z           read 4N (32N) and K (64N), write 4N (32N)
+#   y inverse   read 4N (32N), write 2N (16N)
+#   x inverse   read 2N (16N) and v (8N), write the result (8N)
+# = 280 bytes per voxel.  The compulsory part (v, K and the result once) is
+# 80.  A CG iteration adds the dot product p.Ap (16N), the x / r update
+# (48N) and the p update (24N).
+TOEPLITZ_BYTES_PER_VOXEL = 8 + 16 + 16 + 32 + 32 + 64 + 32 + 32 + 16 + 16 + 8 + 8
+TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL = 8 + 64 + 8
+CG_EXTRA_BYTES_PER_VOXEL = 16 + 48 + 24
+
+
+def find_rho(torch, mri, dist, args, flush, peaks):
+    """Toeplitz product and CG iteration on the headline trajectory and grid."""
+    w = wl.make_workload(HEADLINE)
+    t = to_dev(w, torch)
+    shape = (w.L, w.L, w.L)
+    K = mri.toeplitz_kernel(t["kx"], t["ky"], t["kz"], t["rPhi"], t["iPhi"], shape,
+                            trig=args.trig)
+    rng = np.random.default_rng(77)
+    v = [torch.from_numpy(rng.standard_normal(w.N).astype(np.float32)).cuda() for _ in range(2)]
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    out = {"workload": f"{w.name} trajectory, {w.L}^3 grid (doubled grid {2 * w.L}^3)",
+           "trig_of_q": args.trig}
+    iters = 10
+    for name, fn, per_step, bpv in (
+            ("toeplitz_apply", lambda: mri.toeplitz_apply(K, v[0], v[1], lam=0.01), 1,
+             TOEPLITZ_BYTES_PER_VOXEL),
+            ("cg_iteration", lambda: mri.cg_solve(K, v[0], v[1], lam=0.01, iters=iters), iters,
+             TOEPLITZ_BYTES_PER_VOXEL + CG_EXTRA_BYTES_PER_VOXEL)):
+        res = timed_steps(torch, mri, dist, fn, args.steps, args.warmup, flush)
+        ms = statistics.mean(res["step_ms"]) / per_step
+        achieved = bpv * w.N / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "value": round(w.N / (ms * 1e-3) / 1e9, 3),
+                     "unit": "Gvoxels/s",
+                     "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                                  "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                                  "traffic": None,
+                                  "algorithmic_bytes_per_voxel": bpv,
+                                  "compulsory_bytes_per_voxel":
+                                      TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL}}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    mri.toeplitz_kernel(t["kx"], t["ky"], t["kz"], t["rPhi"], t["iPhi"], shape, trig=args.trig)
+    t1.record()
+    torch.cuda.synchronize()
+    out["toeplitz_kernel_ms_once"] = round(t0.elapsed_time(t1), 2)
+    del t, K, v
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import non_cartesian_mri_gb300 as mri
@@ -625,6 +687,9 @@ def run_ours(args):
             del pt
             torch.cuda.empty_cache()
         line["paths"] = paths
+    if world == 1 and args.workload == HEADLINE and not args.grid_edge and not args.forward and (
+            not args.no_paths or args.find_rho):
+        line["find_rho"] = find_rho(torch, mri, dist, args, flush, peaks)
 
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl.make_workload(args.workload, L=args.grid_edge))

@@ -17,8 +17,10 @@
 // L = 256).  Twiddles e^{-2 pi i k / kFftMaxLen} come from a per-device table
 // evaluated in double precision (the twiddle kernel of kernels_toeplitz.cu)
 // and are staged for the line length in shared memory; the inverse
-// transform conjugates them and does not scale (the caller divides by the
-// size).
+// transform conjugates them where it uses them and does not scale (the
+// caller divides by the size).  The pieces (stage the twiddles, load a tile,
+// run the passes, store a tile) are separate so that a kernel can do more
+// than one transform on a tile, or fuse the work on either side of one.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -75,7 +77,10 @@ __device__ __forceinline__ void fft_pass(float2* buf, const float2* tws, int log
                 float2 x = in[j + r * per];
                 if (r > 0) {
                     const float2 t = tws[(jm * r) << sh];
-                    x = make_float2(x.x * t.x - x.y * t.y, x.x * t.y + x.y * t.x);
+                    if (INVERSE)   // x * conj(t)
+                        x = make_float2(x.x * t.x + x.y * t.y, x.y * t.x - x.x * t.y);
+                    else
+                        x = make_float2(x.x * t.x - x.y * t.y, x.x * t.y + x.y * t.x);
                 }
                 v[r] = x;
             }
@@ -112,39 +117,42 @@ __device__ __forceinline__ void fft_pass(float2* buf, const float2* tws, int log
     __syncthreads();
 }
 
-template <bool INVERSE, int LOG2L>
-__global__ void __launch_bounds__(kFftThreads) fft_axis_kernel(float2* a, int log2inner,
-                                                               int64_t lines, const float2* tw)
+// The tile of a CTA: W lines of L values.  Element e of the tile is line
+// w, position j: on a contiguous axis w = e / L, j = e % L (a warp reads 32
+// consecutive values of one line); on a strided axis j = e / W, w = e % W (a
+// warp reads the same position of W consecutive lines, which are adjacent
+// in memory).
+template <int LOG2L>
+__device__ __forceinline__ void fft_tile_elem(bool contiguous, int e, int& w, int& j)
 {
-    extern __shared__ float2 fft_sm[];
-    constexpr int log2L = LOG2L;
-    constexpr int L = 1 << LOG2L;
     constexpr int log2W = fft_log2_lines(LOG2L);
-    constexpr int W = 1 << log2W;
-    float2* const buf = fft_sm;
-    constexpr int stride = L + 1;                     // padded line
-    float2* const tws = fft_sm + W * stride;          // e^{-+2 pi i m / L}, m < L
-    const int64_t group = int64_t(blockIdx.x) << log2W;
-    const bool contiguous = log2inner == 0;
-    const int64_t inner_mask = (int64_t(1) << log2inner) - 1;
-    // global index of element j of this CTA's line w (line = o * inner + i)
-    auto gidx = [&](int w, int j) -> int64_t {
-        const int64_t line = group + w;
-        if (contiguous) return (line << log2L) + j;
-        const int64_t o = line >> log2inner;
-        return (((o << log2L) + j) << log2inner) + (line & inner_mask);
-    };
+    if (contiguous) { w = e >> LOG2L; j = e & ((1 << LOG2L) - 1); }
+    else { j = e >> log2W; w = e & ((1 << log2W) - 1); }
+}
+
+// Twiddles of length L in shared memory: tws[m] = e^{-2 pi i m / L}, m < L,
+// from the per-device table of e^{-2 pi i k / 2^10}, k < 2^9 (the upper half
+// of the circle is its negation).
+template <int LOG2L>
+__device__ __forceinline__ void fft_stage_twiddles(float2* tws, const float2* tw)
+{
+    constexpr int L = 1 << LOG2L;
     for (int m = threadIdx.x; m < L; m += kFftThreads) {
-        // the table holds e^{-2 pi i k / 2^10} for k < 2^9; the upper half of
-        // the circle is its negation
         const int h = m < (L >> 1) ? m : m - (L >> 1);
-        float2 t = tw[h << (10 - log2L)];
+        float2 t = tw[h << (10 - LOG2L)];
         if (m >= (L >> 1)) t = make_float2(-t.x, -t.y);
-        if (INVERSE) t.y = -t.y;
         tws[m] = t;
     }
-    constexpr int total = W << log2L;
-    // eight loads in flight per thread before their shared-memory stores
+}
+
+// Fill the tile: buf[w][j] = get(w, j) for every element, eight loads in
+// flight per thread before their shared-memory stores.  get returns zero
+// for lines past the end and for positions known to be zero.
+template <int LOG2L, class Get>
+__device__ __forceinline__ void fft_load_tile(float2* buf, bool contiguous, Get get)
+{
+    constexpr int total = (1 << fft_log2_lines(LOG2L)) << LOG2L;
+    constexpr int stride = (1 << LOG2L) + 1;
     constexpr int U = 8;
     for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
         float2 v[U];
@@ -152,30 +160,73 @@ __global__ void __launch_bounds__(kFftThreads) fft_axis_kernel(float2* a, int lo
         for (int u = 0; u < U; ++u) {
             const int e = e0 + u * kFftThreads;
             int w, j;
-            if (contiguous) { w = e >> log2L; j = e & (L - 1); }
-            else { j = e >> log2W; w = e & (W - 1); }
-            v[u] = (e < total && group + w < lines) ? a[gidx(w, j)] : make_float2(0.f, 0.f);
+            fft_tile_elem<LOG2L>(contiguous, e, w, j);
+            v[u] = e < total ? get(w, j) : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = e0 + u * kFftThreads;
             int w, j;
-            if (contiguous) { w = e >> log2L; j = e & (L - 1); }
-            else { j = e >> log2W; w = e & (W - 1); }
+            fft_tile_elem<LOG2L>(contiguous, e, w, j);
             if (e < total) buf[w * stride + j] = v[u];
         }
     }
-    __syncthreads();
-    int log2Ns = 0;
-    if constexpr (LOG2L >= 2)
-        for (; log2L - log2Ns >= 2; log2Ns += 2) fft_pass<INVERSE, 2, LOG2L>(buf, tws, log2Ns);
-    if constexpr (LOG2L % 2 == 1) fft_pass<INVERSE, 1, LOG2L>(buf, tws, log2Ns);
+}
+
+// Hand every element of the tile to put(w, j, value).
+template <int LOG2L, class Put>
+__device__ __forceinline__ void fft_store_tile(const float2* buf, bool contiguous, Put put)
+{
+    constexpr int total = (1 << fft_log2_lines(LOG2L)) << LOG2L;
+    constexpr int stride = (1 << LOG2L) + 1;
     for (int e = threadIdx.x; e < total; e += kFftThreads) {
         int w, j;
-        if (contiguous) { w = e >> log2L; j = e & (L - 1); }
-        else { j = e >> log2W; w = e & (W - 1); }
-        if (group + w < lines) a[gidx(w, j)] = buf[w * stride + j];
+        fft_tile_elem<LOG2L>(contiguous, e, w, j);
+        put(w, j, buf[w * stride + j]);
     }
+}
+
+// The whole transform of the W lines in buf (natural order in and out).
+template <bool INVERSE, int LOG2L>
+__device__ __forceinline__ void fft_tile_passes(float2* buf, const float2* tws)
+{
+    int log2Ns = 0;
+    if constexpr (LOG2L >= 2) {
+#pragma unroll
+        for (; LOG2L - log2Ns >= 2; log2Ns += 2) fft_pass<INVERSE, 2, LOG2L>(buf, tws, log2Ns);
+    }
+    if constexpr (LOG2L % 2 == 1) fft_pass<INVERSE, 1, LOG2L>(buf, tws, log2Ns);
+}
+
+// One axis of a 3-D FFT in place, `lines` lines of length L = 2^LOG2L at
+// element stride inner = 2^log2inner: element j of line (o, i) is
+// a[(o L + j) inner + i].
+template <bool INVERSE, int LOG2L>
+__global__ void __launch_bounds__(kFftThreads) fft_axis_kernel(float2* a, int log2inner,
+                                                               int64_t lines, const float2* tw)
+{
+    extern __shared__ float2 fft_sm[];
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int stride = (1 << LOG2L) + 1;
+    float2* const buf = fft_sm;
+    float2* const tws = fft_sm + (stride << log2W);
+    const int64_t group = int64_t(blockIdx.x) << log2W;
+    const bool contiguous = log2inner == 0;
+    const int64_t inner_mask = (int64_t(1) << log2inner) - 1;
+    auto gidx = [&](int w, int j) -> int64_t {
+        const int64_t line = group + w;
+        const int64_t o = line >> log2inner;
+        return (((o << LOG2L) + j) << log2inner) + (line & inner_mask);
+    };
+    fft_stage_twiddles<LOG2L>(tws, tw);
+    fft_load_tile<LOG2L>(buf, contiguous, [&](int w, int j) {
+        return group + w < lines ? a[gidx(w, j)] : make_float2(0.f, 0.f);
+    });
+    __syncthreads();
+    fft_tile_passes<INVERSE, LOG2L>(buf, tws);
+    fft_store_tile<LOG2L>(buf, contiguous, [&](int w, int j, float2 v) {
+        if (group + w < lines) a[gidx(w, j)] = v;
+    });
 }
 
 }  // namespace mri

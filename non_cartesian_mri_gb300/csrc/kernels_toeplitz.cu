@@ -6,8 +6,10 @@
 // The grid has n = (nx, ny, nz) voxels; the doubled grid 2n holds Q on the
 // circular grid of voxel differences and, zero-padded, the vector being
 // multiplied; (F^H F v)[x] = sum_x' Q(x - x') v[x'] is then the corner of
-// IFFT(FFT(Q) * FFT(pad v)) / |2n|.  All buffers are device memory; the
-// CG scalars stay on the device (no host round trip per iteration).
+// IFFT(FFT(Q) * FFT(pad v)) / |2n|, computed in five fused FFT stages that
+// skip the padding's zeros and the part of the result that is cut away.
+// All buffers are device memory; the CG scalars stay on the device (no host
+// round trip per iteration).
 #include <cstdint>
 #include <type_traits>
 
@@ -53,60 +55,135 @@ __global__ void __launch_bounds__(256) interleave_kernel(const float* r, const f
         out[k] = make_float2(r[k], i[k]);
 }
 
-// v (n grid, SoA) into the corner of the doubled grid, zeros elsewhere
-__global__ void __launch_bounds__(256) pad_kernel(const float* vr, const float* vi, int nx,
-                                                  int ny, int nz, float2* out)
-{
-    const int64_t Lx = 2 * nx, Ly = 2 * ny;
-    const int64_t total = Lx * Ly * 2 * nz;
-    for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < total;
-         k += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t ix = k % Lx;
-        const int64_t rest = k / Lx;
-        const int64_t iy = rest % Ly;
-        const int64_t iz = rest / Ly;
-        float2 v = make_float2(0.0f, 0.0f);
-        if (ix < nx && iy < ny && iz < nz) {
-            const int64_t n = (iz * ny + iy) * nx + ix;
-            v = make_float2(vr[n], vi[n]);
-        }
-        out[k] = v;
-    }
-}
+// ---- the Toeplitz product in five FFT stages over the doubled grid L = 2n.
+// The padded vector is zero outside the corner n and only the corner of the
+// result is kept, so no stage touches more than it must:
+//   x forward   lines (iy < ny, iz < nz): read v (SoA, zero for ix >= nx),
+//               write work[iz][iy][0 .. Lx)
+//   y forward   lines (ix, iz < nz): read iy < ny (zero above), write all Ly
+//   z           lines (ix, iy): read iz < nz (zero above), forward FFT, times
+//               K (the spectrum of Q), inverse FFT, write iz < nz
+//   y inverse   lines (ix, iz < nz): read all Ly, write iy < ny
+//   x inverse   lines (iy < ny, iz < nz): read all Lx, write
+//               out = scale * value + lambda * v (+ out) for ix < nx
+// work is [nz][Ly][Lx] complex (half the doubled grid); K is [Lz][Ly][Lx].
+enum ToeplitzStage : int { kXFwd = 0, kYFwd = 1, kZConv = 2, kYInv = 3, kXInv = 4 };
 
-// a *= K (complex), the spectrum of Q times the spectrum of the padded vector
-__global__ void __launch_bounds__(256) spectrum_mul_kernel(float2* a, const float2* K, int64_t n)
-{
-    for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
-         k += int64_t(gridDim.x) * blockDim.x) {
-        const float2 x = a[k];
-        const float2 y = K[k];
-        a[k] = make_float2(x.x * y.x - x.y * y.y, x.x * y.y + x.y * y.x);
-    }
-}
+struct ToeplitzArgs {
+    const float* ir;        // v, real and imaginary, [nz][ny][nx]
+    const float* ii;
+    float* outr;            // result, [nz][ny][nx] (may alias ir / ii)
+    float* outi;
+    float2* work;           // [nz][2 ny][2 nx]
+    const float2* K;        // [2 nz][2 ny][2 nx]
+    int log2nx, log2ny, log2nz;
+    float scale;            // 1 / |2n|, the inverse transform's normalisation
+    float lambda;
+    int accumulate;
+};
 
-// out = scale * corner(a) + lambda * in (+ out when accumulating)
-__global__ void __launch_bounds__(256) crop_kernel(const float2* a, int nx, int ny, int nz,
-                                                   float scale, float lambda, const float* ir,
-                                                   const float* ii, float* outr, float* outi,
-                                                   int accumulate)
+template <int STAGE, int LOG2L>
+__global__ void __launch_bounds__(kFftThreads) toeplitz_stage_kernel(ToeplitzArgs p,
+                                                                     int64_t lines,
+                                                                     const float2* tw)
 {
-    const int64_t N = int64_t(nx) * ny * nz;
-    for (int64_t n = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; n < N;
-         n += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t ix = n % nx;
-        const int64_t rest = n / nx;
-        const int64_t iy = rest % ny;
-        const int64_t iz = rest / ny;
-        const float2 v = a[(iz * 2 * ny + iy) * 2 * nx + ix];
-        float r = fmaf(lambda, ir[n], v.x * scale);
-        float i = fmaf(lambda, ii[n], v.y * scale);
-        if (accumulate) {
-            r += outr[n];
-            i += outi[n];
+    extern __shared__ float2 fft_sm[];
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int stride = (1 << LOG2L) + 1;
+    float2* const buf = fft_sm;
+    float2* const tws = fft_sm + (stride << log2W);
+    const int64_t group = int64_t(blockIdx.x) << log2W;
+    const int log2Lx = p.log2nx + 1, log2Ly = p.log2ny + 1;
+    const float2 zero = make_float2(0.f, 0.f);
+    fft_stage_twiddles<LOG2L>(tws, tw);
+    if constexpr (STAGE == kXFwd || STAGE == kXInv) {
+        const int nx = 1 << p.log2nx;
+        const int64_t ymask = (int64_t(1) << p.log2ny) - 1;
+        // line l = iz ny + iy: its row of work, and its row of v
+        auto widx = [&](int w, int j) -> int64_t {
+            const int64_t l = group + w;
+            return ((((l >> p.log2ny) << log2Ly) | (l & ymask)) << log2Lx) + j;
+        };
+        auto vidx = [&](int w, int j) -> int64_t { return ((group + w) << p.log2nx) + j; };
+        if constexpr (STAGE == kXFwd) {
+            fft_load_tile<LOG2L>(buf, true, [&](int w, int j) {
+                if (group + w >= lines || j >= nx) return zero;
+                const int64_t n = vidx(w, j);
+                return make_float2(p.ir[n], p.ii[n]);
+            });
+            __syncthreads();
+            fft_tile_passes<false, LOG2L>(buf, tws);
+            fft_store_tile<LOG2L>(buf, true, [&](int w, int j, float2 v) {
+                if (group + w < lines) p.work[widx(w, j)] = v;
+            });
+        } else {
+            fft_load_tile<LOG2L>(buf, true, [&](int w, int j) {
+                return group + w < lines ? p.work[widx(w, j)] : zero;
+            });
+            __syncthreads();
+            fft_tile_passes<true, LOG2L>(buf, tws);
+            fft_store_tile<LOG2L>(buf, true, [&](int w, int j, float2 v) {
+                if (group + w >= lines || j >= nx) return;
+                const int64_t n = vidx(w, j);
+                // v[n] is read before out[n] is written by the same thread
+                float r = fmaf(p.lambda, p.ir[n], v.x * p.scale);
+                float i = fmaf(p.lambda, p.ii[n], v.y * p.scale);
+                if (p.accumulate) {
+                    r += p.outr[n];
+                    i += p.outi[n];
+                }
+                p.outr[n] = r;
+                p.outi[n] = i;
+            });
         }
-        outr[n] = r;
-        outi[n] = i;
+    } else {
+        // y: line l = iz Lx + ix at stride Lx; z: line l = iy Lx + ix at
+        // stride Lx Ly.  Positions j < n_act are the ones held in work.
+        const int log2inner = STAGE == kZConv ? log2Lx + log2Ly : log2Lx;
+        const int n_act = 1 << (STAGE == kZConv ? p.log2nz : p.log2ny);
+        const int64_t imask = (int64_t(1) << log2inner) - 1;
+        auto gidx = [&](int w, int j) -> int64_t {
+            const int64_t l = group + w;
+            return ((((l >> log2inner) << LOG2L) + j) << log2inner) + (l & imask);
+        };
+        fft_load_tile<LOG2L>(buf, false, [&](int w, int j) {
+            return (group + w < lines && (STAGE == kYInv || j < n_act)) ? p.work[gidx(w, j)]
+                                                                         : zero;
+        });
+        __syncthreads();
+        if constexpr (STAGE == kZConv) {
+            fft_tile_passes<false, LOG2L>(buf, tws);
+            constexpr int total = (1 << log2W) << LOG2L;
+            constexpr int U = 8;
+            for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
+                float2 k[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int e = e0 + u * kFftThreads;
+                    int w, j;
+                    fft_tile_elem<LOG2L>(false, e, w, j);
+                    k[u] = (e < total && group + w < lines) ? p.K[gidx(w, j)] : zero;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int e = e0 + u * kFftThreads;
+                    int w, j;
+                    fft_tile_elem<LOG2L>(false, e, w, j);
+                    if (e < total) {
+                        const float2 x = buf[w * stride + j];
+                        buf[w * stride + j] = make_float2(x.x * k[u].x - x.y * k[u].y,
+                                                          x.x * k[u].y + x.y * k[u].x);
+                    }
+                }
+            }
+            __syncthreads();
+            fft_tile_passes<true, LOG2L>(buf, tws);
+        } else {
+            fft_tile_passes<STAGE == kYInv, LOG2L>(buf, tws);
+        }
+        fft_store_tile<LOG2L>(buf, false, [&](int w, int j, float2 v) {
+            if (group + w < lines && (STAGE == kYFwd || j < n_act)) p.work[gidx(w, j)] = v;
+        });
     }
 }
 
@@ -231,47 +308,73 @@ cudaError_t launch_fft_twiddles(float2* tw, cudaStream_t s)
     return cudaGetLastError();
 }
 
+namespace {
+
+// dynamic shared memory, then the launch, of one FFT kernel over `lines`
+// lines of length 2^log2L (the per-length kernels are picked by `pick`)
+template <class Pick>
+cudaError_t launch_by_length(int log2L, int64_t lines, cudaStream_t s, Pick pick)
+{
+    auto go = [&](auto kernel, auto... args) -> cudaError_t {
+        const size_t smem = fft_smem_total(log2L);
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        const int64_t W = int64_t(1) << fft_log2_lines(log2L);
+        kernel<<<unsigned((lines + W - 1) / W), kFftThreads, smem, s>>>(args...);
+        return cudaGetLastError();
+    };
+    switch (log2L) {
+        case 1: return pick(std::integral_constant<int, 1>{}, go);
+        case 2: return pick(std::integral_constant<int, 2>{}, go);
+        case 3: return pick(std::integral_constant<int, 3>{}, go);
+        case 4: return pick(std::integral_constant<int, 4>{}, go);
+        case 5: return pick(std::integral_constant<int, 5>{}, go);
+        case 6: return pick(std::integral_constant<int, 6>{}, go);
+        case 7: return pick(std::integral_constant<int, 7>{}, go);
+        case 8: return pick(std::integral_constant<int, 8>{}, go);
+        case 9: return pick(std::integral_constant<int, 9>{}, go);
+        case 10: return pick(std::integral_constant<int, 10>{}, go);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <bool INVERSE>
+cudaError_t fft_axis(float2* a, int log2L, int log2inner, int64_t lines, const float2* tw,
+                     cudaStream_t s)
+{
+    return launch_by_length(log2L, lines, s, [&](auto len, auto go) {
+        return go(fft_axis_kernel<INVERSE, decltype(len)::value>, a, log2inner, lines, tw);
+    });
+}
+
+template <int STAGE>
+cudaError_t toeplitz_stage(const ToeplitzArgs& p, int log2L, int64_t lines, const float2* tw,
+                           cudaStream_t s)
+{
+    return launch_by_length(log2L, lines, s, [&](auto len, auto go) {
+        return go(toeplitz_stage_kernel<STAGE, decltype(len)::value>, p, lines, tw);
+    });
+}
+
+}  // namespace
+
 cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const float2* tw,
                         cudaStream_t s)
 {
     if (!fft_len_ok(Lx) || !fft_len_ok(Ly) || !fft_len_ok(Lz)) return cudaErrorInvalidValue;
-    const int64_t L[3] = {Lx, Ly, Lz};
-    const int64_t inner[3] = {1, Lx, int64_t(Lx) * Ly};
-    const int64_t outer[3] = {int64_t(Ly) * Lz, Lz, 1};
+    const int64_t total = int64_t(Lx) * Ly * Lz;
+    const int len[3] = {Lx, Ly, Lz};
+    int log2inner = 0;
     for (int ax = 0; ax < 3; ++ax) {
-        if (L[ax] == 1) continue;
-        const int len = int(L[ax]);
-        const int log2L = log2i(len);
-        const size_t smem = fft_smem_total(log2L);
-        const int64_t lines = outer[ax] * inner[ax];
-        const int64_t W = int64_t(1) << fft_log2_lines(log2L);
-        const int64_t groups = (lines + W - 1) / W;
-        auto go = [&](auto kernel) -> cudaError_t {
-            const cudaError_t e = cudaFuncSetAttribute(
-                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        const int log2L = log2i(len[ax]);
+        if (log2L > 0) {
+            const int64_t lines = total >> log2L;
+            const cudaError_t e = inverse ? fft_axis<true>(a, log2L, log2inner, lines, tw, s)
+                                          : fft_axis<false>(a, log2L, log2inner, lines, tw, s);
             if (e != cudaSuccess) return e;
-            kernel<<<unsigned(groups), kFftThreads, smem, s>>>(a, log2i(int(inner[ax])), lines,
-                                                               tw);
-            return cudaGetLastError();
-        };
-        auto by_length = [&](auto inv) -> cudaError_t {
-            constexpr bool I = decltype(inv)::value;
-            switch (log2L) {
-                case 1: return go(fft_axis_kernel<I, 1>);
-                case 2: return go(fft_axis_kernel<I, 2>);
-                case 3: return go(fft_axis_kernel<I, 3>);
-                case 4: return go(fft_axis_kernel<I, 4>);
-                case 5: return go(fft_axis_kernel<I, 5>);
-                case 6: return go(fft_axis_kernel<I, 6>);
-                case 7: return go(fft_axis_kernel<I, 7>);
-                case 8: return go(fft_axis_kernel<I, 8>);
-                case 9: return go(fft_axis_kernel<I, 9>);
-                case 10: return go(fft_axis_kernel<I, 10>);
-            }
-            return cudaErrorInvalidValue;
-        };
-        const cudaError_t e = inverse ? by_length(std::true_type{}) : by_length(std::false_type{});
-        if (e != cudaSuccess) return e;
+        }
+        log2inner += log2L;
     }
     return cudaSuccess;
 }
@@ -293,23 +396,27 @@ cudaError_t launch_interleave(const float* r, const float* i, int64_t n, float2*
 
 cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float lambda,
                                   const float* ir, const float* ii, float* outr, float* outi,
-                                  int accumulate, float2* work, const float2* tw, int grid,
-                                  cudaStream_t s)
+                                  int accumulate, float2* work, const float2* tw, cudaStream_t s)
 {
-    const int64_t n8 = int64_t(8) * nx * ny * nz;
-    pad_kernel<<<grid, 256, 0, s>>>(ir, ii, nx, ny, nz, work);
-    cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) e = launch_fft3(work, 2 * nx, 2 * ny, 2 * nz, false, tw, s);
-    if (e == cudaSuccess) {
-        spectrum_mul_kernel<<<grid, 256, 0, s>>>(work, K, n8);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) e = launch_fft3(work, 2 * nx, 2 * ny, 2 * nz, true, tw, s);
-    if (e == cudaSuccess) {
-        crop_kernel<<<grid, 256, 0, s>>>(work, nx, ny, nz, float(1.0 / double(n8)), lambda, ir,
-                                         ii, outr, outi, accumulate);
-        e = cudaGetLastError();
-    }
+    ToeplitzArgs p;
+    p.ir = ir;
+    p.ii = ii;
+    p.outr = outr;
+    p.outi = outi;
+    p.work = work;
+    p.K = K;
+    p.log2nx = log2i(nx);
+    p.log2ny = log2i(ny);
+    p.log2nz = log2i(nz);
+    p.scale = float(1.0 / (8.0 * double(nx) * ny * nz));
+    p.lambda = lambda;
+    p.accumulate = accumulate;
+    const int64_t Lx = 2 * nx, Ly = 2 * ny;
+    cudaError_t e = toeplitz_stage<kXFwd>(p, p.log2nx + 1, int64_t(ny) * nz, tw, s);
+    if (e == cudaSuccess) e = toeplitz_stage<kYFwd>(p, p.log2ny + 1, Lx * nz, tw, s);
+    if (e == cudaSuccess) e = toeplitz_stage<kZConv>(p, p.log2nz + 1, Lx * Ly, tw, s);
+    if (e == cudaSuccess) e = toeplitz_stage<kYInv>(p, p.log2ny + 1, Lx * nz, tw, s);
+    if (e == cudaSuccess) e = toeplitz_stage<kXInv>(p, p.log2nx + 1, int64_t(ny) * nz, tw, s);
     return e;
 }
 
@@ -326,15 +433,14 @@ cudaError_t launch_cg(const float2* K, int nx, int ny, int nz, float lambda, con
     double* pap = scal + dot_blocks;
     // r = b - A x, p = r, rr[0] = r.r
     cudaError_t e = launch_toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, tw,
-                                          grid, s);
+                                          s);
     if (e != cudaSuccess) return e;
     cg_start_kernel<<<grid, 256, 0, s>>>(br, bi, r_r, r_i, p_r, p_i, N);
     dot_partial_kernel<<<dot_blocks, kDotThreads, 0, s>>>(r_r, r_i, r_r, r_i, N, partial);
     sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, rr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
-        e = launch_toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, tw, grid,
-                                  s);
+        e = launch_toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, tw, s);
         if (e != cudaSuccess) return e;
         dot_partial_kernel<<<dot_blocks, kDotThreads, 0, s>>>(p_r, p_i, a_r, a_i, N, partial);
         sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, pap);

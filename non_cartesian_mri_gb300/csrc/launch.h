@@ -78,7 +78,7 @@ cudaError_t launch_interleave(const float* r, const float* i, int64_t n, float2*
                               cudaStream_t s);
 cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float lambda,
                                   const float* ir, const float* ii, float* outr, float* outi,
-                                  int accumulate, float2* work, const float2* tw, int grid,
+                                  int accumulate, float2* work, const float2* tw,
                                   cudaStream_t s);
 cudaError_t launch_cg(const float2* K, int nx, int ny, int nz, float lambda, const float* br,
                       const float* bi, float* xr, float* xi, int iters, double* rr,

@@ -1038,13 +1038,13 @@ mri_status mri_toeplitz_apply(const float* K, int nx, int ny, int nz, float lamb
     DeviceState* d = nullptr;
     if ((st = prepare(0, accumulate, 1, 0, N, nullptr, 0, vp, 5, &d)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the FFT stages' work array: half the doubled grid, [nz][2 ny][2 nx]
     float2* work = nullptr;
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&work), size_t(8 * N) * sizeof(float2),
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&work), size_t(4 * N) * sizeof(float2),
                                 d->pool, s) != cudaSuccess)
         return cuda_fail();
     if (mri::launch_toeplitz_apply(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rIn,
-                                   iIn, rOut, iOut, accumulate, work, d->fft_tw,
-                                   grid_for(8 * N, d->sms), s) != cudaSuccess)
+                                   iIn, rOut, iOut, accumulate, work, d->fft_tw, s) != cudaSuccess)
         st = cuda_fail();
     if (cudaFreeAsync(work, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
     return st;
@@ -1064,10 +1064,11 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, co
     DeviceState* d = nullptr;
     if ((st = prepare(0, 0, 1, 0, N, nullptr, 0, vp, 6, &d)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // scratch: r, p, Ap (SoA), the doubled-grid work array, the dot partials
+    // scratch: r, p, Ap (SoA), the FFT stages' work array (half the doubled
+    // grid), the dot partials
     const int dot_blocks = int(std::min<int64_t>(ceil_div(N, 256), int64_t(d->sms) * 4));
     const int64_t vec_bytes = align256(6 * N * 4);
-    const int64_t work_bytes = align256(8 * N * int64_t(sizeof(float2)));
+    const int64_t work_bytes = align256(4 * N * int64_t(sizeof(float2)));
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
                                 size_t(vec_bytes + work_bytes + (dot_blocks + 1) * 8), d->pool,
@@ -1077,7 +1078,7 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, co
     float2* work = reinterpret_cast<float2*>(scratch + vec_bytes);
     double* scal = reinterpret_cast<double*>(scratch + vec_bytes + work_bytes);
     if (mri::launch_cg(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rB, iB, rX, iX,
-                       iters, rnorms, vec, work, scal, d->fft_tw, grid_for(8 * N, d->sms),
+                       iters, rnorms, vec, work, scal, d->fft_tw, grid_for(N, d->sms),
                        dot_blocks, s) != cudaSuccess)
         st = cuda_fail();
     if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();

@@ -107,6 +107,27 @@ def test_toeplitz_apply_matches_fhf(mri, shape, spacing, lam, trig):
     assert mri.device_errors(clear=True) == 0
 
 
+@pytest.mark.parametrize("shape,spacing", [((8, 4, 2), (1.0, 0.5, 1.0)),
+                                           ((4, 2, 1), (1.0, 1.0, 1.0)),
+                                           ((1, 1, 512), (1.0, 1.0, 1.0)),
+                                           ((2, 512, 1), (1.0, 0.25, 1.0)),
+                                           ((16, 32, 64), (1.0, 1.0, 1.0))])
+def test_toeplitz_apply_shapes(mri, shape, spacing):
+    """Narrow x (a CTA's 16 strided lines span several outer slabs), one-voxel
+    axes, the longest line (2 n = 1024), and a grid of 32768 voxels checked
+    through the oracle's FFT route (fhf_fft, pinned to the definition)."""
+    k, rPhi, iPhi = samples(600, 40 + shape[2])
+    K = mri.toeplitz_kernel(dev(k[0]), dev(k[1]), dev(k[2]), dev(rPhi), dev(iPhi), shape,
+                            spacing, trig="accurate")
+    rng = np.random.default_rng(41)
+    v = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    r, i = mri.toeplitz_apply(K, dev(v.real.reshape(-1)), dev(v.imag.reshape(-1)), lam=0.3)
+    Qc = T.q_difference_grid(k[0], k[1], k[2], rPhi, iPhi, shape, spacing, threads=0)
+    ref = (T.fhf_fft(Qc, v) + 0.3 * v).reshape(-1)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL["accurate"]
+    assert mri.device_errors(clear=True) == 0
+
+
 @pytest.mark.parametrize("lam", [0.05, 1.0])
 def test_cg_matches_the_oracle(mri, lam):
     shape, spacing = (4, 8, 8), (1.0, 1.0, 1.0)
