@@ -82,37 +82,40 @@ struct ToeplitzArgs {
     int accumulate;
 };
 
+// Every index below fits in 32 bits: the grid is at most 512 per axis, so
+// K has at most 2^30 values.
 template <int STAGE, int LOG2L>
-__global__ void __launch_bounds__(kFftThreads) toeplitz_stage_kernel(ToeplitzArgs p,
-                                                                     int64_t lines,
+__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_stage_kernel(ToeplitzArgs p,
+                                                                     int64_t lines64,
                                                                      const float2* tw)
 {
     extern __shared__ float2 fft_sm[];
     constexpr int log2W = fft_log2_lines(LOG2L);
-    constexpr int stride = (1 << LOG2L) + 1;
+    constexpr int S = fft_line_stride(LOG2L);
     float2* const buf = fft_sm;
-    float2* const tws = fft_sm + (stride << log2W);
-    const int64_t group = int64_t(blockIdx.x) << log2W;
+    float2* const tws = fft_sm + (S << log2W);
+    const uint32_t lines = uint32_t(lines64);
+    const uint32_t group = blockIdx.x << log2W;
     const int log2Lx = p.log2nx + 1, log2Ly = p.log2ny + 1;
     const float2 zero = make_float2(0.f, 0.f);
     fft_stage_twiddles<LOG2L>(tws, tw);
     if constexpr (STAGE == kXFwd || STAGE == kXInv) {
-        const int nx = 1 << p.log2nx;
-        const int64_t ymask = (int64_t(1) << p.log2ny) - 1;
+        const uint32_t ymask = (1u << p.log2ny) - 1;
         // line l = iz ny + iy: its row of work, and its row of v
-        auto widx = [&](int w, int j) -> int64_t {
-            const int64_t l = group + w;
+        auto widx = [&](int w, int j) -> uint32_t {
+            const uint32_t l = group + w;
             return ((((l >> p.log2ny) << log2Ly) | (l & ymask)) << log2Lx) + j;
         };
-        auto vidx = [&](int w, int j) -> int64_t { return ((group + w) << p.log2nx) + j; };
+        auto vidx = [&](int w, int j) -> uint32_t { return ((group + w) << p.log2nx) + j; };
         if constexpr (STAGE == kXFwd) {
-            fft_load_tile<LOG2L>(buf, true, [&](int w, int j) {
-                if (group + w >= lines || j >= nx) return zero;
-                const int64_t n = vidx(w, j);
+            // the positions ix >= nx of the padded line are zero: not loaded
+            fft_load_tile<LOG2L, true>(buf, true, [&](int w, int j) {
+                if (group + w >= lines) return zero;
+                const uint32_t n = vidx(w, j);
                 return make_float2(p.ir[n], p.ii[n]);
             });
             __syncthreads();
-            fft_tile_passes<false, LOG2L>(buf, tws);
+            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
             fft_store_tile<LOG2L>(buf, true, [&](int w, int j, float2 v) {
                 if (group + w < lines) p.work[widx(w, j)] = v;
             });
@@ -121,10 +124,11 @@ __global__ void __launch_bounds__(kFftThreads) toeplitz_stage_kernel(ToeplitzArg
                 return group + w < lines ? p.work[widx(w, j)] : zero;
             });
             __syncthreads();
-            fft_tile_passes<true, LOG2L>(buf, tws);
-            fft_store_tile<LOG2L>(buf, true, [&](int w, int j, float2 v) {
-                if (group + w >= lines || j >= nx) return;
-                const int64_t n = vidx(w, j);
+            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
+            // the corner ix < nx only
+            fft_store_tile<LOG2L, true>(buf, true, [&](int w, int j, float2 v) {
+                if (group + w >= lines) return;
+                const uint32_t n = vidx(w, j);
                 // v[n] is read before out[n] is written by the same thread
                 float r = fmaf(p.lambda, p.ir[n], v.x * p.scale);
                 float i = fmaf(p.lambda, p.ii[n], v.y * p.scale);
@@ -138,21 +142,22 @@ __global__ void __launch_bounds__(kFftThreads) toeplitz_stage_kernel(ToeplitzArg
         }
     } else {
         // y: line l = iz Lx + ix at stride Lx; z: line l = iy Lx + ix at
-        // stride Lx Ly.  Positions j < n_act are the ones held in work.
+        // stride Lx Ly.  work holds the positions j < L / 2 of a z line (and
+        // of a y line before the y forward stage).
         const int log2inner = STAGE == kZConv ? log2Lx + log2Ly : log2Lx;
-        const int n_act = 1 << (STAGE == kZConv ? p.log2nz : p.log2ny);
-        const int64_t imask = (int64_t(1) << log2inner) - 1;
-        auto gidx = [&](int w, int j) -> int64_t {
-            const int64_t l = group + w;
+        const uint32_t imask = (1u << log2inner) - 1;
+        auto gidx = [&](int w, int j) -> uint32_t {
+            const uint32_t l = group + w;
             return ((((l >> log2inner) << LOG2L) + j) << log2inner) + (l & imask);
         };
-        fft_load_tile<LOG2L>(buf, false, [&](int w, int j) {
-            return (group + w < lines && (STAGE == kYInv || j < n_act)) ? p.work[gidx(w, j)]
-                                                                         : zero;
+        constexpr bool half_in = STAGE != kYInv;
+        fft_load_tile<LOG2L, half_in>(buf, false, [&](int w, int j) {
+            return group + w < lines ? p.work[gidx(w, j)] : zero;
         });
         __syncthreads();
         if constexpr (STAGE == kZConv) {
-            fft_tile_passes<false, LOG2L>(buf, tws);
+            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
+            // times the spectrum of Q, eight loads in flight per thread
             constexpr int total = (1 << log2W) << LOG2L;
             constexpr int U = 8;
             for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
@@ -170,25 +175,43 @@ __global__ void __launch_bounds__(kFftThreads) toeplitz_stage_kernel(ToeplitzArg
                     int w, j;
                     fft_tile_elem<LOG2L>(false, e, w, j);
                     if (e < total) {
-                        const float2 x = buf[w * stride + j];
-                        buf[w * stride + j] = make_float2(x.x * k[u].x - x.y * k[u].y,
-                                                          x.x * k[u].y + x.y * k[u].x);
+                        float2& x = buf[fft_at(S, w, j)];
+                        x = make_float2(x.x * k[u].x - x.y * k[u].y, x.x * k[u].y + x.y * k[u].x);
                     }
                 }
             }
             __syncthreads();
-            fft_tile_passes<true, LOG2L>(buf, tws);
+            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
+        } else if constexpr (STAGE == kYFwd) {
+            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
         } else {
-            fft_tile_passes<STAGE == kYInv, LOG2L>(buf, tws);
+            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
         }
-        fft_store_tile<LOG2L>(buf, false, [&](int w, int j, float2 v) {
-            if (group + w < lines && (STAGE == kYFwd || j < n_act)) p.work[gidx(w, j)] = v;
+        constexpr bool half_out = STAGE != kYFwd;
+        fft_store_tile<LOG2L, half_out>(buf, false, [&](int w, int j, float2 v) {
+            if (group + w < lines) p.work[gidx(w, j)] = v;
         });
     }
 }
 
-// ---- conjugate gradients: Re <a, b> in double, per block, then one block sums
+// ---- conjugate gradients: Re <a, b> per thread in float with compensated
+// addition (the FP64 units are few: a conversion and a double FMA per
+// element would bound these kernels), per block and across blocks in double
 constexpr int kDotThreads = 256;
+
+// s + c += x exactly up to the final rounding (TwoSum, Knuth): c collects
+// the rounding error of every addition
+struct FloatSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x)
+    {
+        const float t = s + x;
+        const float z = t - s;
+        c += (s - (t - z)) + (x - z);
+        s = t;
+    }
+    __device__ __forceinline__ double value() const { return double(s) + double(c); }
+};
 
 __device__ __forceinline__ double block_sum(double v, double* sm)
 {
@@ -208,11 +231,13 @@ __global__ void __launch_bounds__(kDotThreads) dot_partial_kernel(const float* a
                                                                   int64_t n, double* partial)
 {
     __shared__ double sm[kDotThreads / 32];
-    double v = 0.0;
+    FloatSum v;
     for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
-         k += int64_t(gridDim.x) * blockDim.x)
-        v += double(ar[k]) * br[k] + double(ai[k]) * bi[k];
-    const double s = block_sum(v, sm);
+         k += int64_t(gridDim.x) * blockDim.x) {
+        v.add(ar[k] * br[k]);
+        v.add(ai[k] * bi[k]);
+    }
+    const double s = block_sum(v.value(), sm);
     if (threadIdx.x == 0) partial[blockIdx.x] = s;
 }
 
@@ -243,7 +268,7 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
 {
     __shared__ double sm[kDotThreads / 32];
     const float alpha = cg_ratio(rr, pap);
-    double v = 0.0;
+    FloatSum v;
     for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
          k += int64_t(gridDim.x) * blockDim.x) {
         xr[k] = fmaf(alpha, pr[k], xr[k]);
@@ -252,9 +277,10 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
         const float b = fmaf(-alpha, api[k], ri[k]);
         rr_[k] = a;
         ri[k] = b;
-        v += double(a) * a + double(b) * b;
+        v.add(a * a);
+        v.add(b * b);
     }
-    const double s = block_sum(v, sm);
+    const double s = block_sum(v.value(), sm);
     if (threadIdx.x == 0) partial[blockIdx.x] = s;
 }
 
@@ -317,8 +343,13 @@ cudaError_t launch_by_length(int log2L, int64_t lines, cudaStream_t s, Pick pick
 {
     auto go = [&](auto kernel, auto... args) -> cudaError_t {
         const size_t smem = fft_smem_total(log2L);
-        const cudaError_t e =
+        cudaError_t e =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        // all of the unified L1 / shared memory as shared memory, so that
+        // fft_min_ctas tiles fit on an SM
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     int(cudaSharedmemCarveoutMaxShared));
         if (e != cudaSuccess) return e;
         const int64_t W = int64_t(1) << fft_log2_lines(log2L);
         kernel<<<unsigned((lines + W - 1) / W), kFftThreads, smem, s>>>(args...);
