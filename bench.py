@@ -474,18 +474,18 @@ def e2e(torch, mri, dist, w, trig, steps, warmup, grid=False):
 # The find-rho step (CG on (F^H F + lambda I) x = F^H D with the Toeplitz
 # product): HBM-bound.  Bytes per product for N voxels, stage by stage (the
 # work array holds half the doubled grid, 4N complex values of 8 bytes; the
-# spectrum K the whole doubled grid, 8N):
+# real spectrum K the whole doubled grid, 8N floats):
 #   x forward   read v (8N), write 2N values (16N)
 #   y forward   read 2N values (16N), write 4N (32N)
-#   z           read 4N (32N) and K (64N), write 4N (32N)
+#   z           read 4N (32N) and K (32N), write 4N (32N)
 #   y inverse   read 4N (32N), write 2N (16N)
 #   x inverse   read 2N (16N) and v (8N), write the result (8N)
-# = 280 bytes per voxel.  The compulsory part (v, K and the result once) is
-# 80.  A CG iteration adds the dot product p.Ap (16N), the x / r update
-# (48N) and the p update (24N).
-TOEPLITZ_BYTES_PER_VOXEL = 8 + 16 + 16 + 32 + 32 + 64 + 32 + 32 + 16 + 16 + 8 + 8
-TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL = 8 + 64 + 8
-CG_EXTRA_BYTES_PER_VOXEL = 16 + 48 + 24
+# = 248 bytes per voxel.  The compulsory part (v, K and the result once) is
+# 48.  A CG iteration adds the x / r update (48N) and the p update (24N);
+# p.Ap is summed inside the last stage.
+TOEPLITZ_BYTES_PER_VOXEL = 8 + 16 + 16 + 32 + 32 + 32 + 32 + 32 + 16 + 16 + 8 + 8
+TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL = 8 + 32 + 8
+CG_EXTRA_BYTES_PER_VOXEL = 48 + 24
 
 
 def find_rho(torch, mri, dist, args, flush, peaks):

@@ -259,15 +259,22 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
  *
  * mri_toeplitz_kernel: Q on the circular grid of voxel differences of the
  * doubled grid (2nx x 2ny x 2nz: difference i h for i < n, (i - 2n) h for
- * i >= n per axis), computed by the grid Q path with trig mode `trig`, then
- * its 3-D FFT, written to K: a device array of 2 * 8 * nx*ny*nz floats, the
- * complex spectrum interleaved (re, im), 8-byte aligned, x fastest.  Samples
- * as mri_q (kx, ky, kz, rPhi, iPhi: M floats each; M = 0 gives K = 0).
+ * i >= n per axis), computed by the grid Q path with trig mode `trig`, with
+ * the planes at index n of every axis set to zero (the difference -n h
+ * occurs between no two voxels of the grid, so the product does not use
+ * them; without them the grid is Hermitian-symmetric because
+ * Q(-d) = conj Q(d)), then the real part of its 3-D FFT (the imaginary part
+ * is rounding), written to K: a device array of 8 * nx*ny*nz floats,
+ * 8-byte aligned, x fastest.  Samples as mri_q (kx, ky, kz, rPhi, iPhi: M
+ * floats each; M = 0 gives K = 0).  Scratch from the stream-ordered pool:
+ * 16 floats per point of the doubled grid.
  *
  * mri_toeplitz_apply: out = (F^H F + lambda I) in, from K, for SoA complex
  * vectors of nx*ny*nz floats (rIn, iIn; rOut, iOut, which may be the same
  * arrays as the inputs); accumulate = 1 adds into out.  Zero-padding to the
- * doubled grid, forward FFT, product with K, inverse FFT, crop.
+ * doubled grid, forward FFT, product with K, inverse FFT, crop -- in five
+ * kernels that never form the padding's zeros nor the part of the result
+ * the crop drops.  Scratch: 4 nx*ny*nz complex values.
  *
  * mri_cg_solve: `iters` conjugate-gradient iterations on
  * (F^H F + lambda I) x = b from K: rB, iB the right-hand side (typically
@@ -276,7 +283,7 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
  * receives ||r_0|| .. ||r_iters||, r = b - (F^H F + lambda I) x.  The
  * iteration's scalars stay on the device (no host synchronisation); once
  * r = 0 the iterate stops changing.  Scratch from the stream-ordered pool:
- * 8 nx*ny*nz complex values plus 6 nx*ny*nz floats.
+ * 4 nx*ny*nz complex values plus 6 nx*ny*nz floats.
  *
  * All three are asynchronous on `stream`.  MRI_ERR_SIZE for a grid edge that
  * is not a power of two in 1 .. 512, a non-finite spacing or lambda, iters

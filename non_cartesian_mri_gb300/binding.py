@@ -470,13 +470,13 @@ def fft3(data, inverse: bool = False, stream=None):
 def toeplitz_kernel(kx, ky, kz, rPhi, iPhi, shape, spacing=(1.0, 1.0, 1.0), *, trig="accurate",
                     stream=None):
     """Spectrum of F^H F on a grid of shape (nz, ny, nx) with voxel spacing
-    (hx, hy, hz) (see mri_toeplitz_kernel): a complex64 tensor of shape
+    (hx, hy, hz) (see mri_toeplitz_kernel): a real float32 tensor of shape
     (2nz, 2ny, 2nx)."""
     nz, ny, nx = (int(v) for v in shape)
     kx, ky, kz, rPhi, iPhi = (_as_tensor(t) for t in (kx, ky, kz, rPhi, iPhi))
     M = kx.numel()
     _same_len("samples", (kx, ky, kz, rPhi, iPhi), M)
-    K = torch.empty((2 * nz, 2 * ny, 2 * nx), dtype=torch.complex64, device=kx.device)
+    K = torch.empty((2 * nz, 2 * ny, 2 * nx), dtype=torch.float32, device=kx.device)
     hx, hy, hz = (float(v) for v in spacing)
     _check(load().mri_toeplitz_kernel(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(rPhi), _ptr(iPhi), M,
                                       nx, ny, nz, hx, hy, hz, _ptr(K), TRIG[trig],
@@ -485,6 +485,8 @@ def toeplitz_kernel(kx, ky, kz, rPhi, iPhi, shape, spacing=(1.0, 1.0, 1.0), *, t
 
 
 def _grid_shape(K):
+    if K.dtype != torch.float32 or K.dim() != 3 or not K.is_cuda or not K.is_contiguous():
+        raise ValueError("K must be the contiguous float32 CUDA tensor of toeplitz_kernel")
     return K.shape[0] // 2, K.shape[1] // 2, K.shape[2] // 2
 
 

@@ -10,6 +10,7 @@
 // skip the padding's zeros and the part of the result that is cut away.
 // All buffers are device memory; the CG scalars stay on the device (no host
 // round trip per iteration).
+#include <algorithm>
 #include <cstdint>
 #include <type_traits>
 
@@ -47,12 +48,67 @@ __global__ void __launch_bounds__(256) diff_axes_kernel(int nx, int ny, int nz, 
     axes[t] = float(i < n ? i : i - 2 * n) * h;
 }
 
-__global__ void __launch_bounds__(256) interleave_kernel(const float* r, const float* i,
-                                                         int64_t n, float2* out)
+// Q (SoA) on the doubled grid into the complex array the spectrum is taken
+// of, with the planes at index n of every axis zeroed: they hold Q at the
+// difference -n h, which no voxel pair of the n grid has, and without them
+// the grid is Hermitian-symmetric (Q(-d) = conj Q(d)), so its spectrum is
+// real.
+__global__ void __launch_bounds__(256) spectrum_input_kernel(const float* r, const float* i,
+                                                             int nx, int ny, int nz,
+                                                             float2* out)
+{
+    const int64_t Lx = 2 * nx, Ly = 2 * ny;
+    const int64_t n = Lx * Ly * 2 * nz;
+    for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
+         k += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t ix = k % Lx;
+        const int64_t iy = (k / Lx) % Ly;
+        const int64_t iz = k / (Lx * Ly);
+        const bool unused = ix == nx || iy == ny || iz == nz;
+        out[k] = unused ? make_float2(0.f, 0.f) : make_float2(r[k], i[k]);
+    }
+}
+
+// K = Re(spectrum); the imaginary part is rounding (Hermitian input)
+__global__ void __launch_bounds__(256) real_part_kernel(const float2* spec, int64_t n, float* K)
 {
     for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
          k += int64_t(gridDim.x) * blockDim.x)
-        out[k] = make_float2(r[k], i[k]);
+        K[k] = spec[k].x;
+}
+
+// ---- sums for the conjugate-gradient scalars: per thread in float with
+// compensated addition (the FP64 units are few: a conversion and a double
+// FMA per element would bound these kernels), per block and across blocks in
+// double
+constexpr int kDotThreads = 256;
+static_assert(kDotThreads == kFftThreads, "the stage kernels reduce with block_sum");
+
+// s + c += x exactly up to the final rounding (TwoSum, Knuth): c collects
+// the rounding error of every addition
+struct FloatSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x)
+    {
+        const float t = s + x;
+        const float z = t - s;
+        c += (s - (t - z)) + (x - z);
+        s = t;
+    }
+    __device__ __forceinline__ double value() const { return double(s) + double(c); }
+};
+
+__device__ __forceinline__ double block_sum(double v, double* sm)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) sm[warp] = v;
+    __syncthreads();
+    double s = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kDotThreads / 32; ++w) s += sm[w];
+    return s;   // thread 0
 }
 
 // ---- the Toeplitz product in five FFT stages over the doubled grid L = 2n.
@@ -66,7 +122,9 @@ __global__ void __launch_bounds__(256) interleave_kernel(const float* r, const f
 //   y inverse   lines (ix, iz < nz): read all Ly, write iy < ny
 //   x inverse   lines (iy < ny, iz < nz): read all Lx, write
 //               out = scale * value + lambda * v (+ out) for ix < nx
-// work is [nz][Ly][Lx] complex (half the doubled grid); K is [Lz][Ly][Lx].
+// work is [nz][Ly][Lx] complex (half the doubled grid); K is [Lz][Ly][Lx]
+// real.  The x inverse stage can also sum Re <v, result> per CTA (the p.Ap
+// of conjugate gradients).
 enum ToeplitzStage : int { kXFwd = 0, kYFwd = 1, kZConv = 2, kYInv = 3, kXInv = 4 };
 
 struct ToeplitzArgs {
@@ -75,7 +133,8 @@ struct ToeplitzArgs {
     float* outr;            // result, [nz][ny][nx] (may alias ir / ii)
     float* outi;
     float2* work;           // [nz][2 ny][2 nx]
-    const float2* K;        // [2 nz][2 ny][2 nx]
+    const float* K;         // [2 nz][2 ny][2 nx], real
+    double* dot;            // x inverse: per CTA Re <v, result> (nullptr: none)
     int log2nx, log2ny, log2nz;
     float scale;            // 1 / |2n|, the inverse transform's normalisation
     float lambda;
@@ -126,19 +185,28 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
             __syncthreads();
             fft_tile_passes<true, LOG2L, false, true>(buf, tws);
             // the corner ix < nx only
+            FloatSum dot;
             fft_store_tile<LOG2L, true>(buf, true, [&](int w, int j, float2 v) {
                 if (group + w >= lines) return;
                 const uint32_t n = vidx(w, j);
                 // v[n] is read before out[n] is written by the same thread
-                float r = fmaf(p.lambda, p.ir[n], v.x * p.scale);
-                float i = fmaf(p.lambda, p.ii[n], v.y * p.scale);
+                const float vr = p.ir[n], vi = p.ii[n];
+                float r = fmaf(p.lambda, vr, v.x * p.scale);
+                float i = fmaf(p.lambda, vi, v.y * p.scale);
                 if (p.accumulate) {
                     r += p.outr[n];
                     i += p.outi[n];
                 }
                 p.outr[n] = r;
                 p.outi[n] = i;
+                dot.add(vr * r);
+                dot.add(vi * i);
             });
+            if (p.dot != nullptr) {
+                __shared__ double sm[kDotThreads / 32];
+                const double total = block_sum(dot.value(), sm);
+                if (threadIdx.x == 0) p.dot[blockIdx.x] = total;
+            }
         }
     } else {
         // y: line l = iz Lx + ix at stride Lx; z: line l = iy Lx + ix at
@@ -157,17 +225,17 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
         __syncthreads();
         if constexpr (STAGE == kZConv) {
             fft_tile_passes<false, LOG2L, true, false>(buf, tws);
-            // times the spectrum of Q, eight loads in flight per thread
+            // times the (real) spectrum of Q, eight loads in flight per thread
             constexpr int total = (1 << log2W) << LOG2L;
             constexpr int U = 8;
             for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
-                float2 k[U];
+                float k[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int e = e0 + u * kFftThreads;
                     int w, j;
                     fft_tile_elem<LOG2L>(false, e, w, j);
-                    k[u] = (e < total && group + w < lines) ? p.K[gidx(w, j)] : zero;
+                    k[u] = (e < total && group + w < lines) ? p.K[gidx(w, j)] : 0.f;
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -176,7 +244,7 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
                     fft_tile_elem<LOG2L>(false, e, w, j);
                     if (e < total) {
                         float2& x = buf[fft_at(S, w, j)];
-                        x = make_float2(x.x * k[u].x - x.y * k[u].y, x.x * k[u].y + x.y * k[u].x);
+                        x = make_float2(x.x * k[u], x.y * k[u]);
                     }
                 }
             }
@@ -194,38 +262,7 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
     }
 }
 
-// ---- conjugate gradients: Re <a, b> per thread in float with compensated
-// addition (the FP64 units are few: a conversion and a double FMA per
-// element would bound these kernels), per block and across blocks in double
-constexpr int kDotThreads = 256;
-
-// s + c += x exactly up to the final rounding (TwoSum, Knuth): c collects
-// the rounding error of every addition
-struct FloatSum {
-    float s = 0.f, c = 0.f;
-    __device__ __forceinline__ void add(float x)
-    {
-        const float t = s + x;
-        const float z = t - s;
-        c += (s - (t - z)) + (x - z);
-        s = t;
-    }
-    __device__ __forceinline__ double value() const { return double(s) + double(c); }
-};
-
-__device__ __forceinline__ double block_sum(double v, double* sm)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) sm[warp] = v;
-    __syncthreads();
-    double s = 0.0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < kDotThreads / 32; ++w) s += sm[w];
-    return s;   // thread 0
-}
-
+// ---- conjugate gradients
 __global__ void __launch_bounds__(kDotThreads) dot_partial_kernel(const float* ar, const float* ai,
                                                                   const float* br, const float* bi,
                                                                   int64_t n, double* partial)
@@ -258,7 +295,14 @@ __device__ __forceinline__ float cg_ratio(const double* num, const double* den)
     return (a > 0.0 && b != 0.0) ? float(a / b) : 0.0f;
 }
 
-// x += alpha p, r -= alpha Ap, partial sums of |r|^2
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 y)
+{
+    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
+// x += alpha p, r -= alpha Ap, partial sums of |r|^2; VEC: four values per
+// access (n a multiple of 4, every array 16-byte aligned)
+template <bool VEC>
 __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi, float* rr_,
                                                             float* ri, const float* pr,
                                                             const float* pi, const float* apr,
@@ -269,31 +313,70 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
     __shared__ double sm[kDotThreads / 32];
     const float alpha = cg_ratio(rr, pap);
     FloatSum v;
-    for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
-         k += int64_t(gridDim.x) * blockDim.x) {
-        xr[k] = fmaf(alpha, pr[k], xr[k]);
-        xi[k] = fmaf(alpha, pi[k], xi[k]);
-        const float a = fmaf(-alpha, apr[k], rr_[k]);
-        const float b = fmaf(-alpha, api[k], ri[k]);
-        rr_[k] = a;
-        ri[k] = b;
-        v.add(a * a);
-        v.add(b * b);
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    if constexpr (VEC) {
+        float4* const x4r = reinterpret_cast<float4*>(xr);
+        float4* const x4i = reinterpret_cast<float4*>(xi);
+        float4* const r4r = reinterpret_cast<float4*>(rr_);
+        float4* const r4i = reinterpret_cast<float4*>(ri);
+        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < (n >> 2);
+             k += stride) {
+            const float4 p_r = reinterpret_cast<const float4*>(pr)[k];
+            const float4 p_i = reinterpret_cast<const float4*>(pi)[k];
+            const float4 a_r = reinterpret_cast<const float4*>(apr)[k];
+            const float4 a_i = reinterpret_cast<const float4*>(api)[k];
+            x4r[k] = fma4(alpha, p_r, x4r[k]);
+            x4i[k] = fma4(alpha, p_i, x4i[k]);
+            const float4 a = fma4(-alpha, a_r, r4r[k]);
+            const float4 b = fma4(-alpha, a_i, r4i[k]);
+            r4r[k] = a;
+            r4i[k] = b;
+            v.add(a.x * a.x);
+            v.add(a.y * a.y);
+            v.add(a.z * a.z);
+            v.add(a.w * a.w);
+            v.add(b.x * b.x);
+            v.add(b.y * b.y);
+            v.add(b.z * b.z);
+            v.add(b.w * b.w);
+        }
+    } else {
+        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n; k += stride) {
+            xr[k] = fmaf(alpha, pr[k], xr[k]);
+            xi[k] = fmaf(alpha, pi[k], xi[k]);
+            const float a = fmaf(-alpha, apr[k], rr_[k]);
+            const float b = fmaf(-alpha, api[k], ri[k]);
+            rr_[k] = a;
+            ri[k] = b;
+            v.add(a * a);
+            v.add(b * b);
+        }
     }
     const double s = block_sum(v.value(), sm);
     if (threadIdx.x == 0) partial[blockIdx.x] = s;
 }
 
-// p = r + beta p, beta = new r.r / old r.r
+// p = r + beta p, beta = new r.r / old r.r (VEC as cg_xr_kernel)
+template <bool VEC>
 __global__ void __launch_bounds__(256) cg_p_kernel(float* pr, float* pi, const float* rr_,
                                                    const float* ri, int64_t n,
                                                    const double* rr_new, const double* rr_old)
 {
     const float beta = cg_ratio(rr_new, rr_old);
-    for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
-         k += int64_t(gridDim.x) * blockDim.x) {
-        pr[k] = fmaf(beta, pr[k], rr_[k]);
-        pi[k] = fmaf(beta, pi[k], ri[k]);
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    if constexpr (VEC) {
+        float4* const p4r = reinterpret_cast<float4*>(pr);
+        float4* const p4i = reinterpret_cast<float4*>(pi);
+        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < (n >> 2);
+             k += stride) {
+            p4r[k] = fma4(beta, p4r[k], reinterpret_cast<const float4*>(rr_)[k]);
+            p4i[k] = fma4(beta, p4i[k], reinterpret_cast<const float4*>(ri)[k]);
+        }
+    } else {
+        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n; k += stride) {
+            pr[k] = fmaf(beta, pr[k], rr_[k]);
+            pi[k] = fmaf(beta, pi[k], ri[k]);
+        }
     }
 }
 
@@ -418,16 +501,30 @@ cudaError_t launch_diff_axes(int nx, int ny, int nz, float hx, float hy, float h
     return cudaGetLastError();
 }
 
-cudaError_t launch_interleave(const float* r, const float* i, int64_t n, float2* out, int grid,
-                              cudaStream_t s)
+cudaError_t launch_spectrum_input(const float* r, const float* i, int nx, int ny, int nz,
+                                  float2* out, int grid, cudaStream_t s)
 {
-    interleave_kernel<<<grid, 256, 0, s>>>(r, i, n, out);
+    spectrum_input_kernel<<<grid, 256, 0, s>>>(r, i, nx, ny, nz, out);
     return cudaGetLastError();
 }
 
-cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float lambda,
-                                  const float* ir, const float* ii, float* outr, float* outi,
-                                  int accumulate, float2* work, const float2* tw, cudaStream_t s)
+cudaError_t launch_real_part(const float2* spec, int64_t n, float* K, int grid, cudaStream_t s)
+{
+    real_part_kernel<<<grid, 256, 0, s>>>(spec, n, K);
+    return cudaGetLastError();
+}
+
+int64_t toeplitz_dot_blocks(int nx, int ny, int nz)
+{
+    const int64_t W = int64_t(1) << fft_log2_lines(log2i(2 * nx));
+    return (int64_t(ny) * nz + W - 1) / W;
+}
+
+namespace {
+
+cudaError_t toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda, const float* ir,
+                           const float* ii, float* outr, float* outi, int accumulate,
+                           float2* work, double* dot, const float2* tw, cudaStream_t s)
 {
     ToeplitzArgs p;
     p.ir = ir;
@@ -436,6 +533,7 @@ cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float
     p.outi = outi;
     p.work = work;
     p.K = K;
+    p.dot = dot;
     p.log2nx = log2i(nx);
     p.log2ny = log2i(ny);
     p.log2nz = log2i(nz);
@@ -451,34 +549,56 @@ cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float
     return e;
 }
 
-cudaError_t launch_cg(const float2* K, int nx, int ny, int nz, float lambda, const float* br,
+}  // namespace
+
+cudaError_t launch_toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda,
+                                  const float* ir, const float* ii, float* outr, float* outi,
+                                  int accumulate, float2* work, const float2* tw, cudaStream_t s)
+{
+    return toeplitz_apply(K, nx, ny, nz, lambda, ir, ii, outr, outi, accumulate, work, nullptr,
+                          tw, s);
+}
+
+cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, const float* br,
                       const float* bi, float* xr, float* xi, int iters, double* rr,
                       float* vec, float2* work, double* scal, const float2* tw, int grid,
                       int dot_blocks, cudaStream_t s)
 {
-    // vec: r (2 N), p (2 N), Ap (2 N); scal: dot partials (dot_blocks), p.Ap
+    // vec: r (2 N), p (2 N), Ap (2 N); scal: dot partials (max(dot_blocks,
+    // toeplitz_dot_blocks)), p.Ap
     const int64_t N = int64_t(nx) * ny * nz;
     float *r_r = vec, *r_i = vec + N, *p_r = vec + 2 * N, *p_i = vec + 3 * N;
     float *a_r = vec + 4 * N, *a_i = vec + 5 * N;
+    const int64_t apply_blocks = toeplitz_dot_blocks(nx, ny, nz);
     double* partial = scal;
-    double* pap = scal + dot_blocks;
+    double* pap = scal + std::max<int64_t>(dot_blocks, apply_blocks);
+    const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(xi) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(vec) & 15u) == 0;
     // r = b - A x, p = r, rr[0] = r.r
-    cudaError_t e = launch_toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, tw,
-                                          s);
+    cudaError_t e = toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, nullptr, tw,
+                                   s);
     if (e != cudaSuccess) return e;
     cg_start_kernel<<<grid, 256, 0, s>>>(br, bi, r_r, r_i, p_r, p_i, N);
     dot_partial_kernel<<<dot_blocks, kDotThreads, 0, s>>>(r_r, r_i, r_r, r_i, N, partial);
     sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, rr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
-        e = launch_toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, tw, s);
+        // Ap, with the per-CTA sums of p.Ap from its last stage
+        e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s);
         if (e != cudaSuccess) return e;
-        dot_partial_kernel<<<dot_blocks, kDotThreads, 0, s>>>(p_r, p_i, a_r, a_i, N, partial);
-        sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, pap);
-        cg_xr_kernel<<<dot_blocks, kDotThreads, 0, s>>>(xr, xi, r_r, r_i, p_r, p_i, a_r, a_i,
-                                                        N, rr + it, pap, partial);
+        sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, int(apply_blocks), pap);
+        if (vec4)
+            cg_xr_kernel<true><<<dot_blocks, kDotThreads, 0, s>>>(
+                xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it, pap, partial);
+        else
+            cg_xr_kernel<false><<<dot_blocks, kDotThreads, 0, s>>>(
+                xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it, pap, partial);
         sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, rr + it + 1);
-        cg_p_kernel<<<grid, 256, 0, s>>>(p_r, p_i, r_r, r_i, N, rr + it + 1, rr + it);
+        if (vec4)
+            cg_p_kernel<true><<<grid, 256, 0, s>>>(p_r, p_i, r_r, r_i, N, rr + it + 1, rr + it);
+        else
+            cg_p_kernel<false><<<grid, 256, 0, s>>>(p_r, p_i, r_r, r_i, N, rr + it + 1, rr + it);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     sqrt_kernel<<<(iters + 1 + 255) / 256, 256, 0, s>>>(rr, iters + 1);

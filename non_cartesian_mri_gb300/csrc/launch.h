@@ -74,13 +74,18 @@ cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const f
                         cudaStream_t s);
 cudaError_t launch_diff_axes(int nx, int ny, int nz, float hx, float hy, float hz, float* axes,
                              cudaStream_t s);
-cudaError_t launch_interleave(const float* r, const float* i, int64_t n, float2* out, int grid,
-                              cudaStream_t s);
-cudaError_t launch_toeplitz_apply(const float2* K, int nx, int ny, int nz, float lambda,
+// Q (SoA, doubled grid) into the complex array whose spectrum is K, the
+// planes at index n of every axis zeroed; K = the real part of a spectrum
+cudaError_t launch_spectrum_input(const float* r, const float* i, int nx, int ny, int nz,
+                                  float2* out, int grid, cudaStream_t s);
+cudaError_t launch_real_part(const float2* spec, int64_t n, float* K, int grid, cudaStream_t s);
+// CTAs of the last Toeplitz stage: the p.Ap partial sums launch_cg keeps
+int64_t toeplitz_dot_blocks(int nx, int ny, int nz);
+cudaError_t launch_toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda,
                                   const float* ir, const float* ii, float* outr, float* outi,
                                   int accumulate, float2* work, const float2* tw,
                                   cudaStream_t s);
-cudaError_t launch_cg(const float2* K, int nx, int ny, int nz, float lambda, const float* br,
+cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, const float* br,
                       const float* bi, float* xr, float* xi, int iters, double* rr,
                       float* vec, float2* work, double* scal, const float2* tw, int grid,
                       int dot_blocks, cudaStream_t s);

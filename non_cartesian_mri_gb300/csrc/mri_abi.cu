@@ -998,16 +998,19 @@ mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz
     DeviceState* d = nullptr;
     if ((st = prepare(int(trig), 0, 1, M, N2, sp, 5, vp, 1, &d)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // scratch: the difference axes, Q (real and imaginary parts)
+    // scratch: the difference axes, Q (real and imaginary parts), the
+    // complex spectrum
     const int64_t axes_n = 2 * (int64_t(nx) + ny + nz);
+    const int64_t q_bytes = align256(2 * N2 * 4);
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(align256(axes_n * 4) + 2 * N2 * 4), d->pool,
+                                size_t(align256(axes_n * 4) + q_bytes + N2 * 8), d->pool,
                                 s) != cudaSuccess)
         return cuda_fail();
     float* axes = reinterpret_cast<float*>(scratch);
     float* q_r = reinterpret_cast<float*>(scratch + align256(axes_n * 4));
     float* q_i = q_r + N2;
+    float2* spec = reinterpret_cast<float2*>(scratch + align256(axes_n * 4) + q_bytes);
     if (mri::launch_diff_axes(nx, ny, nz, hx, hy, hz, axes, s) != cudaSuccess) st = cuda_fail();
     // Q(d) = sum_m |Phi_m|^2 e^{+i 2 pi k_m . d} on the difference grid: the
     // grid Q path (tensor cores for 2 nx >= 8)
@@ -1015,10 +1018,13 @@ mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz
         st = run_grid_call(true, 1, kx, ky, kz, axes, 2 * nx, axes + 2 * nx, 2 * ny,
                            axes + 2 * nx + 2 * ny, 2 * nz, rPhi, iPhi, nullptr, nullptr, M, q_r,
                            q_i, int(trig), 0, d, s);
-    float2* spec = reinterpret_cast<float2*>(K);
+    // the index-n planes zeroed (unused by the product; without them the
+    // spectrum is real), FFT, real part
     if (st == MRI_OK &&
-        (mri::launch_interleave(q_r, q_i, N2, spec, grid_for(N2, d->sms), s) != cudaSuccess ||
-         mri::launch_fft3(spec, 2 * nx, 2 * ny, 2 * nz, false, d->fft_tw, s) != cudaSuccess))
+        (mri::launch_spectrum_input(q_r, q_i, nx, ny, nz, spec, grid_for(N2, d->sms), s) !=
+             cudaSuccess ||
+         mri::launch_fft3(spec, 2 * nx, 2 * ny, 2 * nz, false, d->fft_tw, s) != cudaSuccess ||
+         mri::launch_real_part(spec, N2, K, grid_for(N2, d->sms), s) != cudaSuccess))
         st = cuda_fail();
     if (cudaFreeAsync(scratch, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
     return st;
@@ -1043,7 +1049,7 @@ mri_status mri_toeplitz_apply(const float* K, int nx, int ny, int nz, float lamb
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&work), size_t(4 * N) * sizeof(float2),
                                 d->pool, s) != cudaSuccess)
         return cuda_fail();
-    if (mri::launch_toeplitz_apply(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rIn,
+    if (mri::launch_toeplitz_apply(K, nx, ny, nz, lambda, rIn,
                                    iIn, rOut, iOut, accumulate, work, d->fft_tw, s) != cudaSuccess)
         st = cuda_fail();
     if (cudaFreeAsync(work, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
@@ -1069,15 +1075,16 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, co
     const int dot_blocks = int(std::min<int64_t>(ceil_div(N, 256), int64_t(d->sms) * 4));
     const int64_t vec_bytes = align256(6 * N * 4);
     const int64_t work_bytes = align256(4 * N * int64_t(sizeof(float2)));
+    const int64_t partials = std::max<int64_t>(dot_blocks, mri::toeplitz_dot_blocks(nx, ny, nz));
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(vec_bytes + work_bytes + (dot_blocks + 1) * 8), d->pool,
+                                size_t(vec_bytes + work_bytes + (partials + 1) * 8), d->pool,
                                 s) != cudaSuccess)
         return cuda_fail();
     float* vec = reinterpret_cast<float*>(scratch);
     float2* work = reinterpret_cast<float2*>(scratch + vec_bytes);
     double* scal = reinterpret_cast<double*>(scratch + vec_bytes + work_bytes);
-    if (mri::launch_cg(reinterpret_cast<const float2*>(K), nx, ny, nz, lambda, rB, iB, rX, iX,
+    if (mri::launch_cg(K, nx, ny, nz, lambda, rB, iB, rX, iX,
                        iters, rnorms, vec, work, scal, d->fft_tw, grid_for(N, d->sms),
                        dot_blocks, s) != cudaSuccess)
         st = cuda_fail();

@@ -22,10 +22,14 @@ lets it be formed without F^H F itself.  Readings taken here:
 Functions: q_difference_grid (Q on the circular grid of differences, from
 the oracle's own Q), fhf_direct (the definition: a sum over every voxel
 pair), fhf_fft (the same product through numpy's FFT, the library
-primitive the pages name), cg (the conjugate-gradient iteration).  Pinned in
+primitive the pages name), zero_unused_planes / toeplitz_spectrum /
+fhf_spectrum (the real spectrum the product multiplies by, and the product
+through it), cg (the conjugate-gradient iteration).  Pinned in
 tests/test_oracle_toeplitz.py: fhf_direct against F^H (F rho) formed from
-the oracle's forward model and F^H D, fhf_fft against fhf_direct, cg against
-a dense solve and its own residuals.
+the oracle's forward model and F^H D, fhf_fft and fhf_spectrum against
+fhf_direct, the spectrum's imaginary part against rounding (and the grid
+without the zeroed planes against a large one), cg against a dense solve and
+its own residuals.
 """
 
 from __future__ import annotations
@@ -51,6 +55,38 @@ def q_difference_grid(kx, ky, kz, rPhi, iPhi, shape, spacing=(1.0, 1.0, 1.0), th
     z, y, x = np.meshgrid(dz, dy, dx, indexing="ij")
     Q = q(kx, ky, kz, x.reshape(-1), y.reshape(-1), z.reshape(-1), rPhi, iPhi, threads=threads)
     return Q.reshape(2 * nz, 2 * ny, 2 * nx)
+
+
+def zero_unused_planes(Qc):
+    """Qc with the planes at index n of every axis set to zero.  Those hold
+    Q at the difference -n h, which no pair of voxels of an n grid has
+    (differences stay within -(n-1) .. n-1), so the product is unchanged; with
+    them gone the grid is Hermitian-symmetric, Qc[-j mod 2n] = conj(Qc[j])
+    (Q(-d) is the conjugate of Q(d)), and its spectrum is real."""
+    Z = np.array(Qc, dtype=np.complex128)
+    nz, ny, nx = (s // 2 for s in Z.shape)
+    Z[nz, :, :] = 0
+    Z[:, ny, :] = 0
+    Z[:, :, nx] = 0
+    return Z
+
+
+def toeplitz_spectrum(Qc):
+    """The spectrum the product multiplies by: the real part of the FFT of
+    zero_unused_planes(Qc), and the largest imaginary part dropped relative
+    to the largest real one (rounding only: the pins check it)."""
+    S = np.fft.fftn(zero_unused_planes(Qc))
+    return S.real.copy(), float(np.abs(S.imag).max() / max(np.abs(S.real).max(), 1e-300))
+
+
+def fhf_spectrum(Kr, rho):
+    """F^H F rho through a real spectrum Kr of the doubled grid:
+    crop(IFFT(Kr * FFT(zero-padded rho)))."""
+    rho = np.asarray(rho, dtype=np.complex128)
+    nz, ny, nx = rho.shape
+    pad = np.zeros(Kr.shape, np.complex128)
+    pad[:nz, :ny, :nx] = rho
+    return np.fft.ifftn(Kr * np.fft.fftn(pad))[:nz, :ny, :nx]
 
 
 def fhf_direct(Qc, rho):

@@ -5,6 +5,9 @@
   route through the definition of F -- on non-cubic grids with unequal
   spacings per axis (an axis or sign mix-up in Q's difference grid fails);
 - fhf_fft equals fhf_direct (the circular embedding does not wrap);
+- zeroing the index-n planes of the difference grid leaves the product
+  unchanged and makes the spectrum real (imaginary part at rounding level,
+  while the unzeroed grid's is not);
 - the operator is Hermitian and positive semi-definite;
 - cg after N steps on an N-voxel problem equals the dense solve of
   (A + lambda I) x = b, and its reported residual norms are those of its
@@ -68,6 +71,24 @@ def test_fhf_fft_equals_direct_and_is_hermitian():
     rhs = np.vdot(T.fhf_direct(Qc, u), rho)
     assert abs(lhs - rhs) < 1e-10 * abs(lhs)
     assert np.vdot(rho, a).real > 0 and abs(np.vdot(rho, a).imag) < 1e-9 * abs(np.vdot(rho, a))
+
+
+@pytest.mark.parametrize("shape,spacing", [((3, 4, 5), (1.0, 1.0, 0.5)),
+                                           ((2, 1, 4), (0.5, 1.0, 2.0))])
+def test_real_spectrum_gives_the_same_product(shape, spacing):
+    """Zeroing the index-n planes leaves F^H F unchanged and makes the
+    spectrum real: a wrong difference axis (a sign, an off-by-one in the
+    wrap) or a zeroed plane that is used fails one of the three checks."""
+    k, rPhi, iPhi, xyz, rho = problem(shape, spacing, 300, 7 + shape[2])
+    Qc = T.q_difference_grid(k[0], k[1], k[2], rPhi, iPhi, shape, spacing)
+    Kr, imag = T.toeplitz_spectrum(Qc)
+    assert imag < 1e-12
+    ref = T.fhf_direct(Qc, rho)
+    assert oracle.rel_l2(T.fhf_spectrum(Kr, rho), ref) < 1e-12
+    # the planes are needed for the symmetry: without the zeroing the
+    # spectrum is complex
+    full = np.fft.fftn(Qc)
+    assert np.abs(full.imag).max() > 1e-3 * np.abs(full.real).max()
 
 
 def test_cg_reaches_the_dense_solution():
