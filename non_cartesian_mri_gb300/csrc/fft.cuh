@@ -6,22 +6,22 @@
 // power of two, 2 .. kFftMaxLen) sits between `outer` slabs and `inner`
 // consecutive elements: element j of line (o, i) is a[(o L + j) inner + i].
 // A CTA transforms W lines (16, or 8 for L = 1024): W consecutive i when
-// inner > 1 (so that a warp's loads cover consecutive addresses), W
-// consecutive o when inner == 1 (each line contiguous).  The lines go to
-// shared memory in natural order and the transform is a Stockham
-// auto-sorting FFT: one pass of radix 2^(log2 L mod 4) when that is not 0,
-// then radix-16 passes, each thread reading R values of a line at stride
-// L / R, multiplying by the twiddles of the pass and doing the R-point DFT
-// in registers, then, after a barrier, writing them back in place where the
-// final output ends up in natural order -- no bit reversal, one buffer, two
-// passes at L = 256 (four CTAs per SM at that length).
-// Twiddles e^{-2 pi i k / kFftMaxLen} come from a per-device table
-// evaluated in double precision (the twiddle kernel of kernels_toeplitz.cu)
-// and are staged for the line length in shared memory; the inverse
-// transform conjugates them where it uses them and does not scale (the
-// caller divides by the size).  The pieces (stage the twiddles, load a tile,
-// run the passes, store a tile) are separate so that a kernel can do more
-// than one transform on a tile, or fuse the work on either side of one.
+// inner > 1 (so that a warp's accesses at one position of its lines are
+// contiguous), W consecutive o when inner == 1 (each line contiguous).  The
+// transform is a Stockham auto-sorting FFT (natural order in and out, no bit
+// reversal): one pass of radix 2^(log2 L mod 4) when that is not 0 and
+// radix-16 passes, each thread doing the R-point DFTs of its butterflies in
+// registers.  The first pass reads its inputs straight from global memory
+// into registers and the last pass hands its outputs over in registers;
+// shared memory only carries the values from one pass to the next (one
+// exchange at L = 256), so a kernel can fuse the work on either side of a
+// transform, or keep the result of one transform in registers as the input
+// of the next (the z stage of the Toeplitz product: forward transform,
+// product with the spectrum, inverse transform).  Twiddles
+// e^{-2 pi i k / kFftMaxLen} come from a per-device table evaluated in double
+// precision (the twiddle kernel of kernels_toeplitz.cu) and are staged for
+// the line length in shared memory; the inverse transform conjugates them
+// where it uses them and does not scale (the caller divides by the size).
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -36,9 +36,11 @@ inline bool fft_len_ok(int64_t L) { return L >= 1 && L <= kFftMaxLen && (L & (L 
 // lines per CTA: 16 (2^4), 8 at the largest length (shared memory)
 __host__ __device__ constexpr int fft_log2_lines(int log2L) { return log2L >= 10 ? 3 : 4; }
 
-// CTAs per SM the kernels are compiled for: five up to L = 256 (at most 51
-// registers a thread; 5 x 37 KB of shared memory), else as registers allow.
-__host__ __device__ constexpr int fft_min_ctas(int log2L) { return log2L <= 8 ? 5 : 1; }
+// CTAs per SM the kernels are compiled for: four up to L = 256 (at most 64
+// registers a thread: a radix-16 butterfly and, in the z stage of the
+// Toeplitz product, the 16 spectrum values loaded ahead), else as registers
+// allow.
+__host__ __device__ constexpr int fft_min_ctas(int log2L) { return log2L <= 8 ? 4 : 1; }
 
 // Shared-memory layout of a tile: value i of line w at fft_at(w, i) =
 // w S + i + i / 16, S = L + L / 16 + 1.  The slot after every 16 values
@@ -132,104 +134,176 @@ __device__ __forceinline__ void fft_dft_regs(float2 (&v)[1 << LOG2R])
     for (int i = 0; i < R; ++i) v[i] = t[i];
 }
 
-// One Stockham pass of radix R = 2^LOG2R over the W lines in `buf`, in
-// place, Ns = 2^LOG2NS the length of the sub-transforms already done:
-// butterfly j (< L / R) of a line takes the R values j + r L / R, times
-// e^{-+2 pi i (j mod Ns) r / (Ns R)}, does their R-point DFT and stores
-// output r at (j / Ns) Ns R + (j mod Ns) + r Ns.  Every thread first reads
-// its butterflies into registers and transforms them, then, after a
-// barrier, writes them back.  HALF_IN (first pass only): the values at
-// positions >= L / 2 are zero and are not read.  HALF_OUT (last pass only):
-// only the outputs at positions < L / 2 are written.
-template <bool INVERSE, int LOG2R, int LOG2L, int LOG2NS, bool HALF_IN, bool HALF_OUT>
-__device__ __forceinline__ void fft_pass(float2* buf, const float2* tws)
+// ---- passes
+//
+// A plan is the sequence of radices of the passes: the odd part
+// 2^(log2 L mod 4) first (ODD_FIRST) or last, radix 16 otherwise.  Pass k
+// with radix R = 2^r and Ns = the product of the radices before it (the
+// length of the sub-transforms done) has L / R butterflies per line;
+// butterfly j takes the values at positions j + q L / R, q < R, times
+// e^{-+2 pi i (j mod Ns) q / (Ns R)}, does their R-point DFT and puts output
+// q at (j / Ns) Ns R + (j mod Ns) + q Ns (Stockham: the result of the last
+// pass is in natural order, at j + q L / R).
+template <int LOG2L, bool ODD_FIRST>
+struct FftPlan {
+    static constexpr int odd = LOG2L % 4;
+    static constexpr int passes = LOG2L / 4 + (odd != 0 ? 1 : 0);
+    __host__ __device__ static constexpr int log2r(int k)
+    {
+        if (odd == 0) return 4;
+        return ODD_FIRST ? (k == 0 ? odd : 4) : (k == passes - 1 ? odd : 4);
+    }
+    __host__ __device__ static constexpr int log2ns(int k)
+    {
+        int s = 0;
+        for (int i = 0; i < k; ++i) s += log2r(i);
+        return s;
+    }
+};
+
+// butterflies of a pass of radix 2^LOG2R one thread holds
+__host__ __device__ constexpr int fft_items(int log2L, int log2r)
 {
-    static_assert(!HALF_IN || LOG2NS == 0, "zero inputs are known in the first pass only");
-    static_assert(!HALF_OUT || LOG2NS + LOG2R == LOG2L, "a half is dropped in the last pass only");
-    constexpr int R = 1 << LOG2R;
+    return (1 << (fft_log2_lines(log2L) + log2L - log2r)) >= kFftThreads
+               ? (1 << (fft_log2_lines(log2L) + log2L - log2r)) / kFftThreads
+               : 1;
+}
+
+// Butterfly `it` of this thread in a pass of radix 2^LOG2R: line w, index j
+// (< L / R).  WFAST: consecutive lanes take consecutive lines (a strided
+// axis, whose W lines of a CTA are adjacent in memory: a warp's global
+// accesses at one position are contiguous); otherwise consecutive lanes take
+// consecutive j of one line (a contiguous axis).  Returns false for a
+// thread without that butterfly.
+template <int LOG2L, int LOG2R, bool WFAST>
+__device__ __forceinline__ bool fft_item(int it, int& w, int& j)
+{
     constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int log2per = LOG2L - LOG2R;
+    const int b = threadIdx.x + it * kFftThreads;
+    if (WFAST) { w = b & ((1 << log2W) - 1); j = b >> log2W; }
+    else { w = b >> log2per; j = b & ((1 << log2per) - 1); }
+    return b < (1 << (log2W + log2per));
+}
+
+// the pass twiddles of butterfly j, times its inputs 1 .. R - 1
+template <bool INVERSE, int LOG2L, int LOG2R, int LOG2NS>
+__device__ __forceinline__ void fft_twiddle(float2 (&v)[1 << LOG2R], int j, const float2* tws)
+{
+    if constexpr (LOG2NS > 0) {
+        constexpr int sh = LOG2L - LOG2NS - LOG2R;     // twiddle index unit
+        const int jm = j & ((1 << LOG2NS) - 1);
+#pragma unroll
+        for (int q = 1; q < (1 << LOG2R); ++q) {
+            const float2 t = tws[(jm * q) << sh];
+            const float2 x = v[q];
+            v[q] = INVERSE ? make_float2(x.x * t.x + x.y * t.y, x.y * t.x - x.x * t.y)   // x conj(t)
+                           : make_float2(x.x * t.x - x.y * t.y, x.x * t.y + x.y * t.x);
+        }
+    }
+}
+
+// Between pass A and pass B: A's outputs (ya) to shared memory, then B's
+// inputs (yb) from it, times B's twiddles, and B's DFTs.  The barrier in
+// front keeps the writes behind every read of the previous exchange.
+template <bool INVERSE, int LOG2L, int LOG2RA, int LOG2NSA, int LOG2RB, bool WFAST, int IA, int IB>
+__device__ __forceinline__ void fft_exchange(float2* buf, const float2* tws,
+                                             const float2 (&ya)[IA][1 << LOG2RA],
+                                             float2 (&yb)[IB][1 << LOG2RB])
+{
     constexpr int S = fft_line_stride(LOG2L);
-    constexpr int log2per = LOG2L - LOG2R;          // butterflies per line
-    constexpr int per = 1 << log2per;
-    constexpr int work = 1 << (log2W + log2per);
-    // butterflies one thread holds between the read and the write half
-    constexpr int ITEMS = work >= kFftThreads ? work / kFftThreads : 1;
-    constexpr int sh = LOG2L - LOG2NS - LOG2R;      // twiddle index unit
-    constexpr int ns_mask = (1 << LOG2NS) - 1;
-    float2 y[ITEMS][R];
+    constexpr int nsa_mask = (1 << LOG2NSA) - 1;
+    __syncthreads();
 #pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int b = threadIdx.x + it * kFftThreads;
-        if (b < work) {
-            const int w = b >> log2per;
-            const int j = b & (per - 1);
-            const int jm = j & ns_mask;
+    for (int it = 0; it < IA; ++it) {
+        int w, j;
+        if (fft_item<LOG2L, LOG2RA, WFAST>(it, w, j)) {
+            const int base = ((j >> LOG2NSA) << (LOG2NSA + LOG2RA)) + (j & nsa_mask);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (HALF_IN && r >= R / 2) {   // position j + r L / R >= L / 2
-                    y[it][r] = make_float2(0.f, 0.f);
-                    continue;
-                }
-                float2 x = buf[fft_at(S, w, j + r * per)];
-                if (LOG2NS > 0 && r > 0) {
-                    const float2 t = tws[(jm * r) << sh];
-                    if (INVERSE)   // x * conj(t)
-                        x = make_float2(x.x * t.x + x.y * t.y, x.y * t.x - x.x * t.y);
-                    else
-                        x = make_float2(x.x * t.x - x.y * t.y, x.x * t.y + x.y * t.x);
-                }
-                y[it][r] = x;
-            }
-            fft_dft_regs<INVERSE, LOG2R, HALF_IN>(y[it]);
+            for (int q = 0; q < (1 << LOG2RA); ++q)
+                buf[fft_at(S, w, base + (q << LOG2NSA))] = ya[it][q];
         }
     }
     __syncthreads();
+    constexpr int perb = 1 << (LOG2L - LOG2RB);
 #pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int b = threadIdx.x + it * kFftThreads;
-        if (b < work) {
-            const int w = b >> log2per;
-            const int j = b & (per - 1);
-            const int base = ((j >> LOG2NS) << (LOG2NS + LOG2R)) + (j & ns_mask);
+    for (int it = 0; it < IB; ++it) {
+        int w, j;
+        if (fft_item<LOG2L, LOG2RB, WFAST>(it, w, j)) {
 #pragma unroll
-            for (int r = 0; r < (HALF_OUT ? R / 2 : R); ++r)
-                buf[fft_at(S, w, base + (r << LOG2NS))] = y[it][r];
+            for (int q = 0; q < (1 << LOG2RB); ++q) yb[it][q] = buf[fft_at(S, w, j + q * perb)];
+            fft_twiddle<INVERSE, LOG2L, LOG2RB, LOG2NSA + LOG2RA>(yb[it], j, tws);
+            fft_dft_regs<INVERSE, LOG2RB, false>(yb[it]);
         }
     }
-    __syncthreads();
 }
 
-// The passes from sub-transform length 2^LOG2NS up: first the odd part
-// (radix 2^(log2 L mod 4)), then radix-16 passes.
-template <bool INVERSE, int LOG2L, int LOG2NS, bool HALF_IN, bool HALF_OUT>
-__device__ __forceinline__ void fft_passes_from(float2* buf, const float2* tws)
+// The passes after pass K, whose outputs are in y; then fin(y) with the last
+// pass's outputs: butterfly (w, j) of fft_item, output q at position
+// j + q L / R_last.
+template <bool INVERSE, int LOG2L, bool ODD_FIRST, bool WFAST, int K, int I, int R, class Fin>
+__device__ __forceinline__ void fft_run_from(float2* buf, const float2* tws, float2 (&y)[I][R],
+                                             Fin&& fin)
 {
-    if constexpr (LOG2NS < LOG2L) {
-        constexpr int LOG2R = (LOG2NS == 0 && LOG2L % 4 != 0) ? LOG2L % 4 : 4;
-        constexpr bool last = LOG2NS + LOG2R == LOG2L;
-        fft_pass<INVERSE, LOG2R, LOG2L, LOG2NS, HALF_IN && LOG2NS == 0, HALF_OUT && last>(buf,
-                                                                                           tws);
-        fft_passes_from<INVERSE, LOG2L, LOG2NS + LOG2R, HALF_IN, HALF_OUT>(buf, tws);
+    using P = FftPlan<LOG2L, ODD_FIRST>;
+    if constexpr (K + 1 == P::passes) {
+        fin(y);
+    } else {
+        constexpr int RB = P::log2r(K + 1);
+        constexpr int IB = fft_items(LOG2L, RB);
+        float2 z[IB][1 << RB];
+        fft_exchange<INVERSE, LOG2L, P::log2r(K), P::log2ns(K), RB, WFAST>(buf, tws, y, z);
+        fft_run_from<INVERSE, LOG2L, ODD_FIRST, WFAST, K + 1>(buf, tws, z, fin);
     }
 }
 
-// The tile of a CTA: W lines of L values.  Element e of the tile is line
-// w, position j: on a contiguous axis w = e / L, j = e % L (a warp reads 32
-// consecutive values of one line); on a strided axis j = e / W, w = e % W (a
-// warp reads the same position of W consecutive lines, which are adjacent
-// in memory).
-template <int LOG2L, bool HALF = false>
-__device__ __forceinline__ void fft_tile_elem(bool contiguous, int e, int& w, int& j)
+// The transform of the CTA's W lines: the first pass takes its inputs from
+// load(w, position) straight into registers (HALF_IN: the positions >= L / 2
+// are zero and not loaded, and the first DFT stage skips them), shared
+// memory carries the values between passes only, and fin gets the last
+// pass's outputs in registers (see fft_run_from).  Lines past the end are
+// the loader's and fin's to skip.  The first pass has Ns = 1: no twiddles.
+template <bool INVERSE, int LOG2L, bool ODD_FIRST, bool WFAST, bool HALF_IN, class Load, class Fin>
+__device__ __forceinline__ void fft_lines(float2* buf, const float2* tws, Load&& load, Fin&& fin)
 {
-    constexpr int log2W = fft_log2_lines(LOG2L);
-    constexpr int log2row = HALF ? LOG2L - 1 : LOG2L;   // values per line visited
-    if (contiguous) { w = e >> log2row; j = e & ((1 << log2row) - 1); }
-    else { j = e >> log2W; w = e & ((1 << log2W) - 1); }
+    using P = FftPlan<LOG2L, ODD_FIRST>;
+    constexpr int R0 = P::log2r(0);
+    constexpr int I0 = fft_items(LOG2L, R0);
+    constexpr int per0 = 1 << (LOG2L - R0);
+    float2 y[I0][1 << R0];
+    // every load of the thread in flight before the first use
+#pragma unroll
+    for (int it = 0; it < I0; ++it) {
+        int w, j;
+        const bool on = fft_item<LOG2L, R0, WFAST>(it, w, j);
+#pragma unroll
+        for (int q = 0; q < (1 << R0); ++q)
+            y[it][q] = (on && !(HALF_IN && q >= (1 << R0) / 2)) ? load(w, j + q * per0)
+                                                                 : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int it = 0; it < I0; ++it) fft_dft_regs<INVERSE, R0, HALF_IN>(y[it]);
+    fft_run_from<INVERSE, LOG2L, ODD_FIRST, WFAST, 0>(buf, tws, y, fin);
+}
+
+// The last pass of a plan: its log2 radix, and the stride of its outputs
+// (output q of butterfly j sits at position j + q * fft_last_per).
+template <int LOG2L, bool ODD_FIRST>
+__host__ __device__ constexpr int fft_last_log2r()
+{
+    return FftPlan<LOG2L, ODD_FIRST>::log2r(FftPlan<LOG2L, ODD_FIRST>::passes - 1);
+}
+
+template <int LOG2L, bool ODD_FIRST>
+__host__ __device__ constexpr int fft_last_per()
+{
+    return 1 << (LOG2L - fft_last_log2r<LOG2L, ODD_FIRST>());
 }
 
 // Twiddles of length L in shared memory: tws[m] = e^{-2 pi i m / L}, m < L,
 // from the per-device table of e^{-2 pi i k / 2^10}, k < 2^9 (the upper half
-// of the circle is its negation).
+// of the circle is its negation).  The first exchange's barrier makes them
+// visible before any pass uses them.
 template <int LOG2L>
 __device__ __forceinline__ void fft_stage_twiddles(float2* tws, const float2* tw)
 {
@@ -242,86 +316,40 @@ __device__ __forceinline__ void fft_stage_twiddles(float2* tws, const float2* tw
     }
 }
 
-// Fill the tile: buf[w][j] = get(w, j) for every element (HALF: for the
-// lower half of every line only), eight loads in flight per thread before
-// their shared-memory stores.  get returns zero for lines past the end and
-// for positions known to be zero.
-template <int LOG2L, bool HALF = false, class Get>
-__device__ __forceinline__ void fft_load_tile(float2* buf, bool contiguous, Get get)
-{
-    constexpr int total = (1 << fft_log2_lines(LOG2L)) << (HALF ? LOG2L - 1 : LOG2L);
-    constexpr int S = fft_line_stride(LOG2L);
-    constexpr int U = 8;
-    for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
-        float2 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = e0 + u * kFftThreads;
-            int w, j;
-            fft_tile_elem<LOG2L, HALF>(contiguous, e, w, j);
-            v[u] = e < total ? get(w, j) : make_float2(0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = e0 + u * kFftThreads;
-            int w, j;
-            fft_tile_elem<LOG2L, HALF>(contiguous, e, w, j);
-            if (e < total) buf[fft_at(S, w, j)] = v[u];
-        }
-    }
-}
-
-// Hand every element of the tile (HALF: of the lower half of every line)
-// to put(w, j, value).
-template <int LOG2L, bool HALF = false, class Put>
-__device__ __forceinline__ void fft_store_tile(const float2* buf, bool contiguous, Put put)
-{
-    constexpr int total = (1 << fft_log2_lines(LOG2L)) << (HALF ? LOG2L - 1 : LOG2L);
-    constexpr int S = fft_line_stride(LOG2L);
-    for (int e = threadIdx.x; e < total; e += kFftThreads) {
-        int w, j;
-        fft_tile_elem<LOG2L, HALF>(contiguous, e, w, j);
-        put(w, j, buf[fft_at(S, w, j)]);
-    }
-}
-
-// The whole transform of the W lines in buf (natural order in and out).
-// HALF_IN: the upper half of every line is zero (and need not be in buf);
-// HALF_OUT: only the lower half of the result is wanted.
-template <bool INVERSE, int LOG2L, bool HALF_IN = false, bool HALF_OUT = false>
-__device__ __forceinline__ void fft_tile_passes(float2* buf, const float2* tws)
-{
-    fft_passes_from<INVERSE, LOG2L, 0, HALF_IN, HALF_OUT>(buf, tws);
-}
-
 // One axis of a 3-D FFT in place, `lines` lines of length L = 2^LOG2L at
-// element stride inner = 2^log2inner: element j of line (o, i) is
-// a[(o L + j) inner + i].
-template <bool INVERSE, int LOG2L>
-__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) fft_axis_kernel(float2* a, int log2inner,
-                                                               int64_t lines, const float2* tw)
+// element stride inner = 2^log2inner (CONTIG: inner = 1): element j of line
+// (o, i) is a[(o L + j) inner + i].
+template <bool INVERSE, int LOG2L, bool CONTIG>
+__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
+    fft_axis_kernel(float2* a, int log2inner, int64_t lines, const float2* tw)
 {
     extern __shared__ float2 fft_sm[];
     constexpr int log2W = fft_log2_lines(LOG2L);
     float2* const buf = fft_sm;
     float2* const tws = fft_sm + (fft_line_stride(LOG2L) << log2W);
     const int64_t group = int64_t(blockIdx.x) << log2W;
-    const bool contiguous = log2inner == 0;
     const int64_t inner_mask = (int64_t(1) << log2inner) - 1;
     auto gidx = [&](int w, int j) -> int64_t {
         const int64_t line = group + w;
-        const int64_t o = line >> log2inner;
-        return (((o << LOG2L) + j) << log2inner) + (line & inner_mask);
+        if (CONTIG) return (line << LOG2L) + j;
+        return ((((line >> log2inner) << LOG2L) + j) << log2inner) + (line & inner_mask);
     };
     fft_stage_twiddles<LOG2L>(tws, tw);
-    fft_load_tile<LOG2L>(buf, contiguous, [&](int w, int j) {
-        return group + w < lines ? a[gidx(w, j)] : make_float2(0.f, 0.f);
-    });
-    __syncthreads();
-    fft_tile_passes<INVERSE, LOG2L>(buf, tws);
-    fft_store_tile<LOG2L>(buf, contiguous, [&](int w, int j, float2 v) {
-        if (group + w < lines) a[gidx(w, j)] = v;
-    });
+    constexpr int RL = fft_last_log2r<LOG2L, true>();
+    constexpr int last_per = fft_last_per<LOG2L, true>();
+    fft_lines<INVERSE, LOG2L, true, !CONTIG, false>(
+        buf, tws,
+        [&](int w, int pos) { return group + w < lines ? a[gidx(w, pos)] : make_float2(0.f, 0.f); },
+        [&](auto& y) {
+#pragma unroll
+            for (int it = 0; it < fft_items(LOG2L, RL); ++it) {
+                int w, j;
+                if (fft_item<LOG2L, RL, !CONTIG>(it, w, j) && group + w < lines) {
+#pragma unroll
+                    for (int q = 0; q < (1 << RL); ++q) a[gidx(w, j + q * last_per)] = y[it][q];
+                }
+            }
+        });
 }
 
 }  // namespace mri

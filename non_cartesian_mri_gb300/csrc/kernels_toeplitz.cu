@@ -142,21 +142,27 @@ struct ToeplitzArgs {
 };
 
 // Every index below fits in 32 bits: the grid is at most 512 per axis, so
-// K has at most 2^30 values.
+// K has at most 2^30 values.  Transforms use the plan with the odd radix
+// first; the inverse transform of the z stage, which starts from the forward
+// transform's registers, uses the plan with the odd radix last, so that its
+// first pass has the forward transform's last radix and butterflies.
 template <int STAGE, int LOG2L>
-__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_stage_kernel(ToeplitzArgs p,
-                                                                     int64_t lines64,
-                                                                     const float2* tw)
+__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
+    toeplitz_stage_kernel(ToeplitzArgs p, int64_t lines64, const float2* tw)
 {
     extern __shared__ float2 fft_sm[];
     constexpr int log2W = fft_log2_lines(LOG2L);
-    constexpr int S = fft_line_stride(LOG2L);
     float2* const buf = fft_sm;
-    float2* const tws = fft_sm + (S << log2W);
+    float2* const tws = fft_sm + (fft_line_stride(LOG2L) << log2W);
     const uint32_t lines = uint32_t(lines64);
     const uint32_t group = blockIdx.x << log2W;
     const int log2Lx = p.log2nx + 1, log2Ly = p.log2ny + 1;
     const float2 zero = make_float2(0.f, 0.f);
+    // the last pass of a transform: radix, butterflies a thread holds, and
+    // the stride of its outputs
+    constexpr int RL = fft_last_log2r<LOG2L, true>();
+    constexpr int IL = fft_items(LOG2L, RL);
+    constexpr int per = fft_last_per<LOG2L, true>();
     fft_stage_twiddles<LOG2L>(tws, tw);
     if constexpr (STAGE == kXFwd || STAGE == kXInv) {
         const uint32_t ymask = (1u << p.log2ny) - 1;
@@ -168,40 +174,52 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
         auto vidx = [&](int w, int j) -> uint32_t { return ((group + w) << p.log2nx) + j; };
         if constexpr (STAGE == kXFwd) {
             // the positions ix >= nx of the padded line are zero: not loaded
-            fft_load_tile<LOG2L, true>(buf, true, [&](int w, int j) {
-                if (group + w >= lines) return zero;
-                const uint32_t n = vidx(w, j);
-                return make_float2(p.ir[n], p.ii[n]);
-            });
-            __syncthreads();
-            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
-            fft_store_tile<LOG2L>(buf, true, [&](int w, int j, float2 v) {
-                if (group + w < lines) p.work[widx(w, j)] = v;
-            });
+            fft_lines<false, LOG2L, true, false, true>(
+                buf, tws,
+                [&](int w, int pos) {
+                    if (group + w >= lines) return zero;
+                    const uint32_t n = vidx(w, pos);
+                    return make_float2(p.ir[n], p.ii[n]);
+                },
+                [&](auto& y) {
+#pragma unroll
+                    for (int it = 0; it < IL; ++it) {
+                        int w, j;
+                        if (fft_item<LOG2L, RL, false>(it, w, j) && group + w < lines) {
+#pragma unroll
+                            for (int q = 0; q < (1 << RL); ++q) p.work[widx(w, j + q * per)] = y[it][q];
+                        }
+                    }
+                });
         } else {
-            fft_load_tile<LOG2L>(buf, true, [&](int w, int j) {
-                return group + w < lines ? p.work[widx(w, j)] : zero;
-            });
-            __syncthreads();
-            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
-            // the corner ix < nx only
             FloatSum dot;
-            fft_store_tile<LOG2L, true>(buf, true, [&](int w, int j, float2 v) {
-                if (group + w >= lines) return;
-                const uint32_t n = vidx(w, j);
-                // v[n] is read before out[n] is written by the same thread
-                const float vr = p.ir[n], vi = p.ii[n];
-                float r = fmaf(p.lambda, vr, v.x * p.scale);
-                float i = fmaf(p.lambda, vi, v.y * p.scale);
-                if (p.accumulate) {
-                    r += p.outr[n];
-                    i += p.outi[n];
-                }
-                p.outr[n] = r;
-                p.outi[n] = i;
-                dot.add(vr * r);
-                dot.add(vi * i);
-            });
+            fft_lines<true, LOG2L, true, false, false>(
+                buf, tws,
+                [&](int w, int pos) { return group + w < lines ? p.work[widx(w, pos)] : zero; },
+                [&](auto& y) {
+#pragma unroll
+                    for (int it = 0; it < IL; ++it) {
+                        int w, j;
+                        if (!fft_item<LOG2L, RL, false>(it, w, j) || group + w >= lines) continue;
+                        // the corner ix < nx: outputs q < R / 2
+#pragma unroll
+                        for (int q = 0; q < (1 << RL) / 2; ++q) {
+                            const uint32_t n = vidx(w, j + q * per);
+                            // v[n] is read before out[n] is written by the same thread
+                            const float vr = p.ir[n], vi = p.ii[n];
+                            float r = fmaf(p.lambda, vr, y[it][q].x * p.scale);
+                            float i = fmaf(p.lambda, vi, y[it][q].y * p.scale);
+                            if (p.accumulate) {
+                                r += p.outr[n];
+                                i += p.outi[n];
+                            }
+                            p.outr[n] = r;
+                            p.outi[n] = i;
+                            dot.add(vr * r);
+                            dot.add(vi * i);
+                        }
+                    }
+                });
             if (p.dot != nullptr) {
                 __shared__ double sm[kDotThreads / 32];
                 const double total = block_sum(dot.value(), sm);
@@ -210,55 +228,69 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L)) toeplitz_sta
         }
     } else {
         // y: line l = iz Lx + ix at stride Lx; z: line l = iy Lx + ix at
-        // stride Lx Ly.  work holds the positions j < L / 2 of a z line (and
-        // of a y line before the y forward stage).
+        // stride Lx Ly.  work holds the positions < L / 2 of a z line (and of
+        // a y line before the y forward stage).
         const int log2inner = STAGE == kZConv ? log2Lx + log2Ly : log2Lx;
         const uint32_t imask = (1u << log2inner) - 1;
         auto gidx = [&](int w, int j) -> uint32_t {
             const uint32_t l = group + w;
             return ((((l >> log2inner) << LOG2L) + j) << log2inner) + (l & imask);
         };
-        constexpr bool half_in = STAGE != kYInv;
-        fft_load_tile<LOG2L, half_in>(buf, false, [&](int w, int j) {
-            return group + w < lines ? p.work[gidx(w, j)] : zero;
-        });
-        __syncthreads();
-        if constexpr (STAGE == kZConv) {
-            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
-            // times the (real) spectrum of Q, eight loads in flight per thread
-            constexpr int total = (1 << log2W) << LOG2L;
-            constexpr int U = 8;
-            for (int e0 = threadIdx.x; e0 < total; e0 += U * kFftThreads) {
-                float k[U];
+        auto load = [&](int w, int pos) { return group + w < lines ? p.work[gidx(w, pos)] : zero; };
+        // the lower half of every line to work
+        auto store_half = [&](auto& y, auto rl, auto per_c) {
+            constexpr int R_ = decltype(rl)::value, PER = decltype(per_c)::value;
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int e = e0 + u * kFftThreads;
-                    int w, j;
-                    fft_tile_elem<LOG2L>(false, e, w, j);
-                    k[u] = (e < total && group + w < lines) ? p.K[gidx(w, j)] : 0.f;
-                }
+            for (int it = 0; it < fft_items(LOG2L, R_); ++it) {
+                int w, j;
+                if (fft_item<LOG2L, R_, true>(it, w, j) && group + w < lines) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int e = e0 + u * kFftThreads;
-                    int w, j;
-                    fft_tile_elem<LOG2L>(false, e, w, j);
-                    if (e < total) {
-                        float2& x = buf[fft_at(S, w, j)];
-                        x = make_float2(x.x * k[u], x.y * k[u]);
-                    }
+                    for (int q = 0; q < (1 << R_) / 2; ++q) p.work[gidx(w, j + q * PER)] = y[it][q];
                 }
             }
-            __syncthreads();
-            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
+        };
+        if constexpr (STAGE == kZConv) {
+            // the (real) spectrum at the positions of the forward transform's
+            // last pass, loaded first so that it arrives during the transform
+            float kreg[IL][1 << RL];
+#pragma unroll
+            for (int it = 0; it < IL; ++it) {
+                int w, j;
+                const bool on = fft_item<LOG2L, RL, true>(it, w, j) && group + w < lines;
+#pragma unroll
+                for (int q = 0; q < (1 << RL); ++q) kreg[it][q] = on ? p.K[gidx(w, j + q * per)] : 0.f;
+            }
+            fft_lines<false, LOG2L, true, true, true>(buf, tws, load, [&](auto& y) {
+#pragma unroll
+                for (int it = 0; it < IL; ++it) {
+#pragma unroll
+                    for (int q = 0; q < (1 << RL); ++q)
+                        y[it][q] = make_float2(y[it][q].x * kreg[it][q], y[it][q].y * kreg[it][q]);
+                    // the inverse transform's first pass (Ns = 1, no twiddles)
+                    fft_dft_regs<true, RL, false>(y[it]);
+                }
+                constexpr int RI = fft_last_log2r<LOG2L, false>();
+                fft_run_from<true, LOG2L, false, true, 0>(buf, tws, y, [&](auto& yo) {
+                    store_half(yo, std::integral_constant<int, RI>{},
+                               std::integral_constant<int, fft_last_per<LOG2L, false>()>{});
+                });
+            });
         } else if constexpr (STAGE == kYFwd) {
-            fft_tile_passes<false, LOG2L, true, false>(buf, tws);
+            fft_lines<false, LOG2L, true, true, true>(buf, tws, load, [&](auto& y) {
+#pragma unroll
+                for (int it = 0; it < IL; ++it) {
+                    int w, j;
+                    if (fft_item<LOG2L, RL, true>(it, w, j) && group + w < lines) {
+#pragma unroll
+                        for (int q = 0; q < (1 << RL); ++q) p.work[gidx(w, j + q * per)] = y[it][q];
+                    }
+                }
+            });
         } else {
-            fft_tile_passes<true, LOG2L, false, true>(buf, tws);
+            fft_lines<true, LOG2L, true, true, false>(buf, tws, load, [&](auto& y) {
+                store_half(y, std::integral_constant<int, RL>{}, std::integral_constant<int, per>{});
+            });
         }
-        constexpr bool half_out = STAGE != kYFwd;
-        fft_store_tile<LOG2L, half_out>(buf, false, [&](int w, int j, float2 v) {
-            if (group + w < lines) p.work[gidx(w, j)] = v;
-        });
     }
 }
 
@@ -458,7 +490,9 @@ cudaError_t fft_axis(float2* a, int log2L, int log2inner, int64_t lines, const f
                      cudaStream_t s)
 {
     return launch_by_length(log2L, lines, s, [&](auto len, auto go) {
-        return go(fft_axis_kernel<INVERSE, decltype(len)::value>, a, log2inner, lines, tw);
+        constexpr int L2 = decltype(len)::value;
+        return log2inner == 0 ? go(fft_axis_kernel<INVERSE, L2, true>, a, log2inner, lines, tw)
+                              : go(fft_axis_kernel<INVERSE, L2, false>, a, log2inner, lines, tw);
     });
 }
 
