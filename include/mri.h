@@ -259,15 +259,16 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
  *
  * mri_toeplitz_kernel: Q on the circular grid of voxel differences of the
  * doubled grid (2nx x 2ny x 2nz: difference i h for i < n, (i - 2n) h for
- * i >= n per axis), computed by the grid Q path with trig mode `trig`, with
- * the planes at index n of every axis set to zero (the difference -n h
- * occurs between no two voxels of the grid, so the product does not use
- * them; without them the grid is Hermitian-symmetric because
- * Q(-d) = conj Q(d)), then the real part of its 3-D FFT (the imaginary part
- * is rounding), written to K: a device array of 8 * nx*ny*nz floats,
- * 8-byte aligned, x fastest.  Samples as mri_q (kx, ky, kz, rPhi, iPhi: M
- * floats each; M = 0 gives K = 0).  Scratch from the stream-ordered pool:
- * 16 floats per point of the doubled grid.
+ * i >= n per axis), computed by the grid Q path with trig mode `trig` on
+ * the z planes below nz and taken as Q(-d) = conj Q(d) of the mirrored
+ * point on the others, with the planes at index n of every axis set to zero
+ * (the difference -n h occurs between no two voxels of the grid, so the
+ * product does not use them; without them the grid is Hermitian-symmetric),
+ * then the real part of its 3-D FFT (the imaginary part is rounding),
+ * written to K: a device array of 8 * nx*ny*nz floats, 8-byte aligned, x
+ * fastest.  Samples as mri_q (kx, ky, kz, rPhi, iPhi: M floats each; M = 0
+ * gives K = 0).  Scratch from the stream-ordered pool: 12 bytes per point of
+ * the doubled grid.
  *
  * mri_toeplitz_apply: out = (F^H F + lambda I) in, from K, for SoA complex
  * vectors of nx*ny*nz floats (rIn, iIn; rOut, iOut, which may be the same

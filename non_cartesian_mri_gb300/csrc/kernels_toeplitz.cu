@@ -48,11 +48,12 @@ __global__ void __launch_bounds__(256) diff_axes_kernel(int nx, int ny, int nz, 
     axes[t] = float(i < n ? i : i - 2 * n) * h;
 }
 
-// Q (SoA) on the doubled grid into the complex array the spectrum is taken
-// of, with the planes at index n of every axis zeroed: they hold Q at the
-// difference -n h, which no voxel pair of the n grid has, and without them
-// the grid is Hermitian-symmetric (Q(-d) = conj Q(d)), so its spectrum is
-// real.
+// The complex array the spectrum is taken of, on the doubled grid, from Q
+// (SoA) on its z planes iz < nz: the planes at index n of every axis are
+// zero (they hold Q at the difference -n h, which no voxel pair of the n
+// grid has, and without them the grid is Hermitian-symmetric, so its
+// spectrum is real), and a point with iz > nz is the conjugate of its mirror
+// image (2nz - iz, -iy, -ix) mod 2n, because Q(-d) = conj Q(d).
 __global__ void __launch_bounds__(256) spectrum_input_kernel(const float* r, const float* i,
                                                              int nx, int ny, int nz,
                                                              float2* out)
@@ -64,8 +65,17 @@ __global__ void __launch_bounds__(256) spectrum_input_kernel(const float* r, con
         const int64_t ix = k % Lx;
         const int64_t iy = (k / Lx) % Ly;
         const int64_t iz = k / (Lx * Ly);
-        const bool unused = ix == nx || iy == ny || iz == nz;
-        out[k] = unused ? make_float2(0.f, 0.f) : make_float2(r[k], i[k]);
+        float2 v = make_float2(0.f, 0.f);
+        if (ix != nx && iy != ny && iz != nz) {
+            if (iz < nz) {
+                v = make_float2(r[k], i[k]);
+            } else {
+                const int64_t src = ((2 * nz - iz) * Ly + ((Ly - iy) & (Ly - 1))) * Lx +
+                                    ((Lx - ix) & (Lx - 1));
+                v = make_float2(r[src], -i[src]);
+            }
+        }
+        out[k] = v;
     }
 }
 

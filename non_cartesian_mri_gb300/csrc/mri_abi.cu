@@ -998,10 +998,12 @@ mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz
     DeviceState* d = nullptr;
     if ((st = prepare(int(trig), 0, 1, M, N2, sp, 5, vp, 1, &d)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // scratch: the difference axes, Q (real and imaginary parts), the
-    // complex spectrum
+    // scratch: the difference axes, Q (real and imaginary parts) on the z
+    // planes iz < nz (the others follow by conjugate symmetry), the complex
+    // spectrum
     const int64_t axes_n = 2 * (int64_t(nx) + ny + nz);
-    const int64_t q_bytes = align256(2 * N2 * 4);
+    const int64_t Nq = N2 / 2;
+    const int64_t q_bytes = align256(2 * Nq * 4);
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
                                 size_t(align256(axes_n * 4) + q_bytes + N2 * 8), d->pool,
@@ -1009,17 +1011,18 @@ mri_status mri_toeplitz_kernel(const float* kx, const float* ky, const float* kz
         return cuda_fail();
     float* axes = reinterpret_cast<float*>(scratch);
     float* q_r = reinterpret_cast<float*>(scratch + align256(axes_n * 4));
-    float* q_i = q_r + N2;
+    float* q_i = q_r + Nq;
     float2* spec = reinterpret_cast<float2*>(scratch + align256(axes_n * 4) + q_bytes);
     if (mri::launch_diff_axes(nx, ny, nz, hx, hy, hz, axes, s) != cudaSuccess) st = cuda_fail();
-    // Q(d) = sum_m |Phi_m|^2 e^{+i 2 pi k_m . d} on the difference grid: the
-    // grid Q path (tensor cores for 2 nx >= 8)
+    // Q(d) = sum_m |Phi_m|^2 e^{+i 2 pi k_m . d} on the difference grid's z
+    // planes 0 .. nz - 1: the grid Q path (tensor cores for 2 nx >= 8)
     if (st == MRI_OK)
         st = run_grid_call(true, 1, kx, ky, kz, axes, 2 * nx, axes + 2 * nx, 2 * ny,
-                           axes + 2 * nx + 2 * ny, 2 * nz, rPhi, iPhi, nullptr, nullptr, M, q_r,
+                           axes + 2 * nx + 2 * ny, nz, rPhi, iPhi, nullptr, nullptr, M, q_r,
                            q_i, int(trig), 0, d, s);
-    // the index-n planes zeroed (unused by the product; without them the
-    // spectrum is real), FFT, real part
+    // the other planes by conjugate symmetry, the index-n planes zeroed
+    // (unused by the product; without them the spectrum is real), FFT, real
+    // part
     if (st == MRI_OK &&
         (mri::launch_spectrum_input(q_r, q_i, nx, ny, nz, spec, grid_for(N2, d->sms), s) !=
              cudaSuccess ||
