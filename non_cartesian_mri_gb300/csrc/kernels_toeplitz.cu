@@ -21,6 +21,38 @@ namespace mri {
 
 namespace {
 
+// Programmatic dependent launch: the kernels of a product and of a CG
+// iteration run back to back on one stream, each short.  Each one lets the
+// next one launch as soon as all of its CTAs have started
+// (pdl_launch_dependents), and each one waits for the previous one to finish,
+// with its writes visible (pdl_wait), before it touches any buffer; what
+// comes before the wait (the twiddle staging, index set-up) reads nothing
+// the previous kernel writes.  Launched without the attribute, both are
+// no-ops.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // tw[k] = e^{-2 pi i k / kFftMaxLen}, k < kFftMaxLen / 2, from double precision
 __global__ void __launch_bounds__(256) fft_twiddle_kernel(float2* tw)
 {
@@ -173,7 +205,9 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
     constexpr int RL = fft_last_log2r<LOG2L, true>();
     constexpr int IL = fft_items(LOG2L, RL);
     constexpr int per = fft_last_per<LOG2L, true>();
+    pdl_launch_dependents();
     fft_stage_twiddles<LOG2L>(tws, tw);
+    pdl_wait();
     if constexpr (STAGE == kXFwd || STAGE == kXInv) {
         const uint32_t ymask = (1u << p.log2ny) - 1;
         // line l = iz ny + iy: its row of work, and its row of v
@@ -309,6 +343,8 @@ __global__ void __launch_bounds__(kDotThreads) dot_partial_kernel(const float* a
                                                                   const float* br, const float* bi,
                                                                   int64_t n, double* partial)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ double sm[kDotThreads / 32];
     FloatSum v;
     for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
@@ -323,6 +359,8 @@ __global__ void __launch_bounds__(kDotThreads) dot_partial_kernel(const float* a
 __global__ void __launch_bounds__(kDotThreads) sum_partials_kernel(const double* partial, int n,
                                                                    double* out)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ double sm[kDotThreads / 32];
     double v = 0.0;
     for (int k = threadIdx.x; k < n; k += kDotThreads) v += partial[k];   // fixed order
@@ -352,6 +390,8 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
                                                             const double* rr, const double* pap,
                                                             double* partial)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ double sm[kDotThreads / 32];
     const float alpha = cg_ratio(rr, pap);
     FloatSum v;
@@ -404,6 +444,8 @@ __global__ void __launch_bounds__(256) cg_p_kernel(float* pr, float* pi, const f
                                                    const float* ri, int64_t n,
                                                    const double* rr_new, const double* rr_old)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const float beta = cg_ratio(rr_new, rr_old);
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     if constexpr (VEC) {
@@ -427,6 +469,8 @@ __global__ void __launch_bounds__(256) cg_start_kernel(const float* br, const fl
                                                        float* rr_, float* ri, float* pr,
                                                        float* pi, int64_t n)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n;
          k += int64_t(gridDim.x) * blockDim.x) {
         const float a = br[k] - rr_[k];
@@ -440,6 +484,8 @@ __global__ void __launch_bounds__(256) cg_start_kernel(const float* br, const fl
 
 __global__ void __launch_bounds__(256) sqrt_kernel(double* v, int n)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k < n) v[k] = sqrt(v[k]);
 }
@@ -477,8 +523,7 @@ cudaError_t launch_by_length(int log2L, int64_t lines, cudaStream_t s, Pick pick
                                      int(cudaSharedmemCarveoutMaxShared));
         if (e != cudaSuccess) return e;
         const int64_t W = int64_t(1) << fft_log2_lines(log2L);
-        kernel<<<unsigned((lines + W - 1) / W), kFftThreads, smem, s>>>(args...);
-        return cudaGetLastError();
+        return launch_pdl(kernel, unsigned((lines + W - 1) / W), kFftThreads, smem, s, args...);
     };
     switch (log2L) {
         case 1: return pick(std::integral_constant<int, 1>{}, go);
@@ -623,30 +668,33 @@ cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, cons
     cudaError_t e = toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, nullptr, tw,
                                    s);
     if (e != cudaSuccess) return e;
-    cg_start_kernel<<<grid, 256, 0, s>>>(br, bi, r_r, r_i, p_r, p_i, N);
-    dot_partial_kernel<<<dot_blocks, kDotThreads, 0, s>>>(r_r, r_i, r_r, r_i, N, partial);
-    sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, rr);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(cg_start_kernel, grid, 256, 0, s, br, bi, r_r, r_i, p_r, p_i, N);
+    if (e == cudaSuccess)
+        e = launch_pdl(dot_partial_kernel, dot_blocks, kDotThreads, 0, s, r_r, r_i, r_r, r_i, N,
+                       partial);
+    if (e == cudaSuccess)
+        e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks, rr);
+    if (e != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
         // Ap, with the per-CTA sums of p.Ap from its last stage
         e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s);
+        if (e == cudaSuccess)
+            e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, int(apply_blocks),
+                           pap);
+        if (e == cudaSuccess)
+            e = launch_pdl(vec4 ? cg_xr_kernel<true> : cg_xr_kernel<false>, dot_blocks,
+                           kDotThreads, 0, s, xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it,
+                           pap, partial);
+        if (e == cudaSuccess)
+            e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks,
+                           rr + it + 1);
+        if (e == cudaSuccess)
+            e = launch_pdl(vec4 ? cg_p_kernel<true> : cg_p_kernel<false>, grid, 256, 0, s, p_r, p_i,
+                           r_r, r_i, N, rr + it + 1, rr + it);
         if (e != cudaSuccess) return e;
-        sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, int(apply_blocks), pap);
-        if (vec4)
-            cg_xr_kernel<true><<<dot_blocks, kDotThreads, 0, s>>>(
-                xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it, pap, partial);
-        else
-            cg_xr_kernel<false><<<dot_blocks, kDotThreads, 0, s>>>(
-                xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it, pap, partial);
-        sum_partials_kernel<<<1, kDotThreads, 0, s>>>(partial, dot_blocks, rr + it + 1);
-        if (vec4)
-            cg_p_kernel<true><<<grid, 256, 0, s>>>(p_r, p_i, r_r, r_i, N, rr + it + 1, rr + it);
-        else
-            cg_p_kernel<false><<<grid, 256, 0, s>>>(p_r, p_i, r_r, r_i, N, rr + it + 1, rr + it);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    sqrt_kernel<<<(iters + 1 + 255) / 256, 256, 0, s>>>(rr, iters + 1);
-    return cudaGetLastError();
+    e = launch_pdl(sqrt_kernel, (iters + 1 + 255) / 256, 256, 0, s, rr, iters + 1);
+    return e;
 }
 
 }  // namespace mri
