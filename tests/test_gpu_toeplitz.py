@@ -11,6 +11,10 @@
   iterates and residual norms, and a reconstruction of a seeded image from
   its own samples (D = F rho, b = F^H D) whose error falls with the
   iterations;
+- at the benchmarked size (128^3, radial trajectory): the product against
+  F^H (Phi F v) from the grid forward model and F^H D, Hermitian symmetry,
+  positivity and the lambda term; CG lowering its energy functional at every
+  step and reporting the residual of its iterate;
 - argument errors.
 
 Tolerances: one Toeplitz product is Q (accurate path, ~2e-6) through two
@@ -200,3 +204,81 @@ def test_toeplitz_argument_errors(mri):
     assert lib.mri_fft3(P(C.data_ptr()), 8, 8, 8, 2, None) == 5   # MRI_ERR_MODE
     with pytest.raises(ValueError):
         mri.toeplitz_apply(C, v[:64], v[:64])
+
+
+@pytest.fixture(scope="module")
+def radial_128(mri):
+    """The 128^3 radial workload (the benchmarked find-rho configuration):
+    its trajectory and weights on the device, the spectrum with accurate trig,
+    and a seeded complex vector."""
+    from non_cartesian_mri_gb300 import workloads as wl
+    w = wl.make_workload("fhd_128_radial")
+    k = [dev(w.kx), dev(w.ky), dev(w.kz)]
+    phi = [dev(w.rPhi), dev(w.iPhi)]
+    ax = [dev(a) for a in w.axes()]
+    K = mri.toeplitz_kernel(*k, *phi, (w.L, w.L, w.L), trig="accurate")
+    rng = np.random.default_rng(123)
+    v = [dev(rng.standard_normal(w.N).astype(np.float32)) for _ in range(2)]
+    return w, k, phi, ax, K, v
+
+
+def test_toeplitz_apply_full_size_matches_forward_then_adjoint(mri, radial_128):
+    """At the benchmarked size the oracle cannot form F^H F v, so the product
+    is checked against the other route through the definition: F^H (Phi F v)
+    with the grid forward model and F^H D (both checked against the oracle at
+    this size), accurate trig on every side.  Each side carries ~2e-6."""
+    w, k, phi, ax, K, v = radial_128
+    r, i = mri.toeplitz_apply(K, *v, lam=0.0)
+    fr, fi = mri.forward_grid(*k, *ax, *v, trig="accurate")
+    pr = phi[0] * fr - phi[1] * fi
+    pi = phi[0] * fi + phi[1] * fr
+    dr, di = mri.fhd_grid(*k, *ax, *phi, pr, pi, trig="accurate")
+    assert oracle.rel_l2(cplx(r, i), cplx(dr, di)) < 2e-5
+    assert mri.device_errors(clear=True) == 0
+
+
+def test_toeplitz_apply_full_size_is_hermitian_and_linear(mri, radial_128):
+    """<u, A v> = conj <v, A u>, <v, A v> real and positive, and
+    A(a v) = a A(v) with lambda I added exactly."""
+    w, k, phi, ax, K, v = radial_128
+    rng = np.random.default_rng(124)
+    u = [dev(rng.standard_normal(w.N).astype(np.float32)) for _ in range(2)]
+    Av = cplx(*mri.toeplitz_apply(K, *v))
+    Au = cplx(*mri.toeplitz_apply(K, *u))
+    vv, uu = cplx(*v), cplx(*u)
+    lhs = np.vdot(uu, Av)
+    rhs = np.conj(np.vdot(vv, Au))
+    assert abs(lhs - rhs) < 1e-5 * np.linalg.norm(uu) * np.linalg.norm(Av)
+    q = np.vdot(vv, Av)
+    assert q.real > 0 and abs(q.imag) < 1e-5 * abs(q)
+    lam = 0.75
+    Avl = cplx(*mri.toeplitz_apply(K, *v, lam=lam))
+    assert oracle.rel_l2(Avl, Av + lam * vv) < 1e-6
+
+
+def test_cg_full_size_descends_and_reports_its_residuals(mri, radial_128):
+    """CG at the benchmarked size.  Without density compensation F^H F has a
+    very wide spectrum (the radial centre of k-space is sampled densely), so
+    the residual norm need not fall; what CG guarantees is that every step
+    lowers phi(x) = x^H (A + lambda I) x / 2 - Re b^H x (the energy norm of
+    the error).  Checked over the iterates, plus: the last reported norm is
+    that of b - (A + lambda I) x recomputed from the returned iterate."""
+    w, k, phi, ax, K, v = radial_128
+    lam = 0.01
+    b = cplx(*v)
+
+    def energy(x_r, x_i):
+        x = cplx(x_r, x_i)
+        Ax = cplx(*mri.toeplitz_apply(K, x_r, x_i, lam=lam))
+        return 0.5 * np.vdot(x, Ax).real - np.vdot(b, x).real, Ax
+
+    phis = [0.0]
+    for iters in (1, 2, 5, 10):
+        xr, xi, norms = mri.cg_solve(K, *v, lam=lam, iters=iters)
+        e, Ax = energy(xr, xi)
+        phis.append(e)
+    assert all(b_ < a_ for a_, b_ in zip(phis, phis[1:])), phis
+    n = norms.cpu().numpy()
+    assert np.all(np.isfinite(n))
+    assert abs(np.linalg.norm(b - Ax) - n[-1]) < 1e-3 * n.max()
+    assert mri.device_errors(clear=True) == 0
