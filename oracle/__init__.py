@@ -1,5 +1,6 @@
-"""fp64 CPU oracle for F^H D, Q, batched F^H D, the forward model and (in
-``oracle.toeplitz``) the Toeplitz F^H F product and the CG solve.
+"""fp64 CPU oracle for F^H D, Q, batched F^H D, the forward model, (in
+``oracle.toeplitz``) the Toeplitz F^H F product and the CG solve, and (in
+``oracle.gridding``) the gridding / inverse-DFT reconstruction.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  The product path (the CUDA library and
