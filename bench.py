@@ -103,8 +103,8 @@ def parse_args():
                          "implies --no-paths --no-e2e)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--find-rho", action="store_true",
-                    help="also measure the find-rho step (Toeplitz product, CG iteration) when "
-                         "the other paths are skipped")
+                    help="also measure the find-rho step (Toeplitz product, CG iteration) and "
+                         "the gridding reconstruction when the other paths are skipped")
     return ap.parse_args()
 
 
@@ -530,6 +530,37 @@ def find_rho(torch, mri, dist, args, flush, peaks):
     return out
 
 
+# The gridding reconstruction: bytes per call for M samples on N voxels --
+# the samples read once (k 12, Phi 8, D 8 = 28 B), the grid zeroed (8 B per
+# voxel), the 8M atomic adds (into L2: the grid of a 128^3 image is 16 MB),
+# the inverse FFT's three passes (16 B per voxel each), the signs pass (8 B
+# in, 8 B out).  Algorithmic HBM bytes: 28 M + 72 N.
+GRIDDING_BYTES_PER_SAMPLE = 28
+GRIDDING_BYTES_PER_VOXEL = 8 + 3 * 16 + 16
+
+
+def gridding(torch, mri, dist, args, flush, peaks):
+    """The gridding reconstruction on the headline trajectory and grid."""
+    w = wl.make_workload(HEADLINE)
+    t = to_dev(w, torch)
+    shape = (w.L, w.L, w.L)
+    fn = lambda: mri.gridding(t["kx"], t["ky"], t["kz"], t["rPhi"], t["iPhi"], t["rD"],  # noqa: E731
+                              t["iD"], shape)
+    res = timed_steps(torch, mri, dist, fn, args.steps, args.warmup, flush)
+    ms = statistics.mean(res["step_ms"])
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    nbytes = GRIDDING_BYTES_PER_SAMPLE * w.M + GRIDDING_BYTES_PER_VOXEL * w.N
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: M={w.M:,} samples onto a {w.L}^3 grid",
+            "ms": round(ms, 4), "value": round(w.M / (ms * 1e-3) / 1e9, 3),
+            "unit": "Gsamples/s",
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                         "algorithmic_bytes": nbytes}}
+
+
 def run_ours(args):
     import torch
     import non_cartesian_mri_gb300 as mri
@@ -690,6 +721,7 @@ def run_ours(args):
     if world == 1 and args.workload == HEADLINE and not args.grid_edge and not args.forward and (
             not args.no_paths or args.find_rho):
         line["find_rho"] = find_rho(torch, mri, dist, args, flush, peaks)
+        line["gridding"] = gridding(torch, mri, dist, args, flush, peaks)
 
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl.make_workload(args.workload, L=args.grid_edge))

@@ -309,6 +309,27 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda,
                         const float* rB, const float* iB, float* rX, float* iX,
                         int iters, double* rnorms, void* stream);
 
+/*
+ * The gridding reconstruction (the chapter's comparison method: section
+ * 17.1, Fig. 17.1B; its accuracy in Fig. 17.19).  Each sample's
+ * Mu = conj(Phi) D is interpolated trilinearly onto the 2 x 2 x 2 nearest
+ * points of the Cartesian k-space grid k_g = (g - n/2) / n, g < n, of the
+ * voxel grid (indices modulo n: k is periodic with period 1 on that grid),
+ * then out[iz][iy][ix] = sum_g G[g] e^{+i 2 pi k_g . x} at the voxels
+ * x = (ix - nx/2, iy - ny/2, iz - nz/2) (the integer coordinates of a grid
+ * centred on 0, x fastest).  No density or deapodisation correction beyond
+ * what Phi carries.  Samples as mri_fhd (M floats each, device); rOut, iOut:
+ * nx*ny*nz floats (device); accumulate = 1 adds into them.  nx, ny, nz powers
+ * of two in 1 .. 1024 (MRI_ERR_SIZE otherwise).  Scratch: nx*ny*nz complex
+ * values from the stream-ordered pool.  The grid is summed with atomic adds,
+ * so the summation order (and the last bits of the result) is not fixed.
+ * Asynchronous on `stream`.
+ */
+mri_status mri_gridding(const float* kx, const float* ky, const float* kz,
+                        const float* rPhi, const float* iPhi, const float* rD, const float* iD,
+                        int64_t M, int nx, int ny, int nz, float* rOut, float* iOut,
+                        int accumulate, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* mri_status_string(mri_status status);
 

@@ -88,8 +88,9 @@ def load():
         lib.mri_toeplitz_kernel.argtypes = [P] * 5 + [I64, I, I, I, F, F, F, P, I, P]
         lib.mri_toeplitz_apply.argtypes = [P, I, I, I, F, P, P, P, P, I, P]
         lib.mri_cg_solve.argtypes = [P, I, I, I, F, P, P, P, P, I, P, P]
+        lib.mri_gridding.argtypes = [P] * 7 + [I64, I, I, I, P, P, I, P]
         for f in (lib.mri_fft3, lib.mri_toeplitz_kernel, lib.mri_toeplitz_apply,
-                  lib.mri_cg_solve):
+                  lib.mri_cg_solve, lib.mri_gridding):
             f.restype = ctypes.c_int
         lib.mri_mma_probe.restype = ctypes.c_int
         lib.mri_wait_selftest.restype = ctypes.c_int
@@ -521,3 +522,19 @@ def cg_solve(K, rB, iB, *, lam: float = 0.0, iters: int = 10, x0=None, stream=No
                                _ptr(iX), int(iters), _ptr(norms), _stream_handle(stream)),
            "mri_cg_solve")
     return rX, iX, norms
+
+
+def gridding(kx, ky, kz, rPhi, iPhi, rD, iD, shape, *, accumulate=False, out=None, stream=None):
+    """The gridding reconstruction on a grid of shape (nz, ny, nx) (see
+    mri_gridding): trilinear interpolation of conj(Phi) D onto the Cartesian
+    k-grid, then the inverse DFT onto the voxels x = i - n/2.  Returns
+    (rOut, iOut) of nx*ny*nz floats."""
+    nz, ny, nx = (int(v) for v in shape)
+    kx, ky, kz, rPhi, iPhi, rD, iD = (_as_tensor(t) for t in (kx, ky, kz, rPhi, iPhi, rD, iD))
+    M = kx.numel()
+    _same_len("samples", (kx, ky, kz, rPhi, iPhi, rD, iD), M)
+    r, i = _outputs(out, (nx * ny * nz,), kx.device)
+    _check(load().mri_gridding(_ptr(kx), _ptr(ky), _ptr(kz), _ptr(rPhi), _ptr(iPhi), _ptr(rD),
+                               _ptr(iD), M, nx, ny, nz, _ptr(r), _ptr(i), int(bool(accumulate)),
+                               _stream_handle(stream)), "mri_gridding")
+    return r, i

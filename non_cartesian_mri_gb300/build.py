@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmri.so")
 
 UNITS = ["mri_abi.cu", "kernels_single.cu", "kernels_coils.cu", "kernels_grid.cu",
-         "kernels_grid_tc.cu", "kernels_toeplitz.cu", "microbench.cu", "noalloc.cu"]
+         "kernels_grid_tc.cu", "kernels_toeplitz.cu", "kernels_gridding.cu", "microbench.cu",
+         "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", INCLUDE, "-I", CSRC]

@@ -85,6 +85,13 @@ cudaError_t launch_toeplitz_apply(const float* K, int nx, int ny, int nz, float 
                                   const float* ir, const float* ii, float* outr, float* outi,
                                   int accumulate, float2* work, const float2* tw,
                                   cudaStream_t s);
+// the gridding reconstruction (kernels_gridding.cu): G (nx*ny*nz complex
+// scratch) zeroed, the samples' trilinear scatter, the inverse FFT, the
+// centring signs into out
+cudaError_t launch_gridding(const float* kx, const float* ky, const float* kz, const float* rPhi,
+                            const float* iPhi, const float* rD, const float* iD, int64_t M,
+                            int nx, int ny, int nz, float* outr, float* outi, int accumulate,
+                            float2* G, const float2* tw, int sms, cudaStream_t s);
 cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, const float* br,
                       const float* bi, float* xr, float* xi, int iters, double* rr,
                       float* vec, float2* work, double* scal, const float2* tw, int grid,

@@ -1095,6 +1095,34 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, co
     return st;
 }
 
+// ---------------------------------------------------------------------------
+// the gridding reconstruction
+// ---------------------------------------------------------------------------
+mri_status mri_gridding(const float* kx, const float* ky, const float* kz, const float* rPhi,
+                        const float* iPhi, const float* rD, const float* iD, int64_t M, int nx,
+                        int ny, int nz, float* rOut, float* iOut, int accumulate, void* stream)
+{
+    mri_status st = check_mode(0, accumulate);
+    if (st != MRI_OK) return st;
+    if (!mri::fft_len_ok(nx) || !mri::fft_len_ok(ny) || !mri::fft_len_ok(nz)) return MRI_ERR_SIZE;
+    if (M < 0 || M > kMaxM) return MRI_ERR_SIZE;
+    const int64_t N = int64_t(nx) * ny * nz;
+    const void* sp[7] = {kx, ky, kz, rPhi, iPhi, rD, iD};
+    const void* vp[2] = {rOut, iOut};
+    DeviceState* d = nullptr;
+    if ((st = prepare(0, accumulate, 1, M, N, sp, 7, vp, 2, &d)) != MRI_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2* G = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&G), size_t(N) * sizeof(float2), d->pool,
+                                s) != cudaSuccess)
+        return cuda_fail();
+    if (mri::launch_gridding(kx, ky, kz, rPhi, iPhi, rD, iD, M, nx, ny, nz, rOut, iOut,
+                             accumulate, G, d->fft_tw, d->sms, s) != cudaSuccess)
+        st = cuda_fail();
+    if (cudaFreeAsync(G, s) != cudaSuccess && st == MRI_OK) st = cuda_fail();
+    return st;
+}
+
 const char* mri_status_string(mri_status status)
 {
     switch (status) {
