@@ -481,11 +481,12 @@ def e2e(torch, mri, dist, w, trig, steps, warmup, grid=False):
 #   y inverse   read 4N (32N), write 2N (16N)
 #   x inverse   read 2N (16N) and v (8N), write the result (8N)
 # = 248 bytes per voxel.  The compulsory part (v, K and the result once) is
-# 48.  A CG iteration adds the x / r update (48N) and the p update (24N);
-# p.Ap is summed inside the last stage.
+# 48.  A CG iteration adds the x / r update (48N) and, inside the first
+# stage, the direction update p = r + beta p (r read, p written: 16N); p.Ap
+# is summed inside the last stage.
 TOEPLITZ_BYTES_PER_VOXEL = 8 + 16 + 16 + 32 + 32 + 32 + 32 + 32 + 16 + 16 + 8 + 8
 TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL = 8 + 32 + 8
-CG_EXTRA_BYTES_PER_VOXEL = 48 + 24
+CG_EXTRA_BYTES_PER_VOXEL = 48 + 16
 
 
 def find_rho(torch, mri, dist, args, flush, peaks):

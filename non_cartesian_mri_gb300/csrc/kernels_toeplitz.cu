@@ -153,6 +153,14 @@ __device__ __forceinline__ double block_sum(double v, double* sm)
     return s;   // thread 0
 }
 
+// a CG step ratio, alpha = r.r / p.Ap or beta = new r.r / old r.r (0 once
+// r = 0 or p.Ap = 0)
+__device__ __forceinline__ float cg_ratio(const double* num, const double* den)
+{
+    const double a = *num, b = *den;
+    return (a > 0.0 && b != 0.0) ? float(a / b) : 0.0f;
+}
+
 // ---- the Toeplitz product in five FFT stages over the doubled grid L = 2n.
 // The padded vector is zero outside the corner n and only the corner of the
 // result is kept, so no stage touches more than it must:
@@ -177,6 +185,15 @@ struct ToeplitzArgs {
     float2* work;           // [nz][2 ny][2 nx]
     const float* K;         // [2 nz][2 ny][2 nx], real
     double* dot;            // x inverse: per CTA Re <v, result> (nullptr: none)
+    // x forward, conjugate gradients: v = r + beta v, beta = *rr_new /
+    // *rr_old, is formed, written back to (vw_r, vw_i) = (ir, ii) and
+    // transformed (upd_r == nullptr: v as it is)
+    const float* upd_r;
+    const float* upd_i;
+    const double* rr_new;
+    const double* rr_old;
+    float* vw_r;
+    float* vw_i;
     int log2nx, log2ny, log2nz;
     float scale;            // 1 / |2n|, the inverse transform's normalisation
     float lambda;
@@ -217,13 +234,22 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
         };
         auto vidx = [&](int w, int j) -> uint32_t { return ((group + w) << p.log2nx) + j; };
         if constexpr (STAGE == kXFwd) {
+            const bool upd = p.upd_r != nullptr;
+            const float beta = upd ? cg_ratio(p.rr_new, p.rr_old) : 0.f;
             // the positions ix >= nx of the padded line are zero: not loaded
             fft_lines<false, LOG2L, true, false, true>(
                 buf, tws,
                 [&](int w, int pos) {
                     if (group + w >= lines) return zero;
                     const uint32_t n = vidx(w, pos);
-                    return make_float2(p.ir[n], p.ii[n]);
+                    float vr = p.ir[n], vi = p.ii[n];
+                    if (upd) {   // each v[n] is read and written by this thread only
+                        vr = fmaf(beta, vr, p.upd_r[n]);
+                        vi = fmaf(beta, vi, p.upd_i[n]);
+                        p.vw_r[n] = vr;
+                        p.vw_i[n] = vi;
+                    }
+                    return make_float2(vr, vi);
                 },
                 [&](auto& y) {
 #pragma unroll
@@ -368,12 +394,6 @@ __global__ void __launch_bounds__(kDotThreads) sum_partials_kernel(const double*
     if (threadIdx.x == 0) *out = s;
 }
 
-// step alpha = r.r / p.Ap (0 once r = 0 or p.Ap = 0)
-__device__ __forceinline__ float cg_ratio(const double* num, const double* den)
-{
-    const double a = *num, b = *den;
-    return (a > 0.0 && b != 0.0) ? float(a / b) : 0.0f;
-}
 
 __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y)
 {
@@ -436,32 +456,6 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
     }
     const double s = block_sum(v.value(), sm);
     if (threadIdx.x == 0) partial[blockIdx.x] = s;
-}
-
-// p = r + beta p, beta = new r.r / old r.r (VEC as cg_xr_kernel)
-template <bool VEC>
-__global__ void __launch_bounds__(256) cg_p_kernel(float* pr, float* pi, const float* rr_,
-                                                   const float* ri, int64_t n,
-                                                   const double* rr_new, const double* rr_old)
-{
-    pdl_launch_dependents();
-    pdl_wait();
-    const float beta = cg_ratio(rr_new, rr_old);
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    if constexpr (VEC) {
-        float4* const p4r = reinterpret_cast<float4*>(pr);
-        float4* const p4i = reinterpret_cast<float4*>(pi);
-        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < (n >> 2);
-             k += stride) {
-            p4r[k] = fma4(beta, p4r[k], reinterpret_cast<const float4*>(rr_)[k]);
-            p4i[k] = fma4(beta, p4i[k], reinterpret_cast<const float4*>(ri)[k]);
-        }
-    } else {
-        for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n; k += stride) {
-            pr[k] = fmaf(beta, pr[k], rr_[k]);
-            pi[k] = fmaf(beta, pi[k], ri[k]);
-        }
-    }
 }
 
 // r = b - r (r holds A x), p = r
@@ -611,11 +605,22 @@ int64_t toeplitz_dot_blocks(int nx, int ny, int nz)
 
 namespace {
 
+// upd_r != nullptr: v = (vw_r, vw_i) is first replaced by upd + beta v (the
+// CG direction update, see ToeplitzArgs)
 cudaError_t toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda, const float* ir,
                            const float* ii, float* outr, float* outi, int accumulate,
-                           float2* work, double* dot, const float2* tw, cudaStream_t s)
+                           float2* work, double* dot, const float2* tw, cudaStream_t s,
+                           const float* upd_r = nullptr, const float* upd_i = nullptr,
+                           const double* rr_new = nullptr, const double* rr_old = nullptr,
+                           float* vw_r = nullptr, float* vw_i = nullptr)
 {
     ToeplitzArgs p;
+    p.upd_r = upd_r;
+    p.upd_i = upd_i;
+    p.rr_new = rr_new;
+    p.rr_old = rr_old;
+    p.vw_r = vw_r;
+    p.vw_i = vw_i;
     p.ir = ir;
     p.ii = ii;
     p.outr = outr;
@@ -676,8 +681,14 @@ cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, cons
         e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks, rr);
     if (e != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
-        // Ap, with the per-CTA sums of p.Ap from its last stage
-        e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s);
+        // Ap, with the per-CTA sums of p.Ap from its last stage; from the
+        // second iteration on, its first stage also forms the new direction
+        // p = r + beta p, beta = rr[it] / rr[it - 1]
+        if (it == 0)
+            e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s);
+        else
+            e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s,
+                               r_r, r_i, rr + it, rr + it - 1, p_r, p_i);
         if (e == cudaSuccess)
             e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, int(apply_blocks),
                            pap);
@@ -688,9 +699,6 @@ cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, cons
         if (e == cudaSuccess)
             e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks,
                            rr + it + 1);
-        if (e == cudaSuccess)
-            e = launch_pdl(vec4 ? cg_p_kernel<true> : cg_p_kernel<false>, grid, 256, 0, s, p_r, p_i,
-                           r_r, r_i, N, rr + it + 1, rr + it);
         if (e != cudaSuccess) return e;
     }
     e = launch_pdl(sqrt_kernel, (iters + 1 + 255) / 256, 256, 0, s, rr, iters + 1);
