@@ -33,6 +33,22 @@ constexpr int kFftThreads = 256;
 
 inline bool fft_len_ok(int64_t L) { return L >= 1 && L <= kFftMaxLen && (L & (L - 1)) == 0; }
 
+// Programmatic dependent launch: kernels that run back to back on one
+// stream, each short (the FFT passes, the Toeplitz stages, the CG kernels),
+// are launched with the programmatic-serialisation attribute.  Each one lets
+// the next one launch as soon as all of its CTAs have started
+// (pdl_launch_dependents), and each one waits for the previous one to
+// finish, with its writes visible (pdl_wait), before it touches any buffer;
+// what comes before the wait (twiddle staging, index set-up) reads nothing
+// the previous kernel writes.  Launched without the attribute, both are
+// no-ops.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // lines per CTA: 16 (2^4), 8 at the largest length (shared memory)
 __host__ __device__ constexpr int fft_log2_lines(int log2L) { return log2L >= 10 ? 3 : 4; }
 
@@ -334,7 +350,9 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
         if (CONTIG) return (line << LOG2L) + j;
         return ((((line >> log2inner) << LOG2L) + j) << log2inner) + (line & inner_mask);
     };
+    pdl_launch_dependents();
     fft_stage_twiddles<LOG2L>(tws, tw);
+    pdl_wait();
     constexpr int RL = fft_last_log2r<LOG2L, true>();
     constexpr int last_per = fft_last_per<LOG2L, true>();
     fft_lines<INVERSE, LOG2L, true, !CONTIG, false>(

@@ -21,21 +21,10 @@ namespace mri {
 
 namespace {
 
-// Programmatic dependent launch: the kernels of a product and of a CG
-// iteration run back to back on one stream, each short.  Each one lets the
-// next one launch as soon as all of its CTAs have started
-// (pdl_launch_dependents), and each one waits for the previous one to finish,
-// with its writes visible (pdl_wait), before it touches any buffer; what
-// comes before the wait (the twiddle staging, index set-up) reads nothing
-// the previous kernel writes.  Launched without the attribute, both are
-// no-ops.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
+// Every kernel of a product and of a CG iteration is launched with
+// programmatic dependent launch (see pdl_wait in fft.cuh): each lets the next
+// one launch once its CTAs have started, and waits for the previous one
+// before it touches any buffer.
 template <class... KArgs, class... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
                        cudaStream_t s, Args... args)
