@@ -330,7 +330,7 @@ def peak_per_sm_clk(kind, rates, trig="fast"):
 # The sources a kernel's DRAM traffic depends on (its code and the host code
 # that plans its launch); a stored traffic figure is valid while they are
 # unchanged.
-_COMMON_SOURCES = ("ptx.cuh", "gather.cuh", "sincospi_coeffs.h", "launch.h", "mri_abi.cu")
+_COMMON_SOURCES = ("ptx.cuh", "gather.cuh", "sincospi_coeffs.h", "mri_abi.cu")
 TRAFFIC_SOURCES = {
     "grid_tc": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
                                   "gather_grid_tc_ws.cuh", "kernels_grid_tc.cu"),
@@ -435,9 +435,17 @@ def cpu_baseline(w: wl.Workload, target_s: float = 12.0):
     oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
     dt = time.perf_counter() - t0
     pairs = count * w.M
+    # the same oracle on one core, on a smaller sample (about 2 s)
+    count1 = int(min(max(32 * 2.0 / (dt / count * cores * 32), 16), count))
+    idx1 = wl.voxel_subset(w.N, count1, 11)
+    t0 = time.perf_counter()
+    oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx1, threads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": round(pairs / dt / 1e9, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{count} seeded voxels x all {w.M} samples of {w.name} "
-                      f"({pairs:.3g} pairs, {dt:.1f} s, fp64, OpenMP over voxels)"}
+                      f"({pairs:.3g} pairs, {dt:.1f} s, fp64, OpenMP over voxels)",
+            "one_core": {"value": round(count1 * w.M / dt1 / 1e9, 5), "unit": UNIT,
+                         "sample": f"{count1} seeded voxels x all {w.M} samples, {dt1:.1f} s"}}
 
 
 def e2e(torch, mri, dist, w, trig, steps, warmup, grid=False):
