@@ -336,6 +336,7 @@ TRAFFIC_SOURCES = {
                                   "gather_grid_tc_ws.cuh", "kernels_grid_tc.cu"),
     "grid_tc_fwd": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
                                       "gather_grid_tc_fwd.cuh", "kernels_grid_tc.cu"),
+    "toeplitz": ("fft.cuh", "kernels_toeplitz.cu"),
 }
 
 
@@ -522,7 +523,8 @@ def find_rho(torch, mri, dist, args, flush, peaks):
                      "unit": "Gvoxels/s",
                      "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                                   "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                                  "traffic": None,
+                                  "traffic": (profiled_traffic("toeplitz", "product", w.name)
+                                              if name == "toeplitz_apply" else None),
                                   "algorithmic_bytes_per_voxel": bpv,
                                   "compulsory_bytes_per_voxel":
                                       TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL}}

@@ -286,7 +286,7 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
  * r = 0 the iterate stops changing.  Scratch from the stream-ordered pool:
  * 4 nx*ny*nz complex values plus 6 nx*ny*nz floats.
  *
- * All three are asynchronous on `stream`.  MRI_ERR_SIZE for a grid edge that
+ * These calls are asynchronous on `stream`.  MRI_ERR_SIZE for a grid edge that
  * is not a power of two in 1 .. 512, a non-finite spacing or lambda, iters
  * outside 0 .. 2^20; MRI_ERR_ALIGN for K or rnorms not 8-byte aligned; the
  * other pointer checks as mri_fhd.

@@ -295,7 +295,12 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
             const uint32_t l = group + w;
             return ((((l >> log2inner) << LOG2L) + j) << log2inner) + (l & imask);
         };
-        auto load = [&](int w, int pos) { return group + w < lines ? p.work[gidx(w, pos)] : zero; };
+        // cache hints, measured: the strided stages' work loads in L2 only
+        // (__ldcg) and the once-read spectrum as streaming (__ldcs, evict
+        // first), CG iteration 0.168 -> 0.160 ms at 128^3
+        auto load = [&](int w, int pos) {
+            return group + w < lines ? __ldcg(p.work + gidx(w, pos)) : zero;
+        };
         // the lower half of every line to work
         auto store_half = [&](auto& y, auto rl, auto per_c) {
             constexpr int R_ = decltype(rl)::value, PER = decltype(per_c)::value;
@@ -311,13 +316,15 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
         if constexpr (STAGE == kZConv) {
             // the (real) spectrum at the positions of the forward transform's
             // last pass, loaded first so that it arrives during the transform
+            // (streaming: each value is read once per product)
             float kreg[IL][1 << RL];
 #pragma unroll
             for (int it = 0; it < IL; ++it) {
                 int w, j;
                 const bool on = fft_item<LOG2L, RL, true>(it, w, j) && group + w < lines;
 #pragma unroll
-                for (int q = 0; q < (1 << RL); ++q) kreg[it][q] = on ? p.K[gidx(w, j + q * per)] : 0.f;
+                for (int q = 0; q < (1 << RL); ++q)
+                    kreg[it][q] = on ? __ldcs(p.K + gidx(w, j + q * per)) : 0.f;
             }
             fft_lines<false, LOG2L, true, true, true>(buf, tws, load, [&](auto& y) {
 #pragma unroll
