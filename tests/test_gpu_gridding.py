@@ -7,7 +7,8 @@
   path's);
 - the benchmarked size (128^3, 3D radial trajectory) in full against the
   oracle (which is cheap here: an interpolation and numpy's FFT);
-- accumulate, M = 0, argument errors.
+- the longest FFT lines (1024), all samples at the origin (a constant
+  image), accumulate, M = 0, argument errors.
 
 Tolerance: the interpolation is exact arithmetic up to fp32 rounding of the
 weights and of the atomic sums on the grid (whose order is not fixed), then
@@ -59,6 +60,27 @@ def test_gridding_matches_oracle(mri, shape, M):
     ref = Gr.gridding_recon(*k, *v, shape).reshape(-1)
     assert oracle.rel_l2(cplx(r, i), ref) <= TOL
     assert mri.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1024), (2, 1024, 1), (1024, 2, 2)])
+def test_gridding_longest_lines(mri, shape):
+    """An axis of 1024 voxels (the longest FFT line)."""
+    k, v = samples(3000, sum(shape))
+    r, i = mri.gridding(*(dev(a) for a in k), *(dev(a) for a in v), shape)
+    ref = Gr.gridding_recon(*k, *v, shape).reshape(-1)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL
+
+
+def test_samples_at_the_origin_give_a_constant_image(mri):
+    """Every sample at k = 0: all weight on the grid point k_g = 0, and the
+    image is the constant sum of Mu."""
+    M = 777
+    _, v = samples(M, 77)
+    z = np.zeros(M, np.float32)
+    r, i = mri.gridding(dev(z), dev(z), dev(z), *(dev(a) for a in v), (4, 8, 16))
+    mu = Gr.mu(*v).sum()
+    img = cplx(r, i)
+    assert np.abs(img - mu).max() <= 1e-5 * abs(mu)
 
 
 def test_on_grid_samples_give_fhd(mri):
