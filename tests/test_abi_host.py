@@ -218,3 +218,61 @@ def test_forward_argument_checks(lib):
     bad = list(g[:8])
     bad[6] = P(0x100001)                                             # rRho misaligned
     assert f(*bad, 10, 10, g[8], g[9], 0, 0, None) == ALIGN
+
+
+F32 = ctypes.c_float
+INT = ctypes.c_int
+
+
+def test_find_rho_argument_checks_before_any_cuda_call(lib):
+    """mri_fft3, mri_toeplitz_kernel, mri_toeplitz_apply, mri_cg_solve: grid
+    edges powers of two (FFT lines up to 1024, Toeplitz grids up to 512),
+    modes, finite lambda and spacing, iteration bound, 8-byte alignment --
+    all decided on the host."""
+    g = fake()
+    fft = lib.mri_fft3
+    fft.argtypes = [P, INT, INT, INT, INT, P]
+    fft.restype = INT
+    assert fft(g[0], 6, 8, 8, 0, None) == SIZE
+    assert fft(g[0], 8, 8, 2048, 0, None) == SIZE
+    assert fft(g[0], 8, 8, 8, 2, None) == MODE
+    assert fft(P(0x100004), 8, 8, 8, 0, None) == ALIGN
+    ap = lib.mri_toeplitz_apply
+    ap.argtypes = [P, INT, INT, INT, F32, P, P, P, P, INT, P]
+    ap.restype = INT
+    for n in ((3, 4, 4), (4, 4, 1024), (0, 4, 4), (4, -2, 4)):
+        assert ap(g[0], *n, 0.0, *g[1:5], 0, None) == SIZE, n
+    assert ap(g[0], 4, 4, 4, float("nan"), *g[1:5], 0, None) == SIZE
+    assert ap(g[0], 4, 4, 4, 0.0, *g[1:5], 2, None) == MODE
+    assert ap(P(0x100004), 4, 4, 4, 0.0, *g[1:5], 0, None) == ALIGN
+    cg = lib.mri_cg_solve
+    cg.argtypes = [P, INT, INT, INT, F32, P, P, P, P, INT, P, P]
+    cg.restype = INT
+    assert cg(g[0], 4, 4, 4, 0.0, *g[1:5], -1, g[5], None) == SIZE
+    assert cg(g[0], 4, 4, 4, 0.0, *g[1:5], (1 << 20) + 1, g[5], None) == SIZE
+    assert cg(g[0], 4, 4, 5, 0.0, *g[1:5], 3, g[5], None) == SIZE
+    assert cg(g[0], 4, 4, 4, 0.0, *g[1:5], 3, P(0x100004), None) == ALIGN
+    tk = lib.mri_toeplitz_kernel
+    tk.argtypes = [P] * 5 + [I64, INT, INT, INT, F32, F32, F32, P, INT, P]
+    tk.restype = INT
+    assert tk(*g[:5], 10, 4, 4, 4, 1.0, float("inf"), 1.0, g[5], 0, None) == SIZE
+    assert tk(*g[:5], 10, 4, 4, 4, 1.0, 1.0, 1.0, g[5], 9, None) == MODE
+    assert tk(*g[:5], -1, 4, 4, 4, 1.0, 1.0, 1.0, g[5], 0, None) == SIZE
+    assert tk(*g[:5], 10, 4, 6, 4, 1.0, 1.0, 1.0, g[5], 0, None) == SIZE
+
+
+def test_gridding_argument_checks_before_any_cuda_call(lib):
+    g = fake()
+    f = lib.mri_gridding
+    f.argtypes = [P] * 7 + [I64, INT, INT, INT, P, P, INT, P]
+    f.restype = INT
+    for n in ((3, 4, 4), (4, 4, 2048), (0, 4, 4)):
+        assert f(*g[:7], 16, *n, g[7], g[8], 0, None) == SIZE, n
+    assert f(*g[:7], -1, 4, 4, 4, g[7], g[8], 0, None) == SIZE
+    assert f(*g[:7], 16, 4, 4, 4, g[7], g[8], 2, None) == MODE
+    for i in range(9):
+        bad = list(g[:9])
+        bad[i] = P(None)
+        assert f(*bad[:7], 16, 4, 4, 4, bad[7], bad[8], 0, None) == NULL, i
+        bad[i] = P(0x100001 + 256 * i)
+        assert f(*bad[:7], 16, 4, 4, 4, bad[7], bad[8], 0, None) == ALIGN, i
