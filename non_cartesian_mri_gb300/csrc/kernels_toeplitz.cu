@@ -12,7 +12,10 @@
 // round trip per iteration).
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
+#include <set>
 #include <type_traits>
+#include <utility>
 
 #include "fft.cuh"
 #include "launch.h"
@@ -497,6 +500,27 @@ cudaError_t launch_fft_twiddles(float2* tw, cudaStream_t s)
 
 namespace {
 
+// Kernels whose launch attributes have been set, per device (the attributes
+// are per device; a process may use several).
+std::mutex g_attr_mutex;
+std::set<std::pair<int, const void*>> g_attr_done;
+
+bool attributes_set(const void* kernel)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    return g_attr_done.count({dev, kernel}) != 0;
+}
+
+void mark_attributes_set(const void* kernel)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    g_attr_done.insert({dev, kernel});
+}
+
 // dynamic shared memory, then the launch, of one FFT kernel over `lines`
 // lines of length 2^log2L (the per-length kernels are picked by `pick`)
 template <class Pick>
@@ -504,14 +528,18 @@ cudaError_t launch_by_length(int log2L, int64_t lines, cudaStream_t s, Pick pick
 {
     auto go = [&](auto kernel, auto... args) -> cudaError_t {
         const size_t smem = fft_smem_total(log2L);
-        cudaError_t e =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        // all of the unified L1 / shared memory as shared memory, so that
+        // once per kernel and device: the dynamic shared memory, and all of
+        // the unified L1 / shared memory as shared memory, so that
         // fft_min_ctas tiles fit on an SM
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     int(cudaSharedmemCarveoutMaxShared));
-        if (e != cudaSuccess) return e;
+        if (!attributes_set(reinterpret_cast<const void*>(kernel))) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(smem));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         int(cudaSharedmemCarveoutMaxShared));
+            if (e != cudaSuccess) return e;
+            mark_attributes_set(reinterpret_cast<const void*>(kernel));
+        }
         const int64_t W = int64_t(1) << fft_log2_lines(log2L);
         return launch_pdl(kernel, unsigned((lines + W - 1) / W), kFftThreads, smem, s, args...);
     };
