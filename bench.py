@@ -538,7 +538,28 @@ def find_rho(torch, mri, dist, args, flush, peaks):
     out["toeplitz_kernel_ms_once"] = round(t0.elapsed_time(t1), 2)
     del t, K, v
     torch.cuda.empty_cache()
+    if dist.rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_toeplitz(w)
     return out
+
+
+def cpu_baseline_toeplitz(w):
+    """The oracle's Toeplitz product (oracle.toeplitz.fhf_fft: numpy FFTs of
+    the doubled grid, fp64), as it stands, once on the workload's grid.  Its
+    cost does not depend on the values, so a seeded Q grid of the right shape
+    stands in for the trajectory's (whose oracle evaluation would take hours)."""
+    from oracle import toeplitz as T
+    rng = np.random.default_rng(78)
+    L = w.L
+    Qc = rng.standard_normal((2 * L,) * 3) + 1j * rng.standard_normal((2 * L,) * 3)
+    rho = rng.standard_normal((L,) * 3) + 1j * rng.standard_normal((L,) * 3)
+    t0 = time.perf_counter()
+    T.fhf_fft(Qc, rho)
+    dt = time.perf_counter() - t0
+    return {"value": round(w.N / dt / 1e9, 5), "unit": "Gvoxels/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"one product on the {L}^3 grid ({2 * L}^3 numpy FFTs, fp64, one "
+                      f"thread), {dt:.1f} s"}
 
 
 # The gridding reconstruction: bytes per call for M samples on N voxels --
@@ -564,12 +585,22 @@ def gridding(torch, mri, dist, args, flush, peaks):
     achieved = nbytes / (ms * 1e-3) / 1e9
     del t
     torch.cuda.empty_cache()
-    return {"workload": f"{w.name}: M={w.M:,} samples onto a {w.L}^3 grid",
-            "ms": round(ms, 4), "value": round(w.M / (ms * 1e-3) / 1e9, 3),
-            "unit": "Gsamples/s",
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                         "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
-                         "algorithmic_bytes": nbytes}}
+    out = {"workload": f"{w.name}: M={w.M:,} samples onto a {w.L}^3 grid",
+           "ms": round(ms, 4), "value": round(w.M / (ms * 1e-3) / 1e9, 3),
+           "unit": "Gsamples/s",
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                        "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                        "algorithmic_bytes": nbytes}}
+    if dist.rank == 0 and not args.no_cpu:
+        from oracle import gridding as Gr
+        t0 = time.perf_counter()
+        Gr.gridding_recon(w.kx, w.ky, w.kz, w.rPhi, w.iPhi, w.rD, w.iD, shape)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": round(w.M / dt / 1e9, 5), "unit": "Gsamples/s",
+                               "cores": 1, "kind": "oracle",
+                               "sample": f"the whole reconstruction once (numpy, fp64, one "
+                                         f"thread), {dt:.1f} s"}
+    return out
 
 
 def run_ours(args):
