@@ -60,6 +60,8 @@ struct FwdParams {
     int nx;
     int ncb;                         // column blocks of 128
     const float2* yz_rows;           // (y, z) of every row, padded to whole blocks
+    const float* row_step;           // per group of 8 rows: the y step when the group's
+                                     // rows share z and are evenly spaced in y, else NaN
     int64_t row_blocks;
     int splits;                      // CTAs along the row blocks
     const unsigned char* rho_tab;    // chunks [row block][column block][chunk], kFwChunkBytes each

@@ -73,16 +73,33 @@ __global__ void __launch_bounds__(256) rho_bound_kernel(const float* rr, const f
     if ((threadIdx.x & 31) == 0 && b != 0u) atomicMax(bound, b);
 }
 
-// (y, z) of grid row r = iz * ny + iy, zero past the last row
+// (y, z) of grid row r = iz * ny + iy, zero past the last row; and per group
+// of 8 rows the y step d when the group's rows share z and y_i = y_0 + i d
+// exactly (checked in double; d exact in float), else NaN
 __global__ void __launch_bounds__(256) build_row_coords_kernel(const float* ys, int ny,
                                                                const float* zs, int64_t rows,
-                                                               int64_t padded, float2* yz)
+                                                               int64_t padded, float2* yz,
+                                                               float* step)
 {
     for (int64_t r = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; r < padded;
          r += int64_t(gridDim.x) * blockDim.x) {
         float2 v = make_float2(0.0f, 0.0f);
         if (r < rows) v = make_float2(ys[r % ny], zs[r / ny]);
         yz[r] = v;
+    }
+    for (int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; g < padded / 8;
+         g += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r0 = 8 * g;
+        float st = __int_as_float(0x7fc00000);   // NaN: rows one by one
+        if (r0 + 7 < rows && r0 / ny == (r0 + 7) / ny) {
+            const int64_t i0 = r0 % ny;
+            const double y0 = ys[i0];
+            const double d = double(ys[i0 + 1]) - y0;
+            bool even = double(float(d)) == d;
+            for (int i = 2; i < 8; ++i) even = even && double(ys[i0 + i]) == y0 + i * d;
+            if (even) st = float(d);
+        }
+        step[g] = st;
     }
 }
 
@@ -283,6 +300,8 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
             nkz = -p.kz[m] * p.kscale;
         }
         bool ok = true;
+        // the rotation of the last evenly spaced row group (NaN: none yet)
+        float rot_step = __int_as_float(0x7fc00000), rot_s = 0.0f, rot_c = 1.0f;
         for (int blk = 0; blk < nblk && ok; ++blk) {
             const int cb = blk / nb;
             const int b = blk - cb * nb;
@@ -331,16 +350,45 @@ __global__ void __launch_bounds__(kFwThreads, 1) forward_grid_tc_kernel(FwdParam
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&d_free[buf]);
-            // rows 32 h .. 32 h + 31 of block b_begin + b
-            const float2* yz = p.yz_rows + (b_begin + b) * kFwRows + 32 * h;
+            // rows 32 h .. 32 h + 31 of block b_begin + b, in groups of 8: a
+            // group of evenly spaced rows sharing z takes one sin/cos and
+            // seven rotations by e^{i 2 pi ky d} (rounding drift of at most
+            // seven complex products), any other group a sin/cos per row
+            const int64_t row0 = (b_begin + b) * kFwRows + 32 * h;
+            const float2* yz = p.yz_rows + row0;
+            const float* gst = p.row_step + row0 / 8;
             float bs_r = 0.0f, bs_i = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 c = yz[i];
-                float sn, cs;
-                table_sincos<TRIG>(fmaf(nkz, c.y, nky * c.x), sn, cs);
-                bs_r = fmaf(tr[i], cs, fmaf(-ti[i], sn, bs_r));
-                bs_i = fmaf(tr[i], sn, fmaf(ti[i], cs, bs_i));
+            for (int g = 0; g < 4; ++g) {
+                const float st = gst[g];
+                if (st == st) {
+                    if (st != rot_step) {
+                        table_sincos<TRIG>(nky * st, rot_s, rot_c);
+                        rot_step = st;
+                    }
+                    const float2 c = yz[8 * g];
+                    float sn, cs;
+                    table_sincos<TRIG>(fmaf(nkz, c.y, nky * c.x), sn, cs);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 8 * g + i;
+                        bs_r = fmaf(tr[r], cs, fmaf(-ti[r], sn, bs_r));
+                        bs_i = fmaf(tr[r], sn, fmaf(ti[r], cs, bs_i));
+                        const float nc = fmaf(cs, rot_c, -sn * rot_s);
+                        sn = fmaf(cs, rot_s, sn * rot_c);
+                        cs = nc;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 8 * g + i;
+                        const float2 c = yz[r];
+                        float sn, cs;
+                        table_sincos<TRIG>(fmaf(nkz, c.y, nky * c.x), sn, cs);
+                        bs_r = fmaf(tr[r], cs, fmaf(-ti[r], sn, bs_r));
+                        bs_i = fmaf(tr[r], sn, fmaf(ti[r], cs, bs_i));
+                    }
+                }
             }
             run_r += bs_r;
             run_i += bs_i;

@@ -137,14 +137,15 @@ cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cuda
 cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows, int nx,
                                      int64_t row_blocks, const float* ys, int ny, const float* zs,
                                      unsigned int* bound, unsigned char* tab, float2* yz_rows,
-                                     int grid, cudaStream_t s)
+                                     float* row_step, int grid, cudaStream_t s)
 {
     if (cudaMemsetAsync(bound, 0, sizeof(unsigned int), s) != cudaSuccess)
         return cudaErrorUnknown;
     rho_bound_kernel<<<grid, 256, 0, s>>>(rr, ri, rows * nx, bound);
     build_rho_tiles_kernel<<<grid, 256, 0, s>>>(rr, ri, rows, nx, grid_tc_col_blocks(nx),
                                                 row_blocks, bound, tab);
-    build_row_coords_kernel<<<grid, 256, 0, s>>>(ys, ny, zs, rows, row_blocks * kFwRows, yz_rows);
+    build_row_coords_kernel<<<grid, 256, 0, s>>>(ys, ny, zs, rows, row_blocks * kFwRows, yz_rows,
+                                                 row_step);
     return cudaGetLastError();
 }
 

@@ -45,7 +45,7 @@ cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int gri
 cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t rows, int nx,
                                      int64_t row_blocks, const float* ys, int ny, const float* zs,
                                      unsigned int* bound, unsigned char* tab, float2* yz_rows,
-                                     int grid, cudaStream_t s);
+                                     float* row_step, int grid, cudaStream_t s);
 cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cudaStream_t s);
 // weights of tensor-core grid records times the power of two from the bound word
 cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,

@@ -767,7 +767,7 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
                                      0.5 * ncb, 3.0);
     const int64_t tab_bytes =
         row_blocks * ncb * mri::kFwChunks * int64_t(mri::kFwChunkBytes);
-    const int64_t yz_bytes = row_blocks * mri::kFwRows * 8;
+    const int64_t yz_bytes = row_blocks * mri::kFwRows * 8 + row_blocks * (mri::kFwRows / 8) * 4;
     const int64_t part_bytes = splits > 1 ? int64_t(splits) * 2 * M * 4 : 0;
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
@@ -777,12 +777,13 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
         return cuda_fail();
     unsigned char* tab = reinterpret_cast<unsigned char*>(scratch);
     float2* yz_rows = reinterpret_cast<float2*>(scratch + align256(tab_bytes));
+    float* row_step = reinterpret_cast<float*>(yz_rows + row_blocks * mri::kFwRows);
     unsigned int* bound =
         reinterpret_cast<unsigned int*>(scratch + align256(tab_bytes) + align256(yz_bytes));
     float* part = reinterpret_cast<float*>(scratch + align256(tab_bytes) + align256(yz_bytes) +
                                            kBoundBytes);
     if (mri::launch_forward_grid_prep(rRho, iRho, rows, nx, row_blocks, ys, ny, zs, bound, tab,
-                                      yz_rows, grid_for(row_blocks * ncb * 2048, d->sms),
+                                      yz_rows, row_step, grid_for(row_blocks * ncb * 2048, d->sms),
                                       s) != cudaSuccess)
         st = cuda_fail();
     mri::FwdParams fp{};
@@ -795,6 +796,7 @@ mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz, c
     fp.nx = nx;
     fp.ncb = ncb;
     fp.yz_rows = yz_rows;
+    fp.row_step = row_step;
     fp.row_blocks = row_blocks;
     fp.splits = splits;
     fp.rho_tab = tab;
