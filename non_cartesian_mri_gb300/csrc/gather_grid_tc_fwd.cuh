@@ -26,6 +26,9 @@
 // multiplies by e^{-i2pi(ky y + kz z)} of each row and adds the block's
 // total to its running sums (blocked summation; the row factor distributes
 // over the column blocks); the two threads of a sample combine at the end.
+// The row factors go by groups of 8 rows: a group whose rows share z and are
+// evenly spaced in y (marked in the row table) takes one sin/cos and seven
+// rotations by e^{-i2pi ky d}, any other group a sin/cos per row.
 //
 // Warp roles, as in the F^H D kernel (gather_grid_tc_ws.cuh): D is double
 // buffered (tensor-memory columns 256-383 and 384-511), so the MMAs of row
