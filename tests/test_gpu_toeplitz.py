@@ -117,11 +117,18 @@ def test_toeplitz_apply_matches_fhf(mri, shape, spacing, lam, trig):
                                            ((4, 2, 1), (1.0, 1.0, 1.0)),
                                            ((1, 1, 512), (1.0, 1.0, 1.0)),
                                            ((2, 512, 1), (1.0, 0.25, 1.0)),
-                                           ((16, 32, 64), (1.0, 1.0, 1.0))])
+                                           ((16, 32, 64), (1.0, 1.0, 1.0)),
+                                           ((512, 1, 1), (1.0, 1.0, 1.0)),
+                                           ((256, 2, 2), (1.0, 1.0, 0.5)),
+                                           ((64, 4, 2), (1.0, 1.0, 1.0)),
+                                           ((32, 2, 16), (0.5, 1.0, 1.0))])
 def test_toeplitz_apply_shapes(mri, shape, spacing):
     """Narrow x (a CTA's 16 strided lines span several outer slabs), one-voxel
-    axes, the longest line (2 n = 1024), and a grid of 32768 voxels checked
-    through the oracle's FFT route (fhf_fft, pinned to the definition)."""
+    axes, the longest lines (2 n = 1024) on every axis including z (whose
+    stage keeps a forward transform's registers for the inverse one: the
+    512- and 1024-long plans with an odd radix), and a grid of 32768 voxels,
+    checked through the oracle's FFT route (fhf_fft, pinned to the
+    definition)."""
     k, rPhi, iPhi = samples(600, 40 + shape[2])
     K = mri.toeplitz_kernel(dev(k[0]), dev(k[1]), dev(k[2]), dev(rPhi), dev(iPhi), shape,
                             spacing, trig="accurate")
