@@ -184,3 +184,32 @@ def test_forward_grid_fallback_and_empty(mri):
     e = torch.empty(0, device="cuda")
     rz, iz = mri.forward_grid(*k, e, dev(ys), dev(zs), e, e)      # nx = 0: no voxels
     assert torch.count_nonzero(rz) == 0 and torch.count_nonzero(iz) == 0
+
+
+@pytest.mark.parametrize("trig", ["accurate", "fast"])
+@pytest.mark.parametrize("ys_kind,ny,nz", [("even", 12, 5), ("even", 16, 3), ("mixed", 24, 2),
+                                          ("even", 1, 9)])
+def test_forward_grid_evenly_spaced_rows(mri, trig, ys_kind, ny, nz):
+    """Row factors by rotation: evenly spaced y (step 0.75, offset), groups of
+    8 rows that straddle two z planes (ny = 12), a y axis that is even only
+    in places (mixed), and ny = 1 (every group straddles planes)."""
+    M = 1500
+    w = wl.make_workload("fhd_128_radial")
+    xs = (np.arange(128) - 64).astype(np.float32)
+    if ys_kind == "even":
+        ys = (np.arange(ny) * 0.75 - 3.0).astype(np.float32)
+    else:
+        ys = np.concatenate([np.arange(8) * 0.5, 10.0 + np.array([0.0, 0.3, 1.1, 1.2, 2.0, 2.5,
+                                                                   4.0, 4.25]),
+                             30.0 + np.arange(8) * 1.5]).astype(np.float32)
+    zs = (np.arange(nz) * 2.0 - 5.0).astype(np.float32)
+    rng = np.random.default_rng(ny * 100 + nz)
+    n = 128 * ny * nz
+    rho = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
+    k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
+    r, i = mri.forward_grid(*k, dev(xs), dev(ys), dev(zs), dev(rho.real), dev(rho.imag),
+                            trig=trig)
+    x, y, z = expand(xs, ys, zs)
+    ref = oracle.forward(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, rho)
+    assert oracle.rel_l2(cplx(r, i), ref) <= TOL[trig]
+    assert mri.device_errors(clear=True) == 0
