@@ -9,7 +9,8 @@
 // modulo n.  The centring of both grids is folded into signs:
 // e^{i 2 pi k_g x} = e^{i 2 pi g i / n} (-1)^g (-1)^i (-1)^{n/2}, so the
 // scatter adds Mu w (-1)^g, the library's inverse FFT (fft.cuh, unscaled)
-// does the sum, and the last kernel multiplies by (-1)^i (-1)^{n/2}.
+// does the sum, and its last axis multiplies by (-1)^i (-1)^{n/2} as it
+// writes the output.
 #include <algorithm>
 #include <cstdint>
 
@@ -59,7 +60,98 @@ __global__ void __launch_bounds__(256) grid_scatter_kernel(
     }
 }
 
-// out = c (-1)^(ix + iy + iz) G (+ out), c = (-1)^(nx/2 + ny/2 + nz/2)
+// The last non-trivial axis of the inverse FFT with the output folded in:
+// each transformed value goes straight to out (SoA) times the centring sign
+// c (-1)^(ix + iy + iz), c = (-1)^(nx/2 + ny/2 + nz/2), instead of a separate
+// pass over the grid.  Lines as fft_axis_kernel's (element j of line (o, i)
+// at (o L + j) inner + i, which is also the voxel index).
+template <int LOG2L, bool CONTIG>
+__global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
+    grid_last_axis_kernel(const float2* a, int log2inner, int64_t lines, const float2* tw,
+                          int log2nx, int log2ny, int c, float* outr, float* outi,
+                          int accumulate)
+{
+    extern __shared__ float2 fft_sm[];
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    float2* const buf = fft_sm;
+    float2* const tws = fft_sm + (fft_line_stride(LOG2L) << log2W);
+    const int64_t group = int64_t(blockIdx.x) << log2W;
+    const int64_t inner_mask = (int64_t(1) << log2inner) - 1;
+    auto gidx = [&](int w, int j) -> int64_t {
+        const int64_t line = group + w;
+        if (CONTIG) return (line << LOG2L) + j;
+        return ((((line >> log2inner) << LOG2L) + j) << log2inner) + (line & inner_mask);
+    };
+    pdl_launch_dependents();
+    fft_stage_twiddles<LOG2L>(tws, tw);
+    pdl_wait();
+    constexpr int RL = fft_last_log2r<LOG2L, true>();
+    constexpr int last_per = fft_last_per<LOG2L, true>();
+    const int64_t xmask = (int64_t(1) << log2nx) - 1, ymask = (int64_t(1) << log2ny) - 1;
+    fft_lines<true, LOG2L, true, !CONTIG, false>(
+        buf, tws,
+        [&](int w, int pos) { return group + w < lines ? a[gidx(w, pos)] : make_float2(0.f, 0.f); },
+        [&](auto& y) {
+#pragma unroll
+            for (int it = 0; it < fft_items(LOG2L, RL); ++it) {
+                int w, j;
+                if (!fft_item<LOG2L, RL, !CONTIG>(it, w, j) || group + w >= lines) continue;
+#pragma unroll
+                for (int q = 0; q < (1 << RL); ++q) {
+                    const int64_t n = gidx(w, j + q * last_per);
+                    const int64_t par = (n & xmask) + ((n >> log2nx) & ymask) + (n >> (log2nx + log2ny));
+                    float2 v = y[it][q];
+                    if ((par + c) & 1) v = make_float2(-v.x, -v.y);
+                    if (accumulate) {
+                        v.x += outr[n];
+                        v.y += outi[n];
+                    }
+                    outr[n] = v.x;
+                    outi[n] = v.y;
+                }
+            }
+        });
+}
+
+int log2_of(int n)
+{
+    int b = 0;
+    while ((1 << b) < n) ++b;
+    return b;
+}
+
+template <bool CONTIG>
+cudaError_t launch_last_axis(const float2* G, int log2L, int log2inner, int64_t lines,
+                             const float2* tw, int log2nx, int log2ny, int c, float* outr,
+                             float* outi, int accumulate, cudaStream_t s)
+{
+    auto go = [&](auto kernel) -> cudaError_t {
+        const size_t smem = fft_smem_total(log2L);
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        const int64_t W = int64_t(1) << fft_log2_lines(log2L);
+        kernel<<<unsigned((lines + W - 1) / W), kFftThreads, smem, s>>>(
+            G, log2inner, lines, tw, log2nx, log2ny, c, outr, outi, accumulate);
+        return cudaGetLastError();
+    };
+    switch (log2L) {
+        case 1: return go(grid_last_axis_kernel<1, CONTIG>);
+        case 2: return go(grid_last_axis_kernel<2, CONTIG>);
+        case 3: return go(grid_last_axis_kernel<3, CONTIG>);
+        case 4: return go(grid_last_axis_kernel<4, CONTIG>);
+        case 5: return go(grid_last_axis_kernel<5, CONTIG>);
+        case 6: return go(grid_last_axis_kernel<6, CONTIG>);
+        case 7: return go(grid_last_axis_kernel<7, CONTIG>);
+        case 8: return go(grid_last_axis_kernel<8, CONTIG>);
+        case 9: return go(grid_last_axis_kernel<9, CONTIG>);
+        case 10: return go(grid_last_axis_kernel<10, CONTIG>);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// out = c (-1)^(ix + iy + iz) G (+ out), c = (-1)^(nx/2 + ny/2 + nz/2): the
+// signs alone, for a 1 x 1 x 1 grid (no FFT axis to fold them into)
 __global__ void __launch_bounds__(256) grid_unshift_kernel(const float2* G, int nx, int ny, int nz,
                                                            float* outr, float* outi,
                                                            int accumulate)
@@ -98,10 +190,24 @@ cudaError_t launch_gridding(const float* kx, const float* ky, const float* kz, c
                                                               nx, ny, nz, G);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if ((e = launch_fft3(G, nx, ny, nz, true, tw, s)) != cudaSuccess) return e;
-    const int64_t blocks = std::min<int64_t>((N + 255) / 256, int64_t(sms) * 16);
-    grid_unshift_kernel<<<unsigned(blocks), 256, 0, s>>>(G, nx, ny, nz, outr, outi, accumulate);
-    return cudaGetLastError();
+    // the inverse FFT, its last non-trivial axis writing the output
+    const int n[3] = {nx, ny, nz};
+    int last = 2;
+    while (last >= 0 && n[last] == 1) --last;
+    if (last < 0) {
+        grid_unshift_kernel<<<1, 256, 0, s>>>(G, nx, ny, nz, outr, outi, accumulate);
+        return cudaGetLastError();
+    }
+    for (int ax = 0; ax < last; ++ax)
+        if ((e = launch_fft_axis(G, nx, ny, nz, ax, true, tw, s)) != cudaSuccess) return e;
+    const int log2nx = log2_of(nx), log2ny = log2_of(ny);
+    const int log2inner = last == 0 ? 0 : (last == 1 ? log2nx : log2nx + log2ny);
+    const int log2L = log2_of(n[last]);
+    const int c = ((nx >> 1) + (ny >> 1) + (nz >> 1)) & 1;
+    return last == 0 ? launch_last_axis<true>(G, log2L, 0, N >> log2L, tw, log2nx, log2ny, c,
+                                              outr, outi, accumulate, s)
+                     : launch_last_axis<false>(G, log2L, log2inner, N >> log2L, tw, log2nx,
+                                               log2ny, c, outr, outi, accumulate, s);
 }
 
 }  // namespace mri

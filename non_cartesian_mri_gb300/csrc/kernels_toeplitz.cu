@@ -580,22 +580,27 @@ cudaError_t toeplitz_stage(const ToeplitzArgs& p, int log2L, int64_t lines, cons
 
 }  // namespace
 
+cudaError_t launch_fft_axis(float2* a, int Lx, int Ly, int Lz, int axis, bool inverse,
+                            const float2* tw, cudaStream_t s)
+{
+    if (!fft_len_ok(Lx) || !fft_len_ok(Ly) || !fft_len_ok(Lz) || axis < 0 || axis > 2)
+        return cudaErrorInvalidValue;
+    const int len[3] = {Lx, Ly, Lz};
+    const int log2L = log2i(len[axis]);
+    if (log2L == 0) return cudaSuccess;
+    int log2inner = 0;
+    for (int ax = 0; ax < axis; ++ax) log2inner += log2i(len[ax]);
+    const int64_t lines = (int64_t(Lx) * Ly * Lz) >> log2L;
+    return inverse ? fft_axis<true>(a, log2L, log2inner, lines, tw, s)
+                   : fft_axis<false>(a, log2L, log2inner, lines, tw, s);
+}
+
 cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const float2* tw,
                         cudaStream_t s)
 {
-    if (!fft_len_ok(Lx) || !fft_len_ok(Ly) || !fft_len_ok(Lz)) return cudaErrorInvalidValue;
-    const int64_t total = int64_t(Lx) * Ly * Lz;
-    const int len[3] = {Lx, Ly, Lz};
-    int log2inner = 0;
     for (int ax = 0; ax < 3; ++ax) {
-        const int log2L = log2i(len[ax]);
-        if (log2L > 0) {
-            const int64_t lines = total >> log2L;
-            const cudaError_t e = inverse ? fft_axis<true>(a, log2L, log2inner, lines, tw, s)
-                                          : fft_axis<false>(a, log2L, log2inner, lines, tw, s);
-            if (e != cudaSuccess) return e;
-        }
-        log2inner += log2L;
+        const cudaError_t e = launch_fft_axis(a, Lx, Ly, Lz, ax, inverse, tw, s);
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -72,6 +72,9 @@ cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs
 cudaError_t launch_fft_twiddles(float2* tw, cudaStream_t s);
 cudaError_t launch_fft3(float2* a, int Lx, int Ly, int Lz, bool inverse, const float2* tw,
                         cudaStream_t s);
+// one axis (0 = x, 1 = y, 2 = z) of that 3-D FFT; nothing for a length of 1
+cudaError_t launch_fft_axis(float2* a, int Lx, int Ly, int Lz, int axis, bool inverse,
+                            const float2* tw, cudaStream_t s);
 cudaError_t launch_diff_axes(int nx, int ny, int nz, float hx, float hy, float hz, float* axes,
                              cudaStream_t s);
 // Q (SoA, doubled grid) into the complex array whose spectrum is K, the
