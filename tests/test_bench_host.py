@@ -1,0 +1,51 @@
+"""Host logic of bench.py, no GPU: the stored DRAM traffic records are used
+only while the sources they were measured on are unchanged, and the byte
+accounting of the find-rho and gridding rooflines adds up as documented."""
+
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_traffic_records_follow_their_sources(tmp_path, monkeypatch):
+    rec = {"grid_tc:w:fast": {"source_hash": bench.gather_source_hash("grid_tc"),
+                              "dram_bytes_per_launch": 123},
+           "toeplitz:w:product": {"source_hash": "0" * 16, "dram_bytes_per_launch": 456}}
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    # the hashes come from the repository's sources, the records from the
+    # temporary copy
+    hashes = {k: bench.gather_source_hash(k) for k in ("grid_tc", "toeplitz")}
+    monkeypatch.setattr(bench, "gather_source_hash", lambda kind="grid_tc": hashes[kind])
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("grid_tc", "fast", "w") == 123
+    assert bench.profiled_traffic("toeplitz", "product", "w") is None   # stale hash
+    assert bench.profiled_traffic("grid_tc", "accurate", "w") is None   # no record
+
+
+def test_committed_traffic_records_are_current():
+    """Every record in profiles/traffic.json matches the current sources (a
+    record left stale would make the bench report no traffic)."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+        rec = json.load(fh)
+    for key, entry in rec.items():
+        if key.startswith("_"):
+            continue
+        kind = key.split(":")[0]
+        assert entry["source_hash"] == bench.gather_source_hash(kind), key
+
+
+def test_find_rho_and_gridding_byte_accounting():
+    # five stages: x forward 8 + 16, y forward 16 + 32, z 32 + 32 + 32,
+    # y inverse 32 + 16, x inverse 16 + 8 + 8
+    assert bench.TOEPLITZ_BYTES_PER_VOXEL == 248
+    assert bench.TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL == 48
+    assert bench.CG_EXTRA_BYTES_PER_VOXEL == 64
+    assert bench.GRIDDING_BYTES_PER_SAMPLE == 28
+    assert bench.GRIDDING_BYTES_PER_VOXEL == 72
