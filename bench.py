@@ -63,13 +63,18 @@ ALGO_OPS = {
     "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
 # The accurate paths evaluate sin and cos in software (the MUFU's ~2^-21
-# absolute error is too coarse): the exact reduction to a quarter turn (3
-# FADD), f^2, the odd and even polynomials (3 + 4 FFMA) and f * P: 12 FP32
-# operations per sin/cos pair (the quadrant selects and sign flips run on the
-# ALU pipe).  The accurate paths are reported against the same roofline as
-# the fast ones (their software trig is overhead there), and also against
-# the FP32 pipe with that trig work counted ("frac_fp32_with_trig").
-TRIG_FP32_OPS = 12.0
+# absolute error is too coarse): the exact reduction to a half turn (3 FADD),
+# f^2, the odd and even polynomials (4 + 4 FFMA) and f * P: 13 FP32-pipe
+# operations per sin/cos pair (the sign flip by the half turn's parity runs
+# on the integer pipe).  A path that evaluates all its trig that way is bound
+# by the FP32 pipe with those operations counted: that is its roofline
+# ("frac"); its fraction of the SFU roofline of the fast path is reported
+# beside it ("frac_vs_sfu_roofline").  A fast path whose kernel gives a share
+# of its voxels the polynomial (mri_plan.fast_fp32_voxels) is charged that
+# share on the FP32 pipe (plus the multiply turning radians into half turns)
+# and the rest on the SFU.
+TRIG_FP32_OPS = 13.0
+TRIG_FP32_OPS_FROM_RADIANS = TRIG_FP32_OPS + 1.0
 # The tensor-core grid kernels: one complex multiply-accumulate is
 # 8 real flops per pair; each fp32-accurate product takes three f16 MMA
 # passes (hi*hi + hi*lo + lo*hi), so its peak is the dense f16 peak / 3, and
@@ -77,9 +82,10 @@ TRIG_FP32_OPS = 12.0
 TC_FLOPS_PER_PAIR = 8.0
 TC_PASSES = 3.0
 F16_PER_BF16 = 1.0
-# Per-SM-per-clock issue rates of sm_103a: FP32 FFMA 128 lanes; MUFU sin/cos
-# measured at 32 by the mri_microbench probe (reported live below).
-NOMINAL = {"mufu": 32.0, "fp32": 128.0}
+# Per-SM-per-clock rates of sm_103a, measured live by the mri_microbench
+# probes (one CTA of 1024 threads per SM): FP32 128 lanes (scalar FFMA, and
+# FFMA2, whose packed pairs hold the pipe for two cycles), MUFU sin / cos 16.
+NOMINAL = {"mufu": 16.0, "fp32": 128.0}
 
 
 def parse_args():
@@ -295,26 +301,31 @@ def timed_steps(torch, mri, dist, fn, steps, warmup, flush):
 
 def unit_rates(mri):
     r = {}
-    for probe in ("sin", "cos", "ffma"):
+    for probe in ("sin", "cos", "ffma", "ffma2"):
         mri.microbench(probe, ctas_per_sm=1, threads=1024, iters=1 << 10)
         r[probe] = round(mri.microbench(probe, ctas_per_sm=1, threads=1024,
                                         iters=1 << 13)["per_sm_per_clk"], 2)
     return r
 
 
-def algo_ops(kind, trig="fast"):
-    """Operations per work unit; with trig = "accurate_fp32" the sin/cos pairs
-    move from the MUFU to the FP32 pipe as software trig."""
+def algo_ops(kind, trig="fast", fp32_share=0.0):
+    """Operations per work unit.  trig = "accurate" (or "accurate_fp32"): every
+    sin/cos pair is software trig on the FP32 pipe; a fast path with
+    fp32_share > 0 moves that share of its sin/cos pairs there."""
     ops = dict(ALGO_OPS[kind])
-    if trig == "accurate_fp32" and ops["mufu"]:
-        ops["fp32"] += TRIG_FP32_OPS * ops["mufu"] / 2.0
+    pairs = ops["mufu"] / 2.0                  # sin/cos pairs per work unit
+    if trig in ("accurate", "accurate_fp32") and pairs:
+        ops["fp32"] += TRIG_FP32_OPS * pairs
         ops["mufu"] = 0.0
+    elif trig == "fast" and fp32_share > 0 and pairs:
+        ops["fp32"] += TRIG_FP32_OPS_FROM_RADIANS * pairs * fp32_share
+        ops["mufu"] *= 1.0 - fp32_share
     return ops
 
 
-def peak_per_sm_clk(kind, rates, trig="fast"):
+def peak_per_sm_clk(kind, rates, trig="fast", fp32_share=0.0):
     """Binding roofline in work units per SM per clock: min over the two units."""
-    ops = algo_ops(kind, trig)
+    ops = algo_ops(kind, trig, fp32_share)
     mufu = NOMINAL["mufu"] if rates is None else min(rates["sin"], rates["cos"])
     fp32 = NOMINAL["fp32"] if rates is None else rates["ffma"]
     # nominal integers when the probe agrees within 10%
@@ -337,6 +348,7 @@ TRAFFIC_SOURCES = {
     "grid_tc_fwd": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
                                       "gather_grid_tc_fwd.cuh", "kernels_grid_tc.cu"),
     "toeplitz": ("fft.cuh", "kernels_toeplitz.cu"),
+    "gridding": ("fft.cuh", "kernels_gridding.cu"),
 }
 
 
@@ -397,12 +409,20 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
     launches_per_step = res["gather_launches"] / len(res["step_ms"])
     achieved = units / launches_per_step / per_launch / 1e9
-    per_clk, unit, mufu, fp32 = peak_per_sm_clk(akind, rates, trig)
+    share = 0.0
+    if trig == "fast" and not grid and plan and plan.get("voxels_per_thread"):
+        share = plan.get("fast_fp32_voxels", 0) / plan["voxels_per_thread"]
+    per_clk, unit, mufu, fp32 = peak_per_sm_clk(akind, rates, trig, share)
     peak = per_clk * sms * sm_max_mhz * 1e6 / 1e9
-    ops = algo_ops(akind, trig)
+    ops = algo_ops(akind, trig, share)
     basis = (f"{sms} SMs x {sm_max_mhz:.0f} MHz x min(MUFU {mufu:g}/{ops['mufu']:g}, "
              f"FP32 {fp32:g}/{ops['fp32']:g}) per SM-clock") if ops["mufu"] else (
              f"{sms} SMs x {sm_max_mhz:.0f} MHz x FP32 {fp32:g}/{ops['fp32']:g} per SM-clock")
+    if share:
+        basis += (f"; {share:.3g} of the voxels take the polynomial on the FP32 pipe "
+                  f"({TRIG_FP32_OPS_FROM_RADIANS:g} ops per sin/cos pair)")
+    if trig == "accurate" and ALGO_OPS[akind]["mufu"]:
+        basis += f" ({TRIG_FP32_OPS:g} FP32 ops per software sin/cos pair counted)"
     out = {"bound": "alu", "binding_unit": unit, "achieved": round(achieved, 2),
            "peak": round(peak, 2),
            "unit": "G" + ops["unit"] + "s/s",
@@ -413,12 +433,10 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
     if sm_mhz:
         out["frac_at_sampled_clock"] = round(achieved / (per_clk * sms * sm_mhz * 1e-3), 4)
         out["units_per_sm_clk"] = round(achieved * 1e9 / (sms * sm_mhz * 1e6), 3)
-    if trig == "accurate" and ops["mufu"]:
-        fper, _, _, _ = peak_per_sm_clk(akind, rates, "accurate_fp32")
-        fops = algo_ops(akind, "accurate_fp32")
-        out["frac_fp32_with_trig"] = round(achieved / (fper * sms * sm_max_mhz * 1e-3), 4)
-        out["fp32_with_trig_basis"] = (f"FP32 {fp32:g}/{fops['fp32']:g} per SM-clock "
-                                       f"({TRIG_FP32_OPS:g} FP32 ops per software sin/cos pair)")
+    if ALGO_OPS[akind]["mufu"] and (trig == "accurate" or share):
+        # the fast path's roofline with every sin/cos on the SFU, for comparison
+        sper, _, _, _ = peak_per_sm_clk(akind, rates, "fast", 0.0)
+        out["frac_vs_sfu_roofline"] = round(achieved / (sper * sms * sm_max_mhz * 1e-3), 4)
     return out
 
 
@@ -523,8 +541,10 @@ def find_rho(torch, mri, dist, args, flush, peaks):
                      "unit": "Gvoxels/s",
                      "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                                   "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                                  "traffic": (profiled_traffic("toeplitz", "product", w.name)
-                                              if name == "toeplitz_apply" else None),
+                                  "traffic": profiled_traffic(
+                                      "toeplitz",
+                                      "product" if name == "toeplitz_apply" else "cg_iteration",
+                                      w.name),
                                   "algorithmic_bytes_per_voxel": bpv,
                                   "compulsory_bytes_per_voxel":
                                       TOEPLITZ_COMPULSORY_BYTES_PER_VOXEL}}
@@ -589,7 +609,8 @@ def gridding(torch, mri, dist, args, flush, peaks):
            "ms": round(ms, 4), "value": round(w.M / (ms * 1e-3) / 1e9, 3),
            "unit": "Gsamples/s",
            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                        "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                        "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                        "traffic": profiled_traffic("gridding", "call", w.name),
                         "algorithmic_bytes": nbytes}}
     if dist.rank == 0 and not args.no_cpu:
         from oracle import gridding as Gr
@@ -695,11 +716,20 @@ def run_ours(args):
         paths = {}
         for name, wname, trig, pgrid in (
                 ("fhd_grid_accurate", HEADLINE, "accurate", True),
+                ("fhd_grid_fast_rr", HEADLINE, "fast_rr", True),
                 ("fhd_general_fast", HEADLINE, "fast", False),
+                ("fhd_general_fast_rr", HEADLINE, "fast_rr", False),
                 ("fhd_general_accurate", HEADLINE, "accurate", False),
+                ("fhd_64_grid_fast", "fhd_64", "fast", True),
+                ("fhd_64_grid_accurate", "fhd_64", "accurate", True),
+                ("fhd_64_general_fast", "fhd_64", "fast", False),
+                ("fhd_64_general_accurate", "fhd_64", "accurate", False),
+                ("fhd_tiny_grid_fast", "fhd_tiny", "fast", True),
+                ("fhd_tiny_general_fast", "fhd_tiny", "fast", False),
                 ("q_grid_fast", "q_128", "fast", True),
                 ("q_grid_accurate", "q_128", "accurate", True),
                 ("q_general_fast", "q_128", "fast", False),
+                ("q_general_accurate", "q_128", "accurate", False),
                 ("fhd_batched_grid_fast", "fhd_batched_128", "fast", True),
                 ("fhd_batched_grid_accurate", "fhd_batched_128", "accurate", True),
                 ("fhd_batched_fast", "fhd_batched_128", "fast", False),
@@ -708,8 +738,8 @@ def run_ours(args):
                 ("forward_grid_accurate", HEADLINE, "accurate", True),
                 ("forward_general_fast", HEADLINE, "fast", False),
                 ("forward_general_accurate", HEADLINE, "accurate", False)):
-            if name.startswith("fhd_") and (name.startswith("fhd_grid") == grid) and \
-                    trig == args.trig and not name.startswith("fhd_batched"):
+            if wname == HEADLINE and name.startswith("fhd_") and \
+                    (name.startswith("fhd_grid") == grid) and trig == args.trig:
                 continue                     # the headline itself
             pw = wl.make_workload(wname)
             pt = to_dev(pw, torch)
@@ -728,7 +758,15 @@ def run_ours(args):
                                              pt["y"], pt["z"], rho[0], rho[1], trig=trig)
             else:
                 fn = lambda: call(mri, pw.kind, pt, trig, po, pgrid)  # noqa: E731
-            pres = timed_steps(torch, mri, dist, fn, args.steps, args.warmup, flush)
+            # slow paths (the general kernels on the largest workloads take up
+            # to seconds per call) time fewer steps, at least 3, about 4 s
+            flush()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            one = time.perf_counter() - t0
+            psteps = max(3, min(args.steps, int(4.0 / max(one, 1e-6))))
+            pres = timed_steps(torch, mri, dist, fn, psteps, max(args.warmup - 1, 2), flush)
             pm = statistics.mean(pres["step_ms"]) / 1e3
             punits = pw.pairs * (pw.B if pw.kind == "fhd_batched" else 1)
             if fwd and pgrid:
@@ -749,7 +787,8 @@ def run_ours(args):
                 "ms_per_step": round(pm * 1e3, 3),
                 "roofline": roofline(pw.kind, pw, pres, rates, sms, sm_max_mhz,
                                      clocks.get("sm_mhz"), trig, pgrid, pplan, peaks),
-                "gpu_launches": pplan["launches"] * args.steps,
+                "gpu_launches": pplan["launches"] * psteps,
+                "steps": psteps,
             }
             if fwd:
                 # the forward kernels have their own traffic records

@@ -161,8 +161,8 @@ mri_status mri_forward(const float* kx, const float* ky, const float* kz,
  *     the GPU (different streams, or different host threads) race and must be
  *     serialised by the caller.  Each call rewrites every byte of the array it
  *     reads, so nothing in it needs to start at zero.
- *   - M is limited by the records: ceil(M/256) * 5120 bytes must fit in the
- *     array (M <= 1,677,568 for 32 MiB), else MRI_ERR_SIZE.  The sample
+ *   - M is limited by the records: ceil(M/256) * 12288 bytes must fit in the
+ *     array (M <= 698,880 for 32 MiB), else MRI_ERR_SIZE.  The sample
  *     splits are capped to the partial sums that fit after the records (for
  *     a 128^3 grid none do, and the call runs unsplit).
  */
@@ -351,6 +351,13 @@ typedef struct mri_plan {
     int launches;             /* kernel launches one call makes */
     int64_t scratch_bytes;    /* pool memory one call takes */
     int tensor_cores;         /* 1: the gather runs on the tcgen05 tensor cores */
+    int grid_fold;            /* grid calls with 8 <= nx <= 64: grid rows whose columns share
+                                 one block of 128 when the y axis is evenly spaced within
+                                 groups of that many rows (checked on the device; voxel_ctas
+                                 counts the folded blocks), else 1 */
+    int fast_fp32_voxels;     /* general gather, fast trig: of voxels_per_thread, how many
+                                 take sin/cos from the polynomial on the FMA pipe instead of
+                                 the SFU (both units then share the trig work) */
 } mri_plan;
 
 mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,

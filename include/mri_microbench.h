@@ -13,11 +13,17 @@
  * memory, so exactly ctas_per_sm CTAs share every SM.  Each thread runs `iters` iterations of 8
  * independent dependency chains of the probed instruction:
  *   which = 0: __sinf (MUFU sine),   which = 1: __cosf (MUFU cosine),
- *   which = 2: fmaf (FFMA),          which = 3: exp2f (MUFU base-2 exponential).
+ *   which = 2: fmaf (FFMA),          which = 3: exp2f (MUFU base-2 exponential),
+ *   which = 4: fma.rn.f32x2 (packed FFMA2 on pairs of floats; four chains of
+ *              pairs, so again 8 results per iteration).
  * Each CTA writes its elapsed SM clock cycles (clock64) to cycles[cta] and a
  * value derived from its chains to sink[cta * threads + thread] (so the work
  * is not removed).  Rate per SM per clock =
- *   ctas_per_sm * threads * iters * 8 / cycles.
+ *   ctas_per_sm * threads * iters * 8 / cycles,
+ * which holds for ctas_per_sm = 1: CTAs that share an SM need not start and
+ * finish together, so their own elapsed cycles understate the SM's busy time
+ * and the formula then overstates the rate (measured: up to 1.5x with four
+ * CTAs of 256 threads).  Use one CTA of 1024 threads per SM for rates.
  * cycles: device array of (num_sms * ctas_per_sm) uint64; sink: device array
  * of (num_sms * ctas_per_sm * threads) floats.  num_sms is the current
  * device's SM count.  Returns MRI_ERR_MODE for an unknown probe.

@@ -40,7 +40,8 @@ class _Plan(ctypes.Structure):
                 ("samples_per_tile", ctypes.c_int), ("splits", ctypes.c_int),
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
-                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int)]
+                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int),
+                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int)]
 
 
 def lib_path() -> str:
@@ -415,11 +416,16 @@ class gather_timing:
         return False
 
 
-PROBES = {"sin": 0, "cos": 1, "ffma": 2, "ex2": 3}
+PROBES = {"sin": 0, "cos": 1, "ffma": 2, "ex2": 3, "ffma2": 4}
 
 
-def microbench(which: str, ctas_per_sm: int = 4, threads: int = 256, iters: int = 1 << 14):
-    """Results per SM per clock of one probed instruction (see mri_microbench.h)."""
+def microbench(which: str, ctas_per_sm: int = 1, threads: int = 1024, iters: int = 1 << 14):
+    """Results per SM per clock of one probed instruction (see mri_microbench.h).
+
+    The rate is taken from each CTA's own elapsed cycles, which is the SM's
+    busy time only when the SM holds one CTA: CTAs sharing an SM need not
+    start and finish together, and their per-CTA counts then overstate the
+    rate.  Keep ctas_per_sm = 1 (the default) for a roofline denominator."""
     dev = torch.device("cuda", torch.cuda.current_device())
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     grid = sms * ctas_per_sm

@@ -52,7 +52,7 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
     """Compile and link libmri.so; return its path.
 
-    ``defines`` (e.g. ``["MRI_NP_FP32_Q=3"]``) and ``out`` build a variant
+    ``defines`` (e.g. ``["MRI_PAIR_NP_FP32_Q=2"]``) and ``out`` build a variant
     library elsewhere, for tuning sweeps; the default build is ``LIB``.
     """
     lib = LIB if out is None else out

@@ -49,6 +49,15 @@ struct GridParams {
     int ey_blocks;
     // column blocks of 128 (the last may be partly padding)
     int ncb;
+    // Row folding (nx <= 64): with fold > 1 and the check word `fold_ok`
+    // set, a block's 128 columns are `fold` consecutive grid rows of
+    // 2^log2_fw columns each (column c: row offset c >> log2_fw, x index
+    // c & (2^log2_fw - 1)), and an MMA row is a group of `fold` grid rows;
+    // with the word clear the unfolded layout runs (a CTA whose rows lie past
+    // the folded row count exits at once).
+    int fold;
+    int log2_fw;
+    const unsigned int* fold_ok;
 };
 
 // Forward model on a grid (tensor-core kernel, gather_grid_tc_fwd.cuh).

@@ -234,14 +234,24 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity)
 // block), each block K-major as the MMA reads it.  One thread per (tile,
 // 8-row group, 8-sample chunk, row): consecutive threads write consecutive
 // 16-byte core-matrix rows, so a warp's stores are contiguous.
+//
+// Folded rows (fold > 1 and *fold_ok set, one column block): column gi is x
+// index gi & (2^log2_fw - 1) of grid row offset j = gi >> log2_fw within a row
+// group, and B = e^{i phase(kx[s] x + ky[s] dy[j])} with dy[j] the exact y
+// offset of the group's row j from its first row (fold_dy, from the check).
 template <int TRIG, bool MUB>
 __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, int fields,
                                                              int64_t ntiles, const float* xs,
                                                              int nx, int ncb,
-                                                             unsigned char* s_tab)
+                                                             unsigned char* s_tab, int fold,
+                                                             int log2_fw,
+                                                             const unsigned int* fold_ok,
+                                                             const float* fold_dy)
 {
     // MUB: one weight per sample (fields 3, and 4 unless the weight is real)
     const bool complex_w = fields > 4;
+    const bool folded = fold > 1 && *fold_ok != 0u;
+    const int fmask = (1 << log2_fw) - 1;
     constexpr int ITEMS = kTcCols * kTcTile / 8;       // 512 (column, chunk) items per tile
     const int64_t total = ntiles * ncb * ITEMS;
     for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
@@ -253,11 +263,20 @@ __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, i
         const int gi = ((r >> 5) << 3) | (r & 7);     // column within the block
         const int kc = (r >> 3) & 3;                  // samples 8 kc ..
         const float* kx = rec + t * fields * kTcTile + 8 * kc;
-        const int col = cb * kTcCols + gi;
-        const float xc = col < nx ? xs[col] : 0.0f;   // padding columns are never written
         float br[8], bi[8];
+        if (folded) {
+            const int ix = gi & fmask;
+            const float xc = ix < nx ? xs[ix] : 0.0f;  // padding columns are never written
+            const float dy = fold_dy[gi >> log2_fw];
 #pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+            for (int s8 = 0; s8 < 8; ++s8)
+                table_sincos<TRIG>(fmaf(kx[kTcTile + s8], dy, kx[s8] * xc), bi[s8], br[s8]);
+        } else {
+            const int col = cb * kTcCols + gi;
+            const float xc = col < nx ? xs[col] : 0.0f;   // padding columns are never written
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) table_sincos<TRIG>(kx[s8] * xc, bi[s8], br[s8]);
+        }
         if constexpr (MUB) {
 #pragma unroll
             for (int s8 = 0; s8 < 8; ++s8) {
@@ -280,6 +299,28 @@ __global__ void __launch_bounds__(256) build_ex_tiles_kernel(const float* rec, i
         *reinterpret_cast<uint4*>(tile + kTcSHi + kTcPartBytes + off) = h;
         *reinterpret_cast<uint4*>(tile + kTcSLo + kTcPartBytes + off) = l;
     }
+}
+
+// Row folding for narrow grids.  A block holds 128 columns; for nx <= 64
+// the columns of G = 128 / fw consecutive grid rows (fw = nx rounded up to a
+// power of two) share one block, so the MMA work is that of the real width
+// instead of 128 padded columns.  It is exact when every group of G rows has
+// the same y offsets from its first row: ys[G g + j] - ys[G g] = dy[j] for
+// every g, as real numbers (then ky ys[G g + j] = ky ys[G g] + ky dy[j]).
+inline int grid_tc_fold(int nx, int ny)
+{
+    if (nx < kTcMinCols || nx > kTcCols / 2) return 1;
+    int fw = kTcMinCols;
+    while (fw < nx) fw *= 2;
+    const int G = kTcCols / fw;
+    return ny % G == 0 ? G : 1;
+}
+
+inline int grid_tc_fold_log2_width(int G)
+{
+    int l = 7;
+    while ((1 << (7 - l)) < G) --l;
+    return l;   // fw = 128 / G = 2^l
 }
 
 // The Ey table: for record tile t and block yb of 128 y values,

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
     __shared__ __align__(8) uint64_t ey_free[2];          // EYT: Ey tile read by every generator
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
+    __shared__ int fold_sh[3];                            // G, log2 of its width, row groups
     volatile int* const abort_flag = &abort_sh;
 
     const int tid = threadIdx.x;
@@ -130,18 +131,33 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
     const int64_t t_begin = (p.ntiles * split) / p.splits;
     const int64_t t_end = (p.ntiles * (split + 1)) / p.splits;
     const int nt = int(t_end - t_begin);
-    const int64_t total_rows = int64_t(p.ny) * p.nz;
+    // row folding: an MMA row is a group of G grid rows (the check word says
+    // whether the y axis allows it; the grid is sized for the unfolded rows)
+    int G = 1, log2_fw = 7;
+    if (p.fold > 1 && *p.fold_ok != 0u) {
+        G = p.fold;
+        log2_fw = p.log2_fw;
+    }
     const int64_t row0 = int64_t(blockIdx.x) * RC;
-
-    for (int r = tid; r < RC; r += kWsThreads) {
-        const int64_t row = row0 + r;
-        float2 yz = make_float2(0.f, 0.f);
-        if (row < total_rows) {
-            const int64_t iz = row / p.ny;
-            const int64_t iy = row - iz * p.ny;
-            yz = make_float2(p.ys[iy], p.zs[iz]);
+    {
+        const int nyg = p.ny / G;                      // row groups per z plane
+        const int64_t total_rows = int64_t(nyg) * p.nz;   // MMA rows over the grid
+        if (row0 >= total_rows) return;                // folded: nothing for this CTA
+        for (int r = tid; r < RC; r += kWsThreads) {
+            const int64_t row = row0 + r;
+            float2 yz = make_float2(0.f, 0.f);
+            if (row < total_rows) {
+                const int64_t iz = row / nyg;
+                const int64_t iy = (row - iz * nyg) * G;   // the group's first grid row
+                yz = make_float2(p.ys[iy], p.zs[iz]);
+            }
+            yz_sh[r] = yz;
         }
-        yz_sh[r] = yz;
+        if (tid == 0) {
+            fold_sh[0] = G;
+            fold_sh[1] = log2_fw;
+            fold_sh[2] = nyg;
+        }
     }
     if (warp == 0) tmem_alloc(&tmem_base_sh, kTcTmemCols);
     if (tid == 0) {
@@ -427,13 +443,32 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
         if (!ok) {
             if (lane == 0) atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
         } else if (nt > 0) {
-            // R -> outputs: grid row ra, this warp's D columns
+            // R -> outputs: grid row ra, this warp's D columns (the fold
+            // state is read back from shared memory, not kept in registers)
             const float inv_scale = exp2_int(-tc_scale_exp(*p.wbound));
+            const volatile int* fs = fold_sh;
+            const int G = fs[0], log2_fw = fs[1], nyg = fs[2];
+            const int64_t total_rows = int64_t(nyg) * p.nz;
             const int64_t row = row0 + rr;
             const uint32_t wcols = tc_warp_cols(warp);
             float* const out = (wcols >= 128u ? p.out_i : p.out_r) + split * p.split_stride +
                                coil * p.coil_stride;
-            if (row < total_rows && coil < p.coils) {
+            if (G > 1 && row < total_rows && coil < p.coils) {
+                // column c of the block: grid row G * (row group) + (c >> log2_fw),
+                // x index c & (fw - 1); padding columns (x index >= nx) are not stored
+                const int64_t iz = row / nyg;
+                const int64_t iy = (row - iz * nyg) * G;
+                float* const o = out + (iz * p.ny + iy) * p.nx;
+                const int fmask = (1 << log2_fw) - 1;
+#pragma unroll
+                for (int j = 0; j < kTcColsPerWarp; ++j) {
+                    const int ix = j & fmask;
+                    if (ix < p.nx) {
+                        float* oj = o + int64_t(j >> log2_fw) * p.nx + ix;
+                        *oj = fmaf(R[j], inv_scale, p.accumulate ? *oj : 0.0f);
+                    }
+                }
+            } else if (row < total_rows && coil < p.coils) {
                 const int col0 = int(blockIdx.z) * kTcCols;
                 const int ncols = p.nx - col0 < kTcCols ? p.nx - col0 : kTcCols;
                 float* o = out + row * p.nx + col0 + (wcols & 127u);

@@ -1,17 +1,27 @@
 """Generate the minimax polynomials of the polynomial trig paths.
 
-The gather needs sin(2*pi*t) and cos(2*pi*t).  With u = 4t (quarter turns)
-the kernel reduces exactly, q = rint(u), f = u - q in [-1/2, 1/2], so the
-angle phi = (pi/2) f lies in [-pi/4, pi/4], and evaluates
+The gather needs sin(2*pi*t) and cos(2*pi*t).  Two reductions are used.
+
+Quarter turns (the grid paths' per-factor trig): with u = 4t the kernel
+reduces exactly, q = rint(u), f = u - q in [-1/2, 1/2], so the angle
+phi = (pi/2) f lies in [-pi/4, pi/4], and evaluates
 
     sin(phi) ~ f * P(f^2)        (odd, degree 2*len(P) - 1)
     cos(phi) ~ Q(f^2)            (even, degree 2*len(Q) - 2)
 
 then rotates by q quarter turns (a swap and sign flips from the two low bits
-of q).  On this short interval both series are well conditioned: the float32
-evaluation stays within about one ulp and its mean error is tiny, which
-matters because errors with a consistent sign add up coherently in Q, whose
-weights |Phi|^2 are all positive.
+of q).
+
+Half turns (the general gather, evaluated on pairs of floats): with u = 2t,
+q = rint(u), f = u - q, phi = pi f in [-pi/2, pi/2], the same two series of
+pi f, and e^{i 2 pi t} = (-1)^q e^{i phi}: only a sign flip from the low bit
+of q, no swap, so every step but the flip is a floating-point operation that
+the packed two-float instructions can do.
+
+On these short intervals both series are well conditioned: the float32
+evaluation stays within a few units in the last place and its mean error is
+tiny, which matters because errors with a consistent sign add up coherently
+in Q, whose weights |Phi|^2 are all positive.
 
 P and Q are fitted with the Remez exchange algorithm (E. Ya. Remez, 1934):
 minimise the maximum absolute error on s = f^2 in [0, 1/4], with the error
@@ -83,11 +93,13 @@ def remez(f, basis_count, lo, hi, iters=40):
     return coeffs
 
 
-def fit(p_terms=4, q_terms=5):
+def fit(p_terms=4, q_terms=5, turn=4):
+    """P, Q for phi = (2 pi / turn) f, f in [-1/2, 1/2] (turn = 4: quarter
+    turns, 2: half turns)."""
     quarter = mp.mpf(1) / 4                       # s = f^2 in [0, 1/4]
-    half_pi = mp.pi / 2
+    half_pi = 2 * mp.pi / turn
 
-    def sinc(s):                                  # sin((pi/2) f) / f as a function of s
+    def sinc(s):                                  # sin(half_pi f) / f as a function of s
         if s == 0:
             return half_pi
         f = mp.sqrt(s)
@@ -96,8 +108,18 @@ def fit(p_terms=4, q_terms=5):
     def cosq(s):
         return mp.cos(half_pi * mp.sqrt(s))
 
+    def cosm1(s):                                 # (cos(half_pi f) - 1) / f^2
+        if s == 0:
+            return -half_pi ** 2 / 2
+        return (mp.cos(half_pi * mp.sqrt(s)) - 1) / s
+
     P = remez(sinc, p_terms, mp.mpf(0), quarter)     # sin: degree 2p-1
-    Q = remez(cosq, q_terms, mp.mpf(0), quarter)     # cos: degree 2q-2
+    if turn == 4:
+        Q = remez(cosq, q_terms, mp.mpf(0), quarter)     # cos: degree 2q-2
+    else:
+        # constant term fixed at 1, so that a whole number of half turns
+        # (in particular a phase of exactly 0) gives cos = +-1 exactly
+        Q = [mp.mpf(1)] + remez(cosm1, q_terms - 1, mp.mpf(0), quarter)
     return P, Q
 
 
@@ -133,6 +155,29 @@ def quarter_turn_sincos32(P32, Q32, u):
     return np.float32(sn), np.float32(cs)
 
 
+def half_turn_sincos32(P32, Q32, u):
+    """The kernel's float32 sequence for sin and cos of pi u (u in half
+    turns), vectorised over u."""
+    u = np.asarray(u, np.float32)
+    magic = np.float32(12582912.0)
+    v = (u + magic).astype(np.float32)
+    t = (v - magic).astype(np.float32)
+    f = (u - t).astype(np.float32)
+    s = (f * f).astype(np.float32)
+
+    def horner(c):
+        acc = np.full_like(s, c[-1])
+        for ci in reversed(c[:-1]):
+            acc = (acc.astype(np.float64) * s.astype(np.float64)
+                   + np.float64(ci)).astype(np.float32)
+        return acc
+
+    sf = (f * horner(P32)).astype(np.float32)
+    cf = horner(Q32)
+    odd = (t.astype(np.int64) & 1) != 0
+    return np.where(odd, -sf, sf), np.where(odd, -cf, cf)
+
+
 def check(P32, Q32, n=20001):
     """Max and mean error of the float32 evaluation of sin/cos(2 pi t),
     t = u/4 over four turns."""
@@ -148,15 +193,28 @@ def check(P32, Q32, n=20001):
             float(es.mean()), float(ec.mean()))
 
 
-# (name, sin terms, cos terms)
-SETS = (("Quarter", 4, 5),)
+def check_half(P32, Q32, n=200001):
+    """Max and mean error of the float32 evaluation of sin/cos(2 pi t),
+    t = u/2 over four turns."""
+    u = np.linspace(-8.0, 8.0, n).astype(np.float32)
+    sn, cs = half_turn_sincos32(P32, Q32, u)
+    x = np.pi * u.astype(np.float64)
+    es = sn.astype(np.float64) - np.sin(x)
+    ec = cs.astype(np.float64) - np.cos(x)
+    return (float(np.abs(es).max()), float(np.abs(ec).max()),
+            float(es.mean()), float(ec.mean()))
+
+
+# (name, sin terms, cos terms, turn divisor)
+SETS = (("Quarter", 4, 5, 4), ("Half", 5, 5, 2))
 
 
 def main():
     lines = [
         "// sincospi_coeffs.h -- generated by gen_sincospi.py (Remez exchange, mpmath",
         "// 50 digits, coefficients rounded to float32).  Do not edit by hand.",
-        "//   u in quarter turns, f = u - rint(u) in [-1/2, 1/2], phi = (pi/2) f:",
+        "//   Quarter: u in quarter turns, f = u - rint(u) in [-1/2, 1/2], phi = (pi/2) f;",
+        "//   Half:    u in half turns,    f = u - rint(u) in [-1/2, 1/2], phi = pi f;",
         "//   sin(phi) ~ f * P(f^2),  cos(phi) ~ Q(f^2).",
         "#pragma once",
         "#ifdef __CUDACC__",
@@ -166,11 +224,11 @@ def main():
         "#endif",
         "namespace mri {",
     ]
-    for name, pt, qt in SETS:
-        P, Q = fit(pt, qt)
+    for name, pt, qt, turn in SETS:
+        P, Q = fit(pt, qt, turn)
         P32 = [f32(c) for c in P]
         Q32 = [f32(c) for c in Q]
-        es, ec, ms, mc = check(P32, Q32)
+        es, ec, ms, mc = (check if turn == 4 else check_half)(P32, Q32)
         lines += [
             f"// {name}: degree {2 * pt - 1} / {2 * qt - 2}; float32 evaluation over four turns:",
             f"//   max |error| sin {es:.3e}, cos {ec:.3e}; mean error sin {ms:.2e}, cos {mc:.2e}",

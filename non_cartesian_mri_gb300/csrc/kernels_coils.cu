@@ -7,12 +7,12 @@ namespace {
 template <int BC, int TRIG>
 cudaError_t run_gather(const GatherParams& p, dim3 grid, cudaStream_t s)
 {
-    using Sh = Shape<BC, false>;
+    using Sh = PairCoilShape<BC>;
     const cudaError_t attr = cudaFuncSetAttribute(
-        gather_kernel<BC, false, TRIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        gather_pair_coils_kernel<BC, TRIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         int(Sh::SMEM));
     if (attr != cudaSuccess) return attr;
-    gather_kernel<BC, false, TRIG><<<grid, Sh::THREADS, Sh::SMEM, s>>>(p);
+    gather_pair_coils_kernel<BC, TRIG><<<grid, Sh::THREADS, Sh::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -42,9 +42,9 @@ cudaError_t launch_gather_coils(int bc, int trig, const GatherParams& p, dim3 gr
 cudaError_t launch_prep_coils(int bc, const PrepParams& p, int grid, cudaStream_t s)
 {
     switch (bc) {
-        case 2: prep_records_kernel<2, false><<<grid, 256, 0, s>>>(p); break;
-        case 4: prep_records_kernel<4, false><<<grid, 256, 0, s>>>(p); break;
-        case 8: prep_records_kernel<8, false><<<grid, 256, 0, s>>>(p); break;
+        case 2: prep_pair_coil_records_kernel<2><<<grid, 256, 0, s>>>(p); break;
+        case 4: prep_pair_coil_records_kernel<4><<<grid, 256, 0, s>>>(p); break;
+        case 8: prep_pair_coil_records_kernel<8><<<grid, 256, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -43,16 +43,47 @@ int grid_tc_threads()
     return kWsThreads;
 }
 
-bool grid_tc_ey_table(int trig, int bc, int ny)
+bool grid_tc_ey_table(int trig, int bc, int nx, int ny)
 {
-    return bc == 1 && ny % kTcRows == 0 && trig == TRIG_ACCURATE;
+    return bc == 1 && ny % kTcRows == 0 && trig == TRIG_ACCURATE && grid_tc_fold(nx, ny) == 1;
+}
+
+// One CTA: *ok = 1 when the offsets of every group of G rows from its first
+// row equal those of the first group exactly and are floats themselves;
+// dy[j] = those offsets.  Otherwise *ok = 0 and the unfolded layout runs.
+// The differences are taken in double, where the difference of two floats is
+// exact unless their exponents are far apart; a - d == b confirms it.
+__global__ void __launch_bounds__(256) grid_fold_check_kernel(const float* ys, int ny, int G,
+                                                              unsigned int* ok, float* dy)
+{
+    bool good = true;
+    for (int i = threadIdx.x; i < ny; i += blockDim.x) {
+        const int j = i % G;
+        const double a = ys[i], b = ys[i - j], a0 = ys[j], b0 = ys[0];
+        const double d = a - b, d0 = a0 - b0;
+        good = good && a - d == b && a0 - d0 == b0 && d == d0 && double(float(d0)) == d0;
+    }
+    good = __syncthreads_and(good) != 0;
+    if (int(threadIdx.x) < G) dy[threadIdx.x] = float(double(ys[threadIdx.x]) - double(ys[0]));
+    if (threadIdx.x == 0) *ok = good ? 1u : 0u;
+}
+
+cudaError_t launch_grid_fold_check(const float* ys, int ny, int G, unsigned int* ok, float* dy,
+                                   cudaStream_t s)
+{
+    if (G < 2 || G > kTcCols / kTcMinCols || ny % G != 0) return cudaErrorInvalidValue;
+    grid_fold_check_kernel<<<1, 256, 0, s>>>(ys, ny, G, ok, dy);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, dim3 grid,
                            cudaStream_t s)
 {
     if (!grid_tc_fits(p.nx)) return cudaErrorInvalidValue;
-    const bool eyt = grid_tc_ey_table(trig, bc, p.ny);
+    if (p.fold > 1 && (p.fold != grid_tc_fold(p.nx, p.ny) || p.fold_ok == nullptr ||
+                       p.log2_fw != grid_tc_fold_log2_width(p.fold)))
+        return cudaErrorInvalidValue;
+    const bool eyt = grid_tc_ey_table(trig, bc, p.nx, p.ny);
     if (eyt && (p.ey_tab == nullptr || p.ey_blocks != p.ny / kTcRows)) return cudaErrorInvalidValue;
     if (realw) {
         if (bc != 1) return cudaErrorInvalidValue;
@@ -95,11 +126,16 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
 
 cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,
                                   int64_t ntiles, const float* xs, int nx, unsigned char* s_tab,
-                                  int grid, cudaStream_t s)
+                                  int grid, cudaStream_t s, int fold,
+                                  const unsigned int* fold_ok, const float* fold_dy)
 {
     const int ncb = grid_tc_col_blocks(nx);
+    if (fold > 1 && (ncb != 1 || fold_ok == nullptr || fold_dy == nullptr))
+        return cudaErrorInvalidValue;
+    const int log2_fw = grid_tc_fold_log2_width(fold);
     auto go = [&](auto kernel) {
-        kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx, ncb, s_tab);
+        kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, xs, nx, ncb, s_tab, fold, log2_fw,
+                                    fold_ok, fold_dy);
         return cudaGetLastError();
     };
     switch (trig) {
@@ -179,12 +215,12 @@ cudaError_t launch_prep_grid_tc(bool realw, int bc, const PrepParams& p, int gri
 {
     if (realw) {
         if (bc != 1) return cudaErrorInvalidValue;
-        prep_records_kernel<1, true, kTcTile, true><<<grid, 256, 0, s>>>(p);
+        prep_records_kernel<1, true, kTcTile><<<grid, 256, 0, s>>>(p);
     } else {
         switch (bc) {
-            case 1: prep_records_kernel<1, false, kTcTile, true><<<grid, 256, 0, s>>>(p); break;
-            case 4: prep_records_kernel<4, false, kTcTile, true><<<grid, 256, 0, s>>>(p); break;
-            case 8: prep_records_kernel<8, false, kTcTile, true><<<grid, 256, 0, s>>>(p); break;
+            case 1: prep_records_kernel<1, false, kTcTile><<<grid, 256, 0, s>>>(p); break;
+            case 4: prep_records_kernel<4, false, kTcTile><<<grid, 256, 0, s>>>(p); break;
+            case 8: prep_records_kernel<8, false, kTcTile><<<grid, 256, 0, s>>>(p); break;
             default: return cudaErrorInvalidValue;
         }
     }

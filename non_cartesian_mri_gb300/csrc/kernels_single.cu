@@ -1,5 +1,7 @@
 // kernels_single.cu -- F^H D (one weight vector) and Q instantiations, the
 // prep, reduction and cmpMu kernels.
+#include <type_traits>
+
 #include "launch.h"
 
 namespace mri {
@@ -53,33 +55,34 @@ __global__ void __launch_bounds__(256) mu_kernel(const float* __restrict__ rPhi,
 
 
 namespace {
-template <int BC, bool REALW, int TRIG>
+template <bool REALW, int TRIG>
 cudaError_t run_gather(const GatherParams& p, dim3 grid, cudaStream_t s)
 {
-    using Sh = Shape<BC, REALW>;
+    constexpr size_t smem = PairShape::smem<REALW>();
     const cudaError_t attr = cudaFuncSetAttribute(
-        gather_kernel<BC, REALW, TRIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        int(Sh::SMEM));
+        gather_pair_kernel<REALW, TRIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        int(smem));
     if (attr != cudaSuccess) return attr;
-    gather_kernel<BC, REALW, TRIG><<<grid, Sh::THREADS, Sh::SMEM, s>>>(p);
+    gather_pair_kernel<REALW, TRIG><<<grid, PairShape::THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
 }  // namespace
 
+// one weight vector (F^H D, Q, the forward model): the kernel on pairs of floats
 cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, dim3 grid,
                                  cudaStream_t s)
 {
     if (realw) {
         switch (trig) {
-            case TRIG_ACCURATE: return run_gather<1, true, TRIG_ACCURATE>(p, grid, s);
-            case TRIG_FAST: return run_gather<1, true, TRIG_FAST>(p, grid, s);
-            case TRIG_FAST_RR: return run_gather<1, true, TRIG_FAST_RR>(p, grid, s);
+            case TRIG_ACCURATE: return run_gather<true, TRIG_ACCURATE>(p, grid, s);
+            case TRIG_FAST: return run_gather<true, TRIG_FAST>(p, grid, s);
+            case TRIG_FAST_RR: return run_gather<true, TRIG_FAST_RR>(p, grid, s);
         }
     } else {
         switch (trig) {
-            case TRIG_ACCURATE: return run_gather<1, false, TRIG_ACCURATE>(p, grid, s);
-            case TRIG_FAST: return run_gather<1, false, TRIG_FAST>(p, grid, s);
-            case TRIG_FAST_RR: return run_gather<1, false, TRIG_FAST_RR>(p, grid, s);
+            case TRIG_ACCURATE: return run_gather<false, TRIG_ACCURATE>(p, grid, s);
+            case TRIG_FAST: return run_gather<false, TRIG_FAST>(p, grid, s);
+            case TRIG_FAST_RR: return run_gather<false, TRIG_FAST_RR>(p, grid, s);
         }
     }
     return cudaErrorInvalidValue;
@@ -88,15 +91,17 @@ cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, di
 cudaError_t launch_prep(int bc, bool realw, const PrepParams& p, int grid, cudaStream_t s)
 {
     if (realw) {
-        prep_records_kernel<1, true><<<grid, 256, 0, s>>>(p);
+        prep_pair_records_kernel<true><<<grid, 256, 0, s>>>(p);
         return cudaGetLastError();
     }
     if (bc == 1) {
-        prep_records_kernel<1, false><<<grid, 256, 0, s>>>(p);
+        prep_pair_records_kernel<false><<<grid, 256, 0, s>>>(p);
         return cudaGetLastError();
     }
     return launch_prep_coils(bc, p, grid, s);
 }
+
+float gather_kscale(int, int trig) { return pair_kscale(trig); }
 
 cudaError_t launch_gather(int bc, bool realw, int trig, const GatherParams& p, dim3 grid,
                           cudaStream_t s)
@@ -130,20 +135,31 @@ cudaError_t launch_zero(float* a, int64_t n, int grid, cudaStream_t s)
 KernelShape gather_shape(int bc, bool realw)
 {
     KernelShape k{};
-    auto fill = [&](auto sh, int tile_floats) {
-        using Sh = decltype(sh);
+    auto fill_pair = [&](auto realw_tag) {
+        constexpr bool RW = decltype(realw_tag)::value;
+        k.threads = PairShape::THREADS;
+        k.v = PairShape::V;
+        k.voxels_per_cta = PairShape::VOXELS_PER_CTA;
+        k.min_blocks = PairShape::MIN_BLOCKS;
+        k.smem = PairShape::smem<RW>();
+        k.tile_floats = PairRec<RW>::TILE_FLOATS;
+        k.fast_fp32_voxels = 2 * PairShape::np_fp32<RW>();
+    };
+    auto fill_coils = [&](auto bc_tag) {
+        constexpr int B = decltype(bc_tag)::value;
+        using Sh = PairCoilShape<B>;
         k.threads = Sh::THREADS;
         k.v = Sh::V;
         k.voxels_per_cta = Sh::VOXELS_PER_CTA;
         k.min_blocks = Sh::MIN_BLOCKS;
         k.smem = Sh::SMEM;
-        k.tile_floats = tile_floats;
+        k.tile_floats = PairCoilRec<B>::TILE_FLOATS;
     };
-    if (realw) fill(Shape<1, true>{}, Rec<1, true>::TILE_FLOATS);
-    else if (bc == 1) fill(Shape<1, false>{}, Rec<1, false>::TILE_FLOATS);
-    else if (bc == 2) fill(Shape<2, false>{}, Rec<2, false>::TILE_FLOATS);
-    else if (bc == 4) fill(Shape<4, false>{}, Rec<4, false>::TILE_FLOATS);
-    else fill(Shape<8, false>{}, Rec<8, false>::TILE_FLOATS);
+    if (realw) fill_pair(std::true_type{});
+    else if (bc == 1) fill_pair(std::false_type{});
+    else if (bc == 2) fill_coils(std::integral_constant<int, 2>{});
+    else if (bc == 4) fill_coils(std::integral_constant<int, 4>{});
+    else fill_coils(std::integral_constant<int, 8>{});
     return k;
 }
 

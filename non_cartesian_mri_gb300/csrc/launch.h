@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gather.cuh"
+#include "gather_pair.cuh"
 #include "gather_grid.cuh"
 #include "gather_grid_tc.cuh"
 #include "fft.cuh"
@@ -19,12 +20,16 @@ struct KernelShape {
     int min_blocks;         // CTAs per SM the kernel is built for
     size_t smem;            // dynamic shared memory per CTA
     int tile_floats;        // floats per record tile
+    int fast_fp32_voxels;   // of the v voxels of a thread, those whose fast-path trig is
+                            // the polynomial on the FMA pipe (the rest use the SFU)
 };
 
 // bc: coils in one group (1, 2, 4, 8); realw: Q's real weight (bc == 1).
 KernelShape gather_shape(int bc, bool realw);
 
 cudaError_t launch_prep(int bc, bool realw, const PrepParams& p, int grid, cudaStream_t s);
+// phase units the records of a general gather launch hold (k is multiplied by it)
+float gather_kscale(int bc, int trig);
 cudaError_t launch_gather(int bc, bool realw, int trig, const GatherParams& p, dim3 grid,
                           cudaStream_t s);
 cudaError_t launch_reduce(const float* part, int splits, int bc, int64_t N, float* out_r,
@@ -53,7 +58,11 @@ cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
 // threads per CTA of the tensor-core grid kernel
 int grid_tc_threads();
 // whether a tensor-core grid launch takes its y factors from the Ey table
-bool grid_tc_ey_table(int trig, int bc, int ny);
+bool grid_tc_ey_table(int trig, int bc, int nx, int ny);
+// the row-folding check of a narrow grid (grid_tc_fold(nx, ny) = G > 1): *ok
+// and the G row offsets dy, read by the B-tile build and the kernel
+cudaError_t launch_grid_fold_check(const float* ys, int ny, int G, unsigned int* ok, float* dy,
+                                   cudaStream_t s);
 // the Ey table (ny % 128 == 0) from the records (ky) and ys
 cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
                                   const float* ys, int ny, float2* ey_tab, int grid,
@@ -62,7 +71,9 @@ cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_
 // xs; mub: times the records' (scaled) weight, for single-coil launches
 cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,
                                   int64_t ntiles, const float* xs, int nx, unsigned char* s_tab,
-                                  int grid, cudaStream_t s);
+                                  int grid, cudaStream_t s, int fold = 1,
+                                  const unsigned int* fold_ok = nullptr,
+                                  const float* fold_dy = nullptr);
 // voxel coordinates of a grid the tensor-core kernels do not take (kernels_grid.cu)
 cudaError_t launch_expand_grid(const float* xs, const float* ys, const float* zs, int nx, int ny,
                                int64_t N, float* x, float* y, float* z, int grid, cudaStream_t s);

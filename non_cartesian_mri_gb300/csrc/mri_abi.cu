@@ -247,7 +247,8 @@ mri_status run_group(DeviceState* d, const GroupPlan& g, int sms, const float* k
     float* rec = reinterpret_cast<float*>(scratch);
     float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes));
 
-    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, b0, g.ntiles, kscale_for(trig), rec};
+    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, b0, g.ntiles,
+                       mri::gather_kscale(g.bc, trig), rec};
     if (forward) {
         // e^{-i2pi k.x}: the sign goes into the record scale; weight = rho
         pp.kscale = -pp.kscale;
@@ -371,6 +372,9 @@ struct GridPlan {
     int64_t part_bytes;
     int64_t s_bytes;        // the B operand tiles
     int64_t ey_bytes;       // one weight, accurate, ny % 128 == 0: the Ey table
+    int fold;               // grid rows folded into one block's columns (nx <= 64), else 1
+    int64_t vblocks_launch; // CTAs along the rows launched: the unfolded count when
+                            // fold > 1 (the device-side check may refuse the fold)
 };
 
 // A group of coils of a tensor-core grid call: coils b0 .. b0 + nb - 1 run in
@@ -407,14 +411,17 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int b
     g.ncb = mri::grid_tc_col_blocks(nx);
     g.rows_per_cta = mri::kTcRows / bc;
     g.ntiles = ceil_div(M, mri::kTcTile);
-    g.vblocks = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
+    g.fold = mri::grid_tc_fold(nx, ny);
+    // planned for the folded rows (the y axes of images are evenly spaced)
+    g.vblocks = ceil_div(int64_t(ny / g.fold) * nz, g.rows_per_cta);
+    g.vblocks_launch = ceil_div(int64_t(ny) * nz, g.rows_per_cta);
     g.splits = (g.ntiles > 0 && g.vblocks > 0)
                    ? choose_splits(g.ntiles, g.vblocks * g.ncb, sms > 0 ? sms : 1, nb, N, 1.0, 3.0)
                    : 1;
     g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
     g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
     g.s_bytes = g.ntiles * g.ncb * int64_t(mri::kTcStageBytes);
-    g.ey_bytes = mri::grid_tc_ey_table(trig, bc, ny)
+    g.ey_bytes = mri::grid_tc_ey_table(trig, bc, nx, ny)
                      ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
                      : 0;
     return g;
@@ -427,7 +434,7 @@ mri_status launch_grid_gather(const GridPlan& g, bool realw, int trig,
     mri_status st = MRI_OK;
     cudaEvent_t* ev = timing_slot(d);
     if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) st = cuda_fail();
-    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), unsigned(g.ncb));
+    const dim3 grid(unsigned(g.vblocks_launch), unsigned(g.splits), unsigned(g.ncb));
     if (st == MRI_OK && mri::launch_grid_tc(realw, trig, g.bc, gp, grid, s) != cudaSuccess)
         st = cuda_fail();
     if (st == MRI_OK && ev && cudaEventRecord(ev[1], s) != cudaSuccess) st = cuda_fail();
@@ -509,11 +516,19 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
                                                      align256(part_max) + align256(s_bytes))
                          : nullptr;
     float* rec = reinterpret_cast<float*>(scratch);
+    // the bound slot: the weight bound word, the fold check's word and offsets
     unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(rec_max));
+    unsigned int* fold_ok = wbound + 1;
+    float* fold_dy = reinterpret_cast<float*>(wbound + 4);
     float* part = reinterpret_cast<float*>(scratch + align256(rec_max) + kBoundBytes);
     unsigned char* s_tab = reinterpret_cast<unsigned char*>(scratch + align256(rec_max) +
                                                             kBoundBytes + align256(part_max));
     mri_status st = MRI_OK;
+    // narrow grids: whether ys allows folding G rows into a block's columns
+    const int fold = plans[0].fold;
+    if (fold > 1 &&
+        mri::launch_grid_fold_check(ys, ny, fold, fold_ok, fold_dy, s) != cudaSuccess)
+        st = cuda_fail();
     for (size_t i = 0; i < groups.size() && st == MRI_OK; ++i) {
         const TcGroup& grp = groups[i];
         const GridPlan& g = plans[i];
@@ -537,7 +552,7 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
             mri::launch_build_ex_tiles(trig, grp.bc == 1, rec, fields, g.ntiles, xs, nx, s_tab,
                                        grid_for(g.ntiles * mri::grid_tc_col_blocks(nx) * 512,
                                                 d->sms),
-                                       s) != cudaSuccess)
+                                       s, fold, fold_ok, fold_dy) != cudaSuccess)
             st = cuda_fail();
         // the y factors depend on ky and the rows only: built once, by the
         // first group that reads them
@@ -554,6 +569,9 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         gp.ey_blocks = g.ey_bytes > 0 ? ny / mri::kTcRows : 0;
         gp.coils = grp.nb;
         gp.ncb = mri::grid_tc_col_blocks(nx);
+        gp.fold = fold;
+        gp.log2_fw = mri::grid_tc_fold_log2_width(fold);
+        gp.fold_ok = fold_ok;
         if (g.splits == 1) {
             gp.out_r = out_r + grp.b0 * N;
             gp.out_i = out_i + grp.b0 * N;
@@ -634,6 +652,14 @@ unsigned int* error_word_address(int dev)
         addr[dev] = static_cast<unsigned int*>(p);
     }
     return addr[dev];
+}
+
+// Residency of caller pointers on device `dev` (cudaPointerGetAttributes per
+// pointer; no allocation): MRI_OK, or MRI_ERR_NOT_DEVICE for host, page-locked
+// host or another device's memory.  Used by the allocation-free entry point.
+mri_status check_device_ptrs(const void* const* ptrs, int n, int dev)
+{
+    return check_ptrs(ptrs, n, dev);
 }
 
 }  // namespace mri
@@ -920,7 +946,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
     // single coil); the first group's shape is reported
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
     int64_t rec_max = 0, part_max = 0;
-    plan->launches = 1;
+    plan->launches = 1 + (g.fold > 1 ? 1 : 0);   // the B tiles (and the fold check)
     for (size_t i = 0; i < groups.size(); ++i) {
         const GridPlan gi = plan_grid(realw, M, nx, ny, nz, num_sms, groups[i].bc, groups[i].nb);
         if (i == 0) {
@@ -928,6 +954,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
             plan->voxels_per_thread = mri::kTcRows * mri::kTcCols / mri::kTcThreads;
             plan->splits = gi.splits;
             plan->voxel_ctas = gi.vblocks * gi.ncb;
+            plan->grid_fold = gi.fold;
         }
         rec_max = std::max(rec_max, gi.rec_bytes);
         part_max = std::max(part_max, gi.part_bytes);
@@ -1169,6 +1196,7 @@ mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sm
     const GroupPlan& g0 = plans[realw ? 3 : group_index(B)];
     plan->threads_per_cta = g0.shape.threads;
     plan->voxels_per_thread = g0.shape.v;
+    plan->fast_fp32_voxels = g0.shape.fast_fp32_voxels;
     plan->samples_per_tile = kTile;
     plan->splits = g0.splits;
     plan->voxel_ctas = g0.vblocks;

@@ -20,6 +20,8 @@
 
 namespace mri {
 unsigned int* error_word_address(int dev);   // mri_abi.cu; symbol lookup only
+// mri_abi.cu; the residency check every entry point makes (no allocation)
+mri_status check_device_ptrs(const void* const* ptrs, int n, int dev);
 }
 
 namespace {
@@ -34,6 +36,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 struct NoallocDevice {
     bool ready = false;
+    int dev = -1;
     mri_status status = MRI_OK;
     int sms = 0;
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
@@ -72,6 +75,7 @@ mri_status noalloc_device(NoallocDevice** out)
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return fail_cuda();
             unsigned int* err = mri::error_word_address(dev);
             if (err == nullptr) return fail_cuda();
+            d.dev = dev;
             d.sms = sms;
             d.scratch = static_cast<unsigned char*>(p);
             d.err = err;
@@ -108,7 +112,7 @@ extern "C" mri_status mri_fhd_noalloc(const float* kx, const float* ky, const fl
     if (accumulate != 0 && accumulate != 1) return MRI_ERR_MODE;
     if (M < 0 || N < 0 || N > (int64_t(1) << 40)) return MRI_ERR_SIZE;
     const int64_t ntiles = (M + mri::kTile - 1) / mri::kTile;
-    const int64_t rec_bytes = round256(ntiles * int64_t(mri::Rec<1, false>::TILE_BYTES));
+    const int64_t rec_bytes = round256(ntiles * int64_t(mri::PairRec<false>::TILE_BYTES));
     if (rec_bytes > kNoallocScratchBytes) return MRI_ERR_SIZE;   // M above the fixed maximum
     if (N == 0) return MRI_OK;
 
@@ -128,6 +132,9 @@ extern "C" mri_status mri_fhd_noalloc(const float* kx, const float* ky, const fl
     NoallocDevice* d = nullptr;
     mri_status st = noalloc_device(&d);
     if (st != MRI_OK) return st;
+    // as in mri_fhd: every array must be memory of the current device
+    if ((st = mri::check_device_ptrs(voxel_ptrs, 5, d->dev)) != MRI_OK) return st;
+    if (M > 0 && (st = mri::check_device_ptrs(sample_ptrs, 7, d->dev)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (M == 0) {
@@ -153,10 +160,8 @@ extern "C" mri_status mri_fhd_noalloc(const float* kx, const float* ky, const fl
     float* rec = reinterpret_cast<float*>(d->scratch);
     float* part = reinterpret_cast<float*>(d->scratch + rec_bytes);
 
-    const float kscale = tr == MRI_TRIG_ACCURATE ? 4.0f
-                         : tr == MRI_TRIG_FAST   ? 6.28318530717958647692f
-                                                 : 1.0f;
-    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, ntiles, kscale, rec};
+    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, 0, ntiles, mri::gather_kscale(1, tr),
+                       rec};
     if (mri::launch_prep(1, false, pp, grid_cap(ntiles * mri::kTile, d->sms), s) != cudaSuccess)
         return fail_cuda();
 

@@ -121,7 +121,8 @@ class Plan(ctypes.Structure):
                 ("samples_per_tile", ctypes.c_int), ("splits", ctypes.c_int),
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
-                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int)]
+                ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int),
+                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int)]
 
 
 def plan(lib, kind, B, M, N, sms=152):
@@ -185,6 +186,26 @@ def test_batched_grid_plan_groups(lib):
     assert f(3, 1000, 257, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1
     assert p.voxel_ctas == 3 * c8
     assert lib.mri_plan_grid(2, 1000, 128, 4, 4, 152, ctypes.byref(p)) == MODE
+
+
+def test_grid_fold_plan(lib):
+    """Narrow grids (8 <= nx <= 64) fold 128 / fw grid rows into one block of
+    128 columns, fw = nx rounded up to a power of two, when ny is a multiple
+    of that; the plan counts the folded row blocks."""
+    f = lib.mri_plan_grid
+    f.argtypes = [ctypes.c_int, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.POINTER(Plan)]
+    f.restype = ctypes.c_int
+    for nx, ny, nz, fold in [(64, 64, 64, 2), (48, 64, 3, 2), (32, 64, 1, 4), (20, 8, 2, 4),
+                             (16, 16, 4, 8), (9, 32, 1, 8), (8, 16, 2, 16), (8, 9, 9, 1),
+                             (64, 1, 1, 1), (65, 64, 64, 1), (128, 128, 128, 1),
+                             (32, 6, 5, 1), (7, 64, 64, 0)]:
+        p = Plan()
+        assert f(0, 32768, nx, ny, nz, 152, ctypes.byref(p)) == OK
+        assert p.grid_fold == fold, (nx, ny, nz)
+        if fold:
+            assert p.voxel_ctas == -(-(ny // fold) * nz // 128) * -(-nx // 128)
+            assert p.launches == 1 + (fold > 1) + 3 + (p.splits > 1)
 
 
 def test_batched_grid_argument_checks(lib):

@@ -55,3 +55,24 @@ def test_find_rho_and_gridding_byte_accounting():
     assert bench.CG_EXTRA_BYTES_PER_VOXEL == 64
     assert bench.GRIDDING_BYTES_PER_SAMPLE == 28
     assert bench.GRIDDING_BYTES_PER_VOXEL == 72
+
+
+def test_general_gather_roofline_follows_the_kernel():
+    """The SFU/FP32 bound of the general gather charges each unit what the
+    kernel gives it: every sin/cos on the SFU (fast), every one as the 13-op
+    polynomial on the FP32 pipe (accurate), or a share of them there."""
+    ops = bench.algo_ops("fhd", "fast")
+    assert (ops["mufu"], ops["fp32"]) == (2.0, 7.0)
+    ops = bench.algo_ops("fhd", "accurate")
+    assert (ops["mufu"], ops["fp32"]) == (0.0, 7.0 + 13.0)
+    ops = bench.algo_ops("q", "fast", 0.25)
+    assert ops["mufu"] == 1.5 and abs(ops["fp32"] - (5.0 + 14.0 * 0.25)) < 1e-12
+    per, unit, _, _ = bench.peak_per_sm_clk("fhd", None, "fast")
+    assert (per, unit) == (8.0, "mufu")                  # 16 sin/cos per SM per clock
+    per, unit, _, _ = bench.peak_per_sm_clk("fhd", None, "accurate")
+    assert (per, unit) == (128.0 / 20.0, "fp32")
+    per, unit, _, _ = bench.peak_per_sm_clk("q", None, "fast", 0.25)
+    assert abs(per - 16.0 / 1.5) < 1e-12 and unit == "mufu"
+    # batched, 8 coils: FP32-bound, 3/8 + 4 operations per pair-coil
+    per, unit, _, _ = bench.peak_per_sm_clk("fhd_batched", None, "fast")
+    assert abs(per - 128.0 / 4.375) < 1e-12 and unit == "fp32"

@@ -61,8 +61,13 @@ def calls(lib, M, nx, ny, nz):
         return f(p[0], p[1], p[2], p[3], nx, p[4], ny, p[5], nz, p[6], p[7], M, p[8], p[9],
                  1, 0, None)
 
+    def fhd_noalloc(p):
+        f = lib.mri_fhd_noalloc
+        f.argtypes = [P] * 10 + [I64, I64, P, P, I, I, P]
+        return f(*p[:10], M, N, p[10], p[11], 1, 0, None)
+
     return [("mri_fhd", fhd, 12), ("mri_q", q, 10), ("mri_fhd_grid", fhd_grid, 12),
-            ("mri_forward_grid", forward_grid, 10)]
+            ("mri_forward_grid", forward_grid, 10), ("mri_fhd_noalloc", fhd_noalloc, 12)]
 
 
 def test_host_and_misaligned_pointers(mri, lib):
@@ -98,7 +103,8 @@ def test_pinned_host_memory_is_not_device_memory(mri, lib):
     M, nx, ny, nz = 100, 16, 2, 2
     dev = [torch.zeros(256, device="cuda") for _ in range(12)]
     pinned = torch.zeros(256).pin_memory()
-    name, fn, k = calls(lib, M, nx, ny, nz)[2]
-    p = [ptr(t) for t in dev[:k]]
-    p[0] = ptr(pinned)
-    assert fn(p) == NOT_DEVICE
+    for name, fn, k in (calls(lib, M, nx, ny, nz)[2], calls(lib, M, nx, ny, nz)[4]):
+        for slot in (0, k - 1):
+            p = [ptr(t) for t in dev[:k]]
+            p[slot] = ptr(pinned)
+            assert fn(p) == NOT_DEVICE, f"{name}: pinned host memory in slot {slot}"

@@ -13,6 +13,7 @@ import torch
 
 import oracle
 from non_cartesian_mri_gb300 import workloads as wl
+from tests.sampling import grid_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -40,30 +41,62 @@ def expand(xs, ys, zs):
     return x.reshape(-1), y.reshape(-1), z.reshape(-1)
 
 
+def plan_grid_blocks(mri, kind, w, seed, per):
+    """Voxels from every (row block, column block) the grid launch assigns to
+    a CTA, `per` of them spread over each block's rows."""
+    n = round(w.N ** (1 / 3))
+    p = mri.plan_grid(kind, w.M, n, n, n)
+    if not p["tensor_cores"]:
+        return None
+    # one weight: 128 MMA rows, each a group of grid_fold grid rows (64^3: 2)
+    rows_per_cta = 128 * p["grid_fold"]
+    assert p["voxel_ctas"] == -(-n * n // rows_per_cta) * -(-n // 128)
+    return grid_blocks(n, n, n, rows_per_cta, seed, per=per)
+
+
+_refs = {}
+
+
+def grid_ref(mri, name, kind, per, seed):
+    """Oracle values on the stratified subset, computed once per workload."""
+    if name not in _refs:
+        w = wl.make_workload(name)
+        idx = plan_grid_blocks(mri, kind, w, seed, per)
+        if kind == "q":
+            origin = (64 * 128 + 64) * 128 + 64
+            idx = np.unique(np.concatenate([idx, [origin]]))
+            ref = oracle.q(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
+        else:
+            ref = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD,
+                             idx=idx)
+        _refs[name] = (w, idx, ref)
+    return _refs[name]
+
+
 @pytest.mark.parametrize("trig", ["accurate", "fast", "fast_rr"])
-@pytest.mark.parametrize("name,nsub", [("fhd_tiny", None), ("fhd_64", 2048),
-                                       ("fhd_128_radial", 512)])
-def test_fhd_grid_workloads(mri, name, nsub, trig):
-    w = wl.make_workload(name)
+@pytest.mark.parametrize("name,per", [("fhd_tiny", None), ("fhd_64", 64),
+                                      ("fhd_128_radial", 8)])
+def test_fhd_grid_workloads(mri, name, per, trig):
+    if per is None:
+        w = wl.make_workload(name)
+        idx = None
+        ref = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD)
+    else:
+        w, idx, ref = grid_ref(mri, name, "fhd", per, 201)
     xs, ys, zs = w.axes()
     r, i = mri.fhd_grid(dev(w.kx), dev(w.ky), dev(w.kz), dev(xs), dev(ys), dev(zs),
                         dev(w.rPhi), dev(w.iPhi), dev(w.rD), dev(w.iD), trig=trig)
-    idx = None if nsub is None else wl.voxel_subset(w.N, nsub, 201)
-    ref = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
     got = cplx(r, i) if idx is None else cplx(r, i)[idx]
     assert oracle.rel_l2(got, ref) <= TOL[trig]
+    assert mri.device_errors(clear=True) == 0
 
 
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
 def test_q_grid_128(mri, trig):
-    w = wl.make_workload("q_128")
+    w, idx, ref = grid_ref(mri, "q_128", "q", 8, 202)
     xs, ys, zs = w.axes()
     r, i = mri.q_grid(dev(w.kx), dev(w.ky), dev(w.kz), dev(xs), dev(ys), dev(zs),
                       dev(w.rPhi), dev(w.iPhi), trig=trig)
-    idx = wl.voxel_subset(w.N, 192, 202)
-    origin = (64 * 128 + 64) * 128 + 64
-    idx = np.unique(np.concatenate([idx, [origin]]))
-    ref = oracle.q(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
     assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
 
 

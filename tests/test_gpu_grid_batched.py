@@ -14,6 +14,7 @@ import torch
 
 import oracle
 from non_cartesian_mri_gb300 import workloads as wl
+from tests.sampling import grid_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -121,6 +122,22 @@ def test_coils_of_very_different_scale(mri):
     check_per_coil(cplx(r, i), ref, TOL["accurate"])
 
 
+_batched_ref = {}
+
+
+def batched_ref(mri, w):
+    """One voxel from every (row block, column block) of the 8-coil launch --
+    16 grid rows per CTA, 1,024 blocks -- every coil; computed once."""
+    if not _batched_ref:
+        n = 128
+        p = mri.plan_grid_batched(8, w.M, n, n, n)
+        assert p["tensor_cores"] and p["voxel_ctas"] == n * n // 16
+        idx = grid_blocks(n, n, n, 16, 301)
+        _batched_ref["v"] = (idx, oracle.fhd_batched(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi,
+                                                     w.iPhi, w.rD, w.iD, idx=idx))
+    return _batched_ref["v"]
+
+
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
 def test_batched_grid_128_workload(mri, trig):
     """The 8-coil 128^3 stack-of-spirals workload, sampled voxels."""
@@ -128,9 +145,7 @@ def test_batched_grid_128_workload(mri, trig):
     xs, ys, zs = w.axes()
     r, i = mri.fhd_batched_grid(dev(w.kx), dev(w.ky), dev(w.kz), dev(xs), dev(ys), dev(zs),
                                 dev(w.rPhi), dev(w.iPhi), dev(w.rD), dev(w.iD), trig=trig)
-    idx = wl.voxel_subset(w.N, 48, 301)
-    ref = oracle.fhd_batched(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD,
-                             idx=idx)
+    idx, ref = batched_ref(mri, w)
     check_per_coil(cplx(r, i)[:, idx], ref, TOL[trig])
     assert mri.device_errors(clear=True) == 0
 

@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from non_cartesian_mri_gb300 import workloads as wl
+from tests.sampling import gather_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -56,11 +57,19 @@ def test_fhd_tiny_all_voxels(mri, trig):
     assert oracle.rel_l2(cplx(r, i), ref) <= TOL[trig]
 
 
+def plan_blocks(mri, kind, w, seed, per=1, B=1):
+    """Voxels from every CTA block of the launch the call makes."""
+    p = mri.plan(kind, w.M, w.N, B=B)
+    vpc = p["threads_per_cta"] * p["voxels_per_thread"]
+    assert p["voxel_ctas"] == -(-w.N // vpc)
+    return gather_blocks(w.N, vpc, seed, per=per)
+
+
 @pytest.mark.parametrize("trig", TRIGS)
 def test_fhd_64_subset(mri, trig):
     w = wl.make_workload("fhd_64")
     r, i = mri.fhd(*fhd_inputs(w), trig=trig)
-    idx = wl.voxel_subset(w.N, 4096, 101)
+    idx = plan_blocks(mri, "fhd", w, 101, per=16)
     ref = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
     assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
 
@@ -71,9 +80,9 @@ def radial():
 
 
 @pytest.fixture(scope="module")
-def radial_ref(radial):
+def radial_ref(mri, radial):
     w = radial
-    idx = wl.voxel_subset(w.N, 1024, 102)
+    idx = plan_blocks(mri, "fhd", w, 102)
     corners = np.array([0, w.N - 1, 127, w.N - 128], np.int64)   # largest |x|
     idx = np.unique(np.concatenate([idx, corners]))
     return idx, oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD, idx=idx)
@@ -86,24 +95,49 @@ def test_fhd_128_radial_subset(mri, radial, radial_ref, trig):
     assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
 
 
+@pytest.fixture(scope="module")
+def q128():
+    return wl.make_workload("q_128")
+
+
+@pytest.fixture(scope="module")
+def q128_ref(mri, q128):
+    """One voxel from every CTA block of the full-size launch (1,024 blocks)."""
+    w = q128
+    idx = plan_blocks(mri, "q", w, 103)
+    return idx, oracle.q(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
+
+
 @pytest.mark.parametrize("trig", TRIGS)
-def test_q_128_subset(mri, trig):
-    w = wl.make_workload("q_128")
+def test_q_128_subset(mri, q128, q128_ref, trig):
+    w = q128
     args = [dev(a) for a in (w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi)]
     r, i = mri.q(*args, trig=trig)
-    idx = wl.voxel_subset(w.N, 256, 103)
-    ref = oracle.q(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, idx=idx)
+    idx, ref = q128_ref
     assert oracle.rel_l2(cplx(r, i)[idx], ref) <= TOL[trig]
 
 
+@pytest.fixture(scope="module")
+def batched128():
+    return wl.make_workload("fhd_batched_128")
+
+
+@pytest.fixture(scope="module")
+def batched128_ref(mri, batched128):
+    """One voxel from every CTA block of the coil-group launch (2,048 blocks),
+    all eight coils."""
+    w = batched128
+    idx = plan_blocks(mri, "fhd_batched", w, 104, B=8)
+    return idx, oracle.fhd_batched(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD,
+                                   w.iD, idx=idx)
+
+
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
-def test_batched_128_subset(mri, trig):
-    w = wl.make_workload("fhd_batched_128")
+def test_batched_128_subset(mri, batched128, batched128_ref, trig):
+    w = batched128
     r, i = mri.fhd_batched(*fhd_inputs(w), trig=trig)
     assert tuple(r.shape) == (8, w.N)
-    idx = wl.voxel_subset(w.N, 96, 104)
-    ref = oracle.fhd_batched(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD,
-                             idx=idx)
+    idx, ref = batched128_ref
     got = cplx(r, i)[:, idx]
     assert oracle.rel_l2(got, ref) <= TOL[trig]
     for b in range(8):                       # every coil, not just the total

@@ -19,6 +19,17 @@ def test_ffma_probe(mri):
     assert 32.0 < r["per_sm_per_clk"] <= 130.0
 
 
+def test_ffma2_and_sfu_probes(mri):
+    """Packed pairs deliver (at most) the FMA pipe's 128 results per SM per
+    clock, like scalar FMAs: the pair instruction saves issue slots, not pipe
+    cycles.  The SFU gives 16 sin or cos per SM per clock."""
+    r2 = mri.microbench("ffma2", iters=1 << 10)["per_sm_per_clk"]
+    assert 32.0 < r2 <= 130.0
+    for probe in ("sin", "cos"):
+        r = mri.microbench(probe, iters=1 << 10)["per_sm_per_clk"]
+        assert 8.0 < r <= 17.0, probe
+
+
 @pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_mma_probe(mri, mode):
     """12 MMAs of 128 x 256 x 16 per 32 x 128 x 128 tile: at most 8192 f16

@@ -37,11 +37,39 @@ def coef():
     return parse()["Quarter"]
 
 
-def test_header_matches_generator(coef):
-    (name, pt, qt), = gen.SETS
-    P, Q = gen.fit(pt, qt)
-    assert [gen.f32(c) for c in P] == coef["P"]
-    assert [gen.f32(c) for c in Q] == coef["Q"]
+@pytest.fixture(scope="module")
+def half():
+    return parse()["Half"]
+
+
+def test_header_matches_generator():
+    sets = parse()
+    assert sorted(sets) == sorted(name for name, *_ in gen.SETS)
+    for name, pt, qt, turn in gen.SETS:
+        P, Q = gen.fit(pt, qt, turn)
+        assert [gen.f32(c) for c in P] == sets[name]["P"], name
+        assert [gen.f32(c) for c in Q] == sets[name]["Q"], name
+
+
+def test_half_turn_max_and_mean_error(half):
+    """The general gather's sequence (half-turn reduction, Horner, sign flip
+    by the parity of the half turn) over 32 turns either way."""
+    u = np.linspace(-64.0, 64.0, 400001).astype(np.float32)
+    sn, cs = gen.half_turn_sincos32(half["P"], half["Q"], u)
+    x = np.pi * u.astype(np.float64)
+    es = sn.astype(np.float64) - np.sin(x)
+    ec = cs.astype(np.float64) - np.cos(x)
+    assert np.abs(es).max() <= 1.5e-7 and np.abs(ec).max() <= 3e-7
+    assert abs(es.mean()) <= 2e-9 and abs(ec.mean()) <= 2e-9
+
+
+def test_whole_half_turns_are_exact(half):
+    """A phase of a whole number of half turns (0 in particular) gives sin 0 and
+    cos +-1 exactly: the cos series' constant term is 1 and f = 0."""
+    u = np.array([0.0, 1.0, -1.0, 2.0, -3.0, 2e6, 2e6 + 1], np.float32)
+    sn, cs = gen.half_turn_sincos32(half["P"], half["Q"], u)
+    assert np.all(sn == 0.0)
+    assert np.all(cs == np.where(u.astype(np.int64) % 2 == 0, 1.0, -1.0))
 
 
 def test_max_and_mean_error(coef):

@@ -4,17 +4,24 @@ Callers with a fixed, fully reserved device-memory budget, real-time loops
 that must not wait on an allocator, or frameworks that own every allocation
 cannot let a library allocate scratch.  mri_fhd_noalloc runs the same kernels
 as mri_fhd with its scratch in a fixed array inside the library.  These tests
-call it through the C ABI and check it against mri_fhd, twice in a row on
-different problems (the array keeps the previous call's contents), with the
-tolerances the parity tests use.
+call it through the C ABI and check it against mri_fhd and against the fp64
+oracle on a voxel subset, on calls in a row on different problems (the array
+keeps the previous call's contents), with the tolerances the parity tests
+use; that the 64^3 workload runs with split samples and the 128^3 one
+unsplit (both layouts of the array are used); and, in a fresh process, that
+calls leave the device's free memory unchanged.
 """
 
 import ctypes
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from non_cartesian_mri_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -60,7 +67,26 @@ def rel(a, b):
     return float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(b))
 
 
-def test_matches_mri_fhd_on_calls_in_a_row(api):
+SCRATCH = 32 * 1024 * 1024          # MRI_FHD_NOALLOC_SCRATCH_BYTES
+RECORD_TILE_BYTES = 6 * 2 * 256 * 4  # one tile of F^H D records: 6 fields, each value twice
+
+
+def noalloc_splits(mri, M, N):
+    """The sample splits mri_fhd_noalloc runs with: mri_fhd's plan, capped to
+    the partial sums that fit in the fixed array after the records."""
+    p = mri.plan("fhd", M, N)
+    rec = -(-(p["tiles"] * RECORD_TILE_BYTES) // 256) * 256
+    return max(1, min(p["splits"], (SCRATCH - rec) // (8 * N)))
+
+
+def test_both_layouts_of_the_array_are_used(api):
+    mri, _ = api
+    w64, w128 = wl.make_workload("fhd_64"), wl.make_workload("fhd_128_radial")
+    assert noalloc_splits(mri, w64.M, w64.N) > 1      # records, then split partial sums
+    assert noalloc_splits(mri, w128.M, w128.N) == 1   # records only, unsplit
+
+
+def test_matches_mri_fhd_and_oracle_on_calls_in_a_row(api):
     mri, f = api
     # 128^3 (runs unsplit in the fixed array), then 64^3 (split), then 128^3 again
     for name, trig in (("fhd_128_radial", "accurate"), ("fhd_64", "fast"),
@@ -73,7 +99,63 @@ def test_matches_mri_fhd_on_calls_in_a_row(api):
         torch.cuda.synchronize()
         assert torch.isfinite(out[0]).all() and torch.isfinite(out[1]).all()
         assert rel(out, ref) <= TOL[trig], name
+        idx = wl.voxel_subset(w.N, 256, 401)
+        exact = oracle.fhd(w.kx, w.ky, w.kz, w.x, w.y, w.z, w.rPhi, w.iPhi, w.rD, w.iD,
+                           idx=idx)
+        got = (out[0].cpu().numpy().astype(np.float64)
+               + 1j * out[1].cpu().numpy().astype(np.float64))[idx]
+        assert oracle.rel_l2(got, exact) <= TOL[trig], name
     assert mri.device_errors(clear=True) == 0
+
+
+_FRESH = r"""
+import ctypes, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import non_cartesian_mri_gb300 as mri
+from non_cartesian_mri_gb300 import workloads as wl
+P, I64 = ctypes.c_void_p, ctypes.c_int64
+f = mri.load().mri_fhd_noalloc
+f.argtypes = [P] * 10 + [I64, I64, P, P, ctypes.c_int, ctypes.c_int, P]
+f.restype = ctypes.c_int
+def call(w, t, out):
+    s = P(torch.cuda.current_stream().cuda_stream)
+    return f(*[P(a.data_ptr()) for a in t], w.M, w.N, P(out[0].data_ptr()),
+             P(out[1].data_ptr()), 1, 0, s)
+def prob(M, N, seed):
+    a = wl.random_fhd_inputs(M, N, seed=seed)
+    class W: pass
+    w = W(); w.M, w.N = M, N
+    t = [torch.from_numpy(a[k]).cuda() for k in ("kx", "ky", "kz", "x", "y", "z", "rPhi",
+                                                  "iPhi", "rD", "iD")]
+    return w, t, (torch.empty(N, device="cuda"), torch.empty(N, device="cuda"))
+# every tensor is allocated before the first measurement
+small = [prob(300, 1000, 1), prob(256 * 64, 1000, 2)]
+big = [prob(200000, 300000, 3), prob(20000, 200000, 4)]
+torch.cuda.synchronize()
+for w, t, o in small:                 # first calls: set-up, kernels loaded
+    assert call(w, t, o) == 0
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+for w, t, o in big + big:             # larger problems: a pool would have to grow
+    assert call(w, t, o) == 0
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+print("FREE", free0, free1)
+assert free1 == free0, (free0, free1)
+"""
+
+
+def test_no_device_memory_taken_in_a_fresh_process(api):
+    """In a process that never called mri_fhd (so the library's pool does not
+    exist), calls larger than the warm-up ones leave the device's free
+    memory exactly unchanged: no allocation, and no pool behind the scenes."""
+    mri, _ = api
+    assert noalloc_splits(mri, 256 * 64, 1000) > 1      # the warm-up loads the split path
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
 
 
 def test_accumulate_and_ragged(api):
@@ -90,7 +172,7 @@ def test_accumulate_and_ragged(api):
 
 def test_rejects_M_beyond_the_fixed_array(api):
     _, f = api
-    limit = (32 * 1024 * 1024) // 5120 * 256           # samples whose records fit
+    limit = SCRATCH // RECORD_TILE_BYTES * 256          # samples whose records fit
     fake = [P(0x100000 + 256 * i) for i in range(12)]  # never dereferenced
     stream = P(torch.cuda.current_stream().cuda_stream)
     assert f(*fake[:10], limit + 1, 100, fake[10], fake[11], 0, 0, stream) == MRI_ERR_SIZE
