@@ -395,20 +395,30 @@ __global__ void __launch_bounds__(PairShape::THREADS, PairShape::MIN_BLOCKS)
 
 // ---------------------------------------------------------------------------
 // Coil groups (batched F^H D): one sin/cos per voxel-sample pair shared by BC
-// coils, 4 packed fmas per coil and voxel pair.  Records: kx ky kz, rMu_b,
-// iMu_b (b < BC), every value twice; -sin is formed once per voxel pair and
-// sample and shared by the coils.  The tile's partial sums are added into the
-// outputs (or split partials) in global memory once per tile, so the register
-// file holds only the partials of the tile.
+// coils, 4 packed fmas per coil and voxel pair.  Records: per sample, 2 + BC
+// 16-byte entries, (kx kx ky ky), (kz kz 0 0), then (rMu_b rMu_b iMu_b iMu_b)
+// for each coil: one broadcast LDS.128 per coil gives both of its weights as
+// packed operands.  -sin is formed once per voxel pair and sample and shared
+// by the coils.  The tile's partial sums are added into the outputs (or split
+// partials) in global memory once per tile, so the register file holds only
+// the partials of the tile.
 // ---------------------------------------------------------------------------
 #ifndef MRI_COIL_PAIRS
 #define MRI_COIL_PAIRS 2
 #endif
+// samples per step of the sample loop (measured: two help the accurate
+// path, 4,612 -> 4,687 Gpair-coils/s, and hurt the fast one, 6,360 -> 5,698)
+#ifndef MRI_COIL_UNROLL_ACCURATE
+#define MRI_COIL_UNROLL_ACCURATE 2
+#endif
+#ifndef MRI_COIL_UNROLL_FAST
+#define MRI_COIL_UNROLL_FAST 1
+#endif
 
 template <int BC>
 struct PairCoilRec {
-    static constexpr int F = 3 + 2 * BC;
-    static constexpr int TILE_FLOATS = F * 2 * kTile;
+    static constexpr int Q4 = 2 + BC;                 // 16-byte entries per sample
+    static constexpr int TILE_FLOATS = kTile * 4 * Q4;
     static constexpr uint32_t TILE_BYTES = TILE_FLOATS * 4u;
 };
 
@@ -419,7 +429,7 @@ struct PairCoilShape {
     static constexpr int V = 2 * VP;
     static constexpr int MIN_BLOCKS = 2;
     static constexpr int VOXELS_PER_CTA = THREADS * V;
-    // two CTAs per SM: eight coils (38 KB tiles) keep two stages
+    // two CTAs per SM: eight coils (40 KB tiles) keep two stages
     static constexpr int STAGES = BC >= 8 ? 2 : kStages;
     static constexpr size_t SMEM = size_t(STAGES) * PairCoilRec<BC>::TILE_BYTES;
 };
@@ -431,29 +441,29 @@ __global__ void __launch_bounds__(256) prep_pair_coil_records_kernel(PrepParams 
     const int64_t total = p.ntiles * kTile;
     for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < total;
          m += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t tile = m / kTile;
-        const int j = int(m - tile * kTile);
-        float f[R::F];
+        float4 e[R::Q4];
 #pragma unroll
-        for (int i = 0; i < R::F; ++i) f[i] = 0.0f;
+        for (int i = 0; i < R::Q4; ++i) e[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (m < p.M) {
-            f[0] = p.kx[m] * p.kscale;
-            f[1] = p.ky[m] * p.kscale;
-            f[2] = p.kz[m] * p.kscale;
+            const float kx = p.kx[m] * p.kscale, ky = p.ky[m] * p.kscale;
+            const float kz = p.kz[m] * p.kscale;
+            e[0] = make_float4(kx, kx, ky, ky);
+            e[1] = make_float4(kz, kz, 0.f, 0.f);
             const float rp = p.rPhi[m], ip = p.iPhi[m];
 #pragma unroll
             for (int b = 0; b < BC; ++b) {
                 if (b < p.coils_valid) {
                     const float rd = p.rD[(p.b0 + b) * p.M + m];
                     const float id = p.iD[(p.b0 + b) * p.M + m];
-                    f[3 + b] = fmaf(ip, id, rp * rd);               // Re conj(Phi) D
-                    f[3 + BC + b] = fmaf(-ip, rd, rp * id);         // Im conj(Phi) D
+                    const float rm = fmaf(ip, id, rp * rd);         // Re conj(Phi) D
+                    const float im = fmaf(-ip, rd, rp * id);        // Im conj(Phi) D
+                    e[2 + b] = make_float4(rm, rm, im, im);
                 }
             }
         }
-        float2* base = reinterpret_cast<float2*>(p.rec + tile * R::TILE_FLOATS) + j;
+        float4* dst = reinterpret_cast<float4*>(p.rec) + m * R::Q4;   // tiles are contiguous
 #pragma unroll
-        for (int i = 0; i < R::F; ++i) base[i * kTile] = make_float2(f[i], f[i]);
+        for (int i = 0; i < R::Q4; ++i) dst[i] = e[i];
     }
 }
 
@@ -465,7 +475,6 @@ __global__ void __launch_bounds__(256, 2) gather_pair_coils_kernel(GatherParams 
     constexpr int VP = S::VP;
     constexpr int T = S::THREADS;
     constexpr int KS = S::STAGES;
-    constexpr int FS = 2 * kTile;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float* const ring = reinterpret_cast<float*>(smem_raw);
@@ -522,10 +531,13 @@ __global__ void __launch_bounds__(256, 2) gather_pair_coils_kernel(GatherParams 
             for (int b = 0; b < BC; ++b) pr[i][b] = pi[i][b] = f2_splat(0.0f);
 
         if (ok) {
-#pragma unroll 1
+            constexpr int kUnroll =
+                TRIG == TRIG_ACCURATE ? MRI_COIL_UNROLL_ACCURATE : MRI_COIL_UNROLL_FAST;
+#pragma unroll kUnroll
             for (int j = 0; j < kTile; ++j) {
-                const f2* rec = reinterpret_cast<const f2*>(tile) + j;   // field f at rec[f * kTile]
-                const f2 kx = rec[0], ky = rec[kTile], kz = rec[2 * kTile];
+                const ulonglong2* rec = reinterpret_cast<const ulonglong2*>(tile) + j * R::Q4;
+                const ulonglong2 kxy = rec[0], kzz = rec[1];
+                const f2 kx = kxy.x, ky = kxy.y, kz = kzz.x;
                 f2 sn[VP], cs[VP], ns[VP];
 #pragma unroll
                 for (int i = 0; i < VP; ++i) {
@@ -535,7 +547,8 @@ __global__ void __launch_bounds__(256, 2) gather_pair_coils_kernel(GatherParams 
                 }
 #pragma unroll
                 for (int b = 0; b < BC; ++b) {
-                    const f2 rm = rec[(3 + b) * kTile], im = rec[(3 + BC + b) * kTile];
+                    const ulonglong2 w = rec[2 + b];
+                    const f2 rm = w.x, im = w.y;
 #pragma unroll
                     for (int i = 0; i < VP; ++i) {
                         // (rMu + i iMu)(cos + i sin)
