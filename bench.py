@@ -349,6 +349,9 @@ TRAFFIC_SOURCES = {
                                       "gather_grid_tc_fwd.cuh", "kernels_grid_tc.cu"),
     "toeplitz": ("fft.cuh", "kernels_toeplitz.cu"),
     "gridding": ("fft.cuh", "kernels_gridding.cu"),
+    # the general gather on pairs of floats (F^H D, Q, the forward model)
+    "pair": ("ptx.cuh", "gather.cuh", "gather_pair.cuh", "sincospi_coeffs.h",
+             "kernels_single.cu", "mri_abi.cu"),
 }
 
 
@@ -427,7 +430,9 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
            "peak": round(peak, 2),
            "unit": "G" + ops["unit"] + "s/s",
            "frac": round(achieved / peak, 4),
-           "traffic": profiled_traffic(akind if grid else kind, trig, w.name),
+           "traffic": profiled_traffic(akind if grid else
+                                       ("pair" if kind in ("fhd", "q") else kind), trig,
+                                       w.name),
            "peak_basis": basis,
            "gather_ms_per_launch": round(per_launch * 1e3, 3)}
     if sm_mhz:
