@@ -86,7 +86,7 @@ template <int TRIG>
 __device__ __forceinline__ void table_sincos(float ph, float& s, float& c)
 {
     if (TRIG == TRIG_ACCURATE) {
-        sincos_quarter_turns(ph, s, c);          // records hold 4k: quarter turns
+        sincos_half_turns(ph, s, c);             // records hold 2k: half turns
     } else if (TRIG == TRIG_FAST) {
         __sincosf(ph, &s, &c);                   // records hold 2 pi k: radians
     } else {

@@ -51,6 +51,12 @@
 
 #include "gather_grid_tc.cuh"
 
+// Accurate A generation on pairs of samples (.f32x2) when the Ey table is
+// not used (narrow or folded grids, ny not a multiple of 128).
+#ifndef MRI_TC_PACKED_A
+#define MRI_TC_PACKED_A 1
+#endif
+
 namespace mri {
 
 constexpr int kWsGenWarps = 8;                        // two warpgroups
@@ -373,6 +379,21 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                             const float2 e = ey[(s0 + s8) * kTcRows + ra];
                             ar[s8] = fmaf(fr, e.x, -fi * e.y);
                             ai[s8] = fmaf(fr, e.y, fi * e.x);
+                        }
+                    } else if constexpr (BC == 1 && TRIG == TRIG_ACCURATE && MRI_TC_PACKED_A) {
+                        // the polynomial on pairs of samples (.f32x2)
+                        float ky[8], kz[8];
+                        tc_load8(rec, 1, s0, ky);
+                        tc_load8(rec, 2, s0, kz);
+                        const f2 y2 = f2_splat(yz.x), z2 = f2_splat(yz.y);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const f2 ph = f2_fma(f2_pack(kz[2 * h], kz[2 * h + 1]), z2,
+                                                 f2_mul(f2_pack(ky[2 * h], ky[2 * h + 1]), y2));
+                            f2 sn, cs;
+                            sincos_half_turns2(ph, sn, cs);
+                            f2_unpack(sn, ai[2 * h], ai[2 * h + 1]);
+                            f2_unpack(cs, ar[2 * h], ar[2 * h + 1]);
                         }
                     } else if constexpr (BC == 1) {
                         float ky[8], kz[8];

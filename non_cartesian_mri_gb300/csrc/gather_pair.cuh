@@ -124,45 +124,6 @@ __global__ void __launch_bounds__(256) prep_pair_records_kernel(PrepParams p)
     }
 }
 
-__device__ __forceinline__ void f2_halves(f2 v, uint32_t& lo, uint32_t& hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ f2 f2_from_halves(uint32_t lo, uint32_t hi)
-{
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-
-// sin and cos of pi u for a pair of phases u in half turns (|u| < 2^22):
-// f = u - rint(u) exactly (adding and removing 1.5 * 2^23 rounds to an
-// integer q and leaves it in the low mantissa bits of the sum), the
-// polynomials of pi f, and the sign (-1)^q.
-__device__ __forceinline__ void sincos_half_turns2(f2 u, f2& s, f2& c)
-{
-    using Coef = SinCosHalf;
-    const f2 magic = f2_splat(12582912.0f);
-    const f2 v = f2_add(u, magic);
-    const f2 f = f2_sub(u, f2_sub(v, magic));
-    const f2 f2sq = f2_mul(f, f);
-    f2 p = f2_splat(Coef::P(Coef::P_TERMS - 1));
-#pragma unroll
-    for (int i = Coef::P_TERMS - 2; i >= 0; --i) p = f2_fma(p, f2sq, f2_splat(Coef::P(i)));
-    f2 q = f2_splat(Coef::Q(Coef::Q_TERMS - 1));
-#pragma unroll
-    for (int i = Coef::Q_TERMS - 2; i >= 0; --i) q = f2_fma(q, f2sq, f2_splat(Coef::Q(i)));
-    const f2 sf = f2_mul(f, p);
-    uint32_t vl, vh, sl, sh, cl, ch;
-    f2_halves(v, vl, vh);
-    f2_halves(sf, sl, sh);
-    f2_halves(q, cl, ch);
-    const uint32_t ml = vl << 31, mh = vh << 31;   // bit 31 = parity of q
-    s = f2_from_halves(sl ^ ml, sh ^ mh);
-    c = f2_from_halves(cl ^ ml, ch ^ mh);
-}
-
 // sin and cos of (pi/2) u for a pair of phases u in quarter turns: the
 // reduction and polynomials packed (SinCosQuarter), then per half the
 // rotation by q quarter turns (odd q swaps sin and cos; the signs follow bits

@@ -217,7 +217,7 @@ mri_status check_mode(int trig, int accumulate)
 
 float kscale_for(int trig)
 {
-    if (trig == MRI_TRIG_ACCURATE) return 4.0f;                  // quarter turns
+    if (trig == MRI_TRIG_ACCURATE) return 2.0f;                  // half turns
     if (trig == MRI_TRIG_FAST) return 6.28318530717958647692f;   // radians
     return 1.0f;                                                 // turns
 }
