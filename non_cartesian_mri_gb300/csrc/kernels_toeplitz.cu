@@ -363,6 +363,206 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
     }
 }
 
+// ---- the strided stages (y forward, z, y inverse) as persistent CTAs.
+// Loaded one tile at a time, these stages leave DRAM mostly idle (ncu at
+// 128^3: 31-36 % of its cycles active, the warps waiting on their loads):
+// each CTA loads, transforms, then stores.  Here each CTA walks over the
+// tiles g = blockIdx.x, + gridDim.x, ... and copies the inputs of its next
+// tile (the work lines' loaded positions, and in the z stage the spectrum)
+// into a second shared-memory buffer with cp.async while it transforms the
+// current one, so the copies are in flight during the passes.  The staged
+// values sit at [position][line] (the W lines of a tile are adjacent in
+// memory at every position), read back by the first pass as the loads of
+// toeplitz_stage_kernel read global memory.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// positions of a line the stage loads (complex; the spectrum: all L, z only)
+template <int STAGE, int LOG2L>
+__host__ __device__ constexpr int strided_cpos() { return STAGE == kYInv ? 1 << LOG2L : 1 << (LOG2L - 1); }
+template <int STAGE, int LOG2L>
+__host__ __device__ constexpr int strided_kpos() { return STAGE == kZConv ? 1 << LOG2L : 0; }
+// bytes of one staging buffer
+template <int STAGE, int LOG2L>
+__host__ __device__ constexpr size_t strided_stage_bytes()
+{
+    return (size_t(strided_cpos<STAGE, LOG2L>()) * 8 + size_t(strided_kpos<STAGE, LOG2L>()) * 4)
+           << fft_log2_lines(LOG2L);
+}
+template <int STAGE, int LOG2L>
+size_t strided_smem_total()
+{
+    return fft_smem_total(LOG2L) + 2 * strided_stage_bytes<STAGE, LOG2L>();
+}
+
+// CTAs per SM the persistent kernels are compiled for: two up to L = 256
+// (about 100 KB of shared memory each), then one
+__host__ __device__ constexpr int strided_min_ctas(int log2L) { return log2L <= 8 ? 2 : 1; }
+
+template <int STAGE, int LOG2L>
+__global__ void __launch_bounds__(kFftThreads, strided_min_ctas(LOG2L))
+    toeplitz_strided_kernel(ToeplitzArgs p, int64_t lines64, const float2* tw)
+{
+    static_assert(STAGE == kYFwd || STAGE == kZConv || STAGE == kYInv, "strided stages");
+    extern __shared__ float2 fft_sm[];
+    constexpr int log2W = fft_log2_lines(LOG2L);
+    constexpr int W = 1 << log2W;
+    constexpr int CPOS = strided_cpos<STAGE, LOG2L>();
+    constexpr int KPOS = strided_kpos<STAGE, LOG2L>();
+    constexpr size_t SB = strided_stage_bytes<STAGE, LOG2L>();
+    float2* const buf = fft_sm;
+    float2* const tws = fft_sm + (fft_line_stride(LOG2L) << log2W);
+    unsigned char* const stage0 =
+        reinterpret_cast<unsigned char*>(tws + (1 << LOG2L));   // 8-byte aligned
+    const uint32_t lines = uint32_t(lines64);
+    const uint32_t ngroups = (lines + W - 1) >> log2W;
+    const int log2Lx = p.log2nx + 1, log2Ly = p.log2ny + 1;
+    const float2 zero = make_float2(0.f, 0.f);
+    constexpr int RL = fft_last_log2r<LOG2L, true>();
+    constexpr int IL = fft_items(LOG2L, RL);
+    constexpr int per = fft_last_per<LOG2L, true>();
+    const int log2inner = STAGE == kZConv ? log2Lx + log2Ly : log2Lx;
+    const uint32_t imask = (1u << log2inner) - 1;
+    auto gidx = [&](uint32_t l, int j) -> uint32_t {
+        return ((((l >> log2inner) << LOG2L) + j) << log2inner) + (l & imask);
+    };
+    // the staged complex values and spectrum of a buffer
+    auto cst = [&](int b) { return reinterpret_cast<float2*>(stage0 + b * SB); };
+    auto kst = [&](int b) { return reinterpret_cast<float*>(stage0 + b * SB + size_t(CPOS) * 8 * W); };
+    // 16-byte copies when a tile's W lines are adjacent at every position
+    // (inner >= W and the tile whole), else one element per copy
+    const bool wide = (1u << log2inner) >= uint32_t(W);
+    auto prefetch = [&](uint32_t g, int b) {
+        const uint32_t l0 = g << log2W;
+        float2* const c = cst(b);
+        if (wide && l0 + W <= lines) {
+            for (int e = threadIdx.x; e < CPOS * W / 2; e += kFftThreads) {
+                const int w = (2 * e) & (W - 1), pos = (2 * e) >> log2W;
+                cp_async16(c + 2 * e, p.work + gidx(l0 + w, pos));
+            }
+        } else {
+            for (int e = threadIdx.x; e < CPOS * W; e += kFftThreads) {
+                const int w = e & (W - 1), pos = e >> log2W;
+                if (l0 + w < lines) cp_async8(c + e, p.work + gidx(l0 + w, pos));
+                else c[e] = zero;
+            }
+        }
+        if constexpr (KPOS > 0) {
+            float* const k = kst(b);
+            if (wide && l0 + W <= lines) {
+                for (int e = threadIdx.x; e < KPOS * W / 4; e += kFftThreads) {
+                    const int w = (4 * e) & (W - 1), pos = (4 * e) >> log2W;
+                    cp_async16(k + 4 * e, p.K + gidx(l0 + w, pos));
+                }
+            } else {
+                for (int e = threadIdx.x; e < KPOS * W; e += kFftThreads) {
+                    const int w = e & (W - 1), pos = e >> log2W;
+                    if (l0 + w < lines) cp_async4(k + e, p.K + gidx(l0 + w, pos));
+                    else k[e] = 0.f;
+                }
+            }
+        }
+    };
+    pdl_launch_dependents();
+    fft_stage_twiddles<LOG2L>(tws, tw);
+    pdl_wait();
+
+    int it = 0;
+    if (blockIdx.x < ngroups) prefetch(blockIdx.x, 0);
+    cp_async_commit();
+    for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (g + gridDim.x < ngroups) prefetch(g + gridDim.x, b ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();           // this tile's copies have landed
+        __syncthreads();              // everyone's, and the zeros written beside them
+        const uint32_t group = g << log2W;
+        const float2* const c = cst(b);
+        auto load = [&](int w, int pos) { return c[(pos << log2W) + w]; };
+        // the lower half of every line to work
+        auto store_half = [&](auto& y, auto rl, auto per_c) {
+            constexpr int R_ = decltype(rl)::value, PER = decltype(per_c)::value;
+#pragma unroll
+            for (int i2 = 0; i2 < fft_items(LOG2L, R_); ++i2) {
+                int w, j;
+                if (fft_item<LOG2L, R_, true>(i2, w, j) && group + w < lines) {
+#pragma unroll
+                    for (int q = 0; q < (1 << R_) / 2; ++q)
+                        p.work[gidx(group + w, j + q * PER)] = y[i2][q];
+                }
+            }
+        };
+        if constexpr (STAGE == kZConv) {
+            const float* const k = kst(b);
+            float kreg[IL][1 << RL];
+#pragma unroll
+            for (int i2 = 0; i2 < IL; ++i2) {
+                int w, j;
+                const bool on = fft_item<LOG2L, RL, true>(i2, w, j);
+#pragma unroll
+                for (int q = 0; q < (1 << RL); ++q)
+                    kreg[i2][q] = on ? k[((j + q * per) << log2W) + w] : 0.f;
+            }
+            fft_lines<false, LOG2L, true, true, true>(buf, tws, load, [&](auto& y) {
+#pragma unroll
+                for (int i2 = 0; i2 < IL; ++i2) {
+#pragma unroll
+                    for (int q = 0; q < (1 << RL); ++q)
+                        y[i2][q] = make_float2(y[i2][q].x * kreg[i2][q], y[i2][q].y * kreg[i2][q]);
+                    // the inverse transform's first pass (Ns = 1, no twiddles)
+                    fft_dft_regs<true, RL, false>(y[i2]);
+                }
+                constexpr int RI = fft_last_log2r<LOG2L, false>();
+                fft_run_from<true, LOG2L, false, true, 0>(buf, tws, y, [&](auto& yo) {
+                    store_half(yo, std::integral_constant<int, RI>{},
+                               std::integral_constant<int, fft_last_per<LOG2L, false>()>{});
+                });
+            });
+        } else if constexpr (STAGE == kYFwd) {
+            fft_lines<false, LOG2L, true, true, true>(buf, tws, load, [&](auto& y) {
+#pragma unroll
+                for (int i2 = 0; i2 < IL; ++i2) {
+                    int w, j;
+                    if (fft_item<LOG2L, RL, true>(i2, w, j) && group + w < lines) {
+#pragma unroll
+                        for (int q = 0; q < (1 << RL); ++q)
+                            p.work[gidx(group + w, j + q * per)] = y[i2][q];
+                    }
+                }
+            });
+        } else {
+            fft_lines<true, LOG2L, true, true, false>(buf, tws, load, [&](auto& y) {
+                store_half(y, std::integral_constant<int, RL>{}, std::integral_constant<int, per>{});
+            });
+        }
+        __syncthreads();              // this buffer is read; the next prefetch may refill it
+    }
+    cp_async_wait<0>();
+}
+
 // ---- conjugate gradients
 __global__ void __launch_bounds__(kDotThreads) dot_partial_kernel(const float* ar, const float* ai,
                                                                   const float* br, const float* bi,
@@ -569,12 +769,52 @@ cudaError_t fft_axis(float2* a, int log2L, int log2inner, int64_t lines, const f
     });
 }
 
+// Lines of at least 2^MRI_TOEPLITZ_PERSISTENT_LOG2L take the persistent
+// strided stages (measured: 256^3 grid, doubled grid 512^3, product 1.65 ->
+// 1.49 ms; 128^3 0.128 -> 0.129 ms, 64^3 0.042 -> 0.046: shorter lines
+// keep one tile per CTA, four CTAs per SM).
+#ifndef MRI_TOEPLITZ_PERSISTENT_LOG2L
+#define MRI_TOEPLITZ_PERSISTENT_LOG2L 9
+#endif
+
+// A strided stage as persistent CTAs (toeplitz_strided_kernel): as many as
+// fit on the SMs at once, at most one per tile.
+template <int STAGE, int LOG2L>
+cudaError_t launch_strided(const ToeplitzArgs& p, int64_t lines, const float2* tw, cudaStream_t s)
+{
+    auto kernel = toeplitz_strided_kernel<STAGE, LOG2L>;
+    const size_t smem = strided_smem_total<STAGE, LOG2L>();
+    if (!attributes_set(reinterpret_cast<const void*>(kernel))) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     int(cudaSharedmemCarveoutMaxShared));
+        if (e != cudaSuccess) return e;
+        mark_attributes_set(reinterpret_cast<const void*>(kernel));
+    }
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFftThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t W = int64_t(1) << fft_log2_lines(LOG2L);
+    const int64_t groups = (lines + W - 1) / W;
+    const int64_t grid = std::min<int64_t>(groups, int64_t(sms) * std::max(per_sm, 1));
+    return launch_pdl(kernel, unsigned(grid), kFftThreads, smem, s, p, lines, tw);
+}
+
 template <int STAGE>
 cudaError_t toeplitz_stage(const ToeplitzArgs& p, int log2L, int64_t lines, const float2* tw,
                            cudaStream_t s)
 {
     return launch_by_length(log2L, lines, s, [&](auto len, auto go) {
-        return go(toeplitz_stage_kernel<STAGE, decltype(len)::value>, p, lines, tw);
+        constexpr int L2 = decltype(len)::value;
+        if constexpr (STAGE != kXFwd && STAGE != kXInv && L2 >= MRI_TOEPLITZ_PERSISTENT_LOG2L)
+            return launch_strided<STAGE, L2>(p, lines, tw, s);
+        else
+            return go(toeplitz_stage_kernel<STAGE, L2>, p, lines, tw);
     });
 }
 
