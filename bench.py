@@ -60,6 +60,11 @@ ALGO_OPS = {
     "fhd": {"mufu": 2.0, "fp32": 7.0, "unit": "pair"},
     "q": {"mufu": 2.0, "fp32": 5.0, "unit": "pair"},
     "fhd_batched": {"mufu": 2.0 / 8, "fp32": 3.0 / 8 + 4.0, "unit": "pair-coil"},
+    # batched on the tensor cores (groups of 3-8 coils): the complex
+    # multiply-accumulate is a tensor-core product (8 flops per pair-coil,
+    # 3 f16 passes each: far from binding), the phase and the sin/cos of a
+    # pair stay on the SM, shared by the 8 coils of a group
+    "fhd_batched_tc": {"mufu": 2.0 / 8, "fp32": 3.0 / 8, "unit": "pair-coil"},
     "grid": {"mufu": 0.0, "fp32": 4.0, "unit": "pair"},
 }
 # The accurate paths evaluate sin and cos in software (the MUFU's ~2^-21
@@ -352,6 +357,9 @@ TRAFFIC_SOURCES = {
     # the general gather on pairs of floats (F^H D, Q, the forward model)
     "pair": ("ptx.cuh", "gather.cuh", "gather_pair.cuh", "sincospi_coeffs.h",
              "kernels_single.cu", "mri_abi.cu"),
+    # the batched general gather on the tensor cores
+    "coils_tc": _COMMON_SOURCES + ("gather_grid.cuh", "gather_grid_tc.cuh",
+                                   "gather_coils_tc.cuh", "kernels_coils_tc.cu"),
 }
 
 
@@ -409,6 +417,8 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
                                w.pairs * (w.B if kind == "fhd_batched" else 1))
     units = w.pairs * (w.B if kind == "fhd_batched" else 1)
     akind = "grid" if grid else kind
+    if kind == "fhd_batched" and not grid and plan and plan.get("tensor_cores"):
+        akind = "fhd_batched_tc"
     per_launch = res["gather_ms"] / max(res["gather_launches"], 1) / 1e3
     launches_per_step = res["gather_launches"] / len(res["step_ms"])
     achieved = units / launches_per_step / per_launch / 1e9
@@ -431,8 +441,9 @@ def roofline(kind, w, res, rates, sms, sm_max_mhz, sm_mhz, trig, grid=False, pla
            "unit": "G" + ops["unit"] + "s/s",
            "frac": round(achieved / peak, 4),
            "traffic": profiled_traffic(akind if grid else
-                                       ("pair" if kind in ("fhd", "q") else kind), trig,
-                                       w.name),
+                                       ("pair" if kind in ("fhd", "q") else
+                                        "coils_tc" if akind == "fhd_batched_tc" else kind),
+                                       trig, w.name),
            "peak_basis": basis,
            "gather_ms_per_launch": round(per_launch * 1e3, 3)}
     if sm_mhz:

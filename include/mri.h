@@ -358,6 +358,11 @@ typedef struct mri_plan {
     int fast_fp32_voxels;     /* general gather, fast trig: of voxels_per_thread, how many
                                  take sin/cos from the polynomial on the FMA pipe instead of
                                  the SFU (both units then share the trig work) */
+    int voxels_per_cta;       /* output voxels of one coil that one CTA covers, padding
+                                 included: threads_per_cta * voxels_per_thread on the per-pair
+                                 kernels, 128 on the tensor-core coil kernel (one voxel per
+                                 tensor-memory lane), grid rows per CTA * 128 columns on the
+                                 tensor-core grid kernels */
 } mri_plan;
 
 mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,

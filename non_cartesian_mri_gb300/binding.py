@@ -41,7 +41,8 @@ class _Plan(ctypes.Structure):
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
                 ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int),
-                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int)]
+                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int),
+                ("voxels_per_cta", ctypes.c_int)]
 
 
 def lib_path() -> str:

@@ -22,7 +22,7 @@ LIB = os.path.join(BUILD, "libmri.so")
 
 UNITS = ["mri_abi.cu", "kernels_single.cu", "kernels_coils.cu", "kernels_grid.cu",
          "kernels_grid_tc.cu", "kernels_toeplitz.cu", "kernels_gridding.cu", "microbench.cu",
-         "noalloc.cu"]
+         "noalloc.cu", "kernels_coils_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", INCLUDE, "-I", CSRC]

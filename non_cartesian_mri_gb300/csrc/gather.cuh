@@ -61,11 +61,14 @@ struct PrepParams {
     int64_t M;
     int64_t b0;
     int64_t ntiles;
-    float kscale;           // 4 (quarter turns), 2*pi (radians) or 1 (turns)
+    float kscale;           // 2 (half turns), 2*pi (radians) or 1 (turns)
     float* rec;
     // Optional: raised by atomicMax to the float bits of the largest
     // |w_r| + |w_i| over samples and coils; the caller zeroes it first.
     unsigned int* wbound = nullptr;
+    // With bound_per_coil, wbound holds one word per coil of the group and
+    // coil b's bound goes to wbound[b] (the caller zeroes BC words).
+    bool bound_per_coil = false;
     // Coils b0 .. b0 + coils_valid - 1 exist; the rest of a group get weight 0.
     int coils_valid = 1 << 30;
     // Phi == 1 (rPhi, iPhi unused): the weight is D itself (the forward model)
@@ -97,6 +100,9 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
     using R = Rec<BC, REALW, TILE>;
     const int64_t total = p.ntiles * TILE;
     float wmax = 0.0f;
+    float wcoil[BC];   // per coil (bound_per_coil)
+#pragma unroll
+    for (int b = 0; b < BC; ++b) wcoil[b] = 0.0f;
     for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < total;
          m += int64_t(gridDim.x) * blockDim.x) {
         const int64_t tile = m / TILE;
@@ -128,14 +134,24 @@ __global__ void __launch_bounds__(256) prep_records_kernel(PrepParams p)
                 wmax = fmaxf(wmax, fabsf(f[3]));
             } else {
 #pragma unroll
-                for (int b = 0; b < BC; ++b) wmax = fmaxf(wmax, fabsf(f[3 + b]) + fabsf(f[3 + BC + b]));
+                for (int b = 0; b < BC; ++b) {
+                    const float a = fabsf(f[3 + b]) + fabsf(f[3 + BC + b]);
+                    wmax = fmaxf(wmax, a);
+                    wcoil[b] = fmaxf(wcoil[b], a);
+                }
             }
         }
 #pragma unroll
         for (int i = 0; i < R::F; ++i) base[i * TILE + j] = f[i];
     }
-    if (p.wbound != nullptr) {
-        // non-negative floats order like their bit patterns (a NaN sorts last)
+    // non-negative floats order like their bit patterns (a NaN sorts last)
+    if (p.wbound != nullptr && !REALW && p.bound_per_coil) {
+#pragma unroll
+        for (int b = 0; b < BC; ++b) {
+            const unsigned int w = __reduce_max_sync(0xffffffffu, __float_as_uint(wcoil[b]));
+            if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(p.wbound + b, w);
+        }
+    } else if (p.wbound != nullptr) {
         const unsigned int w = __reduce_max_sync(0xffffffffu, __float_as_uint(wmax));
         if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(p.wbound, w);
     }

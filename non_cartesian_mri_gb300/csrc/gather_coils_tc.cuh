@@ -1,0 +1,335 @@
+// gather_coils_tc.cuh -- batched F^H D for arbitrary voxel coordinates on the
+// tensor cores: a group of up to 8 coils per launch.
+//
+// For a coil group the gather of Fig. 17.11 is, per voxel n and coil c,
+//   FhD_c[n] = sum_m E[n][m] Mu_c[m],   E[n][m] = e^{i 2 pi k_m . x_n}:
+// a complex matrix product (voxels x samples) by (samples x coils).  The
+// per-pair work that remains on the SM is E -- one sin/cos per voxel-sample
+// pair, shared by the coils -- and the multiply-accumulate of every coil goes
+// to the tensor core.  On the SIMT cores the multiply-accumulate (4 FP32
+// operations per pair and coil) binds; here the SFU (fast) or the FP32
+// polynomial (accurate) of E does, once per pair for all coils.
+//
+// A CTA owns 128 voxels (the MMA's M) and a range of the samples.  Per tile of
+// 32 samples its generator warps evaluate A = E (128 voxels x 32 samples),
+// split every value into f16 high and low parts, and store them to tensor
+// memory (thread = MMA row = voxel); B holds the group's weights,
+// S = [-Mu_i; Mu_r; Mu_i] (24 rows: 8 coils each, zero for absent coils),
+// built once per call into a table of operand tiles fetched by TMA; per K
+// step of 16 samples two N = 16 products go into D (16 columns: D_r of the 8
+// coils, then D_i):
+//   [D_r | D_i] += A_r [Mu_r | Mu_i] + A_i [-Mu_i | Mu_r],
+// each real product as hi*hi + hi*lo + lo*hi (the split-f16 scheme of the grid
+// kernels, gather_grid_tc.cuh; the weights of each coil are scaled by their
+// own power of two, so coils of very different magnitude keep full precision
+// each, and D's columns are scaled back per coil).  D is
+// folded into running sums in registers every block of tiles (blocked
+// summation).  Roles meet at mbarriers, every wait bounded: warps 0-7
+// generate A (warps 0-3 also fold D and write the outputs), warp 8 lane 0
+// issues the MMAs, warp 9 lane 0 copies the record and B tiles.  Two CTAs per
+// SM (256 tensor-memory columns each).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gather_grid_tc.cuh"
+
+namespace mri {
+
+constexpr int kCtRows = 128;                        // voxels per CTA = MMA M
+constexpr int kCtCoils = 8;                         // coils per launch (padded)
+constexpr int kCtN = 2 * kCtCoils;                  // D columns: D_r, D_i
+constexpr int kCtSRows = 3 * kCtCoils;              // S = [-Mu_i; Mu_r; Mu_i]
+constexpr int kCtPartBytes = (kCtSRows / 8) * 512;  // one f16 part of S: 1536 B
+constexpr int kCtBBytes = 2 * kCtPartBytes;         // hi, lo: 3 KB per tile
+constexpr int kCtFields = 3 + 2 * kCtCoils;         // record fields (grid-path layout)
+constexpr int kCtRecBytes = kCtFields * kTcTile * 4; // one record tile: 2,432 B
+constexpr int kCtKBytes = 3 * kTcTile * 4;          // its k fields: 384 B
+constexpr int kCtStages = 3;
+constexpr int kCtGenWarps = 8;
+constexpr int kCtThreads = 32 * kCtGenWarps + 64;   // + the MMA and copy warps
+constexpr uint32_t kCtTmemCols = 256;               // two CTAs per SM
+constexpr uint32_t kCtACol = 64;                    // A stages after D (columns 0-15)
+// Dynamic shared memory (operand rings) padded so that at most two CTAs fit an SM,
+// the number whose tensor-memory allocations fit together.
+constexpr size_t kCtSmem = 96 * 1024;
+static_assert(kCtACol + kCtStages * kTcAStageCols <= kCtTmemCols, "A stages fit");
+static_assert(size_t(kCtStages) * (kCtKBytes + kCtBBytes) <= kCtSmem, "rings fit");
+
+struct CoilTcParams {
+    const float* rec;               // grid-path records [tile][19][32] (k scaled, weights scaled)
+    const unsigned char* s_tab;     // B tiles, kCtBBytes each
+    const unsigned int* bounds;     // per coil: float bits of max |w_r| + |w_i| (its scale)
+    int64_t ntiles;
+    int splits;
+    const float *x, *y, *z;
+    int64_t N;
+    float* out_r;                   // coil c of split s at out + s * split_stride + c * coil_stride
+    float* out_i;
+    int64_t coil_stride;
+    int64_t split_stride;
+    int coils;                      // coils present (the rest of the 8 have weight 0)
+    int accumulate;
+    unsigned int* err;
+};
+
+// sin and cos of 8 phases (the records' trig units) into ar (cos) and ai (sin)
+template <int TRIG>
+__device__ __forceinline__ void ct_phase_trig8(const float (&kx)[8], const float (&ky)[8],
+                                               const float (&kz)[8], float x, float y, float z,
+                                               float (&ar)[8], float (&ai)[8])
+{
+    if constexpr (TRIG == TRIG_ACCURATE) {
+        // the polynomial on pairs of samples (.f32x2)
+        const f2 x2 = f2_splat(x), y2 = f2_splat(y), z2 = f2_splat(z);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const f2 ph = f2_fma(f2_pack(kz[2 * h], kz[2 * h + 1]), z2,
+                                 f2_fma(f2_pack(ky[2 * h], ky[2 * h + 1]), y2,
+                                        f2_mul(f2_pack(kx[2 * h], kx[2 * h + 1]), x2)));
+            f2 sn, cs;
+            sincos_half_turns2(ph, sn, cs);
+            f2_unpack(sn, ai[2 * h], ai[2 * h + 1]);
+            f2_unpack(cs, ar[2 * h], ar[2 * h + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            table_sincos<TRIG>(fmaf(kz[s], z, fmaf(ky[s], y, kx[s] * x)), ai[s], ar[s]);
+    }
+}
+
+template <int TRIG>
+__global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
+{
+    constexpr int kS = kCtStages;
+    constexpr int T = kTcTile;
+    constexpr uint32_t ID = umma_idesc_f16(kCtRows, kCtN);   // N = 16
+    constexpr int drain_tiles = (TRIG == TRIG_ACCURATE) ? kTcDrainAccurate : kTcDrainFast;
+    static_assert(drain_tiles >= kS, "at most one block waits for its fold");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* const bring = smem_raw;                          // B tiles
+    float* const kring = reinterpret_cast<float*>(smem_raw + kS * kCtBBytes);   // k fields
+    __shared__ __align__(8) uint64_t full_bar[kS];    // record k fields and B tile landed
+    __shared__ __align__(8) uint64_t a_full[kS];      // A written by every generator warp
+    __shared__ __align__(8) uint64_t mma_bar[kS];     // MMAs of the tile done
+    __shared__ __align__(8) uint64_t d_free;          // D folded (warps 0-3)
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    volatile int* const abort_flag = &abort_sh;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int split = blockIdx.y;
+    const int64_t t_begin = (p.ntiles * split) / p.splits;
+    const int64_t t_end = (p.ntiles * (split + 1)) / p.splits;
+    const int nt = int(t_end - t_begin);
+    const int64_t n0 = int64_t(blockIdx.x) * kCtRows;
+
+    if (warp == 0) tmem_alloc(&tmem_base_sh, kCtTmemCols);
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < kS; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&a_full[i], kCtGenWarps);
+            mbar_init(&mma_bar[i], 1);
+        }
+        mbar_init(&d_free, 4);
+        abort_sh = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == kCtGenWarps) {
+        if (lane == 0) {
+            // ---- MMA issue ----
+            int issued = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int st = t % kS;
+                const bool first = (t % drain_tiles) == 0;
+                bool ok = true;
+                // the first MMA of a block overwrites D: the previous block is folded
+                if (first && t > 0)
+                    ok = ws_wait(&d_free, uint32_t(t / drain_tiles - 1) & 1u, abort_flag);
+                if (ok) ok = ws_wait(&a_full[st], uint32_t(t / kS) & 1u, abort_flag);
+                if (ok) ok = ws_wait(&full_bar[st], uint32_t(t / kS) & 1u, abort_flag);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint64_t d0 = umma_desc_kmajor(bring + st * kCtBBytes, 128, 512);
+                const uint32_t acol = tmem + kCtACol + uint32_t(st) * kTcAStageCols;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    auto a = [&](int part) {
+                        return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
+                    };
+                    // the 16-row window of S at row r0 (8-row groups 512 B apart)
+                    auto sdesc = [&](int base, int r0) {
+                        return umma_desc_add(d0, uint32_t(base + (r0 / 8) * 512 + kb * 256));
+                    };
+                    const uint32_t acc0 = (first && kb == 0) ? 0u : 1u;
+                    // [D_r | D_i] += A_r [Mu_r | Mu_i]
+                    umma_f16_ta(tmem, a(A_RH), sdesc(0, 8), ID, acc0);
+                    umma_f16_ta(tmem, a(A_RH), sdesc(kCtPartBytes, 8), ID, 1u);
+                    umma_f16_ta(tmem, a(A_RL), sdesc(0, 8), ID, 1u);
+                    // [D_r | D_i] += A_i [-Mu_i | Mu_r]
+                    umma_f16_ta(tmem, a(A_IH), sdesc(0, 0), ID, 1u);
+                    umma_f16_ta(tmem, a(A_IH), sdesc(kCtPartBytes, 0), ID, 1u);
+                    umma_f16_ta(tmem, a(A_IL), sdesc(0, 0), ID, 1u);
+                }
+                umma_commit(&mma_bar[st]);
+                issued = t + 1;
+            }
+            // the MMAs issued finish before tensor memory is released
+            if (issued > 0 && !mbar_wait_bounded(&mma_bar[(issued - 1) % kS],
+                                                 uint32_t((issued - 1) / kS) & 1u))
+                atomicOr(p.err, DEVERR_DRAIN_TIMEOUT);
+            if (issued < nt) atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == kCtGenWarps + 1) {
+        if (lane == 0) {
+            // ---- copies: the k fields of record tile u and B tile u ----
+            int issued = 0;
+            for (int u = 0; u < nt; ++u) {
+                const int st = u % kS;
+                if (u >= kS &&
+                    !ws_wait(&mma_bar[st], uint32_t((u - kS) / kS) & 1u, abort_flag))
+                    break;
+                const int64_t tile = t_begin + u;
+                mbar_arrive_expect_tx(&full_bar[st], uint32_t(kCtKBytes + kCtBBytes));
+                tma_bulk_g2s(kring + st * 3 * T,
+                             reinterpret_cast<const unsigned char*>(p.rec) + tile * kCtRecBytes,
+                             uint32_t(kCtKBytes), &full_bar[st]);
+                tma_bulk_g2s(bring + st * kCtBBytes, p.s_tab + tile * kCtBBytes,
+                             uint32_t(kCtBBytes), &full_bar[st]);
+                issued = u + 1;
+            }
+            // copies still in flight land before shared memory is released
+            unsigned int bits = 0;
+            for (int u = issued > kS ? issued - kS : 0; u < issued; ++u)
+                if (!mbar_wait_bounded(&full_bar[u % kS], uint32_t(u / kS) & 1u))
+                    bits |= DEVERR_DRAIN_TIMEOUT;
+            if (issued < nt) bits |= DEVERR_TILE_WAIT_TIMEOUT;
+            if (bits) atomicOr(p.err, bits);
+        }
+        __syncwarp();
+    } else {
+        // ---- generators: thread = tensor-memory lane ra = voxel n0 + ra ----
+        const int ra = 32 * (warp & 3) + lane;
+        const int ah = warp >> 2;                     // samples 16 ah .. 16 ah + 15 of a tile
+        const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
+        const int64_t n = n0 + ra;
+        const bool in = n < p.N;
+        const float vx = in ? p.x[n] : 0.0f, vy = in ? p.y[n] : 0.0f, vz = in ? p.z[n] : 0.0f;
+        const bool folds = warp < 4;                  // warps 0-3 hold the running sums
+        float R[kCtN];
+#pragma unroll
+        for (int j = 0; j < kCtN; ++j) R[j] = 0.0f;
+        auto fold = [&](bool signal) {
+            tc_fence_after_sync();
+            float d[16];
+            tmem_ld16(tmem + lanes, d);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < kCtN; ++j) R[j] += d[j];
+            if (signal) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_free);
+            }
+        };
+
+        bool ok = true;
+        int pend = -1;   // last tile of a block whose D is not folded yet
+        for (int t = 0; t < nt && ok; ++t) {
+            const int st = t % kS;
+            if (folds && pend >= 0) {
+                const bool must = t - kS >= pend;
+                bool done = must ? ws_wait(&mma_bar[pend % kS], uint32_t(pend / kS) & 1u,
+                                           abort_flag)
+                                 : mbar_try_wait(&mma_bar[pend % kS], uint32_t(pend / kS) & 1u);
+                done = __all_sync(0xffffffffu, done);
+                if (must && !done) {
+                    ok = false;
+                } else if (done) {
+                    fold(true);
+                    pend = -1;
+                }
+            }
+            // the stage's previous A (tile t - kS) has been read; the k fields have landed
+            if (ok && t >= kS)
+                ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
+            if (ok) ok = ws_wait(&full_bar[st], uint32_t(t / kS) & 1u, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);   // the tensor-memory stores are .sync.aligned
+            if (!ok) break;
+            tc_fence_after_sync();
+            const float* kt = kring + st * 3 * T;
+            const uint32_t acol = tmem + lanes + kCtACol + uint32_t(st) * kTcAStageCols;
+#pragma unroll
+            for (int c = 0; c < kTcAChunks; ++c) {
+                const int s0 = 8 * (kTcAChunks * ah + c);
+                float kx[8], ky[8], kz[8], ar[8], ai[8];
+                tc_load8(kt, 0, s0, kx);
+                tc_load8(kt, 1, s0, ky);
+                tc_load8(kt, 2, s0, kz);
+                ct_phase_trig8<TRIG>(kx, ky, kz, vx, vy, vz, ar, ai);
+                // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
+                const uint32_t col = acol + uint32_t(s0 / 2);
+                uint4 h, l;
+                tc_split8(ar, h, l);
+                tmem_st4(col + A_RH * kTcAPartCols, h);
+                tmem_st4(col + A_RL * kTcAPartCols, l);
+                tc_split8(ai, h, l);
+                tmem_st4(col + A_IH * kTcAPartCols, h);
+                tmem_st4(col + A_IL * kTcAPartCols, l);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[st]);
+            if (t % drain_tiles == drain_tiles - 1 && t + 1 < nt) pend = t;
+        }
+        if (folds) {
+            // the block still waiting for its fold, then the last block
+            if (ok && pend >= 0) {
+                ok = __all_sync(0xffffffffu, ws_wait(&mma_bar[pend % kS],
+                                                     uint32_t(pend / kS) & 1u, abort_flag));
+                if (ok) fold(true);
+            }
+            if (ok && nt > 0) {
+                ok = __all_sync(0xffffffffu, ws_wait(&mma_bar[(nt - 1) % kS],
+                                                     uint32_t((nt - 1) / kS) & 1u, abort_flag));
+                if (ok) fold(false);
+            }
+            if (!ok) {
+                if (lane == 0) atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
+            } else if (nt > 0 && in) {
+                float* const out_r = p.out_r + split * p.split_stride;
+                float* const out_i = p.out_i + split * p.split_stride;
+#pragma unroll
+                for (int c = 0; c < kCtCoils; ++c) {
+                    if (c < p.coils) {
+                        const float inv_scale = exp2_int(-tc_scale_exp(p.bounds[c]));
+                        float* rp = out_r + c * p.coil_stride + n;
+                        float* ip = out_i + c * p.coil_stride + n;
+                        *rp = fmaf(R[c], inv_scale, p.accumulate ? *rp : 0.0f);
+                        *ip = fmaf(R[kCtCoils + c], inv_scale, p.accumulate ? *ip : 0.0f);
+                    }
+                }
+            }
+        } else if (!ok && lane == 0) {
+            atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, kCtTmemCols);
+}
+
+}  // namespace mri

@@ -13,6 +13,8 @@
 
 namespace mri {
 
+struct CoilTcParams;
+
 struct KernelShape {
     int threads;
     int v;                  // voxels per thread
@@ -117,5 +119,13 @@ cudaError_t launch_gather_single(bool realw, int trig, const GatherParams& p, di
 cudaError_t launch_gather_coils(int bc, int trig, const GatherParams& p, dim3 grid,
                                 cudaStream_t s);
 cudaError_t launch_prep_coils(int bc, const PrepParams& p, int grid, cudaStream_t s);
+// batched F^H D of up to 8 coils on the tensor cores (kernels_coils_tc.cu;
+// CoilTcParams in gather_coils_tc.cuh, which only the TUs that launch or fill
+// it include: its kernel's shared-memory alignment stays out of the others):
+// the weight tiles from the grid-path records of 8 coils and their 8 bound
+// words (each coil scaled by its own power of two), the kernel
+cudaError_t launch_build_mu_tiles(const float* rec, int64_t ntiles, const unsigned int* bounds,
+                                  unsigned char* s_tab, int grid, cudaStream_t s);
+cudaError_t launch_gather_coils_tc(int trig, const CoilTcParams& p, dim3 grid, cudaStream_t s);
 
 }  // namespace mri

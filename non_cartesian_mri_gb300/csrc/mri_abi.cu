@@ -10,6 +10,7 @@
 
 #include <cuda_runtime.h>
 
+#include "gather_coils_tc.cuh"
 #include "launch.h"
 #include "mri.h"
 
@@ -236,6 +237,129 @@ cudaEvent_t* timing_slot(DeviceState* d)
     return &d->ev[2 * i];
 }
 
+// scratch slot of the weight bound the tensor-core kernels scale by
+constexpr int64_t kBoundBytes = 256;
+
+#ifndef MRI_COILS_TC_MIN
+#define MRI_COILS_TC_MIN 3
+#endif
+// Batched F^H D: coil groups of at least this many coils (up to 8) run on the
+// tensor cores (coils_tc_kernel), smaller ones on the per-pair coil kernels.
+constexpr int kTcCoilsMin = MRI_COILS_TC_MIN;
+
+// Coils of a batched call that the per-pair kernels take: all of them without
+// tensor-core groups, else what is left after groups of 8 and one group of
+// the remainder when it has at least kTcCoilsMin coils.
+int64_t pair_coils(bool tc, int64_t B)
+{
+    if (!tc) return B;
+    const int64_t r = B % mri::kCtCoils;
+    return r >= kTcCoilsMin ? 0 : r;
+}
+
+bool use_coils_tc(bool realw, bool forward, int64_t B)
+{
+    return !realw && !forward && B >= kTcCoilsMin;
+}
+
+struct CoilTcPlan {
+    int64_t ntiles;
+    int64_t vblocks;
+    int splits;
+    int64_t rec_bytes;
+    int64_t s_bytes;
+    int64_t part_bytes;
+    int64_t scratch() const
+    {
+        return align256(rec_bytes) + kBoundBytes + align256(s_bytes) + part_bytes;
+    }
+};
+
+// nb: coils of the largest group (the partial sums of a split are per coil)
+CoilTcPlan plan_coils_tc(int64_t M, int64_t N, int sms, int nb)
+{
+    CoilTcPlan g{};
+    g.ntiles = ceil_div(M, mri::kTcTile);
+    g.vblocks = ceil_div(N, mri::kCtRows);
+    // a tile is ~0.5 us of a CTA (two per SM); filling and draining the
+    // operand pipeline costs a few tiles
+    g.splits = (g.ntiles > 0 && g.vblocks > 0)
+                   ? choose_splits(g.ntiles, g.vblocks, int64_t(sms > 0 ? sms : 1) * 2, nb, N,
+                                   0.5, 3.0)
+                   : 1;
+    g.rec_bytes = g.ntiles * int64_t(mri::kCtRecBytes);
+    g.s_bytes = g.ntiles * int64_t(mri::kCtBBytes);
+    g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
+    return g;
+}
+
+// One tensor-core coil group (coils b0 .. b0 + nb - 1, nb <= 8): records of 8
+// coils (absent ones weight 0) and a weight bound per coil, the weight tiles
+// (each coil scaled by its power of two), the gather, the reduction of the
+// splits.
+mri_status run_coils_tc_group(DeviceState* d, const CoilTcPlan& g, const float* kx,
+                              const float* ky, const float* kz, const float* x, const float* y,
+                              const float* z, const float* rPhi, const float* iPhi,
+                              const float* rD, const float* iD, int64_t b0, int nb, int64_t M,
+                              int64_t N, float* out_r, float* out_i, int trig, int accumulate,
+                              char* scratch, cudaStream_t s)
+{
+    float* rec = reinterpret_cast<float*>(scratch);
+    unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(g.rec_bytes));
+    unsigned char* s_tab =
+        reinterpret_cast<unsigned char*>(scratch + align256(g.rec_bytes) + kBoundBytes);
+    float* part = reinterpret_cast<float*>(scratch + align256(g.rec_bytes) + kBoundBytes +
+                                           align256(g.s_bytes));
+    mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, b0, g.ntiles, kscale_for(trig), rec};
+    pp.wbound = wbound;
+    pp.bound_per_coil = true;
+    pp.coils_valid = nb;
+    if (cudaMemsetAsync(wbound, 0, mri::kCtCoils * sizeof(unsigned int), s) != cudaSuccess ||
+        mri::launch_prep_grid_tc(false, mri::kCtCoils, pp,
+                                 grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess ||
+        mri::launch_build_mu_tiles(rec, g.ntiles, wbound, s_tab,
+                                   grid_for(g.ntiles * mri::kCtSRows * (mri::kTcTile / 8), d->sms),
+                                   s) != cudaSuccess)
+        return cuda_fail();
+
+    mri::CoilTcParams cp{};
+    cp.rec = rec;
+    cp.s_tab = s_tab;
+    cp.bounds = wbound;
+    cp.ntiles = g.ntiles;
+    cp.splits = g.splits;
+    cp.x = x;
+    cp.y = y;
+    cp.z = z;
+    cp.N = N;
+    cp.coils = nb;
+    cp.err = d->err;
+    if (g.splits == 1) {
+        cp.out_r = out_r + b0 * N;
+        cp.out_i = out_i + b0 * N;
+        cp.coil_stride = N;
+        cp.split_stride = 0;
+        cp.accumulate = accumulate;
+    } else {
+        // partials [split][coil][r / i][N], the reduction's layout
+        cp.out_r = part;
+        cp.out_i = part + N;
+        cp.coil_stride = 2 * N;
+        cp.split_stride = int64_t(nb) * 2 * N;
+        cp.accumulate = 0;
+    }
+    const dim3 grid(unsigned(g.vblocks), unsigned(g.splits), 1);
+    cudaEvent_t* ev = timing_slot(d);
+    if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) return cuda_fail();
+    if (mri::launch_gather_coils_tc(trig, cp, grid, s) != cudaSuccess) return cuda_fail();
+    if (ev && cudaEventRecord(ev[1], s) != cudaSuccess) return cuda_fail();
+    if (g.splits > 1 &&
+        mri::launch_reduce(part, g.splits, nb, N, out_r + b0 * N, out_i + b0 * N, N, accumulate,
+                           grid_for(int64_t(nb) * 2 * N, d->sms), s) != cudaSuccess)
+        return cuda_fail();
+    return MRI_OK;
+}
+
 // One gather (one coil group): prep records, gather, reduce splits.
 mri_status run_group(DeviceState* d, const GroupPlan& g, int sms, const float* kx, const float* ky,
                      const float* kz, const float* x, const float* y, const float* z,
@@ -329,10 +453,16 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
         }
         return MRI_OK;
     }
+    // tensor-core coil groups first (coils 0 .. B - rest - 1), then the
+    // per-pair groups of the rest
+    const bool tc = use_coils_tc(realw, forward, B);
+    const int64_t rest = pair_coils(tc, B);
+    CoilTcPlan tcp{};
+    if (tc) tcp = plan_coils_tc(M, N, d->sms, int(std::min<int64_t>(B - rest, mri::kCtCoils)));
     GroupPlan plans[4];
     bool used[4];
-    group_plans(realw, B, M, N, d->sms, plans, used);
-    int64_t scratch_bytes = 0;
+    group_plans(realw, rest, M, N, d->sms, plans, used);
+    int64_t scratch_bytes = tc ? tcp.scratch() : 0;
     for (int i = 0; i < 4; ++i) {
         const int64_t b = used[i] ? align256(plans[i].rec_bytes) + plans[i].part_bytes : 0;
         if (b > scratch_bytes) scratch_bytes = b;
@@ -344,6 +474,13 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
 
     mri_status st = MRI_OK;
     for (int64_t b0 = 0; b0 < B && st == MRI_OK;) {
+        if (b0 < B - rest) {
+            const int nb = int(std::min<int64_t>(B - rest - b0, mri::kCtCoils));
+            st = run_coils_tc_group(d, tcp, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, b0, nb, M,
+                                    N, out_r, out_i, trig, accumulate, scratch, s);
+            b0 += nb;
+            continue;
+        }
         const int i = realw ? 3 : group_index(B - b0);
         st = run_group(d, plans[i], d->sms, kx, ky, kz, x, y, z, rPhi, iPhi, rD, iD, b0, M, N,
                        out_r, out_i, trig, accumulate, scratch, d->err, s, forward);
@@ -356,9 +493,6 @@ mri_status run_gather_call(bool realw, int64_t B, const float* kx, const float* 
 // ---------------------------------------------------------------------------
 // separable grids
 // ---------------------------------------------------------------------------
-// scratch slot of the weight bound the tensor-core grid kernel scales by
-constexpr int64_t kBoundBytes = 256;
-
 struct GridPlan {
     bool tensor_cores;      // nx >= 8: the tcgen05 kernel; else coordinates
                             // expanded and the general kernel
@@ -952,6 +1086,7 @@ mri_status plan_grid_call(int kind, int64_t B, int64_t M, int nx, int ny, int nz
         if (i == 0) {
             // voxels whose running sums one generating thread holds
             plan->voxels_per_thread = mri::kTcRows * mri::kTcCols / mri::kTcThreads;
+            plan->voxels_per_cta = gi.rows_per_cta * mri::kTcCols;
             plan->splits = gi.splits;
             plan->voxel_ctas = gi.vblocks * gi.ncb;
             plan->grid_fold = gi.fold;
@@ -1190,19 +1325,41 @@ mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sm
         plan->launches = 2;   // zero fill of both outputs
         return MRI_OK;
     }
+    const bool tc = use_coils_tc(realw, false, B);
+    const int64_t rest = pair_coils(tc, B);
     GroupPlan plans[4];
     bool used[4];
-    group_plans(realw, B, M, N, num_sms, plans, used);
-    const GroupPlan& g0 = plans[realw ? 3 : group_index(B)];
-    plan->threads_per_cta = g0.shape.threads;
-    plan->voxels_per_thread = g0.shape.v;
-    plan->fast_fp32_voxels = g0.shape.fast_fp32_voxels;
-    plan->samples_per_tile = kTile;
-    plan->splits = g0.splits;
-    plan->voxel_ctas = g0.vblocks;
-    plan->tiles = g0.ntiles;
+    group_plans(realw, rest, M, N, num_sms, plans, used);
     int64_t scratch = 0;
-    for (int64_t b0 = 0; b0 < B;) {
+    if (tc) {
+        // the first group's shape: tensor cores, one voxel per tensor-memory
+        // lane (its 2 x 8 running sums in one thread)
+        const CoilTcPlan g = plan_coils_tc(M, N, num_sms, int(std::min<int64_t>(B - rest, 8)));
+        plan->threads_per_cta = mri::kCtThreads;
+        plan->voxels_per_thread = 1;
+        plan->voxels_per_cta = mri::kCtRows;
+        plan->samples_per_tile = mri::kTcTile;
+        plan->splits = g.splits;
+        plan->voxel_ctas = g.vblocks;
+        plan->tiles = g.ntiles;
+        plan->tensor_cores = 1;
+        for (int64_t b0 = 0; b0 < B - rest; b0 += mri::kCtCoils) {
+            plan->coil_groups += 1;
+            plan->launches += 3 + (g.splits > 1 ? 1 : 0);   // prep, tiles, gather
+        }
+        scratch = g.scratch();
+    } else {
+        const GroupPlan& g0 = plans[realw ? 3 : group_index(B)];
+        plan->threads_per_cta = g0.shape.threads;
+        plan->voxels_per_thread = g0.shape.v;
+        plan->voxels_per_cta = g0.shape.voxels_per_cta;
+        plan->fast_fp32_voxels = g0.shape.fast_fp32_voxels;
+        plan->samples_per_tile = kTile;
+        plan->splits = g0.splits;
+        plan->voxel_ctas = g0.vblocks;
+        plan->tiles = g0.ntiles;
+    }
+    for (int64_t b0 = B - rest; b0 < B;) {
         const int i = realw ? 3 : group_index(B - b0);
         plan->coil_groups += 1;
         plan->launches += 2 + (plans[i].splits > 1 ? 1 : 0);

@@ -122,7 +122,8 @@ class Plan(ctypes.Structure):
                 ("voxel_ctas", ctypes.c_int64), ("tiles", ctypes.c_int64),
                 ("coil_groups", ctypes.c_int), ("launches", ctypes.c_int),
                 ("scratch_bytes", ctypes.c_int64), ("tensor_cores", ctypes.c_int),
-                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int)]
+                ("grid_fold", ctypes.c_int), ("fast_fp32_voxels", ctypes.c_int),
+                ("voxels_per_cta", ctypes.c_int)]
 
 
 def plan(lib, kind, B, M, N, sms=152):
@@ -139,11 +140,18 @@ def test_plan_covers_every_voxel_and_sample(lib):
                           (2, 8, 524288, 128 ** 3), (0, 1, 32768, 64 ** 3),
                           (0, 1, 2048, 16 ** 3), (0, 1, 1, 1), (0, 1, 257, 2049)]:
         p = plan(lib, kind, B, M, N)
-        assert p.voxel_ctas * p.threads_per_cta * p.voxels_per_thread >= N
-        assert (p.voxel_ctas - 1) * p.threads_per_cta * p.voxels_per_thread < N
+        vpc = p.voxels_per_cta
+        if p.tensor_cores:
+            assert vpc == 128                       # one voxel per tensor-memory lane
+        else:
+            assert vpc == p.threads_per_cta * p.voxels_per_thread
+        assert p.voxel_ctas * vpc >= N > (p.voxel_ctas - 1) * vpc
         assert p.tiles * p.samples_per_tile >= M > (p.tiles - 1) * p.samples_per_tile
         assert 1 <= p.splits <= p.tiles
-        assert p.launches == p.coil_groups * 2 + (p.coil_groups if p.splits > 1 else 0)
+        # per group: prep and gather (tensor cores: also the weight tiles),
+        # and the reduction of split partials
+        per = 3 if p.tensor_cores else 2
+        assert p.launches == p.coil_groups * (per + (1 if p.splits > 1 else 0))
 
 
 def test_plan_splits_samples_when_voxels_underfill_the_gpu(lib):
@@ -157,9 +165,19 @@ def test_plan_splits_samples_when_voxels_underfill_the_gpu(lib):
 
 
 def test_plan_coil_groups(lib):
-    assert plan(lib, 2, 13, 1000, 5000).coil_groups == 3      # 8 + 4 + 1
+    # groups of 3..8 coils run on the tensor cores, 1 or 2 left over on the
+    # per-pair kernels
+    assert plan(lib, 2, 13, 1000, 5000).coil_groups == 2      # 8 + 5
     assert plan(lib, 2, 8, 1000, 5000).coil_groups == 1
     assert plan(lib, 2, 17, 1000, 5000).coil_groups == 3      # 8 + 8 + 1
+    assert plan(lib, 2, 10, 1000, 5000).coil_groups == 2      # 8 + 2
+    for B in (3, 5, 8):
+        p = plan(lib, 2, B, 1000, 5000)
+        assert p.tensor_cores == 1 and p.coil_groups == 1 and p.threads_per_cta == 320
+    for B in (1, 2):
+        p = plan(lib, 2, B, 1000, 5000)
+        assert p.tensor_cores == 0 and p.coil_groups == 1
+    assert plan(lib, 1, 1, 1000, 5000).tensor_cores == 0      # Q: the per-pair kernel
     p = plan(lib, 0, 1, 0, 100)
     assert p.launches == 2                                   # zero fill only
 
@@ -177,7 +195,11 @@ def test_batched_grid_plan_groups(lib):
         assert p.samples_per_tile * p.tiles >= 524288
     p = Plan()
     assert f(0, 1000, 128, 4, 4, 152, ctypes.byref(p)) == SIZE
-    assert f(3, 1000, 7, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 0
+    # nx < 8: expanded coordinates and the general batched path (3 coils: the
+    # tensor-core coil kernel, not the grid kernel; 1 coil: the per-pair kernel)
+    assert f(3, 1000, 7, 4, 4, 152, ctypes.byref(p)) == OK and p.threads_per_cta == 320
+    assert p.voxels_per_cta == 128 and p.voxel_ctas == 1
+    assert f(1, 1000, 7, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 0
     # nx >= 8 runs on the tensor cores, one CTA column per block of 128
     # columns (the last one padded)
     assert f(3, 1000, 8, 4, 4, 152, ctypes.byref(p)) == OK and p.tensor_cores == 1

@@ -76,3 +76,10 @@ def test_general_gather_roofline_follows_the_kernel():
     # batched, 8 coils: FP32-bound, 3/8 + 4 operations per pair-coil
     per, unit, _, _ = bench.peak_per_sm_clk("fhd_batched", None, "fast")
     assert abs(per - 128.0 / 4.375) < 1e-12 and unit == "fp32"
+    # batched on the tensor cores: the multiply-accumulate leaves the SM's
+    # pipes; 2 sin/cos (fast) or 3 + 13 FP32 operations (accurate) per pair,
+    # shared by 8 coils
+    per, unit, _, _ = bench.peak_per_sm_clk("fhd_batched_tc", None, "fast")
+    assert (per, unit) == (64.0, "mufu")
+    per, unit, _, _ = bench.peak_per_sm_clk("fhd_batched_tc", None, "accurate")
+    assert (per, unit) == (64.0, "fp32")

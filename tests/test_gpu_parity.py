@@ -60,7 +60,7 @@ def test_fhd_tiny_all_voxels(mri, trig):
 def plan_blocks(mri, kind, w, seed, per=1, B=1):
     """Voxels from every CTA block of the launch the call makes."""
     p = mri.plan(kind, w.M, w.N, B=B)
-    vpc = p["threads_per_cta"] * p["voxels_per_thread"]
+    vpc = p["voxels_per_cta"]
     assert p["voxel_ctas"] == -(-w.N // vpc)
     return gather_blocks(w.N, vpc, seed, per=per)
 
