@@ -13,21 +13,30 @@
 // A CTA owns 128 voxels (the MMA's M) and a range of the samples.  Per tile of
 // 32 samples its generator warps evaluate A = E (128 voxels x 32 samples),
 // split every value into f16 high and low parts, and store them to tensor
-// memory (thread = MMA row = voxel); B holds the group's weights,
-// S = [-Mu_i; Mu_r; Mu_i] (24 rows: 8 coils each, zero for absent coils),
-// built once per call into a table of operand tiles fetched by TMA; per K
-// step of 16 samples two N = 16 products go into D (16 columns: D_r of the 8
-// coils, then D_i):
-//   [D_r | D_i] += A_r [Mu_r | Mu_i] + A_i [-Mu_i | Mu_r],
-// each real product as hi*hi + hi*lo + lo*hi (the split-f16 scheme of the grid
-// kernels, gather_grid_tc.cuh; the weights of each coil are scaled by their
-// own power of two, so coils of very different magnitude keep full precision
-// each, and D's columns are scaled back per coil).  D is
-// folded into running sums in registers every block of tiles (blocked
-// summation).  Roles meet at mbarriers, every wait bounded: warps 0-7
-// generate A (warps 0-3 also fold D and write the outputs), warp 8 lane 0
-// issues the MMAs, warp 9 lane 0 copies the record and B tiles.  Two CTAs per
-// SM (256 tensor-memory columns each).
+// memory (thread = MMA row = voxel); B holds the group's weights (8 coils,
+// zero for absent ones), built once per call into a table of operand tiles
+// fetched by TMA.  The f16 parts of the weights lie along N: one MMA of
+// N = 32 multiplies one A part by the high and the low part of the weights
+// at once, into D = [D_r | D_i | D_r' | D_i'] (8 coils each; the fold adds
+// the primed low-part columns).  Per K step of 16 samples four products:
+//   D += A_r^hi W_r + A_r^lo W_r + A_i^hi W_i + A_i^lo W_i,
+//   W_r = [Mu_r^hi | Mu_i^hi | Mu_r^lo | Mu_i^lo],
+//   W_i = [-Mu_i^hi | Mu_r^hi | -Mu_i^lo | Mu_r^lo],
+// i.e. every product of the parts, lo*lo included (the split-f16 scheme of
+// the grid kernels, gather_grid_tc.cuh; the weights of each coil are scaled
+// by their own power of two, so coils of very different magnitude keep full
+// precision each, and D's columns are scaled back per coil).  W_r and W_i are
+// two windows of one tile of eight 8-row groups, taken with a stride of two
+// groups: [-Mu_i^hi, Mu_r^hi, Mu_r^hi, Mu_i^hi, -Mu_i^lo, Mu_r^lo, Mu_r^lo,
+// Mu_i^lo], W_i the even groups, W_r the odd ones.  The tensor core's time
+// per MMA at these small N follows the A operand it reads (about 64 bytes of
+// A per clock), so the fewer, wider products are the cheaper form: 8 MMAs
+// per tile where three N = 16 passes per part pair took 12.  D is folded
+// into running sums in registers every block of tiles (blocked summation).
+// Roles meet at mbarriers, every wait bounded: warps 0-7 generate A (warps
+// 0-3 also fold D and write the outputs), warp 8 lane 0 issues the MMAs,
+// warp 9 lane 0 copies the record and B tiles.  Two CTAs per SM (256
+// tensor-memory columns each).
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -38,23 +47,31 @@ namespace mri {
 
 constexpr int kCtRows = 128;                        // voxels per CTA = MMA M
 constexpr int kCtCoils = 8;                         // coils per launch (padded)
-constexpr int kCtN = 2 * kCtCoils;                  // D columns: D_r, D_i
-constexpr int kCtSRows = 3 * kCtCoils;              // S = [-Mu_i; Mu_r; Mu_i]
-constexpr int kCtPartBytes = (kCtSRows / 8) * 512;  // one f16 part of S: 1536 B
-constexpr int kCtBBytes = 2 * kCtPartBytes;         // hi, lo: 3 KB per tile
+constexpr int kCtN = 2 * kCtCoils;                  // D_r, D_i
+constexpr int kCtMmaN = 2 * kCtN;                   // MMA N: D_r, D_i and their low parts
+constexpr int kCtGroups = 8;                        // 8-row groups of a weight tile
+constexpr int kCtBBytes = kCtGroups * 512;          // one weight tile: 4 KB
 constexpr int kCtFields = 3 + 2 * kCtCoils;         // record fields (grid-path layout)
 constexpr int kCtRecBytes = kCtFields * kTcTile * 4; // one record tile: 2,432 B
 constexpr int kCtKBytes = 3 * kTcTile * 4;          // its k fields: 384 B
-constexpr int kCtStages = 3;
+constexpr int kCtStages = 3;                        // A stages (tensor memory)
+#ifndef MRI_CT_RING
+#define MRI_CT_RING 8
+#endif
+// Shared-memory stages of the copied k fields and weight tiles: more than the
+// A stages, so that the copies run far enough ahead to hide their latency
+// (a stage is refilled once the MMAs of the tile it held are done).
+constexpr int kCtRing = MRI_CT_RING;
 constexpr int kCtGenWarps = 8;
 constexpr int kCtThreads = 32 * kCtGenWarps + 64;   // + the MMA and copy warps
 constexpr uint32_t kCtTmemCols = 256;               // two CTAs per SM
-constexpr uint32_t kCtACol = 64;                    // A stages after D (columns 0-15)
+constexpr uint32_t kCtACol = 64;                    // A stages after D (columns 0-31)
 // Dynamic shared memory (operand rings) padded so that at most two CTAs fit an SM,
 // the number whose tensor-memory allocations fit together.
 constexpr size_t kCtSmem = 96 * 1024;
 static_assert(kCtACol + kCtStages * kTcAStageCols <= kCtTmemCols, "A stages fit");
-static_assert(size_t(kCtStages) * (kCtKBytes + kCtBBytes) <= kCtSmem, "rings fit");
+static_assert(size_t(kCtRing) * (kCtKBytes + kCtBBytes) <= kCtSmem, "rings fit");
+static_assert(kCtRing >= kCtStages, "the ring holds every tile with an A stage");
 
 struct CoilTcParams {
     const float* rec;               // grid-path records [tile][19][32] (k scaled, weights scaled)
@@ -72,6 +89,47 @@ struct CoilTcParams {
     int accumulate;
     unsigned int* err;
 };
+
+#ifndef MRI_CT_SPLIT
+#define MRI_CT_SPLIT 1    // A's split: 0 floating (tc_split8), 1 fixed point (ct_split8_unit)
+#endif
+#ifndef MRI_CT_PHASE2
+#define MRI_CT_PHASE2 1   // fast trig: the phase on pairs of samples (.f32x2)
+#endif
+
+// v = hi + lo for 8 values of magnitude at most 1 (a sine or cosine), in
+// fixed point: hi = v rounded to a multiple of 2^-11 (adding and removing
+// 1.5 * 2^12 rounds there), which f16 holds exactly, and lo = v - hi (exact,
+// |lo| <= 2^-12) rounded to f16, so that |v - hi - lo| <= 2^-24: the
+// absolute error of fp32's own rounding of a unit-modulus value.  All on
+// pairs of floats, no conversion back from f16.
+__device__ __forceinline__ void ct_split8_unit(const float (&v)[8], uint4& hi, uint4& lo)
+{
+    const f2 magic = f2_splat(6144.0f);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const f2 x = f2_pack(v[2 * j], v[2 * j + 1]);
+        const f2 hv = f2_sub(f2_add(x, magic), magic);
+        const f2 lv = f2_sub(x, hv);
+        float a, b;
+        f2_unpack(hv, a, b);
+        h[j] = pack_f16x2(a, b);
+        f2_unpack(lv, a, b);
+        l[j] = pack_f16x2(a, b);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void ct_split8(const float (&v)[8], uint4& hi, uint4& lo)
+{
+    if constexpr (MRI_CT_SPLIT == 1) {
+        ct_split8_unit(v, hi, lo);
+    } else {
+        tc_split8(v, hi, lo);
+    }
+}
 
 // sin and cos of 8 phases (the records' trig units) into ar (cos) and ai (sin)
 template <int TRIG>
@@ -92,6 +150,18 @@ __device__ __forceinline__ void ct_phase_trig8(const float (&kx)[8], const float
             f2_unpack(sn, ai[2 * h], ai[2 * h + 1]);
             f2_unpack(cs, ar[2 * h], ar[2 * h + 1]);
         }
+    } else if (MRI_CT_PHASE2) {
+        const f2 x2 = f2_splat(x), y2 = f2_splat(y), z2 = f2_splat(z);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const f2 ph = f2_fma(f2_pack(kz[2 * h], kz[2 * h + 1]), z2,
+                                 f2_fma(f2_pack(ky[2 * h], ky[2 * h + 1]), y2,
+                                        f2_mul(f2_pack(kx[2 * h], kx[2 * h + 1]), x2)));
+            float p0, p1;
+            f2_unpack(ph, p0, p1);
+            table_sincos<TRIG>(p0, ai[2 * h], ar[2 * h]);
+            table_sincos<TRIG>(p1, ai[2 * h + 1], ar[2 * h + 1]);
+        }
     } else {
 #pragma unroll
         for (int s = 0; s < 8; ++s)
@@ -99,19 +169,47 @@ __device__ __forceinline__ void ct_phase_trig8(const float (&kx)[8], const float
     }
 }
 
+// The four MMAs of one K step, D += A_r^hi W_r + A_r^lo W_r + A_i^hi W_i +
+// A_i^lo W_i, in one block: a = tensor-memory address of A_r^hi (the other
+// parts 16, 32, 48 columns on), wr_lo / wi_lo the low words of the two
+// window descriptors (dhi their common high word), acc = 0: the first
+// overwrites D.  The issuing thread shares its scheduler with the
+// generating warps, so its instructions per MMA are kept to a minimum.
+__device__ __forceinline__ void ct_mma4(uint32_t d, uint32_t a, uint32_t wr_lo, uint32_t wi_lo,
+                                        uint32_t dhi, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 wr, wi;\n\t.reg .b32 a1, a2, a3;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.b32 q, %6, %6;\n\t"
+        "mov.b64 wr, {%2, %4};\n\t"
+        "mov.b64 wi, {%3, %4};\n\t"
+        "add.u32 a1, %1, 16;\n\t"
+        "add.u32 a2, %1, 32;\n\t"
+        "add.u32 a3, %1, 48;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], wr, %5, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], wr, %5, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], wi, %5, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], wi, %5, q;\n\t}" ::"r"(d),
+        "r"(a), "r"(wr_lo), "r"(wi_lo), "r"(dhi), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 template <int TRIG>
 __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
 {
     constexpr int kS = kCtStages;
     constexpr int T = kTcTile;
-    constexpr uint32_t ID = umma_idesc_f16(kCtRows, kCtN);   // N = 16
+    constexpr uint32_t ID = umma_idesc_f16(kCtRows, kCtMmaN);   // N = 32
     constexpr int drain_tiles = (TRIG == TRIG_ACCURATE) ? kTcDrainAccurate : kTcDrainFast;
     static_assert(drain_tiles >= kS, "at most one block waits for its fold");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* const bring = smem_raw;                          // B tiles
-    float* const kring = reinterpret_cast<float*>(smem_raw + kS * kCtBBytes);   // k fields
-    __shared__ __align__(8) uint64_t full_bar[kS];    // record k fields and B tile landed
+    constexpr int kR = kCtRing;
+    unsigned char* const bring = smem_raw;                          // weight tiles
+    float* const kring = reinterpret_cast<float*>(smem_raw + kR * kCtBBytes);   // k fields
+    __shared__ __align__(8) uint64_t full_bar[kR];    // k fields and weight tile landed
+    __shared__ __align__(8) uint64_t ring_free[kR];   // MMAs of the stage's tile done
     __shared__ __align__(8) uint64_t a_full[kS];      // A written by every generator warp
     __shared__ __align__(8) uint64_t mma_bar[kS];     // MMAs of the tile done
     __shared__ __align__(8) uint64_t d_free;          // D folded (warps 0-3)
@@ -131,8 +229,12 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
     if (warp == 0) tmem_alloc(&tmem_base_sh, kCtTmemCols);
     if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < kS; ++i) {
+        for (int i = 0; i < kR; ++i) {
             mbar_init(&full_bar[i], 1);
+            mbar_init(&ring_free[i], 1);
+        }
+#pragma unroll
+        for (int i = 0; i < kS; ++i) {
             mbar_init(&a_full[i], kCtGenWarps);
             mbar_init(&mma_bar[i], 1);
         }
@@ -148,41 +250,37 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
     if (warp == kCtGenWarps) {
         if (lane == 0) {
             // ---- MMA issue ----
+            static_assert(kTcAPartCols == 16 && A_RL == 1 && A_IH == 2 && A_IL == 3,
+                          "ct_mma4's part offsets");
+            // ring stage 0's descriptor (8-row groups 1024 B apart: every
+            // other group of a tile); the other stages are 4096 B further on
+            const uint64_t desc0 = umma_desc_kmajor(bring, 128, 1024);
+            const uint32_t dlo0 = uint32_t(desc0), dhi = uint32_t(desc0 >> 32);
             int issued = 0;
+            int st = 0, rs = 0, tb = 0;               // t % kS, t % kR, t % drain_tiles
+            uint32_t ph_s = 0, ph_r = 0, ph_d = 0;    // (t / kS), (t / kR), (t / drain - 1) & 1
             for (int t = 0; t < nt; ++t) {
-                const int st = t % kS;
-                const bool first = (t % drain_tiles) == 0;
                 bool ok = true;
                 // the first MMA of a block overwrites D: the previous block is folded
-                if (first && t > 0)
-                    ok = ws_wait(&d_free, uint32_t(t / drain_tiles - 1) & 1u, abort_flag);
-                if (ok) ok = ws_wait(&a_full[st], uint32_t(t / kS) & 1u, abort_flag);
-                if (ok) ok = ws_wait(&full_bar[st], uint32_t(t / kS) & 1u, abort_flag);
+                if (tb == 0 && t > 0) {
+                    ok = ws_wait(&d_free, ph_d, abort_flag);
+                    ph_d ^= 1u;
+                }
+                if (ok) ok = ws_wait(&a_full[st], ph_s, abort_flag);
+                if (ok) ok = ws_wait(&full_bar[rs], ph_r, abort_flag);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const uint64_t d0 = umma_desc_kmajor(bring + st * kCtBBytes, 128, 512);
+                const uint32_t dlo = dlo0 + uint32_t(rs) * uint32_t(kCtBBytes >> 4);
                 const uint32_t acol = tmem + kCtACol + uint32_t(st) * kTcAStageCols;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    auto a = [&](int part) {
-                        return acol + uint32_t(part) * kTcAPartCols + uint32_t(8 * kb);
-                    };
-                    // the 16-row window of S at row r0 (8-row groups 512 B apart)
-                    auto sdesc = [&](int base, int r0) {
-                        return umma_desc_add(d0, uint32_t(base + (r0 / 8) * 512 + kb * 256));
-                    };
-                    const uint32_t acc0 = (first && kb == 0) ? 0u : 1u;
-                    // [D_r | D_i] += A_r [Mu_r | Mu_i]
-                    umma_f16_ta(tmem, a(A_RH), sdesc(0, 8), ID, acc0);
-                    umma_f16_ta(tmem, a(A_RH), sdesc(kCtPartBytes, 8), ID, 1u);
-                    umma_f16_ta(tmem, a(A_RL), sdesc(0, 8), ID, 1u);
-                    // [D_r | D_i] += A_i [-Mu_i | Mu_r]
-                    umma_f16_ta(tmem, a(A_IH), sdesc(0, 0), ID, 1u);
-                    umma_f16_ta(tmem, a(A_IH), sdesc(kCtPartBytes, 0), ID, 1u);
-                    umma_f16_ta(tmem, a(A_IL), sdesc(0, 0), ID, 1u);
-                }
+                // K steps of 16 samples: 8 columns of A, 256 B of each weight group
+                ct_mma4(tmem, acol, dlo + (512 >> 4), dlo, dhi, ID, tb == 0 ? 0u : 1u);
+                ct_mma4(tmem, acol + 8, dlo + ((512 + 256) >> 4), dlo + (256 >> 4), dhi, ID, 1u);
                 umma_commit(&mma_bar[st]);
+                umma_commit(&ring_free[rs]);
                 issued = t + 1;
+                if (++st == kS) { st = 0; ph_s ^= 1u; }
+                if (++rs == kR) { rs = 0; ph_r ^= 1u; }
+                if (++tb == drain_tiles) tb = 0;
             }
             // the MMAs issued finish before tensor memory is released
             if (issued > 0 && !mbar_wait_bounded(&mma_bar[(issued - 1) % kS],
@@ -196,23 +294,23 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
             // ---- copies: the k fields of record tile u and B tile u ----
             int issued = 0;
             for (int u = 0; u < nt; ++u) {
-                const int st = u % kS;
-                if (u >= kS &&
-                    !ws_wait(&mma_bar[st], uint32_t((u - kS) / kS) & 1u, abort_flag))
+                const int rs = u % kR;
+                if (u >= kR &&
+                    !ws_wait(&ring_free[rs], uint32_t((u - kR) / kR) & 1u, abort_flag))
                     break;
                 const int64_t tile = t_begin + u;
-                mbar_arrive_expect_tx(&full_bar[st], uint32_t(kCtKBytes + kCtBBytes));
-                tma_bulk_g2s(kring + st * 3 * T,
+                mbar_arrive_expect_tx(&full_bar[rs], uint32_t(kCtKBytes + kCtBBytes));
+                tma_bulk_g2s(kring + rs * 3 * T,
                              reinterpret_cast<const unsigned char*>(p.rec) + tile * kCtRecBytes,
-                             uint32_t(kCtKBytes), &full_bar[st]);
-                tma_bulk_g2s(bring + st * kCtBBytes, p.s_tab + tile * kCtBBytes,
-                             uint32_t(kCtBBytes), &full_bar[st]);
+                             uint32_t(kCtKBytes), &full_bar[rs]);
+                tma_bulk_g2s(bring + rs * kCtBBytes, p.s_tab + tile * kCtBBytes,
+                             uint32_t(kCtBBytes), &full_bar[rs]);
                 issued = u + 1;
             }
             // copies still in flight land before shared memory is released
             unsigned int bits = 0;
-            for (int u = issued > kS ? issued - kS : 0; u < issued; ++u)
-                if (!mbar_wait_bounded(&full_bar[u % kS], uint32_t(u / kS) & 1u))
+            for (int u = issued > kR ? issued - kR : 0; u < issued; ++u)
+                if (!mbar_wait_bounded(&full_bar[u % kR], uint32_t(u / kR) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
             if (issued < nt) bits |= DEVERR_TILE_WAIT_TIMEOUT;
             if (bits) atomicOr(p.err, bits);
@@ -232,11 +330,11 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
         for (int j = 0; j < kCtN; ++j) R[j] = 0.0f;
         auto fold = [&](bool signal) {
             tc_fence_after_sync();
-            float d[16];
-            tmem_ld16(tmem + lanes, d);
+            float d[32];
+            tmem_ld32(tmem + lanes, d);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < kCtN; ++j) R[j] += d[j];
+            for (int j = 0; j < kCtN; ++j) R[j] += d[j] + d[kCtN + j];
             if (signal) {
                 tc_fence_before_sync();
                 __syncwarp();
@@ -264,11 +362,11 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
             // the stage's previous A (tile t - kS) has been read; the k fields have landed
             if (ok && t >= kS)
                 ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
-            if (ok) ok = ws_wait(&full_bar[st], uint32_t(t / kS) & 1u, abort_flag);
+            if (ok) ok = ws_wait(&full_bar[t % kR], uint32_t(t / kR) & 1u, abort_flag);
             ok = __all_sync(0xffffffffu, ok);   // the tensor-memory stores are .sync.aligned
             if (!ok) break;
             tc_fence_after_sync();
-            const float* kt = kring + st * 3 * T;
+            const float* kt = kring + (t % kR) * 3 * T;
             const uint32_t acol = tmem + lanes + kCtACol + uint32_t(st) * kTcAStageCols;
 #pragma unroll
             for (int c = 0; c < kTcAChunks; ++c) {
@@ -281,10 +379,10 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
                 // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
                 const uint32_t col = acol + uint32_t(s0 / 2);
                 uint4 h, l;
-                tc_split8(ar, h, l);
+                ct_split8(ar, h, l);
                 tmem_st4(col + A_RH * kTcAPartCols, h);
                 tmem_st4(col + A_RL * kTcAPartCols, l);
-                tc_split8(ai, h, l);
+                ct_split8(ai, h, l);
                 tmem_st4(col + A_IH * kTcAPartCols, h);
                 tmem_st4(col + A_IL * kTcAPartCols, l);
             }

@@ -5,36 +5,41 @@
 
 namespace mri {
 
-// The B tiles: for record tile t, S (24 rows: -Mu_i, Mu_r, Mu_i of coils 0-7)
-// x 32 samples, f16 hi then lo, K-major core matrices (8 rows x 8 samples).
-// Coil c's weights are multiplied by its power of two 2^e_c (from its bound
-// word, so that every scaled weight is below 2^15 and its f16 parts keep
-// their precision whatever the other coils' magnitudes).  One thread per
-// (tile, row, 8-sample chunk).
+// The weight tiles: for record tile t, eight 8-row groups (row = coil) x 32
+// samples of f16 in K-major core matrices (8 rows x 8 samples, 128 B; 512 B
+// per group), [-Mu_i^hi, Mu_r^hi, Mu_r^hi, Mu_i^hi, -Mu_i^lo, Mu_r^lo, Mu_r^lo,
+// Mu_i^lo]: the even groups are the window the MMAs of A_i read, the odd ones
+// that of A_r.  Coil c's weights are multiplied by its power of two 2^e_c
+// (from its bound word, so that every scaled weight is below 2^15 and its f16
+// parts keep their precision whatever the other coils' magnitudes).  One
+// thread per (tile, coil, 8-sample chunk).
 __global__ void __launch_bounds__(256) build_mu_tiles_kernel(const float* rec, int64_t ntiles,
                                                              const unsigned int* bounds,
                                                              unsigned char* s_tab)
 {
-    constexpr int ITEMS = kCtSRows * (kTcTile / 8);   // 96 per tile
+    constexpr int ITEMS = kCtCoils * (kTcTile / 8);   // 32 per tile
     const int64_t total = ntiles * ITEMS;
     for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
          item += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = item / ITEMS;
         const int r = int(item - t * ITEMS);
-        const int row = r >> 2, kc = r & 3;           // S row, samples 8 kc ..
-        const int coil = row & 7, grp = row >> 3;     // 0: -Mu_i, 1: Mu_r, 2: Mu_i
-        const float* w = rec + t * kCtFields * kTcTile +
-                         (3 + (grp == 1 ? 0 : kCtCoils) + coil) * kTcTile + 8 * kc;
+        const int coil = r >> 2, kc = r & 3;          // samples 8 kc ..
+        const float* wr = rec + t * kCtFields * kTcTile + (3 + coil) * kTcTile + 8 * kc;
+        const float* wi = wr + kCtCoils * kTcTile;
         const float scale = exp2_int(tc_scale_exp(bounds[coil]));
-        float v[8];
+        float vr[8], vi[8];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) v[s] = (grp == 0 ? -w[s] : w[s]) * scale;
-        uint4 h, l;
-        tc_split8(v, h, l);
-        unsigned char* const tile = s_tab + t * kCtBBytes;
-        const int off = (row >> 3) * 512 + kc * 128 + (row & 7) * 16;
-        *reinterpret_cast<uint4*>(tile + off) = h;
-        *reinterpret_cast<uint4*>(tile + kCtPartBytes + off) = l;
+        for (int s = 0; s < 8; ++s) {
+            vr[s] = wr[s] * scale;
+            vi[s] = wi[s] * scale;
+        }
+        uint4 rh, rl, ih, il;
+        tc_split8(vr, rh, rl);
+        tc_split8(vi, ih, il);
+        unsigned char* const row = s_tab + t * kCtBBytes + kc * 128 + coil * 16;
+        const uint4 g[kCtGroups] = {neg_f16x8(ih), rh, rh, ih, neg_f16x8(il), rl, rl, il};
+#pragma unroll
+        for (int j = 0; j < kCtGroups; ++j) *reinterpret_cast<uint4*>(row + j * 512) = g[j];
     }
 }
 

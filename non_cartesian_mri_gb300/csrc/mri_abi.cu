@@ -318,7 +318,7 @@ mri_status run_coils_tc_group(DeviceState* d, const CoilTcPlan& g, const float* 
         mri::launch_prep_grid_tc(false, mri::kCtCoils, pp,
                                  grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess ||
         mri::launch_build_mu_tiles(rec, g.ntiles, wbound, s_tab,
-                                   grid_for(g.ntiles * mri::kCtSRows * (mri::kTcTile / 8), d->sms),
+                                   grid_for(g.ntiles * mri::kCtCoils * (mri::kTcTile / 8), d->sms),
                                    s) != cudaSuccess)
         return cuda_fail();
 
