@@ -152,7 +152,8 @@ def test_batched_grid_128_workload(mri, trig):
 
 def test_batched_grid_fallback_and_empty(mri):
     """nx = 6 goes through expanded coordinates and the general batched
-    kernel; M = 0 gives zeros (or leaves accumulated outputs alone)."""
+    path (3 coils: the tensor-core coil kernel, not the grid kernel); M = 0
+    gives zeros (or leaves accumulated outputs alone)."""
     w = wl.make_workload("fhd_64")
     M, B = 2500, 3
     xs = np.array([-30.0, -7.5, 0.0, 2.0, 19.0, 31.0], np.float32)
@@ -166,7 +167,8 @@ def test_batched_grid_fallback_and_empty(mri):
     ref = oracle.fhd_batched(w.kx[:M], w.ky[:M], w.kz[:M], x, y, z, w.rPhi[:M], w.iPhi[:M],
                              rD, iD)
     check_per_coil(cplx(r, i), ref, TOL["accurate"])
-    assert mri.plan_grid_batched(B, M, 6, 3, 2)["tensor_cores"] == 0
+    p = mri.plan_grid_batched(B, M, 6, 3, 2)
+    assert p["threads_per_cta"] == 320 and p["voxels_per_cta"] == 128 and p["grid_fold"] == 0
     e = torch.empty(0, device="cuda")
     eD = torch.empty((B, 0), device="cuda")
     rz, iz = mri.fhd_batched_grid(e, e, e, dev(xs), dev(ys), dev(zs), e, e, eD, eD)
