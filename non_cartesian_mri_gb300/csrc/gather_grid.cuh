@@ -36,8 +36,9 @@ struct GridParams {
     int64_t split_stride;
     int accumulate;
     unsigned int* err;
-    // float bits of max |w_r| + |w_i| over the samples, and the B operand
-    // tiles (kTcStageBytes per record tile and column block)
+    // per coil of the group: float bits of max |w_r| + |w_i| over the
+    // samples (the coil's weights are scaled by their own power of two); and
+    // the B operand tiles (kTcStageBytes per record tile and column block)
     const unsigned int* wbound;
     const unsigned char* s_tab;
     // coil groups: coils present, and the output offset of one coil

@@ -26,7 +26,9 @@
 // weights are multiplied (once per call, in the records) by a power of two
 // chosen from the largest |w_r| + |w_i| of the call so that every weighted
 // operand is below 2^15, and the results are multiplied back exactly; the
-// phase factors (|e^{i phi}| = 1) need no scale.
+// phase factors (|e^{i phi}| = 1) need no scale.  In a coil group every coil
+// has its own bound and power of two, so a coil far smaller than the others
+// keeps the full precision of its f16 parts.
 //
 // Where the weight goes.  With one coil per CTA (F^H D, Q) the weight Mu is
 // folded into the B table (B = Mu e^{i2pi kx x}, once per call), and A is the

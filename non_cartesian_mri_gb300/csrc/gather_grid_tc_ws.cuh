@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     __shared__ int fold_sh[3];                            // G, log2 of its width, row groups
+    __shared__ unsigned int bound_sh[BC];                 // each coil's weight bound word
     volatile int* const abort_flag = &abort_sh;
 
     const int tid = threadIdx.x;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             }
             yz_sh[r] = yz;
         }
+        if (tid < BC) bound_sh[tid] = p.wbound[tid];
         if (tid == 0) {
             fold_sh[0] = G;
             fold_sh[1] = log2_fw;
@@ -466,7 +468,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
         } else if (nt > 0) {
             // R -> outputs: grid row ra, this warp's D columns (the fold
             // state is read back from shared memory, not kept in registers)
-            const float inv_scale = exp2_int(-tc_scale_exp(*p.wbound));
+            const float inv_scale = exp2_int(-tc_scale_exp(bound_sh[coil]));   // this coil's
             const volatile int* fs = fold_sh;
             const int G = fs[0], log2_fw = fs[1], nyg = fs[2];
             const int64_t total_rows = int64_t(nyg) * p.nz;

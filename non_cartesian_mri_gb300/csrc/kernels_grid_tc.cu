@@ -191,23 +191,25 @@ cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t r
 // kernel multiplies its results by 2^-e.
 __global__ void __launch_bounds__(256) scale_records_kernel(float* rec, int fields,
                                                             int64_t ntiles,
-                                                            const unsigned int* bound)
+                                                            const unsigned int* bound, int bc)
 {
-    const float scale = exp2_int(tc_scale_exp(*bound));
     const int per_tile = (fields - 3) * kTcTile;
     const int64_t total = ntiles * per_tile;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = i / per_tile;
         const int j = int(i - t * per_tile);
-        rec[t * fields * kTcTile + 3 * kTcTile + j] *= scale;
+        // weight field (j / kTcTile) belongs to coil (j / kTcTile) % bc
+        rec[t * fields * kTcTile + 3 * kTcTile + j] *=
+            exp2_int(tc_scale_exp(bound[(j / kTcTile) % bc]));
     }
 }
 
 cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
-                                 const unsigned int* bound, int grid, cudaStream_t s)
+                                 const unsigned int* bound, int bc, int grid, cudaStream_t s)
 {
-    scale_records_kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, bound);
+    if (bc < 1 || (fields - 3) % bc != 0) return cudaErrorInvalidValue;
+    scale_records_kernel<<<grid, 256, 0, s>>>(rec, fields, ntiles, bound, bc);
     return cudaGetLastError();
 }
 

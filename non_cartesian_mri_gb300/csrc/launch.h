@@ -54,9 +54,10 @@ cudaError_t launch_forward_grid_prep(const float* rr, const float* ri, int64_t r
                                      unsigned int* bound, unsigned char* tab, float2* yz_rows,
                                      float* row_step, int grid, cudaStream_t s);
 cudaError_t launch_forward_grid_tc(int trig, const FwdParams& p, dim3 grid, cudaStream_t s);
-// weights of tensor-core grid records times the power of two from the bound word
+// weights of tensor-core grid records (bc coils) times each coil's power of
+// two, from its bound word bound[coil]
 cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
-                                 const unsigned int* bound, int grid, cudaStream_t s);
+                                 const unsigned int* bound, int bc, int grid, cudaStream_t s);
 // threads per CTA of the tensor-core grid kernel
 int grid_tc_threads();
 // whether a tensor-core grid launch takes its y factors from the Ey table

@@ -237,8 +237,10 @@ cudaEvent_t* timing_slot(DeviceState* d)
     return &d->ev[2 * i];
 }
 
-// scratch slot of the weight bound the tensor-core kernels scale by
+// scratch slot of the weight bounds the tensor-core kernels scale by (a
+// word per coil of a group; the grid calls' fold word and row offsets after)
 constexpr int64_t kBoundBytes = 256;
+static_assert((12 + mri::kTcCols / mri::kTcMinCols) * 4 <= kBoundBytes, "bound slot");
 
 #ifndef MRI_COILS_TC_MIN
 #define MRI_COILS_TC_MIN 3
@@ -650,10 +652,11 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
                                                      align256(part_max) + align256(s_bytes))
                          : nullptr;
     float* rec = reinterpret_cast<float*>(scratch);
-    // the bound slot: the weight bound word, the fold check's word and offsets
+    // the bound slot: a weight bound word per coil of a group (8), the fold
+    // check's word, its row offsets (up to 16)
     unsigned int* wbound = reinterpret_cast<unsigned int*>(scratch + align256(rec_max));
-    unsigned int* fold_ok = wbound + 1;
-    float* fold_dy = reinterpret_cast<float*>(wbound + 4);
+    unsigned int* fold_ok = wbound + 8;
+    float* fold_dy = reinterpret_cast<float*>(wbound + 12);
     float* part = reinterpret_cast<float*>(scratch + align256(rec_max) + kBoundBytes);
     unsigned char* s_tab = reinterpret_cast<unsigned char*>(scratch + align256(rec_max) +
                                                             kBoundBytes + align256(part_max));
@@ -670,11 +673,12 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
         mri::PrepParams pp{kx, ky, kz, rPhi, iPhi, rD, iD, M, grp.b0, g.ntiles, kscale_for(trig),
                            rec};
         pp.wbound = wbound;
+        pp.bound_per_coil = true;   // each coil of a group scaled by its own power of two
         pp.coils_valid = grp.nb;
-        if (cudaMemsetAsync(wbound, 0, sizeof(unsigned int), s) != cudaSuccess ||
+        if (cudaMemsetAsync(wbound, 0, grp.bc * sizeof(unsigned int), s) != cudaSuccess ||
             mri::launch_prep_grid_tc(realw, grp.bc, pp,
                                      grid_for(g.ntiles * mri::kTcTile, d->sms), s) != cudaSuccess ||
-            mri::launch_scale_records(rec, fields, g.ntiles, wbound,
+            mri::launch_scale_records(rec, fields, g.ntiles, wbound, realw ? 1 : grp.bc,
                                       grid_for(g.ntiles * (fields - 3) * mri::kTcTile, d->sms),
                                       s) != cudaSuccess)
             st = cuda_fail();

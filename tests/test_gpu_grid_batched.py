@@ -43,13 +43,14 @@ def expand(xs, ys, zs):
 
 
 def coil_data(w, B, M, seed, scales=None):
-    """B coils of D on the first M samples of workload w (D_b = D * coil gain)."""
+    """B coils of D on the first M samples of workload w (D_b = D * coil gain
+    + noise); `scales` multiplies whole coils."""
     rng = np.random.default_rng(seed)
     g = (rng.standard_normal(B) + 1j * rng.standard_normal(B)).astype(np.complex64)
-    if scales is not None:
-        g = g * np.asarray(scales, np.float32)
     d = w.rD[:M] + 1j * w.iD[:M]
     dc = g[:, None] * d[None, :] + 0.1 * (rng.standard_normal((B, M)) + 1j * rng.standard_normal((B, M)))
+    if scales is not None:
+        dc = dc * np.asarray(scales, np.float64)[:, None]
     return dc.real.astype(np.float32), dc.imag.astype(np.float32)
 
 
@@ -105,14 +106,15 @@ def test_batched_grid_accumulates_and_matches_single_coil_calls(mri):
 
 
 def test_coils_of_very_different_scale(mri):
-    """One power-of-two operand scale per coil group: coils 1e-4 and 1e3 times
-    the others still meet the relative bound each."""
+    """Each coil of a group has its own power-of-two operand scale: coils
+    1e-6 and 1e4 times the others (a range no single f16 scale covers with
+    full precision) still meet the relative bound each."""
     w = wl.make_workload("fhd_128_radial")
     M, B = 4000, 4
     xs = (np.arange(128) - 64).astype(np.float32)
     ys = np.array([0.0, 5.0], np.float32)
     zs = np.array([1.0], np.float32)
-    rD, iD = coil_data(w, B, M, 3, scales=[1.0, 1e-4, 1e3, 1.0])
+    rD, iD = coil_data(w, B, M, 3, scales=[1.0, 1e-6, 1e4, 1.0])
     k = [dev(a[:M]) for a in (w.kx, w.ky, w.kz)]
     r, i = mri.fhd_batched_grid(*k, dev(xs), dev(ys), dev(zs), dev(w.rPhi[:M]),
                                 dev(w.iPhi[:M]), dev(rD), dev(iD), trig="accurate")
