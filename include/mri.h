@@ -113,8 +113,11 @@ mri_status mri_q(const float* kx, const float* ky, const float* kz,
  * Batched F^H D: B data vectors (e.g. coils) acquired on one trajectory,
  *   FhD_b[n] = sum_m conj(Phi[m]) D_b[m] e^{+i 2 pi k_m . x_n},   0 <= b < B.
  * rD, iD are coil-major [B][M]; rFhD, iFhD are coil-major [B][N].  Each
- * sin/cos pair is computed once and used for up to 8 coils.  The pages do
- * not describe this variant; it is F^H D applied to several D.
+ * sin/cos pair is computed once and used for up to 8 coils: groups of 3 to
+ * 8 coils run the multiply-accumulate over the coils on the tensor cores
+ * (each coil's weights scaled by its own power of two, undone exactly), a
+ * remainder of 1 or 2 coils the per-pair kernels.  The pages do not
+ * describe this variant; it is F^H D applied to several D.
  * B >= 1.  Other arguments and edge cases as mri_fhd.
  */
 mri_status mri_fhd_batched(const float* kx, const float* ky, const float* kz,
