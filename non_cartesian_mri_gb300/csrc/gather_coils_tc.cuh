@@ -74,8 +74,9 @@ static_assert(size_t(kCtRing) * (kCtKBytes + kCtBBytes) <= kCtSmem, "rings fit")
 static_assert(kCtRing >= kCtStages, "the ring holds every tile with an A stage");
 
 struct CoilTcParams {
-    const float* rec;               // grid-path records [tile][19][32] (k scaled, weights scaled)
-    const unsigned char* s_tab;     // B tiles, kCtBBytes each
+    const float* rec;               // grid-path records [tile][19][32]; the kernel reads the
+                                    // k fields (scaled to the trig unit)
+    const unsigned char* s_tab;     // weight tiles (scaled per coil), kCtBBytes each
     const unsigned int* bounds;     // per coil: float bits of max |w_r| + |w_i| (its scale)
     int64_t ntiles;
     int splits;
@@ -150,7 +151,7 @@ __device__ __forceinline__ void ct_phase_trig8(const float (&kx)[8], const float
             f2_unpack(sn, ai[2 * h], ai[2 * h + 1]);
             f2_unpack(cs, ar[2 * h], ar[2 * h + 1]);
         }
-    } else if (MRI_CT_PHASE2) {
+    } else if constexpr (MRI_CT_PHASE2 != 0) {
         const f2 x2 = f2_splat(x), y2 = f2_splat(y), z2 = f2_splat(z);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
