@@ -300,6 +300,11 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
                     !ws_wait(&ring_free[rs], uint32_t((u - kR) / kR) & 1u, abort_flag))
                     break;
                 const int64_t tile = t_begin + u;
+                if (MRI_DEBUG && (tile < 0 || tile >= p.ntiles)) {
+                    // a bad index copies nothing; the consumers' waits report too
+                    atomicOr(p.err, DEVERR_BOUNDS);
+                    break;
+                }
                 mbar_arrive_expect_tx(&full_bar[rs], uint32_t(kCtKBytes + kCtBBytes));
                 tma_bulk_g2s(kring + rs * 3 * T,
                              reinterpret_cast<const unsigned char*>(p.rec) + tile * kCtRecBytes,

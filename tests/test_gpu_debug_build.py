@@ -75,6 +75,12 @@ for nx, ny, nz in ((16, 5, 3), (200, 3, 2), (16, 128, 1)):
             g = cp(r, i)
             for b in range(3):
                 assert oracle.rel_l2(g[b], ref[b]) <= TOL[trig], ("batched", b, trig)
+            # two coils: the per-pair coil kernel (three run on the tensor cores)
+            r, i = mri.fhd_batched(*k, *X, dev(a["rPhi"]), dev(a["iPhi"]), dev(a["rD"][:2]),
+                                   dev(a["iD"][:2]), trig=trig)
+            g = cp(r, i)
+            for b in range(2):
+                assert oracle.rel_l2(g[b], ref[b]) <= TOL[trig], ("batched2", b, trig)
         bits = mri.device_errors(clear=True)
         assert bits == 0, ("device error bits", bits, nx, ny, trig)
 print("debug build: all kernels clean")
