@@ -350,8 +350,11 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
 
         bool ok = true;
         int pend = -1;   // last tile of a block whose D is not folded yet
+        // t % kS, t % kR, t % drain_tiles and the parities (t / kS) & 1,
+        // (t / kR) & 1, kept incrementally
+        int st = 0, rs = 0, tb = 0;
+        uint32_t ph_s = 0, ph_r = 0;
         for (int t = 0; t < nt && ok; ++t) {
-            const int st = t % kS;
             if (folds && pend >= 0) {
                 const bool must = t - kS >= pend;
                 bool done = must ? ws_wait(&mma_bar[pend % kS], uint32_t(pend / kS) & 1u,
@@ -366,13 +369,12 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
                 }
             }
             // the stage's previous A (tile t - kS) has been read; the k fields have landed
-            if (ok && t >= kS)
-                ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
-            if (ok) ok = ws_wait(&full_bar[t % kR], uint32_t(t / kR) & 1u, abort_flag);
+            if (ok && t >= kS) ok = ws_wait(&mma_bar[st], ph_s ^ 1u, abort_flag);
+            if (ok) ok = ws_wait(&full_bar[rs], ph_r, abort_flag);
             ok = __all_sync(0xffffffffu, ok);   // the tensor-memory stores are .sync.aligned
             if (!ok) break;
             tc_fence_after_sync();
-            const float* kt = kring + (t % kR) * 3 * T;
+            const float* kt = kring + rs * 3 * T;
             const uint32_t acol = tmem + lanes + kCtACol + uint32_t(st) * kTcAStageCols;
 #pragma unroll
             for (int c = 0; c < kTcAChunks; ++c) {
@@ -396,7 +398,16 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[st]);
-            if (t % drain_tiles == drain_tiles - 1 && t + 1 < nt) pend = t;
+            if (tb == drain_tiles - 1 && t + 1 < nt) pend = t;
+            if (++st == kS) {
+                st = 0;
+                ph_s ^= 1u;
+            }
+            if (++rs == kR) {
+                rs = 0;
+                ph_r ^= 1u;
+            }
+            if (++tb == drain_tiles) tb = 0;
         }
         if (folds) {
             // the block still waiting for its fold, then the last block
