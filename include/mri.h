@@ -371,10 +371,8 @@ typedef struct mri_plan {
 mri_status mri_plan_gather(int kind, int64_t B, int64_t M, int64_t N, int num_sms,
                            mri_plan* plan);
 
-/* The same for mri_fhd_grid (kind MRI_KIND_FHD) and mri_q_grid (MRI_KIND_Q).
- * It describes the fast-trig call: with accurate trig on the tensor-core
- * path and ny a multiple of 128, a call also tabulates the y factor once
- * (one more launch, tiles * ny/128 * 32 KiB more scratch). */
+/* The same for mri_fhd_grid (kind MRI_KIND_FHD) and mri_q_grid (MRI_KIND_Q),
+ * for any trig mode. */
 mri_status mri_plan_grid(int kind, int64_t M, int nx, int ny, int nz, int num_sms,
                          mri_plan* plan);
 

@@ -44,10 +44,6 @@ struct GridParams {
     // coil groups: coils present, and the output offset of one coil
     int coils;
     int64_t coil_stride;
-    // the Ey table: per record tile and block of 128 y values,
-    // e^{i phase(ky y)} as [sample][128] float2; ny / 128 blocks
-    const float2* ey_tab;
-    int ey_blocks;
     // column blocks of 128 (the last may be partly padding)
     int ncb;
     // Row folding (nx <= 64): with fold > 1 and the check word `fold_ok`

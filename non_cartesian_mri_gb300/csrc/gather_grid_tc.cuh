@@ -80,11 +80,6 @@ constexpr int kTcPartBytes = kTcRows * kTcTile * 2;  // 128 S rows x 32 f16 (8 K
 constexpr int kTcSBytes = 3 * kTcPartBytes;          // S = [-B_i; B_r; B_i]: 384 x 32 (24 KB)
 constexpr int kTcStageBytes = 2 * kTcSBytes;         // S hi, S lo (48 KB)
 constexpr int kTcStages = MRI_TC_STAGES;             // operand stages in the ring
-// The Ey table replaces the per-(row, sample) sin/cos of the accurate path
-// when a CTA's rows are one z-plane (ny a multiple of 128); its two 32 KB
-// tiles take shared memory from the B ring.
-constexpr int kTcStagesEy = 3;
-constexpr int kTcEyBytes = kTcTile * kTcRows * 8;   // 32 samples x 128 rows of float2
 constexpr int kTcColsPerWarp = 256 * 4 / kTcWarps;  // D columns one warp folds (128)
 constexpr uint32_t kTcDCols = 256;                   // D_r | D_i
 constexpr uint32_t kTcAPartCols = kTcTile / 2;       // one A part: 32 f16 per lane (16 columns)
@@ -323,29 +318,6 @@ inline int grid_tc_fold_log2_width(int G)
     int l = 7;
     while ((1 << (7 - l)) < G) --l;
     return l;   // fw = 128 / G = 2^l
-}
-
-// The Ey table: for record tile t and block yb of 128 y values,
-// e^{i phase(ky[s] ys[128 yb + r])} at [(t * nyb + yb) * 32 + s] * 128 + r
-// (float2: cos, sin).  Consecutive threads take consecutive r.
-template <int TRIG>
-__global__ void __launch_bounds__(256) build_ey_tiles_kernel(const float* rec, int fields,
-                                                             int64_t ntiles, const float* ys,
-                                                             int nyb, float2* ey_tab)
-{
-    const int64_t per_tile = int64_t(nyb) * kTcTile * kTcRows;
-    const int64_t total = ntiles * per_tile;
-    for (int64_t item = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; item < total;
-         item += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = item / per_tile;
-        const int rem = int(item - t * per_tile);
-        const int yb = rem / (kTcTile * kTcRows);
-        const int s = (rem / kTcRows) % kTcTile;
-        const int r = rem % kTcRows;
-        float sn, cs;
-        table_sincos<TRIG>(rec[t * fields * kTcTile + kTcTile + s] * ys[yb * kTcRows + r], sn, cs);
-        ey_tab[item] = make_float2(cs, sn);
-    }
 }
 
 // Bounded wait that also gives up once any role of the CTA has given up (the

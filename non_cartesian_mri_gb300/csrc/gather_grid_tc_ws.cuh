@@ -7,11 +7,8 @@
 // D; D is folded into running sums in registers every block of tiles
 // (blocked summation).  A per case:
 //   BC = 1:         A = e^{i2pi(ky y + kz z)} (the weight is in the B table),
-//                   one sin/cos per element;
-//   BC = 1, EYT:    A = e^{i2pi kz z} e^{i2pi ky y}: the y factor from the
-//                   per-call Ey table (TMA, one tile of 32 x 128 per record
-//                   tile), the z factor once per sample (lane s of every
-//                   generator warp evaluates sample s, shuffled to the rows);
+//                   one sin/cos per element (accurate: the polynomial on
+//                   pairs of samples);
 //   BC = 4 or 8:    A = Mu_coil e^{i2pi(ky y + kz z)}: the row factor of each
 //                   (grid row, sample) evaluated once into shared memory one
 //                   tile ahead, by all generator threads (a named barrier of
@@ -51,8 +48,7 @@
 
 #include "gather_grid_tc.cuh"
 
-// Accurate A generation on pairs of samples (.f32x2) when the Ey table is
-// not used (narrow or folded grids, ny not a multiple of 128).
+// Accurate single-coil A generation on pairs of samples (.f32x2).
 #ifndef MRI_TC_PACKED_A
 #define MRI_TC_PACKED_A 1
 #endif
@@ -68,12 +64,11 @@ static_assert(32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs <= kWsThreads * k
               "warpgroup register budgets exceed the launch");
 static_assert(kWsGenWarps == kTcWarps, "generator warps own the D columns by tc_warp_cols");
 
-inline size_t grid_tc_ws_smem_bytes(bool realw, int bc, bool eyt)
+inline size_t grid_tc_ws_smem_bytes(bool realw, int bc)
 {
     const int F = realw ? 4 : 3 + 2 * bc;
     const int rc = kTcRows / bc;
-    size_t b = size_t(eyt ? kTcStagesEy : kTcStages) * kTcStageBytes;   // B operand stages
-    if (eyt) b += size_t(2) * kTcEyBytes;                               // Ey tiles
+    size_t b = size_t(kTcStages) * kTcStageBytes;                       // B operand stages
     b += size_t(kStages) * F * kTcTile * 4;                             // record ring
     b += size_t(rc) * 8;                                                // (y, z) of the rows
     if (bc > 1) b += size_t(2) * kTcTile * rc * 8;                      // row factors, two tiles
@@ -96,12 +91,11 @@ __device__ __forceinline__ bool ws_gen_sync_and(bool v)
     return r != 0;
 }
 
-template <int BC, bool REALW, int TRIG, bool EYT>
+template <int BC, bool REALW, int TRIG>
 __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridParams p)
 {
-    static_assert(!EYT || BC == 1, "Ey table for single-weight calls");
     static_assert(BC == 1 || (!REALW && (BC == 4 || BC == 8)), "coil group");
-    constexpr int kS = EYT ? kTcStagesEy : kTcStages;   // A / B stages
+    constexpr int kS = kTcStages;                     // A / B stages
     constexpr int T = kTcTile;
     constexpr int F = REALW ? 4 : 3 + 2 * BC;
     constexpr int RC = kTcRows / BC;                  // grid rows per CTA
@@ -112,9 +106,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const ops = smem_raw;
-    float2* const ey_sh = reinterpret_cast<float2*>(ops + kS * kTcStageBytes);   // EYT: 2 tiles
-    float* const ring = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ey_sh) +
-                                                 (EYT ? 2 * kTcEyBytes : 0));
+    float* const ring = reinterpret_cast<float*>(ops + kS * kTcStageBytes);
     float2* const yz_sh = reinterpret_cast<float2*>(ring + kStages * F * T);
     float2* const e_sh = yz_sh + RC;                  // BC > 1: row factors of two tiles
     __shared__ __align__(8) uint64_t full_bar[kStages];   // record tile landed
@@ -123,8 +115,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
     __shared__ __align__(8) uint64_t a_full[kS];          // A tile written by every generator
     __shared__ __align__(8) uint64_t mma_bar[kS];         // MMAs of the tile done
     __shared__ __align__(8) uint64_t d_free;              // D folded by every generator
-    __shared__ __align__(8) uint64_t ey_bar[2];           // EYT: Ey tile landed
-    __shared__ __align__(8) uint64_t ey_free[2];          // EYT: Ey tile read by every generator
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     __shared__ int fold_sh[3];                            // G, log2 of its width, row groups
@@ -181,10 +171,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             mbar_init(&mma_bar[i], 1);
         }
         mbar_init(&d_free, kWsGenWarps);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ey_bar[i], 1);
-            mbar_init(&ey_free[i], kWsGenWarps);
-        }
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -242,10 +228,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                 atomicOr(p.err, DEVERR_DRAIN_TIMEOUT);
             if (issued < nt) atomicOr(p.err, DEVERR_TILE_WAIT_TIMEOUT);
         } else if (warp == kWsGenWarps + 1 && lane == 0) {
-            // ---- copies: record tile u, B tile u (and Ey tile u) ----
-            // EYT: this CTA's 128 rows are grid rows iy0 .. iy0 + 127 of one plane
-            const int64_t ey_block = EYT ? (row0 % p.ny) / kTcRows : 0;
-            int r_issued = 0, b_issued = 0, e_issued = 0;
+            // ---- copies: record tile u, B tile u ----
+            int r_issued = 0, b_issued = 0;
             for (int u = 0; u < nt; ++u) {
                 bool ok = true;
                 if (u >= kStages)
@@ -262,15 +246,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                                  (t_begin + u) * p.ncb + blockIdx.z, p.ntiles * p.ncb,
                                  uint32_t(kTcStageBytes), &s_bar[u % kS], p.err);
                 b_issued = u + 1;
-                if constexpr (EYT) {
-                    if (u >= 2) ok = ws_wait(&ey_free[u & 1], uint32_t((u - 2) >> 1) & 1u, abort_flag);
-                    if (!ok) break;
-                    tma_load_checked(ey_sh + (u & 1) * (T * kTcRows), p.ey_tab,
-                                     (t_begin + u) * p.ey_blocks + ey_block,
-                                     p.ntiles * p.ey_blocks, uint32_t(kTcEyBytes), &ey_bar[u & 1],
-                                     p.err);
-                    e_issued = u + 1;
-                }
             }
             // the latest copy into each slot and stage lands before shared
             // memory is released, whatever the other roles did (the copy
@@ -283,10 +258,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             for (int u = b_issued > kS ? b_issued - kS : 0; u < b_issued; ++u)
                 if (!mbar_wait_bounded(&s_bar[u % kS], uint32_t(u / kS) & 1u))
                     bits |= DEVERR_DRAIN_TIMEOUT;
-            for (int u = e_issued > 2 ? e_issued - 2 : 0; u < e_issued; ++u)
-                if (!mbar_wait_bounded(&ey_bar[u & 1], uint32_t(u >> 1) & 1u))
-                    bits |= DEVERR_DRAIN_TIMEOUT;
-            if (b_issued < nt || (EYT && e_issued < nt)) bits |= DEVERR_TILE_WAIT_TIMEOUT;
+            if (b_issued < nt) bits |= DEVERR_TILE_WAIT_TIMEOUT;
             if (bits) atomicOr(p.err, bits);
         }
         __syncwarp();
@@ -300,7 +272,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
         const int rr = ra % RC;
         const uint32_t lanes = uint32_t(32 * (warp & 3)) << 16;
         const float2 yz = yz_sh[rr];
-        const float z_plane = EYT ? yz_sh[0].y : 0.0f;   // EYT: one plane per CTA
         float R[kTcColsPerWarp];
 #pragma unroll
         for (int j = 0; j < kTcColsPerWarp; ++j) R[j] = 0.0f;
@@ -356,33 +327,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
             if (ok && t >= kS)
                 ok = ws_wait(&mma_bar[st], uint32_t((t - kS) / kS) & 1u, abort_flag);
             if (ok) ok = ws_wait(&full_bar[t % kStages], uint32_t(t / kStages) & 1u, abort_flag);
-            if (EYT && ok) ok = ws_wait(&ey_bar[t & 1], uint32_t(t >> 1) & 1u, abort_flag);
             // warp-uniform: the tensor-memory stores below are .sync.aligned
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after_sync();
                 const float* rec = ring + (t % kStages) * F * T;
                 const uint32_t acol = tmem + lanes + kTcDCols + uint32_t(st) * kTcAStageCols;
-                float ezr = 0.0f, ezi = 0.0f;
-                if constexpr (EYT) {
-                    // e^{i phase(kz z)} of sample `lane`, shuffled to the rows below
-                    table_sincos<TRIG>(rec[2 * T + lane] * z_plane, ezi, ezr);
-                }
 #pragma unroll
                 for (int c = 0; c < kTcAChunks; ++c) {
                     const int s0 = 8 * (kTcAChunks * ah + c);
                     float ar[8], ai[8];
-                    if constexpr (EYT) {
-                        const float2* ey = ey_sh + (t & 1) * (T * kTcRows);
-#pragma unroll
-                        for (int s8 = 0; s8 < 8; ++s8) {
-                            const float fr = __shfl_sync(0xffffffffu, ezr, s0 + s8);
-                            const float fi = __shfl_sync(0xffffffffu, ezi, s0 + s8);
-                            const float2 e = ey[(s0 + s8) * kTcRows + ra];
-                            ar[s8] = fmaf(fr, e.x, -fi * e.y);
-                            ai[s8] = fmaf(fr, e.y, fi * e.x);
-                        }
-                    } else if constexpr (BC == 1 && TRIG == TRIG_ACCURATE && MRI_TC_PACKED_A) {
+                    if constexpr (BC == 1 && TRIG == TRIG_ACCURATE && MRI_TC_PACKED_A) {
                         // the polynomial on pairs of samples (.f32x2)
                         float ky[8], kz[8];
                         tc_load8(rec, 1, s0, ky);
@@ -433,7 +388,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                 if (lane == 0) {
                     mbar_arrive(&a_full[st]);
                     mbar_arrive(&rec_free[t % kStages]);
-                    if (EYT) mbar_arrive(&ey_free[t & 1]);
                 }
                 if (t % drain_tiles == drain_tiles - 1 && t + 1 < nt) pend = t;
                 if constexpr (BC > 1) {

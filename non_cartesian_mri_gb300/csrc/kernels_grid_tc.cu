@@ -8,10 +8,10 @@
 namespace mri {
 
 namespace {
-template <int BC, bool REALW, int TRIG, bool EYT>
+template <int BC, bool REALW, int TRIG>
 cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
 {
-    auto kernel = gather_grid_tc_ws_kernel<BC, REALW, TRIG, EYT>;
+    auto kernel = gather_grid_tc_ws_kernel<BC, REALW, TRIG>;
     // the warpgroup register budgets must fit the registers the CTA is
     // launched with, or a budget increase would wait forever
     cudaFuncAttributes fa{};
@@ -19,20 +19,20 @@ cudaError_t run_ws(const GridParams& p, dim3 grid, cudaStream_t s)
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kWsThreads < 32 * kWsGenWarps * kWsGenRegs + 128 * kWsAuxRegs)
         return cudaErrorInvalidConfiguration;
-    const size_t smem = grid_tc_ws_smem_bytes(REALW, BC, EYT);
+    const size_t smem = grid_tc_ws_smem_bytes(REALW, BC);
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kernel<<<grid, kWsThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int BC, bool REALW, bool EYT>
+template <int BC, bool REALW>
 cudaError_t run_trig(int trig, const GridParams& p, dim3 grid, cudaStream_t s)
 {
     switch (trig) {
-        case TRIG_ACCURATE: return run_ws<BC, REALW, TRIG_ACCURATE, EYT>(p, grid, s);
-        case TRIG_FAST: return run_ws<BC, REALW, TRIG_FAST, EYT>(p, grid, s);
-        case TRIG_FAST_RR: return run_ws<BC, REALW, TRIG_FAST_RR, EYT>(p, grid, s);
+        case TRIG_ACCURATE: return run_ws<BC, REALW, TRIG_ACCURATE>(p, grid, s);
+        case TRIG_FAST: return run_ws<BC, REALW, TRIG_FAST>(p, grid, s);
+        case TRIG_FAST_RR: return run_ws<BC, REALW, TRIG_FAST_RR>(p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -43,10 +43,6 @@ int grid_tc_threads()
     return kWsThreads;
 }
 
-bool grid_tc_ey_table(int trig, int bc, int nx, int ny)
-{
-    return bc == 1 && ny % kTcRows == 0 && trig == TRIG_ACCURATE && grid_tc_fold(nx, ny) == 1;
-}
 
 // One CTA: *ok = 1 when the offsets of every group of G rows from its first
 // row equal those of the first group exactly and are floats themselves;
@@ -83,45 +79,16 @@ cudaError_t launch_grid_tc(bool realw, int trig, int bc, const GridParams& p, di
     if (p.fold > 1 && (p.fold != grid_tc_fold(p.nx, p.ny) || p.fold_ok == nullptr ||
                        p.log2_fw != grid_tc_fold_log2_width(p.fold)))
         return cudaErrorInvalidValue;
-    const bool eyt = grid_tc_ey_table(trig, bc, p.nx, p.ny);
-    if (eyt && (p.ey_tab == nullptr || p.ey_blocks != p.ny / kTcRows)) return cudaErrorInvalidValue;
     if (realw) {
         if (bc != 1) return cudaErrorInvalidValue;
-        return eyt ? run_trig<1, true, true>(trig, p, grid, s)
-                   : run_trig<1, true, false>(trig, p, grid, s);
+        return run_trig<1, true>(trig, p, grid, s);
     }
     switch (bc) {
-        case 1:
-            return eyt ? run_trig<1, false, true>(trig, p, grid, s)
-                       : run_trig<1, false, false>(trig, p, grid, s);
-        case 4: return run_trig<4, false, false>(trig, p, grid, s);
-        case 8: return run_trig<8, false, false>(trig, p, grid, s);
+        case 1: return run_trig<1, false>(trig, p, grid, s);
+        case 4: return run_trig<4, false>(trig, p, grid, s);
+        case 8: return run_trig<8, false>(trig, p, grid, s);
     }
     return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* ys, int ny, float2* ey_tab, int grid,
-                                  cudaStream_t s)
-{
-    if (ny % kTcRows != 0) return cudaErrorInvalidValue;
-    const int nyb = ny / kTcRows;
-    switch (trig) {
-        case TRIG_ACCURATE:
-            build_ey_tiles_kernel<TRIG_ACCURATE><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
-                                                                     ey_tab);
-            break;
-        case TRIG_FAST:
-            build_ey_tiles_kernel<TRIG_FAST><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
-                                                                 ey_tab);
-            break;
-        case TRIG_FAST_RR:
-            build_ey_tiles_kernel<TRIG_FAST_RR><<<grid, 256, 0, s>>>(rec, fields, ntiles, ys, nyb,
-                                                                    ey_tab);
-            break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,

@@ -60,16 +60,10 @@ cudaError_t launch_scale_records(float* rec, int fields, int64_t ntiles,
                                  const unsigned int* bound, int bc, int grid, cudaStream_t s);
 // threads per CTA of the tensor-core grid kernel
 int grid_tc_threads();
-// whether a tensor-core grid launch takes its y factors from the Ey table
-bool grid_tc_ey_table(int trig, int bc, int nx, int ny);
 // the row-folding check of a narrow grid (grid_tc_fold(nx, ny) = G > 1): *ok
 // and the G row offsets dy, read by the B-tile build and the kernel
 cudaError_t launch_grid_fold_check(const float* ys, int ny, int G, unsigned int* ok, float* dy,
                                    cudaStream_t s);
-// the Ey table (ny % 128 == 0) from the records (ky) and ys
-cudaError_t launch_build_ey_tiles(int trig, const float* rec, int fields, int64_t ntiles,
-                                  const float* ys, int ny, float2* ey_tab, int grid,
-                                  cudaStream_t s);
 // B operand tiles of the tensor-core grid kernel from its records (kx) and
 // xs; mub: times the records' (scaled) weight, for single-coil launches
 cudaError_t launch_build_ex_tiles(int trig, bool mub, const float* rec, int fields,

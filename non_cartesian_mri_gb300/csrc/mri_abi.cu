@@ -507,7 +507,6 @@ struct GridPlan {
     int64_t rec_bytes;
     int64_t part_bytes;
     int64_t s_bytes;        // the B operand tiles
-    int64_t ey_bytes;       // one weight, accurate, ny % 128 == 0: the Ey table
     int fold;               // grid rows folded into one block's columns (nx <= 64), else 1
     int64_t vblocks_launch; // CTAs along the rows launched: the unfolded count when
                             // fold > 1 (the device-side check may refuse the fold)
@@ -536,8 +535,7 @@ std::vector<TcGroup> tc_groups(int64_t B)
     return g;
 }
 
-GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int bc = 1, int nb = 1,
-                   int trig = 0)
+GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int bc = 1, int nb = 1)
 {
     GridPlan g{};
     g.tensor_cores = mri::grid_tc_fits(nx);
@@ -557,9 +555,6 @@ GridPlan plan_grid(bool realw, int64_t M, int nx, int ny, int nz, int sms, int b
     g.rec_bytes = g.ntiles * int64_t(realw ? 4 : 3 + 2 * bc) * mri::kTcTile * 4;
     g.part_bytes = g.splits > 1 ? int64_t(g.splits) * nb * 2 * N * 4 : 0;
     g.s_bytes = g.ntiles * g.ncb * int64_t(mri::kTcStageBytes);
-    g.ey_bytes = mri::grid_tc_ey_table(trig, bc, nx, ny)
-                     ? g.ntiles * int64_t(ny / mri::kTcRows) * mri::kTcEyBytes
-                     : 0;
     return g;
 }
 
@@ -632,25 +627,19 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
     // tensor cores: coil groups sharing one table of B operand tiles
     const std::vector<TcGroup> groups = realw ? std::vector<TcGroup>{{0, 1, 1}} : tc_groups(B);
     std::vector<GridPlan> plans;
-    int64_t rec_max = 0, part_max = 0, ey_bytes = 0;
+    int64_t rec_max = 0, part_max = 0;
     for (const TcGroup& grp : groups) {
-        plans.push_back(plan_grid(realw, M, nx, ny, nz, d->sms, grp.bc, grp.nb, trig));
+        plans.push_back(plan_grid(realw, M, nx, ny, nz, d->sms, grp.bc, grp.nb));
         rec_max = std::max(rec_max, plans.back().rec_bytes);
         part_max = std::max(part_max, plans.back().part_bytes);
-        ey_bytes = std::max(ey_bytes, plans.back().ey_bytes);   // single-coil groups only
     }
     const int64_t s_bytes = plans[0].s_bytes;
-    bool ey_built = false;
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
                                 size_t(align256(rec_max) + kBoundBytes + align256(part_max) +
-                                       align256(s_bytes) + ey_bytes),
+                                       align256(s_bytes)),
                                 d->pool, s) != cudaSuccess)
         return cuda_fail();
-    float2* ey_tab = ey_bytes > 0
-                         ? reinterpret_cast<float2*>(scratch + align256(rec_max) + kBoundBytes +
-                                                     align256(part_max) + align256(s_bytes))
-                         : nullptr;
     float* rec = reinterpret_cast<float*>(scratch);
     // the bound slot: a weight bound word per coil of a group (8), the fold
     // check's word, its row offsets (up to 16)
@@ -692,19 +681,9 @@ mri_status run_grid_call(bool realw, int64_t B, const float* kx, const float* ky
                                                 d->sms),
                                        s, fold, fold_ok, fold_dy) != cudaSuccess)
             st = cuda_fail();
-        // the y factors depend on ky and the rows only: built once, by the
-        // first group that reads them
-        if (st == MRI_OK && g.ey_bytes > 0 && !ey_built) {
-            if (mri::launch_build_ey_tiles(trig, rec, fields, g.ntiles, ys, ny, ey_tab,
-                                           grid_for(g.ey_bytes / 8, d->sms), s) != cudaSuccess)
-                st = cuda_fail();
-            ey_built = true;
-        }
         mri::GridParams gp = grid_params(g, rec, xs, nx, ys, ny, zs, nz, d);
         gp.wbound = wbound;
         gp.s_tab = s_tab;
-        gp.ey_tab = g.ey_bytes > 0 ? ey_tab : nullptr;
-        gp.ey_blocks = g.ey_bytes > 0 ? ny / mri::kTcRows : 0;
         gp.coils = grp.nb;
         gp.ncb = mri::grid_tc_col_blocks(nx);
         gp.fold = fold;

@@ -1,8 +1,9 @@
 """The MRI_DEBUG build: every TMA copy's tile index is checked against the
 size of its table before it is issued (DEVERR_BOUNDS otherwise; the copy is
 skipped, nothing traps).  Builds that variant in-tree and runs every kernel
-family through it -- general gather (single, coil groups), tensor-core grid
-F^H D / Q (one coil, Ey table, coil groups, several column blocks), forward
+family through it -- general gather (single, coil groups per pair and on the
+tensor cores), tensor-core grid F^H D / Q (one coil, coil groups, several
+column blocks), forward
 model -- against the oracle, expecting no device error bit.  Runs in a child
 process, since a process loads one library."""
 

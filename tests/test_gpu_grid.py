@@ -197,9 +197,9 @@ def test_tensor_core_weight_scale_is_exact(mri, k, ny):
 
 
 @pytest.mark.parametrize("trig", ["accurate", "fast"])
-def test_tensor_core_y_factor_table_blocks(mri, trig):
-    """ny = 256 (two blocks of 128 rows per plane) and three planes: the
-    accurate path takes the y factors from the per-call table, by block."""
+def test_tensor_core_two_row_blocks_per_plane(mri, trig):
+    """ny = 256 (two blocks of 128 rows per plane) and three planes: the row
+    coordinates of each CTA's block, across plane boundaries."""
     w = wl.make_workload("fhd_128_radial")
     M = 3001
     xs = (np.arange(128) - 64).astype(np.float32)
