@@ -20,16 +20,49 @@ namespace mri {
 
 namespace {
 
-// One thread per sample: its eight corner contributions by atomic adds of
-// (re, im) pairs.  g0 = floor(k n) + n/2 and f = k n - floor(k n) are exact
-// in float (k n is k scaled by a power of two).
+// The central block of the k-grid a CTA accumulates in shared memory:
+// kHot^3 grid points around k = 0 (indices n/2 - kHot/2 .. n/2 + kHot/2 - 1
+// of each axis of at least kHot points; a shorter axis is all central).
+// Trajectories that pass through the centre (radial lines, spiral
+// interleaves) put a large share of their samples' contributions on these
+// few points, and atomic adds to one address are serialised in L2: summed
+// per CTA first, each central point then takes one global add per CTA.
+#ifndef MRI_GRID_HOT
+#define MRI_GRID_HOT 8
+#endif
+#ifndef MRI_GRID_CTAS_PER_SM
+#define MRI_GRID_CTAS_PER_SM 4
+#endif
+constexpr int kHot = MRI_GRID_HOT;
+
+// Grid-point index a of an axis of n points (power of two) -> its index in
+// the central block, or -1 when outside it.
+__device__ __forceinline__ int hot_index(int a, int n)
+{
+    const int h = n < kHot ? n : kHot;
+    const int r = a - (n >> 1) + (h >> 1);   // the block starts at n/2 - h/2
+    return (r >= 0 && r < h) ? r : -1;
+}
+
+// Each CTA takes a contiguous run of samples (one thread per sample per
+// pass): their eight corner contributions go by atomic adds of (re, im)
+// pairs to the grid, those on the central block to the CTA's shared copy,
+// which is added to the grid at the end.  g0 = floor(k n) + n/2 and
+// f = k n - floor(k n) are exact in float (k n is k scaled by a power of
+// two).
 __global__ void __launch_bounds__(256) grid_scatter_kernel(
     const float* __restrict__ kx, const float* __restrict__ ky, const float* __restrict__ kz,
     const float* __restrict__ rPhi, const float* __restrict__ iPhi, const float* __restrict__ rD,
     const float* __restrict__ iD, int64_t M, int nx, int ny, int nz, float2* G)
 {
-    for (int64_t m = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; m < M;
-         m += int64_t(gridDim.x) * blockDim.x) {
+    __shared__ float hot_r[kHot * kHot * kHot], hot_i[kHot * kHot * kHot];
+    for (int i = threadIdx.x; i < kHot * kHot * kHot; i += blockDim.x) hot_r[i] = hot_i[i] = 0.f;
+    __syncthreads();
+    const int n[3] = {nx, ny, nz};
+    const int64_t per = (M + gridDim.x - 1) / gridDim.x;
+    const int64_t m0 = blockIdx.x * per;
+    const int64_t m1 = m0 + per < M ? m0 + per : M;
+    for (int64_t m = m0 + threadIdx.x; m < m1; m += blockDim.x) {
         // Mu = conj(Phi) D
         const float pr = rPhi[m], pi = iPhi[m], dr = rD[m], di = iD[m];
         const float mr = pr * dr + pi * di;
@@ -37,7 +70,6 @@ __global__ void __launch_bounds__(256) grid_scatter_kernel(
         int g[3];
         float f[3];
         const float k[3] = {kx[m], ky[m], kz[m]};
-        const int n[3] = {nx, ny, nz};
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
             const float u = k[a] * float(n[a]);
@@ -55,8 +87,26 @@ __global__ void __launch_bounds__(256) grid_scatter_kernel(
             float w = (cx ? f[0] : 1.f - f[0]) * (cy ? f[1] : 1.f - f[1]) *
                       (cz ? f[2] : 1.f - f[2]);
             if ((gx + gy + gz) & 1) w = -w;   // (-1)^g of the centring
-            atomicAdd(&G[(int64_t(gz) * ny + gy) * nx + gx], make_float2(w * mr, w * mi));
+            const int hx = hot_index(gx, nx), hy = hot_index(gy, ny), hz = hot_index(gz, nz);
+            if ((hx | hy | hz) >= 0) {
+                const int h = (hz * kHot + hy) * kHot + hx;
+                atomicAdd(&hot_r[h], w * mr);
+                atomicAdd(&hot_i[h], w * mi);
+            } else {
+                atomicAdd(&G[(int64_t(gz) * ny + gy) * nx + gx], make_float2(w * mr, w * mi));
+            }
         }
+    }
+    __syncthreads();
+    // the CTA's central sums, one global add per point it touched
+    const int hx0 = (nx >> 1) - ((nx < kHot ? nx : kHot) >> 1);
+    const int hy0 = (ny >> 1) - ((ny < kHot ? ny : kHot) >> 1);
+    const int hz0 = (nz >> 1) - ((nz < kHot ? nz : kHot) >> 1);
+    for (int i = threadIdx.x; i < kHot * kHot * kHot; i += blockDim.x) {
+        const float vr = hot_r[i], vi = hot_i[i];
+        if (vr == 0.f && vi == 0.f) continue;
+        const int gx = hx0 + i % kHot, gy = hy0 + (i / kHot) % kHot, gz = hz0 + i / (kHot * kHot);
+        atomicAdd(&G[(int64_t(gz) * ny + gy) * nx + gx], make_float2(vr, vi));
     }
 }
 
@@ -185,7 +235,10 @@ cudaError_t launch_gridding(const float* kx, const float* ky, const float* kz, c
     cudaError_t e = cudaMemsetAsync(G, 0, size_t(N) * sizeof(float2), s);
     if (e != cudaSuccess) return e;
     if (M > 0) {
-        const int64_t blocks = std::min<int64_t>((M + 255) / 256, int64_t(sms) * 16);
+        // a few CTAs per SM, each over a contiguous run of samples: the
+        // central grid points take one global add per CTA
+        const int64_t blocks =
+            std::min<int64_t>((M + 255) / 256, int64_t(sms) * MRI_GRID_CTAS_PER_SM);
         grid_scatter_kernel<<<unsigned(blocks), 256, 0, s>>>(kx, ky, kz, rPhi, iPhi, rD, iD, M,
                                                               nx, ny, nz, G);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
