@@ -145,6 +145,31 @@ __device__ __forceinline__ double block_sum(double v, double* sm)
     return s;   // thread 0
 }
 
+// Once every CTA of the grid has written partial[blockIdx.x] (thread 0),
+// the last CTA to arrive adds them up in index order (a fixed order, so the
+// result does not depend on which CTA is last) into *out and resets *count
+// for the next use: the total without a separate launch.  Every thread of
+// the CTA calls it.
+__device__ __forceinline__ void finish_sum(const double* partial, double* out,
+                                           unsigned int* count, double* sm)
+{
+    __shared__ unsigned int ticket;
+    if (threadIdx.x == 0) {
+        __threadfence();   // this CTA's partial is visible before its ticket
+        ticket = atomicAdd(count, 1u);
+    }
+    __syncthreads();
+    if (ticket != gridDim.x - 1) return;
+    __threadfence();
+    double v = 0.0;
+    for (int k = threadIdx.x; k < int(gridDim.x); k += kDotThreads) v += __ldcg(partial + k);
+    const double total = block_sum(v, sm);
+    if (threadIdx.x == 0) {
+        *out = total;
+        *count = 0u;
+    }
+}
+
 // a CG step ratio, alpha = r.r / p.Ap or beta = new r.r / old r.r (0 once
 // r = 0 or p.Ap = 0)
 __device__ __forceinline__ float cg_ratio(const double* num, const double* den)
@@ -177,6 +202,8 @@ struct ToeplitzArgs {
     float2* work;           // [nz][2 ny][2 nx]
     const float* K;         // [2 nz][2 ny][2 nx], real
     double* dot;            // x inverse: per CTA Re <v, result> (nullptr: none)
+    double* dot_total;      // and their sum, by the last CTA (nullptr: not formed)
+    unsigned int* dot_count;   // its arrival counter (zero between uses)
     // x forward, conjugate gradients: v = r + beta v, beta = *rr_new /
     // *rr_old, is formed, written back to (vw_r, vw_i) = (ir, ii) and
     // transformed (upd_r == nullptr: v as it is)
@@ -286,6 +313,7 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
                 __shared__ double sm[kDotThreads / 32];
                 const double total = block_sum(dot.value(), sm);
                 if (threadIdx.x == 0) p.dot[blockIdx.x] = total;
+                if (p.dot_total != nullptr) finish_sum(p.dot, p.dot_total, p.dot_count, sm);
             }
         }
     } else {
@@ -599,7 +627,8 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y)
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
 }
 
-// x += alpha p, r -= alpha Ap, partial sums of |r|^2; VEC: four values per
+// x += alpha p, r -= alpha Ap, partial sums of |r|^2 and (the last CTA)
+// their total into *rr_next; VEC: four values per
 // access (n a multiple of 4, every array 16-byte aligned)
 template <bool VEC>
 __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi, float* rr_,
@@ -607,7 +636,8 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
                                                             const float* pi, const float* apr,
                                                             const float* api, int64_t n,
                                                             const double* rr, const double* pap,
-                                                            double* partial)
+                                                            double* partial, double* rr_next,
+                                                            unsigned int* count)
 {
     pdl_launch_dependents();
     pdl_wait();
@@ -655,6 +685,7 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
     }
     const double s = block_sum(v.value(), sm);
     if (threadIdx.x == 0) partial[blockIdx.x] = s;
+    finish_sum(partial, rr_next, count, sm);   // the new r.r
 }
 
 // r = b - r (r holds A x), p = r
@@ -879,6 +910,7 @@ namespace {
 cudaError_t toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda, const float* ir,
                            const float* ii, float* outr, float* outi, int accumulate,
                            float2* work, double* dot, const float2* tw, cudaStream_t s,
+                           double* dot_total = nullptr, unsigned int* dot_count = nullptr,
                            const float* upd_r = nullptr, const float* upd_i = nullptr,
                            const double* rr_new = nullptr, const double* rr_old = nullptr,
                            float* vw_r = nullptr, float* vw_i = nullptr)
@@ -897,6 +929,8 @@ cudaError_t toeplitz_apply(const float* K, int nx, int ny, int nz, float lambda,
     p.work = work;
     p.K = K;
     p.dot = dot;
+    p.dot_total = dot_total;
+    p.dot_count = dot_count;
     p.log2nx = log2i(nx);
     p.log2ny = log2i(ny);
     p.log2nz = log2i(nz);
@@ -928,19 +962,21 @@ cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, cons
                       int dot_blocks, cudaStream_t s)
 {
     // vec: r (2 N), p (2 N), Ap (2 N); scal: dot partials (max(dot_blocks,
-    // toeplitz_dot_blocks)), p.Ap
+    // toeplitz_dot_blocks)), p.Ap, then two arrival counters (one double's room)
     const int64_t N = int64_t(nx) * ny * nz;
     float *r_r = vec, *r_i = vec + N, *p_r = vec + 2 * N, *p_i = vec + 3 * N;
     float *a_r = vec + 4 * N, *a_i = vec + 5 * N;
     const int64_t apply_blocks = toeplitz_dot_blocks(nx, ny, nz);
     double* partial = scal;
     double* pap = scal + std::max<int64_t>(dot_blocks, apply_blocks);
+    unsigned int* count = reinterpret_cast<unsigned int*>(pap + 1);   // [0]: p.Ap, [1]: r.r
     const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0 &&
                       (reinterpret_cast<uintptr_t>(xi) & 15u) == 0 &&
                       (reinterpret_cast<uintptr_t>(vec) & 15u) == 0;
+    cudaError_t e = cudaMemsetAsync(count, 0, 2 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
     // r = b - A x, p = r, rr[0] = r.r
-    cudaError_t e = toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, nullptr, tw,
-                                   s);
+    e = toeplitz_apply(K, nx, ny, nz, lambda, xr, xi, r_r, r_i, 0, work, nullptr, tw, s);
     if (e != cudaSuccess) return e;
     e = launch_pdl(cg_start_kernel, grid, 256, 0, s, br, bi, r_r, r_i, p_r, p_i, N);
     if (e == cudaSuccess)
@@ -950,24 +986,20 @@ cudaError_t launch_cg(const float* K, int nx, int ny, int nz, float lambda, cons
         e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks, rr);
     if (e != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
-        // Ap, with the per-CTA sums of p.Ap from its last stage; from the
+        // Ap, with p.Ap summed by the last CTA of its last stage; from the
         // second iteration on, its first stage also forms the new direction
         // p = r + beta p, beta = rr[it] / rr[it - 1]
         if (it == 0)
-            e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s);
+            e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s,
+                               pap, count);
         else
             e = toeplitz_apply(K, nx, ny, nz, lambda, p_r, p_i, a_r, a_i, 0, work, partial, tw, s,
-                               r_r, r_i, rr + it, rr + it - 1, p_r, p_i);
-        if (e == cudaSuccess)
-            e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, int(apply_blocks),
-                           pap);
+                               pap, count, r_r, r_i, rr + it, rr + it - 1, p_r, p_i);
+        // x += alpha p, r -= alpha Ap, rr[it + 1] = r.r (by its last CTA)
         if (e == cudaSuccess)
             e = launch_pdl(vec4 ? cg_xr_kernel<true> : cg_xr_kernel<false>, dot_blocks,
                            kDotThreads, 0, s, xr, xi, r_r, r_i, p_r, p_i, a_r, a_i, N, rr + it,
-                           pap, partial);
-        if (e == cudaSuccess)
-            e = launch_pdl(sum_partials_kernel, 1, kDotThreads, 0, s, partial, dot_blocks,
-                           rr + it + 1);
+                           pap, partial, rr + it + 1, count + 1);
         if (e != cudaSuccess) return e;
     }
     e = launch_pdl(sqrt_kernel, (iters + 1 + 255) / 256, 256, 0, s, rr, iters + 1);

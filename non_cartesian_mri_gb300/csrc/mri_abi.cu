@@ -1221,14 +1221,14 @@ mri_status mri_cg_solve(const float* K, int nx, int ny, int nz, float lambda, co
     if ((st = prepare(0, 0, 1, 0, N, nullptr, 0, vp, 6, &d)) != MRI_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // scratch: r, p, Ap (SoA), the FFT stages' work array (half the doubled
-    // grid), the dot partials
+    // grid), the dot partials, p.Ap and two arrival counters
     const int dot_blocks = int(std::min<int64_t>(ceil_div(N, 256), int64_t(d->sms) * 4));
     const int64_t vec_bytes = align256(6 * N * 4);
     const int64_t work_bytes = align256(4 * N * int64_t(sizeof(float2)));
     const int64_t partials = std::max<int64_t>(dot_blocks, mri::toeplitz_dot_blocks(nx, ny, nz));
     char* scratch = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch),
-                                size_t(vec_bytes + work_bytes + (partials + 1) * 8), d->pool,
+                                size_t(vec_bytes + work_bytes + (partials + 2) * 8), d->pool,
                                 s) != cudaSuccess)
         return cuda_fail();
     float* vec = reinterpret_cast<float*>(scratch);
