@@ -84,13 +84,16 @@ def test_tiny_shapes(mri, M, N):
     no_device_errors(mri)
 
 
-def test_sample_splits_and_accumulate(mri):
+@pytest.mark.parametrize("B", [8, 13, 17])
+def test_sample_splits_and_accumulate(mri, B):
     """Few voxels and many samples: the samples split across CTAs and the
-    partial sums are reduced; accumulate adds onto the outputs."""
-    M, N, B = 40000, 300, 8
+    partial sums are reduced; accumulate adds onto the outputs.  13 and 17
+    coils: a second group of 5 (its partials laid out for 5 coils in the
+    buffer sized for 8), and a trailing single coil on the per-pair kernel."""
+    M, N = 40000, 300
     p = mri.plan("fhd_batched", M, N, B=B)
     assert p["tensor_cores"] == 1 and p["splits"] > 1
-    a = wl.random_fhd_inputs(M, N, seed=5, B=B)
+    a = wl.random_fhd_inputs(M, N, seed=5 + B, B=B)
     args = [dev(a[k]) for k in KEYS]
     ref = oracle.fhd_batched(**a)
     r, i = mri.fhd_batched(*args, trig="accurate")
