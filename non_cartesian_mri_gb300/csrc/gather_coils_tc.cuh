@@ -92,7 +92,10 @@ struct CoilTcParams {
 };
 
 #ifndef MRI_CT_SPLIT
-#define MRI_CT_SPLIT 1    // A's split: 0 floating (tc_split8), 1 fixed point (ct_split8_unit)
+#define MRI_CT_SPLIT 1    // A's split, accurate trig: 0 floating (tc_split8), 1 fixed point
+#endif
+#ifndef MRI_CT_SPLIT_FAST
+#define MRI_CT_SPLIT_FAST 0   // the same for the fast trig paths (measured: floating 1 % faster)
 #endif
 #ifndef MRI_CT_PHASE2
 #define MRI_CT_PHASE2 1   // fast trig: the phase on pairs of samples (.f32x2)
@@ -123,9 +126,10 @@ __device__ __forceinline__ void ct_split8_unit(const float (&v)[8], uint4& hi, u
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+template <int TRIG>
 __device__ __forceinline__ void ct_split8(const float (&v)[8], uint4& hi, uint4& lo)
 {
-    if constexpr (MRI_CT_SPLIT == 1) {
+    if constexpr ((TRIG == TRIG_ACCURATE ? MRI_CT_SPLIT : MRI_CT_SPLIT_FAST) == 1) {
         ct_split8_unit(v, hi, lo);
     } else {
         tc_split8(v, hi, lo);
@@ -387,10 +391,10 @@ __global__ void __launch_bounds__(kCtThreads, 2) coils_tc_kernel(CoilTcParams p)
                 // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
                 const uint32_t col = acol + uint32_t(s0 / 2);
                 uint4 h, l;
-                ct_split8(ar, h, l);
+                ct_split8<TRIG>(ar, h, l);
                 tmem_st4(col + A_RH * kTcAPartCols, h);
                 tmem_st4(col + A_RL * kTcAPartCols, l);
-                ct_split8(ai, h, l);
+                ct_split8<TRIG>(ai, h, l);
                 tmem_st4(col + A_IH * kTcAPartCols, h);
                 tmem_st4(col + A_IL * kTcAPartCols, l);
             }
