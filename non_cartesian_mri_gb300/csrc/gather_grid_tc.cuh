@@ -185,10 +185,46 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t d)
     return make_float2(a, b);
 }
 
+// The low f16 parts of a and b given their high parts h (pack_f16x2(a, b)):
+// the remainders a - hi and b - hi, each formed in fp32 by one
+// mixed-precision FMA (the f16 hi times -1 plus the fp32 value: exact, since
+// hi is the value rounded), rounded to f16 and packed.
+__device__ __forceinline__ uint32_t split_lo_f16x2(float a, float b, uint32_t h)
+{
+    uint32_t l;
+    asm("{\n\t.reg .b16 h0, h1, m;\n\t.reg .f32 l0, l1;\n\t"
+        "mov.b32 {h0, h1}, %3;\n\t"
+        "mov.b16 m, 0xBC00;\n\t"            // f16 -1
+        "fma.rn.f32.f16 l0, h0, m, %1;\n\t"
+        "fma.rn.f32.f16 l1, h1, m, %2;\n\t"
+        "cvt.rn.f16x2.f32 %0, l1, l0;\n\t}"
+        : "=r"(l)
+        : "f"(a), "f"(b), "r"(h));
+    return l;
+}
+
 // v = hi + lo for 8 values, two per word: hi = v rounded to f16, lo = the
 // exact float remainder v - hi rounded to f16 (|lo| <= 2^-11 |v|, either
-// sign, so the dropped lo*lo term has no preferred sign)
+// sign, so the dropped lo*lo term has no preferred sign).  The remainder by
+// the mixed-precision FMA (split_lo_f16x2).
 __device__ __forceinline__ void tc_split8(const float (&v)[8], uint4& hi, uint4& lo)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        h[j] = pack_f16x2(v[2 * j], v[2 * j + 1]);
+        l[j] = split_lo_f16x2(v[2 * j], v[2 * j + 1], h[j]);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// The same parts, bit for bit, with the remainder taken after converting hi
+// back to fp32 (two conversions and two subtractions per word instead of two
+// FMAs).  The coil-group generators of the grid kernel run 1-2 % faster with
+// it; everywhere else the FMA form is as fast or faster (single-coil grid
+// paths 1-2 %, the coil kernel at arbitrary coordinates 3 %).
+__device__ __forceinline__ void tc_split8_rt(const float (&v)[8], uint4& hi, uint4& lo)
 {
     uint32_t h[4], l[4];
 #pragma unroll

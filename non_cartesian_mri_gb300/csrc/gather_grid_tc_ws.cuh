@@ -375,10 +375,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) gather_grid_tc_ws_kernel(GridPa
                     // samples s0 .. s0 + 7 = columns s0 / 2 .. of each part
                     const uint32_t col = acol + uint32_t(s0 / 2);
                     uint4 h, l;
-                    tc_split8(ar, h, l);
+                    if constexpr (BC == 1) tc_split8(ar, h, l); else tc_split8_rt(ar, h, l);
                     tmem_st4(col + A_RH * kTcAPartCols, h);
                     tmem_st4(col + A_RL * kTcAPartCols, l);
-                    tc_split8(ai, h, l);
+                    if constexpr (BC == 1) tc_split8(ai, h, l); else tc_split8_rt(ai, h, l);
                     tmem_st4(col + A_IH * kTcAPartCols, h);
                     tmem_st4(col + A_IL * kTcAPartCols, l);
                 }
