@@ -273,14 +273,24 @@ __device__ __forceinline__ void fft_run_from(float2* buf, const float2* tws, flo
     }
 }
 
+struct FftNoKeep {
+    __device__ __forceinline__ void operator()(int, int, float2) const {}
+};
+
 // The transform of the CTA's W lines: the first pass takes its inputs from
 // load(w, position) straight into registers (HALF_IN: the positions >= L / 2
 // are zero and not loaded, and the first DFT stage skips them), shared
 // memory carries the values between passes only, and fin gets the last
 // pass's outputs in registers (see fft_run_from).  Lines past the end are
-// the loader's and fin's to skip.  The first pass has Ns = 1: no twiddles.
-template <bool INVERSE, int LOG2L, bool ODD_FIRST, bool WFAST, bool HALF_IN, class Load, class Fin>
-__device__ __forceinline__ void fft_lines(float2* buf, const float2* tws, Load&& load, Fin&& fin)
+// the loader's, keep's and fin's to skip.  The first pass has Ns = 1: no
+// twiddles.  keep(w, position, value) sees every loaded value once all the
+// loads are issued: a store it makes (the CG direction written back) holds
+// back no load, which a store inside load would (the compiler cannot tell
+// the arrays apart).
+template <bool INVERSE, int LOG2L, bool ODD_FIRST, bool WFAST, bool HALF_IN, class Load, class Fin,
+          class Keep>
+__device__ __forceinline__ void fft_lines(float2* buf, const float2* tws, Load&& load, Fin&& fin,
+                                          Keep&& keep)
 {
     using P = FftPlan<LOG2L, ODD_FIRST>;
     constexpr int R0 = P::log2r(0);
@@ -298,8 +308,22 @@ __device__ __forceinline__ void fft_lines(float2* buf, const float2* tws, Load&&
                                                                  : make_float2(0.f, 0.f);
     }
 #pragma unroll
+    for (int it = 0; it < I0; ++it) {
+        int w, j;
+        if (!fft_item<LOG2L, R0, WFAST>(it, w, j)) continue;
+#pragma unroll
+        for (int q = 0; q < (HALF_IN ? (1 << R0) / 2 : (1 << R0)); ++q)
+            keep(w, j + q * per0, y[it][q]);
+    }
+#pragma unroll
     for (int it = 0; it < I0; ++it) fft_dft_regs<INVERSE, R0, HALF_IN>(y[it]);
     fft_run_from<INVERSE, LOG2L, ODD_FIRST, WFAST, 0>(buf, tws, y, fin);
+}
+
+template <bool INVERSE, int LOG2L, bool ODD_FIRST, bool WFAST, bool HALF_IN, class Load, class Fin>
+__device__ __forceinline__ void fft_lines(float2* buf, const float2* tws, Load&& load, Fin&& fin)
+{
+    fft_lines<INVERSE, LOG2L, ODD_FIRST, WFAST, HALF_IN>(buf, tws, load, fin, FftNoKeep{});
 }
 
 // The last pass of a plan: its log2 radix, and the stride of its outputs

@@ -262,11 +262,9 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
                     if (group + w >= lines) return zero;
                     const uint32_t n = vidx(w, pos);
                     float vr = p.ir[n], vi = p.ii[n];
-                    if (upd) {   // each v[n] is read and written by this thread only
+                    if (upd) {
                         vr = fmaf(beta, vr, p.upd_r[n]);
                         vi = fmaf(beta, vi, p.upd_i[n]);
-                        p.vw_r[n] = vr;
-                        p.vw_i[n] = vi;
                     }
                     return make_float2(vr, vi);
                 },
@@ -279,6 +277,14 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
                             for (int q = 0; q < (1 << RL); ++q) p.work[widx(w, j + q * per)] = y[it][q];
                         }
                     }
+                },
+                [&](int w, int pos, float2 v) {
+                    // the new direction, written back once every load is
+                    // issued (each v[n] is read and written by this thread only)
+                    if (!upd || group + w >= lines) return;
+                    const uint32_t n = vidx(w, pos);
+                    p.vw_r[n] = v.x;
+                    p.vw_i[n] = v.y;
                 });
         } else {
             FloatSum dot;
@@ -290,12 +296,22 @@ __global__ void __launch_bounds__(kFftThreads, fft_min_ctas(LOG2L))
                     for (int it = 0; it < IL; ++it) {
                         int w, j;
                         if (!fft_item<LOG2L, RL, false>(it, w, j) || group + w >= lines) continue;
-                        // the corner ix < nx: outputs q < R / 2
+                        // the corner ix < nx: outputs q < R / 2.  Every v[n] of
+                        // the item is loaded before the first out[n] is stored
+                        // (v and out may be one array, each n this thread's
+                        // only; a load after a store would wait for it)
+                        constexpr int H = (1 << RL) / 2;
+                        float vr_[H], vi_[H];
 #pragma unroll
-                        for (int q = 0; q < (1 << RL) / 2; ++q) {
+                        for (int q = 0; q < H; ++q) {
                             const uint32_t n = vidx(w, j + q * per);
-                            // v[n] is read before out[n] is written by the same thread
-                            const float vr = p.ir[n], vi = p.ii[n];
+                            vr_[q] = p.ir[n];
+                            vi_[q] = p.ii[n];
+                        }
+#pragma unroll
+                        for (int q = 0; q < H; ++q) {
+                            const uint32_t n = vidx(w, j + q * per);
+                            const float vr = vr_[q], vi = vi_[q];
                             float r = fmaf(p.lambda, vr, y[it][q].x * p.scale);
                             float i = fmaf(p.lambda, vi, y[it][q].y * p.scale);
                             if (p.accumulate) {
@@ -629,7 +645,10 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y)
 
 // x += alpha p, r -= alpha Ap, partial sums of |r|^2 and (the last CTA)
 // their total into *rr_next; VEC: four values per
-// access (n a multiple of 4, every array 16-byte aligned)
+// access (n a multiple of 4, every array 16-byte aligned).  Every load of an
+// element comes before its stores: the arrays may alias as far as the
+// compiler knows, so a load after a store would wait for it, one access in
+// flight at a time.
 template <bool VEC>
 __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi, float* rr_,
                                                             float* ri, const float* pr,
@@ -656,10 +675,11 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
             const float4 p_i = reinterpret_cast<const float4*>(pi)[k];
             const float4 a_r = reinterpret_cast<const float4*>(apr)[k];
             const float4 a_i = reinterpret_cast<const float4*>(api)[k];
-            x4r[k] = fma4(alpha, p_r, x4r[k]);
-            x4i[k] = fma4(alpha, p_i, x4i[k]);
-            const float4 a = fma4(-alpha, a_r, r4r[k]);
-            const float4 b = fma4(-alpha, a_i, r4i[k]);
+            const float4 x_r = x4r[k], x_i = x4i[k], r_r = r4r[k], r_i = r4i[k];
+            x4r[k] = fma4(alpha, p_r, x_r);
+            x4i[k] = fma4(alpha, p_i, x_i);
+            const float4 a = fma4(-alpha, a_r, r_r);
+            const float4 b = fma4(-alpha, a_i, r_i);
             r4r[k] = a;
             r4i[k] = b;
             v.add(a.x * a.x);
@@ -673,10 +693,12 @@ __global__ void __launch_bounds__(kDotThreads) cg_xr_kernel(float* xr, float* xi
         }
     } else {
         for (int64_t k = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; k < n; k += stride) {
-            xr[k] = fmaf(alpha, pr[k], xr[k]);
-            xi[k] = fmaf(alpha, pi[k], xi[k]);
-            const float a = fmaf(-alpha, apr[k], rr_[k]);
-            const float b = fmaf(-alpha, api[k], ri[k]);
+            const float p_r = pr[k], p_i = pi[k], a_r = apr[k], a_i = api[k];
+            const float x_r = xr[k], x_i = xi[k], r_r = rr_[k], r_i = ri[k];
+            xr[k] = fmaf(alpha, p_r, x_r);
+            xi[k] = fmaf(alpha, p_i, x_i);
+            const float a = fmaf(-alpha, a_r, r_r);
+            const float b = fmaf(-alpha, a_i, r_i);
             rr_[k] = a;
             ri[k] = b;
             v.add(a * a);
