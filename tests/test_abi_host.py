@@ -154,6 +154,42 @@ def test_plan_covers_every_voxel_and_sample(lib):
         assert p.launches == p.coil_groups * (per + (1 if p.splits > 1 else 0))
 
 
+def test_plan_invariants_over_shapes(lib):
+    """Every plan over a sweep of shapes and SM counts: voxels and samples
+    covered with no empty CTA column or tile, splits within the sample tiles
+    (at most 1024, far inside the 65,535 a launch's y dimension allows), a
+    voxel grid within 2^31 - 1 CTAs, the launch count of its groups, and
+    scratch that holds the split partials."""
+    for kind, Bs in ((0, (1,)), (1, (1,)), (2, (1, 2, 3, 5, 8, 9, 13, 17))):
+        for B in Bs:
+            for M in (1, 31, 32, 33, 1000, 32768, 262144, 1 << 20, 1 << 24):
+                for N in (1, 127, 128, 129, 2049, 64 ** 3, 128 ** 3, 256 ** 3):
+                    for sms in (1, 8, 152):
+                        p = plan(lib, kind, B, M, N, sms)
+                        vpc = p.voxels_per_cta
+                        assert p.voxel_ctas * vpc >= N > (p.voxel_ctas - 1) * vpc
+                        assert p.voxel_ctas <= 2 ** 31 - 1
+                        spt = p.samples_per_tile
+                        assert p.tiles * spt >= M > (p.tiles - 1) * spt
+                        assert 1 <= p.splits <= min(p.tiles, 1024)
+                        # groups of 8 (and one of 3-7) on the tensor cores, 3
+                        # launches each; 1 or 2 coils left on the per-pair
+                        # kernel, 2; one more per group whose samples split
+                        if p.tensor_cores:
+                            n_pair = int(B > 8 and B % 8 in (1, 2))
+                        else:
+                            n_pair = p.coil_groups
+                        n_tc = p.coil_groups - n_pair
+                        base = 3 * n_tc + 2 * n_pair
+                        if n_pair == 0 or n_tc == 0:
+                            assert p.launches == base + p.coil_groups * (p.splits > 1)
+                        else:
+                            assert base <= p.launches <= base + p.coil_groups
+                        if p.splits > 1:
+                            assert p.scratch_bytes >= p.splits * 2 * N * 4
+                        assert p.scratch_bytes >= 0
+
+
 def test_plan_splits_samples_when_voxels_underfill_the_gpu(lib):
     small = plan(lib, 0, 1, 32768, 64 ** 3)        # 128 voxel CTAs < 304 slots
     assert small.splits > 1
