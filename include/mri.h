@@ -187,14 +187,17 @@ mri_status mri_fhd_noalloc(const float* kx, const float* ky, const float* kz,
  * the kernel tabulates the x factor per column and Mu times the (y, z)
  * factor per row and spends one complex multiply-accumulate per
  * voxel-sample pair; sin/cos are evaluated per (sample, column) and
- * (sample, row) only.  With nx = 64 or a multiple of 128 the sum over
- * samples is done as a complex matrix product on the tensor cores (tcgen05,
- * f16 operands split into high and low parts so that each product keeps ~22
- * bits, fp32 accumulation, blocked summation; columns in blocks of 128,
- * nx = 64 padded to one block); the results meet the same tolerances as the
- * other paths.  The table kernel covers the other nx in {16, 32}; other
- * grids are expanded to coordinates and take the general kernel.
- * Edge cases as mri_fhd.
+ * (sample, row) only.  For nx >= 8 the sum over samples is done as a
+ * complex matrix product on the tensor cores (tcgen05, f16 operands split
+ * into high and low parts so that each product keeps ~22 bits, fp32
+ * accumulation, blocked summation): columns in blocks of 128, the last one
+ * padded; a grid 8 to 64 wide folds G = 128 / (nx rounded up to a power of
+ * two) rows into one block when every group of G rows has the same y
+ * offsets from its first row (checked on the device; otherwise the padded
+ * layout runs).  The results meet the same tolerances as the other paths.
+ * Grids with nx < 8 are expanded to coordinates and take the general
+ * kernel.  nx up to 8,388,480 (65,535 blocks of columns; a wider grid's
+ * launch is refused: MRI_ERR_CUDA).  Edge cases as mri_fhd.
  */
 mri_status mri_fhd_grid(const float* kx, const float* ky, const float* kz,
                         const float* xs, int nx, const float* ys, int ny,
@@ -216,11 +219,11 @@ mri_status mri_q_grid(const float* kx, const float* ky, const float* kz,
  * phase is tabulated once per call and the (y, z) factor once per (row,
  * sample) for up to 8 coils at a time, each sin/cos pair serving every coil
  * of the group.  As for mri_fhd_batched, the pages do not describe this
- * variant; it is F^H D applied to several D.  nx = 64 or a multiple of 128
- * runs on the tensor cores with the coils of a group sharing each MMA's
- * rows; other grids are
- * expanded to coordinates and take mri_fhd_batched.  Edge cases as
- * mri_fhd_batched.
+ * variant; it is F^H D applied to several D.  nx >= 8 runs on the tensor
+ * cores as mri_fhd_grid does, with the coils of a group sharing each MMA's
+ * rows (groups of 8, and the remainder as a group padded to 4 or 8 coils;
+ * a remainder of one coil takes the single-coil kernel); grids with nx < 8 are expanded to coordinates and
+ * take mri_fhd_batched.  Edge cases as mri_fhd_batched.
  */
 mri_status mri_fhd_batched_grid(const float* kx, const float* ky, const float* kz,
                                 const float* xs, int nx, const float* ys, int ny,
@@ -233,12 +236,12 @@ mri_status mri_fhd_batched_grid(const float* kx, const float* ky, const float* k
 /*
  * The forward model of mri_forward on a separable grid: rho (rRho, iRho) on
  * the grid xs x ys x zs (voxel order as mri_fhd_grid, N = nx*ny*nz), D (rD,
- * iD) at the M samples.  With nx = 64 or a multiple of 128 (columns in
- * blocks of 128, nx = 64 padded) the sum over the columns is a complex
- * matrix product on the tensor cores (the samples are the MMA rows; f16
- * operands split into high and low parts, fp32 accumulation) and the sum
- * over rows follows in the epilogue with blocked summation; other grids are
- * expanded to coordinates and take mri_forward.  Edge cases as mri_forward.
+ * iD) at the M samples.  For nx >= 8 (columns in blocks of 128, the last
+ * one padded) the sum over the columns is a complex matrix product on the
+ * tensor cores (the samples are the MMA rows; f16 operands split into high
+ * and low parts, fp32 accumulation) and the sum over rows follows in the
+ * epilogue with blocked summation; grids with nx < 8 are expanded to
+ * coordinates and take mri_forward.  Edge cases as mri_forward.
  */
 mri_status mri_forward_grid(const float* kx, const float* ky, const float* kz,
                             const float* xs, int nx, const float* ys, int ny,
