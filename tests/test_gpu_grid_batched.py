@@ -67,8 +67,8 @@ def test_tensor_core_coil_groups(mri, B, trig):
     w = wl.make_workload("fhd_128_radial")
     M = 5001
     xs = (np.arange(128) - 64).astype(np.float32)
-    # B = 9: a group of 8 and a single coil; ny = 128 lets the single coil
-    # take the y-factor table on the accurate path
+    # B = 9: a group of 8 and a single coil, on whole 128-row planes (each
+    # CTA's rows one z plane)
     ys = (np.arange(128) - 64).astype(np.float32) if B == 9 else np.array([-40, 3, 57], np.float32)
     zs = np.array([-30.0, 6.0], np.float32) if B == 9 else (np.arange(7) * 9 - 30).astype(np.float32)
     rD, iD = coil_data(w, B, M, 10 + B)
